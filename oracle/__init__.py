@@ -1,0 +1,177 @@
+"""Float64 CPU oracle for the selective scan -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never does, and
+this package never imports the product library: the two share no code.
+
+The arithmetic lives in ``ss_oracle.c`` (plain C, float64, sequential over the
+scan).  This module compiles it with gcc into ``liboracle.so`` beside the
+source and calls it through ctypes with NumPy float64 arrays.
+
+Conventions (see the C file's header for the equations and their sources):
+    u [batch, dim, L], delta [batch, K, dim, L], A [K*dim, N],
+    B, C [batch, K, G, N, L], D / delta_bias [K*dim], z [batch, dim, L],
+    h0 / last_state [batch, K, dim, N]; per-direction Delta, B, C are indexed by
+    position, and a direction's order is one of ORDER_*.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+ORDER_FWD = 0       # positions 0..L-1 (row-major for an H x W map)
+ORDER_REV = 1       # positions L-1..0
+ORDER_COL = 2       # column-major over an H x W map
+ORDER_COL_REV = 3   # reverse of column-major
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ss_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ss_oracle.c into liboracle.so (no fast-math, no vectorisation flags)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC",
+                               "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    i64 = ctypes.c_int64
+    lib.ssor_scan.restype = ctypes.c_int
+    lib.ssor_scan.argtypes = [i64, i64, i64, i64, i64, i64, i64,
+                              ctypes.POINTER(ctypes.c_int),
+                              dp, dp, dp, dp, dp, dp, dp, dp,
+                              ctypes.c_int, ctypes.c_int, dp, dp, dp, dp]
+    lib.ssor_softplus_scalar.restype = ctypes.c_double
+    lib.ssor_softplus_scalar.argtypes = [ctypes.c_double]
+    lib.ssor_position_of.restype = ctypes.c_int64
+    lib.ssor_position_of.argtypes = [ctypes.c_int, i64, i64, i64]
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(build())
+    return _lib
+
+
+def _f64(a, shape, name):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    if tuple(a.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(a.shape)}")
+    return a
+
+
+def _ptr(a):
+    if a is None:
+        return ctypes.POINTER(ctypes.c_double)()
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+         orders=(ORDER_FWD,), H=None, W=None, zoh=False, h0=None, _lib_handle=None):
+    """Run the oracle.
+
+    ``delta`` is [batch, K, dim, L] and ``B``/``C`` are [batch, K, G, N, L]; for a
+    single direction the K axis may be omitted (``delta`` [batch, dim, L],
+    ``B``/``C`` [batch, G, N, L]).  ``H``/``W`` default to 1 x L.
+    Returns ``(out [batch, dim, L], last_state [batch, K, dim, N])`` as float64.
+    """
+    u = np.asarray(u)
+    batch, dim, L = u.shape
+    K = len(orders)
+    delta = np.asarray(delta)
+    B = np.asarray(B)
+    C = np.asarray(C)
+    if delta.ndim == 3:
+        delta = delta[:, None]
+    if B.ndim == 4:
+        B = B[:, None]
+    if C.ndim == 4:
+        C = C[:, None]
+    G, N = B.shape[2], B.shape[3]
+    if H is None and W is None:
+        H, W = 1, L
+    if H * W != L:
+        raise ValueError("H*W must equal L")
+    u = _f64(u, (batch, dim, L), "u")
+    delta = _f64(delta, (batch, K, dim, L), "delta")
+    A = _f64(np.asarray(A).reshape(K * dim, N), (K * dim, N), "A")
+    B = _f64(B, (batch, K, G, N, L), "B")
+    C = _f64(C, (batch, K, G, N, L), "C")
+    D = _f64(None if D is None else np.asarray(D).reshape(K * dim), (K * dim,), "D")
+    z = _f64(z, (batch, dim, L), "z")
+    delta_bias = _f64(None if delta_bias is None else np.asarray(delta_bias).reshape(K * dim),
+                      (K * dim,), "delta_bias")
+    h0 = _f64(None if h0 is None else np.asarray(h0).reshape(batch, K, dim, N),
+              (batch, K, dim, N), "h0")
+    out = np.empty((batch, dim, L), dtype=np.float64)
+    last = np.empty((batch, K, dim, N), dtype=np.float64)
+    work = np.empty((N,), dtype=np.float64)
+    ords = (ctypes.c_int * K)(*[int(o) for o in orders])
+    lib = _lib_handle if _lib_handle is not None else _load()
+    rc = lib.ssor_scan(batch, dim, H, W, N, G, K, ords,
+                           _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                           _ptr(delta_bias), int(bool(delta_softplus)), int(bool(zoh)),
+                           _ptr(h0), _ptr(out), _ptr(last), _ptr(work))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out, last
+
+
+def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                   zoh=False, h0=None):
+    """One forward direction: delta [batch, dim, L], B/C [batch, G, N, L], A [dim, N]."""
+    out, last = scan(u, delta, A, B, C, D, z, delta_bias, delta_softplus, (ORDER_FWD,),
+                     zoh=zoh, h0=h0)
+    return out, last[:, 0]
+
+
+def bidir_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True):
+    """Forward + reversed direction, outputs summed: delta [batch, 2, dim, L]."""
+    return scan(u, delta, A, B, C, D, z, delta_bias, delta_softplus, (ORDER_FWD, ORDER_REV))
+
+
+# The SS2D direction set, in the order the key-code listing stacks them:
+# row-major, column-major, reversed row-major, reversed column-major.
+SS2D_ORDERS = (ORDER_FWD, ORDER_COL, ORDER_REV, ORDER_COL_REV)
+
+
+def cross_scan2d(u, delta, A, B, C, H, W, D=None, z=None, delta_bias=None, delta_softplus=True):
+    """SS2D: u [batch, dim, H, W]; delta [batch, 4, dim, H, W]; B/C [batch, 4, G, N, H, W]."""
+    u = np.asarray(u)
+    batch, dim = u.shape[:2]
+    L = H * W
+    delta = np.asarray(delta).reshape(batch, 4, dim, L)
+    B = np.asarray(B)
+    C = np.asarray(C)
+    B = B.reshape(B.shape[0], 4, B.shape[2], B.shape[3], L)
+    C = C.reshape(C.shape[0], 4, C.shape[2], C.shape[3], L)
+    zz = None if z is None else np.asarray(z).reshape(batch, dim, L)
+    out, last = scan(u.reshape(batch, dim, L), delta, A, B, C, D, zz, delta_bias, delta_softplus,
+                     SS2D_ORDERS, H=H, W=W)
+    return out.reshape(batch, dim, H, W), last
+
+
+def softplus(x: float) -> float:
+    return _load().ssor_softplus_scalar(float(x))
+
+
+def position(order: int, s: int, H: int, W: int) -> int:
+    return _load().ssor_position_of(int(order), int(s), int(H), int(W))

@@ -1,0 +1,157 @@
+/*
+ * ss_oracle.c -- float64 CPU oracle for the selective state-space scan.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke
+ * check and the CPU-baseline leg of the benchmark may load this file's
+ * library.  It shares no code, header or constant with the CUDA library.
+ *
+ * What it computes (sources, by page title and section):
+ *   - "Mamba Series from Selective State Spaces to Visual State Space Models",
+ *     section "选择性 SSM 的数学形式" (the mathematical form of the selective SSM):
+ *       discretisation  Abar = exp(Delta*A),
+ *                       Bbar = (Delta*A)^-1 (exp(Delta*A) - I) * Delta*B   (zero-order hold),
+ *       selection       Delta = softplus(W_Delta x + b_Delta), B = W_B x, C = W_C x.
+ *     The simplified (Euler) input matrix Bbar = Delta*B is the default; the
+ *     zero-order-hold form is selected by a flag.
+ *   - same page, block diagram "Mamba Block (1D)": the scan output is multiplied
+ *     by SiLU of the gate branch z.
+ *   - same page, "关键代码" (key code), SS2D forward: four traversal orders of an
+ *     H x W map (row-major, column-major, and the reverse of each), one scan per
+ *     order, outputs mapped back to H x W and summed; softplus is applied to
+ *     Delta + delta_bias, and a skip term D*u is part of each scan.
+ *   - "从LSTM到Mamba：为什么说双向状态空间模型是处理视觉序列的'潜力股'？",
+ *     section 3.1: bidirectional scan = a forward scan plus a scan of the reversed
+ *     sequence with its own parameters.  The two outputs are SUMMED here (not
+ *     concatenated), with the backward output flipped back to token order.
+ *
+ * Recurrence, per (batch b, direction k, channel d), over scan steps s = 0..L-1
+ * visiting positions p = pi_k(s):
+ *     dt      = Delta_k[d, p] + bias_k[d];   dt = softplus(dt) if requested
+ *     h_n     = exp(dt*A_k[d,n]) * h_n + Bbar_{k,n}(p) * u[d, p]      (n = 0..N-1)
+ *     y_k(p)  = sum_n C_k[g, n, p] * h_n + D_k[d] * u[d, p]
+ * with h = 0 (or a caller-given h0) before the first step, then
+ *     out[d, p] = (sum_k y_k(p)) * (z ? z*sigmoid(z) : 1).
+ * Per-direction Delta, B, C are indexed by position p (not by scan step).
+ * Channel d uses group g = d / (dim / ngroups).
+ *
+ * Everything is float64 and strictly sequential; libm exp/log1p only.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+
+/* Traversal orders of one direction. */
+#define SSOR_ORDER_FWD 0     /* positions 0, 1, ..., L-1 (row-major for a map) */
+#define SSOR_ORDER_REV 1     /* positions L-1, ..., 0                          */
+#define SSOR_ORDER_COL 2     /* column-major over an H x W map                 */
+#define SSOR_ORDER_COL_REV 3 /* reverse of column-major                        */
+
+/* softplus(x) = log(1 + exp(x)), written in the overflow-free form. */
+static double ssor_softplus(double x) {
+    return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));
+}
+
+/* Position visited at scan step s by a direction with the given order, for an
+ * H x W map stored row-major (a plain sequence is H = 1, W = L). */
+static int64_t ssor_position(int order, int64_t s, int64_t H, int64_t W) {
+    int64_t L = H * W;
+    int64_t r;
+    switch (order) {
+    case SSOR_ORDER_FWD: return s;
+    case SSOR_ORDER_REV: return L - 1 - s;
+    case SSOR_ORDER_COL: return (s % H) * W + s / H;
+    case SSOR_ORDER_COL_REV: r = L - 1 - s; return (r % H) * W + r / H;
+    default: return -1;
+    }
+}
+
+/*
+ * ssor_scan: the general oracle.
+ *
+ * Layouts (all float64, C-contiguous):
+ *   u          [batch, dim, L]              L = H*W
+ *   delta      [batch, K, dim, L]
+ *   A          [K*dim, N]
+ *   Bm, Cm     [batch, K, ngroups, N, L]
+ *   Dv         [K*dim]        (NULL: no skip term)
+ *   z          [batch, dim, L] (NULL: no gate)
+ *   bias       [K*dim]        (NULL: zero)
+ *   h0         [batch, K, dim, N] (NULL: zero initial state)
+ *   out        [batch, dim, L]
+ *   last_state [batch, K, dim, N] (NULL: not written)
+ *   orders     [K]  one SSOR_ORDER_* per direction
+ * Returns 0, or -1 on an invalid argument.
+ */
+int ssor_scan(int64_t batch, int64_t dim, int64_t H, int64_t W, int64_t N, int64_t ngroups,
+              int64_t K, const int *orders,
+              const double *u, const double *delta, const double *A, const double *Bm,
+              const double *Cm, const double *Dv, const double *z, const double *bias,
+              int delta_softplus, int zoh, const double *h0, double *out, double *last_state,
+              double *h_work /* scratch of N doubles */) {
+    if (batch < 0 || dim <= 0 || H <= 0 || W <= 0 || N <= 0 || ngroups <= 0 || K <= 0) return -1;
+    if (dim % ngroups != 0) return -1;
+    if (!orders || !u || !delta || !A || !Bm || !Cm || !out || !h_work) return -1;
+    const int64_t L = H * W;
+    const int64_t dpg = dim / ngroups;
+
+    for (int64_t i = 0; i < batch * dim * L; ++i) out[i] = 0.0;
+
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t k = 0; k < K; ++k) {
+            for (int64_t d = 0; d < dim; ++d) {
+                const int64_t g = d / dpg;
+                const double *A_row = A + (k * dim + d) * N;
+                const double Dd = Dv ? Dv[k * dim + d] : 0.0;
+                const double bd = bias ? bias[k * dim + d] : 0.0;
+                const double *u_row = u + (b * dim + d) * L;
+                const double *dl_row = delta + ((b * K + k) * dim + d) * L;
+                const double *B_grp = Bm + ((b * K + k) * ngroups + g) * N * L;
+                const double *C_grp = Cm + ((b * K + k) * ngroups + g) * N * L;
+                double *o_row = out + (b * dim + d) * L;
+                double *h = h_work;
+                for (int64_t n = 0; n < N; ++n)
+                    h[n] = h0 ? h0[((b * K + k) * dim + d) * N + n] : 0.0;
+
+                for (int64_t s = 0; s < L; ++s) {
+                    const int64_t p = ssor_position(orders[k], s, H, W);
+                    if (p < 0) return -1;
+                    double dt = dl_row[p] + bd;
+                    if (delta_softplus) dt = ssor_softplus(dt);
+                    const double up = u_row[p];
+                    double y = 0.0;
+                    for (int64_t n = 0; n < N; ++n) {
+                        const double a = A_row[n];
+                        const double abar = exp(dt * a);
+                        double bbar;
+                        if (zoh && a != 0.0)
+                            bbar = (abar - 1.0) / a * B_grp[n * L + p];   /* (dA)^-1 (e^{dA}-1) dB */
+                        else
+                            bbar = dt * B_grp[n * L + p];                 /* Euler: dB */
+                        h[n] = abar * h[n] + bbar * up;
+                        y += C_grp[n * L + p] * h[n];
+                    }
+                    o_row[p] += y + Dd * up;
+                }
+                if (last_state)
+                    for (int64_t n = 0; n < N; ++n)
+                        last_state[((b * K + k) * dim + d) * N + n] = h[n];
+            }
+        }
+    }
+
+    if (z) {
+        for (int64_t i = 0; i < batch * dim * L; ++i) {
+            const double zi = z[i];
+            out[i] *= zi / (1.0 + exp(-zi));   /* SiLU(z) = z * sigmoid(z) */
+        }
+    }
+    return 0;
+}
+
+/* Exposed for the oracle's own pin tests: the softplus used above. */
+double ssor_softplus_scalar(double x) { return ssor_softplus(x); }
+
+/* Exposed for the oracle's own pin tests: the position map used above. */
+int64_t ssor_position_of(int order, int64_t s, int64_t H, int64_t W) {
+    return ssor_position(order, s, H, W);
+}
