@@ -1,0 +1,207 @@
+/*
+ * ssscan.h -- C ABI of the B300 selective-scan library (libssscan.so).
+ *
+ * The library computes the forward pass of the selective state-space scan of
+ * Mamba (S6) and its two vision variants, on an NVIDIA B300 (sm_103a):
+ *
+ *   ss_selective_scan_fwd  one direction over a sequence
+ *   ss_bidir_scan_fwd      Vision Mamba's bidirectional scan (forward + reversed, summed)
+ *   ss_cross_scan2d_fwd    VMamba's SS2D: four traversal orders of an H x W map, merged by sum
+ *
+ * Sources (page title, section):
+ *   "Mamba Series from Selective State Spaces to Visual State Space Models",
+ *     "mathematical form of the selective SSM": Abar = exp(Delta*A); input matrix
+ *     (Euler form used here) Bbar = Delta*B; Delta = softplus(W_Delta x + b_Delta);
+ *     block diagram "Mamba Block (1D)": output gated by SiLU(z);
+ *     "key code" (cross_scan_fwd, SS2Dv0.forwardv0): the four orders (row-major,
+ *     column-major, and the reverse of each), selective_scan(xs, dts, As, Bs, Cs,
+ *     Ds, delta_bias, delta_softplus), and the merge (flip back, transpose back, sum).
+ *   "From LSTM to Mamba: why bidirectional state-space models suit visual sequences",
+ *     section 3.1: a forward scan plus a scan of the reversed sequence with its own
+ *     parameters.
+ *
+ * Per (batch b, direction k, channel d) the scan visits positions p = pi_k(s),
+ * s = 0..L-1, starting from h = 0:
+ *     dt    = Delta_k[d,p] + delta_bias_k[d];  dt = softplus(dt) if delta_softplus
+ *     h_n   = exp(dt * A_k[d,n]) * h_n + dt * B_k[g,n,p] * u[d,p]          n < dstate
+ *     y_k   = sum_n C_k[g,n,p] * h_n + D_k[d] * u[d,p]
+ *     out[d,p] = (sum_k y_k(p)) * (z ? z*sigmoid(z) : 1)     (z[d,p])
+ * Channel d uses group g = d / (dim / ngroups).  Per-direction Delta, B and C are
+ * indexed by POSITION p (the H x W map order), not by scan step; this is the
+ * layout a pointwise projection of the map produces, and it needs no permuted
+ * copies.
+ *
+ * Layouts: every tensor is dense and C-contiguous (last index fastest).
+ *   dtype ss_dtype io:  u, delta, B, C, z, out          (SS_F32 or SS_BF16)
+ *   float32 always:     A, D, delta_bias, last_state
+ * Rounding: internal arithmetic is float32; out is rounded to the I/O type
+ * (round-to-nearest-even).
+ *
+ * Ownership and synchronisation: the caller owns every buffer.  All tensor
+ * pointers are DEVICE pointers.  The library never allocates device memory and
+ * never synchronises the stream (except ss_get_device_status); work is enqueued
+ * on `stream` and the call returns.  Kernel faults surface on the caller's next
+ * synchronisation.  Each call validates its arguments before launching
+ * anything; on error nothing is launched.
+ *
+ * Errors: every function returns ss_status; ss_last_error_string() gives a
+ * thread-local message for the last failing call on the calling thread.
+ */
+#ifndef SSSCAN_H
+#define SSSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle type as cudaStream_t (struct CUstream_st*); NULL = legacy default stream. */
+typedef struct CUstream_st *ss_stream_t;
+
+typedef int ss_status;
+#define SS_OK 0
+#define SS_ERR_INVALID_ARG 1  /* null required pointer, negative size, dim % ngroups != 0, aliasing */
+#define SS_ERR_UNSUPPORTED 2  /* dstate not in {1,2,4,8,16,32,64}, unknown dtype, shape beyond limits */
+#define SS_ERR_ALIGNMENT 3    /* a tensor base pointer is not 16-byte aligned */
+#define SS_ERR_WORKSPACE 4    /* workspace missing or smaller than ss_workspace_bytes() */
+#define SS_ERR_CUDA 5         /* a CUDA runtime/driver call failed (launch, tensor-map encode) */
+#define SS_ERR_TIMEOUT 6      /* a kernel gave up a bounded wait (reported by ss_get_device_status) */
+
+typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
+
+/* Direction order codes of ss_cross_scan2d_fwd, in the order its tensors stack them. */
+#define SS_DIR_ROW 0     /* row-major: position t                          */
+#define SS_DIR_COL 1     /* column-major: position (t % H) * W + t / H     */
+#define SS_DIR_ROW_REV 2 /* reversed row-major                             */
+#define SS_DIR_COL_REV 3 /* reversed column-major                          */
+
+/* Kinds for ss_workspace_bytes. */
+#define SS_KIND_SCAN 0
+#define SS_KIND_BIDIR 1
+#define SS_KIND_CROSS2D 2
+
+/*
+ * ss_selective_scan_fwd -- one forward direction (Mamba S6 selective scan).
+ *
+ *   u          [batch, dim, seqlen]            io
+ *   delta      [batch, dim, seqlen]            io    (raw Delta, before bias/softplus)
+ *   A          [dim, dstate]                   float (already negative: A = -exp(A_log))
+ *   B, C       [batch, ngroups, dstate, seqlen] io
+ *   D          [dim]                           float, nullable (no skip term)
+ *   z          [batch, dim, seqlen]            io, nullable (no gate)
+ *   delta_bias [dim]                           float, nullable (zero)
+ *   delta_softplus                             0 or 1
+ *   out        [batch, dim, seqlen]            io, must not overlap any input
+ *   last_state [batch, dim, dstate]            float, nullable; the state after the last step
+ *   workspace  device scratch of at least ss_workspace_bytes(SS_KIND_SCAN, ...) bytes;
+ *              may be NULL when that is 0.  Contents on entry are ignored.
+ *
+ * Empty inputs (batch, dim or seqlen = 0) return SS_OK without touching memory.
+ * Long sequences with little batch*dim parallelism run a chunked path (per-chunk
+ * local states, a carry pass, a fix-up pass) that uses the workspace.
+ */
+ss_status ss_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dstate,
+                                int ngroups, ss_dtype io, const void *u, const void *delta,
+                                const float *A, const void *B, const void *C, const float *D,
+                                const void *z, const float *delta_bias, int delta_softplus,
+                                void *out, float *last_state, void *workspace,
+                                size_t workspace_bytes, ss_stream_t stream);
+
+/* Options of ss_selective_scan_fwd_opts.  Zero-initialise, then set fields. */
+typedef struct ss_scan_options {
+    /* Sequence split.  0: automatic; 1: one pass over the whole sequence;
+     * n >= 2: the chunked long-sequence path with at most n L-chunks (each a
+     * multiple of the kernel's step tile; fewer if the sequence is short). */
+    int chunks;
+    int reserved[7]; /* must be zero */
+} ss_scan_options;
+
+/* ss_selective_scan_fwd with options (NULL options = automatic). */
+ss_status ss_selective_scan_fwd_opts(int64_t batch, int64_t dim, int64_t seqlen, int dstate,
+                                     int ngroups, ss_dtype io, const void *u, const void *delta,
+                                     const float *A, const void *B, const void *C,
+                                     const float *D, const void *z, const float *delta_bias,
+                                     int delta_softplus, void *out, float *last_state,
+                                     void *workspace, size_t workspace_bytes,
+                                     const ss_scan_options *options, ss_stream_t stream);
+
+/*
+ * ss_bidir_scan_fwd -- Vision Mamba bidirectional scan: direction 0 visits
+ * positions 0..L-1, direction 1 visits L-1..0, each with its own parameters;
+ * the two outputs are summed and then gated once by SiLU(z).
+ *
+ *   u          [batch, dim, seqlen]               io
+ *   delta      [batch, 2, dim, seqlen]            io (indexed by position)
+ *   A          [2*dim, dstate]                    float
+ *   B, C       [batch, 2, ngroups, dstate, seqlen] io (indexed by position)
+ *   D, delta_bias [2*dim]                         float, nullable
+ *   z          [batch, dim, seqlen]               io, nullable
+ *   out        [batch, dim, seqlen]               io
+ *   last_state [batch, 2, dim, dstate]            float, nullable (direction 1: state after position 0)
+ * No workspace is needed (the merge is done on chip); pass NULL, 0.
+ */
+ss_status ss_bidir_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int ngroups,
+                            ss_dtype io, const void *u, const void *delta, const float *A,
+                            const void *B, const void *C, const float *D, const void *z,
+                            const float *delta_bias, int delta_softplus, void *out,
+                            float *last_state, void *workspace, size_t workspace_bytes,
+                            ss_stream_t stream);
+
+/*
+ * ss_cross_scan2d_fwd -- VMamba SS2D cross-scan, four selective scans and
+ * cross-merge, fused: no permuted copies of the map are made.
+ *
+ *   u          [batch, dim, H, W]                 io
+ *   delta      [batch, 4, dim, H, W]              io (direction k = SS_DIR_*, by position)
+ *   A          [4*dim, dstate]                    float
+ *   B, C       [batch, 4, ngroups, dstate, H, W]  io (by position)
+ *   D, delta_bias [4*dim]                         float, nullable
+ *   z          [batch, dim, H, W]                 io, nullable (VMamba gates after a norm,
+ *                                                  so its SS2D passes NULL)
+ *   out        [batch, dim, H, W]                 io: sum over the four directions
+ *   last_state [batch, 4, dim, dstate]            float, nullable
+ * The whole map of a channel is merged in shared memory: H*W is limited by the
+ * per-block shared-memory size (SS_ERR_UNSUPPORTED beyond it).  No workspace.
+ */
+ss_status ss_cross_scan2d_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, int dstate,
+                              int ngroups, ss_dtype io, const void *u, const void *delta,
+                              const float *A, const void *B, const void *C, const float *D,
+                              const float *delta_bias, int delta_softplus, const void *z,
+                              void *out, float *last_state, void *workspace,
+                              size_t workspace_bytes, ss_stream_t stream);
+
+/* Workspace bytes a call of the given kind and shape needs (0 if none), for
+ * either I/O dtype (the larger of the two).  For SS_KIND_CROSS2D pass
+ * seqlen = H*W.  Host computation only. */
+size_t ss_workspace_bytes(int kind, int64_t batch, int64_t dim, int64_t seqlen, int dstate);
+
+/* Same for ss_selective_scan_fwd_opts with the given options. */
+size_t ss_workspace_bytes_opts(int kind, int64_t batch, int64_t dim, int64_t seqlen, int dstate,
+                               const ss_scan_options *options);
+
+/* Reads and clears the library's device error word for the current device after
+ * synchronising `stream` (this call does synchronise).  Returns SS_OK, or
+ * SS_ERR_TIMEOUT if a kernel abandoned a bounded wait since the last call, or
+ * SS_ERR_CUDA if the synchronisation itself failed. */
+ss_status ss_get_device_status(ss_stream_t stream);
+
+/* Thread-local message describing the last error returned on this thread. */
+const char *ss_last_error_string(void);
+
+/* Version string of the library build. */
+const char *ss_version(void);
+
+/* Diagnostics: sets the time budget, in nanoseconds, of every bounded wait in
+ * the kernels on the current device (default 1 s; 0 restores the default).
+ * A wait that runs out records SS_ERR_TIMEOUT for ss_get_device_status, lets
+ * the copies it issued land, and ends its CTA; outputs of that call are then
+ * undefined.  Used to test the timeout path. */
+ss_status ss_debug_set_wait_budget_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSSCAN_H */

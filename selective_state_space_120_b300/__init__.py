@@ -1,0 +1,168 @@
+"""B300-native selective state-space scan (Mamba S6, Vision Mamba bidirectional,
+VMamba SS2D) -- torch-facing wrappers over the C ABI of libssscan.so.
+
+The wrappers check shapes and dtypes, allocate outputs and workspace with
+PyTorch, and call the library on the current CUDA stream.  All arithmetic runs
+in the library's sm_103a kernels; there is no fallback.
+
+    out = selective_scan_fwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus=True)
+    out = bidir_scan_fwd(u, delta2, A2, B2, C2, D2, z, bias2)
+    out = cross_scan2d_fwd(u_map, delta4, A4, B4, C4, D4, bias4)
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _binding as _b
+from ._binding import SSError, load as load_library, version  # noqa: F401
+
+__all__ = ["selective_scan_fwd", "bidir_scan_fwd", "cross_scan2d_fwd", "device_status",
+           "workspace_bytes", "SSError", "load_library", "version"]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _io_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return _b.SS_BF16
+    if t.dtype == torch.float32:
+        return _b.SS_F32
+    raise TypeError(f"I/O tensors must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check_io(name, t, dtype, device, shape=None):
+    torch = _torch()
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _stream(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def workspace_bytes(kind: int, batch: int, dim: int, seqlen: int, dstate: int, chunks: int = 0):
+    return _b.workspace_bytes(kind, batch, dim, seqlen, dstate, chunks)
+
+
+def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                       return_last_state=False, out=None, chunks=0, workspace=None, stream=None):
+    """One-direction selective scan.
+
+    u, delta, z: [batch, dim, L]; A: [dim, N] float32; B, C: [batch, G, N, L];
+    D, delta_bias: [dim] float32.  Returns out [batch, dim, L] (and last_state
+    [batch, dim, N] float32 if requested).  ``chunks`` forces the sequence split
+    (0 automatic, 1 single pass, n >= 2 chunked path); ``workspace`` is an
+    optional preallocated uint8 CUDA tensor."""
+    torch = _torch()
+    lib = _b.load()
+    batch, dim, L = u.shape
+    G, N = B.shape[1], B.shape[2]
+    io, dev = u.dtype, u.device
+    _check_io("u", u, io, dev)
+    _check_io("delta", delta, io, dev, (batch, dim, L))
+    _check_io("B", B, io, dev, (batch, G, N, L))
+    _check_io("C", C, io, dev, (batch, G, N, L))
+    _check_io("z", z, io, dev, (batch, dim, L))
+    _check_io("A", A, torch.float32, dev, (dim, N))
+    _check_io("D", D, torch.float32, dev, (dim,))
+    _check_io("delta_bias", delta_bias, torch.float32, dev, (dim,))
+    if out is None:
+        out = torch.empty_like(u)
+    _check_io("out", out, io, dev, (batch, dim, L))
+    last = torch.empty(batch, dim, N, dtype=torch.float32, device=dev) if return_last_state else None
+    opts = _b.options(chunks)
+    wsb = int(lib.ss_workspace_bytes_opts(_b.SS_KIND_SCAN, batch, dim, L, N, ctypes.byref(opts)))
+    if wsb and (workspace is None or workspace.numel() < wsb):
+        workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    ws_ptr = _ptr(workspace) if wsb else None
+    ws_len = workspace.numel() if wsb else 0
+    _b.check(lib.ss_selective_scan_fwd_opts(
+        batch, dim, L, N, G, _io_code(u), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+        _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(out), _ptr(last),
+        ws_ptr, ws_len, ctypes.byref(opts), _stream(stream, dev)))
+    return (out, last) if return_last_state else out
+
+
+def bidir_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                   return_last_state=False, out=None, stream=None):
+    """Bidirectional scan: delta [batch, 2, dim, L]; A [2*dim, N]; B, C [batch, 2, G, N, L];
+    D, delta_bias [2*dim].  Returns out [batch, dim, L] (and last_state [batch, 2, dim, N])."""
+    torch = _torch()
+    lib = _b.load()
+    batch, dim, L = u.shape
+    G, N = B.shape[2], B.shape[3]
+    io, dev = u.dtype, u.device
+    _check_io("u", u, io, dev)
+    _check_io("delta", delta, io, dev, (batch, 2, dim, L))
+    _check_io("B", B, io, dev, (batch, 2, G, N, L))
+    _check_io("C", C, io, dev, (batch, 2, G, N, L))
+    _check_io("z", z, io, dev, (batch, dim, L))
+    _check_io("A", A, torch.float32, dev, (2 * dim, N))
+    _check_io("D", D, torch.float32, dev, (2 * dim,))
+    _check_io("delta_bias", delta_bias, torch.float32, dev, (2 * dim,))
+    if out is None:
+        out = torch.empty_like(u)
+    _check_io("out", out, io, dev, (batch, dim, L))
+    last = torch.empty(batch, 2, dim, N, dtype=torch.float32, device=dev) if return_last_state else None
+    _b.check(lib.ss_bidir_scan_fwd(
+        batch, dim, L, N, G, _io_code(u), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+        _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(out), _ptr(last),
+        None, 0, _stream(stream, dev)))
+    return (out, last) if return_last_state else out
+
+
+def cross_scan2d_fwd(u, delta, A, B, C, D=None, delta_bias=None, delta_softplus=True, z=None,
+                     return_last_state=False, out=None, stream=None):
+    """SS2D: u [batch, dim, H, W]; delta [batch, 4, dim, H, W]; A [4*dim, N];
+    B, C [batch, 4, G, N, H, W]; D, delta_bias [4*dim].  Returns out [batch, dim, H, W]
+    (and last_state [batch, 4, dim, N])."""
+    torch = _torch()
+    lib = _b.load()
+    batch, dim, H, W = u.shape
+    G, N = B.shape[2], B.shape[3]
+    io, dev = u.dtype, u.device
+    _check_io("u", u, io, dev)
+    _check_io("delta", delta, io, dev, (batch, 4, dim, H, W))
+    _check_io("B", B, io, dev, (batch, 4, G, N, H, W))
+    _check_io("C", C, io, dev, (batch, 4, G, N, H, W))
+    _check_io("z", z, io, dev, (batch, dim, H, W))
+    _check_io("A", A, torch.float32, dev, (4 * dim, N))
+    _check_io("D", D, torch.float32, dev, (4 * dim,))
+    _check_io("delta_bias", delta_bias, torch.float32, dev, (4 * dim,))
+    if out is None:
+        out = torch.empty_like(u)
+    _check_io("out", out, io, dev, (batch, dim, H, W))
+    last = torch.empty(batch, 4, dim, N, dtype=torch.float32, device=dev) if return_last_state else None
+    _b.check(lib.ss_cross_scan2d_fwd(
+        batch, dim, H, W, N, G, _io_code(u), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+        _ptr(D), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(z), _ptr(out), _ptr(last),
+        None, 0, _stream(stream, dev)))
+    return (out, last) if return_last_state else out
+
+
+def device_status(stream=None) -> None:
+    """Synchronises the stream and raises SSError if a kernel abandoned a bounded wait."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _b.check(_b.load().ss_get_device_status(_stream(stream, dev)))

@@ -1,0 +1,107 @@
+"""ctypes binding of libssscan.so (the C ABI in include/ssscan.h).
+
+Argument marshalling only: every step of the scan runs in the library's CUDA
+kernels.  If the compiled library is missing the calls raise: there is no CPU
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libssscan.so")
+
+SS_OK = 0
+SS_ERR_INVALID_ARG = 1
+SS_ERR_UNSUPPORTED = 2
+SS_ERR_ALIGNMENT = 3
+SS_ERR_WORKSPACE = 4
+SS_ERR_CUDA = 5
+SS_ERR_TIMEOUT = 6
+SS_F32 = 0
+SS_BF16 = 1
+SS_KIND_SCAN, SS_KIND_BIDIR, SS_KIND_CROSS2D = 0, 1, 2
+STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_ARG", 2: "SS_ERR_UNSUPPORTED",
+                3: "SS_ERR_ALIGNMENT", 4: "SS_ERR_WORKSPACE", 5: "SS_ERR_CUDA",
+                6: "SS_ERR_TIMEOUT"}
+
+# Every function the header declares.
+EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_opts", "ss_bidir_scan_fwd",
+           "ss_cross_scan2d_fwd", "ss_workspace_bytes", "ss_workspace_bytes_opts",
+           "ss_get_device_status", "ss_last_error_string", "ss_version",
+           "ss_debug_set_wait_budget_ns")
+
+
+class SSError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class ScanOptions(ctypes.Structure):
+    _fields_ = [("chunks", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads and types the library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"libssscan.so not found at {path}; run "
+                               "`python -m selective_state_space_120_b300.build`")
+        lib = ctypes.CDLL(path)
+        i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+        scan_args = [i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp,
+                     vp, sz]
+        lib.ss_selective_scan_fwd.argtypes = scan_args + [vp]
+        lib.ss_selective_scan_fwd_opts.argtypes = scan_args + [ctypes.POINTER(ScanOptions), vp]
+        lib.ss_bidir_scan_fwd.argtypes = scan_args + [vp]
+        lib.ss_cross_scan2d_fwd.argtypes = [i64, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp,
+                                            vp, vp, i32, vp, vp, vp, vp, sz, vp]
+        for f in ("ss_selective_scan_fwd", "ss_selective_scan_fwd_opts", "ss_bidir_scan_fwd",
+                  "ss_cross_scan2d_fwd", "ss_get_device_status", "ss_debug_set_wait_budget_ns"):
+            getattr(lib, f).restype = ctypes.c_int
+        lib.ss_workspace_bytes.argtypes = [i32, i64, i64, i64, i32]
+        lib.ss_workspace_bytes.restype = sz
+        lib.ss_workspace_bytes_opts.argtypes = [i32, i64, i64, i64, i32,
+                                                ctypes.POINTER(ScanOptions)]
+        lib.ss_workspace_bytes_opts.restype = sz
+        lib.ss_get_device_status.argtypes = [vp]
+        lib.ss_last_error_string.restype = ctypes.c_char_p
+        lib.ss_version.restype = ctypes.c_char_p
+        lib.ss_debug_set_wait_budget_ns.argtypes = [ctypes.c_uint64]
+        _lib = lib
+        return lib
+
+
+def check(status: int) -> None:
+    if status != SS_OK:
+        raise SSError(status, load().ss_last_error_string().decode())
+
+
+def last_error() -> str:
+    return load().ss_last_error_string().decode()
+
+
+def version() -> str:
+    return load().ss_version().decode()
+
+
+def options(chunks: int = 0) -> ScanOptions:
+    o = ScanOptions()
+    o.chunks = int(chunks)
+    return o
+
+
+def workspace_bytes(kind: int, batch: int, dim: int, seqlen: int, dstate: int,
+                    chunks: int = 0) -> int:
+    o = options(chunks)
+    return int(load().ss_workspace_bytes_opts(kind, batch, dim, seqlen, dstate, ctypes.byref(o)))

@@ -1,0 +1,261 @@
+// C ABI of the selective-scan library: argument validation and dispatch.
+// The arithmetic is in the kernels (ss_kernels.cu); nothing here touches tensor
+// data, so every check below runs before any work is enqueued.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <initializer_list>
+
+#include "ss_internal.h"
+#include "ssscan.h"
+
+namespace ssi {
+
+namespace {
+thread_local char g_msg[512] = "no error";
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Byte range [p, p + n) for overlap checks.
+struct Span {
+    const char *p;
+    int64_t n;
+};
+bool overlaps(Span a, Span b) {
+    if (!a.p || !b.p || a.n <= 0 || b.n <= 0) return false;
+    return a.p < b.p + b.n && b.p < a.p + a.n;
+}
+
+bool valid_dstate(int n) {
+    return n == 1 || n == 2 || n == 4 || n == 8 || n == 16 || n == 32 || n == 64;
+}
+
+// Common checks of all three calls.  Returns SS_OK and sets *empty when there
+// is nothing to compute.
+ss_status check_common(const char *fn, int64_t batch, int64_t dim, int64_t L, int dstate,
+                       int ngroups, int io, int K, const void *u, const void *delta,
+                       const float *A, const void *B, const void *C, const float *D,
+                       const void *z, const float *bias, const void *out,
+                       const float *last_state, bool *empty) {
+    *empty = false;
+    if (batch < 0 || dim < 0 || L < 0)
+        return fail(SS_ERR_INVALID_ARG, "%s: negative size (batch=%lld dim=%lld seqlen=%lld)", fn,
+                    (long long)batch, (long long)dim, (long long)L);
+    if (io != SS_F32 && io != SS_BF16)
+        return fail(SS_ERR_UNSUPPORTED, "%s: unknown I/O dtype %d", fn, io);
+    if (!valid_dstate(dstate))
+        return fail(SS_ERR_UNSUPPORTED, "%s: dstate %d is not one of 1,2,4,8,16,32,64", fn, dstate);
+    if (ngroups < 1) return fail(SS_ERR_INVALID_ARG, "%s: ngroups must be >= 1", fn);
+    if (dim > 0 && dim % ngroups != 0)
+        return fail(SS_ERR_INVALID_ARG, "%s: dim %lld is not a multiple of ngroups %d", fn,
+                    (long long)dim, ngroups);
+    if (batch == 0 || dim == 0 || L == 0) {
+        *empty = true;
+        return SS_OK;
+    }
+    if (!u || !delta || !A || !B || !C || !out)
+        return fail(SS_ERR_INVALID_ARG, "%s: u, delta, A, B, C and out are required", fn);
+    const void *ptrs[] = {u, delta, A, B, C, D, z, bias, out, last_state};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p))
+            return fail(SS_ERR_ALIGNMENT, "%s: tensor at %p is not 16-byte aligned", fn, p);
+    if (batch * dim >= (1ll << 31) || L >= (1ll << 31) || batch * ngroups * dstate >= (1ll << 31) ||
+        batch * K * dim >= (1ll << 31) || dim / ngroups >= (1ll << 30))
+        return fail(SS_ERR_UNSUPPORTED, "%s: shape exceeds the 2^31 row/position limits", fn);
+    const int64_t es = io == SS_BF16 ? 2 : 4;
+    const int64_t nel = batch * dim * L;
+    const Span so{static_cast<const char *>(out), nel * es};
+    const Span ins[] = {{static_cast<const char *>(u), nel * es},
+                        {static_cast<const char *>(delta), nel * K * es},
+                        {static_cast<const char *>(B), batch * K * ngroups * dstate * L * es},
+                        {static_cast<const char *>(C), batch * K * ngroups * dstate * L * es},
+                        {static_cast<const char *>(z), z ? nel * es : 0},
+                        {reinterpret_cast<const char *>(last_state),
+                         last_state ? batch * K * dim * dstate * 4 : 0}};
+    for (const Span &s : ins)
+        if (overlaps(so, s)) return fail(SS_ERR_INVALID_ARG, "%s: out overlaps an input or last_state", fn);
+    return SS_OK;
+}
+
+ss_status check_workspace(const char *fn, size_t need, const void *ws, size_t have) {
+    if (need == 0) return SS_OK;
+    if (!ws || have < need)
+        return fail(SS_ERR_WORKSPACE, "%s: needs %zu bytes of workspace, got %zu%s", fn, need, have,
+                    ws ? "" : " (null)");
+    if (!aligned16(ws)) return fail(SS_ERR_ALIGNMENT, "%s: workspace is not 16-byte aligned", fn);
+    return SS_OK;
+}
+
+ScanArgs scan_args(int64_t batch, int64_t dim, int64_t L, int dstate, int ngroups, int io,
+                   const void *u, const void *delta, const float *A, const void *B, const void *C,
+                   const float *D, const void *z, const float *bias, int softplus, void *out,
+                   float *last_state, void *ws, size_t ws_bytes, ss_stream_t stream) {
+    ScanArgs a;
+    a.batch = batch;
+    a.dim = dim;
+    a.L = L;
+    a.H = 1;
+    a.W = L;
+    a.N = dstate;
+    a.G = ngroups;
+    a.io = io;
+    a.u = u;
+    a.delta = delta;
+    a.A = A;
+    a.B = B;
+    a.C = C;
+    a.D = D;
+    a.z = z;
+    a.bias = bias;
+    a.softplus = softplus ? 1 : 0;
+    a.out = out;
+    a.last_state = last_state;
+    a.ws = ws;
+    a.ws_bytes = ws_bytes;
+    a.stream = stream;
+    return a;
+}
+
+size_t ws_scan1d_any_dtype(int64_t batch, int64_t dim, int64_t L, int dstate, int chunks) {
+    if (batch <= 0 || dim <= 0 || L <= 0 || !valid_dstate(dstate)) return 0;
+    size_t best = 0;
+    for (int io : {SS_F32, SS_BF16}) {
+        ScanArgs a;
+        a.batch = batch;
+        a.dim = dim;
+        a.L = L;
+        a.W = L;
+        a.N = dstate;
+        a.io = io;
+        a.chunks = chunks;
+        const size_t w = scan1d_workspace_bytes(a);
+        if (w > best) best = w;
+    }
+    return best;
+}
+
+}  // namespace
+
+ss_status fail(ss_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+}  // namespace ssi
+
+using namespace ssi;
+
+extern "C" {
+
+ss_status ss_selective_scan_fwd_opts(int64_t batch, int64_t dim, int64_t seqlen, int dstate,
+                                     int ngroups, ss_dtype io, const void *u, const void *delta,
+                                     const float *A, const void *B, const void *C, const float *D,
+                                     const void *z, const float *delta_bias, int delta_softplus,
+                                     void *out, float *last_state, void *workspace,
+                                     size_t workspace_bytes, const ss_scan_options *options,
+                                     ss_stream_t stream) {
+    static const char *fn = "ss_selective_scan_fwd";
+    bool empty = false;
+    ss_status st = check_common(fn, batch, dim, seqlen, dstate, ngroups, io, 1, u, delta, A, B, C,
+                                D, z, delta_bias, out, last_state, &empty);
+    if (st != SS_OK || empty) return st;
+    int chunks = 0;
+    if (options) {
+        for (int r : options->reserved)
+            if (r != 0) return fail(SS_ERR_INVALID_ARG, "%s: reserved option fields must be zero", fn);
+        if (options->chunks < 0) return fail(SS_ERR_INVALID_ARG, "%s: options.chunks < 0", fn);
+        chunks = options->chunks;
+    }
+    ScanArgs a = scan_args(batch, dim, seqlen, dstate, ngroups, io, u, delta, A, B, C, D, z,
+                           delta_bias, delta_softplus, out, last_state, workspace,
+                           workspace_bytes, stream);
+    a.chunks = chunks;
+    if ((st = check_workspace(fn, scan1d_workspace_bytes(a), workspace, workspace_bytes))) return st;
+    return launch_scan1d(a);
+}
+
+ss_status ss_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dstate,
+                                int ngroups, ss_dtype io, const void *u, const void *delta,
+                                const float *A, const void *B, const void *C, const float *D,
+                                const void *z, const float *delta_bias, int delta_softplus,
+                                void *out, float *last_state, void *workspace,
+                                size_t workspace_bytes, ss_stream_t stream) {
+    return ss_selective_scan_fwd_opts(batch, dim, seqlen, dstate, ngroups, io, u, delta, A, B, C,
+                                      D, z, delta_bias, delta_softplus, out, last_state,
+                                      workspace, workspace_bytes, nullptr, stream);
+}
+
+ss_status ss_bidir_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int ngroups,
+                            ss_dtype io, const void *u, const void *delta, const float *A,
+                            const void *B, const void *C, const float *D, const void *z,
+                            const float *delta_bias, int delta_softplus, void *out,
+                            float *last_state, void *workspace, size_t workspace_bytes,
+                            ss_stream_t stream) {
+    static const char *fn = "ss_bidir_scan_fwd";
+    (void)workspace;
+    (void)workspace_bytes;
+    bool empty = false;
+    ss_status st = check_common(fn, batch, dim, seqlen, dstate, ngroups, io, 2, u, delta, A, B, C,
+                                D, z, delta_bias, out, last_state, &empty);
+    if (st != SS_OK || empty) return st;
+    ScanArgs a = scan_args(batch, dim, seqlen, dstate, ngroups, io, u, delta, A, B, C, D, z,
+                           delta_bias, delta_softplus, out, last_state, nullptr, 0, stream);
+    a.K = 2;
+    a.orders[0] = ORD_ROW;
+    a.orders[1] = ORD_ROW_REV;
+    return launch_multidir(a);
+}
+
+ss_status ss_cross_scan2d_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, int dstate,
+                              int ngroups, ss_dtype io, const void *u, const void *delta,
+                              const float *A, const void *B, const void *C, const float *D,
+                              const float *delta_bias, int delta_softplus, const void *z,
+                              void *out, float *last_state, void *workspace,
+                              size_t workspace_bytes, ss_stream_t stream) {
+    static const char *fn = "ss_cross_scan2d_fwd";
+    (void)workspace;
+    (void)workspace_bytes;
+    if (H < 0 || W < 0) return fail(SS_ERR_INVALID_ARG, "%s: negative map size", fn);
+    if (H >= (1ll << 31) || W >= (1ll << 31) || (H > 0 && W > (INT64_MAX / H)))
+        return fail(SS_ERR_UNSUPPORTED, "%s: map too large", fn);
+    bool empty = false;
+    ss_status st = check_common(fn, batch, dim, H * W, dstate, ngroups, io, 4, u, delta, A, B, C,
+                                D, z, delta_bias, out, last_state, &empty);
+    if (st != SS_OK || empty) return st;
+    ScanArgs a = scan_args(batch, dim, H * W, dstate, ngroups, io, u, delta, A, B, C, D, z,
+                           delta_bias, delta_softplus, out, last_state, nullptr, 0, stream);
+    a.K = 4;
+    a.H = H;
+    a.W = W;
+    a.orders[0] = ORD_ROW;
+    a.orders[1] = ORD_COL;
+    a.orders[2] = ORD_ROW_REV;
+    a.orders[3] = ORD_COL_REV;
+    return launch_multidir(a);
+}
+
+size_t ss_workspace_bytes_opts(int kind, int64_t batch, int64_t dim, int64_t seqlen, int dstate,
+                               const ss_scan_options *options) {
+    if (kind != SS_KIND_SCAN) return 0;  // the multi-direction calls merge on chip
+    return ws_scan1d_any_dtype(batch, dim, seqlen, dstate, options ? options->chunks : 0);
+}
+
+size_t ss_workspace_bytes(int kind, int64_t batch, int64_t dim, int64_t seqlen, int dstate) {
+    return ss_workspace_bytes_opts(kind, batch, dim, seqlen, dstate, nullptr);
+}
+
+ss_status ss_get_device_status(ss_stream_t stream) { return read_device_status(stream); }
+
+ss_status ss_debug_set_wait_budget_ns(uint64_t ns) {
+    return set_wait_budget(ns ? (unsigned long long)ns : 1000000000ull);
+}
+
+const char *ss_last_error_string(void) { return g_msg; }
+
+const char *ss_version(void) { return "ssscan 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,210 @@
+// Device-side building blocks of the selective-scan kernels (sm_103a).
+//
+// Math follows "Mamba Series from Selective State Spaces to Visual State Space
+// Models", section "mathematical form of the selective SSM":
+//   Abar = exp(Delta*A), Bbar*u = Delta*B*u, Delta = softplus(raw + bias),
+// and the Mamba block's SiLU gate.  Exponentials run on the SFU as base-2
+// exponentials: A is pre-scaled by log2(e) once per channel, so
+// exp(Delta*A) = ex2(Delta * A*log2(e)).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace ssk {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr unsigned kFull = 0xffffffffu;
+
+// Status word of the library on each device: bit 0 = a bounded wait gave up.
+// (All kernels live in one translation unit, which includes this header once.)
+__device__ unsigned int g_status = 0;
+// Time budget (ns) of every bounded wait; 1 s unless changed for diagnostics.
+__device__ unsigned long long g_wait_budget_ns = 1000000000ull;
+
+// ------------------------------------------------------------------ SFU math
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// softplus(x) = ln(1 + e^x).  With e = 2^(x*log2 e):
+//   e < 1/32 : the Taylor series ln(1+e) = e - e^2/2 + e^3/3 - e^4/4
+//              (dropped terms below e^5/5, i.e. relative error < 2e-7), which
+//              keeps full relative accuracy for tiny Delta where ln(1+e)
+//              computed through 1+e would lose it;
+//   otherwise: ln2 * log2(1 + e);
+//   x > 15   : x itself (the two differ by less than 3.1e-7 relative).
+__device__ __forceinline__ float softplus(float x) {
+    const float e = ex2(x * kLog2e);
+    const float series = e * fmaf(e, fmaf(e, fmaf(e, -0.25f, 0.333333343f), -0.5f), 1.0f);
+    const float via_log = kLn2 * lg2(1.0f + e);
+    const float r = (e < 0.03125f) ? series : via_log;
+    return (x > 15.0f) ? x : r;
+}
+
+// SiLU(z) = z * sigmoid(z) = z / (1 + e^-z).  For z -> -inf the exponential
+// overflows to +inf, the reciprocal to 0 and the result to -0.
+__device__ __forceinline__ float silu(float z) { return z * rcp(1.0f + ex2(-z * kLog2e)); }
+
+// ------------------------------------------------------------------ I/O types
+template <typename IO> struct IOT;
+template <> struct IOT<float> {
+    static __device__ __forceinline__ float from_f(float v) { return v; }
+    static __device__ __forceinline__ float load(const float *p) { return __ldg(p); }
+};
+template <> struct IOT<__nv_bfloat16> {
+    static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+    static __device__ __forceinline__ float load(const __nv_bfloat16 *p) {
+        const unsigned short b = __ldg(reinterpret_cast<const unsigned short *>(p));
+        return __uint_as_float(static_cast<uint32_t>(b) << 16);
+    }
+};
+
+// Unpacks a 32-bit word of the I/O type into floats (2 bf16 values or 1 float).
+__device__ __forceinline__ void unpack_word(uint32_t w, float *dst, __nv_bfloat16 *) {
+    dst[0] = __uint_as_float(w << 16);
+    dst[1] = __uint_as_float(w & 0xffff0000u);
+}
+__device__ __forceinline__ void unpack_word(uint32_t w, float *dst, float *) {
+    dst[0] = __uint_as_float(w);
+}
+
+// ------------------------------------------------------------------ smem tiles
+// Raw tiles are written by TMA with 64-byte rows and the 64-byte swizzle:
+// address bits [7:8] are XORed into bits [4:5] (16-byte chunk index).  Tiles
+// start on 1024-byte boundaries, so offsets within a tile can be swizzled alone.
+__device__ __forceinline__ int swz64(int off) { return off ^ (((off >> 7) & 3) << 4); }
+
+// Step-pair slots of the prepared (Delta', x) and (gate, D*u*gate) rows are
+// XOR-swizzled inside groups of eight 16-byte slots so that the prep lanes,
+// which each own a run of consecutive slots, store with few bank conflicts.
+__device__ __forceinline__ int swz_slot(int tp) { return tp ^ ((tp >> 3) & 7); }
+
+// Reads E consecutive I/O elements of row `row` of a swizzled 64-byte-row tile,
+// starting at column col0, widened to float.
+template <typename IO, int E>
+__device__ __forceinline__ void load_tile_row(const uint8_t *tile, int row, int col0, float *v) {
+    constexpr int ES = sizeof(IO);
+    constexpr int BYTES = E * ES;
+    constexpr int PER = 4 / ES;  // elements per 32-bit word
+    const int off = row * 64 + col0 * ES;
+    if constexpr (BYTES >= 16) {
+#pragma unroll
+        for (int c = 0; c < BYTES / 16; ++c) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(tile + swz64(off + 16 * c));
+            float *d = v + (16 / ES) * c;
+            unpack_word(w.x, d + 0 * PER, (IO *)nullptr);
+            unpack_word(w.y, d + 1 * PER, (IO *)nullptr);
+            unpack_word(w.z, d + 2 * PER, (IO *)nullptr);
+            unpack_word(w.w, d + 3 * PER, (IO *)nullptr);
+        }
+    } else if constexpr (BYTES == 8) {
+        const uint2 w = *reinterpret_cast<const uint2 *>(tile + swz64(off));
+        unpack_word(w.x, v, (IO *)nullptr);
+        unpack_word(w.y, v + PER, (IO *)nullptr);
+    } else {
+        static_assert(BYTES == 4, "prep lanes read at least one 32-bit word");
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(tile + swz64(off));
+        unpack_word(w, v, (IO *)nullptr);
+    }
+}
+
+// ------------------------------------------------------------------ mbarrier / TMA
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Waits for the phase with the given parity to complete, for at most `budget`
+// nanoseconds.  Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t budget) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > budget) return false;
+    }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void report_timeout() { atomicOr(&g_status, 1u); }
+
+// ------------------------------------------------------------------ lane-group reduction
+// R lanes (consecutive, R a power of two) each hold R partial sums v[0..R): one
+// per step of an R-step block.  Afterwards the lane with group index g holds the
+// sum over the R lanes of v[g].  log2(R) butterfly rounds; each round halves the
+// values a lane keeps and exchanges the other half with its partner.
+template <int R>
+__device__ __forceinline__ float transpose_reduce(float (&v)[R], int g) {
+    if constexpr (R == 1) {
+        return v[0];
+    } else {
+#pragma unroll
+        for (int m = R / 2; m >= 1; m >>= 1) {
+            const bool up = (g & m) != 0;
+#pragma unroll
+            for (int i = 0; i < m; ++i) {
+                const float send = up ? v[i] : v[i + m];
+                const float keep = up ? v[i + m] : v[i];
+                v[i] = keep + __shfl_xor_sync(kFull, send, m);
+            }
+        }
+        return v[0];
+    }
+}
+
+}  // namespace ssk

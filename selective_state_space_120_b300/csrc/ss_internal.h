@@ -1,0 +1,46 @@
+// Host-side interface between the C ABI layer (ss_api.cpp) and the kernel
+// translation unit (ss_kernels.cu).  Not part of the public API.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "ssscan.h"
+
+namespace ssi {
+
+// One call's arguments after validation.  Sequences are H x W maps; a plain
+// sequence is H = 1, W = L.  orders[k] is the traversal of direction k.
+struct ScanArgs {
+    int64_t batch = 0, dim = 0, L = 0, H = 1, W = 0;
+    int N = 0, G = 1, K = 1;
+    int io = SS_BF16;
+    const void *u = nullptr, *delta = nullptr, *B = nullptr, *C = nullptr, *z = nullptr;
+    const float *A = nullptr, *D = nullptr, *bias = nullptr;
+    int softplus = 1;
+    void *out = nullptr;
+    float *last_state = nullptr;
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    int orders[4] = {0, 1, 2, 3};
+    int chunks = 0;  // single direction: 0 automatic, 1 direct, >= 2 chunked with that many L-chunks
+    ss_stream_t stream = nullptr;
+};
+
+// Direction traversal codes used by the kernels (match SS_DIR_*).
+enum { ORD_ROW = 0, ORD_COL = 1, ORD_ROW_REV = 2, ORD_COL_REV = 3 };
+
+// Sets the thread-local error message and returns `st`.
+ss_status fail(ss_status st, const char *fmt, ...);
+
+// True when the single-direction call runs the TMA path (16-byte aligned rows).
+bool scan1d_uses_tma(const ScanArgs &a);
+// Workspace the single-direction path needs for this call (0 when it runs direct).
+size_t scan1d_workspace_bytes(const ScanArgs &a);
+
+ss_status launch_scan1d(const ScanArgs &a);
+ss_status launch_multidir(const ScanArgs &a);
+ss_status read_device_status(ss_stream_t stream);
+ss_status set_wait_budget(unsigned long long ns);
+
+}  // namespace ssi

@@ -1,0 +1,342 @@
+// Kernel instantiations and launchers of the selective-scan library (sm_103a).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "ss_device.cuh"
+#include "ss_internal.h"
+#include "ss_multidir.cuh"
+#include "ss_scan1d.cuh"
+
+namespace ssi {
+
+namespace {
+
+// ---------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D map over a [rows, cols] row-major tensor; boxes of [box_rows, box_cols]
+// with 64-byte rows and the 64-byte swizzle.  Out-of-range boxes read zeros.
+ss_status make_map(CUtensorMap *m, const void *base, int io, uint64_t cols, uint64_t rows,
+                   uint32_t box_cols, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(SS_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const uint64_t es = (io == SS_BF16) ? 2 : 4;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * es};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, io == SS_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(SS_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return SS_OK;
+}
+
+ss_status check_launch(const char *what) {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SS_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
+    return SS_OK;
+}
+
+int num_sms() {
+    int dev = 0, n = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 148;
+    } else {
+        cudaGetLastError();  // no device on this host: size for a B300 (148 SMs)
+    }
+    return n;
+}
+
+// ---------------------------------------------------------------- single direction
+template <class C>
+struct Scan1d {
+    static ss_status run(const ScanArgs &a, int J) {
+        using namespace ssk;
+        const int io = a.io;
+        const int64_t rows = a.batch * a.dim;
+        CUtensorMap mu, md, mz, mb, mc;
+        ss_status st;
+        if ((st = make_map(&mu, a.u, io, a.L, rows, C::T, C::CB))) return st;
+        if ((st = make_map(&md, a.delta, io, a.L, rows, C::T, C::CB))) return st;
+        if ((st = make_map(&mz, a.z ? a.z : a.u, io, a.L, rows, C::T, C::CB))) return st;
+        if ((st = make_map(&mb, a.B, io, a.L, (uint64_t)a.batch * a.G * C::N, C::T, C::N))) return st;
+        if ((st = make_map(&mc, a.C, io, a.L, (uint64_t)a.batch * a.G * C::N, C::T, C::N))) return st;
+
+        auto kern = k_scan1d<C>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
+
+        Scan1dParams p{};
+        p.dim = a.dim;
+        p.L = a.L;
+        p.G = a.G;
+        p.dpg = (int)(a.dim / a.G);
+        p.A = a.A;
+        p.D = a.D;
+        p.bias = a.bias;
+        p.softplus = a.softplus;
+        p.has_z = a.z != nullptr;
+        p.out = a.out;
+        p.last_state = a.last_state;
+        const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);
+        const unsigned bgs = (unsigned)(a.batch * a.G);
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(a.stream);
+        const int64_t Lc = chunk_len(a.L, J);
+        J = (int)((a.L + Lc - 1) / Lc);
+        if (J <= 1) {
+            p.Lc = a.L;
+            p.J = 1;
+            p.jbase = 0;
+            p.pass = 0;
+            kern<<<dim3(cblocks, bgs, 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
+            return check_launch("scan");
+        }
+        // chunked path: L-chunks of Lc steps (a multiple of T)
+        float *ws = reinterpret_cast<float *>(a.ws);
+        p.Lc = Lc;
+        p.J = J;
+        p.hend = ws;
+        p.carry = ws + rows * J * C::N;
+        p.sdt = ws + 2 * rows * J * C::N;
+        p.pass = 1;
+        p.jbase = 0;
+        kern<<<dim3(cblocks, bgs, J - 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
+        if ((st = check_launch("scan chunk-local pass"))) return st;
+        const int64_t nthr = rows * C::N;
+        k_carry<<<(unsigned)((nthr + 255) / 256), 256, 0, s>>>(rows, a.dim, J, C::N, a.A, p.hend,
+                                                            p.sdt, const_cast<float *>(p.carry));
+        if ((st = check_launch("carry"))) return st;
+        p.pass = 2;
+        p.jbase = 1;
+        kern<<<dim3(cblocks, bgs, J - 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
+        return check_launch("scan fix-up pass");
+    }
+    // Steps per L-chunk for a requested chunk count: a multiple of the T-tile.
+    static int64_t chunk_len(int64_t L, int J) {
+        if (J <= 1) return L;
+        return ((L + J - 1) / J + C::T - 1) / C::T * C::T;
+    }
+};
+
+// Configuration per (I/O type, N): NPT states per lane; W warps per CTA;
+// 3-stage TMA ring.
+template <typename IO, int N>
+struct Pick1d;
+template <typename IO> struct Pick1d<IO, 1> { using C = ssk::Cfg1<IO, 1, 1, 4, 3>; };
+template <typename IO> struct Pick1d<IO, 2> { using C = ssk::Cfg1<IO, 2, 2, 4, 3>; };
+template <typename IO> struct Pick1d<IO, 4> { using C = ssk::Cfg1<IO, 4, 4, 4, 3>; };
+template <typename IO> struct Pick1d<IO, 8> { using C = ssk::Cfg1<IO, 8, 4, 4, 3>; };
+template <typename IO> struct Pick1d<IO, 16> { using C = ssk::Cfg1<IO, 16, 4, 4, 3>; };
+template <typename IO> struct Pick1d<IO, 32> { using C = ssk::Cfg1<IO, 32, 4, 4, 3>; };
+template <typename IO> struct Pick1d<IO, 64> { using C = ssk::Cfg1<IO, 64, 8, 4, 3>; };
+
+// L-chunks to use: 1 (direct) when the direct path fills the GPU.
+template <class C>
+int choose_chunks(const ScanArgs &a) {
+    const int64_t rows = a.batch * a.dim;
+    const int64_t threads = rows * C::R;
+    const int64_t want = (int64_t)num_sms() * 16 * 32;  // about 16 warps per SM
+    if (threads * 2 >= want) return 1;
+    int64_t J = (want + threads - 1) / threads + 1;
+    const int64_t maxJ = a.L / (4 * C::T);  // keep L-chunks at least 4 T-chunks long
+    if (J > maxJ) J = maxJ;
+    return J < 2 ? 1 : (int)J;
+}
+
+template <typename IO, int N>
+int chunks_for(const ScanArgs &a) {
+    using C = typename Pick1d<IO, N>::C;
+    const int J = a.chunks > 0 ? a.chunks : choose_chunks<C>(a);
+    const int64_t Lc = Scan1d<C>::chunk_len(a.L, J);
+    return (int)((a.L + Lc - 1) / Lc);
+}
+
+template <typename IO, int N>
+ss_status dispatch1d(const ScanArgs &a) {
+    using C = typename Pick1d<IO, N>::C;
+    return Scan1d<C>::run(a, chunks_for<IO, N>(a));
+}
+
+template <typename IO, int N>
+size_t ws1d(const ScanArgs &a) {
+    const int J = chunks_for<IO, N>(a);
+    if (J <= 1) return 0;
+    const int64_t rows = a.batch * a.dim;
+    return (size_t)rows * J * (2 * N + 1) * sizeof(float);
+}
+
+// ---------------------------------------------------------------- multi direction
+template <class C>
+ss_status run_multi(const ScanArgs &a) {
+    using namespace ssk;
+    const int64_t smem = C::smem_bytes(a.L);
+    int dev = 0, maxsm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (smem > maxsm)
+        return fail(SS_ERR_UNSUPPORTED,
+                    "sequence of %lld positions needs %lld bytes of shared memory (limit %d)",
+                    (long long)a.L, (long long)smem, maxsm);
+    auto kern = k_multidir<C>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return fail(SS_ERR_CUDA, "cannot reserve %lld bytes of shared memory", (long long)smem);
+    MultiParams p{};
+    p.dim = a.dim;
+    p.L = a.L;
+    p.H = (int)a.H;
+    p.W = (int)a.W;
+    p.G = a.G;
+    p.dpg = (int)(a.dim / a.G);
+    for (int k = 0; k < 4; ++k) p.orders[k] = a.orders[k];
+    p.divH = FastDiv((uint32_t)a.H);
+    p.u = a.u;
+    p.delta = a.delta;
+    p.B = a.B;
+    p.C = a.C;
+    p.z = a.z;
+    p.A = a.A;
+    p.D = a.D;
+    p.bias = a.bias;
+    p.softplus = a.softplus;
+    p.out = a.out;
+    p.last_state = a.last_state;
+    const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(a.stream);
+    kern<<<dim3(cblocks, (unsigned)(a.batch * a.G), 1), C::THREADS, (size_t)smem, s>>>(p);
+    return check_launch("multi-direction scan");
+}
+
+// NPT states per lane (at most 8 lanes per channel); WPD warps per direction.
+template <typename IO, int N, int K>
+struct PickM;
+template <typename IO, int K> struct PickM<IO, 1, K> { using C = ssk::CfgM<IO, 1, 1, K, 1>; };
+template <typename IO, int K> struct PickM<IO, 2, K> { using C = ssk::CfgM<IO, 2, 1, K, (K == 4 ? 1 : 4)>; };
+template <typename IO, int K> struct PickM<IO, 4, K> { using C = ssk::CfgM<IO, 4, 2, K, (K == 4 ? 1 : 4)>; };
+template <typename IO, int K> struct PickM<IO, 8, K> { using C = ssk::CfgM<IO, 8, 2, K, (K == 4 ? 1 : 2)>; };
+template <typename IO, int K> struct PickM<IO, 16, K> { using C = ssk::CfgM<IO, 16, 2, K, (K == 4 ? 1 : 4)>; };
+template <typename IO, int K> struct PickM<IO, 32, K> { using C = ssk::CfgM<IO, 32, 4, K, (K == 4 ? 1 : 2)>; };
+template <typename IO, int K> struct PickM<IO, 64, K> { using C = ssk::CfgM<IO, 64, 8, K, (K == 4 ? 1 : 2)>; };
+
+template <typename IO, int K>
+ss_status dispatch_multi_n(const ScanArgs &a) {
+    switch (a.N) {
+    case 1: return run_multi<typename PickM<IO, 1, K>::C>(a);
+    case 2: return run_multi<typename PickM<IO, 2, K>::C>(a);
+    case 4: return run_multi<typename PickM<IO, 4, K>::C>(a);
+    case 8: return run_multi<typename PickM<IO, 8, K>::C>(a);
+    case 16: return run_multi<typename PickM<IO, 16, K>::C>(a);
+    case 32: return run_multi<typename PickM<IO, 32, K>::C>(a);
+    case 64: return run_multi<typename PickM<IO, 64, K>::C>(a);
+    default: return fail(SS_ERR_UNSUPPORTED, "dstate %d is not supported on this path", a.N);
+    }
+}
+
+template <typename IO>
+ss_status dispatch_multi(const ScanArgs &a) {
+    switch (a.K) {
+    case 1: return dispatch_multi_n<IO, 1>(a);
+    case 2: return dispatch_multi_n<IO, 2>(a);
+    case 4: return dispatch_multi_n<IO, 4>(a);
+    default: return fail(SS_ERR_INVALID_ARG, "directions must be 1, 2 or 4");
+    }
+}
+
+template <typename IO>
+ss_status dispatch1d_n(const ScanArgs &a) {
+    switch (a.N) {
+    case 1: return dispatch1d<IO, 1>(a);
+    case 2: return dispatch1d<IO, 2>(a);
+    case 4: return dispatch1d<IO, 4>(a);
+    case 8: return dispatch1d<IO, 8>(a);
+    case 16: return dispatch1d<IO, 16>(a);
+    case 32: return dispatch1d<IO, 32>(a);
+    case 64: return dispatch1d<IO, 64>(a);
+    default: return fail(SS_ERR_UNSUPPORTED, "dstate %d is not one of 1,2,4,8,16,32,64", a.N);
+    }
+}
+
+template <typename IO>
+size_t ws1d_n(const ScanArgs &a) {
+    switch (a.N) {
+    case 1: return ws1d<IO, 1>(a);
+    case 2: return ws1d<IO, 2>(a);
+    case 4: return ws1d<IO, 4>(a);
+    case 8: return ws1d<IO, 8>(a);
+    case 16: return ws1d<IO, 16>(a);
+    case 32: return ws1d<IO, 32>(a);
+    case 64: return ws1d<IO, 64>(a);
+    default: return 0;
+    }
+}
+
+}  // namespace
+
+// The TMA path needs 16-byte aligned rows: seqlen * element size % 16 == 0.
+bool scan1d_uses_tma(const ScanArgs &a) {
+    const int64_t es = (a.io == SS_BF16) ? 2 : 4;
+    return (a.L * es) % 16 == 0 && a.batch * a.dim < (1ll << 31) &&
+           a.batch * a.G * a.N < (1ll << 31) && a.L < (1ll << 31);
+}
+
+size_t scan1d_workspace_bytes(const ScanArgs &a) {
+    if (!scan1d_uses_tma(a)) return 0;
+    return a.io == SS_BF16 ? ws1d_n<__nv_bfloat16>(a) : ws1d_n<float>(a);
+}
+
+ss_status launch_scan1d(const ScanArgs &a) {
+    if (!scan1d_uses_tma(a)) {
+        ScanArgs m = a;
+        m.K = 1;
+        m.H = 1;
+        m.W = a.L;
+        m.orders[0] = ORD_ROW;
+        return a.io == SS_BF16 ? dispatch_multi<__nv_bfloat16>(m) : dispatch_multi<float>(m);
+    }
+    return a.io == SS_BF16 ? dispatch1d_n<__nv_bfloat16>(a) : dispatch1d_n<float>(a);
+}
+
+ss_status launch_multidir(const ScanArgs &a) {
+    return a.io == SS_BF16 ? dispatch_multi<__nv_bfloat16>(a) : dispatch_multi<float>(a);
+}
+
+ss_status read_device_status(ss_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, ssk::g_status, sizeof(v));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(ssk::g_status, &zero, sizeof(zero));
+    if (e != cudaSuccess) return fail(SS_ERR_CUDA, "device status read failed: %s", cudaGetErrorString(e));
+    if (v & 1u) return fail(SS_ERR_TIMEOUT, "a kernel abandoned a bounded wait (timeout)");
+    return SS_OK;
+}
+
+ss_status set_wait_budget(unsigned long long ns) {
+    const cudaError_t e = cudaMemcpyToSymbol(ssk::g_wait_budget_ns, &ns, sizeof(ns));
+    if (e != cudaSuccess) return fail(SS_ERR_CUDA, "cannot set the wait budget: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+
+}  // namespace ssi

@@ -1,0 +1,164 @@
+"""Host-side checks of the C ABI (no kernel is launched).
+
+The library loads and exports every function include/ssscan.h declares; bad
+arguments are rejected with the documented status before anything is
+enqueued; workspace sizing is a host computation.  The calls with fake
+addresses all fail validation; they run only where no GPU is present, so that
+a validation bug could never hand a fake address to a kernel.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_120_b300 import _binding as b
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssscan.h")
+
+
+def _gpu_present():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:  # noqa: BLE001
+        return False
+
+
+fake_ptrs = pytest.mark.skipif(_gpu_present(), reason="fake-address checks run on CPU hosts only")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from selective_state_space_120_b300 import build
+    build.build()
+    return b.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:ss_status|size_t|const char \*)\s*(ss_\w+)\s*\(", text,
+                                 re.M)))
+
+
+def test_header_declarations_match_binding():
+    assert _declared() == sorted(b.EXPORTS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert b.version().startswith("ssscan")
+
+
+A16 = 0x10000  # a 16-byte aligned fake address
+
+
+def _scan(lib, batch=1, dim=8, L=32, N=16, G=1, io=b.SS_BF16, u=A16, delta=A16 + 0x100000,
+          A=A16 + 0x200000, B=A16 + 0x300000, C=A16 + 0x400000, D=None, z=None, bias=None,
+          out=A16 + 0x500000, last=None, ws=None, wsb=0):
+    return lib.ss_selective_scan_fwd(batch, dim, L, N, G, io, u, delta, A, B, C, D, z, bias, 1,
+                                     out, last, ws, wsb, None)
+
+
+@fake_ptrs
+def test_rejects_null_required_pointers(lib):
+    assert _scan(lib, u=None) == b.SS_ERR_INVALID_ARG
+    assert _scan(lib, B=None) == b.SS_ERR_INVALID_ARG
+    assert _scan(lib, out=None) == b.SS_ERR_INVALID_ARG
+    assert "required" in b.last_error()
+
+
+@fake_ptrs
+def test_rejects_bad_sizes(lib):
+    assert _scan(lib, batch=-1, out=None) == b.SS_ERR_INVALID_ARG
+    assert _scan(lib, dim=6, G=4, out=None) == b.SS_ERR_INVALID_ARG      # 6 % 4 != 0
+    assert _scan(lib, G=0, out=None) == b.SS_ERR_INVALID_ARG
+
+
+@fake_ptrs
+@pytest.mark.parametrize("N", [0, 3, 5, 12, 128])
+def test_rejects_unsupported_dstate(lib, N):
+    assert _scan(lib, N=N, out=None) == b.SS_ERR_UNSUPPORTED
+
+
+@fake_ptrs
+def test_rejects_unknown_dtype(lib):
+    assert _scan(lib, io=7, out=None) == b.SS_ERR_UNSUPPORTED
+
+
+@fake_ptrs
+def test_rejects_misaligned_pointers(lib):
+    assert _scan(lib, u=A16 + 2) == b.SS_ERR_ALIGNMENT
+    assert _scan(lib, z=A16 + 0x600008) == b.SS_ERR_ALIGNMENT
+    assert _scan(lib, out=A16 + 0x500004) == b.SS_ERR_ALIGNMENT
+
+
+@fake_ptrs
+def test_rejects_out_aliasing_inputs(lib):
+    assert _scan(lib, out=A16) == b.SS_ERR_INVALID_ARG                  # out == u
+    assert _scan(lib, out=A16 + 0x100000 + 64) == b.SS_ERR_INVALID_ARG  # inside delta
+    assert "overlap" in b.last_error()
+
+
+@fake_ptrs
+def test_rejects_missing_workspace_on_chunked_path(lib):
+    opts = b.options(chunks=4)
+    need = b.workspace_bytes(b.SS_KIND_SCAN, 1, 8, 4096, 16, chunks=4)
+    assert need > 0
+    args = (1, 8, 4096, 16, 1, b.SS_BF16, A16, A16 + 0x100000, A16 + 0x200000, A16 + 0x300000,
+            A16 + 0x400000, None, None, None, 1, A16 + 0x500000, None)
+    st = lib.ss_selective_scan_fwd_opts(*args, None, 0, ctypes.byref(opts), None)
+    assert st == b.SS_ERR_WORKSPACE
+    st = lib.ss_selective_scan_fwd_opts(*args, A16 + 0x700000, need - 1, ctypes.byref(opts), None)
+    assert st == b.SS_ERR_WORKSPACE
+    st = lib.ss_selective_scan_fwd_opts(*args, A16 + 0x700008, need, ctypes.byref(opts), None)
+    assert st == b.SS_ERR_ALIGNMENT
+
+
+@fake_ptrs
+def test_rejects_nonzero_reserved_options(lib):
+    opts = b.options()
+    opts.reserved[3] = 1
+    st = lib.ss_selective_scan_fwd_opts(1, 8, 32, 16, 1, b.SS_BF16, A16, A16 + 0x100000,
+                                        A16 + 0x200000, A16 + 0x300000, A16 + 0x400000, None, None,
+                                        None, 1, A16 + 0x500000, None, None, 0, ctypes.byref(opts),
+                                        None)
+    assert st == b.SS_ERR_INVALID_ARG
+
+
+@fake_ptrs
+def test_empty_inputs_return_ok_without_pointers(lib):
+    assert _scan(lib, batch=0, u=None, delta=None, A=None, B=None, C=None, out=None) == b.SS_OK
+    assert _scan(lib, L=0, u=None, delta=None, A=None, B=None, C=None, out=None) == b.SS_OK
+    st = lib.ss_cross_scan2d_fwd(2, 4, 0, 5, 16, 1, b.SS_BF16, None, None, None, None, None, None,
+                                 None, 1, None, None, None, None, 0, None)
+    assert st == b.SS_OK
+
+
+@fake_ptrs
+def test_bidir_and_cross2d_validate(lib):
+    st = lib.ss_bidir_scan_fwd(1, 8, 32, 16, 1, b.SS_BF16, A16, None, A16, A16, A16, None, None,
+                               None, 1, A16 + 0x500000, None, None, 0, None)
+    assert st == b.SS_ERR_INVALID_ARG
+    st = lib.ss_cross_scan2d_fwd(1, 8, -3, 4, 16, 1, b.SS_BF16, A16, A16, A16, A16, A16, None,
+                                 None, 1, None, A16 + 0x500000, None, None, 0, None)
+    assert st == b.SS_ERR_INVALID_ARG
+    st = lib.ss_cross_scan2d_fwd(1, 8, 3, 4, 12, 1, b.SS_BF16, A16, A16, A16, A16, A16, None,
+                                 None, 1, None, A16 + 0x500000, None, None, 0, None)
+    assert st == b.SS_ERR_UNSUPPORTED
+
+
+def test_workspace_sizing_is_host_only(lib):
+    # the multi-direction calls merge on chip: no workspace
+    assert b.workspace_bytes(b.SS_KIND_BIDIR, 128, 768, 197, 16) == 0
+    assert b.workspace_bytes(b.SS_KIND_CROSS2D, 32, 192, 3136, 16) == 0
+    # plenty of batch*dim parallelism: single pass, no workspace
+    assert b.workspace_bytes(b.SS_KIND_SCAN, 8, 1536, 2048, 16) == 0
+    # forced chunks: hend + carry (N floats each) + one float per row and chunk
+    need = b.workspace_bytes(b.SS_KIND_SCAN, 2, 8, 4096, 16, chunks=4)
+    assert need == 2 * 8 * 4 * (2 * 16 + 1) * 4
+    assert b.workspace_bytes(b.SS_KIND_SCAN, 0, 8, 4096, 16) == 0
+    # long sequence with few rows: the automatic choice splits it
+    assert b.workspace_bytes(b.SS_KIND_SCAN, 1, 5120, 131072, 16) > 0

@@ -1,0 +1,197 @@
+"""GPU parity: the CUDA library against the float64 oracle, element by element,
+on the same seeded inputs (B300 only).
+
+Small cases span several channel blocks and time tiles and end on ragged
+tails; full-size workloads are checked on sampled channels, which the oracle
+computes independently (each channel's scan depends only on its own row).
+"""
+import numpy as np
+import pytest
+
+from selective_state_space_120_b300 import workloads as wk
+from tests import scan_cases as sc
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import selective_state_space_120_b300 as ss
+    ss.load_library()
+
+
+def _check(oracle, wl, chunks=0):
+    inp = wk.make_inputs(wl, seed=0)
+    out, last = sc.gpu_run(inp, chunks=chunks)
+    ref, ref_last = sc.oracle_run(oracle, inp)
+    e = sc.assert_close(sc.from_torch(out), ref, wl.io)
+    got_last = last.cpu().numpy().astype(np.float64)
+    if wl.K == 1:
+        ref_last = ref_last[:, 0]
+    sc.assert_close(got_last, ref_last, wl.io, "last_state")
+    return e
+
+
+# ---------------------------------------------------------------- single direction
+def test_tiny_f32_config(oracle):
+    """1 x 16 x 64, N = 16, float32 I/O (the tiny S6 workload), whole output."""
+    _check(oracle, wk.TINY_F32)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16, 32, 64])
+def test_scan_all_dstates(oracle, io, N):
+    _check(oracle, sc.workload(f"n{N}", 2, 40, 208, N=N, io=io))
+
+
+@pytest.mark.parametrize("L", [8, 16, 200, 264, 1000])
+def test_scan_ragged_lengths_tma_path(oracle, L):
+    _check(oracle, sc.workload(f"l{L}", 2, 36, L, G=2))
+
+
+@pytest.mark.parametrize("L", [1, 7, 31, 33, 197, 257])
+def test_scan_unaligned_lengths(oracle, L):
+    """Rows that are not 16-byte multiples take the gather path."""
+    _check(oracle, sc.workload(f"u{L}", 2, 20, L))
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_scan_without_gate_or_skip(oracle, io):
+    _check(oracle, sc.workload("nozd", 1, 33, 96, io=io, with_z=False, with_D=False))
+
+
+@pytest.mark.parametrize("chunks", [2, 3, 5])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_chunked_long_sequence_path(oracle, chunks, io):
+    """The chunk-local pass, carry and fix-up reproduce the sequential scan."""
+    _check(oracle, sc.workload("chunked", 1, 24, 1200, io=io), chunks=chunks)
+
+
+def test_chunked_equals_direct_to_fp32_rounding():
+    wl = sc.workload("cmp", 2, 64, 2048, io="f32")
+    inp = wk.make_inputs(wl)
+    o1, l1 = sc.gpu_run(inp, chunks=1)
+    o4, l4 = sc.gpu_run(inp, chunks=4)
+    assert sc.rel_err(sc.from_torch(o4), sc.from_torch(o1)) < 2e-5
+    assert sc.rel_err(l4.cpu().numpy(), l1.cpu().numpy()) < 2e-5
+
+
+def test_deterministic_and_guarded():
+    """Two runs give identical bits; nothing is written outside `out`."""
+    import torch
+    import selective_state_space_120_b300 as ss
+    wl = sc.workload("det", 2, 40, 136)
+    inp = wk.make_inputs(wl)
+    t = sc.device_inputs(inp)
+    n = t["u"].numel()
+    pad = 4096
+    guard = torch.full((n + 2 * pad,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = guard[pad:pad + n].view_as(t["u"])
+    outs = []
+    for _ in range(2):
+        ss.selective_scan_fwd(t["u"], t["delta"][:, 0], t["A"], t["B"][:, 0], t["C"][:, 0], t["D"],
+                              t["z"], t["delta_bias"], True, out=out)
+        outs.append(out.clone())
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.isnan(guard[:pad]).all() and torch.isnan(guard[pad + n:]).all()
+
+
+def test_multidir_deterministic():
+    import torch
+    for wl in (sc.workload("bi_det", 2, 24, 197, K=2),
+               sc.workload("ss_det", 2, 12, 64, K=4, with_z=False, H=8, W=8)):
+        inp = wk.make_inputs(wl)
+        t = sc.device_inputs(inp)
+        a, _ = sc.gpu_run(inp, t=t)
+        b, _ = sc.gpu_run(inp, t=t)
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), wl.name
+
+
+def test_empty_inputs_are_noops():
+    import torch
+    import selective_state_space_120_b300 as ss
+    u = torch.empty(0, 8, 32, dtype=torch.bfloat16, device="cuda")
+    B = torch.empty(0, 1, 16, 32, dtype=torch.bfloat16, device="cuda")
+    A = -torch.ones(8, 16, device="cuda")
+    out = ss.selective_scan_fwd(u, u, A, B, B)
+    assert out.shape == u.shape
+
+
+def test_timeout_path_reports_and_recovers(oracle):
+    """A 1 ns wait budget makes TMA waits give up: the call reports SS_ERR_TIMEOUT
+    through the device status, and the next call with the default budget is exact."""
+    import selective_state_space_120_b300 as ss
+    from selective_state_space_120_b300 import _binding as b
+    lib = b.load()
+    wl = sc.workload("to", 4, 256, 2048)
+    inp = wk.make_inputs(wl)
+    ss.device_status()
+    b.check(lib.ss_debug_set_wait_budget_ns(1))
+    try:
+        sc.gpu_run(inp)
+        with pytest.raises(ss.SSError) as ei:
+            ss.device_status()
+        assert ei.value.status == b.SS_ERR_TIMEOUT
+    finally:
+        b.check(lib.ss_debug_set_wait_budget_ns(0))
+    ss.device_status()  # cleared
+    inp2 = wk.make_inputs(sc.workload("after", 1, 40, 96))
+    out, _ = sc.gpu_run(inp2)
+    ref, _ = sc.oracle_run(oracle, inp2)
+    sc.assert_close(sc.from_torch(out), ref, "bf16")
+    ss.device_status()
+
+
+# ---------------------------------------------------------------- bidirectional
+@pytest.mark.parametrize("L", [1, 7, 33, 197, 256])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bidirectional(oracle, L, io):
+    _check(oracle, sc.workload(f"bi{L}", 2, 24, L, K=2, io=io))
+
+
+def test_bidirectional_groups_dstate(oracle):
+    _check(oracle, sc.workload("bi_g", 2, 32, 50, N=8, G=2, K=2))
+
+
+# ---------------------------------------------------------------- SS2D
+@pytest.mark.parametrize("H,W", [(1, 1), (3, 5), (5, 3), (8, 8), (7, 16), (56, 56)])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_cross_scan2d(oracle, H, W, io):
+    _check(oracle, sc.workload(f"ss2d{H}x{W}", 2, 12, H * W, K=4, io=io, with_z=False, H=H, W=W))
+
+
+def test_cross_scan2d_gated_groups(oracle):
+    _check(oracle, sc.workload("ss2d_gz", 1, 16, 6 * 10, N=4, G=2, K=4, H=6, W=10))
+
+
+# ---------------------------------------------------------------- full-size workloads
+def _sampled(oracle, wl, nrows=12, seed=1):
+    import torch
+    inp = wk.make_inputs(wl, seed=0)
+    out, last = sc.gpu_run(inp)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(seed)
+    rows = [(int(rng.integers(wl.batch)), int(rng.integers(wl.dim))) for _ in range(nrows)]
+    rows += [(0, 0), (wl.batch - 1, wl.dim - 1)]
+    ref, ref_last = sc.oracle_run(oracle, inp, rows)
+    got = np.stack([sc.from_torch(out[b, d]) for b, d in rows])
+    sc.assert_close(got, ref, wl.io)
+    if wl.K == 1:
+        got_l = np.stack([last[b, d].cpu().numpy() for b, d in rows])
+        sc.assert_close(got_l, ref_last[:, 0], wl.io, "last_state")
+    else:
+        got_l = np.stack([last[b, :, d].cpu().numpy() for b, d in rows])
+        sc.assert_close(got_l, ref_last, wl.io, "last_state")
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("wl", [wk.MAMBA_LAYER, wk.LONG_SEQ, wk.VIM_BIDIR, wk.VMAMBA_SS2D],
+                         ids=lambda w: w.name)
+def test_full_size_sampled(oracle, wl):
+    _sampled(oracle, wl)
