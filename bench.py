@@ -1,0 +1,525 @@
+"""Benchmark of the B300 selective-scan library.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-others] [--no-cpu]
+
+Prints ONE JSON line.  A step is one call of the library over one batch of the
+workload (inputs resident in HBM).  The headline workload is the Mamba-130M
+layer-shaped scan (batch 8, 1536 channels, L = 2048, N = 16, bf16 I/O, fp32
+state, z gate and D skip); the long-sequence, bidirectional and SS2D workloads
+are measured the same way and reported under "workloads".
+
+Timing: W untimed warm-up steps, then K steps between a barrier and a device
+synchronisation on each side, timed with CUDA events on the launching stream;
+each launch is also bracketed by its own events to give the kernel's average
+duration for the roofline.  Inputs rotate over several copies whose total size
+exceeds the 126 MB L2, so every step reads cold data.  SM clocks and throttle
+reasons are sampled through NVML during the timed region.
+
+Multi-GPU: the scan shards over batch and channels with no exchange, so each
+rank runs an independent replica (weak scaling); value = all ranks' elements /
+the slowest rank's time.
+
+--impl reference times the float64 CPU oracle (the only other arm: the pages
+ship no code) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from selective_state_space_120_b300 import workloads as wk  # noqa: E402
+
+METRIC = "selective-scan Gelem/s (B·D·L) and achieved HBM GB/s vs ~8 TB/s peak"
+UNIT = "Gelem/s"
+L2_BYTES = 126 * 2 ** 20
+FALLBACK_HBM_GBS = 6400.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+CSRC = os.path.join(ROOT, "selective_state_space_120_b300", "csrc")
+
+WORKLOADS = {w.name: w for w in wk.ALL}
+HEADLINE = wk.MAMBA_LAYER
+OTHERS = (wk.LONG_SEQ, wk.VIM_BIDIR, wk.VMAMBA_SS2D)
+
+
+# ------------------------------------------------------------------ accounting
+def algorithmic_bytes(wl: wk.Workload) -> int:
+    """Bytes a step must move at least: every input element read once, the
+    output written once (and last_state if returned).  B/C are shared by the
+    channels of a group, so they count once per (batch, direction, group)."""
+    es = 2 if wl.io == "bf16" else 4
+    per_chan = wl.batch * wl.dim * wl.L * es
+    n = per_chan * (1 + wl.K)                     # u, Delta per direction
+    if wl.with_z:
+        n += per_chan                             # z
+    n += per_chan                                 # out
+    n += 2 * wl.batch * wl.K * wl.G * wl.N * wl.L * es   # B, C
+    n += wl.K * wl.dim * (wl.N + 2) * 4           # A, D, delta_bias
+    if wl.last_state:
+        n += wl.batch * wl.K * wl.dim * wl.N * 4
+    return n
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(wl: wk.Workload):
+    """DRAM bytes per launch of the workload's dominant kernel from the committed
+    ncu summary, or None if absent or taken on different kernel sources."""
+    try:
+        with open(PROFILE_TRAFFIC) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    ent = rec.get("workloads", {}).get(wl.name)
+    return None if ent is None else ent.get("dram_bytes_per_launch")
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+            0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+            0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """Samples the SM clock and the clock-event reasons through NVML in a thread."""
+
+    def __init__(self, index: int, period_s: float = 0.002):
+        self.period = period_s
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thr = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+        except Exception:  # noqa: BLE001 -- clocks are reported as unavailable
+            self._nv = None
+
+    def _reasons(self):
+        nv = self._nv
+        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return fn(self._h)
+
+    def _sample(self):
+        self.samples.append(self._nv.nvmlDeviceGetClockInfo(self._h, self._nv.NVML_CLOCK_SM))
+        self.reasons |= int(self._reasons())
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self._sample()
+            except Exception:  # noqa: BLE001
+                pass
+            self._stop.wait(self.period)
+
+    def __enter__(self):
+        if self._nv is not None:
+            self._thr = threading.Thread(target=self._run, daemon=True)
+            self._thr.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._thr is not None:
+            self._stop.set()
+            self._thr.join()
+
+    def summary(self):
+        if self._nv is None or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"],
+                    "samples": 0}
+        names = [n for bit, n in _REASONS.items() if self.reasons & bit]
+        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ GPU arm
+class Runner:
+    """Holds device inputs of one workload (several rotating copies) and issues
+    one library call per step through the C ABI with prebuilt arguments."""
+
+    def __init__(self, wl: wk.Workload, device, seed: int = 0):
+        import torch
+        import selective_state_space_120_b300 as ss
+        from selective_state_space_120_b300 import _binding as b
+        self.wl, self.dev = wl, device
+        self.lib = b.load()
+        inp = wk.make_inputs(wl, seed=seed)
+        self.host = inp
+        t = {n: self._to_dev(getattr(inp, n)) for n in
+             ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")}
+        set_bytes = algorithmic_bytes(wl)
+        self.copies = max(2, int(np.ceil(3 * L2_BYTES / set_bytes)) + 1)
+        self.copies = min(self.copies, 8)
+        self.sets = []
+        for i in range(self.copies):
+            s = {k: (None if v is None else (v if i == 0 else v.clone())) for k, v in t.items()}
+            s["out"] = torch.empty_like(s["u"])
+            s["last"] = (torch.empty(wl.batch, wl.K, wl.dim, wl.N, dtype=torch.float32,
+                                     device=device) if wl.last_state else None)
+            self.sets.append(s)
+        self.stream = torch.cuda.current_stream(device)
+        self.ws = None
+        self.opts = b.options(0)
+        if wl.K == 1:
+            wsb = int(self.lib.ss_workspace_bytes_opts(b.SS_KIND_SCAN, wl.batch, wl.dim, wl.L,
+                                                       wl.N, ctypes.byref(self.opts)))
+            if wsb:
+                self.ws = torch.empty(wsb, dtype=torch.uint8, device=device)
+        self.args = [self._args(s) for s in self.sets]
+        self.launches_per_step = self._launches()
+        self._ss = ss
+
+    @staticmethod
+    def _to_dev(a):
+        import torch
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    def _args(self, s):
+        wl = self.wl
+        p = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        io = 1 if wl.io == "bf16" else 0
+        st = ctypes.c_void_p(self.stream.cuda_stream)
+        ws = p(self.ws)
+        wsb = 0 if self.ws is None else self.ws.numel()
+        if wl.K == 1:
+            return (self.lib.ss_selective_scan_fwd_opts,
+                    (wl.batch, wl.dim, wl.L, wl.N, wl.G, io, p(s["u"]), p(s["delta"]), p(s["A"]),
+                     p(s["B"]), p(s["C"]), p(s["D"]), p(s["z"]), p(s["delta_bias"]), 1,
+                     p(s["out"]), p(s["last"]), ws, wsb, ctypes.byref(self.opts), st))
+        if wl.K == 2:
+            return (self.lib.ss_bidir_scan_fwd,
+                    (wl.batch, wl.dim, wl.L, wl.N, wl.G, io, p(s["u"]), p(s["delta"]), p(s["A"]),
+                     p(s["B"]), p(s["C"]), p(s["D"]), p(s["z"]), p(s["delta_bias"]), 1,
+                     p(s["out"]), p(s["last"]), None, 0, st))
+        return (self.lib.ss_cross_scan2d_fwd,
+                (wl.batch, wl.dim, wl.H, wl.W, wl.N, wl.G, io, p(s["u"]), p(s["delta"]),
+                 p(s["A"]), p(s["B"]), p(s["C"]), p(s["D"]), p(s["delta_bias"]), 1, p(s["z"]),
+                 p(s["out"]), p(s["last"]), None, 0, st))
+
+    def _launches(self):
+        """Kernels one step launches: 1, or 3 on the chunked long-sequence path."""
+        return 3 if self.ws is not None else 1
+
+    def step(self, i: int):
+        fn, args = self.args[i % self.copies]
+        st = fn(*args)
+        if st != 0:
+            from selective_state_space_120_b300 import _binding as b
+            b.check(st)
+
+    def timed(self, steps: int, warmup: int, barrier=None):
+        import torch
+        for i in range(warmup):
+            self.step(i)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        if barrier:
+            barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            t0.record(self.stream)
+            for i in range(steps):
+                ev[i][0].record(self.stream)
+                self.step(warmup + i)
+                ev[i][1].record(self.stream)
+            t1.record(self.stream)
+            torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        self._ss.device_status()
+        total_ms = t0.elapsed_time(t1)
+        kern_ms = [a.elapsed_time(b) for a, b in ev]
+        return total_ms, float(np.mean(kern_ms)), clk.summary()
+
+    def e2e(self, steps: int, warmup: int):
+        """Same metric through the public call with the step's inputs copied from
+        pinned host memory and the output read back, every step."""
+        import torch
+        s = self.sets[0]
+        names = [n for n in ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")
+                 if s[n] is not None]
+        host = {n: s[n].cpu().pin_memory() for n in names}
+        out_h = torch.empty(s["out"].shape, dtype=s["out"].dtype).pin_memory()
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+        d2h = out_h.numel() * out_h.element_size()
+        if s["last"] is not None:
+            last_h = torch.empty(s["last"].shape, dtype=torch.float32).pin_memory()
+            d2h += last_h.numel() * 4
+        else:
+            last_h = None
+
+        def one():
+            for n in names:
+                s[n].copy_(host[n], non_blocking=True)
+            self.step(0)
+            out_h.copy_(s["out"], non_blocking=True)
+            if last_h is not None:
+                last_h.copy_(s["last"], non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(self.stream)
+        for _ in range(steps):
+            one()
+        t1.record(self.stream)
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / steps
+        return {"value": self.wl.elems / (ms * 1e-3) / 1e9, "unit": UNIT,
+                "ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------ CPU oracle arm
+def oracle_sample(wl: wk.Workload, budget_s: float = 12.0, threads: int | None = None):
+    """Times the float64 oracle on whole (batch, channel) rows of the workload
+    until about `budget_s` of wall time is spent, in parallel over rows (ctypes
+    releases the GIL).  Returns (Gelem/s, rows, threads, seconds)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    oracle.build()
+    threads = threads or os.cpu_count() or 1
+    # a reduced copy of the workload: one batch entry and as many channels as keep
+    # the host arrays near 4 M elements, with the same per-row shape and recipe
+    dim = min(wl.dim, max(wl.G, ((1 << 22) // wl.L) // wl.G * wl.G))
+    small = wk.scaled(wl, wl.name + "_oracle_sample", batch=1, dim=dim)
+    inp = wk.make_inputs(small, seed=0)
+    K = wl.K
+    orders = {1: (oracle.ORDER_FWD,), 2: (oracle.ORDER_FWD, oracle.ORDER_REV),
+              4: oracle.SS2D_ORDERS}[K]
+    H, W = (wl.H, wl.W) if K == 4 else (1, wl.L)
+    u, dl, A, B, C = (inp.as_f64(n) for n in ("u", "delta", "A", "B", "C"))
+    D, z, bias = inp.as_f64("D"), inp.as_f64("z"), inp.as_f64("delta_bias")
+    dpg = small.dim // wl.G
+    rows = [(0, d) for d in range(small.dim)]
+
+    def one(bd):
+        b, d = bd
+        g = d // dpg
+        sel = [k * small.dim + d for k in range(K)]
+        oracle.scan(u[b:b + 1, d:d + 1], dl[b:b + 1, :, d:d + 1], A[sel],
+                    B[b:b + 1, :, g:g + 1], C[b:b + 1, :, g:g + 1],
+                    None if D is None else D[sel], None if z is None else z[b:b + 1, d:d + 1],
+                    bias[sel], True, orders, H=H, W=W)
+
+    done = 0
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        while time.perf_counter() - t0 < budget_s:
+            batch = [rows[(done + i) % len(rows)] for i in range(threads * 4)]
+            list(ex.map(one, batch))
+            done += len(batch)
+    dt = time.perf_counter() - t0
+    return done * wl.L / dt / 1e9, done, threads, dt
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# ------------------------------------------------------------------ main
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def config_of(wl: wk.Workload, n_gpus: int, copies: int | None = None):
+    c = {"workload": wl.name, "batch": wl.batch, "dim": wl.dim, "seq_len": wl.L,
+         "d_state": wl.N, "groups": wl.G, "directions": wl.K, "io_dtype": wl.io,
+         "state_dtype": "f32", "z_gate": wl.with_z, "d_skip": wl.with_D,
+         "last_state": wl.last_state, "delta_softplus": True,
+         "parallelism": f"replicas{n_gpus}" if n_gpus > 1 else "single"}
+    if wl.K == 4:
+        c["H"], c["W"] = wl.H, wl.W
+    if copies:
+        c["l2"] = (f"inputs rotate over {copies} copies "
+                   f"({copies * algorithmic_bytes(wl) / 1e6:.0f} MB > 126 MB L2)")
+    return c
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    wl = WORKLOADS.get(args.workload, HEADLINE)
+    steps, warmup = args.steps, args.warmup
+    budget = max(1.0, min(20.0, 60.0 / max(1, steps + warmup)))
+    vals = []
+    info = None
+    for i in range(warmup + steps):
+        v, rows, thr, dt = oracle_sample(wl, budget_s=budget)
+        if i >= warmup:
+            vals.append(v)
+            info = (rows, thr, dt)
+    v = float(np.median(vals))
+    rows, thr, dt = info
+    sample = (f"whole (batch, channel) rows of the workload (L={wl.L}, N={wl.N}, K={wl.K}), "
+              f"{rows} rows in {dt:.1f} s per step, parallel over rows on {thr} threads; "
+              f"host CPU {cpu_model()}")
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": steps,
+            "warmup": warmup, "ms_per_step": wl.elems / (v * 1e9) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded NumPy PCG64; recipe of the workload)",
+            "config": config_of(wl, 1), "impl": "reference",
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def measure_gpu(wl, steps, warmup, barrier=None):
+    r = Runner(wl, "cuda")
+    total_ms, kern_ms, clocks = r.timed(steps, warmup, barrier)
+    return r, total_ms / steps, kern_ms, clocks
+
+
+def roofline(wl, kern_ms, peak, peak_kind):
+    alg = algorithmic_bytes(wl)
+    ach = alg / (kern_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+            "peak_source": f"{peak_kind} (copy bandwidth)",
+            "algorithmic_bytes_per_launch": alg, "traffic": ncu_traffic(wl)}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        barrier = dist.barrier
+    import selective_state_space_120_b300 as ss
+    ss.load_library()
+
+    wl = WORKLOADS[args.workload]
+    peak, peak_kind = measured_peaks()
+    r, ms, kern_ms, clocks = measure_gpu(wl, args.steps, args.warmup, barrier)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = world * wl.elems / (ms * 1e-3) / 1e9
+    e2e = r.e2e(args.e2e_steps, 3)
+    e2e["value"] *= world
+    copies = r.copies
+    launches = r.launches_per_step * args.steps
+    del r
+    torch.cuda.empty_cache()
+
+    others = {}
+    if not args.no_others:
+        for owl in OTHERS:
+            if owl.name == wl.name:
+                continue
+            try:
+                osteps = max(3, min(args.steps, 50))
+                r2, oms, okern, _ = measure_gpu(owl, osteps, max(3, min(args.warmup, 5)), barrier)
+                others[owl.name] = {
+                    "value": owl.elems / (oms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": oms,
+                    "kernel_launches_per_step": r2.launches_per_step,
+                    "roofline": roofline(owl, oms, peak, peak_kind),
+                    "config": config_of(owl, world, r2.copies)}
+                del r2
+                torch.cuda.empty_cache()
+            except Exception as e:  # noqa: BLE001 -- reported, not hidden
+                others[owl.name] = {"error": f"{type(e).__name__}: {e}"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        v, rows, thr, dt = oracle_sample(wl, budget_s=12.0)
+        cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
+               "sample": f"{rows} whole (batch, channel) rows of the workload (L={wl.L}) "
+                         f"in {dt:.1f} s, threads over rows; host CPU {cpu_model()}"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic (seeded NumPy PCG64; recipe of the workload)",
+                "config": config_of(wl, world, copies),
+                "roofline": roofline(wl, kern_ms, peak, peak_kind),
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clocks, "kernel_ms": kern_ms, "workloads": others}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -200,6 +200,16 @@ const char *ss_version(void);
  * undefined.  Used to test the timeout path. */
 ss_status ss_debug_set_wait_budget_ns(uint64_t ns);
 
+/* Diagnostics: flags of the current device (0 = normal operation).
+ * SS_DEBUG_SKIP_FIRST_COPY: in every launch of the single-direction TMA scan,
+ * the first thread block never issues the copies of its first tile, so its
+ * bounded wait for that tile runs out: the call then reports SS_ERR_TIMEOUT
+ * through ss_get_device_status and the outputs of that call are undefined.
+ * This is how the timeout path is tested without faulting or hanging the GPU.
+ * Returns SS_ERR_INVALID_ARG for unknown bits. */
+#define SS_DEBUG_SKIP_FIRST_COPY 1u
+ss_status ss_debug_set_flags(uint32_t flags);
+
 #ifdef __cplusplus
 }
 #endif

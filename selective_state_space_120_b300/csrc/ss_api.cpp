@@ -254,6 +254,12 @@ ss_status ss_debug_set_wait_budget_ns(uint64_t ns) {
     return set_wait_budget(ns ? (unsigned long long)ns : 1000000000ull);
 }
 
+ss_status ss_debug_set_flags(uint32_t flags) {
+    if (flags & ~uint32_t(SS_DEBUG_SKIP_FIRST_COPY))
+        return fail(SS_ERR_INVALID_ARG, "ss_debug_set_flags: unknown flag bits 0x%x", flags);
+    return set_debug_flags(flags);
+}
+
 const char *ss_last_error_string(void) { return g_msg; }
 
 const char *ss_version(void) { return "ssscan 0.1 (sm_103a)"; }

@@ -25,6 +25,10 @@ constexpr unsigned kFull = 0xffffffffu;
 __device__ unsigned int g_status = 0;
 // Time budget (ns) of every bounded wait; 1 s unless changed for diagnostics.
 __device__ unsigned long long g_wait_budget_ns = 1000000000ull;
+// Diagnostics only (0 in normal use).  Bit 0: the first CTA of each TMA scan
+// launch never issues the copies of its first tile, so its wait for that tile
+// runs out after the wait budget -- the way the timeout path is tested.
+__device__ unsigned int g_debug_flags = 0;
 
 // ------------------------------------------------------------------ SFU math
 __device__ __forceinline__ float ex2(float x) {

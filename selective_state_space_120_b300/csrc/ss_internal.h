@@ -42,5 +42,6 @@ ss_status launch_scan1d(const ScanArgs &a);
 ss_status launch_multidir(const ScanArgs &a);
 ss_status read_device_status(ss_stream_t stream);
 ss_status set_wait_budget(unsigned long long ns);
+ss_status set_debug_flags(unsigned int flags);
 
 }  // namespace ssi

@@ -333,6 +333,12 @@ ss_status read_device_status(ss_stream_t stream) {
     return SS_OK;
 }
 
+ss_status set_debug_flags(unsigned int flags) {
+    const cudaError_t e = cudaMemcpyToSymbol(ssk::g_debug_flags, &flags, sizeof(flags));
+    if (e != cudaSuccess) return fail(SS_ERR_CUDA, "cannot set the debug flags: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+
 ss_status set_wait_budget(unsigned long long ns) {
     const cudaError_t e = cudaMemcpyToSymbol(ssk::g_wait_budget_ns, &ns, sizeof(ns));
     if (e != cudaSuccess) return fail(SS_ERR_CUDA, "cannot set the wait budget: %s", cudaGetErrorString(e));

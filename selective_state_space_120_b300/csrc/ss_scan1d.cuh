@@ -232,7 +232,11 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
     }
     __syncthreads();
 
+    // diagnostics: this CTA leaves its first tile's barrier without arrivals
+    const bool skip_first = (g_debug_flags & 1u) && blockIdx.x == 0 && blockIdx.y == 0 &&
+                            blockIdx.z == 0;
     auto issue = [&](int i) {
+        if (i == 0 && skip_first) return;
         const int s = i % C::STAGES;
         const uint32_t bar = bar0 + 8 * s;
         const uint32_t st = smem0 + s * C::STAGE;
@@ -291,7 +295,8 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
                 // let every copy this CTA issued land before its smem goes away
 #pragma unroll 1
                 for (int k = i; k < nchunks && k < i + C::STAGES; ++k)
-                    (void)mbar_wait_bounded(bar0 + 8 * (k % C::STAGES), (k / C::STAGES) & 1,
+                    if (!(k == 0 && skip_first))
+                        (void)mbar_wait_bounded(bar0 + 8 * (k % C::STAGES), (k / C::STAGES) & 1,
                                             1000000000ull);
             }
             return;

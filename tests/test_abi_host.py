@@ -150,6 +150,12 @@ def test_bidir_and_cross2d_validate(lib):
     assert st == b.SS_ERR_UNSUPPORTED
 
 
+@fake_ptrs
+def test_debug_flags_reject_unknown_bits(lib):
+    assert lib.ss_debug_set_flags(2) == b.SS_ERR_INVALID_ARG
+    assert "unknown flag" in b.last_error()
+
+
 def test_workspace_sizing_is_host_only(lib):
     # the multi-direction calls merge on chip: no workspace
     assert b.workspace_bytes(b.SS_KIND_BIDIR, 128, 768, 197, 16) == 0
