@@ -172,6 +172,46 @@ ss_status ss_cross_scan2d_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, 
                               void *out, float *last_state, void *workspace,
                               size_t workspace_bytes, ss_stream_t stream);
 
+/*
+ * ss_selective_scan_fwd_noalloc -- ss_selective_scan_fwd_opts for callers that
+ * cannot allocate device memory.  (Library addition: the pages have no
+ * counterpart; it computes exactly what ss_selective_scan_fwd_opts computes.)
+ *
+ * Who needs it: code that runs where device allocation is not allowed or not
+ * affordable -- a plug-in executed inside another engine's enqueue step, where
+ * the host engine owns all device memory; a real-time loop in which a
+ * cudaMalloc/cudaFree (which may synchronise the device) would break its
+ * latency budget; a caller without access to any allocator at all.  Such a
+ * caller cannot supply the workspace that the long-sequence chunked path of
+ * ss_selective_scan_fwd needs.
+ *
+ * Instead of a workspace, this call uses one fixed scratch array of
+ * SS_NOALLOC_SCRATCH_BYTES bytes that the library holds as static device memory
+ * on every GPU that loads it, until the process exits.  It calls no cudaMalloc,
+ * no cudaFree and no allocating library routine.  Arguments, layouts, options
+ * and results are those of ss_selective_scan_fwd_opts, without the workspace.
+ *
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current).  Make that first call
+ *   before any stream capture on the device.
+ * - Calls whose chunked path would need more than SS_NOALLOC_SCRATCH_BYTES
+ *   (see ss_workspace_bytes_opts) return SS_ERR_UNSUPPORTED before launching
+ *   anything; pass fewer chunks or use ss_selective_scan_fwd with a workspace.
+ * - Every call on a device shares the one array, which keeps the last call's
+ *   contents; the chunked path writes every scratch word before reading it, so
+ *   nothing needs clearing between calls.  Calls that can overlap on the GPU
+ *   (different streams without ordering, or several host threads) race on the
+ *   array and produce undefined results: order them on one stream.
+ */
+#define SS_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+ss_status ss_selective_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t seqlen, int dstate,
+                                        int ngroups, ss_dtype io, const void *u,
+                                        const void *delta, const float *A, const void *B,
+                                        const void *C, const float *D, const void *z,
+                                        const float *delta_bias, int delta_softplus, void *out,
+                                        float *last_state, const ss_scan_options *options,
+                                        ss_stream_t stream);
+
 /* Workspace bytes a call of the given kind and shape needs (0 if none), for
  * either I/O dtype (the larger of the two).  For SS_KIND_CROSS2D pass
  * seqlen = H*W.  Host computation only. */

@@ -189,6 +189,44 @@ ss_status ss_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int 
                                       workspace, workspace_bytes, nullptr, stream);
 }
 
+ss_status ss_selective_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t seqlen, int dstate,
+                                        int ngroups, ss_dtype io, const void *u,
+                                        const void *delta, const float *A, const void *B,
+                                        const void *C, const float *D, const void *z,
+                                        const float *delta_bias, int delta_softplus, void *out,
+                                        float *last_state, const ss_scan_options *options,
+                                        ss_stream_t stream) {
+    static const char *fn = "ss_selective_scan_fwd_noalloc";
+    bool empty = false;
+    ss_status st = check_common(fn, batch, dim, seqlen, dstate, ngroups, io, 1, u, delta, A, B, C,
+                                D, z, delta_bias, out, last_state, &empty);
+    if (st != SS_OK || empty) return st;
+    int chunks = 0;
+    if (options) {
+        for (int r : options->reserved)
+            if (r != 0) return fail(SS_ERR_INVALID_ARG, "%s: reserved option fields must be zero", fn);
+        if (options->chunks < 0) return fail(SS_ERR_INVALID_ARG, "%s: options.chunks < 0", fn);
+        chunks = options->chunks;
+    }
+    ScanArgs a = scan_args(batch, dim, seqlen, dstate, ngroups, io, u, delta, A, B, C, D, z,
+                           delta_bias, delta_softplus, out, last_state, nullptr, 0, stream);
+    a.chunks = chunks;
+    const size_t need = scan1d_workspace_bytes(a);
+    if (need > SS_NOALLOC_SCRATCH_BYTES)
+        return fail(SS_ERR_UNSUPPORTED,
+                    "%s: this shape needs %zu bytes of scratch, more than the fixed %zu bytes "
+                    "the library holds; request fewer chunks, or call ss_selective_scan_fwd "
+                    "with a workspace",
+                    fn, need, (size_t)SS_NOALLOC_SCRATCH_BYTES);
+    if (need > 0) {
+        void *scratch = nullptr;
+        if ((st = noalloc_scratch(&scratch))) return st;
+        a.ws = scratch;
+        a.ws_bytes = SS_NOALLOC_SCRATCH_BYTES;
+    }
+    return launch_scan1d(a);
+}
+
 ss_status ss_bidir_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int ngroups,
                             ss_dtype io, const void *u, const void *delta, const float *A,
                             const void *B, const void *C, const float *D, const void *z,

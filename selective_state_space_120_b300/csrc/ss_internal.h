@@ -43,5 +43,8 @@ ss_status launch_multidir(const ScanArgs &a);
 ss_status read_device_status(ss_stream_t stream);
 ss_status set_wait_budget(unsigned long long ns);
 ss_status set_debug_flags(unsigned int flags);
+// Device address of the fixed scratch array of ss_selective_scan_fwd_noalloc on
+// the current device (looked up once per device).
+ss_status noalloc_scratch(void **ptr);
 
 }  // namespace ssi

@@ -333,6 +333,34 @@ ss_status read_device_status(ss_stream_t stream) {
     return SS_OK;
 }
 
+// Scratch of ss_selective_scan_fwd_noalloc: fixed-size static device memory,
+// present on every device that loads the library, shared by all its calls.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SS_NOALLOC_SCRATCH_BYTES];
+
+// In host code g_noalloc_scratch names a host-side shadow, not device memory:
+// the device address comes from cudaGetSymbolAddress, once per device, with
+// that device current.  Guarded by a mutex for callers on several threads.
+ss_status noalloc_scratch(void **ptr) {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static void *addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SS_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(SS_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(SS_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed: %s",
+                        cudaGetErrorString(e));
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return SS_OK;
+}
+
 ss_status set_debug_flags(unsigned int flags) {
     const cudaError_t e = cudaMemcpyToSymbol(ssk::g_debug_flags, &flags, sizeof(flags));
     if (e != cudaSuccess) return fail(SS_ERR_CUDA, "cannot set the debug flags: %s", cudaGetErrorString(e));
