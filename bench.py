@@ -111,42 +111,82 @@ _REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_
             0x100: "display_clock_setting"}
 
 
+class _Nvml:
+    """Minimal NVML reader through ctypes (libnvidia-ml ships with the driver):
+    SM clock, its maximum, and the active clock-event (throttle) reasons."""
+
+    def __init__(self, index: int):
+        import ctypes.util
+        lib = None
+        for name in ("libnvidia-ml.so.1", ctypes.util.find_library("nvidia-ml")):
+            if not name:
+                continue
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if lib is None:
+            raise OSError("libnvidia-ml not found")
+        self.lib = lib
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise OSError("nvmlDeviceGetHandleByIndex failed")
+        fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self._reasons_fn = fn or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_mhz(self) -> int:
+        v = ctypes.c_uint()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(v)) != 0:  # NVML_CLOCK_SM
+            raise OSError("nvmlDeviceGetClockInfo failed")
+        return int(v.value)
+
+    def sm_max_mhz(self) -> int:
+        v = ctypes.c_uint()
+        if self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(v)) != 0:
+            raise OSError("nvmlDeviceGetMaxClockInfo failed")
+        return int(v.value)
+
+    def reasons(self) -> int:
+        v = ctypes.c_ulonglong()
+        if self._reasons_fn(self.h, ctypes.byref(v)) != 0:
+            raise OSError("clock event reasons query failed")
+        return int(v.value)
+
+
 class ClockSampler:
-    """Samples the SM clock and the clock-event reasons through NVML in a thread."""
+    """Samples the SM clock and the clock-event reasons through NVML in a thread
+    while the timed region runs (reading only; no GPU setting is changed)."""
 
     def __init__(self, index: int, period_s: float = 0.002):
         self.period = period_s
         self.samples = []
         self.reasons = 0
         self.max_mhz = None
+        self.error = None
         self._stop = threading.Event()
         self._thr = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nv = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-        except Exception:  # noqa: BLE001 -- clocks are reported as unavailable
+            self._nv = _Nvml(index)
+            self.max_mhz = self._nv.sm_max_mhz()
+        except Exception as e:  # noqa: BLE001 -- clocks are reported as unavailable
             self._nv = None
-
-    def _reasons(self):
-        nv = self._nv
-        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
-        return fn(self._h)
+            self.error = f"{type(e).__name__}: {e}"
 
     def _sample(self):
-        self.samples.append(self._nv.nvmlDeviceGetClockInfo(self._h, self._nv.NVML_CLOCK_SM))
-        self.reasons |= int(self._reasons())
+        self.samples.append(self._nv.sm_mhz())
+        self.reasons |= self._nv.reasons()
 
     def _run(self):
-        while not self._stop.is_set():
+        while True:
             try:
                 self._sample()
-            except Exception:  # noqa: BLE001
-                pass
-            self._stop.wait(self.period)
+            except Exception as e:  # noqa: BLE001
+                self.error = f"{type(e).__name__}: {e}"
+            if self._stop.wait(self.period):
+                break
 
     def __enter__(self):
         if self._nv is not None:
@@ -162,7 +202,7 @@ class ClockSampler:
     def summary(self):
         if self._nv is None or not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"],
-                    "samples": 0}
+                    "samples": 0, "error": self.error}
         names = [n for bit, n in _REASONS.items() if self.reasons & bit]
         return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
                 "reasons": names, "samples": len(self.samples)}
@@ -196,11 +236,11 @@ class Runner:
         self.stream = torch.cuda.current_stream(device)
         self.ws = None
         self.opts = b.options(0)
-        if wl.K == 1:
-            wsb = int(self.lib.ss_workspace_bytes_opts(b.SS_KIND_SCAN, wl.batch, wl.dim, wl.L,
-                                                       wl.N, ctypes.byref(self.opts)))
-            if wsb:
-                self.ws = torch.empty(wsb, dtype=torch.uint8, device=device)
+        kind = {1: b.SS_KIND_SCAN, 2: b.SS_KIND_BIDIR, 4: b.SS_KIND_CROSS2D}[wl.K]
+        wsb = int(self.lib.ss_workspace_bytes_opts(kind, wl.batch, wl.dim, wl.L, wl.N,
+                                                   ctypes.byref(self.opts)))
+        if wsb:
+            self.ws = torch.empty(wsb, dtype=torch.uint8, device=device)
         self.args = [self._args(s) for s in self.sets]
         self.launches_per_step = self._launches()
         self._ss = ss
@@ -230,15 +270,18 @@ class Runner:
             return (self.lib.ss_bidir_scan_fwd,
                     (wl.batch, wl.dim, wl.L, wl.N, wl.G, io, p(s["u"]), p(s["delta"]), p(s["A"]),
                      p(s["B"]), p(s["C"]), p(s["D"]), p(s["z"]), p(s["delta_bias"]), 1,
-                     p(s["out"]), p(s["last"]), None, 0, st))
+                     p(s["out"]), p(s["last"]), ws, wsb, st))
         return (self.lib.ss_cross_scan2d_fwd,
                 (wl.batch, wl.dim, wl.H, wl.W, wl.N, wl.G, io, p(s["u"]), p(s["delta"]),
                  p(s["A"]), p(s["B"]), p(s["C"]), p(s["D"]), p(s["delta_bias"]), 1, p(s["z"]),
-                 p(s["out"]), p(s["last"]), None, 0, st))
+                 p(s["out"]), p(s["last"]), ws, wsb, st))
 
     def _launches(self):
-        """Kernels one step launches: 1, or 3 on the chunked long-sequence path."""
-        return 3 if self.ws is not None else 1
+        """Kernels one step launches: 1; 3 on the chunked long-sequence path; one
+        per direction when the multi-direction call merges through its workspace."""
+        if self.ws is None:
+            return 1
+        return 3 if self.wl.K == 1 else self.wl.K
 
     def step(self, i: int):
         fn, args = self.args[i % self.copies]
@@ -438,7 +481,7 @@ def roofline(wl, kern_ms, peak, peak_kind):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(WORKLOADS))

@@ -20,16 +20,18 @@
  *     section 3.1: a forward scan plus a scan of the reversed sequence with its own
  *     parameters.
  *
- * Per (batch b, direction k, channel d) the scan visits positions p = pi_k(s),
- * s = 0..L-1, starting from h = 0:
- *     dt    = Delta_k[d,p] + delta_bias_k[d];  dt = softplus(dt) if delta_softplus
- *     h_n   = exp(dt * A_k[d,n]) * h_n + dt * B_k[g,n,p] * u[d,p]          n < dstate
- *     y_k   = sum_n C_k[g,n,p] * h_n + D_k[d] * u[d,p]
+ * Per (batch b, direction k, channel d) the scan takes steps s = 0..L-1, step s
+ * visiting position p = pi_k(s), starting from h = 0:
+ *     dt    = Delta_k[d,s] + delta_bias_k[d];  dt = softplus(dt) if delta_softplus
+ *     h_n   = exp(dt * A_k[d,n]) * h_n + dt * B_k[g,n,s] * u[d,p]          n < dstate
+ *     y_k(p) = sum_n C_k[g,n,s] * h_n + D_k[d] * u[d,p]
  *     out[d,p] = (sum_k y_k(p)) * (z ? z*sigmoid(z) : 1)     (z[d,p])
- * Channel d uses group g = d / (dim / ngroups).  Per-direction Delta, B and C are
- * indexed by POSITION p (the H x W map order), not by scan step; this is the
- * layout a pointwise projection of the map produces, and it needs no permuted
- * copies.
+ * Channel d uses group g = d / (dim / ngroups).  u, z and out are indexed by
+ * POSITION p (token order, or the H x W map in row-major order).  Each
+ * direction's Delta_k, B_k and C_k are indexed by its own SCAN STEP s, the
+ * layout in which the key code computes them (by projecting the already
+ * reordered sequences); u is gathered by index arithmetic, with no permuted
+ * copy.
  *
  * Layouts: every tensor is dense and C-contiguous (last index fastest).
  *   dtype ss_dtype io:  u, delta, B, C, z, out          (SS_F32 or SS_BF16)
@@ -133,14 +135,21 @@ ss_status ss_selective_scan_fwd_opts(int64_t batch, int64_t dim, int64_t seqlen,
  * the two outputs are summed and then gated once by SiLU(z).
  *
  *   u          [batch, dim, seqlen]               io
- *   delta      [batch, 2, dim, seqlen]            io (indexed by position)
+ *   delta      [batch, 2, dim, seqlen]            io (direction 1 in reversed order:
+ *                                                   its step s is token L-1-s)
  *   A          [2*dim, dstate]                    float
- *   B, C       [batch, 2, ngroups, dstate, seqlen] io (indexed by position)
+ *   B, C       [batch, 2, ngroups, dstate, seqlen] io (scan order, as delta)
  *   D, delta_bias [2*dim]                         float, nullable
  *   z          [batch, dim, seqlen]               io, nullable
  *   out        [batch, dim, seqlen]               io
  *   last_state [batch, 2, dim, dstate]            float, nullable (direction 1: state after position 0)
- * No workspace is needed (the merge is done on chip); pass NULL, 0.
+ *   workspace  ss_workspace_bytes(SS_KIND_BIDIR, ...) bytes of device scratch, 16-byte
+ *              aligned, not overlapping any tensor; NULL when that is 0.
+ * When rows are 16-byte aligned (seqlen * element size % 16 == 0) the two
+ * directions run as two TMA-staged scans that merge through the workspace, an
+ * fp32 [batch, dim, seqlen] accumulator (first direction stores, second adds,
+ * gates and writes out: deterministic).  Otherwise the call merges on chip and
+ * needs no workspace.
  */
 ss_status ss_bidir_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int ngroups,
                             ss_dtype io, const void *u, const void *delta, const float *A,
@@ -154,16 +163,21 @@ ss_status ss_bidir_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dsta
  * cross-merge, fused: no permuted copies of the map are made.
  *
  *   u          [batch, dim, H, W]                 io
- *   delta      [batch, 4, dim, H, W]              io (direction k = SS_DIR_*, by position)
+ *   delta      [batch, 4, dim, H*W]               io (direction k = SS_DIR_*, in its scan order)
  *   A          [4*dim, dstate]                    float
- *   B, C       [batch, 4, ngroups, dstate, H, W]  io (by position)
+ *   B, C       [batch, 4, ngroups, dstate, H*W]   io (scan order of each direction)
  *   D, delta_bias [4*dim]                         float, nullable
  *   z          [batch, dim, H, W]                 io, nullable (VMamba gates after a norm,
  *                                                  so its SS2D passes NULL)
  *   out        [batch, dim, H, W]                 io: sum over the four directions
  *   last_state [batch, 4, dim, dstate]            float, nullable
- * The whole map of a channel is merged in shared memory: H*W is limited by the
- * per-block shared-memory size (SS_ERR_UNSUPPORTED beyond it).  No workspace.
+ *   workspace  ss_workspace_bytes(SS_KIND_CROSS2D, batch, dim, H*W, dstate) bytes,
+ *              16-byte aligned, not overlapping any tensor; NULL when that is 0.
+ * When rows are 16-byte aligned (H*W * element size % 16 == 0) the four
+ * directions run as four TMA-staged scans in SS_DIR_* order that merge through
+ * the workspace (an fp32 [batch, dim, H*W] accumulator; deterministic).
+ * Otherwise the whole map of a channel is merged in shared memory: H*W is then
+ * limited by the per-block shared-memory size (SS_ERR_UNSUPPORTED beyond it).
  */
 ss_status ss_cross_scan2d_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, int dstate,
                               int ngroups, ss_dtype io, const void *u, const void *delta,
@@ -214,7 +228,8 @@ ss_status ss_selective_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t seql
 
 /* Workspace bytes a call of the given kind and shape needs (0 if none), for
  * either I/O dtype (the larger of the two).  For SS_KIND_CROSS2D pass
- * seqlen = H*W.  Host computation only. */
+ * seqlen = H*W.  Host computation only.  A call given a non-NULL workspace of
+ * at least this size never fails for lack of one. */
 size_t ss_workspace_bytes(int kind, int64_t batch, int64_t dim, int64_t seqlen, int dstate);
 
 /* Same for ss_selective_scan_fwd_opts with the given options. */

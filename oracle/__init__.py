@@ -11,8 +11,9 @@ source and calls it through ctypes with NumPy float64 arrays.
 Conventions (see the C file's header for the equations and their sources):
     u [batch, dim, L], delta [batch, K, dim, L], A [K*dim, N],
     B, C [batch, K, G, N, L], D / delta_bias [K*dim], z [batch, dim, L],
-    h0 / last_state [batch, K, dim, N]; per-direction Delta, B, C are indexed by
-    position, and a direction's order is one of ORDER_*.
+    h0 / last_state [batch, K, dim, N]; u, z and the output are indexed by
+    position, the per-direction Delta, B, C by that direction's scan step, and a
+    direction's order is one of ORDER_*.
 """
 from __future__ import annotations
 
@@ -154,7 +155,8 @@ SS2D_ORDERS = (ORDER_FWD, ORDER_COL, ORDER_REV, ORDER_COL_REV)
 
 
 def cross_scan2d(u, delta, A, B, C, H, W, D=None, z=None, delta_bias=None, delta_softplus=True):
-    """SS2D: u [batch, dim, H, W]; delta [batch, 4, dim, H, W]; B/C [batch, 4, G, N, H, W]."""
+    """SS2D: u [batch, dim, H, W]; delta [batch, 4, dim, H*W] and B/C
+    [batch, 4, G, N, H*W], each direction in its own scan order."""
     u = np.asarray(u)
     batch, dim = u.shape[:2]
     L = H * W

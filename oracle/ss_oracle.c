@@ -18,7 +18,10 @@
  *   - same page, "关键代码" (key code), SS2D forward: four traversal orders of an
  *     H x W map (row-major, column-major, and the reverse of each), one scan per
  *     order, outputs mapped back to H x W and summed; softplus is applied to
- *     Delta + delta_bias, and a skip term D*u is part of each scan.
+ *     Delta + delta_bias, and a skip term D*u is part of each scan.  There the
+ *     per-direction Delta, B and C are projections of the already reordered
+ *     sequences xs, so each direction receives them in its own scan order;
+ *     only the input x (u here) is gathered from the map.
  *   - "从LSTM到Mamba：为什么说双向状态空间模型是处理视觉序列的'潜力股'？",
  *     section 3.1: bidirectional scan = a forward scan plus a scan of the reversed
  *     sequence with its own parameters.  The two outputs are SUMMED here (not
@@ -26,12 +29,13 @@
  *
  * Recurrence, per (batch b, direction k, channel d), over scan steps s = 0..L-1
  * visiting positions p = pi_k(s):
- *     dt      = Delta_k[d, p] + bias_k[d];   dt = softplus(dt) if requested
- *     h_n     = exp(dt*A_k[d,n]) * h_n + Bbar_{k,n}(p) * u[d, p]      (n = 0..N-1)
- *     y_k(p)  = sum_n C_k[g, n, p] * h_n + D_k[d] * u[d, p]
+ *     dt      = Delta_k[d, s] + bias_k[d];   dt = softplus(dt) if requested
+ *     h_n     = exp(dt*A_k[d,n]) * h_n + Bbar_{k,n}(s) * u[d, p]      (n = 0..N-1)
+ *     y_k(p)  = sum_n C_k[g, n, s] * h_n + D_k[d] * u[d, p]
  * with h = 0 (or a caller-given h0) before the first step, then
  *     out[d, p] = (sum_k y_k(p)) * (z ? z*sigmoid(z) : 1).
- * Per-direction Delta, B, C are indexed by position p (not by scan step).
+ * u, z and out are indexed by position p; the per-direction Delta, B, C are
+ * indexed by scan step s (each direction's own order).
  * Channel d uses group g = d / (dim / ngroups).
  *
  * Everything is float64 and strictly sequential; libm exp/log1p only.
@@ -70,9 +74,9 @@ static int64_t ssor_position(int order, int64_t s, int64_t H, int64_t W) {
  *
  * Layouts (all float64, C-contiguous):
  *   u          [batch, dim, L]              L = H*W
- *   delta      [batch, K, dim, L]
+ *   delta      [batch, K, dim, L]            (scan order of each direction)
  *   A          [K*dim, N]
- *   Bm, Cm     [batch, K, ngroups, N, L]
+ *   Bm, Cm     [batch, K, ngroups, N, L]     (scan order of each direction)
  *   Dv         [K*dim]        (NULL: no skip term)
  *   z          [batch, dim, L] (NULL: no gate)
  *   bias       [K*dim]        (NULL: zero)
@@ -115,7 +119,7 @@ int ssor_scan(int64_t batch, int64_t dim, int64_t H, int64_t W, int64_t N, int64
                 for (int64_t s = 0; s < L; ++s) {
                     const int64_t p = ssor_position(orders[k], s, H, W);
                     if (p < 0) return -1;
-                    double dt = dl_row[p] + bd;
+                    double dt = dl_row[s] + bd;
                     if (delta_softplus) dt = ssor_softplus(dt);
                     const double up = u_row[p];
                     double y = 0.0;
@@ -124,11 +128,11 @@ int ssor_scan(int64_t batch, int64_t dim, int64_t H, int64_t W, int64_t N, int64
                         const double abar = exp(dt * a);
                         double bbar;
                         if (zoh && a != 0.0)
-                            bbar = (abar - 1.0) / a * B_grp[n * L + p];   /* (dA)^-1 (e^{dA}-1) dB */
+                            bbar = (abar - 1.0) / a * B_grp[n * L + s];   /* (dA)^-1 (e^{dA}-1) dB */
                         else
-                            bbar = dt * B_grp[n * L + p];                 /* Euler: dB */
+                            bbar = dt * B_grp[n * L + s];                 /* Euler: dB */
                         h[n] = abar * h[n] + bbar * up;
-                        y += C_grp[n * L + p] * h[n];
+                        y += C_grp[n * L + s] * h[n];
                     }
                     o_row[p] += y + Dd * up;
                 }

@@ -8,6 +8,9 @@ in the library's sm_103a kernels; there is no fallback.
     out = selective_scan_fwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus=True)
     out = bidir_scan_fwd(u, delta2, A2, B2, C2, D2, z, bias2)
     out = cross_scan2d_fwd(u_map, delta4, A4, B4, C4, D4, bias4)
+
+u, z and out are indexed by position; each direction's delta, B and C are in
+that direction's scan order.
 """
 from __future__ import annotations
 
@@ -104,10 +107,20 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta
     return (out, last) if return_last_state else out
 
 
+def _multidir_workspace(lib, kind, batch, dim, L, N, dev, workspace):
+    torch = _torch()
+    wsb = int(lib.ss_workspace_bytes(kind, batch, dim, L, N))
+    if wsb and (workspace is None or workspace.numel() < wsb):
+        workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    return (_ptr(workspace), workspace.numel()) if wsb else (None, 0)
+
+
 def bidir_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-                   return_last_state=False, out=None, stream=None):
-    """Bidirectional scan: delta [batch, 2, dim, L]; A [2*dim, N]; B, C [batch, 2, G, N, L];
-    D, delta_bias [2*dim].  Returns out [batch, dim, L] (and last_state [batch, 2, dim, N])."""
+                   return_last_state=False, out=None, workspace=None, stream=None):
+    """Bidirectional scan: delta [batch, 2, dim, L] and B, C [batch, 2, G, N, L], the
+    reversed direction (index 1) in its own scan order (its step s is token L-1-s);
+    A [2*dim, N]; D, delta_bias [2*dim].  Returns out [batch, dim, L] (and
+    last_state [batch, 2, dim, N])."""
     torch = _torch()
     lib = _b.load()
     batch, dim, L = u.shape
@@ -125,27 +138,30 @@ def bidir_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_sof
         out = torch.empty_like(u)
     _check_io("out", out, io, dev, (batch, dim, L))
     last = torch.empty(batch, 2, dim, N, dtype=torch.float32, device=dev) if return_last_state else None
+    ws, wsb = _multidir_workspace(lib, _b.SS_KIND_BIDIR, batch, dim, L, N, dev, workspace)
     _b.check(lib.ss_bidir_scan_fwd(
         batch, dim, L, N, G, _io_code(u), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
         _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(out), _ptr(last),
-        None, 0, _stream(stream, dev)))
+        ws, wsb, _stream(stream, dev)))
     return (out, last) if return_last_state else out
 
 
 def cross_scan2d_fwd(u, delta, A, B, C, D=None, delta_bias=None, delta_softplus=True, z=None,
-                     return_last_state=False, out=None, stream=None):
-    """SS2D: u [batch, dim, H, W]; delta [batch, 4, dim, H, W]; A [4*dim, N];
-    B, C [batch, 4, G, N, H, W]; D, delta_bias [4*dim].  Returns out [batch, dim, H, W]
-    (and last_state [batch, 4, dim, N])."""
+                     return_last_state=False, out=None, workspace=None, stream=None):
+    """SS2D: u [batch, dim, H, W]; delta [batch, 4, dim, H*W] and B, C
+    [batch, 4, G, N, H*W], each direction in its own scan order (row-major,
+    column-major, reversed row-major, reversed column-major); A [4*dim, N];
+    D, delta_bias [4*dim].  Returns out [batch, dim, H, W] (and last_state
+    [batch, 4, dim, N])."""
     torch = _torch()
     lib = _b.load()
     batch, dim, H, W = u.shape
     G, N = B.shape[2], B.shape[3]
     io, dev = u.dtype, u.device
     _check_io("u", u, io, dev)
-    _check_io("delta", delta, io, dev, (batch, 4, dim, H, W))
-    _check_io("B", B, io, dev, (batch, 4, G, N, H, W))
-    _check_io("C", C, io, dev, (batch, 4, G, N, H, W))
+    _check_io("delta", delta, io, dev, (batch, 4, dim, H * W))
+    _check_io("B", B, io, dev, (batch, 4, G, N, H * W))
+    _check_io("C", C, io, dev, (batch, 4, G, N, H * W))
     _check_io("z", z, io, dev, (batch, dim, H, W))
     _check_io("A", A, torch.float32, dev, (4 * dim, N))
     _check_io("D", D, torch.float32, dev, (4 * dim,))
@@ -154,10 +170,11 @@ def cross_scan2d_fwd(u, delta, A, B, C, D=None, delta_bias=None, delta_softplus=
         out = torch.empty_like(u)
     _check_io("out", out, io, dev, (batch, dim, H, W))
     last = torch.empty(batch, 4, dim, N, dtype=torch.float32, device=dev) if return_last_state else None
+    ws, wsb = _multidir_workspace(lib, _b.SS_KIND_CROSS2D, batch, dim, H * W, N, dev, workspace)
     _b.check(lib.ss_cross_scan2d_fwd(
         batch, dim, H, W, N, G, _io_code(u), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
         _ptr(D), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(z), _ptr(out), _ptr(last),
-        None, 0, _stream(stream, dev)))
+        ws, wsb, _stream(stream, dev)))
     return (out, last) if return_last_state else out
 
 

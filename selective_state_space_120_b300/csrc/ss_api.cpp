@@ -78,6 +78,25 @@ ss_status check_common(const char *fn, int64_t batch, int64_t dim, int64_t L, in
     return SS_OK;
 }
 
+// The merge accumulator of the multi-direction calls must not overlap any tensor.
+ss_status check_ws_overlap(const char *fn, const ScanArgs &a) {
+    if (!a.ws || a.ws_bytes == 0) return SS_OK;
+    const int64_t es = a.io == SS_BF16 ? 2 : 4;
+    const int64_t nel = a.batch * a.dim * a.L;
+    const Span w{static_cast<const char *>(a.ws), (int64_t)a.ws_bytes};
+    const Span all[] = {{static_cast<const char *>(a.out), nel * es},
+                        {static_cast<const char *>(a.u), nel * es},
+                        {static_cast<const char *>(a.delta), nel * a.K * es},
+                        {static_cast<const char *>(a.B), a.batch * a.K * a.G * a.N * a.L * es},
+                        {static_cast<const char *>(a.C), a.batch * a.K * a.G * a.N * a.L * es},
+                        {static_cast<const char *>(a.z), a.z ? nel * es : 0},
+                        {reinterpret_cast<const char *>(a.last_state),
+                         a.last_state ? a.batch * a.K * a.dim * a.N * 4 : 0}};
+    for (const Span &t : all)
+        if (overlaps(w, t)) return fail(SS_ERR_INVALID_ARG, "%s: workspace overlaps a tensor", fn);
+    return SS_OK;
+}
+
 ss_status check_workspace(const char *fn, size_t need, const void *ws, size_t have) {
     if (need == 0) return SS_OK;
     if (!ws || have < need)
@@ -130,6 +149,23 @@ size_t ws_scan1d_any_dtype(int64_t batch, int64_t dim, int64_t L, int dstate, in
         a.io = io;
         a.chunks = chunks;
         const size_t w = scan1d_workspace_bytes(a);
+        if (w > best) best = w;
+    }
+    return best;
+}
+
+size_t ws_multidir_any_dtype(int64_t batch, int64_t dim, int64_t L, int dstate) {
+    if (batch <= 0 || dim <= 0 || L <= 0 || !valid_dstate(dstate)) return 0;
+    size_t best = 0;
+    for (int io : {SS_F32, SS_BF16}) {
+        ScanArgs a;
+        a.batch = batch;
+        a.dim = dim;
+        a.L = L;
+        a.W = L;
+        a.N = dstate;
+        a.io = io;
+        const size_t w = multidir_workspace_bytes(a);
         if (w > best) best = w;
     }
     return best;
@@ -234,17 +270,18 @@ ss_status ss_bidir_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dsta
                             float *last_state, void *workspace, size_t workspace_bytes,
                             ss_stream_t stream) {
     static const char *fn = "ss_bidir_scan_fwd";
-    (void)workspace;
-    (void)workspace_bytes;
     bool empty = false;
     ss_status st = check_common(fn, batch, dim, seqlen, dstate, ngroups, io, 2, u, delta, A, B, C,
                                 D, z, delta_bias, out, last_state, &empty);
     if (st != SS_OK || empty) return st;
     ScanArgs a = scan_args(batch, dim, seqlen, dstate, ngroups, io, u, delta, A, B, C, D, z,
-                           delta_bias, delta_softplus, out, last_state, nullptr, 0, stream);
+                           delta_bias, delta_softplus, out, last_state, workspace,
+                           workspace_bytes, stream);
     a.K = 2;
     a.orders[0] = ORD_ROW;
     a.orders[1] = ORD_ROW_REV;
+    if ((st = check_workspace(fn, multidir_workspace_bytes(a), workspace, workspace_bytes))) return st;
+    if ((st = check_ws_overlap(fn, a))) return st;
     return launch_multidir(a);
 }
 
@@ -255,8 +292,6 @@ ss_status ss_cross_scan2d_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, 
                               void *out, float *last_state, void *workspace,
                               size_t workspace_bytes, ss_stream_t stream) {
     static const char *fn = "ss_cross_scan2d_fwd";
-    (void)workspace;
-    (void)workspace_bytes;
     if (H < 0 || W < 0) return fail(SS_ERR_INVALID_ARG, "%s: negative map size", fn);
     if (H >= (1ll << 31) || W >= (1ll << 31) || (H > 0 && W > (INT64_MAX / H)))
         return fail(SS_ERR_UNSUPPORTED, "%s: map too large", fn);
@@ -265,7 +300,8 @@ ss_status ss_cross_scan2d_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, 
                                 D, z, delta_bias, out, last_state, &empty);
     if (st != SS_OK || empty) return st;
     ScanArgs a = scan_args(batch, dim, H * W, dstate, ngroups, io, u, delta, A, B, C, D, z,
-                           delta_bias, delta_softplus, out, last_state, nullptr, 0, stream);
+                           delta_bias, delta_softplus, out, last_state, workspace,
+                           workspace_bytes, stream);
     a.K = 4;
     a.H = H;
     a.W = W;
@@ -273,12 +309,16 @@ ss_status ss_cross_scan2d_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, 
     a.orders[1] = ORD_COL;
     a.orders[2] = ORD_ROW_REV;
     a.orders[3] = ORD_COL_REV;
+    if ((st = check_workspace(fn, multidir_workspace_bytes(a), workspace, workspace_bytes))) return st;
+    if ((st = check_ws_overlap(fn, a))) return st;
     return launch_multidir(a);
 }
 
 size_t ss_workspace_bytes_opts(int kind, int64_t batch, int64_t dim, int64_t seqlen, int dstate,
                                const ss_scan_options *options) {
-    if (kind != SS_KIND_SCAN) return 0;  // the multi-direction calls merge on chip
+    if (kind == SS_KIND_BIDIR || kind == SS_KIND_CROSS2D)
+        return ws_multidir_any_dtype(batch, dim, seqlen, dstate);
+    if (kind != SS_KIND_SCAN) return 0;
     return ws_scan1d_any_dtype(batch, dim, seqlen, dstate, options ? options->chunks : 0);
 }
 

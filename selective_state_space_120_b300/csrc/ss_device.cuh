@@ -68,17 +68,35 @@ __device__ __forceinline__ float silu(float z) { return z * rcp(1.0f + ex2(-z * 
 
 // ------------------------------------------------------------------ I/O types
 template <typename IO> struct IOT;
+// load_raw / widen split a load from its conversion, so a prefetched value can
+// stay in flight until it is used.
 template <> struct IOT<float> {
+    using Raw = float;
     static __device__ __forceinline__ float from_f(float v) { return v; }
     static __device__ __forceinline__ float load(const float *p) { return __ldg(p); }
+    static __device__ __forceinline__ Raw load_raw(const float *p) { return __ldg(p); }
+    static __device__ __forceinline__ float widen(Raw r) { return r; }
 };
 template <> struct IOT<__nv_bfloat16> {
+    using Raw = unsigned short;
     static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
     static __device__ __forceinline__ float load(const __nv_bfloat16 *p) {
         const unsigned short b = __ldg(reinterpret_cast<const unsigned short *>(p));
         return __uint_as_float(static_cast<uint32_t>(b) << 16);
     }
+    static __device__ __forceinline__ Raw load_raw(const __nv_bfloat16 *p) {
+        return __ldg(reinterpret_cast<const unsigned short *>(p));
+    }
+    static __device__ __forceinline__ float widen(Raw r) {
+        return __uint_as_float(static_cast<uint32_t>(r) << 16);
+    }
 };
+
+// Two floats -> one 32-bit word of two bf16 (round to nearest even), low half first.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
 
 // Unpacks a 32-bit word of the I/O type into floats (2 bf16 values or 1 float).
 __device__ __forceinline__ void unpack_word(uint32_t w, float *dst, __nv_bfloat16 *) {
@@ -187,12 +205,45 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
 }
 __device__ __forceinline__ void report_timeout() { atomicOr(&g_status, 1u); }
 
+// ------------------------------------------------------------------ traversal orders
+// Division by a runtime-invariant divisor through a multiply-high (Granlund and
+// Montgomery, "Division by Invariant Integers using Multiplication", 1994):
+// for 1 <= d < 2^31 and 0 <= n < 2^31, n / d = (mulhi(m, n) + n) >> l with
+// l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1.
+struct FastDiv {
+    uint32_t d, m, l;
+    __host__ __device__ FastDiv() : d(1), m(1), l(0) {}
+    __host__ explicit FastDiv(uint32_t dv) : d(dv) {
+        l = 0;
+        while ((1ull << l) < dv) ++l;
+        m = (uint32_t)((((1ull << l) - dv) << 32) / dv + 1);
+    }
+    __device__ __forceinline__ uint32_t div(uint32_t n) const {
+        return (uint32_t)(((uint64_t)__umulhi(m, n) + n) >> l);
+    }
+};
+
+// Position (row-major index on the H x W map; a plain sequence is H = 1) that
+// scan step s of a direction with the given order visits:
+//   0 row-major, 1 column-major (the transposed map), 2 and 3 their reverses.
+__device__ __forceinline__ int64_t position_of(int order, int64_t s, int64_t L, int H, int W,
+                                               const FastDiv &divH) {
+    if (order == 2 || order == 3) s = L - 1 - s;  // reversed orders
+    if (order == 1 || order == 3) {               // column-major
+        const uint32_t q = divH.div((uint32_t)s);
+        const uint32_t r = (uint32_t)s - q * (uint32_t)H;
+        return (int64_t)r * W + q;
+    }
+    return s;
+}
+
 // ------------------------------------------------------------------ lane-group reduction
-// R lanes (consecutive, R a power of two) each hold R partial sums v[0..R): one
+// R lanes (R a power of two) each hold R partial sums v[0..R): one
 // per step of an R-step block.  Afterwards the lane with group index g holds the
 // sum over the R lanes of v[g].  log2(R) butterfly rounds; each round halves the
 // values a lane keeps and exchanges the other half with its partner.
-template <int R>
+// The R lanes of a group sit LSTRIDE lanes apart (lane = g * LSTRIDE + q).
+template <int R, int LSTRIDE = 1>
 __device__ __forceinline__ float transpose_reduce(float (&v)[R], int g) {
     if constexpr (R == 1) {
         return v[0];
@@ -204,7 +255,7 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[R], int g) {
             for (int i = 0; i < m; ++i) {
                 const float send = up ? v[i] : v[i + m];
                 const float keep = up ? v[i + m] : v[i];
-                v[i] = keep + __shfl_xor_sync(kFull, send, m);
+                v[i] = keep + __shfl_xor_sync(kFull, send, m * LSTRIDE);
             }
         }
         return v[0];

@@ -38,6 +38,9 @@ bool scan1d_uses_tma(const ScanArgs &a);
 // Workspace the single-direction path needs for this call (0 when it runs direct).
 size_t scan1d_workspace_bytes(const ScanArgs &a);
 
+// Workspace the bidirectional / SS2D call needs (0 when it merges on chip).
+size_t multidir_workspace_bytes(const ScanArgs &a);
+
 ss_status launch_scan1d(const ScanArgs &a);
 ss_status launch_multidir(const ScanArgs &a);
 ss_status read_device_status(ss_stream_t stream);

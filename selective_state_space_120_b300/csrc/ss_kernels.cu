@@ -85,7 +85,7 @@ struct Scan1d {
         if ((st = make_map(&mb, a.B, io, a.L, (uint64_t)a.batch * a.G * C::N, C::T, C::N))) return st;
         if ((st = make_map(&mc, a.C, io, a.L, (uint64_t)a.batch * a.G * C::N, C::T, C::N))) return st;
 
-        auto kern = k_scan1d<C>;
+        auto kern = k_scan1d<C, false>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
             return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
 
@@ -94,6 +94,15 @@ struct Scan1d {
         p.L = a.L;
         p.G = a.G;
         p.dpg = (int)(a.dim / a.G);
+        p.K = 1;
+        p.k = 0;
+        p.order = ORD_ROW;
+        p.H = 1;
+        p.W = (int)a.L;
+        p.divH = FastDiv(1);
+        p.mode = OUT_STORE;
+        p.u_g = a.u;
+        p.z_g = a.z;
         p.A = a.A;
         p.D = a.D;
         p.bias = a.bias;
@@ -134,6 +143,62 @@ struct Scan1d {
         kern<<<dim3(cblocks, bgs, J - 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
         return check_launch("scan fix-up pass");
     }
+    // K directions (bidirectional or SS2D) as K launches over one fp32
+    // accumulator by position: direction k reads its Delta_k, B_k, C_k rows in
+    // scan order and u at the positions its order visits; the first launch
+    // stores y_0 + D_0*u, the middle ones add, the last adds, gates and writes out.
+    static ss_status run_dirs(const ScanArgs &a) {
+        using namespace ssk;
+        const int io = a.io;
+        const int64_t rows = a.batch * a.dim;
+        const int K = a.K;
+        CUtensorMap mu, md, mz, mb, mc;
+        ss_status st;
+        if ((st = make_map(&mu, a.u, io, a.L, rows, C::T, C::CB))) return st;
+        if ((st = make_map(&md, a.delta, io, a.L, (uint64_t)rows * K, C::T, C::CB))) return st;
+        if ((st = make_map(&mz, a.z ? a.z : a.u, io, a.L, rows, C::T, C::CB))) return st;
+        const uint64_t bcrows = (uint64_t)a.batch * K * a.G * C::N;
+        if ((st = make_map(&mb, a.B, io, a.L, bcrows, C::T, C::N))) return st;
+        if ((st = make_map(&mc, a.C, io, a.L, bcrows, C::T, C::N))) return st;
+        auto kern = k_scan1d<C, true>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
+        Scan1dParams p{};
+        p.dim = a.dim;
+        p.L = a.L;
+        p.G = a.G;
+        p.dpg = (int)(a.dim / a.G);
+        p.Lc = a.L;
+        p.J = 1;
+        p.jbase = 0;
+        p.pass = 0;
+        p.K = K;
+        p.H = (int)a.H;
+        p.W = (int)a.W;
+        p.divH = FastDiv((uint32_t)a.H);
+        p.acc = reinterpret_cast<float *>(a.ws);
+        p.u_g = a.u;
+        p.z_g = a.z;
+        p.A = a.A;
+        p.D = a.D;
+        p.bias = a.bias;
+        p.softplus = a.softplus;
+        p.has_z = a.z != nullptr;
+        p.out = a.out;
+        p.last_state = a.last_state;
+        const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);
+        const unsigned bgs = (unsigned)(a.batch * a.G);
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(a.stream);
+        for (int k = 0; k < K; ++k) {
+            p.k = k;
+            p.order = a.orders[k];
+            p.mode = (k == 0) ? OUT_ACC_FIRST : (k == K - 1) ? OUT_ACC_LAST : OUT_ACC_ADD;
+            kern<<<dim3(cblocks, bgs, 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
+            if ((st = check_launch("direction scan"))) return st;
+        }
+        return SS_OK;
+    }
+
     // Steps per L-chunk for a requested chunk count: a multiple of the T-tile.
     static int64_t chunk_len(int64_t L, int J) {
         if (J <= 1) return L;
@@ -141,26 +206,31 @@ struct Scan1d {
     }
 };
 
-// Configuration per (I/O type, N): NPT states per lane; W warps per CTA;
-// 3-stage TMA ring.
+// Configuration per (I/O type, N): NPT states per lane, W warps per CTA, a
+// 3-stage TMA ring, CL channels per lane (CL > 1 reuses each B/C value read
+// from shared memory for several channels).
 template <typename IO, int N>
 struct Pick1d;
-template <typename IO> struct Pick1d<IO, 1> { using C = ssk::Cfg1<IO, 1, 1, 4, 3>; };
-template <typename IO> struct Pick1d<IO, 2> { using C = ssk::Cfg1<IO, 2, 2, 4, 3>; };
-template <typename IO> struct Pick1d<IO, 4> { using C = ssk::Cfg1<IO, 4, 4, 4, 3>; };
-template <typename IO> struct Pick1d<IO, 8> { using C = ssk::Cfg1<IO, 8, 4, 4, 3>; };
-template <typename IO> struct Pick1d<IO, 16> { using C = ssk::Cfg1<IO, 16, 4, 4, 3>; };
-template <typename IO> struct Pick1d<IO, 32> { using C = ssk::Cfg1<IO, 32, 4, 4, 3>; };
-template <typename IO> struct Pick1d<IO, 64> { using C = ssk::Cfg1<IO, 64, 8, 4, 3>; };
+template <typename IO> struct Pick1d<IO, 1> { using C = ssk::Cfg1<IO, 1, 1, 2, 3, 1, 1>; };
+template <typename IO> struct Pick1d<IO, 2> { using C = ssk::Cfg1<IO, 2, 2, 2, 3, 1, 1>; };
+template <typename IO> struct Pick1d<IO, 4> { using C = ssk::Cfg1<IO, 4, 4, 2, 3, 1, 1>; };
+template <typename IO> struct Pick1d<IO, 8> { using C = ssk::Cfg1<IO, 8, 4, 4, 3, 1, 1>; };
+template <typename IO> struct Pick1d<IO, 16> { using C = ssk::Cfg1<IO, 16, 4, 4, 3, 1, 1>; };
+template <typename IO> struct Pick1d<IO, 32> { using C = ssk::Cfg1<IO, 32, 4, 4, 3, 1, 1>; };
+template <typename IO> struct Pick1d<IO, 64> { using C = ssk::Cfg1<IO, 64, 8, 4, 3, 1, 1>; };
 
-// L-chunks to use: 1 (direct) when the direct path fills the GPU.
+// L-chunks to use: 1 (direct) when the direct path gives every SM sub-partition
+// at least two warps; otherwise enough chunks for about eight warps each (the
+// chunked path rescans all but the first chunk, so it only pays off when the
+// direct path would leave the sub-partitions short of warps; on the B300 the
+// 1 x 5120 x 131072 scan is fastest at 8-12 chunks).
 template <class C>
 int choose_chunks(const ScanArgs &a) {
     const int64_t rows = a.batch * a.dim;
-    const int64_t threads = rows * C::R;
-    const int64_t want = (int64_t)num_sms() * 16 * 32;  // about 16 warps per SM
-    if (threads * 2 >= want) return 1;
-    int64_t J = (want + threads - 1) / threads + 1;
+    const int64_t threads = rows * C::R / C::CL;
+    const int64_t one_per_smsp = (int64_t)num_sms() * 4 * 32;
+    if (threads >= 2 * one_per_smsp) return 1;
+    int64_t J = (8 * one_per_smsp + threads - 1) / threads;
     const int64_t maxJ = a.L / (4 * C::T);  // keep L-chunks at least 4 T-chunks long
     if (J > maxJ) J = maxJ;
     return J < 2 ? 1 : (int)J;
@@ -178,6 +248,12 @@ template <typename IO, int N>
 ss_status dispatch1d(const ScanArgs &a) {
     using C = typename Pick1d<IO, N>::C;
     return Scan1d<C>::run(a, chunks_for<IO, N>(a));
+}
+
+template <typename IO, int N>
+ss_status dispatch_dirs(const ScanArgs &a) {
+    using C = typename Pick1d<IO, N>::C;
+    return Scan1d<C>::run_dirs(a);
 }
 
 template <typename IO, int N>
@@ -236,7 +312,7 @@ template <typename IO, int K> struct PickM<IO, 1, K> { using C = ssk::CfgM<IO, 1
 template <typename IO, int K> struct PickM<IO, 2, K> { using C = ssk::CfgM<IO, 2, 1, K, (K == 4 ? 1 : 4)>; };
 template <typename IO, int K> struct PickM<IO, 4, K> { using C = ssk::CfgM<IO, 4, 2, K, (K == 4 ? 1 : 4)>; };
 template <typename IO, int K> struct PickM<IO, 8, K> { using C = ssk::CfgM<IO, 8, 2, K, (K == 4 ? 1 : 2)>; };
-template <typename IO, int K> struct PickM<IO, 16, K> { using C = ssk::CfgM<IO, 16, 2, K, (K == 4 ? 1 : 4)>; };
+template <typename IO, int K> struct PickM<IO, 16, K> { using C = ssk::CfgM<IO, 16, 2, K, (K == 4 ? 1 : 4), 16>; };
 template <typename IO, int K> struct PickM<IO, 32, K> { using C = ssk::CfgM<IO, 32, 4, K, (K == 4 ? 1 : 2)>; };
 template <typename IO, int K> struct PickM<IO, 64, K> { using C = ssk::CfgM<IO, 64, 8, K, (K == 4 ? 1 : 2)>; };
 
@@ -274,6 +350,20 @@ ss_status dispatch1d_n(const ScanArgs &a) {
     case 16: return dispatch1d<IO, 16>(a);
     case 32: return dispatch1d<IO, 32>(a);
     case 64: return dispatch1d<IO, 64>(a);
+    default: return fail(SS_ERR_UNSUPPORTED, "dstate %d is not one of 1,2,4,8,16,32,64", a.N);
+    }
+}
+
+template <typename IO>
+ss_status dispatch_dirs_n(const ScanArgs &a) {
+    switch (a.N) {
+    case 1: return dispatch_dirs<IO, 1>(a);
+    case 2: return dispatch_dirs<IO, 2>(a);
+    case 4: return dispatch_dirs<IO, 4>(a);
+    case 8: return dispatch_dirs<IO, 8>(a);
+    case 16: return dispatch_dirs<IO, 16>(a);
+    case 32: return dispatch_dirs<IO, 32>(a);
+    case 64: return dispatch_dirs<IO, 64>(a);
     default: return fail(SS_ERR_UNSUPPORTED, "dstate %d is not one of 1,2,4,8,16,32,64", a.N);
     }
 }
@@ -318,7 +408,14 @@ ss_status launch_scan1d(const ScanArgs &a) {
     return a.io == SS_BF16 ? dispatch1d_n<__nv_bfloat16>(a) : dispatch1d_n<float>(a);
 }
 
+size_t multidir_workspace_bytes(const ScanArgs &a) {
+    if (!scan1d_uses_tma(a)) return 0;  // rows not 16-byte aligned: on-chip merge path
+    return (size_t)a.batch * a.dim * a.L * sizeof(float);
+}
+
 ss_status launch_multidir(const ScanArgs &a) {
+    if (multidir_workspace_bytes(a) > 0)
+        return a.io == SS_BF16 ? dispatch_dirs_n<__nv_bfloat16>(a) : dispatch_dirs_n<float>(a);
     return a.io == SS_BF16 ? dispatch_multi<__nv_bfloat16>(a) : dispatch_multi<float>(a);
 }
 

@@ -11,10 +11,11 @@
 //
 // Design: one CTA owns CB channels of one (batch, group) and runs all K
 // directions at once, one group of WPD warps per direction.  No permuted copy of
-// the map is made: each direction reads u, Delta_k, B_k and C_k at the position
-// its traversal visits (index arithmetic on the H x W map), and adds its
-// readout y_k into an fp32 accumulator of the channel's whole map in shared
-// memory.  After the last step the CTA adds (sum_k D_k) * u, applies the gate
+// the map is made: each direction reads u at the position its traversal visits
+// (index arithmetic on the H x W map), reads its own Delta_k, B_k and C_k in its
+// scan order (as the key code's projections of the reordered sequences produce
+// them), and adds its readout y_k into an fp32 accumulator of the channel's
+// whole map in shared memory.  After the last step the CTA adds (sum_k D_k) * u, applies the gate
 // and writes the map once.  Each accumulator receives at most two addends per
 // position (K = 4 uses one accumulator for the two row-major directions and one
 // for the two column-major ones), so the sum does not depend on the order in
@@ -29,33 +30,18 @@
 
 namespace ssk {
 
-// Division by a runtime-invariant divisor through a multiply-high (Granlund and
-// Montgomery, "Division by Invariant Integers using Multiplication", 1994):
-// for 1 <= d < 2^31 and 0 <= n < 2^31, n / d = (mulhi(m, n) + n) >> l with
-// l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1.
-struct FastDiv {
-    uint32_t d, m, l;
-    __host__ __device__ FastDiv() : d(1), m(1), l(0) {}
-    __host__ explicit FastDiv(uint32_t dv) : d(dv) {
-        l = 0;
-        while ((1ull << l) < dv) ++l;
-        m = (uint32_t)((((1ull << l) - dv) << 32) / dv + 1);
-    }
-    __device__ __forceinline__ uint32_t div(uint32_t n) const {
-        return (uint32_t)(((uint64_t)__umulhi(m, n) + n) >> l);
-    }
-};
-
-template <typename IO_, int N_, int NPT_, int K_, int WPD_>
+template <typename IO_, int N_, int NPT_, int K_, int WPD_, int T_ = 32>
 struct CfgM {
     using IO = IO_;
     static constexpr int N = N_, NPT = NPT_, K = K_, WPD = WPD_;
     static constexpr int R = N / NPT;
     static constexpr int CPW = 32 / R;
+    static constexpr int CL = 1;                // channels per lane (scan_chunk_pipe)
+    static constexpr bool BCW = false;          // B/C staged as fp32 pairs
     static constexpr int CB = WPD * CPW;        // channels per CTA
     static constexpr int DT = 32 * WPD;         // threads per direction
     static constexpr int THREADS = K * DT;
-    static constexpr int T = 16;                // steps per chunk
+    static constexpr int T = T_;                // steps per chunk
     static constexpr int TP = T / 2;
     static constexpr int E = T / R;             // steps gathered and prepped by one lane
     static constexpr int NACC = (K == 4) ? 2 : 1;
@@ -86,17 +72,6 @@ struct MultiParams {
     float *last_state;
 };
 
-__device__ __forceinline__ int64_t position_of(int order, int64_t s, int64_t L, int H, int W,
-                                               const FastDiv &divH) {
-    if (order == 2 || order == 3) s = L - 1 - s;  // reversed orders
-    if (order == 1 || order == 3) {               // column-major
-        const uint32_t q = divH.div((uint32_t)s);
-        const uint32_t r = (uint32_t)s - q * (uint32_t)H;
-        return (int64_t)r * W + q;
-    }
-    return s;
-}
-
 template <class C>
 __global__ void __launch_bounds__(C::THREADS) k_multidir(const MultiParams p) {
     using IO = typename C::IO;
@@ -106,7 +81,7 @@ __global__ void __launch_bounds__(C::THREADS) k_multidir(const MultiParams p) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int k = warp / C::WPD;                  // direction of this warp
     const int td = tid - k * C::DT;               // thread index within the direction
-    const int c = lane / R, g = lane % R;
+    const int c = lane % C::CPW, g = lane / C::CPW;  // slice-major lanes
     const int ch = (warp % C::WPD) * C::CPW + c;  // channel within the CTA
     const int cblk = blockIdx.x;
     const int bg = blockIdx.y;
@@ -125,13 +100,13 @@ __global__ void __launch_bounds__(C::THREADS) k_multidir(const MultiParams p) {
     const IO *Bk = reinterpret_cast<const IO *>(p.B) + (((int64_t)b * K + k) * p.G + grp) * N * L;
     const IO *Ck = reinterpret_cast<const IO *>(p.C) + (((int64_t)b * K + k) * p.G + grp) * N * L;
 
-    float2 A2p[NPT];
-    float h[NPT];
+    float2 A2p[1][NPT];
+    float h[1][NPT];
 #pragma unroll
     for (int j = 0; j < NPT; ++j) {
         const float a = __ldg(p.A + ((int64_t)k * p.dim + d) * N + g * NPT + j) * kLog2e;
-        A2p[j] = make_float2(a, a);
-        h[j] = 0.f;
+        A2p[0][j] = make_float2(a, a);
+        h[0][j] = 0.f;
     }
     const float bk = p.bias ? __ldg(p.bias + (int64_t)k * p.dim + d) : 0.f;
 
@@ -158,7 +133,7 @@ __global__ void __launch_bounds__(C::THREADS) k_multidir(const MultiParams p) {
             if (s < L) {
                 const int64_t pos = position_of(order, s, L, p.H, p.W, p.divH);
                 ru[e] = IOT<IO>::load(u_row + pos);
-                rd[e] = IOT<IO>::load(dl_row + pos);
+                rd[e] = IOT<IO>::load(dl_row + s);
             } else {
                 ru[e] = 0.f;
                 rd[e] = 0.f;
@@ -173,10 +148,7 @@ __global__ void __launch_bounds__(C::THREADS) k_multidir(const MultiParams p) {
             const int isC = rest / N;
             const int64_t s = (int64_t)i * T + e;
             float v = 0.f;
-            if (vi < C::NBC && s < L) {
-                const int64_t pos = position_of(order, s, L, p.H, p.W, p.divH);
-                v = IOT<IO>::load((isC ? Ck : Bk) + (int64_t)n * L + pos);
-            }
+            if (vi < C::NBC && s < L) v = IOT<IO>::load((isC ? Ck : Bk) + (int64_t)n * L + s);
             rbc[m] = v;
         }
     };
@@ -212,7 +184,8 @@ __global__ void __launch_bounds__(C::THREADS) k_multidir(const MultiParams p) {
         if (i + 1 < nchunks) fetch(i + 1);
         __syncthreads();
 
-        scan_chunk<C, true>(dxrow, bc, g, h, A2p, [&](float y, int t) {
+        const float4 *const dxrows[1] = {dxrow};
+        scan_chunk_pipe<C, true>(dxrows, bc, g, h, A2p, [&](int, float y, int t) {
             const int64_t s = (int64_t)i * T + t;
             if (s < L) {
                 const int64_t pos = position_of(order, s, L, p.H, p.W, p.divH);
@@ -252,7 +225,7 @@ __global__ void __launch_bounds__(C::THREADS) k_multidir(const MultiParams p) {
     if (valid && p.last_state) {
 #pragma unroll
         for (int j = 0; j < NPT; ++j)
-            p.last_state[(((int64_t)b * K + k) * p.dim + d) * N + g * NPT + j] = h[j];
+            p.last_state[(((int64_t)b * K + k) * p.dim + d) * N + g * NPT + j] = h[0][j];
     }
 }
 

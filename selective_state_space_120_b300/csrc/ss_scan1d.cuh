@@ -1,27 +1,39 @@
 // Single-direction selective scan, TMA-staged (sm_103a).
 //
 // Work split: a CTA owns CB consecutive channels of one (batch, group) and
-// walks the sequence in chunks of T steps.  Inside a warp, lane = c*R + g:
-// channel c of the warp, and state slice g holding NPT of the N states.  The
-// fp32 states stay in registers for the whole sequence; Abar and Bbar are
-// formed on the fly and never stored (the "do not materialise Abar, Bbar"
-// point of the hardware-aware scan: "Mamba Series ..." review, core insight 1,
-// and the Mamba reading notes, section 3.3.2).
+// walks the sequence in chunks of T steps.  Inside a warp, lane = g*CPW + q:
+// state slice g (NPT of the N states) of channel group q (CL consecutive
+// channels).  Slice-major lanes put eight lanes that read the same B/C words
+// in each quarter-warp, which halves the shared-memory wavefronts of the
+// 16-byte B/C loads (the hardware serves a 16-byte load per quarter-warp and
+// broadcasts a single address within it).  The fp32 states stay
+// in registers for the whole sequence; Abar and Bbar are formed on the fly and
+// never stored (the "do not materialise Abar, Bbar" point of the
+// hardware-aware scan: "Mamba Series ..." review, core insight 1, and the
+// Mamba reading notes, section 3.3.2).
 //
-// Per chunk:
+// Why CL channels per lane: B and C are shared by every channel of a group,
+// and shared memory delivers at most 128 bytes of lane data per clock per SM.
+// A lane that reads its NPT states' B/C once and uses them for CL channels
+// divides that traffic by CL, which is what bounds this kernel otherwise.
+//
+// Per chunk i (the prep of chunk i+1 runs in the same barrier interval as the
+// scan of chunk i, so the two independent instruction streams interleave):
 //   1. TMA (64-byte rows, 64B swizzle) has landed the u, Delta, z tiles
-//      [CB x T] and the B, C tiles [N x T] of this chunk in a STAGES-deep ring.
-//   2. All threads convert B and C to fp32 in a pair-interleaved layout
-//      (B[t], B[t+1]) so a lane reads its NPT states' inputs for two steps with
-//      vector loads; every lane "preps" its own E steps of its channel:
-//      Delta' = softplus(Delta + bias), x = Delta'*u, gate = SiLU(z), D*u*gate.
-//   3. Barrier; thread 0 refills the ring slot just consumed.
-//   4. Each warp scans its channels: per step pair and state n,
+//      [CB x T] and the B, C tiles [N x T] of chunk i+1 in a STAGES-deep ring.
+//   2. All threads convert chunk i+1's B and C to fp32 in a pair-interleaved
+//      layout (B[t], B[t+1]) so a lane reads its NPT states' inputs for two
+//      steps with vector loads; each thread "preps" E consecutive steps of one
+//      channel: Delta' = softplus(Delta + bias), x = Delta'*u, gate = SiLU(z),
+//      D*u*gate -- into the other half of double-buffered rows.
+//   3. Each warp scans chunk i for its channels: per step pair, state n and
+//      channel c,
 //         (a_t, a_t+1) = ex2(Delta' * A*log2e)   h = a*h + x*B   y += C*h
 //      with packed f32x2 multiplies over the two steps.  Every R steps the R
 //      partial readouts of a channel are combined by a butterfly so that lane g
 //      ends with the full y of step g, applies y*gate + D*u*gate and stages it.
-//   5. The warp writes its staged outputs with 16-byte coalesced stores.
+//   4. The warp writes its staged outputs with 16-byte coalesced stores.
+//   5. Barrier; thread 0 refills the ring slot of chunk i+1.
 //
 // The same kernel runs the long-sequence chunked path: pass 1 scans L-chunks
 // from a zero state and records each chunk's end state and sum of Delta';
@@ -32,20 +44,28 @@
 
 namespace ssk {
 
-template <typename IO_, int N_, int NPT_, int W_, int STAGES_>
+template <typename IO_, int N_, int NPT_, int W_, int STAGES_, int CL_ = 1, int PIPE_ = 0,
+          int OVL_ = 0>
 struct Cfg1 {
     using IO = IO_;
-    static constexpr int N = N_, NPT = NPT_, W = W_, STAGES = STAGES_;
-    static constexpr int R = N / NPT;    // lanes sharing one channel
-    static constexpr int CPW = 32 / R;   // channels per warp
-    static constexpr int CB = W * CPW;   // channels per CTA
+    static constexpr int N = N_, NPT = NPT_, W = W_, STAGES = STAGES_, CL = CL_;
+    static constexpr bool PIPE = PIPE_ != 0;  // software-pipelined step loop
+    // OVL: the prep of chunk i+1 shares a barrier interval with the scan of
+    // chunk i (double-buffered prep rows); otherwise prep, barrier, scan.
+    static constexpr bool OVL = OVL_ != 0;
+    static constexpr int R = N / NPT;    // lanes sharing one channel group
+    static constexpr int CPW = 32 / R;   // channel groups per warp
+    static constexpr int CHW = CPW * CL; // channels per warp
+    static constexpr int CB = W * CHW;   // channels per CTA
     static constexpr int THREADS = 32 * W;
     static constexpr int ES = sizeof(IO);
     static constexpr int T = 64 / ES;    // steps per chunk (raw rows are 64 bytes)
     static constexpr int TP = T / 2;     // step pairs per chunk
-    static constexpr int E = T / R;      // consecutive steps prepped by one lane
+    static constexpr int PT = R / CL;    // prep threads per channel
+    static constexpr int E = T / PT;     // consecutive steps prepped by one thread
     static_assert(N % NPT == 0 && R >= 1 && R <= 32 && (R & (R - 1)) == 0, "lane split");
-    static_assert(E >= 2 && E % 2 == 0 && E * ES >= 4, "a prep lane owns whole step pairs");
+    static_assert(CL >= 1 && CL <= R && R % CL == 0, "channels per lane");
+    static_assert(E >= 2 && E % 2 == 0 && E * ES >= 4, "a prep thread owns whole step pairs");
     static_assert(CB <= 256 && N <= 256, "TMA box rows");
 
     static constexpr int al(int x) { return (x + 1023) & ~1023; }
@@ -54,16 +74,33 @@ struct Cfg1 {
     static constexpr int STAGE = 3 * TILE_CH + 2 * TILE_BC;
     static constexpr int OFF_U = 0, OFF_DL = TILE_CH, OFF_Z = 2 * TILE_CH;
     static constexpr int OFF_B = 3 * TILE_CH, OFF_C = 3 * TILE_CH + TILE_BC;
-    static constexpr int BCBUF = TP * 4 * N * 4;  // fp32 B/C of one chunk
+    // BCW: keep B/C as bf16 pairs (B[t], B[t+1]) in one 32-bit word (exact for
+    // bf16 inputs), halving the shared-memory bytes each lane reads at the cost
+    // of two integer ops per word to widen them.  Measured slower on the B300
+    // for N = 16 (the step loop is issue-bound, not shared-memory-bound), so off.
+    static constexpr bool BCW = false;
+    static constexpr int BCBUF = TP * (BCW ? 2 : 4) * N * 4;  // B/C of one chunk
+    static_assert(!BCW || PIPE, "packed B/C words are read by the pipelined step loop");
     static constexpr int OFF_BC = STAGES * STAGE;
     static constexpr int DXROW = (TP + 1) * 16;  // one padding slot per row
+    static constexpr int PREPBUF = 2 * CB * DXROW;  // dx and gd rows of one chunk
+    static constexpr int NPREP = OVL ? 2 : 1;      // prep row buffers
     static constexpr int OFF_DX = OFF_BC + 2 * BCBUF;
     static constexpr int OFF_GD = OFF_DX + CB * DXROW;
-    static constexpr int OBROW = T * ES + 16;
-    static constexpr int OFF_OB = OFF_GD + CB * DXROW;
+    static constexpr int OBROW = T * 4 + 16;  // staged outputs (I/O type, or fp32 partials)
+    static constexpr int OFF_OB = OFF_DX + NPREP * PREPBUF;
     static constexpr int OFF_BAR = (OFF_OB + CB * OBROW + 7) & ~7;
     static constexpr int SMEM = OFF_BAR + 8 * STAGES + 1024;  // + alignment slack
+    static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
 };
+
+// Output modes of one launch.  A single-direction scan stores its gated output
+// (OUT_STORE).  A K-direction scan runs K launches in direction order over one
+// fp32 accumulator of y_k + D_k*u by position: the first stores it, the middle
+// ones add to it, and the last adds its own term, applies the gate and writes
+// the I/O-typed output.  Each position receives its terms in launch order, so
+// the merged result is deterministic.
+enum { OUT_STORE = 0, OUT_ACC_FIRST = 1, OUT_ACC_ADD = 2, OUT_ACC_LAST = 3 };
 
 struct Scan1dParams {
     int64_t dim, L;
@@ -72,20 +109,46 @@ struct Scan1dParams {
     int J;        // number of L-chunks
     int jbase;    // L-chunk index of blockIdx.z == 0
     int pass;     // 0 direct, 1 chunk-local pass, 2 chunk fix-up pass
+    int K, k;     // directions of the call, and the one this launch scans
+    int order;    // traversal of direction k (0 row, 1 column, 2, 3 reversed)
+    int H, W;     // map of the column orders (a plain sequence: H = 1, W = L)
+    FastDiv divH;
+    int mode;     // OUT_*
+    float *acc;   // [batch*dim, L] fp32 merge accumulator by position (modes 1-3)
+    const void *u_g, *z_g;  // u and z for the gathers of the column orders
     const float *A, *D, *bias;
     int softplus, has_z;
     void *out;
-    float *last_state;
+    float *last_state;      // [batch, K, dim, N]
     float *hend;          // [rows, J, N] end state of an L-chunk scanned from zero
     float *sdt;           // [rows, J]    sum of Delta' over an L-chunk
     const float *carry;   // [rows, J, N] state entering an L-chunk
 };
 
-// B/C tiles -> fp32, layout per step pair tp: [B: N pairs (t, t+1)][C: N pairs].
+// B/C tiles -> per step pair tp: [B: N pairs (t, t+1)][C: N pairs], as fp32
+// pairs, or (C::BCW) as bf16 pairs packed in one 32-bit word -- which is
+// exactly the word the tile holds at columns (t, t+1), so it is only moved.
 template <class C>
 __device__ __forceinline__ void convert_bc(const uint8_t *tB, const uint8_t *tC, float *bc, int tid) {
     using IO = typename C::IO;
     constexpr int VPC = 16 / C::ES;  // values per 16-byte chunk
+    if constexpr (C::BCW) {
+        uint32_t *bw = reinterpret_cast<uint32_t *>(bc);
+#pragma unroll 1
+        for (int task = tid; task < 8 * C::N; task += C::THREADS) {
+            const int n = task % C::N;
+            const int isC = (task / C::N) & 1;
+            const int q = task / (2 * C::N);  // 16-byte chunk of the 64-byte row
+            const uint4 w = *reinterpret_cast<const uint4 *>((isC ? tC : tB) + swz64(n * 64 + q * 16));
+            const int tp0 = q * 4;            // four step pairs per 16 bytes
+            uint32_t *dst = bw + tp0 * 2 * C::N + isC * C::N + n;
+            dst[0] = w.x;
+            dst[2 * C::N] = w.y;
+            dst[4 * C::N] = w.z;
+            dst[6 * C::N] = w.w;
+        }
+        return;
+    }
 #pragma unroll 1
     for (int task = tid; task < 8 * C::N; task += C::THREADS) {
         const int n = task % C::N;
@@ -169,55 +232,422 @@ __device__ __forceinline__ void scan_chunk(const float4 *dxrow, const float *bc,
     }
 }
 
+// Scans one chunk of T steps for this lane's CL channels and state slice.
+// DO_Y selects the readout (off in the chunk-local pass, which only needs the
+// end states).  `emit(c, y, t)` receives the full readout y of channel c of the
+// lane's group at local step t (one lane per step).
+template <class C, bool DO_Y, class Emit>
+__device__ __forceinline__ void scan_chunk_cl(const float4 *const (&dxrow)[C::CL], const float *bc,
+                                              int g, float (&h)[C::CL][C::NPT],
+                                              const float2 (&A2p)[C::CL][C::NPT], Emit &&emit) {
+    constexpr int R = C::R, NPT = C::NPT, N = C::N, CL = C::CL;
+    constexpr int BS = R >= 2 ? R : 2;  // steps per readout block
+    constexpr int PPB = BS / 2;
+#pragma unroll
+    for (int blk = 0; blk < C::T / BS; ++blk) {
+        float v[CL][BS];
+#pragma unroll
+        for (int pp = 0; pp < PPB; ++pp) {
+            const int tp = blk * PPB + pp;
+            const float *bB = bc + tp * 4 * N + 2 * NPT * g;
+            const float *bC = bB + 2 * N;
+            float Bv[2 * NPT], Cv[2 * NPT];
+            if constexpr (NPT == 1) {
+                const float2 b2 = *reinterpret_cast<const float2 *>(bB);
+                Bv[0] = b2.x; Bv[1] = b2.y;
+                if constexpr (DO_Y) {
+                    const float2 c2 = *reinterpret_cast<const float2 *>(bC);
+                    Cv[0] = c2.x; Cv[1] = c2.y;
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < NPT / 2; ++k) {
+                    const float4 b4 = reinterpret_cast<const float4 *>(bB)[k];
+                    Bv[4 * k] = b4.x; Bv[4 * k + 1] = b4.y; Bv[4 * k + 2] = b4.z; Bv[4 * k + 3] = b4.w;
+                    if constexpr (DO_Y) {
+                        const float4 c4 = reinterpret_cast<const float4 *>(bC)[k];
+                        Cv[4 * k] = c4.x; Cv[4 * k + 1] = c4.y; Cv[4 * k + 2] = c4.z; Cv[4 * k + 3] = c4.w;
+                    }
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < CL; ++c) {
+                const float4 d4 = dxrow[c][swz_slot(tp)];
+                const float2 dl = make_float2(d4.x, d4.y);
+                const float2 xx = make_float2(d4.z, d4.w);
+                float2 y2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < NPT; ++j) {
+                    const float2 da = __fmul2_rn(dl, A2p[c][j]);
+                    const float a0 = ex2(da.x), a1 = ex2(da.y);
+                    const float2 bx = __fmul2_rn(xx, make_float2(Bv[2 * j], Bv[2 * j + 1]));
+                    const float h0 = fmaf(a0, h[c][j], bx.x);
+                    const float h1 = fmaf(a1, h0, bx.y);
+                    h[c][j] = h1;
+                    if constexpr (DO_Y)
+                        y2 = __ffma2_rn(make_float2(Cv[2 * j], Cv[2 * j + 1]), make_float2(h0, h1), y2);
+                }
+                v[c][2 * pp] = y2.x;
+                v[c][2 * pp + 1] = y2.y;
+            }
+        }
+        if constexpr (DO_Y) {
+#pragma unroll
+            for (int c = 0; c < CL; ++c) {
+                if constexpr (R >= 2) {
+                    const float y = transpose_reduce<R, C::CPW>(v[c], g);
+                    emit(c, y, blk * R + g);
+                } else {
+                    emit(c, v[c][0], blk * 2);
+                    emit(c, v[c][1], blk * 2 + 1);
+                }
+            }
+        }
+    }
+}
+
+// Registers of one step pair of scan_chunk_pipe: the exponentials, the input
+// terms x*B and the readout weights C for the lane's channels and states.
 template <class C>
+struct StepRegs {
+    float a[C::CL][C::NPT][2];
+    float2 bx[C::CL][C::NPT];
+    float Cv[2 * C::NPT];
+};
+
+// Loads and evaluates everything of step pair tp that does not depend on the
+// state: smem loads, Delta'*A, ex2, x*B.
+template <class C, bool DO_Y>
+__device__ __forceinline__ void stage_step(StepRegs<C> &r, const float4 *const (&dxrow)[C::CL],
+                                           const float *bc, int g, int tp,
+                                           const float2 (&A2p)[C::CL][C::NPT]) {
+    constexpr int NPT = C::NPT, N = C::N, CL = C::CL;
+    float Bv[2 * NPT];
+    if constexpr (C::BCW) {
+        // bf16 pairs: low half step t, high half step t+1
+        const uint32_t *wB = reinterpret_cast<const uint32_t *>(bc) + tp * 2 * N + NPT * g;
+        const uint32_t *wC = wB + N;
+        uint32_t bw[NPT], cw[NPT];
+        if constexpr (NPT % 4 == 0) {
+#pragma unroll
+            for (int k = 0; k < NPT / 4; ++k) {
+                const uint4 b4 = reinterpret_cast<const uint4 *>(wB)[k];
+                bw[4 * k] = b4.x; bw[4 * k + 1] = b4.y; bw[4 * k + 2] = b4.z; bw[4 * k + 3] = b4.w;
+                if constexpr (DO_Y) {
+                    const uint4 c4 = reinterpret_cast<const uint4 *>(wC)[k];
+                    cw[4 * k] = c4.x; cw[4 * k + 1] = c4.y; cw[4 * k + 2] = c4.z; cw[4 * k + 3] = c4.w;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) {
+                bw[j] = wB[j];
+                if constexpr (DO_Y) cw[j] = wC[j];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) {
+            Bv[2 * j] = __uint_as_float(bw[j] << 16);
+            Bv[2 * j + 1] = __uint_as_float(bw[j] & 0xffff0000u);
+            if constexpr (DO_Y) {
+                r.Cv[2 * j] = __uint_as_float(cw[j] << 16);
+                r.Cv[2 * j + 1] = __uint_as_float(cw[j] & 0xffff0000u);
+            }
+        }
+    } else {
+    const float *bB = bc + tp * 4 * N + 2 * NPT * g;
+    const float *bC = bB + 2 * N;
+    if constexpr (NPT == 1) {
+        const float2 b2 = *reinterpret_cast<const float2 *>(bB);
+        Bv[0] = b2.x; Bv[1] = b2.y;
+        if constexpr (DO_Y) {
+            const float2 c2 = *reinterpret_cast<const float2 *>(bC);
+            r.Cv[0] = c2.x; r.Cv[1] = c2.y;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < NPT / 2; ++k) {
+            const float4 b4 = reinterpret_cast<const float4 *>(bB)[k];
+            Bv[4 * k] = b4.x; Bv[4 * k + 1] = b4.y; Bv[4 * k + 2] = b4.z; Bv[4 * k + 3] = b4.w;
+            if constexpr (DO_Y) {
+                const float4 c4 = reinterpret_cast<const float4 *>(bC)[k];
+                r.Cv[4 * k] = c4.x; r.Cv[4 * k + 1] = c4.y; r.Cv[4 * k + 2] = c4.z; r.Cv[4 * k + 3] = c4.w;
+            }
+        }
+    }
+    }
+#pragma unroll
+    for (int c = 0; c < CL; ++c) {
+        const float4 d4 = dxrow[c][swz_slot(tp)];
+        const float2 dl = make_float2(d4.x, d4.y);
+        const float2 xx = make_float2(d4.z, d4.w);
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) {
+            const float2 da = __fmul2_rn(dl, A2p[c][j]);
+            r.a[c][j][0] = ex2(da.x);
+            r.a[c][j][1] = ex2(da.y);
+            r.bx[c][j] = __fmul2_rn(xx, make_float2(Bv[2 * j], Bv[2 * j + 1]));
+        }
+    }
+}
+
+// scan_chunk_cl with a one-step-pair software pipeline: the loads and
+// exponentials of step pair tp+1 are issued before the state updates of tp, so
+// their latency overlaps the dependent FMA chain.
+template <class C, bool DO_Y, class Emit>
+__device__ __forceinline__ void scan_chunk_pipe(const float4 *const (&dxrow)[C::CL], const float *bc,
+                                                int g, float (&h)[C::CL][C::NPT],
+                                                const float2 (&A2p)[C::CL][C::NPT], Emit &&emit) {
+    constexpr int R = C::R, NPT = C::NPT, CL = C::CL;
+    constexpr int BS = R >= 2 ? R : 2;  // steps per readout block
+    constexpr int PPB = BS / 2;
+    StepRegs<C> cur, nxt;
+    stage_step<C, DO_Y>(nxt, dxrow, bc, g, 0, A2p);
+    float v[CL][BS];
+#pragma unroll
+    for (int tp = 0; tp < C::TP; ++tp) {
+        cur = nxt;
+        if (tp + 1 < C::TP) stage_step<C, DO_Y>(nxt, dxrow, bc, g, tp + 1, A2p);
+        const int pp = tp % PPB;
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+            // two readout accumulators halve the dependent FMA chain
+            float2 y2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) {
+                const float h0 = fmaf(cur.a[c][j][0], h[c][j], cur.bx[c][j].x);
+                const float h1 = fmaf(cur.a[c][j][1], h0, cur.bx[c][j].y);
+                h[c][j] = h1;
+                if constexpr (DO_Y)
+                    y2[j & 1] = __ffma2_rn(make_float2(cur.Cv[2 * j], cur.Cv[2 * j + 1]),
+                                           make_float2(h0, h1), y2[j & 1]);
+            }
+            if constexpr (NPT > 1) y2[0] = __fadd2_rn(y2[0], y2[1]);
+            v[c][2 * pp] = y2[0].x;
+            v[c][2 * pp + 1] = y2[0].y;
+        }
+        if constexpr (DO_Y) {
+            if (pp == PPB - 1) {
+                const int blk = tp / PPB;
+#pragma unroll
+                for (int c = 0; c < CL; ++c) {
+                    if constexpr (R >= 2) {
+                        const float y = transpose_reduce<R, C::CPW>(v[c], g);
+                        emit(c, y, blk * R + g);
+                    } else {
+                        emit(c, v[c][0], blk * 2);
+                        emit(c, v[c][1], blk * 2 + 1);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Epilogue of the merge modes for one chunk (steps s0 .. s0+T-1 of direction
+// k): the warp's staged fp32 partials y_k + D_k*u go to the accumulator at the
+// positions the steps visit (stored, added, or -- for the last direction --
+// added, gated by SiLU(z) and written to out in the I/O type).  Each lane owns
+// TPL tasks of four steps: a row order maps them to four consecutive positions
+// (ascending or descending), one 16-byte access; the column orders scatter.
+// MergeRegs holds what a task reads from global memory (the accumulator and z),
+// loaded one chunk early by load_partials so the latency hides behind the scan.
+template <class C>
+struct MergeRegs {
+    static constexpr int QG = C::T / 4;  // groups of four steps per chunk
+    static constexpr int TPL = (C::CHW * QG + 31) / 32;
+    float4 acc[TPL];
+    typename IOT<typename C::IO>::Raw z[TPL][4];
+};
+
+template <class C>
+__device__ __forceinline__ bool merge_task(const Scan1dParams &p, int warp, int lane, int cblk, int64_t s0,
+                                           int m, int &chr, int &dgr, int64_t &sg) {
+    constexpr int QG = MergeRegs<C>::QG;
+    const int task = lane + 32 * m;
+    if (task >= C::CHW * QG) return false;
+    const int rr = task / QG, qq = task % QG;
+    chr = warp * C::CHW + rr;
+    dgr = cblk * C::CB + chr;
+    sg = s0 + qq * 4;
+    return dgr < p.dpg && sg < p.L;
+}
+
+template <class C>
+__device__ __forceinline__ void load_partials(const Scan1dParams &p, MergeRegs<C> &mr, int warp, int lane,
+                                              int cblk, int64_t row0, int64_t s0) {
+    using IO = typename C::IO;
+    if (p.mode == OUT_ACC_FIRST) return;
+#pragma unroll
+    for (int m = 0; m < MergeRegs<C>::TPL; ++m) {
+        int chr, dgr;
+        int64_t sg;
+        if (!merge_task<C>(p, warp, lane, cblk, s0, m, chr, dgr, sg)) continue;
+        const int64_t row = row0 + dgr;
+        const float *accr = p.acc + row * p.L;
+        const IO *zr = reinterpret_cast<const IO *>(p.z_g) + row * p.L;
+        const bool gate = p.mode == OUT_ACC_LAST && p.has_z;
+        if (p.order == 0 || p.order == 2) {
+            const int64_t pos0 = (p.order == 2) ? p.L - 4 - sg : sg;
+            mr.acc[m] = *reinterpret_cast<const float4 *>(accr + pos0);
+            if (gate) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) mr.z[m][j] = IOT<IO>::load_raw(zr + pos0 + j);
+            }
+        } else {
+            float a[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t pos = position_of(p.order, sg + j, p.L, p.H, p.W, p.divH);
+                a[j] = accr[pos];
+                if (gate) mr.z[m][j] = IOT<IO>::load_raw(zr + pos);
+            }
+            mr.acc[m] = make_float4(a[0], a[1], a[2], a[3]);
+        }
+    }
+}
+
+template <class C>
+__device__ __forceinline__ void store_partials(const Scan1dParams &p, const MergeRegs<C> &mr,
+                                               const uint8_t *smem, int warp, int lane, int cblk,
+                                               int64_t row0, int64_t s0) {
+    using IO = typename C::IO;
+#pragma unroll
+    for (int m = 0; m < MergeRegs<C>::TPL; ++m) {
+        int chr, dgr;
+        int64_t sg;
+        if (!merge_task<C>(p, warp, lane, cblk, s0, m, chr, dgr, sg)) continue;
+        const int qq = (int)((sg - s0) / 4);
+        const float4 v = *reinterpret_cast<const float4 *>(smem + C::OFF_OB + chr * C::OBROW + qq * 16);
+        const int64_t row = row0 + dgr;
+        float *accr = p.acc + row * p.L;
+        IO *outr = reinterpret_cast<IO *>(p.out) + row * p.L;
+        const bool gate = p.mode == OUT_ACC_LAST && p.has_z;
+        // w[j] is the term of step sg + j; a row order reversed reads back to front
+        float w[4] = {v.x, v.y, v.z, v.w};
+        if (p.mode != OUT_ACC_FIRST) {
+            // the prefetched accumulator is in position order for the row orders
+            const float4 o = mr.acc[m];
+            if (p.order == 2) {
+                w[0] += o.w; w[1] += o.z; w[2] += o.y; w[3] += o.x;
+            } else {
+                w[0] += o.x; w[1] += o.y; w[2] += o.z; w[3] += o.w;
+            }
+        }
+        if (gate) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int jz = (p.order == 2) ? 3 - j : j;  // z prefetched in position order
+                w[j] *= silu(IOT<IO>::widen(mr.z[m][jz]));
+            }
+        }
+        if (p.order == 0 || p.order == 2) {
+            const bool rev = p.order == 2;
+            const int64_t pos0 = rev ? p.L - 4 - sg : sg;
+            float q[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) q[j] = rev ? w[3 - j] : w[j];  // position order
+            if (p.mode != OUT_ACC_LAST) {
+                *reinterpret_cast<float4 *>(accr + pos0) = make_float4(q[0], q[1], q[2], q[3]);
+            } else if constexpr (sizeof(IO) == 2) {
+                uint2 packed;
+                packed.x = pack_bf16x2(q[0], q[1]);
+                packed.y = pack_bf16x2(q[2], q[3]);
+                *reinterpret_cast<uint2 *>(outr + pos0) = packed;
+            } else {
+                *reinterpret_cast<float4 *>(outr + pos0) = make_float4(q[0], q[1], q[2], q[3]);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t pos = position_of(p.order, sg + j, p.L, p.H, p.W, p.divH);
+                if (p.mode != OUT_ACC_LAST) accr[pos] = w[j];
+                else outr[pos] = IOT<IO>::from_f(w[j]);
+            }
+        }
+    }
+}
+
+// MULTI = false: a single-direction scan (order 0, OUT_STORE, one direction),
+// with those fields fixed at compile time; MULTI = true: one direction of a
+// multi-direction call, as the params say.
+template <class C, bool MULTI>
 __global__ void __launch_bounds__(C::THREADS)
 k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
          const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
-         const __grid_constant__ CUtensorMap tm_C, const Scan1dParams p) {
+         const __grid_constant__ CUtensorMap tm_C, const Scan1dParams p_in) {
     using IO = typename C::IO;
-    constexpr int N = C::N, NPT = C::NPT, R = C::R, T = C::T, E = C::E;
+    Scan1dParams p = p_in;
+    if constexpr (!MULTI) {
+        p.K = 1;
+        p.k = 0;
+        p.order = 0;
+        p.mode = OUT_STORE;
+    }
+    constexpr int N = C::N, NPT = C::NPT, T = C::T, E = C::E, CL = C::CL;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = lane / R, g = lane % R;
+    const int q = lane % C::CPW, g = lane / C::CPW;
     const int cblk = blockIdx.x;
     const int bg = blockIdx.y;
     const int b = bg / p.G, grp = bg % p.G;
     const int jc = p.jbase + blockIdx.z;
-    const int ch = warp * C::CPW + c;
-    const int dg = cblk * C::CB + ch;
-    const bool valid = dg < p.dpg;
-    const int d = grp * p.dpg + (valid ? dg : p.dpg - 1);
-    const int64_t row = (int64_t)b * p.dim + d;
-    const int row_tma = (int)((int64_t)b * p.dim + (int64_t)grp * p.dpg + (int64_t)cblk * C::CB);
-    const int bcrow_tma = bg * N;
+    const int64_t row0 = (int64_t)b * p.dim + (int64_t)grp * p.dpg;  // row of the group's channel 0
+    const int row_tma = (int)(row0 + (int64_t)cblk * C::CB);          // u, z, out rows
+    // Delta rows of direction k: [batch, K, dim]; B/C rows: [batch, K, G, N]
+    const int dlrow_tma = (int)(((int64_t)b * p.K + p.k) * p.dim + (int64_t)grp * p.dpg +
+                                (int64_t)cblk * C::CB);
+    const int bcrow_tma = (int)((((int64_t)b * p.K + p.k) * p.G + grp) * N);
+    const bool u_tiled = (p.order == 0 || p.order == 2);  // u (and z) arrive as tiles
+    const bool gate_in_prep = (p.mode == OUT_STORE) && p.has_z;
     const int64_t t_begin = (int64_t)jc * p.Lc;
     const int64_t t_end = min(p.L, t_begin + p.Lc);
     const int nchunks = (int)((t_end - t_begin + T - 1) / T);
     const bool do_y = (p.pass != 1) || (jc == 0);
 
-    float2 A2p[NPT];
-    float h[NPT];
+    // scan role: channels ch[c] (within the CTA) of this lane's group
+    int chs[CL];
+    bool valid[CL];
+    int64_t rows[CL];
+    float2 A2p[CL][NPT];
+    float h[CL][NPT];
 #pragma unroll
-    for (int j = 0; j < NPT; ++j) {
-        const int n = g * NPT + j;
-        const float a = __ldg(p.A + (int64_t)d * N + n) * kLog2e;
-        A2p[j] = make_float2(a, a);
-        h[j] = (p.pass == 2) ? __ldg(p.carry + (row * p.J + jc) * N + n) : 0.f;
+    for (int c = 0; c < CL; ++c) {
+        chs[c] = warp * C::CHW + q * CL + c;
+        const int dg = cblk * C::CB + chs[c];
+        valid[c] = dg < p.dpg;
+        const int64_t d = (int64_t)grp * p.dpg + (valid[c] ? dg : p.dpg - 1);
+        rows[c] = (int64_t)b * p.dim + d;
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) {
+            const int n = g * NPT + j;
+            const float a = __ldg(p.A + ((int64_t)p.k * p.dim + d) * N + n) * kLog2e;
+            A2p[c][j] = make_float2(a, a);
+            h[c][j] = (p.pass == 2) ? __ldg(p.carry + (rows[c] * p.J + jc) * N + n) : 0.f;
+        }
     }
-    const float Dd = p.D ? __ldg(p.D + d) : 0.f;
-    const float bd = p.bias ? __ldg(p.bias + d) : 0.f;
+    // prep role: E consecutive steps of channel pch, starting at step pt0 of the chunk
+    const int pch = tid / C::PT;
+    const int pt0 = (tid % C::PT) * E;
+    const int pdg = cblk * C::CB + pch;
+    const bool pvalid = pdg < p.dpg;
+    const int64_t pd = (int64_t)grp * p.dpg + (pvalid ? pdg : p.dpg - 1);
+    const float Dd = p.D ? __ldg(p.D + (int64_t)p.k * p.dim + pd) : 0.f;
+    const float bd = p.bias ? __ldg(p.bias + (int64_t)p.k * p.dim + pd) : 0.f;
+    const int64_t prow = (int64_t)b * p.dim + pd;  // u/z row of the prep channel
 
     float *bcbuf0 = reinterpret_cast<float *>(smem + C::OFF_BC);
-    const float4 *dxrow_c = reinterpret_cast<const float4 *>(smem + C::OFF_DX + ch * C::DXROW);
-    float4 *dxrow = reinterpret_cast<float4 *>(smem + C::OFF_DX + ch * C::DXROW);
-    float4 *gdrow = reinterpret_cast<float4 *>(smem + C::OFF_GD + ch * C::DXROW);
-    uint8_t *obrow = smem + C::OFF_OB + ch * C::OBROW;
+    uint8_t *obrows[CL];
+#pragma unroll
+    for (int c = 0; c < CL; ++c) obrows[c] = smem + C::OFF_OB + chs[c] * C::OBROW;
     const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
     const uint32_t smem0 = smem_u32(smem);
-    const uint32_t tx_bytes = (p.has_z ? 3u : 2u) * C::CB * 64u + 2u * N * 64u;
+    const bool z_tiled = u_tiled && gate_in_prep;
+    const uint32_t tx_bytes = (1u + (u_tiled ? 1u : 0u) + (z_tiled ? 1u : 0u)) * C::CB * 64u +
+                              2u * N * 64u;
     const uint64_t budget = g_wait_budget_ns;
 
     if (tid == 0) {
@@ -241,10 +671,13 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
         const uint32_t bar = bar0 + 8 * s;
         const uint32_t st = smem0 + s * C::STAGE;
         const int x = (int)(t_begin + (int64_t)i * T);
+        // u/z tile of a reversed row order: positions L-(i+1)T .. L-1-iT (may
+        // start below 0 on the last chunk; the copy fills zeros there)
+        const int xu = (p.order == 2) ? (int)(p.L - (int64_t)(i + 1) * T) : x;
         mbar_expect_tx(bar, tx_bytes);
-        tma_load_2d(st + C::OFF_U, &tm_u, x, row_tma, bar);
-        tma_load_2d(st + C::OFF_DL, &tm_dl, x, row_tma, bar);
-        if (p.has_z) tma_load_2d(st + C::OFF_Z, &tm_z, x, row_tma, bar);
+        if (u_tiled) tma_load_2d(st + C::OFF_U, &tm_u, xu, row_tma, bar);
+        tma_load_2d(st + C::OFF_DL, &tm_dl, x, dlrow_tma, bar);
+        if (z_tiled) tma_load_2d(st + C::OFF_Z, &tm_z, xu, row_tma, bar);
         tma_load_2d(st + C::OFF_B, &tm_B, x, bcrow_tma, bar);
         tma_load_2d(st + C::OFF_C, &tm_C, x, bcrow_tma, bar);
     };
@@ -254,99 +687,205 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
     }
 
     float sdt_acc = 0.f;
+    // Column orders: this thread's u (and z) values of a chunk, gathered at the
+    // positions the steps visit one chunk before they are prepped.
+    using Raw = typename IOT<IO>::Raw;
+    Raw gu[E], gz[E];
+    auto gather = [&](int i) {
+        if (!MULTI || u_tiled) return;
+        const IO *urow = reinterpret_cast<const IO *>(p.u_g) + prow * p.L;
+        const IO *zrow = reinterpret_cast<const IO *>(p.z_g) + prow * p.L;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int64_t sg = t_begin + (int64_t)i * T + pt0 + e;
+            const bool in = sg < p.L;
+            const int64_t pos = in ? position_of(p.order, sg, p.L, p.H, p.W, p.divH) : 0;
+            gu[e] = in ? IOT<IO>::load_raw(urow + pos) : Raw(0);
+            if (gate_in_prep) gz[e] = in ? IOT<IO>::load_raw(zrow + pos) : Raw(0);
+        }
+    };
+    MergeRegs<C> mr;
+    // Converts B/C and preps the steps of chunk i into buffer half (i & 1).
+    auto prep_chunk = [&](int i) {
+        const int s = i % C::STAGES;
+        const uint8_t *st = smem + s * C::STAGE;
+        convert_bc<C>(st + C::OFF_B, st + C::OFF_C, bcbuf0 + (i & 1) * (C::BCBUF / 4), tid);
+        const int pb = C::OVL ? (i & 1) : 0;
+        float4 *pdxrow = reinterpret_cast<float4 *>(smem + C::OFF_DX + pb * C::PREPBUF +
+                                                    pch * C::DXROW);
+        float4 *pgdrow = reinterpret_cast<float4 *>(smem + C::OFF_GD + pb * C::PREPBUF +
+                                                    pch * C::DXROW);
+        float uu[E], dd[E], zz[E];
+        load_tile_row<IO, E>(st + C::OFF_DL, pch, pt0, dd);
+        if (p.order == 0) {
+            load_tile_row<IO, E>(st + C::OFF_U, pch, pt0, uu);
+            if (z_tiled) load_tile_row<IO, E>(st + C::OFF_Z, pch, pt0, zz);
+        } else if (p.order == 2) {
+            // reversed tile: step pt0+e sits at tile column T-1-(pt0+e)
+            float tmp[E];
+            load_tile_row<IO, E>(st + C::OFF_U, pch, T - pt0 - E, tmp);
+#pragma unroll
+            for (int e = 0; e < E; ++e) uu[e] = tmp[E - 1 - e];
+            if (z_tiled) {
+                load_tile_row<IO, E>(st + C::OFF_Z, pch, T - pt0 - E, tmp);
+#pragma unroll
+                for (int e = 0; e < E; ++e) zz[e] = tmp[E - 1 - e];
+            }
+        } else {
+            // column orders: u (and z) were gathered one chunk early
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                uu[e] = IOT<IO>::widen(gu[e]);
+                if (gate_in_prep) zz[e] = IOT<IO>::widen(gz[e]);
+            }
+        }
+        // steps of this chunk at or past the end of the L-chunk leave h unchanged
+        const int lim = (int)min((int64_t)T, t_end - (t_begin + (int64_t)i * T)) - pt0;
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+            float dl[2], xx[2], ga[2], du[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                float v = dd[e + k] + bd;
+                if (p.softplus) v = softplus(v);
+                if (e + k >= lim) v = 0.f;
+                dl[k] = v;
+                xx[k] = v * uu[e + k];
+                ga[k] = gate_in_prep ? silu(zz[e + k]) : 1.f;
+                du[k] = Dd * uu[e + k] * ga[k];
+                if (p.pass == 1) sdt_acc += v;
+            }
+            const int slot = swz_slot((pt0 + e) >> 1);
+            pdxrow[slot] = make_float4(dl[0], dl[1], xx[0], xx[1]);
+            pgdrow[slot] = make_float4(ga[0], du[0], ga[1], du[1]);
+        }
+    };
+    // Bounded wait for chunk i's tiles; on timeout the whole CTA drains its
+    // copies and exits (returns true then).
+    auto abandon = [&](int i, bool ok) -> bool {
+        if (!__syncthreads_or(!ok)) return false;
+        if (tid == 0) {
+            report_timeout();
+            // let every copy this CTA issued land before its smem goes away
+#pragma unroll 1
+            for (int k = i; k < nchunks && k < i + C::STAGES; ++k)
+                if (!(k == 0 && skip_first))
+                    (void)mbar_wait_bounded(bar0 + 8 * (k % C::STAGES), (k / C::STAGES) & 1,
+                                            1000000000ull);
+        }
+        return true;
+    };
+
+    if (nchunks > 0) gather(0);
+    if (C::OVL && nchunks > 0) {
+        const bool ok = mbar_wait_bounded(bar0, 0, budget);
+        if (ok) prep_chunk(0);
+        if (nchunks > 1) gather(1);
+        if (abandon(0, ok)) return;
+        if (tid == 0 && C::STAGES < nchunks) {
+            fence_proxy_async_smem();
+            issue(C::STAGES);
+        }
+    }
 #pragma unroll 1
     for (int i = 0; i < nchunks; ++i) {
-        const int s = i % C::STAGES;
-        const bool ok = mbar_wait_bounded(bar0 + 8 * s, (i / C::STAGES) & 1, budget);
-        const uint8_t *st = smem + s * C::STAGE;
-        float *bc = bcbuf0 + (i & 1) * (C::BCBUF / 4);
-        convert_bc<C>(st + C::OFF_B, st + C::OFF_C, bc, tid);
-
-        // prep: this lane's E consecutive steps of its channel
-        {
-            float uu[E], dd[E], zz[E];
-            load_tile_row<IO, E>(st + C::OFF_U, ch, E * g, uu);
-            load_tile_row<IO, E>(st + C::OFF_DL, ch, E * g, dd);
-            if (p.has_z) load_tile_row<IO, E>(st + C::OFF_Z, ch, E * g, zz);
-            const int64_t t0 = t_begin + (int64_t)i * T + E * g;
-#pragma unroll
-            for (int e = 0; e < E; e += 2) {
-                float dl[2], xx[2], ga[2], du[2];
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    float v = dd[e + k] + bd;
-                    if (p.softplus) v = softplus(v);
-                    if (t0 + e + k >= t_end) v = 0.f;  // steps past the end leave h unchanged
-                    dl[k] = v;
-                    xx[k] = v * uu[e + k];
-                    ga[k] = p.has_z ? silu(zz[e + k]) : 1.f;
-                    du[k] = Dd * uu[e + k] * ga[k];
-                    sdt_acc += v;
-                }
-                const int slot = swz_slot((E * g + e) >> 1);
-                dxrow[slot] = make_float4(dl[0], dl[1], xx[0], xx[1]);
-                gdrow[slot] = make_float4(ga[0], du[0], ga[1], du[1]);
+        const bool more = i + 1 < nchunks;
+        bool ok = true;
+        if constexpr (C::OVL) {
+            if (more) {
+                ok = mbar_wait_bounded(bar0 + 8 * ((i + 1) % C::STAGES), ((i + 1) / C::STAGES) & 1,
+                                       budget);
+                if (ok) prep_chunk(i + 1);
+                if (i + 2 < nchunks) gather(i + 2);
             }
-        }
-        const int any_fail = __syncthreads_or(!ok);
-        if (any_fail) {
-            if (tid == 0) {
-                report_timeout();
-                // let every copy this CTA issued land before its smem goes away
-#pragma unroll 1
-                for (int k = i; k < nchunks && k < i + C::STAGES; ++k)
-                    if (!(k == 0 && skip_first))
-                        (void)mbar_wait_bounded(bar0 + 8 * (k % C::STAGES), (k / C::STAGES) & 1,
-                                            1000000000ull);
-            }
-            return;
-        }
-        if (tid == 0 && i + C::STAGES < nchunks) {
-            fence_proxy_async_smem();
-            issue(i + C::STAGES);
-        }
-
-        if (do_y) {
-            scan_chunk<C, true>(dxrow_c, bc, g, h, A2p, [&](float y, int t) {
-                const float2 ge = reinterpret_cast<const float2 *>(gdrow + swz_slot(t >> 1))[t & 1];
-                reinterpret_cast<IO *>(obrow)[t] = IOT<IO>::from_f(fmaf(y, ge.x, ge.y));
-            });
         } else {
-            scan_chunk<C, false>(dxrow_c, bc, g, h, A2p, [](float, int) {});
+            // classic order: tiles of chunk i, prep, barrier, refill, scan
+            ok = mbar_wait_bounded(bar0 + 8 * (i % C::STAGES), (i / C::STAGES) & 1, budget);
+            if (ok) prep_chunk(i);
+            if (more) gather(i + 1);
+            if (abandon(i, ok)) return;
+            if (tid == 0 && i + C::STAGES < nchunks) {
+                fence_proxy_async_smem();
+                issue(i + C::STAGES);
+            }
+        }
+        const int rb = C::OVL ? (i & 1) : 0;
+        if (MULTI && do_y) load_partials<C>(p, mr, warp, lane, cblk, row0, (int64_t)i * T);
+
+        const float *bc = bcbuf0 + (i & 1) * (C::BCBUF / 4);
+        const float4 *dxrows[CL];
+        const float4 *gdrows[CL];
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+            dxrows[c] = reinterpret_cast<const float4 *>(smem + C::OFF_DX + rb * C::PREPBUF +
+                                                         chs[c] * C::DXROW);
+            gdrows[c] = reinterpret_cast<const float4 *>(smem + C::OFF_GD + rb * C::PREPBUF +
+                                                         chs[c] * C::DXROW);
+        }
+        auto emit = [&](int c, float y, int t) {
+            const float2 ge = reinterpret_cast<const float2 *>(gdrows[c] + swz_slot(t >> 1))[t & 1];
+            const float v = fmaf(y, ge.x, ge.y);
+            if (p.mode == OUT_STORE) reinterpret_cast<IO *>(obrows[c])[t] = IOT<IO>::from_f(v);
+            else reinterpret_cast<float *>(obrows[c])[t] = v;
+        };
+        if constexpr (C::PIPE) {
+            if (do_y) scan_chunk_pipe<C, true>(dxrows, bc, g, h, A2p, emit);
+            else scan_chunk_pipe<C, false>(dxrows, bc, g, h, A2p, [](int, float, int) {});
+        } else {
+            if (do_y) scan_chunk_cl<C, true>(dxrows, bc, g, h, A2p, emit);
+            else scan_chunk_cl<C, false>(dxrows, bc, g, h, A2p, [](int, float, int) {});
         }
         __syncwarp();
 
-        if (do_y) {
+        if (do_y && p.mode != OUT_STORE) {
+            store_partials<C>(p, mr, smem, warp, lane, cblk, row0, (int64_t)i * T);
+            __syncwarp();
+        } else if (do_y) {
             constexpr int VPC = 16 / C::ES;
 #pragma unroll 1
-            for (int k = lane; k < C::CPW * 4; k += 32) {
-                const int rr = k >> 2, q = k & 3;
-                const int chr = warp * C::CPW + rr;
+            for (int k = lane; k < C::CHW * 4; k += 32) {
+                const int rr = k >> 2, qq = k & 3;
+                const int chr = warp * C::CHW + rr;
                 const int dgr = cblk * C::CB + chr;
-                const int64_t t = t_begin + (int64_t)i * T + q * VPC;
+                const int64_t t = t_begin + (int64_t)i * T + qq * VPC;
                 if (dgr < p.dpg && t < t_end) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(smem + C::OFF_OB + chr * C::OBROW + q * 16);
-                    IO *dst = reinterpret_cast<IO *>(p.out) +
-                              ((int64_t)b * p.dim + (int64_t)grp * p.dpg + dgr) * p.L + t;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(smem + C::OFF_OB + chr * C::OBROW + qq * 16);
+                    IO *dst = reinterpret_cast<IO *>(p.out) + (row0 + dgr) * p.L + t;
                     *reinterpret_cast<uint4 *>(dst) = v;
                 }
             }
             __syncwarp();
         }
+        if constexpr (C::OVL) {
+            // chunk i+1's tiles are consumed and chunk i's rows are read: refill
+            if (abandon(i + 1, ok)) return;
+            if (tid == 0 && more && i + 1 + C::STAGES < nchunks) {
+                fence_proxy_async_smem();
+                issue(i + 1 + C::STAGES);
+            }
+        }
     }
 
-    if (!valid) return;
-    const bool last_chunk = (jc == p.J - 1);
-    if (p.last_state && (p.pass == 0 || (p.pass == 2 && last_chunk))) {
-#pragma unroll
-        for (int j = 0; j < NPT; ++j) p.last_state[row * N + g * NPT + j] = h[j];
-    }
     if (p.pass == 1) {
+        // sum of Delta' over this L-chunk: reduce over the channel's PT prep threads
 #pragma unroll
-        for (int j = 0; j < NPT; ++j) p.hend[(row * p.J + jc) * N + g * NPT + j] = h[j];
+        for (int m = 1; m < C::PT; m <<= 1) sdt_acc += __shfl_xor_sync(kFull, sdt_acc, m);
+        if (pvalid && (tid % C::PT) == 0) p.sdt[(row0 + pdg) * p.J + jc] = sdt_acc;
+    }
+    const bool last_chunk = (jc == p.J - 1);
 #pragma unroll
-        for (int m = 1; m < R; m <<= 1) sdt_acc += __shfl_xor_sync(kFull, sdt_acc, m);
-        if (g == 0) p.sdt[row * p.J + jc] = sdt_acc;
+    for (int c = 0; c < CL; ++c) {
+        if (!valid[c]) continue;
+        if (p.last_state && (p.pass == 0 || (p.pass == 2 && last_chunk))) {
+            // last_state [batch, K, dim, N]
+            const int64_t ls = (((int64_t)b * p.K + p.k) * p.dim + (rows[c] - (int64_t)b * p.dim)) * N;
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) p.last_state[ls + g * NPT + j] = h[c][j];
+        }
+        if (p.pass == 1) {
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) p.hend[(rows[c] * p.J + jc) * N + g * NPT + j] = h[c][j];
+        }
     }
 }
 

@@ -96,9 +96,8 @@ def gpu_run(inp, chunks=0, t=None):
     H, W = wl.H, wl.W
     bsz, dim, L = t["u"].shape
     G, N = t["B"].shape[2], t["B"].shape[3]
-    out, last = ss.cross_scan2d_fwd(t["u"].view(bsz, dim, H, W), t["delta"].view(bsz, 4, dim, H, W),
-                                    t["A"], t["B"].view(bsz, 4, G, N, H, W),
-                                    t["C"].view(bsz, 4, G, N, H, W), t["D"], t["delta_bias"], True,
+    out, last = ss.cross_scan2d_fwd(t["u"].view(bsz, dim, H, W), t["delta"],
+                                    t["A"], t["B"], t["C"], t["D"], t["delta_bias"], True,
                                     z=None if t["z"] is None else t["z"].view(bsz, dim, H, W),
                                     return_last_state=True)
     return out.view(bsz, dim, L), last

@@ -170,7 +170,21 @@ def test_cross_scan2d(oracle, H, W, io):
 
 
 def test_cross_scan2d_gated_groups(oracle):
+    """Unaligned rows (60 bf16 = 120 bytes): the on-chip merge path."""
     _check(oracle, sc.workload("ss2d_gz", 1, 16, 6 * 10, N=4, G=2, K=4, H=6, W=10))
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_cross_scan2d_gated_groups_workspace_path(oracle, io):
+    """Aligned rows: four TMA-staged direction scans merged through the fp32
+    workspace, with a z gate, two groups, N = 8 and a channel count that leaves
+    a partial channel block."""
+    _check(oracle, sc.workload("ss2d_gzw", 2, 40, 4 * 8, N=8, G=2, K=4, io=io, H=4, W=8))
+
+
+@pytest.mark.parametrize("L", [64, 200])
+def test_bidirectional_workspace_path_groups(oracle, L):
+    _check(oracle, sc.workload(f"bi_w{L}", 2, 48, L, N=16, G=2, K=2))
 
 
 # ---------------------------------------------------------------- full-size workloads

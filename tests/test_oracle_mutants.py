@@ -21,17 +21,19 @@ MUTANTS = {
     "drop_skip_D": ("o_row[p] += y + Dd * up;", "o_row[p] += y;"),
     "flip_sign_of_A": ("const double abar = exp(dt * a);", "const double abar = exp(-dt * a);"),
     "no_state_decay": ("h[n] = abar * h[n] + bbar * up;", "h[n] = h[n] + bbar * up;"),
-    "swap_B_for_C_in_input": ("bbar = dt * B_grp[n * L + p];", "bbar = dt * C_grp[n * L + p];"),
-    "swap_C_for_B_in_readout": ("y += C_grp[n * L + p] * h[n];", "y += B_grp[n * L + p] * h[n];"),
-    "drop_delta_bias": ("double dt = dl_row[p] + bd;", "double dt = dl_row[p];"),
+    "swap_B_for_C_in_input": ("bbar = dt * B_grp[n * L + s];", "bbar = dt * C_grp[n * L + s];"),
+    "swap_C_for_B_in_readout": ("y += C_grp[n * L + s] * h[n];", "y += B_grp[n * L + s] * h[n];"),
+    "drop_delta_bias": ("double dt = dl_row[s] + bd;", "double dt = dl_row[s];"),
     "softplus_without_log1p": ("log1p(exp(-fabs(x)))", "exp(-fabs(x))"),
     "sigmoid_instead_of_silu": ("out[i] *= zi / (1.0 + exp(-zi));", "out[i] *= 1.0 / (1.0 + exp(-zi));"),
     "reverse_off_by_one": ("case SSOR_ORDER_REV: return L - 1 - s;",
                            "case SSOR_ORDER_REV: return (L - s) % L;"),
     "column_map_transposed": ("case SSOR_ORDER_COL: return (s % H) * W + s / H;",
                               "case SSOR_ORDER_COL: return (s % W) * H + s / W;"),
-    "zoh_divides_wrong_way": ("bbar = (abar - 1.0) / a * B_grp[n * L + p];",
-                              "bbar = (abar - 1.0) * a * B_grp[n * L + p];"),
+    "zoh_divides_wrong_way": ("bbar = (abar - 1.0) / a * B_grp[n * L + s];",
+                              "bbar = (abar - 1.0) * a * B_grp[n * L + s];"),
+    "delta_by_position": ("double dt = dl_row[s] + bd;", "double dt = dl_row[p] + bd;"),
+    "B_by_position": ("bbar = dt * B_grp[n * L + s];", "bbar = dt * B_grp[n * L + p];"),
     "group_map_interleaved": ("const int64_t g = d / dpg;", "const int64_t g = d % ngroups;"),
     "ignores_initial_state": ("h[n] = h0 ? h0[((b * K + k) * dim + d) * N + n] : 0.0;",
                               "h[n] = 0.0;"),

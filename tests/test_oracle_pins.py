@@ -170,11 +170,15 @@ def test_softplus_matches_library(oracle):
 
 # ---------------------------------------------------------------- directions
 def test_reverse_is_flipped_forward(oracle):
+    """A reversed direction reads u (and writes out) from the last position back
+    to the first, with its Delta, B, C already in its own scan order: it equals
+    a forward scan of the flipped u (and z) with the same Delta, B, C, flipped
+    back."""
     rng = np.random.default_rng(4)
     u, delta, A, B, C, D, z, bias = _rand_case(rng, 2, 3, 31, 4, 1)
     out_r, last_r = oracle.scan(u, delta, A, B, C, D, z, bias, True, (oracle.ORDER_REV,))
     fl = lambda a: np.ascontiguousarray(a[..., ::-1])  # noqa: E731
-    out_f, last_f = oracle.scan(fl(u), fl(delta), A, fl(B), fl(C), D, fl(z), bias, True,
+    out_f, last_f = oracle.scan(fl(u), delta, A, B, C, D, fl(z), bias, True,
                                 (oracle.ORDER_FWD,))
     np.testing.assert_allclose(out_r, fl(out_f), rtol=1e-13, atol=1e-14)
     np.testing.assert_allclose(last_r, last_f, rtol=1e-13)
@@ -195,8 +199,9 @@ def test_bidirectional_is_sum_of_two_scans(oracle):
 
 @pytest.mark.parametrize("H,W", [(3, 5), (5, 3), (1, 1), (4, 4), (2, 7)])
 def test_ss2d_equals_four_permuted_scans(oracle, H, W):
-    """SS2D = four independent 1-D forward scans of explicitly permuted copies
-    (row-major, transposed, and both flipped), mapped back and summed."""
+    """SS2D = four independent 1-D forward scans of explicitly permuted copies of
+    the map (row-major, transposed, and both flipped), each with its own Delta,
+    B, C in its scan order, mapped back and summed."""
     rng = np.random.default_rng(6 + H * 10 + W)
     batch, dim, N, G = 2, 3, 4, 1
     L = H * W
@@ -220,8 +225,8 @@ def test_ss2d_equals_four_permuted_scans(oracle, H, W):
 
     total = np.zeros((batch, dim, L))
     for k in range(4):
-        yk, lk = oracle.scan(to_seq(u, k), to_seq(delta[:, k:k + 1], k), A[k * dim:(k + 1) * dim],
-                             to_seq(B[:, k:k + 1], k), to_seq(C[:, k:k + 1], k),
+        yk, lk = oracle.scan(to_seq(u, k), delta[:, k:k + 1], A[k * dim:(k + 1) * dim],
+                             B[:, k:k + 1], C[:, k:k + 1],
                              D[k * dim:(k + 1) * dim], None, bias[k * dim:(k + 1) * dim], True,
                              (oracle.ORDER_FWD,))
         total += from_seq(yk, k)
