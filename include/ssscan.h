@@ -174,8 +174,10 @@ ss_status ss_bidir_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dsta
  *   workspace  ss_workspace_bytes(SS_KIND_CROSS2D, batch, dim, H*W, dstate) bytes,
  *              16-byte aligned, not overlapping any tensor; NULL when that is 0.
  * When rows are 16-byte aligned (H*W * element size % 16 == 0) the four
- * directions run as four TMA-staged scans in SS_DIR_* order that merge through
- * the workspace (an fp32 [batch, dim, H*W] accumulator; deterministic).
+ * directions run as TMA-staged scans, two side by side per launch, that merge
+ * through the workspace: two fp32 [batch, dim, H*W] accumulators (row pair,
+ * column pair; each receives its terms in a fixed order, so the result is
+ * deterministic), summed and gated by a final merge.
  * Otherwise the whole map of a channel is merged in shared memory: H*W is then
  * limited by the per-block shared-memory size (SS_ERR_UNSUPPORTED beyond it).
  */

@@ -63,6 +63,9 @@ ss_status check_common(const char *fn, int64_t batch, int64_t dim, int64_t L, in
     if (batch * dim >= (1ll << 31) || L >= (1ll << 31) || batch * ngroups * dstate >= (1ll << 31) ||
         batch * K * dim >= (1ll << 31) || dim / ngroups >= (1ll << 30))
         return fail(SS_ERR_UNSUPPORTED, "%s: shape exceeds the 2^31 row/position limits", fn);
+    if (batch * ngroups > 65535)
+        return fail(SS_ERR_UNSUPPORTED, "%s: batch * ngroups %lld exceeds the 65535 grid rows", fn,
+                    (long long)(batch * ngroups));
     const int64_t es = io == SS_BF16 ? 2 : 4;
     const int64_t nel = batch * dim * L;
     const Span so{static_cast<const char *>(out), nel * es};
@@ -154,7 +157,7 @@ size_t ws_scan1d_any_dtype(int64_t batch, int64_t dim, int64_t L, int dstate, in
     return best;
 }
 
-size_t ws_multidir_any_dtype(int64_t batch, int64_t dim, int64_t L, int dstate) {
+size_t ws_multidir_any_dtype(int64_t batch, int64_t dim, int64_t L, int dstate, int K) {
     if (batch <= 0 || dim <= 0 || L <= 0 || !valid_dstate(dstate)) return 0;
     size_t best = 0;
     for (int io : {SS_F32, SS_BF16}) {
@@ -165,6 +168,7 @@ size_t ws_multidir_any_dtype(int64_t batch, int64_t dim, int64_t L, int dstate) 
         a.W = L;
         a.N = dstate;
         a.io = io;
+        a.K = K;
         const size_t w = multidir_workspace_bytes(a);
         if (w > best) best = w;
     }
@@ -317,7 +321,7 @@ ss_status ss_cross_scan2d_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, 
 size_t ss_workspace_bytes_opts(int kind, int64_t batch, int64_t dim, int64_t seqlen, int dstate,
                                const ss_scan_options *options) {
     if (kind == SS_KIND_BIDIR || kind == SS_KIND_CROSS2D)
-        return ws_multidir_any_dtype(batch, dim, seqlen, dstate);
+        return ws_multidir_any_dtype(batch, dim, seqlen, dstate, kind == SS_KIND_BIDIR ? 2 : 4);
     if (kind != SS_KIND_SCAN) return 0;
     return ws_scan1d_any_dtype(batch, dim, seqlen, dstate, options ? options->chunks : 0);
 }

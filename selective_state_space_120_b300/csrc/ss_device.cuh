@@ -68,13 +68,34 @@ __device__ __forceinline__ float silu(float z) { return z * rcp(1.0f + ex2(-z * 
 
 // ------------------------------------------------------------------ I/O types
 template <typename IO> struct IOT;
+// Prefetch loads as volatile asm: the compiler keeps them where they are
+// written (before the barrier and scan that hide their latency) instead of
+// sinking them to their first use.
+__device__ __forceinline__ unsigned short ld_pref_u16(const void *p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float ld_pref_f32(const void *p) {
+    float v;
+    asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float4 ld_pref_v4(const void *p) {
+    float4 v;
+    asm volatile("ld.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 // load_raw / widen split a load from its conversion, so a prefetched value can
 // stay in flight until it is used.
 template <> struct IOT<float> {
     using Raw = float;
     static __device__ __forceinline__ float from_f(float v) { return v; }
     static __device__ __forceinline__ float load(const float *p) { return __ldg(p); }
-    static __device__ __forceinline__ Raw load_raw(const float *p) { return __ldg(p); }
+    static __device__ __forceinline__ Raw load_raw(const float *p) { return ld_pref_f32(p); }
     static __device__ __forceinline__ float widen(Raw r) { return r; }
 };
 template <> struct IOT<__nv_bfloat16> {
@@ -85,7 +106,7 @@ template <> struct IOT<__nv_bfloat16> {
         return __uint_as_float(static_cast<uint32_t>(b) << 16);
     }
     static __device__ __forceinline__ Raw load_raw(const __nv_bfloat16 *p) {
-        return __ldg(reinterpret_cast<const unsigned short *>(p));
+        return ld_pref_u16(p);
     }
     static __device__ __forceinline__ float widen(Raw r) {
         return __uint_as_float(static_cast<uint32_t>(r) << 16);

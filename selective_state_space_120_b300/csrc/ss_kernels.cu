@@ -2,6 +2,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -189,14 +190,43 @@ struct Scan1d {
         const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);
         const unsigned bgs = (unsigned)(a.batch * a.G);
         cudaStream_t s = reinterpret_cast<cudaStream_t>(a.stream);
-        for (int k = 0; k < K; ++k) {
-            p.k = k;
-            p.order = a.orders[k];
-            p.mode = (k == 0) ? OUT_ACC_FIRST : (k == K - 1) ? OUT_ACC_LAST : OUT_ACC_ADD;
-            kern<<<dim3(cblocks, bgs, 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
-            if ((st = check_launch("direction scan"))) return st;
+        float *acc0 = reinterpret_cast<float *>(a.ws);
+        if (K != 4) {
+            // directions in order over one accumulator: store, add, ..., add + gate + write
+            for (int k = 0; k < K; ++k) {
+                p.nz = 1;
+                p.k0 = k;
+                p.orders_z[0] = a.orders[k];
+                p.modes_z[0] = (k == 0) ? OUT_ACC_FIRST : (k == K - 1) ? OUT_ACC_LAST : OUT_ACC_ADD;
+                p.accs_z[0] = acc0;
+                kern<<<dim3(cblocks, bgs, 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
+                if ((st = check_launch("direction scan"))) return st;
+            }
+            return SS_OK;
         }
-        return SS_OK;
+        // SS2D: two launches of two directions side by side -- (row, column) into
+        // two accumulators, then (reversed row, reversed column) added to them --
+        // then one merge.  Twice the warps of one direction per launch, and each
+        // accumulator still receives its terms in a fixed order.  The column
+        // pair's accumulator is the transposed map, so its accesses stay
+        // contiguous; the merge transposes it back.
+        float *acc1 = acc0 + rows * a.L;
+        for (int half = 0; half < 2; ++half) {
+            p.nz = 2;
+            p.k0 = 2 * half;
+            for (int d = 0; d < 2; ++d) {
+                p.orders_z[d] = a.orders[2 * half + d];
+                p.modes_z[d] = half == 0 ? OUT_ACC_FIRST : OUT_ACC_ADD;
+                p.accs_z[d] = d == 0 ? acc0 : acc1;
+            }
+            kern<<<dim3(cblocks, bgs, 2), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
+            if ((st = check_launch("direction pair scan"))) return st;
+        }
+        using IO = typename C::IO;
+        const dim3 mgrid((unsigned)rows, (unsigned)((a.W + 31) / 32), (unsigned)((a.H + 31) / 32));
+        k_merge2<IO><<<mgrid, dim3(32, 8), 0, s>>>(acc0, acc1, reinterpret_cast<const IO *>(a.z),
+                                                  reinterpret_cast<IO *>(a.out), (int)a.H, (int)a.W);
+        return check_launch("merge");
     }
 
     // Steps per L-chunk for a requested chunk count: a multiple of the T-tile.
@@ -410,7 +440,8 @@ ss_status launch_scan1d(const ScanArgs &a) {
 
 size_t multidir_workspace_bytes(const ScanArgs &a) {
     if (!scan1d_uses_tma(a)) return 0;  // rows not 16-byte aligned: on-chip merge path
-    return (size_t)a.batch * a.dim * a.L * sizeof(float);
+    // one fp32 accumulator; SS2D scans two pairs of directions side by side into two
+    return (size_t)a.batch * a.dim * a.L * sizeof(float) * (a.K == 4 ? 2 : 1);
 }
 
 ss_status launch_multidir(const ScanArgs &a) {

@@ -115,6 +115,12 @@ struct Scan1dParams {
     FastDiv divH;
     int mode;     // OUT_*
     float *acc;   // [batch*dim, L] fp32 merge accumulator by position (modes 1-3)
+    // Multi-direction launches may scan several directions side by side:
+    // blockIdx.z = d selects direction k0 + d with its own order, mode and
+    // accumulator (entries [0, nz)).
+    int nz, k0;
+    int orders_z[2], modes_z[2];
+    float *accs_z[2];
     const void *u_g, *z_g;  // u and z for the gathers of the column orders
     const float *A, *D, *bias;
     int softplus, has_z;
@@ -445,13 +451,16 @@ __device__ __forceinline__ void scan_chunk_pipe(const float4 *const (&dxrow)[C::
 }
 
 // Epilogue of the merge modes for one chunk (steps s0 .. s0+T-1 of direction
-// k): the warp's staged fp32 partials y_k + D_k*u go to the accumulator at the
-// positions the steps visit (stored, added, or -- for the last direction --
-// added, gated by SiLU(z) and written to out in the I/O type).  Each lane owns
-// TPL tasks of four steps: a row order maps them to four consecutive positions
-// (ascending or descending), one 16-byte access; the column orders scatter.
-// MergeRegs holds what a task reads from global memory (the accumulator and z),
-// loaded one chunk early by load_partials so the latency hides behind the scan.
+// k): the warp's staged fp32 partials y_k + D_k*u go to the accumulator
+// (stored, added, or -- for the last direction -- added, gated by SiLU(z) and
+// written to out in the I/O type).  An accumulator is indexed in its pair's
+// traversal: by position for the row orders, by column-major index (the
+// transposed map) for the column orders, so that in both cases step s of the
+// forward order sits at index s and of the reversed order at index L-1-s; four
+// steps are one 16-byte access.  Only row orders run the last mode (the column
+// pair is transposed back by the final merge).  MergeRegs holds what a task
+// reads from global memory (the accumulator and z), loaded one chunk early by
+// load_partials so the latency hides behind the scan.
 template <class C>
 struct MergeRegs {
     static constexpr int QG = C::T / 4;  // groups of four steps per chunk
@@ -487,22 +496,12 @@ __device__ __forceinline__ void load_partials(const Scan1dParams &p, MergeRegs<C
         const float *accr = p.acc + row * p.L;
         const IO *zr = reinterpret_cast<const IO *>(p.z_g) + row * p.L;
         const bool gate = p.mode == OUT_ACC_LAST && p.has_z;
-        if (p.order == 0 || p.order == 2) {
-            const int64_t pos0 = (p.order == 2) ? p.L - 4 - sg : sg;
-            mr.acc[m] = *reinterpret_cast<const float4 *>(accr + pos0);
-            if (gate) {
+        const bool rev = p.order >= 2;
+        const int64_t pos0 = rev ? p.L - 4 - sg : sg;
+        mr.acc[m] = ld_pref_v4(accr + pos0);
+        if (gate) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) mr.z[m][j] = IOT<IO>::load_raw(zr + pos0 + j);
-            }
-        } else {
-            float a[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int64_t pos = position_of(p.order, sg + j, p.L, p.H, p.W, p.divH);
-                a[j] = accr[pos];
-                if (gate) mr.z[m][j] = IOT<IO>::load_raw(zr + pos);
-            }
-            mr.acc[m] = make_float4(a[0], a[1], a[2], a[3]);
+            for (int j = 0; j < 4; ++j) mr.z[m][j] = IOT<IO>::load_raw(zr + pos0 + j);
         }
     }
 }
@@ -523,12 +522,12 @@ __device__ __forceinline__ void store_partials(const Scan1dParams &p, const Merg
         float *accr = p.acc + row * p.L;
         IO *outr = reinterpret_cast<IO *>(p.out) + row * p.L;
         const bool gate = p.mode == OUT_ACC_LAST && p.has_z;
-        // w[j] is the term of step sg + j; a row order reversed reads back to front
+        // w[j] is the term of step sg + j; a reversed order runs back to front
+        const bool rev = p.order >= 2;
         float w[4] = {v.x, v.y, v.z, v.w};
         if (p.mode != OUT_ACC_FIRST) {
-            // the prefetched accumulator is in position order for the row orders
-            const float4 o = mr.acc[m];
-            if (p.order == 2) {
+            const float4 o = mr.acc[m];  // prefetched, in accumulator order
+            if (rev) {
                 w[0] += o.w; w[1] += o.z; w[2] += o.y; w[3] += o.x;
             } else {
                 w[0] += o.x; w[1] += o.y; w[2] += o.z; w[3] += o.w;
@@ -536,34 +535,21 @@ __device__ __forceinline__ void store_partials(const Scan1dParams &p, const Merg
         }
         if (gate) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int jz = (p.order == 2) ? 3 - j : j;  // z prefetched in position order
-                w[j] *= silu(IOT<IO>::widen(mr.z[m][jz]));
-            }
+            for (int j = 0; j < 4; ++j) w[j] *= silu(IOT<IO>::widen(mr.z[m][rev ? 3 - j : j]));
         }
-        if (p.order == 0 || p.order == 2) {
-            const bool rev = p.order == 2;
-            const int64_t pos0 = rev ? p.L - 4 - sg : sg;
-            float q[4];
+        const int64_t pos0 = rev ? p.L - 4 - sg : sg;
+        float q[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) q[j] = rev ? w[3 - j] : w[j];  // position order
-            if (p.mode != OUT_ACC_LAST) {
-                *reinterpret_cast<float4 *>(accr + pos0) = make_float4(q[0], q[1], q[2], q[3]);
-            } else if constexpr (sizeof(IO) == 2) {
-                uint2 packed;
-                packed.x = pack_bf16x2(q[0], q[1]);
-                packed.y = pack_bf16x2(q[2], q[3]);
-                *reinterpret_cast<uint2 *>(outr + pos0) = packed;
-            } else {
-                *reinterpret_cast<float4 *>(outr + pos0) = make_float4(q[0], q[1], q[2], q[3]);
-            }
+        for (int j = 0; j < 4; ++j) q[j] = rev ? w[3 - j] : w[j];  // accumulator order
+        if (p.mode != OUT_ACC_LAST) {
+            *reinterpret_cast<float4 *>(accr + pos0) = make_float4(q[0], q[1], q[2], q[3]);
+        } else if constexpr (sizeof(IO) == 2) {
+            uint2 packed;
+            packed.x = pack_bf16x2(q[0], q[1]);
+            packed.y = pack_bf16x2(q[2], q[3]);
+            *reinterpret_cast<uint2 *>(outr + pos0) = packed;
         } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int64_t pos = position_of(p.order, sg + j, p.L, p.H, p.W, p.divH);
-                if (p.mode != OUT_ACC_LAST) accr[pos] = w[j];
-                else outr[pos] = IOT<IO>::from_f(w[j]);
-            }
+            *reinterpret_cast<float4 *>(outr + pos0) = make_float4(q[0], q[1], q[2], q[3]);
         }
     }
 }
@@ -583,6 +569,12 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
         p.k = 0;
         p.order = 0;
         p.mode = OUT_STORE;
+    } else {
+        const int dz = (int)blockIdx.z;  // direction of this slice of the grid
+        p.k = p.k0 + dz;
+        p.order = p.orders_z[dz];
+        p.mode = p.modes_z[dz];
+        p.acc = p.accs_z[dz];
     }
     constexpr int N = C::N, NPT = C::NPT, T = C::T, E = C::E, CL = C::CL;
     extern __shared__ uint8_t smem_raw[];
@@ -594,7 +586,7 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
     const int cblk = blockIdx.x;
     const int bg = blockIdx.y;
     const int b = bg / p.G, grp = bg % p.G;
-    const int jc = p.jbase + blockIdx.z;
+    const int jc = MULTI ? 0 : p.jbase + (int)blockIdx.z;
     const int64_t row0 = (int64_t)b * p.dim + (int64_t)grp * p.dpg;  // row of the group's channel 0
     const int row_tma = (int)(row0 + (int64_t)cblk * C::CB);          // u, z, out rows
     // Delta rows of direction k: [batch, K, dim]; B/C rows: [batch, K, G, N]
@@ -885,6 +877,43 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
         if (p.pass == 1) {
 #pragma unroll
             for (int j = 0; j < NPT; ++j) p.hend[(rows[c] * p.J + jc) * N + g * NPT + j] = h[c][j];
+        }
+    }
+}
+
+// Final merge of a four-direction call scanned as two pairs: out = (row-pair
+// accumulator + column-pair accumulator transposed back) gated by SiLU(z), in
+// the I/O type.  acc_row is [rows, H, W]; acc_col is [rows, W, H] (column-major
+// map).  One 32 x 32 tile of one row per block: the column-pair tile is read
+// along its contiguous axis into shared memory and written out along the map's.
+template <typename IO>
+__global__ void __launch_bounds__(256) k_merge2(const float *__restrict__ acc_row,
+                                                const float *__restrict__ acc_col,
+                                                const IO *__restrict__ z, IO *__restrict__ out,
+                                                int H, int W) {
+    __shared__ float tile[32][33];
+    const int64_t row = blockIdx.x;
+    const int64_t L = (int64_t)H * W;
+    const int c0 = blockIdx.y * 32, r0 = blockIdx.z * 32;
+    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+    const float *ac = acc_col + row * L;
+#pragma unroll
+    for (int k = 0; k < 32; k += 8) {
+        const int c = c0 + ty + k, r = r0 + tx;
+        if (c < W && r < H) tile[ty + k][tx] = ac[(int64_t)c * H + r];
+    }
+    __syncthreads();
+    const float *ar = acc_row + row * L;
+    IO *o = out + row * L;
+    const IO *zr = z ? z + row * L : nullptr;
+#pragma unroll
+    for (int k = 0; k < 32; k += 8) {
+        const int r = r0 + ty + k, c = c0 + tx;
+        if (c < W && r < H) {
+            const int64_t pos = (int64_t)r * W + c;
+            float v = ar[pos] + tile[tx][ty + k];
+            if (zr) v *= silu(IOT<IO>::load(zr + pos));
+            o[pos] = IOT<IO>::from_f(v);
         }
     }
 }
