@@ -411,6 +411,25 @@ def cpu_model() -> str:
     return "unknown"
 
 
+# ------------------------------------------------------------------ replicas
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank runs its own replica of the workload
+    (the scan shards over batch and channels with no exchange), so the job is
+    as fast as its slowest rank."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(elems_per_rank: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput in Gelem/s: all ranks' elements over the slowest time."""
+    return world * elems_per_rank / (max_ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ main
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
@@ -510,12 +529,8 @@ def main(argv=None):
     wl = WORKLOADS[args.workload]
     peak, peak_kind = measured_peaks()
     r, ms, kern_ms, clocks = measure_gpu(wl, args.steps, args.warmup, barrier)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    value = world * wl.elems / (ms * 1e-3) / 1e9
+    ms = max_over_ranks(ms, world, "cuda")
+    value = job_value(wl.elems, world, ms)
     e2e = r.e2e(args.e2e_steps, 3)
     e2e["value"] *= world
     copies = r.copies

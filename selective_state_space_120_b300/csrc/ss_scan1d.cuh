@@ -417,20 +417,25 @@ __device__ __forceinline__ void scan_chunk_pipe(const float4 *const (&dxrow)[C::
         const int pp = tp % PPB;
 #pragma unroll
         for (int c = 0; c < CL; ++c) {
-            // two readout accumulators halve the dependent FMA chain
-            float2 y2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            // written phase by phase (every state's first step, then every
+            // state's second step, then the readout) so that independent FMAs
+            // sit between each dependent pair
+            float hs0[NPT];
 #pragma unroll
-            for (int j = 0; j < NPT; ++j) {
-                const float h0 = fmaf(cur.a[c][j][0], h[c][j], cur.bx[c][j].x);
-                const float h1 = fmaf(cur.a[c][j][1], h0, cur.bx[c][j].y);
-                h[c][j] = h1;
-                if constexpr (DO_Y)
+            for (int j = 0; j < NPT; ++j) hs0[j] = fmaf(cur.a[c][j][0], h[c][j], cur.bx[c][j].x);
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) h[c][j] = fmaf(cur.a[c][j][1], hs0[j], cur.bx[c][j].y);
+            if constexpr (DO_Y) {
+                // two readout accumulators halve the dependent FMA chain
+                float2 y2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                for (int j = 0; j < NPT; ++j)
                     y2[j & 1] = __ffma2_rn(make_float2(cur.Cv[2 * j], cur.Cv[2 * j + 1]),
-                                           make_float2(h0, h1), y2[j & 1]);
+                                           make_float2(hs0[j], h[c][j]), y2[j & 1]);
+                if constexpr (NPT > 1) y2[0] = __fadd2_rn(y2[0], y2[1]);
+                v[c][2 * pp] = y2[0].x;
+                v[c][2 * pp + 1] = y2[0].y;
             }
-            if constexpr (NPT > 1) y2[0] = __fadd2_rn(y2[0], y2[1]);
-            v[c][2 * pp] = y2[0].x;
-            v[c][2 * pp + 1] = y2[0].y;
         }
         if constexpr (DO_Y) {
             if (pp == PPB - 1) {
@@ -467,34 +472,43 @@ struct MergeRegs {
     static constexpr int TPL = (C::CHW * QG + 31) / 32;
     float4 acc[TPL];
     typename IOT<typename C::IO>::Raw z[TPL][4];
+    // per task, fixed for the whole launch: the row offset (row * L, or -1 when
+    // the task has no channel), the staged row in shared memory, the group
+    int64_t rowL[TPL];
+    int chr[TPL], qq[TPL];
+
+    __device__ __forceinline__ void init(const Scan1dParams &p, int warp, int lane, int cblk, int64_t row0) {
+#pragma unroll
+        for (int m = 0; m < TPL; ++m) {
+            const int task = lane + 32 * m;
+            const int rr = task / QG;
+            qq[m] = task % QG;
+            chr[m] = warp * C::CHW + rr;
+            const int dgr = cblk * C::CB + chr[m];
+            rowL[m] = (task < C::CHW * QG && dgr < p.dpg) ? (row0 + dgr) * p.L : -1;
+        }
+    }
 };
 
+// Task m of this lane in the chunk starting at step s0: false if it has no
+// channel or lies past the end; sg = its first step.
 template <class C>
-__device__ __forceinline__ bool merge_task(const Scan1dParams &p, int warp, int lane, int cblk, int64_t s0,
-                                           int m, int &chr, int &dgr, int64_t &sg) {
-    constexpr int QG = MergeRegs<C>::QG;
-    const int task = lane + 32 * m;
-    if (task >= C::CHW * QG) return false;
-    const int rr = task / QG, qq = task % QG;
-    chr = warp * C::CHW + rr;
-    dgr = cblk * C::CB + chr;
-    sg = s0 + qq * 4;
-    return dgr < p.dpg && sg < p.L;
+__device__ __forceinline__ bool merge_task(const Scan1dParams &p, const MergeRegs<C> &mr, int64_t s0,
+                                           int m, int64_t &sg) {
+    sg = s0 + mr.qq[m] * 4;
+    return mr.rowL[m] >= 0 && sg < p.L;
 }
 
 template <class C>
-__device__ __forceinline__ void load_partials(const Scan1dParams &p, MergeRegs<C> &mr, int warp, int lane,
-                                              int cblk, int64_t row0, int64_t s0) {
+__device__ __forceinline__ void load_partials(const Scan1dParams &p, MergeRegs<C> &mr, int64_t s0) {
     using IO = typename C::IO;
     if (p.mode == OUT_ACC_FIRST) return;
 #pragma unroll
     for (int m = 0; m < MergeRegs<C>::TPL; ++m) {
-        int chr, dgr;
         int64_t sg;
-        if (!merge_task<C>(p, warp, lane, cblk, s0, m, chr, dgr, sg)) continue;
-        const int64_t row = row0 + dgr;
-        const float *accr = p.acc + row * p.L;
-        const IO *zr = reinterpret_cast<const IO *>(p.z_g) + row * p.L;
+        if (!merge_task<C>(p, mr, s0, m, sg)) continue;
+        const float *accr = p.acc + mr.rowL[m];
+        const IO *zr = reinterpret_cast<const IO *>(p.z_g) + mr.rowL[m];
         const bool gate = p.mode == OUT_ACC_LAST && p.has_z;
         const bool rev = p.order >= 2;
         const int64_t pos0 = rev ? p.L - 4 - sg : sg;
@@ -508,19 +522,16 @@ __device__ __forceinline__ void load_partials(const Scan1dParams &p, MergeRegs<C
 
 template <class C>
 __device__ __forceinline__ void store_partials(const Scan1dParams &p, const MergeRegs<C> &mr,
-                                               const uint8_t *smem, int warp, int lane, int cblk,
-                                               int64_t row0, int64_t s0) {
+                                               const uint8_t *smem, int64_t s0) {
     using IO = typename C::IO;
 #pragma unroll
     for (int m = 0; m < MergeRegs<C>::TPL; ++m) {
-        int chr, dgr;
         int64_t sg;
-        if (!merge_task<C>(p, warp, lane, cblk, s0, m, chr, dgr, sg)) continue;
-        const int qq = (int)((sg - s0) / 4);
-        const float4 v = *reinterpret_cast<const float4 *>(smem + C::OFF_OB + chr * C::OBROW + qq * 16);
-        const int64_t row = row0 + dgr;
-        float *accr = p.acc + row * p.L;
-        IO *outr = reinterpret_cast<IO *>(p.out) + row * p.L;
+        if (!merge_task<C>(p, mr, s0, m, sg)) continue;
+        const float4 v = *reinterpret_cast<const float4 *>(smem + C::OFF_OB + mr.chr[m] * C::OBROW +
+                                                           mr.qq[m] * 16);
+        float *accr = p.acc + mr.rowL[m];
+        IO *outr = reinterpret_cast<IO *>(p.out) + mr.rowL[m];
         const bool gate = p.mode == OUT_ACC_LAST && p.has_z;
         // w[j] is the term of step sg + j; a reversed order runs back to front
         const bool rev = p.order >= 2;
@@ -570,11 +581,11 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
         p.order = 0;
         p.mode = OUT_STORE;
     } else {
-        const int dz = (int)blockIdx.z;  // direction of this slice of the grid
-        p.k = p.k0 + dz;
-        p.order = p.orders_z[dz];
-        p.mode = p.modes_z[dz];
-        p.acc = p.accs_z[dz];
+        const bool z1 = blockIdx.z != 0;  // direction of this slice of the grid
+        p.k = p.k0 + (z1 ? 1 : 0);
+        p.order = z1 ? p_in.orders_z[1] : p_in.orders_z[0];  // selects, not a dynamic
+        p.mode = z1 ? p_in.modes_z[1] : p_in.modes_z[0];     // index (which would copy
+        p.acc = z1 ? p_in.accs_z[1] : p_in.accs_z[0];        // the params to the stack)
     }
     constexpr int N = C::N, NPT = C::NPT, T = C::T, E = C::E, CL = C::CL;
     extern __shared__ uint8_t smem_raw[];
@@ -687,16 +698,29 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
         if (!MULTI || u_tiled) return;
         const IO *urow = reinterpret_cast<const IO *>(p.u_g) + prow * p.L;
         const IO *zrow = reinterpret_cast<const IO *>(p.z_g) + prow * p.L;
+        // the map cell (r, c) of the first step, then one row down (forward) or
+        // up (reversed) per step, wrapping into the next / previous column
+        const int64_t s_first = t_begin + (int64_t)i * T + pt0;
+        const bool rev = p.order == 3;
+        // column-major index of the first step's cell: s (forward) or L-1-s (reversed)
+        const uint32_t cm = (uint32_t)(rev ? p.L - 1 - min(s_first, p.L - 1) : min(s_first, p.L - 1));
+        int c = (int)p.divH.div(cm);
+        int r = (int)(cm - (uint32_t)c * (uint32_t)p.H);
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-            const int64_t sg = t_begin + (int64_t)i * T + pt0 + e;
-            const bool in = sg < p.L;
-            const int64_t pos = in ? position_of(p.order, sg, p.L, p.H, p.W, p.divH) : 0;
+            const bool in = s_first + e < p.L;
+            const int64_t pos = (int64_t)r * p.W + c;
             gu[e] = in ? IOT<IO>::load_raw(urow + pos) : Raw(0);
             if (gate_in_prep) gz[e] = in ? IOT<IO>::load_raw(zrow + pos) : Raw(0);
+            if (!rev) {
+                if (++r == p.H) { r = 0; ++c; }
+            } else {
+                if (--r < 0) { r = p.H - 1; --c; }
+            }
         }
     };
     MergeRegs<C> mr;
+    if (MULTI) mr.init(p, warp, lane, cblk, row0);
     // Converts B/C and preps the steps of chunk i into buffer half (i & 1).
     auto prep_chunk = [&](int i) {
         const int s = i % C::STAGES;
@@ -802,7 +826,7 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
             }
         }
         const int rb = C::OVL ? (i & 1) : 0;
-        if (MULTI && do_y) load_partials<C>(p, mr, warp, lane, cblk, row0, (int64_t)i * T);
+        if (MULTI && do_y) load_partials<C>(p, mr, (int64_t)i * T);
 
         const float *bc = bcbuf0 + (i & 1) * (C::BCBUF / 4);
         const float4 *dxrows[CL];
@@ -830,7 +854,7 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
         __syncwarp();
 
         if (do_y && p.mode != OUT_STORE) {
-            store_partials<C>(p, mr, smem, warp, lane, cblk, row0, (int64_t)i * T);
+            store_partials<C>(p, mr, smem, (int64_t)i * T);
             __syncwarp();
         } else if (do_y) {
             constexpr int VPC = 16 / C::ES;
