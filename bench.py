@@ -489,6 +489,65 @@ def measure_gpu(wl, steps, warmup, barrier=None):
     return r, total_ms / steps, kern_ms, clocks
 
 
+DECODE_NAME = "decode_step_b8_d1536_n16"
+
+
+def measure_decode(steps: int):
+    """Token-by-token inference on the Mamba-130M layer shape: one state-update
+    call per step (batch 8, dim 1536, N 16, bf16 I/O, fp32 state updated in
+    place), over `steps` consecutive tokens with inputs resident in HBM."""
+    import torch
+    import selective_state_space_120_b300 as ss
+    wl = wk.Workload(DECODE_NAME, 8, 1536, steps, N=16)
+    inp = wk.make_inputs(wl, 0)
+    dev = lambda a: None if a is None else Runner._to_dev(a)  # noqa: E731
+    u, dl, A = dev(inp.u), dev(inp.delta[:, 0]), dev(inp.A)
+    B, C = dev(inp.B[:, 0]), dev(inp.C[:, 0])
+    D, z, bias = dev(inp.D), dev(inp.z), dev(inp.delta_bias)
+    # one token per step: per-token slices laid out contiguously
+    xs = u.permute(2, 0, 1).contiguous()
+    ds = dl.permute(2, 0, 1).contiguous()
+    zs = z.permute(2, 0, 1).contiguous()
+    Bs = B.permute(3, 0, 1, 2).contiguous()
+    Cs = C.permute(3, 0, 1, 2).contiguous()
+    state = torch.zeros(wl.batch, wl.dim, wl.N, device="cuda")
+    out = torch.empty(wl.batch, wl.dim, dtype=u.dtype, device="cuda")
+    def step(k):
+        ss.selective_state_update(xs[k], ds[k], A, Bs[k], Cs[k], state, D, zs[k], bias, True,
+                                  out=out)
+    for k in range(min(3, steps)):
+        step(k)
+    torch.cuda.synchronize()
+    # the steps are captured in a CUDA graph so that the host's per-call cost
+    # (argument checks, ctypes) is not what gets timed
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for k in range(steps):
+                step(k)
+    torch.cuda.current_stream().wait_stream(side)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 3
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * steps)
+    rows = wl.batch * wl.dim
+    # per channel and token: state read + write, A row, x, delta, z, out; B/C per batch
+    nbytes = rows * (2 * wl.N * 4 + wl.N * 4 + 4 * 2) + wl.batch * 2 * wl.N * 2
+    return {"value": rows / (ms * 1e-3) / 1e9, "unit": "Gelem/s (channel-tokens)",
+            "ms_per_step": ms, "kernel_launches_per_step": 1, "bytes_per_step": nbytes,
+            "note": "launch-latency bound: the state of a layer (786 KB) stays in L2",
+            "config": {"workload": DECODE_NAME, "batch": wl.batch, "dim": wl.dim,
+                       "d_state": wl.N, "io_dtype": "bf16", "tokens": steps}}
+
+
 def roofline(wl, kern_ms, peak, peak_kind):
     alg = algorithmic_bytes(wl)
     ach = alg / (kern_ms * 1e-3) / 1e9
@@ -555,6 +614,10 @@ def main(argv=None):
                 torch.cuda.empty_cache()
             except Exception as e:  # noqa: BLE001 -- reported, not hidden
                 others[owl.name] = {"error": f"{type(e).__name__}: {e}"}
+        try:
+            others[DECODE_NAME] = measure_decode(256)
+        except Exception as e:  # noqa: BLE001 -- reported, not hidden
+            others[DECODE_NAME] = {"error": f"{type(e).__name__}: {e}"}
 
     cpu = None
     if rank == 0 and not args.no_cpu:

@@ -117,8 +117,21 @@ typedef struct ss_scan_options {
      * n >= 2: the chunked long-sequence path with at most n L-chunks (each a
      * multiple of the kernel's step tile; fewer if the sequence is short). */
     int chunks;
-    int reserved[7]; /* must be zero */
+    /* Bit flags, SS_SCAN_* (0 for the default Euler step from a zero state). */
+    unsigned int flags;
+    /* Initial state [batch, dim, dstate] float32 (device, 16-byte aligned), or
+     * NULL for h = 0.  With last_state this continues a sequence across calls:
+     * scanning L1 steps, then L2 steps from the first call's last_state, equals
+     * one scan of L1 + L2 steps (the recurrent form the reading notes give for
+     * inference). */
+    const float *h0;
+    int reserved[4]; /* must be zero */
 } ss_scan_options;
+
+/* Zero-order-hold input matrix: Bbar = (Delta*A)^-1 (exp(Delta*A) - 1) * Delta*B
+ * ("Mamba Series ...", mathematical form of the selective SSM) instead of the
+ * default Euler Bbar = Delta*B.  For A = 0 it is Delta*B. */
+#define SS_SCAN_ZOH 1u
 
 /* ss_selective_scan_fwd with options (NULL options = automatic). */
 ss_status ss_selective_scan_fwd_opts(int64_t batch, int64_t dim, int64_t seqlen, int dstate,
@@ -227,6 +240,32 @@ ss_status ss_selective_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t seql
                                         const float *delta_bias, int delta_softplus, void *out,
                                         float *last_state, const ss_scan_options *options,
                                         ss_stream_t stream);
+
+/*
+ * ss_selective_state_update -- one step of the recurrence, for token-by-token
+ * inference (the recurrent mode of the reading notes and of the review's
+ * "selective SSM" form): with h the running state,
+ *     dt = Delta[b,d] + delta_bias[d];  dt = softplus(dt) if delta_softplus
+ *     h[b,d,n] = exp(dt * A[d,n]) * h[b,d,n] + dt * B[b,g,n] * x[b,d]    (Euler)
+ *     out[b,d] = (sum_n C[b,g,n] * h[b,d,n] + D[d] * x[b,d]) * SiLU(z[b,d])
+ * It equals ss_selective_scan_fwd over one step with h0 = state and
+ * last_state = state.
+ *
+ *   x, delta, z  [batch, dim]          io (z nullable)
+ *   A            [dim, dstate]         float
+ *   B, C         [batch, ngroups, dstate] io
+ *   D, delta_bias [dim]                float, nullable
+ *   state        [batch, dim, dstate]  float, read and overwritten in place
+ *   out          [batch, dim]          io
+ * flags: 0 or SS_SCAN_ZOH.  All pointers device, 16-byte aligned; out must
+ * not overlap the inputs or the state.  Asynchronous on `stream`.
+ */
+ss_status ss_selective_state_update(int64_t batch, int64_t dim, int dstate, int ngroups,
+                                    ss_dtype io, const void *x, const void *delta,
+                                    const float *A, const void *B, const void *C,
+                                    const float *D, const void *z, const float *delta_bias,
+                                    int delta_softplus, unsigned int flags, float *state,
+                                    void *out, ss_stream_t stream);
 
 /* Workspace bytes a call of the given kind and shape needs (0 if none), for
  * either I/O dtype (the larger of the two).  For SS_KIND_CROSS2D pass

@@ -19,7 +19,8 @@ import ctypes
 from . import _binding as _b
 from ._binding import SSError, load as load_library, version  # noqa: F401
 
-__all__ = ["selective_scan_fwd", "bidir_scan_fwd", "cross_scan2d_fwd", "device_status",
+__all__ = ["selective_scan_fwd", "bidir_scan_fwd", "cross_scan2d_fwd", "selective_state_update",
+           "device_status",
            "workspace_bytes", "SSError", "load_library", "version"]
 
 
@@ -69,14 +70,17 @@ def workspace_bytes(kind: int, batch: int, dim: int, seqlen: int, dstate: int, c
 
 
 def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-                       return_last_state=False, out=None, chunks=0, workspace=None, stream=None):
+                       return_last_state=False, out=None, chunks=0, workspace=None, stream=None,
+                       h0=None, zoh=False):
     """One-direction selective scan.
 
     u, delta, z: [batch, dim, L]; A: [dim, N] float32; B, C: [batch, G, N, L];
     D, delta_bias: [dim] float32.  Returns out [batch, dim, L] (and last_state
     [batch, dim, N] float32 if requested).  ``chunks`` forces the sequence split
     (0 automatic, 1 single pass, n >= 2 chunked path); ``workspace`` is an
-    optional preallocated uint8 CUDA tensor."""
+    optional preallocated uint8 CUDA tensor; ``h0`` [batch, dim, N] float32 is
+    the initial state (default zero); ``zoh`` selects the zero-order-hold input
+    matrix instead of the Euler one."""
     torch = _torch()
     lib = _b.load()
     batch, dim, L = u.shape
@@ -90,11 +94,12 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta
     _check_io("A", A, torch.float32, dev, (dim, N))
     _check_io("D", D, torch.float32, dev, (dim,))
     _check_io("delta_bias", delta_bias, torch.float32, dev, (dim,))
+    _check_io("h0", h0, torch.float32, dev, (batch, dim, N))
     if out is None:
         out = torch.empty_like(u)
     _check_io("out", out, io, dev, (batch, dim, L))
     last = torch.empty(batch, dim, N, dtype=torch.float32, device=dev) if return_last_state else None
-    opts = _b.options(chunks)
+    opts = _b.options(chunks, _b.SS_SCAN_ZOH if zoh else 0, _ptr(h0))
     wsb = int(lib.ss_workspace_bytes_opts(_b.SS_KIND_SCAN, batch, dim, L, N, ctypes.byref(opts)))
     if wsb and (workspace is None or workspace.numel() < wsb):
         workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
@@ -176,6 +181,37 @@ def cross_scan2d_fwd(u, delta, A, B, C, D=None, delta_bias=None, delta_softplus=
         _ptr(D), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(z), _ptr(out), _ptr(last),
         ws, wsb, _stream(stream, dev)))
     return (out, last) if return_last_state else out
+
+
+def selective_state_update(x, delta, A, B, C, state, D=None, z=None, delta_bias=None,
+                           delta_softplus=True, zoh=False, out=None, stream=None):
+    """One recurrence step for token-by-token inference, updating ``state`` in place.
+
+    x, delta, z: [batch, dim]; A: [dim, N] float32; B, C: [batch, G, N];
+    D, delta_bias: [dim] float32; state: [batch, dim, N] float32.  Returns out
+    [batch, dim]."""
+    torch = _torch()
+    lib = _b.load()
+    batch, dim = x.shape
+    G, N = B.shape[1], B.shape[2]
+    io, dev = x.dtype, x.device
+    _check_io("x", x, io, dev)
+    _check_io("delta", delta, io, dev, (batch, dim))
+    _check_io("B", B, io, dev, (batch, G, N))
+    _check_io("C", C, io, dev, (batch, G, N))
+    _check_io("z", z, io, dev, (batch, dim))
+    _check_io("A", A, torch.float32, dev, (dim, N))
+    _check_io("D", D, torch.float32, dev, (dim,))
+    _check_io("delta_bias", delta_bias, torch.float32, dev, (dim,))
+    _check_io("state", state, torch.float32, dev, (batch, dim, N))
+    if out is None:
+        out = torch.empty_like(x)
+    _check_io("out", out, io, dev, (batch, dim))
+    _b.check(lib.ss_selective_state_update(
+        batch, dim, N, G, _io_code(x), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+        _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _b.SS_SCAN_ZOH if zoh else 0,
+        _ptr(state), _ptr(out), _stream(stream, dev)))
+    return out
 
 
 def device_status(stream=None) -> None:

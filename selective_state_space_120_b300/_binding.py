@@ -34,7 +34,7 @@ EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_opts", "ss_bidir_scan
            "ss_cross_scan2d_fwd", "ss_workspace_bytes", "ss_workspace_bytes_opts",
            "ss_get_device_status", "ss_last_error_string", "ss_version",
            "ss_debug_set_wait_budget_ns", "ss_debug_set_flags",
-           "ss_selective_scan_fwd_noalloc")
+           "ss_selective_scan_fwd_noalloc", "ss_selective_state_update")
 
 
 class SSError(RuntimeError):
@@ -44,7 +44,11 @@ class SSError(RuntimeError):
 
 
 class ScanOptions(ctypes.Structure):
-    _fields_ = [("chunks", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
+    _fields_ = [("chunks", ctypes.c_int), ("flags", ctypes.c_uint), ("h0", ctypes.c_void_p),
+                ("reserved", ctypes.c_int * 4)]
+
+
+SS_SCAN_ZOH = 1
 
 
 _lock = threading.Lock()
@@ -67,13 +71,16 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ss_selective_scan_fwd.argtypes = scan_args + [vp]
         lib.ss_selective_scan_fwd_opts.argtypes = scan_args + [ctypes.POINTER(ScanOptions), vp]
         lib.ss_bidir_scan_fwd.argtypes = scan_args + [vp]
+        lib.ss_selective_state_update.argtypes = [i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                                  vp, vp, i32, ctypes.c_uint, vp, vp, vp]
         lib.ss_selective_scan_fwd_noalloc.argtypes = scan_args[:-2] + [
             ctypes.POINTER(ScanOptions), vp]
         lib.ss_cross_scan2d_fwd.argtypes = [i64, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp,
                                             vp, vp, i32, vp, vp, vp, vp, sz, vp]
         for f in ("ss_selective_scan_fwd", "ss_selective_scan_fwd_opts", "ss_bidir_scan_fwd",
                   "ss_cross_scan2d_fwd", "ss_get_device_status", "ss_debug_set_wait_budget_ns",
-                  "ss_debug_set_flags", "ss_selective_scan_fwd_noalloc"):
+                  "ss_debug_set_flags", "ss_selective_scan_fwd_noalloc",
+                  "ss_selective_state_update"):
             getattr(lib, f).restype = ctypes.c_int
         lib.ss_workspace_bytes.argtypes = [i32, i64, i64, i64, i32]
         lib.ss_workspace_bytes.restype = sz
@@ -102,9 +109,11 @@ def version() -> str:
     return load().ss_version().decode()
 
 
-def options(chunks: int = 0) -> ScanOptions:
+def options(chunks: int = 0, flags: int = 0, h0: int | None = None) -> ScanOptions:
     o = ScanOptions()
     o.chunks = int(chunks)
+    o.flags = int(flags)
+    o.h0 = h0
     return o
 
 

@@ -81,6 +81,26 @@ ss_status check_common(const char *fn, int64_t batch, int64_t dim, int64_t L, in
     return SS_OK;
 }
 
+// Options of the single-direction calls: reserved fields zero, known flags, a
+// 16-byte aligned initial state that does not overlap the output.
+ss_status check_options(const char *fn, const ss_scan_options *o, int64_t batch, int64_t dim,
+                        int dstate, const void *out, int io, int64_t L) {
+    if (!o) return SS_OK;
+    for (int r : o->reserved)
+        if (r != 0) return fail(SS_ERR_INVALID_ARG, "%s: reserved option fields must be zero", fn);
+    if (o->chunks < 0) return fail(SS_ERR_INVALID_ARG, "%s: options.chunks < 0", fn);
+    if (o->flags & ~SS_SCAN_ZOH)
+        return fail(SS_ERR_INVALID_ARG, "%s: unknown option flags 0x%x", fn, o->flags);
+    if (o->h0) {
+        if (!aligned16(o->h0)) return fail(SS_ERR_ALIGNMENT, "%s: options.h0 is not 16-byte aligned", fn);
+        const int64_t es = io == SS_BF16 ? 2 : 4;
+        const Span so{static_cast<const char *>(out), batch * dim * L * es};
+        const Span sh{reinterpret_cast<const char *>(o->h0), batch * dim * dstate * 4};
+        if (overlaps(so, sh)) return fail(SS_ERR_INVALID_ARG, "%s: out overlaps options.h0", fn);
+    }
+    return SS_OK;
+}
+
 // The merge accumulator of the multi-direction calls must not overlap any tensor.
 ss_status check_ws_overlap(const char *fn, const ScanArgs &a) {
     if (!a.ws || a.ws_bytes == 0) return SS_OK;
@@ -204,16 +224,16 @@ ss_status ss_selective_scan_fwd_opts(int64_t batch, int64_t dim, int64_t seqlen,
                                 D, z, delta_bias, out, last_state, &empty);
     if (st != SS_OK || empty) return st;
     int chunks = 0;
-    if (options) {
-        for (int r : options->reserved)
-            if (r != 0) return fail(SS_ERR_INVALID_ARG, "%s: reserved option fields must be zero", fn);
-        if (options->chunks < 0) return fail(SS_ERR_INVALID_ARG, "%s: options.chunks < 0", fn);
-        chunks = options->chunks;
-    }
+    if ((st = check_options(fn, options, batch, dim, dstate, out, io, seqlen))) return st;
+    if (options) chunks = options->chunks;
     ScanArgs a = scan_args(batch, dim, seqlen, dstate, ngroups, io, u, delta, A, B, C, D, z,
                            delta_bias, delta_softplus, out, last_state, workspace,
                            workspace_bytes, stream);
     a.chunks = chunks;
+    if (options) {
+        a.h0 = options->h0;
+        a.zoh = (options->flags & SS_SCAN_ZOH) ? 1 : 0;
+    }
     if ((st = check_workspace(fn, scan1d_workspace_bytes(a), workspace, workspace_bytes))) return st;
     return launch_scan1d(a);
 }
@@ -242,15 +262,15 @@ ss_status ss_selective_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t seql
                                 D, z, delta_bias, out, last_state, &empty);
     if (st != SS_OK || empty) return st;
     int chunks = 0;
-    if (options) {
-        for (int r : options->reserved)
-            if (r != 0) return fail(SS_ERR_INVALID_ARG, "%s: reserved option fields must be zero", fn);
-        if (options->chunks < 0) return fail(SS_ERR_INVALID_ARG, "%s: options.chunks < 0", fn);
-        chunks = options->chunks;
-    }
+    if ((st = check_options(fn, options, batch, dim, dstate, out, io, seqlen))) return st;
+    if (options) chunks = options->chunks;
     ScanArgs a = scan_args(batch, dim, seqlen, dstate, ngroups, io, u, delta, A, B, C, D, z,
                            delta_bias, delta_softplus, out, last_state, nullptr, 0, stream);
     a.chunks = chunks;
+    if (options) {
+        a.h0 = options->h0;
+        a.zoh = (options->flags & SS_SCAN_ZOH) ? 1 : 0;
+    }
     const size_t need = scan1d_workspace_bytes(a);
     if (need > SS_NOALLOC_SCRATCH_BYTES)
         return fail(SS_ERR_UNSUPPORTED,
@@ -316,6 +336,26 @@ ss_status ss_cross_scan2d_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, 
     if ((st = check_workspace(fn, multidir_workspace_bytes(a), workspace, workspace_bytes))) return st;
     if ((st = check_ws_overlap(fn, a))) return st;
     return launch_multidir(a);
+}
+
+ss_status ss_selective_state_update(int64_t batch, int64_t dim, int dstate, int ngroups,
+                                    ss_dtype io, const void *x, const void *delta,
+                                    const float *A, const void *B, const void *C,
+                                    const float *D, const void *z, const float *delta_bias,
+                                    int delta_softplus, unsigned int flags, float *state,
+                                    void *out, ss_stream_t stream) {
+    static const char *fn = "ss_selective_state_update";
+    bool empty = false;
+    if (flags & ~SS_SCAN_ZOH) return fail(SS_ERR_INVALID_ARG, "%s: unknown flags 0x%x", fn, flags);
+    ss_status st = check_common(fn, batch, dim, 1, dstate, ngroups, io, 1, x, delta, A, B, C, D, z,
+                                delta_bias, out, state, &empty);
+    if (st != SS_OK || empty) return st;
+    if (!state) return fail(SS_ERR_INVALID_ARG, "%s: state is required", fn);
+    if (!aligned16(state)) return fail(SS_ERR_ALIGNMENT, "%s: state is not 16-byte aligned", fn);
+    ScanArgs a = scan_args(batch, dim, 1, dstate, ngroups, io, x, delta, A, B, C, D, z, delta_bias,
+                           delta_softplus, out, nullptr, nullptr, 0, stream);
+    a.zoh = (flags & SS_SCAN_ZOH) ? 1 : 0;
+    return launch_step(a, state);
 }
 
 size_t ss_workspace_bytes_opts(int kind, int64_t batch, int64_t dim, int64_t seqlen, int dstate,

@@ -24,6 +24,8 @@ struct ScanArgs {
     size_t ws_bytes = 0;
     int orders[4] = {0, 1, 2, 3};
     int chunks = 0;  // single direction: 0 automatic, 1 direct, >= 2 chunked with that many L-chunks
+    const float *h0 = nullptr;  // single direction: initial state [batch, dim, N] (nullable)
+    int zoh = 0;                // single direction: zero-order-hold input matrix
     ss_stream_t stream = nullptr;
 };
 
@@ -42,6 +44,8 @@ size_t scan1d_workspace_bytes(const ScanArgs &a);
 size_t multidir_workspace_bytes(const ScanArgs &a);
 
 ss_status launch_scan1d(const ScanArgs &a);
+// One recurrence step (seqlen 1) updating `state` [batch*dim, N] in place.
+ss_status launch_step(const ScanArgs &a, float *state);
 ss_status launch_multidir(const ScanArgs &a);
 ss_status read_device_status(ss_stream_t stream);
 ss_status set_wait_budget(unsigned long long ns);

@@ -11,6 +11,7 @@
 #include "ss_internal.h"
 #include "ss_multidir.cuh"
 #include "ss_scan1d.cuh"
+#include "ss_step.cuh"
 
 namespace ssi {
 
@@ -109,6 +110,8 @@ struct Scan1d {
         p.bias = a.bias;
         p.softplus = a.softplus;
         p.has_z = a.z != nullptr;
+        p.zoh = a.zoh;
+        p.h0 = a.h0;
         p.out = a.out;
         p.last_state = a.last_state;
         const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);
@@ -328,6 +331,8 @@ ss_status run_multi(const ScanArgs &a) {
     p.bias = a.bias;
     p.softplus = a.softplus;
     p.out = a.out;
+    p.zoh = a.zoh;
+    p.h0 = a.h0;
     p.last_state = a.last_state;
     const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(a.stream);
@@ -448,6 +453,46 @@ ss_status launch_multidir(const ScanArgs &a) {
     if (multidir_workspace_bytes(a) > 0)
         return a.io == SS_BF16 ? dispatch_dirs_n<__nv_bfloat16>(a) : dispatch_dirs_n<float>(a);
     return a.io == SS_BF16 ? dispatch_multi<__nv_bfloat16>(a) : dispatch_multi<float>(a);
+}
+
+namespace {
+template <typename IO>
+ss_status launch_step_io(const ScanArgs &a, float *state) {
+    ssk::StepParams p{};
+    p.rows = a.batch * a.dim;
+    p.dim = a.dim;
+    p.G = a.G;
+    p.dpg = (int)(a.dim / a.G);
+    p.x = a.u;
+    p.delta = a.delta;
+    p.B = a.B;
+    p.C = a.C;
+    p.z = a.z;
+    p.A = a.A;
+    p.D = a.D;
+    p.bias = a.bias;
+    p.softplus = a.softplus;
+    p.zoh = a.zoh;
+    p.state = state;
+    p.out = a.out;
+    const unsigned blocks = (unsigned)((p.rows + 127) / 128);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(a.stream);
+    switch (a.N) {
+    case 1: ssk::k_step<IO, 1><<<blocks, 128, 0, s>>>(p); break;
+    case 2: ssk::k_step<IO, 2><<<blocks, 128, 0, s>>>(p); break;
+    case 4: ssk::k_step<IO, 4><<<blocks, 128, 0, s>>>(p); break;
+    case 8: ssk::k_step<IO, 8><<<blocks, 128, 0, s>>>(p); break;
+    case 16: ssk::k_step<IO, 16><<<blocks, 128, 0, s>>>(p); break;
+    case 32: ssk::k_step<IO, 32><<<blocks, 128, 0, s>>>(p); break;
+    case 64: ssk::k_step<IO, 64><<<blocks, 128, 0, s>>>(p); break;
+    default: return fail(SS_ERR_UNSUPPORTED, "dstate %d is not one of 1,2,4,8,16,32,64", a.N);
+    }
+    return check_launch("state update");
+}
+}  // namespace
+
+ss_status launch_step(const ScanArgs &a, float *state) {
+    return a.io == SS_BF16 ? launch_step_io<__nv_bfloat16>(a, state) : launch_step_io<float>(a, state);
 }
 
 ss_status read_device_status(ss_stream_t stream) {

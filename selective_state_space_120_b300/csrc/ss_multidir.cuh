@@ -68,6 +68,8 @@ struct MultiParams {
     const void *u, *delta, *B, *C, *z;
     const float *A, *D, *bias;
     int softplus;
+    int zoh;            // single direction only: zero-order-hold input matrix
+    const float *h0;    // single direction only: initial state [batch*dim, N]
     void *out;
     float *last_state;
 };
@@ -102,12 +104,15 @@ __global__ void __launch_bounds__(C::THREADS) k_multidir(const MultiParams p) {
 
     float2 A2p[1][NPT];
     float h[1][NPT];
+    float iAv[NPT];  // 1/A (0 where A = 0), for the zero-order hold
 #pragma unroll
     for (int j = 0; j < NPT; ++j) {
-        const float a = __ldg(p.A + ((int64_t)k * p.dim + d) * N + g * NPT + j) * kLog2e;
-        A2p[0][j] = make_float2(a, a);
-        h[0][j] = 0.f;
+        const float araw = __ldg(p.A + ((int64_t)k * p.dim + d) * N + g * NPT + j);
+        A2p[0][j] = make_float2(araw * kLog2e, araw * kLog2e);
+        iAv[j] = araw != 0.f ? 1.f / araw : 0.f;
+        h[0][j] = (K == 1 && p.h0) ? __ldg(p.h0 + ((int64_t)b * p.dim + d) * N + g * NPT + j) : 0.f;
     }
+    const bool zoh = K == 1 && p.zoh;
     const float bk = p.bias ? __ldg(p.bias + (int64_t)k * p.dim + d) : 0.f;
 
     float *acc = reinterpret_cast<float *>(smem);
@@ -168,7 +173,7 @@ __global__ void __launch_bounds__(C::THREADS) k_multidir(const MultiParams p) {
                 if (p.softplus) v = softplus(v);
                 if ((int64_t)i * T + E * g + e + q >= L) v = 0.f;
                 dlv[q] = v;
-                xv[q] = v * ru[e + q];
+                xv[q] = zoh ? ru[e + q] : v * ru[e + q];
             }
             dxrow[swz_slot((E * g + e) >> 1)] = make_float4(dlv[0], dlv[1], xv[0], xv[1]);
         }
@@ -194,7 +199,7 @@ __global__ void __launch_bounds__(C::THREADS) k_multidir(const MultiParams p) {
                 else
                     atomicAdd(my_acc + pos, y);
             }
-        });
+        }, zoh ? iAv : nullptr);
     }
     __syncthreads();
 

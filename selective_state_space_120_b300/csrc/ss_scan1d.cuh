@@ -124,6 +124,8 @@ struct Scan1dParams {
     const void *u_g, *z_g;  // u and z for the gathers of the column orders
     const float *A, *D, *bias;
     int softplus, has_z;
+    int zoh;                // zero-order-hold input matrix (single direction)
+    const float *h0;        // initial state [batch*dim, N] (single direction; nullable)
     void *out;
     float *last_state;      // [batch, K, dim, N]
     float *hend;          // [rows, J, N] end state of an L-chunk scanned from zero
@@ -326,7 +328,7 @@ struct StepRegs {
 template <class C, bool DO_Y>
 __device__ __forceinline__ void stage_step(StepRegs<C> &r, const float4 *const (&dxrow)[C::CL],
                                            const float *bc, int g, int tp,
-                                           const float2 (&A2p)[C::CL][C::NPT]) {
+                                           const float2 (&A2p)[C::CL][C::NPT], const float *iA) {
     constexpr int NPT = C::NPT, N = C::N, CL = C::CL;
     float Bv[2 * NPT];
     if constexpr (C::BCW) {
@@ -393,6 +395,23 @@ __device__ __forceinline__ void stage_step(StepRegs<C> &r, const float4 *const (
             r.a[c][j][0] = ex2(da.x);
             r.a[c][j][1] = ex2(da.y);
             r.bx[c][j] = __fmul2_rn(xx, make_float2(Bv[2 * j], Bv[2 * j + 1]));
+            if (iA) {
+                // zero-order hold: Bbar*u = (exp(x) - 1)/A * B*u with x = Delta'*A
+                // (the slots hold u, not Delta'*u).  For |x| < 1/16 use
+                // Delta' * expm1(x)/x = Delta' (1 + x/2 + x^2/6 + x^3/24), whose
+                // truncation error x^4/120 < 1.3e-7 avoids the cancellation of
+                // exp(x) - 1; otherwise (exp(x) - 1) * (1/A).
+                const float ia = iA[c * NPT + j];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const float x = (q ? da.y : da.x) * kLn2;
+                    const float dlt = q ? dl.y : dl.x;
+                    const float series = dlt * fmaf(x, fmaf(x, fmaf(x, 1.f / 24.f, 1.f / 6.f), 0.5f), 1.f);
+                    const float coef = fabsf(x) < 0.0625f ? series : (r.a[c][j][q] - 1.f) * ia;
+                    if (q) r.bx[c][j].y *= coef;
+                    else r.bx[c][j].x *= coef;
+                }
+            }
         }
     }
 }
@@ -403,17 +422,18 @@ __device__ __forceinline__ void stage_step(StepRegs<C> &r, const float4 *const (
 template <class C, bool DO_Y, class Emit>
 __device__ __forceinline__ void scan_chunk_pipe(const float4 *const (&dxrow)[C::CL], const float *bc,
                                                 int g, float (&h)[C::CL][C::NPT],
-                                                const float2 (&A2p)[C::CL][C::NPT], Emit &&emit) {
+                                                const float2 (&A2p)[C::CL][C::NPT], Emit &&emit,
+                                                const float *iA = nullptr) {
     constexpr int R = C::R, NPT = C::NPT, CL = C::CL;
     constexpr int BS = R >= 2 ? R : 2;  // steps per readout block
     constexpr int PPB = BS / 2;
     StepRegs<C> cur, nxt;
-    stage_step<C, DO_Y>(nxt, dxrow, bc, g, 0, A2p);
+    stage_step<C, DO_Y>(nxt, dxrow, bc, g, 0, A2p, iA);
     float v[CL][BS];
 #pragma unroll
     for (int tp = 0; tp < C::TP; ++tp) {
         cur = nxt;
-        if (tp + 1 < C::TP) stage_step<C, DO_Y>(nxt, dxrow, bc, g, tp + 1, A2p);
+        if (tp + 1 < C::TP) stage_step<C, DO_Y>(nxt, dxrow, bc, g, tp + 1, A2p, iA);
         const int pp = tp % PPB;
 #pragma unroll
         for (int c = 0; c < CL; ++c) {
@@ -617,6 +637,7 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
     int64_t rows[CL];
     float2 A2p[CL][NPT];
     float h[CL][NPT];
+    float iAv[CL * NPT];  // 1/A (0 where A = 0), for the zero-order hold
 #pragma unroll
     for (int c = 0; c < CL; ++c) {
         chs[c] = warp * C::CHW + q * CL + c;
@@ -627,9 +648,12 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
 #pragma unroll
         for (int j = 0; j < NPT; ++j) {
             const int n = g * NPT + j;
-            const float a = __ldg(p.A + ((int64_t)p.k * p.dim + d) * N + n) * kLog2e;
+            const float araw = __ldg(p.A + ((int64_t)p.k * p.dim + d) * N + n);
+            const float a = araw * kLog2e;
             A2p[c][j] = make_float2(a, a);
-            h[c][j] = (p.pass == 2) ? __ldg(p.carry + (rows[c] * p.J + jc) * N + n) : 0.f;
+            iAv[c * NPT + j] = araw != 0.f ? 1.f / araw : 0.f;
+            h[c][j] = (p.pass == 2) ? __ldg(p.carry + (rows[c] * p.J + jc) * N + n)
+                      : (p.h0 && jc == 0) ? __ldg(p.h0 + rows[c] * N + n) : 0.f;
         }
     }
     // prep role: E consecutive steps of channel pch, starting at step pt0 of the chunk
@@ -642,6 +666,7 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
     const float bd = p.bias ? __ldg(p.bias + (int64_t)p.k * p.dim + pd) : 0.f;
     const int64_t prow = (int64_t)b * p.dim + pd;  // u/z row of the prep channel
 
+    const float *zoh_iA = (!MULTI && p.zoh) ? iAv : nullptr;
     float *bcbuf0 = reinterpret_cast<float *>(smem + C::OFF_BC);
     uint8_t *obrows[CL];
 #pragma unroll
@@ -766,7 +791,7 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
                 if (p.softplus) v = softplus(v);
                 if (e + k >= lim) v = 0.f;
                 dl[k] = v;
-                xx[k] = v * uu[e + k];
+                xx[k] = (!MULTI && p.zoh) ? uu[e + k] : v * uu[e + k];
                 ga[k] = gate_in_prep ? silu(zz[e + k]) : 1.f;
                 du[k] = Dd * uu[e + k] * ga[k];
                 if (p.pass == 1) sdt_acc += v;
@@ -845,8 +870,8 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
             else reinterpret_cast<float *>(obrows[c])[t] = v;
         };
         if constexpr (C::PIPE) {
-            if (do_y) scan_chunk_pipe<C, true>(dxrows, bc, g, h, A2p, emit);
-            else scan_chunk_pipe<C, false>(dxrows, bc, g, h, A2p, [](int, float, int) {});
+            if (do_y) scan_chunk_pipe<C, true>(dxrows, bc, g, h, A2p, emit, zoh_iA);
+            else scan_chunk_pipe<C, false>(dxrows, bc, g, h, A2p, [](int, float, int) {}, zoh_iA);
         } else {
             if (do_y) scan_chunk_cl<C, true>(dxrows, bc, g, h, A2p, emit);
             else scan_chunk_cl<C, false>(dxrows, bc, g, h, A2p, [](int, float, int) {});

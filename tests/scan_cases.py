@@ -49,7 +49,7 @@ def workload(name, batch, dim, L, N=16, G=1, K=1, io="bf16", with_z=True, with_D
                        last_state=True, H=H, W=W)
 
 
-def oracle_run(oracle, inp, rows=None):
+def oracle_run(oracle, inp, rows=None, h0=None, zoh=False):
     """Oracle output for the whole workload, or for a list of (b, d) rows.
     Returns (out [batch | len(rows), dim | -, L], last [.., K, .., N])."""
     wl = inp.wl
@@ -60,7 +60,8 @@ def oracle_run(oracle, inp, rows=None):
               4: oracle.SS2D_ORDERS}[K]
     H, W = (wl.H, wl.W) if K == 4 else (1, wl.L)
     if rows is None:
-        return oracle.scan(u, dl, A, B, C, D, z, bias, True, orders, H=H, W=W)
+        return oracle.scan(u, dl, A, B, C, D, z, bias, True, orders, H=H, W=W, zoh=zoh,
+                           h0=None if h0 is None else np.asarray(h0, np.float64)[:, None])
     outs, lasts = [], []
     dpg = wl.dim // wl.G
     for (b, d) in rows:
@@ -81,7 +82,7 @@ def device_inputs(inp):
                                                    "delta_bias")}
 
 
-def gpu_run(inp, chunks=0, t=None):
+def gpu_run(inp, chunks=0, t=None, h0=None, zoh=False):
     """Runs the library on the workload; returns (out, last_state) as torch tensors."""
     import selective_state_space_120_b300 as ss
     wl = inp.wl
@@ -89,7 +90,8 @@ def gpu_run(inp, chunks=0, t=None):
     if wl.K == 1:
         return ss.selective_scan_fwd(t["u"], t["delta"][:, 0], t["A"], t["B"][:, 0], t["C"][:, 0],
                                      t["D"], t["z"], t["delta_bias"], True,
-                                     return_last_state=True, chunks=chunks)
+                                     return_last_state=True, chunks=chunks,
+                                     h0=None if h0 is None else to_torch(h0), zoh=zoh)
     if wl.K == 2:
         return ss.bidir_scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
                                  t["delta_bias"], True, return_last_state=True)

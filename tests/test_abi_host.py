@@ -151,6 +151,34 @@ def test_bidir_and_cross2d_validate(lib):
 
 
 @fake_ptrs
+def test_scan_options_are_validated(lib):
+    base = (1, 8, 32, 16, 1, b.SS_BF16, A16, A16 + 0x100000, A16 + 0x200000, A16 + 0x300000,
+            A16 + 0x400000, None, None, None, 1, A16 + 0x500000, None, None, 0)
+    bad_flag = b.options(flags=4)
+    assert lib.ss_selective_scan_fwd_opts(*base, ctypes.byref(bad_flag), None) == b.SS_ERR_INVALID_ARG
+    assert "flags" in b.last_error()
+    bad_h0 = b.options(h0=A16 + 0x600004)
+    assert lib.ss_selective_scan_fwd_opts(*base, ctypes.byref(bad_h0), None) == b.SS_ERR_ALIGNMENT
+    h0_on_out = b.options(h0=A16 + 0x500000)
+    assert lib.ss_selective_scan_fwd_opts(*base, ctypes.byref(h0_on_out), None) == b.SS_ERR_INVALID_ARG
+    assert ctypes.sizeof(b.ScanOptions) == 32
+
+
+@fake_ptrs
+def test_state_update_validates(lib):
+    args = [2, 8, 16, 1, b.SS_BF16, A16, A16 + 0x1000, A16 + 0x2000, A16 + 0x3000, A16 + 0x4000,
+            None, None, None, 1, 0, A16 + 0x5000, A16 + 0x6000, None]
+    bad = list(args); bad[15] = None           # no state
+    assert lib.ss_selective_state_update(*bad) == b.SS_ERR_INVALID_ARG
+    bad = list(args); bad[15] = A16 + 0x5004   # misaligned state
+    assert lib.ss_selective_state_update(*bad) == b.SS_ERR_ALIGNMENT
+    bad = list(args); bad[14] = 2              # unknown flag
+    assert lib.ss_selective_state_update(*bad) == b.SS_ERR_INVALID_ARG
+    bad = list(args); bad[2] = 12              # unsupported dstate
+    assert lib.ss_selective_state_update(*bad) == b.SS_ERR_UNSUPPORTED
+
+
+@fake_ptrs
 def test_debug_flags_reject_unknown_bits(lib):
     assert lib.ss_debug_set_flags(2) == b.SS_ERR_INVALID_ARG
     assert "unknown flag" in b.last_error()

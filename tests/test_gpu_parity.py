@@ -151,6 +151,132 @@ def test_timeout_path_reports_and_recovers(oracle):
     ss.device_status()
 
 
+# ---------------------------------------------------------------- options: h0, ZOH
+def _h0(wl, seed=11):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((wl.batch, wl.dim, wl.N)) * 0.5).astype(np.float32)
+
+
+@pytest.mark.parametrize("chunks", [1, 3])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_initial_state(oracle, chunks, io):
+    """A given initial state, on the direct and the chunked path (TMA rows)."""
+    wl = sc.workload("h0", 2, 40, 1024, io=io)
+    inp = wk.make_inputs(wl)
+    h0 = _h0(wl)
+    out, last = sc.gpu_run(inp, chunks=chunks, h0=h0)
+    ref, ref_last = sc.oracle_run(oracle, inp, h0=h0)
+    sc.assert_close(sc.from_torch(out), ref, io)
+    sc.assert_close(last.cpu().numpy(), ref_last[:, 0], io, "last_state")
+
+
+def test_initial_state_unaligned_rows(oracle):
+    wl = sc.workload("h0u", 2, 24, 77)
+    inp = wk.make_inputs(wl)
+    h0 = _h0(wl)
+    out, last = sc.gpu_run(inp, h0=h0)
+    ref, ref_last = sc.oracle_run(oracle, inp, h0=h0)
+    sc.assert_close(sc.from_torch(out), ref, "bf16")
+    sc.assert_close(last.cpu().numpy(), ref_last[:, 0], "bf16", "last_state")
+
+
+def test_continuing_a_sequence_across_calls():
+    """Scanning L1 steps, then L2 steps from the first call's last_state, gives
+    the output and final state of one scan over L1 + L2 steps (fp32 I/O)."""
+    import torch
+    import selective_state_space_120_b300 as ss
+    wl = sc.workload("split", 2, 32, 1024, io="f32")
+    inp = wk.make_inputs(wl)
+    t = sc.device_inputs(inp)
+    full, last_full = sc.gpu_run(inp, t=t)
+    cut = 512
+    parts = {k: (None if v is None else v) for k, v in t.items()}
+    def piece(a, lo, hi):
+        return None if a is None else a[..., lo:hi].contiguous()
+    o1, l1 = ss.selective_scan_fwd(piece(parts["u"], 0, cut), piece(parts["delta"][:, 0], 0, cut),
+                                   parts["A"], piece(parts["B"][:, 0], 0, cut),
+                                   piece(parts["C"][:, 0], 0, cut), parts["D"],
+                                   piece(parts["z"], 0, cut), parts["delta_bias"], True,
+                                   return_last_state=True)
+    o2, l2 = ss.selective_scan_fwd(piece(parts["u"], cut, None), piece(parts["delta"][:, 0], cut, None),
+                                   parts["A"], piece(parts["B"][:, 0], cut, None),
+                                   piece(parts["C"][:, 0], cut, None), parts["D"],
+                                   piece(parts["z"], cut, None), parts["delta_bias"], True,
+                                   return_last_state=True, h0=l1)
+    torch.cuda.synchronize()
+    got = torch.cat([o1, o2], dim=-1)
+    assert sc.rel_err(got.cpu().numpy(), full.cpu().numpy()) < 2e-5
+    assert sc.rel_err(l2.cpu().numpy(), last_full.cpu().numpy()) < 2e-5
+
+
+@pytest.mark.parametrize("chunks", [1, 4])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_zero_order_hold(oracle, chunks, io):
+    """SS_SCAN_ZOH: Bbar = (exp(Delta A) - 1)/A * B, against the oracle's ZOH."""
+    wl = sc.workload("zoh", 2, 36, 1024, io=io)
+    inp = wk.make_inputs(wl)
+    out, last = sc.gpu_run(inp, chunks=chunks, zoh=True)
+    ref, ref_last = sc.oracle_run(oracle, inp, zoh=True)
+    sc.assert_close(sc.from_torch(out), ref, io)
+    sc.assert_close(last.cpu().numpy(), ref_last[:, 0], io, "last_state")
+
+
+def test_zero_order_hold_large_steps_and_unaligned_rows(oracle):
+    """Large Delta (|Delta A| well above the series threshold) and rows the TMA
+    path does not take."""
+    wl = sc.workload("zohu", 1, 24, 61, io="f32")
+    inp = wk.make_inputs(wl)
+    inp.delta_bias[:] = 1.5  # Delta' ~ 1.7: exp(Delta A) far from 1 for every state
+    out, last = sc.gpu_run(inp, zoh=True)
+    ref, ref_last = sc.oracle_run(oracle, inp, zoh=True)
+    sc.assert_close(sc.from_torch(out), ref, "f32")
+    sc.assert_close(last.cpu().numpy(), ref_last[:, 0], "f32", "last_state")
+
+
+# ---------------------------------------------------------------- single-step decode
+@pytest.mark.parametrize("N", [1, 4, 16, 64])
+@pytest.mark.parametrize("io,zoh", [("f32", False), ("bf16", False), ("f32", True)])
+def test_state_update_one_step(oracle, N, io, zoh):
+    """One decode step from a random state equals the oracle over one step with
+    h0 = state; the state is updated in place."""
+    import torch
+    import selective_state_space_120_b300 as ss
+    wl = sc.workload("step", 3, 40, 1, N=N, G=2, io=io)
+    inp = wk.make_inputs(wl)
+    h0 = _h0(wl)
+    t = sc.device_inputs(inp)
+    state = sc.to_torch(h0).clone()
+    out = ss.selective_state_update(t["u"][:, :, 0].contiguous(), t["delta"][:, 0, :, 0].contiguous(),
+                                    t["A"], t["B"][:, 0, :, :, 0].contiguous(),
+                                    t["C"][:, 0, :, :, 0].contiguous(), state, t["D"],
+                                    t["z"][:, :, 0].contiguous(), t["delta_bias"], True, zoh=zoh)
+    torch.cuda.synchronize()
+    ref, ref_last = sc.oracle_run(oracle, inp, h0=h0, zoh=zoh)
+    sc.assert_close(sc.from_torch(out), ref[:, :, 0], io)
+    sc.assert_close(state.cpu().numpy(), ref_last[:, 0], io, "state")
+
+
+def test_state_update_chain_equals_scan():
+    """T decode steps from a zero state reproduce the scan over T steps (fp32)."""
+    import torch
+    import selective_state_space_120_b300 as ss
+    wl = sc.workload("chain", 2, 24, 40, io="f32")
+    inp = wk.make_inputs(wl)
+    t = sc.device_inputs(inp)
+    full, last = sc.gpu_run(inp, t=t)
+    state = torch.zeros(wl.batch, wl.dim, wl.N, device="cuda")
+    outs = []
+    for k in range(wl.L):
+        outs.append(ss.selective_state_update(
+            t["u"][:, :, k].contiguous(), t["delta"][:, 0, :, k].contiguous(), t["A"],
+            t["B"][:, 0, :, :, k].contiguous(), t["C"][:, 0, :, :, k].contiguous(), state, t["D"],
+            t["z"][:, :, k].contiguous(), t["delta_bias"], True))
+    torch.cuda.synchronize()
+    got = torch.stack(outs, dim=-1)
+    assert sc.rel_err(got.cpu().numpy(), full.cpu().numpy()) < 2e-5
+    assert sc.rel_err(state.cpu().numpy(), last.cpu().numpy()) < 2e-5
+
+
 # ---------------------------------------------------------------- bidirectional
 @pytest.mark.parametrize("L", [1, 7, 33, 197, 256])
 @pytest.mark.parametrize("io", ["f32", "bf16"])
