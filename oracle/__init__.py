@@ -55,6 +55,8 @@ def _bind(path: str):
                               ctypes.POINTER(ctypes.c_int),
                               dp, dp, dp, dp, dp, dp, dp, dp,
                               ctypes.c_int, ctypes.c_int, dp, dp, dp, dp]
+    lib.ssor_conv_silu.restype = ctypes.c_int
+    lib.ssor_conv_silu.argtypes = [i64, i64, i64, i64, dp, dp, dp, dp, dp]
     lib.ssor_softplus_scalar.restype = ctypes.c_double
     lib.ssor_softplus_scalar.argtypes = [ctypes.c_double]
     lib.ssor_position_of.restype = ctypes.c_int64
@@ -169,6 +171,23 @@ def cross_scan2d(u, delta, A, B, C, H, W, D=None, z=None, delta_bias=None, delta
     out, last = scan(u.reshape(batch, dim, L), delta, A, B, C, D, zz, delta_bias, delta_softplus,
                      SS2D_ORDERS, H=H, W=W)
     return out.reshape(batch, dim, H, W), last
+
+
+def conv_silu(x, w, bias=None, x0=None):
+    """The Mamba block's Conv1D -> SiLU before the scan: x [batch, dim, L],
+    w [dim, KW], bias [dim], x0 [batch, dim, KW-1] (inputs before the
+    sequence, oldest first; default zeros).  Returns u [batch, dim, L] float64."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    batch, dim, L = x.shape
+    w = _f64(w, (dim, np.asarray(w).shape[-1]), "w")
+    KW = w.shape[1]
+    bias = _f64(bias, (dim,), "bias")
+    x0 = _f64(x0, (batch, dim, KW - 1), "x0")
+    u = np.empty_like(x)
+    rc = _load().ssor_conv_silu(batch, dim, L, KW, _ptr(x), _ptr(w), _ptr(bias), _ptr(x0), _ptr(u))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return u
 
 
 def softplus(x: float) -> float:

@@ -152,6 +152,40 @@ int ssor_scan(int64_t batch, int64_t dim, int64_t H, int64_t W, int64_t N, int64
     return 0;
 }
 
+/*
+ * ssor_conv_silu: the Mamba block's input branch before the scan ("Mamba
+ * Series ...", block diagram "Mamba Block (1D)": Conv1D(k=4) -> SiLU -> SSM):
+ * a causal depthwise convolution of width KW along the sequence, plus a bias,
+ * then SiLU:
+ *     v = bias[d] + sum_{j=0..KW-1} w[d, j] * x[b, d, t - (KW-1) + j]
+ *     u[b, d, t] = v * sigmoid(v)
+ * Steps before the sequence read x0[b, d, 0..KW-2] (the KW-1 inputs that came
+ * before it, oldest first), or zeros when x0 is NULL.
+ *   x, u [batch, dim, L]; w [dim, KW]; bias [dim] (NULL: 0).  Returns 0 or -1.
+ */
+int ssor_conv_silu(int64_t batch, int64_t dim, int64_t L, int64_t KW, const double *x,
+                   const double *w, const double *bias, const double *x0, double *u) {
+    if (batch < 0 || dim <= 0 || L < 0 || KW <= 0 || !x || !w || !u) return -1;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const double *xr = x + (b * dim + d) * L;
+            const double *x0r = x0 ? x0 + (b * dim + d) * (KW - 1) : NULL;
+            for (int64_t t = 0; t < L; ++t) {
+                double v = bias ? bias[d] : 0.0;
+                for (int64_t j = 0; j < KW; ++j) {
+                    const int64_t s = t - (KW - 1) + j;   /* input step */
+                    double xv;
+                    if (s >= 0) xv = xr[s];
+                    else xv = x0r ? x0r[(KW - 1) + s] : 0.0;
+                    v += w[d * KW + j] * xv;
+                }
+                u[(b * dim + d) * L + t] = v / (1.0 + exp(-v));
+            }
+        }
+    }
+    return 0;
+}
+
 /* Exposed for the oracle's own pin tests: the softplus used above. */
 double ssor_softplus_scalar(double x) { return ssor_softplus(x); }
 

@@ -34,6 +34,9 @@ MUTANTS = {
                               "bbar = (abar - 1.0) * a * B_grp[n * L + s];"),
     "delta_by_position": ("double dt = dl_row[s] + bd;", "double dt = dl_row[p] + bd;"),
     "B_by_position": ("bbar = dt * B_grp[n * L + s];", "bbar = dt * B_grp[n * L + p];"),
+    "conv_kernel_reversed": ("v += w[d * KW + j] * xv;", "v += w[d * KW + (KW - 1 - j)] * xv;"),
+    "conv_history_off_by_one": ("else xv = x0r ? x0r[(KW - 1) + s] : 0.0;",
+                                "else xv = x0r ? x0r[(KW - 2) + s] : 0.0;"),
     "group_map_interleaved": ("const int64_t g = d / dpg;", "const int64_t g = d % ngroups;"),
     "ignores_initial_state": ("h[n] = h0 ? h0[((b * K + k) * dim + d) * N + n] : 0.0;",
                               "h[n] = 0.0;"),
@@ -63,6 +66,20 @@ class _Variant:
     def bidir_scan(self, u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True):
         return self.scan(u, delta, A, B, C, D, z, delta_bias, delta_softplus,
                          (self.ORDER_FWD, self.ORDER_REV))
+
+    def conv_silu(self, x, w, bias=None, x0=None):
+        x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+        batch, dim, L = x.shape
+        w = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
+        KW = w.shape[1]
+        bias = None if bias is None else np.ascontiguousarray(np.asarray(bias, dtype=np.float64))
+        x0 = None if x0 is None else np.ascontiguousarray(np.asarray(x0, dtype=np.float64))
+        u = np.empty_like(x)
+        rc = self.lib.ssor_conv_silu(batch, dim, L, KW, _oracle._ptr(x), _oracle._ptr(w),
+                                     _oracle._ptr(bias), _oracle._ptr(x0), _oracle._ptr(u))
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+        return u
 
     def softplus(self, x):
         return self.lib.ssor_softplus_scalar(float(x))

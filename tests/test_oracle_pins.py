@@ -328,3 +328,44 @@ def test_group_mapping_contiguous_blocks(oracle):
     out2, _ = oracle.scan(u, delta, A, B2, C, D, z, bias, True)
     np.testing.assert_array_equal(out2[:, :2], out[:, :2])
     assert np.all(out2[:, 2:] != out[:, 2:])
+
+
+# ---------------------------------------------------------------- Conv1D -> SiLU (Mamba block input branch)
+def test_conv_silu_identity_kernel_is_silu(oracle):
+    """Kernel [0, 0, 0, 1] with no bias passes x through: u = SiLU(x)."""
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((2, 3, 17))
+    w = np.tile([0.0, 0.0, 0.0, 1.0], (3, 1))
+    np.testing.assert_allclose(oracle.conv_silu(x, w), _silu(x), rtol=1e-15, atol=0)
+
+
+def test_conv_silu_equals_numpy_correlation(oracle):
+    """Causal width-4 convolution against np.convolve of the zero-padded row."""
+    rng = np.random.default_rng(22)
+    batch, dim, L = 2, 3, 29
+    x = rng.standard_normal((batch, dim, L))
+    w = rng.standard_normal((dim, 4))
+    bias = rng.standard_normal(dim)
+    got = oracle.conv_silu(x, w, bias)
+    for b in range(batch):
+        for d in range(dim):
+            padded = np.concatenate([np.zeros(3), x[b, d]])
+            # out[t] = sum_j w[j] x[t - 3 + j]: a 'valid' correlation, i.e. a
+            # convolution with the flipped kernel
+            v = np.convolve(padded, w[d][::-1], mode="valid") + bias[d]
+            np.testing.assert_allclose(got[b, d], _silu(v), rtol=1e-13, atol=1e-15)
+
+
+def test_conv_silu_continues_across_a_split(oracle):
+    """x0 = the last three inputs of the first part continues the convolution."""
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((1, 2, 40))
+    w = rng.standard_normal((2, 4))
+    bias = rng.standard_normal(2)
+    full = oracle.conv_silu(x, w, bias)
+    second = oracle.conv_silu(x[..., 25:], w, bias, x0=x[..., 22:25])
+    np.testing.assert_allclose(second, full[..., 25:], rtol=1e-14, atol=1e-15)
+    # and it is causal: changing a later input leaves earlier outputs alone
+    x2 = x.copy()
+    x2[..., 30] += 1.0
+    np.testing.assert_array_equal(oracle.conv_silu(x2, w, bias)[..., :30], full[..., :30])
