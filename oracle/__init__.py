@@ -55,6 +55,8 @@ def _bind(path: str):
                               ctypes.POINTER(ctypes.c_int),
                               dp, dp, dp, dp, dp, dp, dp, dp,
                               ctypes.c_int, ctypes.c_int, dp, dp, dp, dp]
+    lib.ssor_scan_bwd.restype = ctypes.c_int
+    lib.ssor_scan_bwd.argtypes = [i64, i64, i64, i64, i64] + [dp] * 8 + [ctypes.c_int] + [dp] * 10
     lib.ssor_conv_silu.restype = ctypes.c_int
     lib.ssor_conv_silu.argtypes = [i64, i64, i64, i64, dp, dp, dp, dp, dp]
     lib.ssor_softplus_scalar.restype = ctypes.c_double
@@ -171,6 +173,41 @@ def cross_scan2d(u, delta, A, B, C, H, W, D=None, z=None, delta_bias=None, delta
     out, last = scan(u.reshape(batch, dim, L), delta, A, B, C, D, zz, delta_bias, delta_softplus,
                      SS2D_ORDERS, H=H, W=W)
     return out.reshape(batch, dim, H, W), last
+
+
+def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None,
+                       delta_softplus=True):
+    """Gradients of one forward direction (Euler, zero initial state) for the
+    upstream gradient dy [batch, dim, L].  delta [batch, dim, L], B/C
+    [batch, G, N, L], A [dim, N].  Returns a dict of float64 arrays: du, ddelta
+    [batch, dim, L]; dA [dim, N]; dB, dC [batch, G, N, L]; dD, ddelta_bias
+    [dim] (None when D / delta_bias are None); dz [batch, dim, L] (None
+    without z)."""
+    u = _f64(u, np.asarray(u).shape, "u")
+    batch, dim, L = u.shape
+    G, N = np.asarray(B).shape[1], np.asarray(B).shape[2]
+    delta = _f64(delta, (batch, dim, L), "delta")
+    A = _f64(A, (dim, N), "A")
+    B = _f64(B, (batch, G, N, L), "B")
+    C = _f64(C, (batch, G, N, L), "C")
+    dy = _f64(dy, (batch, dim, L), "dy")
+    D = _f64(D, (dim,), "D")
+    z = _f64(z, (batch, dim, L), "z")
+    bias = _f64(delta_bias, (dim,), "delta_bias")
+    out = {k: np.empty(sh) for k, sh in (("du", u.shape), ("ddelta", u.shape), ("dA", A.shape),
+                                          ("dB", B.shape), ("dC", C.shape))}
+    out["dD"] = np.empty(dim) if D is not None else None
+    out["dz"] = np.empty(u.shape) if z is not None else None
+    out["ddelta_bias"] = np.empty(dim) if bias is not None else None
+    work = np.empty(L * N)
+    rc = _load().ssor_scan_bwd(batch, dim, L, N, G, _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                               _ptr(D), _ptr(z), _ptr(bias), int(bool(delta_softplus)), _ptr(dy),
+                               _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dA"]),
+                               _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dz"]),
+                               _ptr(out["ddelta_bias"]), _ptr(work))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out
 
 
 def conv_silu(x, w, bias=None, x0=None):

@@ -186,6 +186,105 @@ int ssor_conv_silu(int64_t batch, int64_t dim, int64_t L, int64_t KW, const doub
     return 0;
 }
 
+/*
+ * ssor_scan_bwd: gradients of the single-direction scan (Euler input matrix,
+ * zero initial state) for an upstream gradient dy of out.  The forward pass is
+ * the recurrence above; the pages state that the backward pass recomputes the
+ * intermediate states rather than storing them ("Mamba Series ...", core
+ * insight 1, item 3; reading notes 3.3.2) -- here simply by storing one row's
+ * states in h_work.  Per (b, d), with s_t = C_t . h_t + D u_t and y_t = s_t g_t,
+ * g = SiLU(z):
+ *     ds_t  = dy_t g_t;            dz_t = dy_t s_t SiLU'(z_t)
+ *     dh_t  = ds_t C_t + abar_{t+1} (.) dh_{t+1}          (reverse in t)
+ *     dabar = dh_t (.) h_{t-1}
+ *     dDelta'_t = sum_n (dabar A abar + dh B u)_n;  dDelta_t = dDelta'_t softplus'(.)
+ *     dA_n += dabar abar Delta';  dB_t += dh Delta' u;  dC_t += ds h;
+ *     du_t  = ds D + sum_n dh Delta' B;  dD += ds u;  dbias += dDelta_t
+ * dA, dD, dbias sum over the batch; dB, dC sum over the channels of a group.
+ * Layouts as ssor_scan with K = 1; h_work holds L*N doubles.  Outputs are
+ * overwritten.  Returns 0 or -1.
+ */
+int ssor_scan_bwd(int64_t batch, int64_t dim, int64_t L, int64_t N, int64_t ngroups,
+                  const double *u, const double *delta, const double *A, const double *Bm,
+                  const double *Cm, const double *Dv, const double *z, const double *bias,
+                  int delta_softplus, const double *dy, double *du, double *ddelta, double *dA,
+                  double *dB, double *dC, double *dD, double *dz, double *dbias,
+                  double *h_work) {
+    if (batch < 0 || dim <= 0 || L <= 0 || N <= 0 || ngroups <= 0 || dim % ngroups) return -1;
+    if (!u || !delta || !A || !Bm || !Cm || !dy || !du || !ddelta || !dA || !dB || !dC || !h_work)
+        return -1;
+    const int64_t dpg = dim / ngroups;
+    for (int64_t i = 0; i < batch * dim * L; ++i) du[i] = ddelta[i] = 0.0;
+    if (dz) for (int64_t i = 0; i < batch * dim * L; ++i) dz[i] = 0.0;
+    for (int64_t i = 0; i < dim * N; ++i) dA[i] = 0.0;
+    for (int64_t i = 0; i < batch * ngroups * N * L; ++i) dB[i] = dC[i] = 0.0;
+    if (dD) for (int64_t i = 0; i < dim; ++i) dD[i] = 0.0;
+    if (dbias) for (int64_t i = 0; i < dim; ++i) dbias[i] = 0.0;
+
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const int64_t grp = d / dpg;
+            const double *Ar = A + d * N;
+            const double Dd = Dv ? Dv[d] : 0.0;
+            const double bd = bias ? bias[d] : 0.0;
+            const int64_t row = (b * dim + d) * L;
+            const double *Bg = Bm + (b * ngroups + grp) * N * L;
+            const double *Cg = Cm + (b * ngroups + grp) * N * L;
+            double *dBg = dB + (b * ngroups + grp) * N * L;
+            double *dCg = dC + (b * ngroups + grp) * N * L;
+            /* forward: states of every step */
+            for (int64_t t = 0; t < L; ++t) {
+                double dt = delta[row + t] + bd;
+                if (delta_softplus) dt = ssor_softplus(dt);
+                for (int64_t n = 0; n < N; ++n) {
+                    const double prev = t ? h_work[(t - 1) * N + n] : 0.0;
+                    h_work[t * N + n] = exp(dt * Ar[n]) * prev + dt * Bg[n * L + t] * u[row + t];
+                }
+            }
+            /* reverse: dh carries the gradient of the state after step t */
+            double dh_next_scaled[64 + 1];
+            double *carry = N <= 64 ? dh_next_scaled : NULL;
+            if (!carry) return -1;
+            for (int64_t n = 0; n < N; ++n) carry[n] = 0.0;   /* abar_{t+1} dh_{t+1} */
+            for (int64_t t = L - 1; t >= 0; --t) {
+                const double r = delta[row + t] + bd;
+                const double dt = delta_softplus ? ssor_softplus(r) : r;
+                const double dsp = delta_softplus ? 1.0 / (1.0 + exp(-r)) : 1.0;  /* softplus' */
+                double s = Dd * u[row + t];
+                for (int64_t n = 0; n < N; ++n) s += Cg[n * L + t] * h_work[t * N + n];
+                double gate = 1.0;
+                if (z) {
+                    const double zz = z[row + t];
+                    const double sg = 1.0 / (1.0 + exp(-zz));
+                    gate = zz * sg;
+                    dz[row + t] = dy[row + t] * s * sg * (1.0 + zz * (1.0 - sg));
+                }
+                const double ds = dy[row + t] * gate;
+                if (dD) dD[d] += ds * u[row + t];
+                double dut = ds * Dd;
+                double ddt = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    const double a = Ar[n];
+                    const double abar = exp(a * dt);
+                    const double prev = t ? h_work[(t - 1) * N + n] : 0.0;
+                    const double dh = ds * Cg[n * L + t] + carry[n];
+                    dCg[n * L + t] += ds * h_work[t * N + n];
+                    const double dabar = dh * prev;
+                    ddt += dabar * abar * a + dh * Bg[n * L + t] * u[row + t];
+                    dA[d * N + n] += dabar * abar * dt;
+                    dBg[n * L + t] += dh * dt * u[row + t];
+                    dut += dh * dt * Bg[n * L + t];
+                    carry[n] = abar * dh;
+                }
+                du[row + t] = dut;
+                ddelta[row + t] = ddt * dsp;
+                if (dbias) dbias[d] += ddt * dsp;
+            }
+        }
+    }
+    return 0;
+}
+
 /* Exposed for the oracle's own pin tests: the softplus used above. */
 double ssor_softplus_scalar(double x) { return ssor_softplus(x); }
 

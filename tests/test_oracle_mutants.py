@@ -35,6 +35,11 @@ MUTANTS = {
     "delta_by_position": ("double dt = dl_row[s] + bd;", "double dt = dl_row[p] + bd;"),
     "B_by_position": ("bbar = dt * B_grp[n * L + s];", "bbar = dt * B_grp[n * L + p];"),
     "conv_kernel_reversed": ("v += w[d * KW + j] * xv;", "v += w[d * KW + (KW - 1 - j)] * xv;"),
+    "bwd_no_decay_of_dh": ("carry[n] = abar * dh;", "carry[n] = dh;"),
+    "bwd_dA_missing_dt": ("dA[d * N + n] += dabar * abar * dt;", "dA[d * N + n] += dabar * abar;"),
+    "bwd_dB_uses_C": ("dBg[n * L + t] += dh * dt * u[row + t];",
+                      "dBg[n * L + t] += ds * dt * u[row + t];"),
+    "bwd_softplus_derivative": ("1.0 / (1.0 + exp(-r)) : 1.0;", "1.0 / (1.0 + exp(r)) : 1.0;"),
     "conv_history_off_by_one": ("else xv = x0r ? x0r[(KW - 1) + s] : 0.0;",
                                 "else xv = x0r ? x0r[(KW - 2) + s] : 0.0;"),
     "group_map_interleaved": ("const int64_t g = d / dpg;", "const int64_t g = d % ngroups;"),
@@ -66,6 +71,14 @@ class _Variant:
     def bidir_scan(self, u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True):
         return self.scan(u, delta, A, B, C, D, z, delta_bias, delta_softplus,
                          (self.ORDER_FWD, self.ORDER_REV))
+
+    def selective_scan_bwd(self, *a, **k):
+        real = _oracle._load
+        _oracle._load = lambda: self.lib
+        try:
+            return _oracle.selective_scan_bwd(*a, **k)
+        finally:
+            _oracle._load = real
 
     def conv_silu(self, x, w, bias=None, x0=None):
         x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))

@@ -369,3 +369,68 @@ def test_conv_silu_continues_across_a_split(oracle):
     x2 = x.copy()
     x2[..., 30] += 1.0
     np.testing.assert_array_equal(oracle.conv_silu(x2, w, bias)[..., :30], full[..., :30])
+
+
+# ---------------------------------------------------------------- backward pass
+def _fd_case(seed, softplus=True, with_z=True, G=2):
+    rng = np.random.default_rng(seed)
+    batch, dim, L, N = 2, 4, 6, 3
+    u = rng.standard_normal((batch, dim, L))
+    delta = rng.standard_normal((batch, dim, L)) * 0.5
+    A = -np.exp(rng.standard_normal((dim, N)) * 0.5)
+    B = rng.standard_normal((batch, G, N, L))
+    C = rng.standard_normal((batch, G, N, L))
+    D = rng.standard_normal(dim)
+    z = rng.standard_normal((batch, dim, L)) if with_z else None
+    bias = rng.standard_normal(dim) * 0.5 - 0.5
+    dy = rng.standard_normal((batch, dim, L))
+    return dict(u=u, delta=delta, A=A, B=B, C=C, D=D, z=z, delta_bias=bias), dy, softplus
+
+
+@pytest.mark.parametrize("seed,softplus,with_z,G", [(41, True, True, 2), (42, False, False, 1)])
+def test_backward_matches_finite_differences(oracle, seed, softplus, with_z, G):
+    """Every gradient of the oracle's backward pass against central finite
+    differences of its forward scan, for the loss sum(dy * out)."""
+    args, dy, sp = _fd_case(seed, softplus, with_z, G)
+
+    def loss(a):
+        out, _ = oracle.selective_scan(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                                       a["delta_bias"], sp)
+        return float(np.sum(dy * out))
+
+    grads = oracle.selective_scan_bwd(args["u"], args["delta"], args["A"], args["B"], args["C"], dy,
+                                      args["D"], args["z"], args["delta_bias"], sp)
+    names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "z": "dz", "delta_bias": "ddelta_bias"}
+    eps = 1e-6
+    for name, gname in names.items():
+        if args[name] is None:
+            assert grads[gname] is None
+            continue
+        x = args[name]
+        fd = np.empty_like(x)
+        for idx in np.ndindex(x.shape):
+            keep = x[idx]
+            x[idx] = keep + eps
+            lp = loss(args)
+            x[idx] = keep - eps
+            lm = loss(args)
+            x[idx] = keep
+            fd[idx] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(grads[gname], fd, rtol=2e-6, atol=2e-7, err_msg=name)
+
+
+def test_backward_single_step_closed_form(oracle):
+    """N = 1, L = 1, no gate, no softplus: y = C dt B u + D u, so dy/du = C dt B + D,
+    dy/ddelta = C B u, dy/dB = C dt u, dy/dC = dt B u, dy/dD = u, and dA = 0
+    (the state starts at zero)."""
+    u, dt, B, C, D, A = 0.7, 0.3, -1.2, 0.5, 0.25, -2.0
+    g = oracle.selective_scan_bwd(np.full((1, 1, 1), u), np.full((1, 1, 1), dt), np.full((1, 1), A),
+                                  np.full((1, 1, 1, 1), B), np.full((1, 1, 1, 1), C),
+                                  np.ones((1, 1, 1)), np.array([D]), None, None, False)
+    np.testing.assert_allclose(g["du"].ravel(), [C * dt * B + D], rtol=1e-15)
+    np.testing.assert_allclose(g["ddelta"].ravel(), [C * B * u], rtol=1e-15)
+    np.testing.assert_allclose(g["dB"].ravel(), [C * dt * u], rtol=1e-15)
+    np.testing.assert_allclose(g["dC"].ravel(), [dt * B * u], rtol=1e-15)
+    np.testing.assert_allclose(g["dD"].ravel(), [u], rtol=1e-15)
+    np.testing.assert_array_equal(g["dA"], np.zeros((1, 1)))
