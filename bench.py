@@ -50,9 +50,9 @@ FALLBACK_HBM_GBS = 6400.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 CSRC = os.path.join(ROOT, "selective_state_space_120_b300", "csrc")
 
-WORKLOADS = {w.name: w for w in wk.ALL}
+WORKLOADS = {w.name: w for w in wk.ALL + (wk.MAMBA_LAYER_CONV,)}
 HEADLINE = wk.MAMBA_LAYER
-OTHERS = (wk.LONG_SEQ, wk.VIM_BIDIR, wk.VMAMBA_SS2D)
+OTHERS = (wk.LONG_SEQ, wk.VIM_BIDIR, wk.VMAMBA_SS2D, wk.MAMBA_LAYER_CONV)
 
 
 # ------------------------------------------------------------------ accounting
@@ -222,7 +222,7 @@ class Runner:
         inp = wk.make_inputs(wl, seed=seed)
         self.host = inp
         t = {n: self._to_dev(getattr(inp, n)) for n in
-             ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")}
+             ("u", "delta", "A", "B", "C", "D", "z", "delta_bias", "conv_w", "conv_b")}
         set_bytes = algorithmic_bytes(wl)
         self.copies = max(2, int(np.ceil(3 * L2_BYTES / set_bytes)) + 1)
         self.copies = min(self.copies, 8)
@@ -235,7 +235,10 @@ class Runner:
             self.sets.append(s)
         self.stream = torch.cuda.current_stream(device)
         self.ws = None
-        self.opts = b.options(0)
+        conv_w, conv_b = self.sets[0]["conv_w"], self.sets[0]["conv_b"]
+        self.opts = b.options(0, b.SS_SCAN_CONV_SILU if wl.conv else 0, None,
+                              None if conv_w is None else conv_w.data_ptr(),
+                              None if conv_b is None else conv_b.data_ptr())
         kind = {1: b.SS_KIND_SCAN, 2: b.SS_KIND_BIDIR, 4: b.SS_KIND_CROSS2D}[wl.K]
         wsb = int(self.lib.ss_workspace_bytes_opts(kind, wl.batch, wl.dim, wl.L, wl.N,
                                                    ctypes.byref(self.opts)))

@@ -125,13 +125,27 @@ typedef struct ss_scan_options {
      * one scan of L1 + L2 steps (the recurrent form the reading notes give for
      * inference). */
     const float *h0;
-    int reserved[4]; /* must be zero */
+    /* With SS_SCAN_CONV_SILU: the Mamba block's input branch is fused in front
+     * of the scan, and `u` is its input x.  The scan then runs on
+     *     u[t] = SiLU(conv_b[d] + sum_{j<4} conv_w[d, j] * x[t - 3 + j])
+     * (causal depthwise Conv1D of width 4, "Mamba Block (1D)" diagram), which
+     * is also the u of the D*u skip term.  conv_w [dim, 4] float32 (required),
+     * conv_b [dim] float32 (NULL: 0), conv_x0 [batch, dim, 3] float32: the
+     * three inputs before the sequence, oldest first (NULL: zeros) -- with h0
+     * this continues a sequence.  Rows must be 16-byte aligned (seqlen *
+     * element size % 16 == 0), else SS_ERR_UNSUPPORTED. */
+    const float *conv_w;
+    const float *conv_b;
+    const float *conv_x0;
+    int reserved[6]; /* must be zero */
 } ss_scan_options;
 
 /* Zero-order-hold input matrix: Bbar = (Delta*A)^-1 (exp(Delta*A) - 1) * Delta*B
  * ("Mamba Series ...", mathematical form of the selective SSM) instead of the
  * default Euler Bbar = Delta*B.  For A = 0 it is Delta*B. */
 #define SS_SCAN_ZOH 1u
+/* Fuse the causal Conv1D(k=4) + SiLU input branch in front of the scan. */
+#define SS_SCAN_CONV_SILU 2u
 
 /* ss_selective_scan_fwd with options (NULL options = automatic). */
 ss_status ss_selective_scan_fwd_opts(int64_t batch, int64_t dim, int64_t seqlen, int dstate,

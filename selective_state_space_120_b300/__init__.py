@@ -71,7 +71,7 @@ def workspace_bytes(kind: int, batch: int, dim: int, seqlen: int, dstate: int, c
 
 def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
                        return_last_state=False, out=None, chunks=0, workspace=None, stream=None,
-                       h0=None, zoh=False):
+                       h0=None, zoh=False, conv_w=None, conv_b=None, conv_x0=None):
     """One-direction selective scan.
 
     u, delta, z: [batch, dim, L]; A: [dim, N] float32; B, C: [batch, G, N, L];
@@ -80,7 +80,10 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta
     (0 automatic, 1 single pass, n >= 2 chunked path); ``workspace`` is an
     optional preallocated uint8 CUDA tensor; ``h0`` [batch, dim, N] float32 is
     the initial state (default zero); ``zoh`` selects the zero-order-hold input
-    matrix instead of the Euler one."""
+    matrix instead of the Euler one.  With ``conv_w`` [dim, 4] float32 the
+    Mamba block's causal Conv1D + SiLU (bias ``conv_b`` [dim], history
+    ``conv_x0`` [batch, dim, 3]) is fused in front of the scan and ``u`` is its
+    input."""
     torch = _torch()
     lib = _b.load()
     batch, dim, L = u.shape
@@ -95,11 +98,15 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta
     _check_io("D", D, torch.float32, dev, (dim,))
     _check_io("delta_bias", delta_bias, torch.float32, dev, (dim,))
     _check_io("h0", h0, torch.float32, dev, (batch, dim, N))
+    _check_io("conv_w", conv_w, torch.float32, dev, (dim, 4))
+    _check_io("conv_b", conv_b, torch.float32, dev, (dim,))
+    _check_io("conv_x0", conv_x0, torch.float32, dev, (batch, dim, 3))
     if out is None:
         out = torch.empty_like(u)
     _check_io("out", out, io, dev, (batch, dim, L))
     last = torch.empty(batch, dim, N, dtype=torch.float32, device=dev) if return_last_state else None
-    opts = _b.options(chunks, _b.SS_SCAN_ZOH if zoh else 0, _ptr(h0))
+    flags = (_b.SS_SCAN_ZOH if zoh else 0) | (_b.SS_SCAN_CONV_SILU if conv_w is not None else 0)
+    opts = _b.options(chunks, flags, _ptr(h0), _ptr(conv_w), _ptr(conv_b), _ptr(conv_x0))
     wsb = int(lib.ss_workspace_bytes_opts(_b.SS_KIND_SCAN, batch, dim, L, N, ctypes.byref(opts)))
     if wsb and (workspace is None or workspace.numel() < wsb):
         workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)

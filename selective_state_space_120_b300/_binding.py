@@ -45,10 +45,12 @@ class SSError(RuntimeError):
 
 class ScanOptions(ctypes.Structure):
     _fields_ = [("chunks", ctypes.c_int), ("flags", ctypes.c_uint), ("h0", ctypes.c_void_p),
-                ("reserved", ctypes.c_int * 4)]
+                ("conv_w", ctypes.c_void_p), ("conv_b", ctypes.c_void_p),
+                ("conv_x0", ctypes.c_void_p), ("reserved", ctypes.c_int * 6)]
 
 
 SS_SCAN_ZOH = 1
+SS_SCAN_CONV_SILU = 2
 
 
 _lock = threading.Lock()
@@ -109,11 +111,15 @@ def version() -> str:
     return load().ss_version().decode()
 
 
-def options(chunks: int = 0, flags: int = 0, h0: int | None = None) -> ScanOptions:
+def options(chunks: int = 0, flags: int = 0, h0: int | None = None, conv_w: int | None = None,
+            conv_b: int | None = None, conv_x0: int | None = None) -> ScanOptions:
     o = ScanOptions()
     o.chunks = int(chunks)
     o.flags = int(flags)
     o.h0 = h0
+    o.conv_w = conv_w
+    o.conv_b = conv_b
+    o.conv_x0 = conv_x0
     return o
 
 

@@ -89,8 +89,18 @@ ss_status check_options(const char *fn, const ss_scan_options *o, int64_t batch,
     for (int r : o->reserved)
         if (r != 0) return fail(SS_ERR_INVALID_ARG, "%s: reserved option fields must be zero", fn);
     if (o->chunks < 0) return fail(SS_ERR_INVALID_ARG, "%s: options.chunks < 0", fn);
-    if (o->flags & ~SS_SCAN_ZOH)
+    if (o->flags & ~(SS_SCAN_ZOH | SS_SCAN_CONV_SILU))
         return fail(SS_ERR_INVALID_ARG, "%s: unknown option flags 0x%x", fn, o->flags);
+    if (o->flags & SS_SCAN_CONV_SILU) {
+        if (!o->conv_w) return fail(SS_ERR_INVALID_ARG, "%s: SS_SCAN_CONV_SILU needs conv_w", fn);
+        for (const void *q : {(const void *)o->conv_w, (const void *)o->conv_b, (const void *)o->conv_x0})
+            if (q && !aligned16(q)) return fail(SS_ERR_ALIGNMENT, "%s: a conv tensor is not 16-byte aligned", fn);
+        const int64_t es = io == SS_BF16 ? 2 : 4;
+        if ((L * es) % 16 != 0)
+            return fail(SS_ERR_UNSUPPORTED, "%s: the fused Conv1D needs 16-byte aligned rows", fn);
+    } else if (o->conv_w || o->conv_b || o->conv_x0) {
+        return fail(SS_ERR_INVALID_ARG, "%s: conv tensors given without SS_SCAN_CONV_SILU", fn);
+    }
     if (o->h0) {
         if (!aligned16(o->h0)) return fail(SS_ERR_ALIGNMENT, "%s: options.h0 is not 16-byte aligned", fn);
         const int64_t es = io == SS_BF16 ? 2 : 4;
@@ -233,6 +243,10 @@ ss_status ss_selective_scan_fwd_opts(int64_t batch, int64_t dim, int64_t seqlen,
     if (options) {
         a.h0 = options->h0;
         a.zoh = (options->flags & SS_SCAN_ZOH) ? 1 : 0;
+        a.conv = (options->flags & SS_SCAN_CONV_SILU) ? 1 : 0;
+        a.conv_w = options->conv_w;
+        a.conv_b = options->conv_b;
+        a.conv_x0 = options->conv_x0;
     }
     if ((st = check_workspace(fn, scan1d_workspace_bytes(a), workspace, workspace_bytes))) return st;
     return launch_scan1d(a);
@@ -270,6 +284,10 @@ ss_status ss_selective_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t seql
     if (options) {
         a.h0 = options->h0;
         a.zoh = (options->flags & SS_SCAN_ZOH) ? 1 : 0;
+        a.conv = (options->flags & SS_SCAN_CONV_SILU) ? 1 : 0;
+        a.conv_w = options->conv_w;
+        a.conv_b = options->conv_b;
+        a.conv_x0 = options->conv_x0;
     }
     const size_t need = scan1d_workspace_bytes(a);
     if (need > SS_NOALLOC_SCRATCH_BYTES)

@@ -26,6 +26,9 @@ struct ScanArgs {
     int chunks = 0;  // single direction: 0 automatic, 1 direct, >= 2 chunked with that many L-chunks
     const float *h0 = nullptr;  // single direction: initial state [batch, dim, N] (nullable)
     int zoh = 0;                // single direction: zero-order-hold input matrix
+    // single direction: fused Conv1D(k=4) + SiLU in front of the scan
+    int conv = 0;
+    const float *conv_w = nullptr, *conv_b = nullptr, *conv_x0 = nullptr;
     ss_stream_t stream = nullptr;
 };
 

@@ -87,7 +87,8 @@ struct Scan1d {
         if ((st = make_map(&mb, a.B, io, a.L, (uint64_t)a.batch * a.G * C::N, C::T, C::N))) return st;
         if ((st = make_map(&mc, a.C, io, a.L, (uint64_t)a.batch * a.G * C::N, C::T, C::N))) return st;
 
-        auto kern = k_scan1d<C, false>;
+        // the plain kernel unless the zero-order hold or the fused Conv1D is asked for
+        auto kern = (a.zoh || a.conv) ? k_scan1d<C, false, true> : k_scan1d<C, false, false>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
             return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
 
@@ -112,6 +113,10 @@ struct Scan1d {
         p.has_z = a.z != nullptr;
         p.zoh = a.zoh;
         p.h0 = a.h0;
+        p.conv = a.conv;
+        p.conv_w = a.conv_w;
+        p.conv_b = a.conv_b;
+        p.conv_x0 = a.conv_x0;
         p.out = a.out;
         p.last_state = a.last_state;
         const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);

@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(C::THREADS) k_multidir(const MultiParams p) {
         __syncthreads();
 
         const float4 *const dxrows[1] = {dxrow};
-        scan_chunk_pipe<C, true>(dxrows, bc, g, h, A2p, [&](int, float y, int t) {
+        auto emit = [&](int, float y, int t) {
             const int64_t s = (int64_t)i * T + t;
             if (s < L) {
                 const int64_t pos = position_of(order, s, L, p.H, p.W, p.divH);
@@ -199,7 +199,9 @@ __global__ void __launch_bounds__(C::THREADS) k_multidir(const MultiParams p) {
                 else
                     atomicAdd(my_acc + pos, y);
             }
-        }, zoh ? iAv : nullptr);
+        };
+        if (zoh) scan_chunk_pipe<C, true, true>(dxrows, bc, g, h, A2p, emit, iAv);
+        else scan_chunk_pipe<C, true>(dxrows, bc, g, h, A2p, emit);
     }
     __syncthreads();
 

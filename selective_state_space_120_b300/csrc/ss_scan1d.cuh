@@ -89,7 +89,9 @@ struct Cfg1 {
     static constexpr int OFF_GD = OFF_DX + CB * DXROW;
     static constexpr int OBROW = T * 4 + 16;  // staged outputs (I/O type, or fp32 partials)
     static constexpr int OFF_OB = OFF_DX + NPREP * PREPBUF;
-    static constexpr int OFF_BAR = (OFF_OB + CB * OBROW + 7) & ~7;
+    // fused Conv1D: each channel's last three inputs of a chunk, double-buffered
+    static constexpr int OFF_HALO = OFF_OB + CB * OBROW;
+    static constexpr int OFF_BAR = (OFF_HALO + 2 * CB * 16 + 7) & ~7;
     static constexpr int SMEM = OFF_BAR + 8 * STAGES + 1024;  // + alignment slack
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
 };
@@ -126,6 +128,8 @@ struct Scan1dParams {
     int softplus, has_z;
     int zoh;                // zero-order-hold input matrix (single direction)
     const float *h0;        // initial state [batch*dim, N] (single direction; nullable)
+    int conv;               // fused Conv1D(k=4) + SiLU before the scan (single direction)
+    const float *conv_w, *conv_b, *conv_x0;  // [dim, 4], [dim], [batch*dim, 3]
     void *out;
     float *last_state;      // [batch, K, dim, N]
     float *hend;          // [rows, J, N] end state of an L-chunk scanned from zero
@@ -240,6 +244,16 @@ __device__ __forceinline__ void scan_chunk(const float4 *dxrow, const float *bc,
     }
 }
 
+// One element of row `row`, column `col` of a swizzled 64-byte-row tile.
+template <typename IO>
+__device__ __forceinline__ float load_tile_elem(const uint8_t *tile, int row, int col) {
+    const int off = swz64(row * 64 + col * (int)sizeof(IO));
+    if constexpr (sizeof(IO) == 2)
+        return __uint_as_float((uint32_t)(*reinterpret_cast<const unsigned short *>(tile + off)) << 16);
+    else
+        return *reinterpret_cast<const float *>(tile + off);
+}
+
 // Scans one chunk of T steps for this lane's CL channels and state slice.
 // DO_Y selects the readout (off in the chunk-local pass, which only needs the
 // end states).  `emit(c, y, t)` receives the full readout y of channel c of the
@@ -325,7 +339,7 @@ struct StepRegs {
 
 // Loads and evaluates everything of step pair tp that does not depend on the
 // state: smem loads, Delta'*A, ex2, x*B.
-template <class C, bool DO_Y>
+template <class C, bool DO_Y, bool ZOH>
 __device__ __forceinline__ void stage_step(StepRegs<C> &r, const float4 *const (&dxrow)[C::CL],
                                            const float *bc, int g, int tp,
                                            const float2 (&A2p)[C::CL][C::NPT], const float *iA) {
@@ -395,7 +409,7 @@ __device__ __forceinline__ void stage_step(StepRegs<C> &r, const float4 *const (
             r.a[c][j][0] = ex2(da.x);
             r.a[c][j][1] = ex2(da.y);
             r.bx[c][j] = __fmul2_rn(xx, make_float2(Bv[2 * j], Bv[2 * j + 1]));
-            if (iA) {
+            if constexpr (ZOH) {
                 // zero-order hold: Bbar*u = (exp(x) - 1)/A * B*u with x = Delta'*A
                 // (the slots hold u, not Delta'*u).  For |x| < 1/16 use
                 // Delta' * expm1(x)/x = Delta' (1 + x/2 + x^2/6 + x^3/24), whose
@@ -419,7 +433,10 @@ __device__ __forceinline__ void stage_step(StepRegs<C> &r, const float4 *const (
 // scan_chunk_cl with a one-step-pair software pipeline: the loads and
 // exponentials of step pair tp+1 are issued before the state updates of tp, so
 // their latency overlaps the dependent FMA chain.
-template <class C, bool DO_Y, class Emit>
+// ZOH selects the zero-order-hold input matrix at compile time (iA = 1/A per
+// state); a runtime branch inside the unrolled step loop costs the scheduler
+// its freedom to interleave across states and step pairs.
+template <class C, bool DO_Y, bool ZOH = false, class Emit>
 __device__ __forceinline__ void scan_chunk_pipe(const float4 *const (&dxrow)[C::CL], const float *bc,
                                                 int g, float (&h)[C::CL][C::NPT],
                                                 const float2 (&A2p)[C::CL][C::NPT], Emit &&emit,
@@ -428,12 +445,12 @@ __device__ __forceinline__ void scan_chunk_pipe(const float4 *const (&dxrow)[C::
     constexpr int BS = R >= 2 ? R : 2;  // steps per readout block
     constexpr int PPB = BS / 2;
     StepRegs<C> cur, nxt;
-    stage_step<C, DO_Y>(nxt, dxrow, bc, g, 0, A2p, iA);
+    stage_step<C, DO_Y, ZOH>(nxt, dxrow, bc, g, 0, A2p, iA);
     float v[CL][BS];
 #pragma unroll
     for (int tp = 0; tp < C::TP; ++tp) {
         cur = nxt;
-        if (tp + 1 < C::TP) stage_step<C, DO_Y>(nxt, dxrow, bc, g, tp + 1, A2p, iA);
+        if (tp + 1 < C::TP) stage_step<C, DO_Y, ZOH>(nxt, dxrow, bc, g, tp + 1, A2p, iA);
         const int pp = tp % PPB;
 #pragma unroll
         for (int c = 0; c < CL; ++c) {
@@ -588,7 +605,10 @@ __device__ __forceinline__ void store_partials(const Scan1dParams &p, const Merg
 // MULTI = false: a single-direction scan (order 0, OUT_STORE, one direction),
 // with those fields fixed at compile time; MULTI = true: one direction of a
 // multi-direction call, as the params say.
-template <class C, bool MULTI>
+// EXT = true compiles the optional input paths of a single direction (the
+// zero-order hold and the fused Conv1D); the plain instantiation carries none
+// of their code, which keeps the default scan's registers and schedule.
+template <class C, bool MULTI, bool EXT = false>
 __global__ void __launch_bounds__(C::THREADS)
 k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
          const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
@@ -651,7 +671,7 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
             const float araw = __ldg(p.A + ((int64_t)p.k * p.dim + d) * N + n);
             const float a = araw * kLog2e;
             A2p[c][j] = make_float2(a, a);
-            iAv[c * NPT + j] = araw != 0.f ? 1.f / araw : 0.f;
+            if (EXT) iAv[c * NPT + j] = araw != 0.f ? 1.f / araw : 0.f;
             h[c][j] = (p.pass == 2) ? __ldg(p.carry + (rows[c] * p.J + jc) * N + n)
                       : (p.h0 && jc == 0) ? __ldg(p.h0 + rows[c] * N + n) : 0.f;
         }
@@ -665,8 +685,14 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
     const float Dd = p.D ? __ldg(p.D + (int64_t)p.k * p.dim + pd) : 0.f;
     const float bd = p.bias ? __ldg(p.bias + (int64_t)p.k * p.dim + pd) : 0.f;
     const int64_t prow = (int64_t)b * p.dim + pd;  // u/z row of the prep channel
+    // fused Conv1D: weights of the prep channel and the three inputs before this
+    // launch's first step (the given history at the start of the sequence, the
+    // previous L-chunk's last inputs otherwise)
+    // (loaded inside the prep, so they hold no registers across the chunk loop)
+    const bool conv = EXT && !MULTI && !C::OVL && p.conv;  // (the overlapped order would need a deeper halo)
+    float *halo = reinterpret_cast<float *>(smem + C::OFF_HALO);  // [2][CB][4]
 
-    const float *zoh_iA = (!MULTI && p.zoh) ? iAv : nullptr;
+    const float *zoh_iA = (EXT && !MULTI && p.zoh) ? iAv : nullptr;
     float *bcbuf0 = reinterpret_cast<float *>(smem + C::OFF_BC);
     uint8_t *obrows[CL];
 #pragma unroll
@@ -780,6 +806,46 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
                 if (gate_in_prep) zz[e] = IOT<IO>::widen(gz[e]);
             }
         }
+        if (conv) {
+            // raw inputs at columns pt0-3 .. pt0-1: this tile, or the previous
+            // chunk's last three (the halo), or the history for the first chunk
+            const float4 w4 = __ldg(reinterpret_cast<const float4 *>(p.conv_w) + pd);
+            const float cw[4] = {w4.x, w4.y, w4.z, w4.w};
+            const float cb = p.conv_b ? __ldg(p.conv_b + pd) : 0.f;
+            float hx[3];
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+                const int col = pt0 - 3 + j;
+                if (col >= 0) {
+                    hx[j] = load_tile_elem<IO>(st + C::OFF_U, pch, col);
+                } else if (i == 0) {
+                    // before this launch's first step: the given history at the
+                    // start of the sequence, else the previous L-chunk's inputs
+                    const int hj = col + 3;
+                    hx[j] = t_begin == 0
+                                ? (p.conv_x0 ? __ldg(p.conv_x0 + prow * 3 + hj) : 0.f)
+                                : IOT<IO>::load(reinterpret_cast<const IO *>(p.u_g) + prow * p.L +
+                                                t_begin - 3 + hj);
+                } else {
+                    hx[j] = halo[((i & 1) * C::CB + pch) * 4 + col + 3];
+                }
+            }
+            // keep this chunk's last three inputs for the next chunk
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                if (pt0 + e >= T - 3) halo[((((i + 1) & 1) * C::CB) + pch) * 4 + pt0 + e - (T - 3)] = uu[e];
+            float uc[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float x3 = e >= 3 ? uu[e - 3] : hx[e];
+                const float x2 = e >= 2 ? uu[e - 2] : hx[e + 1];
+                const float x1 = e >= 1 ? uu[e - 1] : hx[2];
+                const float v = fmaf(cw[3], uu[e], fmaf(cw[2], x1, fmaf(cw[1], x2, fmaf(cw[0], x3, cb))));
+                uc[e] = silu(v);
+            }
+#pragma unroll
+            for (int e = 0; e < E; ++e) uu[e] = uc[e];
+        }
         // steps of this chunk at or past the end of the L-chunk leave h unchanged
         const int lim = (int)min((int64_t)T, t_end - (t_begin + (int64_t)i * T)) - pt0;
 #pragma unroll
@@ -791,7 +857,7 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
                 if (p.softplus) v = softplus(v);
                 if (e + k >= lim) v = 0.f;
                 dl[k] = v;
-                xx[k] = (!MULTI && p.zoh) ? uu[e + k] : v * uu[e + k];
+                xx[k] = (EXT && !MULTI && p.zoh) ? uu[e + k] : v * uu[e + k];
                 ga[k] = gate_in_prep ? silu(zz[e + k]) : 1.f;
                 du[k] = Dd * uu[e + k] * ga[k];
                 if (p.pass == 1) sdt_acc += v;
@@ -870,8 +936,14 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
             else reinterpret_cast<float *>(obrows[c])[t] = v;
         };
         if constexpr (C::PIPE) {
-            if (do_y) scan_chunk_pipe<C, true>(dxrows, bc, g, h, A2p, emit, zoh_iA);
-            else scan_chunk_pipe<C, false>(dxrows, bc, g, h, A2p, [](int, float, int) {}, zoh_iA);
+            auto none = [](int, float, int) {};
+            if (EXT && zoh_iA) {
+                if (do_y) scan_chunk_pipe<C, true, true>(dxrows, bc, g, h, A2p, emit, zoh_iA);
+                else scan_chunk_pipe<C, false, true>(dxrows, bc, g, h, A2p, none, zoh_iA);
+            } else {
+                if (do_y) scan_chunk_pipe<C, true>(dxrows, bc, g, h, A2p, emit);
+                else scan_chunk_pipe<C, false>(dxrows, bc, g, h, A2p, none);
+            }
         } else {
             if (do_y) scan_chunk_cl<C, true>(dxrows, bc, g, h, A2p, emit);
             else scan_chunk_cl<C, false>(dxrows, bc, g, h, A2p, [](int, float, int) {});

@@ -14,6 +14,7 @@ Recipe (the workloads of the Mamba / Vim / VMamba pages, with synthetic data):
     A[k, d, n]      = -(n + 1)                          [K*dim, N]
     B_k, C_k        ~ N(0, 1)                           [batch, K, G, N, L]
     D               = 1                                 [K*dim]
+    conv workloads, drawn last: conv_w ~ N(0, 0.5^2) [dim, 4], conv_b ~ N(0, 0.1^2)
 Inputs of a bf16 workload are rounded to bf16 (round-to-nearest-even) on the
 host; A, D and delta_bias stay float32.
 """
@@ -41,6 +42,7 @@ class Workload:
     last_state: bool = False
     H: int = 1
     W: int = 0            # W = L for a plain sequence
+    conv: bool = False    # u is the input of a fused Conv1D(k=4) + SiLU
 
     @property
     def elems(self) -> int:
@@ -60,6 +62,10 @@ VMAMBA_SS2D = Workload("vmamba_t_ss2d_b32_d192_56x56_n16", 32, 192, 56 * 56, K=4
                        with_z=False, H=56, W=56)
 
 ALL = (TINY_F32, MAMBA_LAYER, LONG_SEQ, VIM_BIDIR, VMAMBA_SS2D)
+
+# The Mamba layer with its Conv1D(k=4) + SiLU input branch fused in front of the
+# scan (weights ~ N(0, 0.5^2), bias ~ N(0, 0.1^2)).
+MAMBA_LAYER_CONV = Workload("mamba130m_layer_conv_b8_d1536_l2048_n16", 8, 1536, 2048, conv=True)
 
 
 def round_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -101,6 +107,8 @@ class Inputs:
     z: np.ndarray | None
     delta_bias: np.ndarray   # [K*dim] float32
     extra: dict = field(default_factory=dict)
+    conv_w: np.ndarray | None = None   # [dim, 4] float32 (conv workloads)
+    conv_b: np.ndarray | None = None   # [dim] float32
 
     def as_f64(self, name: str) -> np.ndarray | None:
         """The exact values handed to the GPU, widened to float64."""
@@ -134,8 +142,14 @@ def make_inputs(wl: Workload, seed: int = 0) -> Inputs:
         cv = round_bf16_bits
     else:
         cv = lambda x: np.ascontiguousarray(x, dtype=np.float32)  # noqa: E731
-    return Inputs(wl, cv(u), cv(raw), A, cv(Bm), cv(Cm), D,
-                  None if z is None else cv(z), bias)
+    inp = Inputs(wl, cv(u), cv(raw), A, cv(Bm), cv(Cm), D,
+                 None if z is None else cv(z), bias)
+    if wl.conv:
+        # drawn after everything else, so the other inputs are those of the
+        # same workload without the conv
+        inp.conv_w = (rng.standard_normal((d, 4)) * 0.5).astype(np.float32)
+        inp.conv_b = (rng.standard_normal(d) * 0.1).astype(np.float32)
+    return inp
 
 
 def scaled(wl: Workload, name: str | None = None, **changes) -> Workload:

@@ -161,7 +161,15 @@ def test_scan_options_are_validated(lib):
     assert lib.ss_selective_scan_fwd_opts(*base, ctypes.byref(bad_h0), None) == b.SS_ERR_ALIGNMENT
     h0_on_out = b.options(h0=A16 + 0x500000)
     assert lib.ss_selective_scan_fwd_opts(*base, ctypes.byref(h0_on_out), None) == b.SS_ERR_INVALID_ARG
-    assert ctypes.sizeof(b.ScanOptions) == 32
+    no_w = b.options(flags=b.SS_SCAN_CONV_SILU)
+    assert lib.ss_selective_scan_fwd_opts(*base, ctypes.byref(no_w), None) == b.SS_ERR_INVALID_ARG
+    w_no_flag = b.options(conv_w=A16 + 0x700000)
+    assert lib.ss_selective_scan_fwd_opts(*base, ctypes.byref(w_no_flag), None) == b.SS_ERR_INVALID_ARG
+    unaligned_rows = list(base)
+    unaligned_rows[2] = 33                  # 66-byte rows: no fused conv
+    conv = b.options(flags=b.SS_SCAN_CONV_SILU, conv_w=A16 + 0x700000)
+    assert lib.ss_selective_scan_fwd_opts(*unaligned_rows, ctypes.byref(conv), None) == b.SS_ERR_UNSUPPORTED
+    assert ctypes.sizeof(b.ScanOptions) == 64
 
 
 @fake_ptrs

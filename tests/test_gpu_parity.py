@@ -233,6 +233,52 @@ def test_zero_order_hold_large_steps_and_unaligned_rows(oracle):
     sc.assert_close(last.cpu().numpy(), ref_last[:, 0], "f32", "last_state")
 
 
+# ---------------------------------------------------------------- fused Conv1D + SiLU
+def _conv_params(dim, seed=31):
+    rng = np.random.default_rng(seed)
+    return ((rng.standard_normal((dim, 4)) * 0.5).astype(np.float32),
+            (rng.standard_normal(dim) * 0.1).astype(np.float32))
+
+
+def _conv_case(oracle, wl, chunks, with_history):
+    import torch
+    import selective_state_space_120_b300 as ss
+    inp = wk.make_inputs(wl)
+    w, cb = _conv_params(wl.dim)
+    rng = np.random.default_rng(32)
+    x0 = rng.standard_normal((wl.batch, wl.dim, 3)).astype(np.float32) if with_history else None
+    h0 = _h0(wl) if with_history else None
+    t = sc.device_inputs(inp)
+    out, last = ss.selective_scan_fwd(t["u"], t["delta"][:, 0], t["A"], t["B"][:, 0], t["C"][:, 0],
+                                      t["D"], t["z"], t["delta_bias"], True, return_last_state=True,
+                                      chunks=chunks, h0=None if h0 is None else sc.to_torch(h0),
+                                      conv_w=sc.to_torch(w), conv_b=sc.to_torch(cb),
+                                      conv_x0=None if x0 is None else sc.to_torch(x0))
+    torch.cuda.synchronize()
+    u = oracle.conv_silu(inp.as_f64("u"), w.astype(np.float64), cb.astype(np.float64),
+                         None if x0 is None else x0.astype(np.float64))
+    ref, ref_last = oracle.scan(u, inp.as_f64("delta"), inp.as_f64("A"), inp.as_f64("B"),
+                                inp.as_f64("C"), inp.as_f64("D"), inp.as_f64("z"),
+                                inp.as_f64("delta_bias"), True,
+                                h0=None if h0 is None else h0.astype(np.float64)[:, None])
+    sc.assert_close(sc.from_torch(out), ref, wl.io)
+    sc.assert_close(last.cpu().numpy(), ref_last[:, 0], wl.io, "last_state")
+
+
+@pytest.mark.parametrize("chunks", [1, 3])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_fused_conv_silu(oracle, chunks, io):
+    """The Conv1D(k=4) + SiLU input branch fused in front of the scan, on the
+    direct and the chunked path, against the oracle's conv followed by its scan."""
+    _conv_case(oracle, sc.workload("conv", 2, 40, 1024, io=io), chunks, False)
+
+
+@pytest.mark.parametrize("chunks", [1, 4])
+def test_fused_conv_silu_continuing(oracle, chunks):
+    """Conv history and initial state given: the call continues a sequence."""
+    _conv_case(oracle, sc.workload("convh", 2, 24, 520), chunks, True)
+
+
 # ---------------------------------------------------------------- single-step decode
 @pytest.mark.parametrize("N", [1, 4, 16, 64])
 @pytest.mark.parametrize("io,zoh", [("f32", False), ("bf16", False), ("f32", True)])
