@@ -84,6 +84,10 @@ def kernel_source_hash() -> str:
 def ncu_traffic(wl: wk.Workload):
     """DRAM bytes per launch of the workload's dominant kernel from the committed
     ncu summary, or None if absent or taken on different kernel sources."""
+    return ncu_traffic_named(wl.name)
+
+
+def ncu_traffic_named(name: str):
     try:
         with open(PROFILE_TRAFFIC) as fh:
             rec = json.load(fh)
@@ -91,7 +95,7 @@ def ncu_traffic(wl: wk.Workload):
         return None
     if rec.get("source_hash") != kernel_source_hash():
         return None
-    ent = rec.get("workloads", {}).get(wl.name)
+    ent = rec.get("workloads", {}).get(name)
     return None if ent is None else ent.get("dram_bytes_per_launch")
 
 
@@ -551,6 +555,104 @@ def measure_decode(steps: int):
                        "d_state": wl.N, "io_dtype": "bf16", "tokens": steps}}
 
 
+BWD_NAME = "mamba130m_layer_bwd_b8_d1536_l2048_n16"
+# Algorithmic fp32 lane operations of the backward pass (an FMA counts once):
+# per element and state, the state recompute (Delta'*A, x*B, the state FMA, the
+# readout FMA: 4) and the reverse recurrence (dh FMA, carry, two products for
+# the Abar term, dDelta', dA and sum_n dh*B FMAs, dB and dC products and their
+# sums over channels: 11); per element about 20 more (softplus, sigmoid, SiLU
+# and its derivative, the du, ddelta and dz epilogue).
+BWD_OPS_PER_STATE = 15
+BWD_OPS_PER_ELEM = 20
+FP32_LANES_PER_SM = 128
+
+
+def bwd_algorithmic_bytes(wl: wk.Workload) -> int:
+    """u, delta, z, dout read and du, ddelta, dz written once; B, C read and dB,
+    dC (fp32) written once per group; A, D, bias read and their gradients written."""
+    es = 2 if wl.io == "bf16" else 4
+    per_chan = wl.batch * wl.dim * wl.L * es
+    bc = wl.batch * wl.G * wl.N * wl.L
+    return 7 * per_chan + 2 * bc * es + 2 * bc * 4 + 2 * wl.dim * (wl.N + 2) * 4
+
+
+def measure_bwd(steps: int, warmup: int, peak_gbs: float, peak_kind: str):
+    """Backward pass of the Mamba-130M layer shape (8 x 1536 x 2048, N = 16,
+    bf16 I/O): one ss_selective_scan_bwd call per step on resident inputs,
+    rotating over two input sets (each larger than L2)."""
+    import torch
+    from selective_state_space_120_b300 import _binding as b
+    wl = wk.MAMBA_LAYER
+    lib = b.load()
+    inp = wk.make_inputs(wl, 0)
+    dout = wk.make_dout(wl, 0)
+    dev = lambda a: None if a is None else Runner._to_dev(a)  # noqa: E731
+    base = {"u": dev(inp.u), "delta": dev(inp.delta[:, 0]), "A": dev(inp.A),
+            "B": dev(inp.B[:, 0]), "C": dev(inp.C[:, 0]), "D": dev(inp.D), "z": dev(inp.z),
+            "bias": dev(inp.delta_bias), "dout": dev(dout)}
+    f32 = dict(dtype=torch.float32, device="cuda")
+    sets = []
+    for i in range(2):
+        s = {k: (v if i == 0 else v.clone()) for k, v in base.items()}
+        s.update(du=torch.empty_like(s["u"]), ddelta=torch.empty_like(s["u"]),
+                 dz=torch.empty_like(s["u"]), dA=torch.empty(wl.dim, wl.N, **f32),
+                 dB=torch.empty(wl.batch, wl.G, wl.N, wl.L, **f32),
+                 dC=torch.empty(wl.batch, wl.G, wl.N, wl.L, **f32),
+                 dD=torch.empty(wl.dim, **f32), dbias=torch.empty(wl.dim, **f32))
+        sets.append(s)
+    wsb = int(lib.ss_workspace_bytes(b.SS_KIND_SCAN_BWD, wl.batch, wl.dim, wl.L, wl.N))
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    st = ctypes.c_void_p(stream.cuda_stream)
+    p = lambda t: t.data_ptr()  # noqa: E731
+    calls = [(wl.batch, wl.dim, wl.L, wl.N, wl.G, 1, p(s["u"]), p(s["delta"]), p(s["A"]),
+              p(s["B"]), p(s["C"]), p(s["D"]), p(s["z"]), p(s["bias"]), 1, p(s["dout"]),
+              p(s["du"]), p(s["ddelta"]), p(s["dA"]), p(s["dB"]), p(s["dC"]), p(s["dD"]),
+              p(s["dz"]), p(s["dbias"]), p(ws), wsb, st) for s in sets]
+
+    def step(i):
+        b.check(lib.ss_selective_scan_bwd(*calls[i % 2]))
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    import selective_state_space_120_b300 as ss
+    ss.device_status()
+    ms = float(np.mean([a.elapsed_time(c) for a, c in ev]))
+    props = torch.cuda.get_device_properties(0)
+    max_mhz = 2032
+    try:
+        max_mhz = _Nvml(torch.cuda.current_device()).sm_max_mhz() or max_mhz
+    except Exception:  # noqa: BLE001 -- NVML missing: the B300's maximum SM clock
+        pass
+    peak_tops = props.multi_processor_count * FP32_LANES_PER_SM * max_mhz * 1e6 / 1e12
+    ops = wl.elems * (wl.N * BWD_OPS_PER_STATE + BWD_OPS_PER_ELEM)
+    ach = ops / (ms * 1e-3) / 1e12
+    alg = bwd_algorithmic_bytes(wl)
+    return {"value": wl.elems / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
+            "kernel_launches_per_step": 1, "memsets_per_step": 5,
+            "roofline": {"bound": "alu", "achieved": ach, "peak": peak_tops, "unit": "TFLOP/s",
+                         "frac": ach / peak_tops,
+                         "peak_source": f"fp32 lane ops: {props.multi_processor_count} SMs x "
+                                        f"{FP32_LANES_PER_SM} lanes x {max_mhz} MHz",
+                         "ops_per_launch": ops,
+                         "hbm_achieved_gbs": alg / (ms * 1e-3) / 1e9,
+                         "hbm_frac": alg / (ms * 1e-3) / 1e9 / peak_gbs,
+                         "hbm_peak_source": peak_kind,
+                         "algorithmic_bytes_per_launch": alg, "traffic": ncu_traffic_named(BWD_NAME)},
+            "config": {"workload": BWD_NAME, "batch": wl.batch, "dim": wl.dim,
+                       "seq_len": wl.L, "d_state": wl.N, "groups": wl.G, "io_dtype": "bf16",
+                       "z_gate": True, "d_skip": True, "delta_softplus": True,
+                       "l2": "inputs rotate over 2 copies (201 MB of inputs each > 126 MB L2)"}}
+
+
 def roofline(wl, kern_ms, peak, peak_kind):
     alg = algorithmic_bytes(wl)
     ach = alg / (kern_ms * 1e-3) / 1e9
@@ -621,6 +723,11 @@ def main(argv=None):
             others[DECODE_NAME] = measure_decode(256)
         except Exception as e:  # noqa: BLE001 -- reported, not hidden
             others[DECODE_NAME] = {"error": f"{type(e).__name__}: {e}"}
+        try:
+            others[BWD_NAME] = measure_bwd(max(3, min(args.steps, 30)), 3, peak, peak_kind)
+            torch.cuda.empty_cache()
+        except Exception as e:  # noqa: BLE001 -- reported, not hidden
+            others[BWD_NAME] = {"error": f"{type(e).__name__}: {e}"}
 
     cpu = None
     if rank == 0 and not args.no_cpu:

@@ -83,6 +83,7 @@ typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
 #define SS_KIND_SCAN 0
 #define SS_KIND_BIDIR 1
 #define SS_KIND_CROSS2D 2
+#define SS_KIND_SCAN_BWD 3 /* ss_selective_scan_bwd */
 
 /*
  * ss_selective_scan_fwd -- one forward direction (Mamba S6 selective scan).
@@ -280,6 +281,43 @@ ss_status ss_selective_state_update(int64_t batch, int64_t dim, int dstate, int 
                                     const float *D, const void *z, const float *delta_bias,
                                     int delta_softplus, unsigned int flags, float *state,
                                     void *out, ss_stream_t stream);
+
+/*
+ * ss_selective_scan_bwd -- gradients of ss_selective_scan_fwd (Euler input
+ * matrix, zero initial state, no options) for an upstream gradient `dout` of
+ * out.  The forward call computes ("Mamba Series from Selective State Spaces
+ * to Visual State Space Models": mathematical form of the selective SSM, and
+ * the Mamba Block (1D) diagram)
+ *     Delta'_t = softplus(delta_t + delta_bias)   (delta_t + delta_bias without the flag)
+ *     h_t = exp(Delta'_t A) h_{t-1} + Delta'_t B_t u_t,   h_{-1} = 0
+ *     out_t = (C_t . h_t + D u_t) * SiLU(z_t)
+ * and this call writes its derivatives:
+ *   du, ddelta   [batch, dim, seqlen]             io     (ddelta is w.r.t. the raw delta)
+ *   dz           [batch, dim, seqlen]             io     required iff z is given, else NULL
+ *   dA           [dim, dstate]                    float  summed over batch and time
+ *   dB, dC       [batch, ngroups, dstate, seqlen] float  summed over the group's channels
+ *   dD           [dim]                            float  nullable; summed over batch and time
+ *   ddelta_bias  [dim]                            float  nullable; summed over batch and time
+ * The inputs u ... delta_softplus are the forward call's (same layouts and
+ * rules), and dout [batch, dim, seqlen] is io.  The forward call keeps no
+ * intermediate states; this call recomputes them, holding a checkpoint every 16
+ * steps in `workspace`: at least ss_workspace_bytes(SS_KIND_SCAN_BWD, batch,
+ * dim, seqlen, dstate) = batch*dim*ceil(seqlen/16)*dstate*4 bytes, 16-byte
+ * aligned, contents ignored.  Rows must be 16-byte aligned (seqlen * element
+ * size % 16 == 0), else SS_ERR_UNSUPPORTED.  All pointers are device pointers,
+ * 16-byte aligned; no output may overlap an input, another output or the
+ * workspace.  Outputs are overwritten: the summed ones are zeroed on `stream`
+ * first, then accumulated with fp32 atomic adds, so their last bits may differ
+ * between calls.  With batch, dim or seqlen = 0 the summed outputs are zeroed
+ * and nothing else is touched.  Asynchronous on `stream`.
+ */
+ss_status ss_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, int dstate,
+                                int ngroups, ss_dtype io, const void *u, const void *delta,
+                                const float *A, const void *B, const void *C, const float *D,
+                                const void *z, const float *delta_bias, int delta_softplus,
+                                const void *dout, void *du, void *ddelta, float *dA, float *dB,
+                                float *dC, float *dD, void *dz, float *ddelta_bias,
+                                void *workspace, size_t workspace_bytes, ss_stream_t stream);
 
 /* Workspace bytes a call of the given kind and shape needs (0 if none), for
  * either I/O dtype (the larger of the two).  For SS_KIND_CROSS2D pass

@@ -8,6 +8,7 @@ in the library's sm_103a kernels; there is no fallback.
     out = selective_scan_fwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus=True)
     out = bidir_scan_fwd(u, delta2, A2, B2, C2, D2, z, bias2)
     out = cross_scan2d_fwd(u_map, delta4, A4, B4, C4, D4, bias4)
+    grads = selective_scan_bwd(u, delta, A, B, C, dout, D, z, delta_bias)
 
 u, z and out are indexed by position; each direction's delta, B and C are in
 that direction's scan order.
@@ -117,6 +118,48 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta
         _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(out), _ptr(last),
         ws_ptr, ws_len, ctypes.byref(opts), _stream(stream, dev)))
     return (out, last) if return_last_state else out
+
+
+def selective_scan_bwd(u, delta, A, B, C, dout, D=None, z=None, delta_bias=None,
+                       delta_softplus=True, workspace=None, stream=None):
+    """Gradients of :func:`selective_scan_fwd` (Euler, zero initial state, no
+    options) for the upstream gradient ``dout`` [batch, dim, L] of its output.
+
+    Returns a dict: du, ddelta [batch, dim, L] and dz (None without z) in the
+    I/O dtype; dA [dim, N], dB, dC [batch, G, N, L], dD (None without D) and
+    ddelta_bias (None without delta_bias) in float32.  ``workspace`` is an
+    optional preallocated uint8 CUDA tensor for the 16-step state checkpoints."""
+    torch = _torch()
+    lib = _b.load()
+    batch, dim, L = u.shape
+    G, N = B.shape[1], B.shape[2]
+    io, dev = u.dtype, u.device
+    _check_io("u", u, io, dev)
+    for name, t in (("delta", delta), ("z", z), ("dout", dout)):
+        _check_io(name, t, io, dev, (batch, dim, L))
+    _check_io("B", B, io, dev, (batch, G, N, L))
+    _check_io("C", C, io, dev, (batch, G, N, L))
+    _check_io("A", A, torch.float32, dev, (dim, N))
+    _check_io("D", D, torch.float32, dev, (dim,))
+    _check_io("delta_bias", delta_bias, torch.float32, dev, (dim,))
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = {"du": torch.empty_like(u), "ddelta": torch.empty_like(u),
+         "dz": torch.empty_like(u) if z is not None else None,
+         "dA": torch.empty(dim, N, **f32), "dB": torch.empty(batch, G, N, L, **f32),
+         "dC": torch.empty(batch, G, N, L, **f32),
+         "dD": torch.empty(dim, **f32) if D is not None else None,
+         "ddelta_bias": torch.empty(dim, **f32) if delta_bias is not None else None}
+    wsb = int(lib.ss_workspace_bytes(_b.SS_KIND_SCAN_BWD, batch, dim, L, N))
+    if wsb and (workspace is None or workspace.numel() < wsb):
+        workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    _b.check(lib.ss_selective_scan_bwd(
+        batch, dim, L, N, G, _io_code(u), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+        _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(dout),
+        _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+        _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["ddelta_bias"]),
+        _ptr(workspace) if wsb else None, workspace.numel() if wsb else 0,
+        _stream(stream, dev)))
+    return g
 
 
 def _multidir_workspace(lib, kind, batch, dim, L, N, dev, workspace):

@@ -22,7 +22,7 @@ SS_ERR_CUDA = 5
 SS_ERR_TIMEOUT = 6
 SS_F32 = 0
 SS_BF16 = 1
-SS_KIND_SCAN, SS_KIND_BIDIR, SS_KIND_CROSS2D = 0, 1, 2
+SS_KIND_SCAN, SS_KIND_BIDIR, SS_KIND_CROSS2D, SS_KIND_SCAN_BWD = 0, 1, 2, 3
 SS_DEBUG_SKIP_FIRST_COPY = 1
 SS_NOALLOC_SCRATCH_BYTES = 16 << 20
 STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_ARG", 2: "SS_ERR_UNSUPPORTED",
@@ -34,7 +34,8 @@ EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_opts", "ss_bidir_scan
            "ss_cross_scan2d_fwd", "ss_workspace_bytes", "ss_workspace_bytes_opts",
            "ss_get_device_status", "ss_last_error_string", "ss_version",
            "ss_debug_set_wait_budget_ns", "ss_debug_set_flags",
-           "ss_selective_scan_fwd_noalloc", "ss_selective_state_update")
+           "ss_selective_scan_fwd_noalloc", "ss_selective_state_update",
+           "ss_selective_scan_bwd")
 
 
 class SSError(RuntimeError):
@@ -79,10 +80,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             ctypes.POINTER(ScanOptions), vp]
         lib.ss_cross_scan2d_fwd.argtypes = [i64, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp,
                                             vp, vp, i32, vp, vp, vp, vp, sz, vp]
+        # u ... delta_softplus as the forward call, then dout, du, ddelta, dA, dB, dC, dD, dz,
+        # ddelta_bias, workspace, workspace_bytes, stream
+        lib.ss_selective_scan_bwd.argtypes = scan_args[:15] + [vp] * 9 + [vp, sz, vp]
         for f in ("ss_selective_scan_fwd", "ss_selective_scan_fwd_opts", "ss_bidir_scan_fwd",
                   "ss_cross_scan2d_fwd", "ss_get_device_status", "ss_debug_set_wait_budget_ns",
                   "ss_debug_set_flags", "ss_selective_scan_fwd_noalloc",
-                  "ss_selective_state_update"):
+                  "ss_selective_state_update", "ss_selective_scan_bwd"):
             getattr(lib, f).restype = ctypes.c_int
         lib.ss_workspace_bytes.argtypes = [i32, i64, i64, i64, i32]
         lib.ss_workspace_bytes.restype = sz

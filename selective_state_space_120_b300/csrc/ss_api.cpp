@@ -205,6 +205,58 @@ size_t ws_multidir_any_dtype(int64_t batch, int64_t dim, int64_t L, int dstate, 
     return best;
 }
 
+// Backward pass: required gradient pointers, alignment, and that no output
+// overlaps an input, another output or the workspace.
+ss_status check_bwd(const char *fn, int64_t batch, int64_t dim, int64_t L, int N, int G, int io,
+                    const void *u, const void *delta, const float *A, const void *B,
+                    const void *C, const float *D, const void *z, const float *bias,
+                    const void *dout, const void *du, const void *ddelta, const float *dA,
+                    const float *dB, const float *dC, const float *dD, const void *dz,
+                    const float *dbias, const void *ws, size_t ws_bytes) {
+    if (!dout || !du || !ddelta || !dA || !dB || !dC)
+        return fail(SS_ERR_INVALID_ARG, "%s: dout, du, ddelta, dA, dB and dC are required", fn);
+    if (z && !dz) return fail(SS_ERR_INVALID_ARG, "%s: dz is required when z is given", fn);
+    if (!z && dz) return fail(SS_ERR_INVALID_ARG, "%s: dz given without z", fn);
+    for (const void *q : {dout, du, ddelta, (const void *)dA, (const void *)dB, (const void *)dC,
+                          (const void *)dD, dz, (const void *)dbias})
+        if (q && !aligned16(q))
+            return fail(SS_ERR_ALIGNMENT, "%s: tensor at %p is not 16-byte aligned", fn, q);
+    const int64_t es = io == SS_BF16 ? 2 : 4;
+    if ((L * es) % 16 != 0)
+        return fail(SS_ERR_UNSUPPORTED,
+                    "%s: rows must be 16-byte aligned (seqlen * element size %% 16 == 0)", fn);
+    const int64_t nel = batch * dim * L;
+    const int64_t nbc = batch * G * N * L;
+    const Span outs[] = {{static_cast<const char *>(du), nel * es},
+                         {static_cast<const char *>(ddelta), nel * es},
+                         {static_cast<const char *>(dz), dz ? nel * es : 0},
+                         {reinterpret_cast<const char *>(dA), dim * N * 4},
+                         {reinterpret_cast<const char *>(dB), nbc * 4},
+                         {reinterpret_cast<const char *>(dC), nbc * 4},
+                         {reinterpret_cast<const char *>(dD), dD ? dim * 4 : 0},
+                         {reinterpret_cast<const char *>(dbias), dbias ? dim * 4 : 0},
+                         {static_cast<const char *>(ws), ws ? (int64_t)ws_bytes : 0}};
+    const Span ins[] = {{static_cast<const char *>(u), nel * es},
+                        {static_cast<const char *>(delta), nel * es},
+                        {reinterpret_cast<const char *>(A), dim * N * 4},
+                        {static_cast<const char *>(B), nbc * es},
+                        {static_cast<const char *>(C), nbc * es},
+                        {reinterpret_cast<const char *>(D), D ? dim * 4 : 0},
+                        {static_cast<const char *>(z), z ? nel * es : 0},
+                        {reinterpret_cast<const char *>(bias), bias ? dim * 4 : 0},
+                        {static_cast<const char *>(dout), nel * es}};
+    const int nout = sizeof(outs) / sizeof(outs[0]);
+    for (int i = 0; i < nout; ++i) {
+        for (const Span &t : ins)
+            if (overlaps(outs[i], t))
+                return fail(SS_ERR_INVALID_ARG, "%s: a gradient output or the workspace overlaps an input", fn);
+        for (int j = i + 1; j < nout; ++j)
+            if (overlaps(outs[i], outs[j]))
+                return fail(SS_ERR_INVALID_ARG, "%s: two gradient outputs (or the workspace) overlap", fn);
+    }
+    return SS_OK;
+}
+
 }  // namespace
 
 ss_status fail(ss_status st, const char *fmt, ...) {
@@ -376,10 +428,49 @@ ss_status ss_selective_state_update(int64_t batch, int64_t dim, int dstate, int 
     return launch_step(a, state);
 }
 
+ss_status ss_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, int dstate,
+                                int ngroups, ss_dtype io, const void *u, const void *delta,
+                                const float *A, const void *B, const void *C, const float *D,
+                                const void *z, const float *delta_bias, int delta_softplus,
+                                const void *dout, void *du, void *ddelta, float *dA, float *dB,
+                                float *dC, float *dD, void *dz, float *ddelta_bias,
+                                void *workspace, size_t workspace_bytes, ss_stream_t stream) {
+    static const char *fn = "ss_selective_scan_bwd";
+    bool empty = false;
+    ss_status st = check_common(fn, batch, dim, seqlen, dstate, ngroups, io, 1, u, delta, A, B, C,
+                                D, z, delta_bias, du, nullptr, &empty);
+    if (st != SS_OK) return st;
+    BwdArgs a;
+    a.f = scan_args(batch, dim, seqlen, dstate, ngroups, io, u, delta, A, B, C, D, z, delta_bias,
+                    delta_softplus, nullptr, nullptr, nullptr, 0, stream);
+    a.dout = dout;
+    a.du = du;
+    a.ddelta = ddelta;
+    a.dz = dz;
+    a.dA = dA;
+    a.dB = dB;
+    a.dC = dC;
+    a.dD = dD;
+    a.dbias = ddelta_bias;
+    a.ws = workspace;
+    a.ws_bytes = workspace_bytes;
+    if (empty) return launch_scan_bwd(a, true);  // the gradient of an empty sum is zero
+    if ((st = check_bwd(fn, batch, dim, seqlen, dstate, ngroups, io, u, delta, A, B, C, D, z,
+                        delta_bias, dout, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias, workspace,
+                        workspace_bytes)))
+        return st;
+    if ((st = check_workspace(fn, scan_bwd_workspace_bytes(batch, dim, seqlen, dstate), workspace,
+                              workspace_bytes)))
+        return st;
+    return launch_scan_bwd(a, false);
+}
+
 size_t ss_workspace_bytes_opts(int kind, int64_t batch, int64_t dim, int64_t seqlen, int dstate,
                                const ss_scan_options *options) {
     if (kind == SS_KIND_BIDIR || kind == SS_KIND_CROSS2D)
         return ws_multidir_any_dtype(batch, dim, seqlen, dstate, kind == SS_KIND_BIDIR ? 2 : 4);
+    if (kind == SS_KIND_SCAN_BWD)
+        return valid_dstate(dstate) ? scan_bwd_workspace_bytes(batch, dim, seqlen, dstate) : 0;
     if (kind != SS_KIND_SCAN) return 0;
     return ws_scan1d_any_dtype(batch, dim, seqlen, dstate, options ? options->chunks : 0);
 }

@@ -32,6 +32,19 @@ struct ScanArgs {
     ss_stream_t stream = nullptr;
 };
 
+// Backward pass of one direction: the forward call's inputs in `f` (its out,
+// last_state and workspace fields unused), the upstream gradient and the
+// gradient outputs.
+struct BwdArgs {
+    ScanArgs f;
+    const void *dout = nullptr;
+    void *du = nullptr, *ddelta = nullptr, *dz = nullptr;  // I/O type
+    float *dA = nullptr, *dB = nullptr, *dC = nullptr;     // fp32
+    float *dD = nullptr, *dbias = nullptr;                 // fp32, nullable
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+};
+
 // Direction traversal codes used by the kernels (match SS_DIR_*).
 enum { ORD_ROW = 0, ORD_COL = 1, ORD_ROW_REV = 2, ORD_COL_REV = 3 };
 
@@ -50,6 +63,11 @@ ss_status launch_scan1d(const ScanArgs &a);
 // One recurrence step (seqlen 1) updating `state` [batch*dim, N] in place.
 ss_status launch_step(const ScanArgs &a, float *state);
 ss_status launch_multidir(const ScanArgs &a);
+// Checkpoint workspace of the backward pass: 16-step state checkpoints, fp32.
+size_t scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t L, int N);
+// Zeroes the summed gradient outputs, then runs the backward kernel (nothing
+// but the zeroing when `empty`).
+ss_status launch_scan_bwd(const BwdArgs &a, bool empty);
 ss_status read_device_status(ss_stream_t stream);
 ss_status set_wait_budget(unsigned long long ns);
 ss_status set_debug_flags(unsigned int flags);

@@ -7,6 +7,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "ss_bwd.cuh"
 #include "ss_device.cuh"
 #include "ss_internal.h"
 #include "ss_multidir.cuh"
@@ -498,6 +499,99 @@ ss_status launch_step_io(const ScanArgs &a, float *state) {
 
 ss_status launch_step(const ScanArgs &a, float *state) {
     return a.io == SS_BF16 ? launch_step_io<__nv_bfloat16>(a, state) : launch_step_io<float>(a, state);
+}
+
+// ---------------------------------------------------------------- backward
+namespace {
+constexpr int kBwdBlock = 16;  // steps between state checkpoints (CfgB::TS)
+
+template <class C>
+ss_status run_scan_bwd(const BwdArgs &a) {
+    using namespace ssk;
+    static_assert(C::TS == kBwdBlock, "checkpoint interval");
+    const ScanArgs &f = a.f;
+    const int io = f.io;
+    const int64_t rows = f.batch * f.dim;
+    const uint64_t bcrows = (uint64_t)f.batch * f.G * C::N;
+    CUtensorMap mu, md, mz, mdy, mb, mc;
+    ss_status st;
+    if ((st = make_map(&mu, f.u, io, f.L, rows, C::T, C::CB))) return st;
+    if ((st = make_map(&md, f.delta, io, f.L, rows, C::T, C::CB))) return st;
+    if ((st = make_map(&mz, f.z ? f.z : f.u, io, f.L, rows, C::T, C::CB))) return st;
+    if ((st = make_map(&mdy, a.dout, io, f.L, rows, C::T, C::CB))) return st;
+    if ((st = make_map(&mb, f.B, io, f.L, bcrows, C::T, C::N))) return st;
+    if ((st = make_map(&mc, f.C, io, f.L, bcrows, C::T, C::N))) return st;
+    auto kern = k_scan_bwd<C>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+        return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
+    BwdParams p{};
+    p.dim = f.dim;
+    p.L = f.L;
+    p.G = f.G;
+    p.dpg = (int)(f.dim / f.G);
+    p.nblk = (int)((f.L + kBwdBlock - 1) / kBwdBlock);
+    p.A = f.A;
+    p.D = f.D;
+    p.bias = f.bias;
+    p.softplus = f.softplus;
+    p.has_z = f.z != nullptr;
+    p.ckpt = reinterpret_cast<float *>(a.ws);
+    p.du = a.du;
+    p.ddelta = a.ddelta;
+    p.dz = a.dz;
+    p.dA = a.dA;
+    p.dB = a.dB;
+    p.dC = a.dC;
+    p.dD = a.dD;
+    p.dbias = a.dbias;
+    const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);
+    const unsigned bgs = (unsigned)(f.batch * f.G);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(f.stream);
+    kern<<<dim3(cblocks, bgs, 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mdy, mb, mc, p);
+    return check_launch("scan backward");
+}
+
+template <typename IO>
+ss_status dispatch_bwd(const BwdArgs &a) {
+    using namespace ssk;
+    switch (a.f.N) {
+    case 1: return run_scan_bwd<CfgB<IO, 1, 2>>(a);
+    case 2: return run_scan_bwd<CfgB<IO, 2, 2>>(a);
+    case 4: return run_scan_bwd<CfgB<IO, 4, 2>>(a);
+    case 8: return run_scan_bwd<CfgB<IO, 8, 4>>(a);
+    case 16: return run_scan_bwd<CfgB<IO, 16, 4>>(a);
+    case 32: return run_scan_bwd<CfgB<IO, 32, 4>>(a);
+    case 64: return run_scan_bwd<CfgB<IO, 64, 4>>(a);
+    default: return fail(SS_ERR_UNSUPPORTED, "dstate %d is not one of 1,2,4,8,16,32,64", a.f.N);
+    }
+}
+
+ss_status zero_async(void *p, size_t bytes, cudaStream_t s) {
+    if (!p || bytes == 0) return SS_OK;
+    const cudaError_t e = cudaMemsetAsync(p, 0, bytes, s);
+    if (e != cudaSuccess) return fail(SS_ERR_CUDA, "cudaMemsetAsync failed: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+}  // namespace
+
+size_t scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t L, int N) {
+    if (batch <= 0 || dim <= 0 || L <= 0 || N <= 0) return 0;
+    return (size_t)batch * dim * ((L + kBwdBlock - 1) / kBwdBlock) * N * sizeof(float);
+}
+
+ss_status launch_scan_bwd(const BwdArgs &a, bool empty) {
+    const ScanArgs &f = a.f;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(f.stream);
+    // outputs that are sums (over batch, time or channels) start from zero
+    const size_t bc = (size_t)f.batch * f.G * f.N * f.L * sizeof(float);
+    ss_status st;
+    if ((st = zero_async(a.dA, (size_t)f.dim * f.N * sizeof(float), s))) return st;
+    if ((st = zero_async(a.dB, bc, s))) return st;
+    if ((st = zero_async(a.dC, bc, s))) return st;
+    if ((st = zero_async(a.dD, (size_t)f.dim * sizeof(float), s))) return st;
+    if ((st = zero_async(a.dbias, (size_t)f.dim * sizeof(float), s))) return st;
+    if (empty) return SS_OK;
+    return f.io == SS_BF16 ? dispatch_bwd<__nv_bfloat16>(a) : dispatch_bwd<float>(a);
 }
 
 ss_status read_device_status(ss_stream_t stream) {

@@ -15,6 +15,8 @@ Recipe (the workloads of the Mamba / Vim / VMamba pages, with synthetic data):
     B_k, C_k        ~ N(0, 1)                           [batch, K, G, N, L]
     D               = 1                                 [K*dim]
     conv workloads, drawn last: conv_w ~ N(0, 0.5^2) [dim, 4], conv_b ~ N(0, 0.1^2)
+    backward pass: the upstream gradient dout ~ N(0, 1) [batch, dim, L], from
+                   its own PCG64 stream seeded with (seed, 1) (make_dout)
 Inputs of a bf16 workload are rounded to bf16 (round-to-nearest-even) on the
 host; A, D and delta_bias stay float32.
 """
@@ -150,6 +152,14 @@ def make_inputs(wl: Workload, seed: int = 0) -> Inputs:
         inp.conv_w = (rng.standard_normal((d, 4)) * 0.5).astype(np.float32)
         inp.conv_b = (rng.standard_normal(d) * 0.1).astype(np.float32)
     return inp
+
+
+def make_dout(wl: Workload, seed: int = 0) -> np.ndarray:
+    """Upstream gradient of the scan's output for the backward pass, in the
+    workload's I/O representation (float32, or bf16 bits in uint16)."""
+    rng = np.random.Generator(np.random.PCG64([seed, 1]))
+    g = _normal(rng, (wl.batch, wl.dim, wl.L))
+    return round_bf16_bits(g) if wl.io == "bf16" else g
 
 
 def scaled(wl: Workload, name: str | None = None, **changes) -> Workload:

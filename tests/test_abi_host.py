@@ -206,3 +206,49 @@ def test_workspace_sizing_is_host_only(lib):
     assert b.workspace_bytes(b.SS_KIND_SCAN, 0, 8, 4096, 16) == 0
     # long sequence with few rows: the automatic choice splits it
     assert b.workspace_bytes(b.SS_KIND_SCAN, 1, 5120, 131072, 16) > 0
+
+
+def _bwd_args(batch=1, dim=8, L=32, N=16, G=1, io=b.SS_BF16, **kw):
+    """Arguments of ss_selective_scan_bwd with fake aligned addresses, each
+    tensor in its own 1 MiB window; keyword overrides by name."""
+    names = ("u", "delta", "A", "B", "C", "D", "z", "bias", "dout", "du", "ddelta", "dA", "dB",
+             "dC", "dD", "dz", "dbias", "ws")
+    ptr = {n: A16 + i * 0x100000 for i, n in enumerate(names)}
+    for n in ("D", "z", "bias", "dD", "dz", "dbias"):
+        ptr[n] = None
+    wsb = kw.pop("wsb", b.workspace_bytes(b.SS_KIND_SCAN_BWD, batch, dim, L, N))
+    ptr.update(kw)
+    return (batch, dim, L, N, G, io, ptr["u"], ptr["delta"], ptr["A"], ptr["B"], ptr["C"],
+            ptr["D"], ptr["z"], ptr["bias"], 1, ptr["dout"], ptr["du"], ptr["ddelta"], ptr["dA"],
+            ptr["dB"], ptr["dC"], ptr["dD"], ptr["dz"], ptr["dbias"], ptr["ws"], wsb, None)
+
+
+@fake_ptrs
+def test_backward_validates(lib):
+    bwd = lib.ss_selective_scan_bwd
+    assert bwd(*_bwd_args(dout=None)) == b.SS_ERR_INVALID_ARG
+    assert bwd(*_bwd_args(dC=None)) == b.SS_ERR_INVALID_ARG
+    # dz exactly when z is given
+    assert bwd(*_bwd_args(z=A16 + 0x6_000000)) == b.SS_ERR_INVALID_ARG
+    assert "dz is required" in b.last_error()
+    assert bwd(*_bwd_args(dz=A16 + 0x6_000000)) == b.SS_ERR_INVALID_ARG
+    assert bwd(*_bwd_args(dB=A16 + 0x4_000008)) == b.SS_ERR_ALIGNMENT
+    # rows of 20 bf16 values are not 16-byte aligned
+    assert bwd(*_bwd_args(L=20)) == b.SS_ERR_UNSUPPORTED
+    assert bwd(*_bwd_args(N=12)) == b.SS_ERR_UNSUPPORTED
+    # a gradient output on top of an input, or two outputs on top of each other
+    assert bwd(*_bwd_args(du=A16 + 0x100000)) == b.SS_ERR_INVALID_ARG
+    assert bwd(*_bwd_args(dA=A16 + 0xa00000)) == b.SS_ERR_INVALID_ARG
+    assert bwd(*_bwd_args(ws=A16 + 0x900000)) == b.SS_ERR_INVALID_ARG
+    # workspace missing or short
+    assert bwd(*_bwd_args(ws=None)) == b.SS_ERR_WORKSPACE
+    assert bwd(*_bwd_args(wsb=b.workspace_bytes(b.SS_KIND_SCAN_BWD, 1, 8, 32, 16) - 1)) == \
+        b.SS_ERR_WORKSPACE
+
+
+def test_backward_workspace_is_one_checkpoint_per_16_steps(lib):
+    # [batch*dim, ceil(L/16), N] float32
+    assert b.workspace_bytes(b.SS_KIND_SCAN_BWD, 8, 1536, 2048, 16) == 8 * 1536 * 128 * 16 * 4
+    assert b.workspace_bytes(b.SS_KIND_SCAN_BWD, 2, 3, 17, 4) == 2 * 3 * 2 * 4 * 4
+    assert b.workspace_bytes(b.SS_KIND_SCAN_BWD, 2, 3, 0, 4) == 0
+    assert b.workspace_bytes(b.SS_KIND_SCAN_BWD, 2, 3, 64, 12) == 0

@@ -1,0 +1,218 @@
+"""GPU parity of the backward pass: ss_selective_scan_bwd against the float64
+oracle's gradients (oracle.selective_scan_bwd), on the same seeded inputs and
+upstream gradient (B300 only).
+
+Tolerance.  Each gradient tensor g with float64 reference r must satisfy
+    max |g - r| / (rms(r) + |r|) <= 1e-3 (float32 I/O) or 1e-2 (bf16 I/O).
+The float32 arithmetic follows chains of up to 1/(Delta' |A|) ~ 1000 steps
+(Delta' >= 1e-3 in the workload recipe, |A| >= 1), along which the relative
+error of the hardware exponential (about 2^-22) compounds to ~2.4e-4; the
+bf16 outputs (du, ddelta, dz) add their rounding of 2^-9.  dA, dB, dC, dD and
+ddelta_bias are sums with cancellation over batch, time or channels, so the
+scale is the tensor's rms rather than 1.
+"""
+import numpy as np
+import pytest
+
+from selective_state_space_120_b300 import workloads as wk
+from tests import scan_cases as sc
+
+pytestmark = pytest.mark.gpu
+
+TOL_BWD = {"f32": 1e-3, "bf16": 1e-2}
+NAMES = ("du", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddelta_bias")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import selective_state_space_120_b300 as ss
+    ss.load_library()
+
+
+def _dout_f64(wl, dout):
+    return (wk.bf16_bits_to_f32(dout) if wl.io == "bf16" else dout).astype(np.float64)
+
+
+def gpu_bwd(inp, dout, use_D=True, use_z=True, use_bias=True, softplus=True, workspace=None):
+    import selective_state_space_120_b300 as ss
+    t = sc.device_inputs(inp)
+    g = ss.selective_scan_bwd(t["u"], t["delta"][:, 0], t["A"], t["B"][:, 0], t["C"][:, 0],
+                              sc.to_torch(dout), t["D"] if use_D else None,
+                              t["z"] if use_z else None,
+                              t["delta_bias"] if use_bias else None, softplus,
+                              workspace=workspace)
+    return {k: (None if v is None else sc.from_torch(v)) for k, v in g.items()}
+
+
+def oracle_bwd(oracle, inp, dout, use_D=True, use_z=True, use_bias=True, softplus=True):
+    return oracle.selective_scan_bwd(
+        inp.as_f64("u"), inp.as_f64("delta")[:, 0], inp.as_f64("A"), inp.as_f64("B")[:, 0],
+        inp.as_f64("C")[:, 0], _dout_f64(inp.wl, dout),
+        D=inp.as_f64("D") if use_D else None, z=inp.as_f64("z") if use_z else None,
+        delta_bias=inp.as_f64("delta_bias") if use_bias else None, delta_softplus=softplus)
+
+
+def grad_err(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), "non-finite gradient"
+    scale = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    den = scale + np.abs(ref)
+    diff = np.abs(got - ref)
+    if not np.any(den > 0):
+        return float(np.max(diff)) if diff.size else 0.0
+    return float(np.max(np.where(den > 0, diff / np.where(den > 0, den, 1.0), diff)))
+
+
+def assert_grads(got, ref, io, names=NAMES):
+    errs = {}
+    for k in names:
+        if ref[k] is None:
+            assert got[k] is None, k
+            continue
+        e = grad_err(got[k], ref[k])
+        errs[k] = e
+        assert e <= TOL_BWD[io], f"{k}: error {e:.3e} > {TOL_BWD[io]:.0e} (errors so far {errs})"
+    return errs
+
+
+def _check(oracle, wl, **kw):
+    inp = wk.make_inputs(wl, seed=0)
+    dout = wk.make_dout(wl, seed=0)
+    return assert_grads(gpu_bwd(inp, dout, **kw), oracle_bwd(oracle, inp, dout, **kw), wl.io)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16, 32, 64])
+def test_bwd_all_dstates(oracle, io, N):
+    """Several channel blocks (the last one partly empty) and a ragged last
+    tile and checkpoint block (200 = 6 * 32 + 8 = 12 * 16 + 8 steps)."""
+    _check(oracle, sc.workload(f"bn{N}", 2, 40, 200, N=N, io=io))
+
+
+@pytest.mark.parametrize("L", [8, 16, 32, 48, 520])
+def test_bwd_lengths(oracle, L):
+    """Shorter than one tile, exactly one checkpoint block, one tile, and a
+    tail past the last checkpoint; groups of 18 channels sharing B and C."""
+    _check(oracle, sc.workload(f"bl{L}", 2, 36, L, G=2))
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bwd_without_gate_skip_bias(oracle, io):
+    wl = sc.workload(f"bopt_{io}", 2, 24, 136, io=io)
+    _check(oracle, wl, use_z=False)
+    _check(oracle, wl, use_D=False)
+    _check(oracle, wl, use_bias=False)
+
+
+def test_bwd_softplus_off(oracle):
+    """Without the softplus (and without a bias) Delta' is delta itself, and
+    ddelta = dDelta'."""
+    wl = sc.workload("bsp", 1, 20, 96, io="f32")
+    inp = wk.make_inputs(wl, seed=3)
+    # without softplus and bias Delta' is delta itself: keep it positive, so
+    # that Abar = exp(Delta' A) stays below 1
+    inp.delta = np.abs(inp.delta).astype(np.float32) + 0.01
+    dout = wk.make_dout(wl, seed=3)
+    got = gpu_bwd(inp, dout, softplus=False, use_bias=False)
+    ref = oracle_bwd(oracle, inp, dout, softplus=False, use_bias=False)
+    assert_grads(got, ref, wl.io)
+
+
+def test_bwd_long_row(oracle):
+    """4096 steps: 128 tiles and 256 checkpoints per row."""
+    _check(oracle, sc.workload("blong", 1, 48, 4096))
+
+
+def test_bwd_many_groups(oracle):
+    _check(oracle, sc.workload("bg4", 3, 64, 104, G=4, io="f32"))
+
+
+def test_bwd_repeatable(oracle):
+    """The summed outputs use atomic adds: two calls agree to float32 rounding,
+    and the per-element outputs are identical."""
+    wl = sc.workload("brep", 2, 96, 256)
+    inp = wk.make_inputs(wl, seed=1)
+    dout = wk.make_dout(wl, seed=1)
+    a = gpu_bwd(inp, dout)
+    b = gpu_bwd(inp, dout)
+    for k in ("du", "ddelta", "dz"):
+        assert np.array_equal(a[k], b[k]), k
+    for k in ("dA", "dB", "dC", "dD", "ddelta_bias"):
+        scale = np.max(np.abs(a[k])) + 1e-30
+        assert np.max(np.abs(a[k] - b[k])) <= 1e-5 * scale, k
+
+
+def test_bwd_empty_zeroes_sums():
+    import torch
+
+    import selective_state_space_120_b300 as ss
+    dev = torch.device("cuda")
+    u = torch.zeros(2, 8, 0, dtype=torch.bfloat16, device=dev)
+    B = torch.zeros(2, 1, 16, 0, dtype=torch.bfloat16, device=dev)
+    A = -torch.ones(8, 16, device=dev)
+    g = ss.selective_scan_bwd(u, u.clone(), A, B, B.clone(), u.clone(),
+                              D=torch.ones(8, device=dev), delta_bias=torch.zeros(8, device=dev))
+    torch.cuda.synchronize()
+    for k in ("dA", "dD", "ddelta_bias"):
+        assert torch.count_nonzero(g[k]).item() == 0, k
+
+
+def test_bwd_timeout_path_reports_and_recovers(oracle):
+    """With SS_DEBUG_SKIP_FIRST_COPY the first thread block never issues its
+    first tile's copies: its bounded wait runs out after the 2 ms budget, the
+    call reports SS_ERR_TIMEOUT through the device status, and the next call is
+    exact."""
+    import selective_state_space_120_b300 as ss
+    from selective_state_space_120_b300 import _binding as b
+    lib = b.load()
+    wl = sc.workload("bto", 2, 64, 512)
+    inp = wk.make_inputs(wl)
+    dout = wk.make_dout(wl)
+    ss.device_status()
+    b.check(lib.ss_debug_set_wait_budget_ns(2_000_000))
+    b.check(lib.ss_debug_set_flags(b.SS_DEBUG_SKIP_FIRST_COPY))
+    try:
+        t = sc.device_inputs(inp)
+        # the abandoned thread block leaves its part of the outputs unwritten
+        ss.selective_scan_bwd(t["u"], t["delta"][:, 0], t["A"], t["B"][:, 0], t["C"][:, 0],
+                              sc.to_torch(dout), t["D"], t["z"], t["delta_bias"], True)
+        with pytest.raises(ss.SSError) as ei:
+            ss.device_status()
+        assert ei.value.status == b.SS_ERR_TIMEOUT
+    finally:
+        b.check(lib.ss_debug_set_flags(0))
+        b.check(lib.ss_debug_set_wait_budget_ns(0))
+    ss.device_status()
+    assert_grads(gpu_bwd(inp, dout), oracle_bwd(oracle, inp, dout), wl.io)
+    ss.device_status()
+
+
+@pytest.mark.slow
+def test_bwd_full_size_sampled(oracle):
+    """The Mamba-130M layer shape (8 x 1536 x 2048, N = 16, bf16) in the launch
+    configuration the benchmark times.  Against the oracle: every per-element
+    gradient of batch 0 and dB, dC of batch 0 (one full group: all 1536
+    channels), and dA, dD, ddelta_bias of eight channels summed over all eight
+    batches."""
+    wl = wk.MAMBA_LAYER
+    inp = wk.make_inputs(wl, seed=0)
+    dout = wk.make_dout(wl, seed=0)
+    got = gpu_bwd(inp, dout)
+    f = {n: inp.as_f64(n) for n in ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")}
+    g64 = _dout_f64(wl, dout)
+    r0 = oracle.selective_scan_bwd(f["u"][:1], f["delta"][:1, 0], f["A"], f["B"][:1, 0],
+                                   f["C"][:1, 0], g64[:1], D=f["D"], z=f["z"][:1],
+                                   delta_bias=f["delta_bias"])
+    sub = {k: (got[k][:1] if got[k] is not None else None) for k in ("du", "ddelta", "dz", "dB", "dC")}
+    assert_grads(sub, r0, wl.io, names=("du", "ddelta", "dz", "dB", "dC"))
+    ch = np.array([0, 1, 31, 32, 700, 1024, 1534, 1535])
+    rc = oracle.selective_scan_bwd(f["u"][:, ch], f["delta"][:, 0][:, ch], f["A"][ch], f["B"][:, 0],
+                                   f["C"][:, 0], g64[:, ch], D=f["D"][ch], z=f["z"][:, ch],
+                                   delta_bias=f["delta_bias"][ch])
+    sums = {"dA": got["dA"][ch], "dD": got["dD"][ch], "ddelta_bias": got["ddelta_bias"][ch]}
+    assert_grads(sums, rc, wl.io, names=("dA", "dD", "ddelta_bias"))
