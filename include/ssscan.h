@@ -300,9 +300,9 @@ ss_status ss_selective_state_update(int64_t batch, int64_t dim, int dstate, int 
  *   ddelta_bias  [dim]                            float  nullable; summed over batch and time
  * The inputs u ... delta_softplus are the forward call's (same layouts and
  * rules), and dout [batch, dim, seqlen] is io.  The forward call keeps no
- * intermediate states; this call recomputes them, holding a checkpoint every 16
- * steps in `workspace`: at least ss_workspace_bytes(SS_KIND_SCAN_BWD, batch,
- * dim, seqlen, dstate) = batch*dim*ceil(seqlen/16)*dstate*4 bytes, 16-byte
+ * intermediate states; this call recomputes them, holding a checkpoint every 8
+ * or 16 steps in `workspace`: at least ss_workspace_bytes(SS_KIND_SCAN_BWD, batch,
+ * dim, seqlen, dstate) = batch*dim*ceil(seqlen/8)*dstate*4 bytes, 16-byte
  * aligned, contents ignored.  Rows must be 16-byte aligned (seqlen * element
  * size % 16 == 0), else SS_ERR_UNSUPPORTED.  All pointers are device pointers,
  * 16-byte aligned; no output may overlap an input, another output or the

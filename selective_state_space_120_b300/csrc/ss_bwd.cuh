@@ -18,50 +18,59 @@
 // intermediate states are recomputed on chip rather than stored in HBM and
 // read back.  This kernel recomputes them from sparse checkpoints.
 //
-// Work split as in the forward scan: a CTA owns CB channels of one (batch,
-// group); lane = g*CPW + c holds NPT of the N states of channel c of its warp.
+// Work split: a CTA owns CB channels of one (batch, group).  Inside a warp,
+// lane = g*CPW + q holds NPT of the N states (slice g) of CL channels (group q).
 // Each CTA walks its rows twice through one TMA ring:
-//   pass F, tiles 0 .. nt-1: the states only, storing them every TS = 16 steps
-//     as checkpoints (fp32, N values per channel per 16 steps: 4 bytes per
-//     element at N = 16);
-//   pass B, tiles nt-1 .. 0, each tile's 16-step blocks last to first: from
-//     the block's checkpoint the lane recomputes its chains' 16 states into
-//     registers together with the readout s_t, then runs the reverse
-//     recurrence over the block; Abar (.) dh is carried in registers from block
-//     to block.
-// Sums over the N states (s_t, dDelta'_t, sum_n dh B) are combined across a
-// channel's R lanes by the transposing butterfly, R steps at a time, so that
-// lane g finishes step g of each R-step group.  dB and dC are sums over the
-// channels of a group: per step a transposing butterfly over the CPW lanes of
-// a state slice, then per-warp sums in shared memory that the CTA adds up after
-// each block and adds to the fp32 outputs with 16-byte atomic adds.  dA, dD and
-// dbias are per-channel sums over time held in registers, added over the batch
-// with atomics at the end.
+//   pass F, tiles 0 .. nt-1: the states only, storing them every TS steps as
+//     checkpoints in the workspace (fp32);
+//   pass B, tiles nt-1 .. 0, each tile's TS-step blocks last to first: from the
+//     block's checkpoint the lane recomputes its chains' TS states into
+//     registers together with the readout s_t, then runs the reverse recurrence
+//     over the block; Abar (.) dh is carried in registers from block to block.
+// State math runs on pairs of states with packed f32x2 operations.  Sums over
+// the N states (s_t, dDelta'_t, sum_n dh B) are combined across a channel's R
+// lanes by the transposing butterfly, R steps at a time, so that lane g
+// finishes step g of each R-step group.  dB and dC are sums over the channels
+// of a group: in registers over a lane's CL channels, then per step a
+// transposing butterfly over the CPW lanes of a state slice, then per-warp sums
+// in shared memory that the CTA adds up after each block and adds to the fp32
+// outputs with 16-byte atomic adds.  The shared-memory footprint is kept small
+// enough (two ring stages, one sums buffer) for three CTAs of the N = 16
+// configuration to share an SM: a Mamba-layer call then runs in a single wave.  dA, dD and dbias are per-channel sums over
+// time held in registers, added over the batch with atomics at the end.
 #pragma once
 
 #include "ss_device.cuh"
 
 namespace ssk {
 
-template <typename IO_, int N_, int W_, int STAGES_ = 3>
+template <typename IO_, int N_, int W_, int CL_ = 1, int NPT_ = 4, int TS_ = 16 / CL_,
+          int MINB_ = 1, int STAGES_ = 2>
 struct CfgB {
     using IO = IO_;
-    static constexpr int N = N_, W = W_, STAGES = STAGES_;
-    static constexpr int NPT = N < 4 ? N : 4;  // states per lane
-    static constexpr int R = N / NPT;          // lanes per channel
-    static constexpr int CPW = 32 / R;         // channels per warp
-    static constexpr int CB = W * CPW;         // channels per CTA
+    static constexpr int N = N_, W = W_, CL = CL_, STAGES = STAGES_;
+    static constexpr int MINB = MINB_;             // CTAs per SM the register budget allows
+    static constexpr int NPT = N < NPT_ ? N : NPT_;  // states per lane
+    static constexpr int NPE = NPT < 2 ? 2 : NPT;  // padded to whole pairs (N = 1: a phantom state)
+    static constexpr int NP = NPE / 2;             // state pairs per lane
+    static constexpr int NB = N < 2 ? 2 : N;       // B (and C) slots per step in shared memory
+    static constexpr int R = N / NPT;              // lanes per channel group
+    static constexpr int CPW = 32 / R;             // channel groups per warp
+    static constexpr int CHW = CPW * CL;           // channels per warp
+    static constexpr int CB = W * CHW;             // channels per CTA
     static constexpr int THREADS = 32 * W;
     static constexpr int ES = sizeof(IO);
-    static constexpr int T = 64 / ES;          // steps per tile (64-byte raw rows)
-    static constexpr int TS = 16;              // steps per register block = checkpoint interval
-    static constexpr int NS = T / TS;          // register blocks per tile
-    static constexpr int RB = TS / R;          // R-step readout groups per block
-    static constexpr int E = T / R;            // steps one thread preps (R threads per channel)
-    static constexpr int EP = E < 8 ? E : 8;   // steps converted at a time
-    static constexpr int V = 2 * NPT;          // dB and dC terms of a lane per step
+    static constexpr int T = 64 / ES;              // steps per tile (64-byte raw rows)
+    static constexpr int TS = TS_;                 // steps per register block = checkpoint interval
+    static constexpr int NS = T / TS;              // register blocks per tile
+    static constexpr int RB = TS / R;              // R-step readout groups per block
+    static constexpr int PT = R / CL;              // prep threads per channel
+    static constexpr int E = T / PT;               // steps one thread preps
+    static constexpr int EP = E < 8 ? E : 8;       // steps converted at a time
+    static constexpr int V = 2 * NPE;              // dB and dC terms of a lane per step
     static_assert(N % NPT == 0 && (R & (R - 1)) == 0 && R <= TS && TS % R == 0, "lane split");
-    static_assert(T % TS == 0 && E % EP == 0 && EP * ES >= 4, "tile split");
+    static_assert(CL >= 1 && R % CL == 0 && T % TS == 0 && TS % 4 == 0, "block split");
+    static_assert(E % EP == 0 && EP * ES >= 4, "prep split");
     static_assert(CB <= 256 && N <= 256, "TMA box rows");
 
     static constexpr int al(int x) { return (x + 1023) & ~1023; }
@@ -70,25 +79,29 @@ struct CfgB {
     static constexpr int STAGE = 4 * TILE_CH + 2 * TILE_BC;
     static constexpr int OFF_U = 0, OFF_DL = TILE_CH, OFF_Z = 2 * TILE_CH, OFF_DY = 3 * TILE_CH;
     static constexpr int OFF_B = 4 * TILE_CH, OFF_C = 4 * TILE_CH + TILE_BC;
-    static constexpr int BCF = T * 2 * N * 4;       // fp32 B, C of a tile: [t][B_0..N-1 | C_0..N-1]
+    static constexpr int BCF = T * 2 * NB * 4;      // fp32 B, C of a tile: [t][B_0..NB-1 | C_0..NB-1]
     static constexpr int OFF_BCF = STAGES * STAGE;  // two tiles' worth (tile parity)
     static constexpr int P0ROW = (T + 1) * 16;      // per step {Delta', Delta'u, ds, softplus'}
-    static constexpr int P1ROW = (T + 2) * 8;       // per step {u, dout SiLU'(z)}
+    static constexpr int P1ROW = (T + 1) * 8;       // per step {u, dout SiLU'(z)}
     static constexpr int OFF_P0 = OFF_BCF + 2 * BCF;
     static constexpr int OFF_P1 = OFF_P0 + CB * P0ROW;
     static constexpr int OBROW = 64 + 16;           // staged du / ddelta / dz rows (I/O type)
     static constexpr int OFF_OB = OFF_P1 + CB * P1ROW;
     static constexpr int REDW = TS * 2 * N * 4;     // one warp's dB/dC sums over one block
     static constexpr int OFF_RED = OFF_OB + 3 * CB * OBROW;
-    static constexpr int OFF_BAR = (OFF_RED + 2 * W * REDW + 7) & ~7;
+    static constexpr int OFF_BAR = (OFF_RED + W * REDW + 7) & ~7;
     static constexpr int SMEM = OFF_BAR + 8 * STAGES + 1024;  // + alignment slack
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
+    // Per-step rows of channel ch sit in order (ch % CL, ch / CL): the CPW lanes
+    // of a quarter-warp read CPW consecutive rows, whose odd 16-byte stride
+    // spreads them over all banks.
+    static __device__ __forceinline__ int prow(int ch) { return (ch % CL) * (CB / CL) + ch / CL; }
 };
 
 struct BwdParams {
     int64_t dim, L;
     int G, dpg;
-    int nblk;                 // 16-step blocks per row
+    int nblk;                 // checkpoint blocks per row
     const float *A, *D, *bias;
     int softplus, has_z;
     float *ckpt;              // [batch*dim, nblk, N]: state after each block (pass F)
@@ -98,64 +111,54 @@ struct BwdParams {
     float *dD, *dbias;        // [dim], nullable
 };
 
-template <int NPT>
-__device__ __forceinline__ void lds_npt(const float *p, float (&v)[NPT]) {
-    if constexpr (NPT == 4) {
-        const float4 q = *reinterpret_cast<const float4 *>(p);
-        v[0] = q.x;
-        v[1] = q.y;
-        v[2] = q.z;
-        v[3] = q.w;
-    } else {
-#pragma unroll
-        for (int j = 0; j < NPT; ++j) v[j] = p[j];
-    }
-}
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 ex2x2(float2 v) { return make_float2(ex2(v.x), ex2(v.y)); }
 
-__device__ __forceinline__ float sigmoid(float x) { return rcp(1.0f + ex2(-x * kLog2e)); }
-
-// Sums the V dB/dC terms of one step over the P channel lanes of a state slice
-// (lanes g*P + c, c = 0..P-1) and writes the sums to dst = [dB_0..N-1 | dC_0..N-1]
-// of that step.  Term vi of a lane is dB of state g*NPT + vi for vi < NPT and
-// dC of state g*NPT + vi - NPT otherwise.
-template <int V, int P, int N, int NPT>
-__device__ __forceinline__ void reduce_bc_store(float (&v)[V], int c, int g, float *dst) {
-    auto slot = [&](int vi) { return (vi < NPT ? 0 : N) + g * NPT + (vi % NPT); };
+// Sums the V dB/dC terms of one step over the P channel-group lanes of a state
+// slice (lanes g*P + q, q = 0..P-1) and writes the sums to dst = [dB_0..N-1 |
+// dC_0..N-1] of that step.  Term vi is dB of state g*NPT + vi for vi < NPE and
+// dC of state g*NPT + vi - NPE otherwise (padded states are dropped).
+template <int V, int P, int N, int NPT, int NPE>
+__device__ __forceinline__ void reduce_bc_store(float (&v)[V], int q, int g, float *dst) {
+    auto put = [&](int vi, float x) {
+        const int j = vi % NPE;
+        if (j < NPT) dst[(vi < NPE ? 0 : N) + g * NPT + j] = x;
+    };
     if constexpr (P == 1) {
 #pragma unroll
-        for (int vi = 0; vi < V; ++vi) dst[slot(vi)] = v[vi];
+        for (int vi = 0; vi < V; ++vi) put(vi, v[vi]);
     } else if constexpr (V >= P) {
 #pragma unroll
         for (int m = 0; m < V / P; ++m) {
             float part[P];
 #pragma unroll
             for (int k = 0; k < P; ++k) part[k] = v[m * P + k];
-            const float r = transpose_reduce<P, 1>(part, c);
-            dst[slot(m * P + c)] = r;
+            put(m * P + q, transpose_reduce<P, 1>(part, q));
         }
     } else {
-        float r = transpose_reduce<V, 1>(v, c & (V - 1));
+        float r = transpose_reduce<V, 1>(v, q & (V - 1));
 #pragma unroll
         for (int m = V; m < P; m <<= 1) r += __shfl_xor_sync(kFull, r, m);
-        if (c < V) dst[slot(c)] = r;
+        if (q < V) put(q, r);
     }
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS)
+__global__ void __launch_bounds__(C::THREADS, C::MINB)
 k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
            const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dy,
            const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_C,
            const BwdParams p) {
     using IO = typename C::IO;
-    constexpr int N = C::N, NPT = C::NPT, R = C::R, CPW = C::CPW, T = C::T, TS = C::TS;
-    constexpr int E = C::E, EP = C::EP, STAGES = C::STAGES;
+    constexpr int N = C::N, NPT = C::NPT, NPE = C::NPE, NP = C::NP, NB = C::NB, R = C::R;
+    constexpr int CPW = C::CPW, CL = C::CL, T = C::T, TS = C::TS, E = C::E, EP = C::EP;
+    constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = lane % CPW, g = lane / CPW;
+    const int q = lane % CPW, g = lane / CPW;
     const int cblk = blockIdx.x, bg = blockIdx.y;
     const int b = bg / p.G, grp = bg % p.G;
     const int64_t L = p.L;
@@ -165,40 +168,49 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
     const int nt = (int)((L + T - 1) / T);
     const int nq = 2 * nt;  // ring order: pass F tiles 0..nt-1, then pass B tiles nt-1..0
 
-    // scan role: NPT states of channel ch
-    const int ch = warp * CPW + c;
-    const int dg = cblk * C::CB + ch;
-    const bool valid = dg < p.dpg;
-    const int64_t d = (int64_t)grp * p.dpg + (valid ? dg : p.dpg - 1);
-    const int64_t row = (int64_t)b * p.dim + d;
-    float A2[NPT], h[NPT], carry[NPT], dA[NPT];
+    // scan role: states g*NPT .. of channels chs[c]
+    int chs[CL];
+    bool valid[CL];
+    int64_t dch[CL];
+    float2 A2[CL][NP], carry[CL][NP], dA[CL][NP];
+    float Dd[CL], dD_acc[CL], dbias_acc[CL];
+    float *ck[CL];
+    const float4 *P0[CL];
+    const float2 *P1[CL];
 #pragma unroll
-    for (int j = 0; j < NPT; ++j) {
-        A2[j] = __ldg(p.A + d * N + g * NPT + j) * kLog2e;
-        h[j] = 0.f;
-        carry[j] = 0.f;
-        dA[j] = 0.f;
+    for (int c = 0; c < CL; ++c) {
+        chs[c] = warp * C::CHW + q * CL + c;
+        const int dg = cblk * C::CB + chs[c];
+        valid[c] = dg < p.dpg;
+        dch[c] = (int64_t)grp * p.dpg + (valid[c] ? dg : p.dpg - 1);
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+            const int j0 = 2 * k, j1 = 2 * k + 1;
+            const float a0 = __ldg(p.A + dch[c] * N + g * NPT + j0) * kLog2e;
+            const float a1 = j1 < NPT ? __ldg(p.A + dch[c] * N + g * NPT + j1) * kLog2e : 0.f;
+            A2[c][k] = make_float2(a0, a1);
+            carry[c][k] = make_float2(0.f, 0.f);
+            dA[c][k] = make_float2(0.f, 0.f);
+        }
+        Dd[c] = p.D ? __ldg(p.D + dch[c]) : 0.f;
+        dD_acc[c] = 0.f;
+        dbias_acc[c] = 0.f;
+        ck[c] = p.ckpt + ((int64_t)b * p.dim + dch[c]) * p.nblk * N + g * NPT;
+        P0[c] = reinterpret_cast<const float4 *>(smem + C::OFF_P0 + C::prow(chs[c]) * C::P0ROW);
+        P1[c] = reinterpret_cast<const float2 *>(smem + C::OFF_P1 + C::prow(chs[c]) * C::P1ROW);
     }
-    const float Dd = p.D ? __ldg(p.D + d) : 0.f;
-    float dD_acc = 0.f, dbias_acc = 0.f;
-    float *ck = p.ckpt + row * p.nblk * N + g * NPT;  // this lane's checkpoint slots
-    const float4 *P0 = reinterpret_cast<const float4 *>(smem + C::OFF_P0 + ch * C::P0ROW);
-    const float2 *P1 = reinterpret_cast<const float2 *>(smem + C::OFF_P1 + ch * C::P1ROW);
-    IO *ob0 = reinterpret_cast<IO *>(smem + C::OFF_OB + ch * C::OBROW);
-    IO *ob1 = reinterpret_cast<IO *>(smem + C::OFF_OB + (C::CB + ch) * C::OBROW);
-    IO *ob2 = reinterpret_cast<IO *>(smem + C::OFF_OB + (2 * C::CB + ch) * C::OBROW);
     float *red0 = reinterpret_cast<float *>(smem + C::OFF_RED);
     float *bcf0 = reinterpret_cast<float *>(smem + C::OFF_BCF);
 
     // prep role: E consecutive steps of channel pch (a channel of this warp)
-    const int pch = tid / R;
-    const int pt0 = (tid % R) * E;
+    const int pch = tid / C::PT;
+    const int pt0 = (tid % C::PT) * E;
     const int pdg = cblk * C::CB + pch;
     const bool pvalid = pdg < p.dpg;
     const int64_t pd = (int64_t)grp * p.dpg + (pvalid ? pdg : p.dpg - 1);
     const float pbias = p.bias ? __ldg(p.bias + pd) : 0.f;
-    float4 *q0row = reinterpret_cast<float4 *>(smem + C::OFF_P0 + pch * C::P0ROW);
-    float2 *q1row = reinterpret_cast<float2 *>(smem + C::OFF_P1 + pch * C::P1ROW);
+    float4 *q0row = reinterpret_cast<float4 *>(smem + C::OFF_P0 + C::prow(pch) * C::P0ROW);
+    float2 *q1row = reinterpret_cast<float2 *>(smem + C::OFF_P1 + C::prow(pch) * C::P1ROW);
 
     const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
     const uint32_t smem0 = smem_u32(smem);
@@ -217,18 +229,23 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
         for (int s = 0; s < STAGES; ++s) mbar_init(bar0 + 8 * s, 1);
         fence_mbar_init();
     }
+    // padded B/C slots (N = 1) stay zero, so the padded state stays zero
+    if (NB > N) {
+        for (int i = tid; i < 2 * T * 2 * NB; i += C::THREADS)
+            if (i % NB >= N) bcf0[i] = 0.f;
+    }
     __syncthreads();
 
     // diagnostics: this CTA leaves its first tile's barrier without arrivals
     const bool skip_first = (g_debug_flags & 1u) && blockIdx.x == 0 && blockIdx.y == 0;
-    auto tile_of = [&](int q) { return q < nt ? q : nq - 1 - q; };
-    auto issue = [&](int q) {
-        if (q == 0 && skip_first) return;
-        const int s = q % STAGES;
+    auto tile_of = [&](int qs) { return qs < nt ? qs : nq - 1 - qs; };
+    auto issue = [&](int qs) {
+        if (qs == 0 && skip_first) return;
+        const int s = qs % STAGES;
         const uint32_t bar = bar0 + 8 * s;
         const uint32_t st = smem0 + s * C::STAGE;
-        const bool bwd = q >= nt;
-        const int x = tile_of(q) * T;
+        const bool bwd = qs >= nt;
+        const int x = tile_of(qs) * T;
         mbar_expect_tx(bar, bwd ? txB : txF);
         tma_load_2d(st + C::OFF_U, &tm_u, x, row_tma, bar);
         tma_load_2d(st + C::OFF_DL, &tm_dl, x, row_tma, bar);
@@ -241,13 +258,13 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
     };
     if (tid == 0) {
 #pragma unroll 1
-        for (int q = 0; q < STAGES && q < nq; ++q) issue(q);
+        for (int qs = 0; qs < STAGES && qs < nq; ++qs) issue(qs);
     }
 
-    // Converts ring item q (tile i) into fp32 B (and C) and per-step rows.
-    auto prep = [&](int q, int i, bool bwd) {
-        const uint8_t *st = smem + (q % STAGES) * C::STAGE;
-        float *bcf = bcf0 + (q & 1) * (C::BCF / 4);
+    // Converts ring item qs (tile i) into fp32 B (and C) and per-step rows.
+    auto prep = [&](int qs, int i, bool bwd) {
+        const uint8_t *st = smem + (qs % STAGES) * C::STAGE;
+        float *bcf = bcf0 + (qs & 1) * (C::BCF / 4);
         constexpr int VPC = 16 / C::ES;
         const int na = bwd ? 2 : 1;
 #pragma unroll 1
@@ -258,7 +275,7 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
             float v[VPC];
             load_tile_row<IO, VPC>(st + (arr ? C::OFF_C : C::OFF_B), n, qq * VPC, v);
 #pragma unroll
-            for (int e = 0; e < VPC; ++e) bcf[(qq * VPC + e) * 2 * N + arr * N + n] = v[e];
+            for (int e = 0; e < VPC; ++e) bcf[(qq * VPC + e) * 2 * NB + arr * NB + n] = v[e];
         }
         const int64_t tb0 = (int64_t)i * T;
 #pragma unroll
@@ -277,15 +294,21 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
                 // unchanged and contribute nothing
                 const bool in = pvalid && tb0 + tl < L;
                 const float v = dd[e] + pbias;
-                const float dl = in ? (p.softplus ? softplus(v) : v) : 0.f;
+                float dl = v, dsp = 1.f;
+                if (p.softplus) {
+                    // softplus and its derivative (the logistic function) from one exponential
+                    const float ev = ex2(v * kLog2e);
+                    dl = softplus_from_exp(v, ev);
+                    dsp = v > 15.f ? 1.f - rcp(ev) : ev * rcp(1.f + ev);
+                }
+                if (!in) dl = 0.f;
                 const float x = dl * uu[e];
                 if (!bwd) {
                     *reinterpret_cast<float2 *>(q0row + tl) = make_float2(dl, x);
                 } else {
-                    const float dsp = p.softplus ? sigmoid(v) : 1.f;
                     float ds = gy[e], dzf = 0.f;
                     if (p.has_z) {
-                        const float sg = sigmoid(zz[e]);
+                        const float sg = rcp(1.f + ex2(-zz[e] * kLog2e));
                         ds = gy[e] * zz[e] * sg;
                         dzf = gy[e] * sg * fmaf(zz[e], 1.f - sg, 1.f);
                     }
@@ -295,32 +318,64 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
             }
         }
     };
-    // Bounded wait for ring item q; on timeout the whole CTA drains its copies
+    // Bounded wait for ring item qs; on timeout the whole CTA drains its copies
     // and exits (returns true then).
-    auto abandon = [&](int q, bool ok) -> bool {
+    auto abandon = [&](int qs, bool ok) -> bool {
         if (!__syncthreads_or(!ok)) return false;
         if (tid == 0) {
             report_timeout();
 #pragma unroll 1
-            for (int k = q; k < nq && k < q + STAGES; ++k)
+            for (int k = qs; k < nq && k < qs + STAGES; ++k)
                 if (!(k == 0 && skip_first))
                     (void)mbar_wait_bounded(bar0 + 8 * (k % STAGES), (k / STAGES) & 1, 1000000000ull);
         }
         return true;
     };
+    // this lane's B or C pairs at tile-local step t
+    auto ld_pairs = [&](const float *bcf, int t, int arr, float2 (&v)[NP]) {
+        const float *src = bcf + t * 2 * NB + arr * NB + g * NPE;
+        if constexpr (NP == 2) {
+            const float4 w = *reinterpret_cast<const float4 *>(src);
+            v[0] = make_float2(w.x, w.y);
+            v[1] = make_float2(w.z, w.w);
+        } else {
+#pragma unroll
+            for (int k = 0; k < NP; ++k) v[k] = *reinterpret_cast<const float2 *>(src + 2 * k);
+        }
+    };
+
+    // checkpoint kc of channel c (the state after block kc; zero before block 0)
+    auto ld_ckpt = [&](int c, int kc, float2 (&v)[NP]) {
+#pragma unroll
+        for (int kk = 0; kk < NP; ++kk) v[kk] = make_float2(0.f, 0.f);
+        if (kc >= 0) {
+#pragma unroll
+            for (int kk = 0; kk < NP; ++kk) {
+                const float *src = ck[c] + (int64_t)kc * N + 2 * kk;
+                v[kk].x = src[0];
+                if (2 * kk + 1 < NPT) v[kk].y = src[1];
+            }
+        }
+    };
+
+    float2 h[CL][NP], hbn[CL][NP];
+#pragma unroll
+    for (int c = 0; c < CL; ++c)
+#pragma unroll
+        for (int k = 0; k < NP; ++k) h[c][k] = make_float2(0.f, 0.f);
 
 #pragma unroll 1
-    for (int q = 0; q < nq; ++q) {
-        const bool bwd = q >= nt;
-        const int i = tile_of(q);
-        const bool ok = mbar_wait_bounded(bar0 + 8 * (q % STAGES), (q / STAGES) & 1, budget);
-        if (ok) prep(q, i, bwd);
-        if (abandon(q, ok)) return;
-        if (tid == 0 && q + STAGES < nq) {
+    for (int qs = 0; qs < nq; ++qs) {
+        const bool bwd = qs >= nt;
+        const int i = tile_of(qs);
+        const bool ok = mbar_wait_bounded(bar0 + 8 * (qs % STAGES), (qs / STAGES) & 1, budget);
+        if (ok) prep(qs, i, bwd);
+        if (abandon(qs, ok)) return;
+        if (tid == 0 && qs + STAGES < nq) {
             fence_proxy_async_smem();
-            issue(q + STAGES);
+            issue(qs + STAGES);
         }
-        const float *bcf = bcf0 + (q & 1) * (C::BCF / 4);
+        const float *bcf = bcf0 + (qs & 1) * (C::BCF / 4);
 
         if (!bwd) {
             // ---------------- pass F: checkpoints after each block
@@ -330,15 +385,28 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
                 if (k >= p.nblk - 1) break;  // no later block starts from this state
 #pragma unroll
                 for (int tb = 0; tb < TS; ++tb) {
-                    const float2 pp = *reinterpret_cast<const float2 *>(P0 + s * TS + tb);
-                    float Bv[NPT];
-                    lds_npt<NPT>(bcf + (s * TS + tb) * 2 * N + g * NPT, Bv);
+                    const int t = s * TS + tb;
+                    float2 B2[NP];
+                    ld_pairs(bcf, t, 0, B2);
 #pragma unroll
-                    for (int j = 0; j < NPT; ++j) h[j] = fmaf(ex2(pp.x * A2[j]), h[j], pp.y * Bv[j]);
+                    for (int c = 0; c < CL; ++c) {
+                        const float2 pp = *reinterpret_cast<const float2 *>(P0[c] + t);
+#pragma unroll
+                        for (int kk = 0; kk < NP; ++kk) {
+                            const float2 a = ex2x2(__fmul2_rn(f2(pp.x), A2[c][kk]));
+                            h[c][kk] = __ffma2_rn(a, h[c][kk], __fmul2_rn(f2(pp.y), B2[kk]));
+                        }
+                    }
                 }
-                if (valid) {
 #pragma unroll
-                    for (int j = 0; j < NPT; ++j) ck[(int64_t)k * N + j] = h[j];
+                for (int c = 0; c < CL; ++c) {
+                    if (!valid[c]) continue;
+                    float *dst = ck[c] + (int64_t)k * N;
+#pragma unroll
+                    for (int kk = 0; kk < NP; ++kk) {
+                        dst[2 * kk] = h[c][kk].x;
+                        if (2 * kk + 1 < NPT) dst[2 * kk + 1] = h[c][kk].y;
+                    }
                 }
             }
             __syncwarp();
@@ -346,97 +414,130 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
         }
 
         // ---------------- pass B: blocks of tile i, last to first
+        if (qs == nt) {
+            // state entering the first block scanned backwards
+            const int kf = p.nblk - 1;
+#pragma unroll
+            for (int c = 0; c < CL; ++c) ld_ckpt(c, kf - 1, hbn[c]);
+        }
 #pragma unroll 1
         for (int s = C::NS - 1; s >= 0; --s) {
             const int k = i * C::NS + s;
             if (k >= p.nblk) continue;  // the block lies past the sequence end
             const int t0b = s * TS;
-            float hb[NPT];
+            float2 hb[CL][NP];
 #pragma unroll
-            for (int j = 0; j < NPT; ++j) hb[j] = k > 0 ? ck[(int64_t)(k - 1) * N + j] : 0.f;
+            for (int c = 0; c < CL; ++c) {
+#pragma unroll
+                for (int kk = 0; kk < NP; ++kk) hb[c][kk] = hbn[c][kk];
+                ld_ckpt(c, k - 2, hbn[c]);  // for the next block, one block ahead
+            }
 
             // recompute the block's states and readouts
-            float hs[TS][NPT];
-            float sv[C::RB];
+            float2 hs[TS][CL][NP];
+            float sv[CL][C::RB];
             {
-                float hc[NPT];
+                float2 hc[CL][NP];
 #pragma unroll
-                for (int j = 0; j < NPT; ++j) hc[j] = hb[j];
+                for (int c = 0; c < CL; ++c)
+#pragma unroll
+                    for (int kk = 0; kk < NP; ++kk) hc[c][kk] = hb[c][kk];
 #pragma unroll
                 for (int rb = 0; rb < C::RB; ++rb) {
-                    float sp[R];
+                    float sp[CL][R];
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const int tb = rb * R + r;
-                        const float4 pp = P0[t0b + tb];
-                        float Bv[NPT], Cv[NPT];
-                        lds_npt<NPT>(bcf + (t0b + tb) * 2 * N + g * NPT, Bv);
-                        lds_npt<NPT>(bcf + (t0b + tb) * 2 * N + N + g * NPT, Cv);
-                        float acc = 0.f;
+                        float2 B2[NP], C2[NP];
+                        ld_pairs(bcf, t0b + tb, 0, B2);
+                        ld_pairs(bcf, t0b + tb, 1, C2);
 #pragma unroll
-                        for (int j = 0; j < NPT; ++j) {
-                            hc[j] = fmaf(ex2(pp.x * A2[j]), hc[j], pp.y * Bv[j]);
-                            hs[tb][j] = hc[j];
-                            acc = fmaf(Cv[j], hc[j], acc);
+                        for (int c = 0; c < CL; ++c) {
+                            const float2 pp = *reinterpret_cast<const float2 *>(P0[c] + t0b + tb);
+                            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int kk = 0; kk < NP; ++kk) {
+                                const float2 a = ex2x2(__fmul2_rn(f2(pp.x), A2[c][kk]));
+                                hc[c][kk] = __ffma2_rn(a, hc[c][kk], __fmul2_rn(f2(pp.y), B2[kk]));
+                                hs[tb][c][kk] = hc[c][kk];
+                                acc = __ffma2_rn(C2[kk], hc[c][kk], acc);
+                            }
+                            sp[c][r] = acc.x + acc.y;
                         }
-                        sp[r] = acc;
                     }
-                    sv[rb] = transpose_reduce<R, CPW>(sp, g);
+#pragma unroll
+                    for (int c = 0; c < CL; ++c) sv[c][rb] = transpose_reduce<R, CPW>(sp[c], g);
                 }
             }
 
             // reverse recurrence over the block
-            float *redw = red0 + ((k & 1) * C::W + warp) * (TS * 2 * N);
+            float *redw = red0 + warp * (TS * 2 * N);
 #pragma unroll
             for (int rb = C::RB - 1; rb >= 0; --rb) {
-                float p1v[R], p2v[R];
+                float p1v[CL][R], p2v[CL][R];
 #pragma unroll
                 for (int r = R - 1; r >= 0; --r) {
                     const int tb = rb * R + r;
-                    const float4 pp = P0[t0b + tb];  // Delta', Delta'u, ds, softplus'
-                    float Bv[NPT], Cv[NPT];
-                    lds_npt<NPT>(bcf + (t0b + tb) * 2 * N + g * NPT, Bv);
-                    lds_npt<NPT>(bcf + (t0b + tb) * 2 * N + N + g * NPT, Cv);
-                    float vals[C::V];
-                    float p1 = 0.f, p2 = 0.f;
+                    float2 B2[NP], C2[NP], vb[NP], vc[NP];
+                    ld_pairs(bcf, t0b + tb, 0, B2);
+                    ld_pairs(bcf, t0b + tb, 1, C2);
 #pragma unroll
-                    for (int j = 0; j < NPT; ++j) {
-                        const float a = ex2(pp.x * A2[j]);
-                        const float dh = fmaf(pp.z, Cv[j], carry[j]);
-                        const float hp = tb > 0 ? hs[tb - 1][j] : hb[j];
-                        const float w = dh * hp * a;
-                        p1 = fmaf(w, A2[j], p1);
-                        dA[j] = fmaf(w, pp.x, dA[j]);
-                        p2 = fmaf(dh, Bv[j], p2);
-                        vals[j] = dh * pp.y;
-                        vals[NPT + j] = pp.z * hs[tb][j];
-                        carry[j] = a * dh;
+                    for (int c = 0; c < CL; ++c) {
+                        const float4 pp = P0[c][t0b + tb];  // Delta', Delta'u, ds, softplus'
+                        const float2 dl2 = f2(pp.x), x2 = f2(pp.y), ds2 = f2(pp.z);
+                        float2 p1 = make_float2(0.f, 0.f), p2 = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int kk = 0; kk < NP; ++kk) {
+                            const float2 a = ex2x2(__fmul2_rn(dl2, A2[c][kk]));
+                            const float2 dh = __ffma2_rn(ds2, C2[kk], carry[c][kk]);
+                            const float2 hp = tb > 0 ? hs[tb - 1][c][kk] : hb[c][kk];
+                            const float2 w = __fmul2_rn(__fmul2_rn(dh, hp), a);
+                            p1 = __ffma2_rn(w, A2[c][kk], p1);
+                            dA[c][kk] = __ffma2_rn(w, dl2, dA[c][kk]);
+                            p2 = __ffma2_rn(dh, B2[kk], p2);
+                            const float2 db = __fmul2_rn(dh, x2);
+                            const float2 dc = __fmul2_rn(ds2, hs[tb][c][kk]);
+                            vb[kk] = c == 0 ? db : __fadd2_rn(vb[kk], db);
+                            vc[kk] = c == 0 ? dc : __fadd2_rn(vc[kk], dc);
+                            carry[c][kk] = __fmul2_rn(a, dh);
+                        }
+                        p1v[c][r] = p1.x + p1.y;
+                        p2v[c][r] = p2.x + p2.y;
                     }
-                    p1v[r] = p1;
-                    p2v[r] = p2;
-                    reduce_bc_store<C::V, CPW, N, NPT>(vals, c, g, redw + tb * 2 * N);
+                    float vals[C::V];
+#pragma unroll
+                    for (int kk = 0; kk < NP; ++kk) {
+                        vals[2 * kk] = vb[kk].x;
+                        vals[2 * kk + 1] = vb[kk].y;
+                        vals[NPE + 2 * kk] = vc[kk].x;
+                        vals[NPE + 2 * kk + 1] = vc[kk].y;
+                    }
+                    reduce_bc_store<C::V, CPW, N, NPT, NPE>(vals, q, g, redw + tb * 2 * N);
                 }
-                // lane g finishes step rb*R + g of the block
-                const float P1s = transpose_reduce<R, CPW>(p1v, g) * kLn2;  // sum dh h Abar A
-                const float P2s = transpose_reduce<R, CPW>(p2v, g);         // sum dh B
+                // lane g finishes step rb*R + g of the block for each of its channels
                 const int tl = t0b + rb * R + g;
-                const float4 pp = P0[tl];
-                const float2 q1 = P1[tl];
-                const float ddl = fmaf(P2s, q1.x, P1s);
-                const float ddelta = ddl * pp.w;
-                const float du = fmaf(pp.z, Dd, pp.x * P2s);
-                dD_acc = fmaf(pp.z, q1.x, dD_acc);
-                dbias_acc += ddelta;
-                ob0[tl] = IOT<IO>::from_f(du);
-                ob1[tl] = IOT<IO>::from_f(ddelta);
-                if (p.has_z) ob2[tl] = IOT<IO>::from_f(fmaf(Dd, q1.x, sv[rb]) * q1.y);
+#pragma unroll
+                for (int c = 0; c < CL; ++c) {
+                    const float P1s = transpose_reduce<R, CPW>(p1v[c], g) * kLn2;  // sum dh h Abar A
+                    const float P2s = transpose_reduce<R, CPW>(p2v[c], g);         // sum dh B
+                    const float4 pp = P0[c][tl];
+                    const float2 q1 = P1[c][tl];
+                    const float ddelta = fmaf(P2s, q1.x, P1s) * pp.w;
+                    dD_acc[c] = fmaf(pp.z, q1.x, dD_acc[c]);
+                    dbias_acc[c] += ddelta;
+                    IO *ob = reinterpret_cast<IO *>(smem + C::OFF_OB + chs[c] * C::OBROW);
+                    ob[tl] = IOT<IO>::from_f(fmaf(pp.z, Dd[c], pp.x * P2s));        // du
+                    ob[C::CB * C::OBROW / C::ES + tl] = IOT<IO>::from_f(ddelta);
+                    if (p.has_z)                                                    // dz
+                        ob[2 * C::CB * C::OBROW / C::ES + tl] =
+                            IOT<IO>::from_f(fmaf(Dd[c], q1.x, sv[c][rb]) * q1.y);
+                }
             }
 
             // dB, dC of the block: sum the warps' terms, add to the outputs
             __syncthreads();
             {
-                const float *rb_all = red0 + (k & 1) * C::W * (TS * 2 * N);
-                float *dBC = nullptr;
+                const float *rb_all = red0;
 #pragma unroll 1
                 for (int gi = tid; gi < 2 * N * (TS / 4); gi += C::THREADS) {
                     const int n = gi % N;
@@ -452,12 +553,13 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
                         acc.w += src[6 * N];
                     }
                     const int64_t t = (int64_t)k * TS + 4 * t4;
-                    dBC = arr ? p.dC : p.dB;
+                    float *dBC = arr ? p.dC : p.dB;
                     if (t < L)
                         atomicAdd(reinterpret_cast<float4 *>(dBC + (((int64_t)b * p.G + grp) * N + n) * L + t),
                                   acc);
                 }
             }
+            __syncthreads();  // the sums buffer is refilled by the next block
         }
 
         // the tile's du, ddelta (and dz) rows: 16-byte stores of this warp's channels
@@ -466,11 +568,11 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
             constexpr int VPC = 16 / C::ES;
             const int narr = p.has_z ? 3 : 2;
 #pragma unroll 1
-            for (int kk = lane; kk < narr * CPW * 4; kk += 32) {
-                const int arr = kk / (CPW * 4);
-                const int rem = kk % (CPW * 4);
+            for (int kk = lane; kk < narr * C::CHW * 4; kk += 32) {
+                const int arr = kk / (C::CHW * 4);
+                const int rem = kk % (C::CHW * 4);
                 const int rr = rem >> 2, qq = rem & 3;
-                const int chr = warp * CPW + rr;
+                const int chr = warp * C::CHW + rr;
                 const int dgr = cblk * C::CB + chr;
                 const int64_t t = (int64_t)i * T + qq * VPC;
                 if (dgr < p.dpg && t < L) {
@@ -486,16 +588,21 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
 
     // per-channel sums: over the channel's R lanes, then over the batch (atomics)
 #pragma unroll
-    for (int m = 1; m < R; m <<= 1) {
-        dD_acc += __shfl_xor_sync(kFull, dD_acc, m * CPW);
-        dbias_acc += __shfl_xor_sync(kFull, dbias_acc, m * CPW);
-    }
-    if (valid) {
+    for (int c = 0; c < CL; ++c) {
 #pragma unroll
-        for (int j = 0; j < NPT; ++j) atomicAdd(p.dA + d * N + g * NPT + j, dA[j]);
+        for (int m = 1; m < R; m <<= 1) {
+            dD_acc[c] += __shfl_xor_sync(kFull, dD_acc[c], m * CPW);
+            dbias_acc[c] += __shfl_xor_sync(kFull, dbias_acc[c], m * CPW);
+        }
+        if (!valid[c]) continue;
+#pragma unroll
+        for (int kk = 0; kk < NP; ++kk) {
+            atomicAdd(p.dA + dch[c] * N + g * NPT + 2 * kk, dA[c][kk].x);
+            if (2 * kk + 1 < NPT) atomicAdd(p.dA + dch[c] * N + g * NPT + 2 * kk + 1, dA[c][kk].y);
+        }
         if (g == 0) {
-            if (p.dD) atomicAdd(p.dD + d, dD_acc);
-            if (p.dbias) atomicAdd(p.dbias + d, dbias_acc);
+            if (p.dD) atomicAdd(p.dD + dch[c], dD_acc[c]);
+            if (p.dbias) atomicAdd(p.dbias + dch[c], dbias_acc[c]);
         }
     }
 }

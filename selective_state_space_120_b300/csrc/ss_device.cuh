@@ -54,13 +54,14 @@ __device__ __forceinline__ float rcp(float x) {
 //              computed through 1+e would lose it;
 //   otherwise: ln2 * log2(1 + e);
 //   x > 15   : x itself (the two differ by less than 3.1e-7 relative).
-__device__ __forceinline__ float softplus(float x) {
-    const float e = ex2(x * kLog2e);
+// softplus_from_exp takes e = 2^(x*log2 e) computed by the caller.
+__device__ __forceinline__ float softplus_from_exp(float x, float e) {
     const float series = e * fmaf(e, fmaf(e, fmaf(e, -0.25f, 0.333333343f), -0.5f), 1.0f);
     const float via_log = kLn2 * lg2(1.0f + e);
     const float r = (e < 0.03125f) ? series : via_log;
     return (x > 15.0f) ? x : r;
 }
+__device__ __forceinline__ float softplus(float x) { return softplus_from_exp(x, ex2(x * kLog2e)); }
 
 // SiLU(z) = z * sigmoid(z) = z / (1 + e^-z).  For z -> -inf the exponential
 // overflows to +inf, the reciprocal to 0 and the result to -0.

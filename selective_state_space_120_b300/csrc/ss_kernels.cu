@@ -503,12 +503,14 @@ ss_status launch_step(const ScanArgs &a, float *state) {
 
 // ---------------------------------------------------------------- backward
 namespace {
-constexpr int kBwdBlock = 16;  // steps between state checkpoints (CfgB::TS)
+// Checkpoint workspace: every configuration checkpoints every 8 or 16 steps; the
+// workspace is sized for 8.
+constexpr int kBwdMinBlock = 8;
 
 template <class C>
 ss_status run_scan_bwd(const BwdArgs &a) {
     using namespace ssk;
-    static_assert(C::TS == kBwdBlock, "checkpoint interval");
+    static_assert(C::TS >= kBwdMinBlock, "checkpoint interval");
     const ScanArgs &f = a.f;
     const int io = f.io;
     const int64_t rows = f.batch * f.dim;
@@ -529,7 +531,7 @@ ss_status run_scan_bwd(const BwdArgs &a) {
     p.L = f.L;
     p.G = f.G;
     p.dpg = (int)(f.dim / f.G);
-    p.nblk = (int)((f.L + kBwdBlock - 1) / kBwdBlock);
+    p.nblk = (int)((f.L + C::TS - 1) / C::TS);
     p.A = f.A;
     p.D = f.D;
     p.bias = f.bias;
@@ -554,14 +556,18 @@ ss_status run_scan_bwd(const BwdArgs &a) {
 template <typename IO>
 ss_status dispatch_bwd(const BwdArgs &a) {
     using namespace ssk;
+    // CfgB<IO, N, warps per CTA, channels per lane, states per lane, steps per
+    // block, CTAs per SM for the register budget>
+    // float32 I/O has twice the prep registers: a budget of two CTAs per SM
+    constexpr int MB = sizeof(IO) == 2 ? 3 : 2;
     switch (a.f.N) {
-    case 1: return run_scan_bwd<CfgB<IO, 1, 2>>(a);
-    case 2: return run_scan_bwd<CfgB<IO, 2, 2>>(a);
-    case 4: return run_scan_bwd<CfgB<IO, 4, 2>>(a);
-    case 8: return run_scan_bwd<CfgB<IO, 8, 4>>(a);
-    case 16: return run_scan_bwd<CfgB<IO, 16, 4>>(a);
-    case 32: return run_scan_bwd<CfgB<IO, 32, 4>>(a);
-    case 64: return run_scan_bwd<CfgB<IO, 64, 4>>(a);
+    case 1: return run_scan_bwd<CfgB<IO, 1, 2, 1, 4, 16, 2>>(a);
+    case 2: return run_scan_bwd<CfgB<IO, 2, 2, 1, 4, 16, 2>>(a);
+    case 4: return run_scan_bwd<CfgB<IO, 4, 2, 1, 4, 16, 2>>(a);
+    case 8: return run_scan_bwd<CfgB<IO, 8, 2, 1, 4, 16, MB>>(a);
+    case 16: return run_scan_bwd<CfgB<IO, 16, 4, 1, 4, 16, MB>>(a);
+    case 32: return run_scan_bwd<CfgB<IO, 32, 4, 1, 4, 16, MB>>(a);
+    case 64: return run_scan_bwd<CfgB<IO, 64, 4, 1, 4, 16, 2>>(a);
     default: return fail(SS_ERR_UNSUPPORTED, "dstate %d is not one of 1,2,4,8,16,32,64", a.f.N);
     }
 }
@@ -576,7 +582,7 @@ ss_status zero_async(void *p, size_t bytes, cudaStream_t s) {
 
 size_t scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t L, int N) {
     if (batch <= 0 || dim <= 0 || L <= 0 || N <= 0) return 0;
-    return (size_t)batch * dim * ((L + kBwdBlock - 1) / kBwdBlock) * N * sizeof(float);
+    return (size_t)batch * dim * ((L + kBwdMinBlock - 1) / kBwdMinBlock) * N * sizeof(float);
 }
 
 ss_status launch_scan_bwd(const BwdArgs &a, bool empty) {

@@ -246,9 +246,9 @@ def test_backward_validates(lib):
         b.SS_ERR_WORKSPACE
 
 
-def test_backward_workspace_is_one_checkpoint_per_16_steps(lib):
-    # [batch*dim, ceil(L/16), N] float32
-    assert b.workspace_bytes(b.SS_KIND_SCAN_BWD, 8, 1536, 2048, 16) == 8 * 1536 * 128 * 16 * 4
-    assert b.workspace_bytes(b.SS_KIND_SCAN_BWD, 2, 3, 17, 4) == 2 * 3 * 2 * 4 * 4
+def test_backward_workspace_holds_a_checkpoint_per_8_steps(lib):
+    # [batch*dim, ceil(L/8), N] float32
+    assert b.workspace_bytes(b.SS_KIND_SCAN_BWD, 8, 1536, 2048, 16) == 8 * 1536 * 256 * 16 * 4
+    assert b.workspace_bytes(b.SS_KIND_SCAN_BWD, 2, 3, 17, 4) == 2 * 3 * 3 * 4 * 4
     assert b.workspace_bytes(b.SS_KIND_SCAN_BWD, 2, 3, 0, 4) == 0
     assert b.workspace_bytes(b.SS_KIND_SCAN_BWD, 2, 3, 64, 12) == 0
