@@ -667,7 +667,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(WORKLOADS) + [BWD_NAME],
+                    help="forward workload to time (the backward pass: its own line only)")
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -690,8 +691,25 @@ def main(argv=None):
     import selective_state_space_120_b300 as ss
     ss.load_library()
 
-    wl = WORKLOADS[args.workload]
     peak, peak_kind = measured_peaks()
+    if args.workload == BWD_NAME:
+        # the backward pass alone, on one GPU per rank (replicas), device-resident inputs
+        r = measure_bwd(args.steps, args.warmup, peak, peak_kind)
+        ms = max_over_ranks(r["ms_per_step"], world, "cuda")
+        if rank == 0:
+            line = {"metric": "selective-scan backward Gelem/s (B·D·L)",
+                    "value": job_value(wk.MAMBA_LAYER.elems, world, ms), "unit": UNIT,
+                    "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                    "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                    "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded NumPy PCG64)",
+                    "config": r["config"], "roofline": r["roofline"],
+                    "gpu_launches": args.steps * r["kernel_launches_per_step"]}
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+    wl = WORKLOADS[args.workload]
     r, ms, kern_ms, clocks = measure_gpu(wl, args.steps, args.warmup, barrier)
     ms = max_over_ranks(ms, world, "cuda")
     value = job_value(wl.elems, world, ms)

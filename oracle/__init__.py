@@ -28,6 +28,12 @@ ORDER_FWD = 0       # positions 0..L-1 (row-major for an H x W map)
 ORDER_REV = 1       # positions L-1..0
 ORDER_COL = 2       # column-major over an H x W map
 ORDER_COL_REV = 3   # reverse of column-major
+# windowed orders (LocalMamba): w x w windows visited one after another, the
+# windows of the last band of rows / last column cut short
+ORDER_WIN = 4          # windows row-major, each window row-major
+ORDER_WIN_REV = 5      # reverse of ORDER_WIN
+ORDER_WIN_COL = 6      # windows column-major, each window column-major
+ORDER_WIN_COL_REV = 7  # reverse of ORDER_WIN_COL
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "ss_oracle.c")
@@ -52,7 +58,7 @@ def _bind(path: str):
     i64 = ctypes.c_int64
     lib.ssor_scan.restype = ctypes.c_int
     lib.ssor_scan.argtypes = [i64, i64, i64, i64, i64, i64, i64,
-                              ctypes.POINTER(ctypes.c_int),
+                              ctypes.POINTER(ctypes.c_int), i64,
                               dp, dp, dp, dp, dp, dp, dp, dp,
                               ctypes.c_int, ctypes.c_int, dp, dp, dp, dp]
     lib.ssor_scan_bwd.restype = ctypes.c_int
@@ -63,6 +69,8 @@ def _bind(path: str):
     lib.ssor_softplus_scalar.argtypes = [ctypes.c_double]
     lib.ssor_position_of.restype = ctypes.c_int64
     lib.ssor_position_of.argtypes = [ctypes.c_int, i64, i64, i64]
+    lib.ssor_order_table.restype = ctypes.c_int
+    lib.ssor_order_table.argtypes = [ctypes.c_int, i64, i64, i64, ctypes.POINTER(i64)]
     return lib
 
 
@@ -90,12 +98,13 @@ def _ptr(a):
 
 
 def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-         orders=(ORDER_FWD,), H=None, W=None, zoh=False, h0=None, _lib_handle=None):
+         orders=(ORDER_FWD,), H=None, W=None, zoh=False, h0=None, win=0, _lib_handle=None):
     """Run the oracle.
 
     ``delta`` is [batch, K, dim, L] and ``B``/``C`` are [batch, K, G, N, L]; for a
     single direction the K axis may be omitted (``delta`` [batch, dim, L],
-    ``B``/``C`` [batch, G, N, L]).  ``H``/``W`` default to 1 x L.
+    ``B``/``C`` [batch, G, N, L]).  ``H``/``W`` default to 1 x L; ``win`` is the
+    window size of the windowed orders.
     Returns ``(out [batch, dim, L], last_state [batch, K, dim, N])`` as float64.
     """
     u = np.asarray(u)
@@ -131,7 +140,7 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True
     work = np.empty((N,), dtype=np.float64)
     ords = (ctypes.c_int * K)(*[int(o) for o in orders])
     lib = _lib_handle if _lib_handle is not None else _load()
-    rc = lib.ssor_scan(batch, dim, H, W, N, G, K, ords,
+    rc = lib.ssor_scan(batch, dim, H, W, N, G, K, ords, int(win),
                            _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                            _ptr(delta_bias), int(bool(delta_softplus)), int(bool(zoh)),
                            _ptr(h0), _ptr(out), _ptr(last), _ptr(work))
@@ -233,3 +242,13 @@ def softplus(x: float) -> float:
 
 def position(order: int, s: int, H: int, W: int) -> int:
     return _load().ssor_position_of(int(order), int(s), int(H), int(W))
+
+
+def order_table(order: int, H: int, W: int, win: int = 0) -> np.ndarray:
+    """Positions visited by steps 0 .. H*W-1 of a direction with the given order."""
+    pos = np.empty(H * W, dtype=np.int64)
+    rc = _load().ssor_order_table(int(order), int(H), int(W), int(win),
+                                  pos.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return pos

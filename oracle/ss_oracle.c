@@ -43,12 +43,22 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 /* Traversal orders of one direction. */
 #define SSOR_ORDER_FWD 0     /* positions 0, 1, ..., L-1 (row-major for a map) */
 #define SSOR_ORDER_REV 1     /* positions L-1, ..., 0                          */
 #define SSOR_ORDER_COL 2     /* column-major over an H x W map                 */
 #define SSOR_ORDER_COL_REV 3 /* reverse of column-major                        */
+/* Windowed orders ("LocalMamba: Visual State Space Model with Windowed Selective
+ * Scan", abstract: the image is divided into windows and scanned window by
+ * window).  Read here as: the map is cut into w x w windows -- the windows of
+ * the last band of rows and of the last column are cut short when w does not
+ * divide H or W -- and the windows are visited one after another. */
+#define SSOR_ORDER_WIN 4         /* windows row-major, each window row-major          */
+#define SSOR_ORDER_WIN_REV 5     /* reverse of SSOR_ORDER_WIN                          */
+#define SSOR_ORDER_WIN_COL 6     /* windows column-major, each window column-major     */
+#define SSOR_ORDER_WIN_COL_REV 7 /* reverse of SSOR_ORDER_WIN_COL                      */
 
 /* softplus(x) = log(1 + exp(x)), written in the overflow-free form. */
 static double ssor_softplus(double x) {
@@ -69,6 +79,48 @@ static int64_t ssor_position(int order, int64_t s, int64_t H, int64_t W) {
     }
 }
 
+/* Positions of a windowed order, step by step, written out by nested loops over
+ * the windows and the cells inside each (col = 0: rows outer; col = 1: the
+ * transposed map, columns outer).  Fills pos[0 .. H*W). */
+static void ssor_window_walk(int64_t H, int64_t W, int64_t w, int col, int64_t *pos) {
+    int64_t s = 0;
+    if (!col) {
+        for (int64_t r0 = 0; r0 < H; r0 += w)
+            for (int64_t c0 = 0; c0 < W; c0 += w)
+                for (int64_t r = r0; r < r0 + w && r < H; ++r)
+                    for (int64_t c = c0; c < c0 + w && c < W; ++c) pos[s++] = r * W + c;
+    } else {
+        for (int64_t c0 = 0; c0 < W; c0 += w)
+            for (int64_t r0 = 0; r0 < H; r0 += w)
+                for (int64_t c = c0; c < c0 + w && c < W; ++c)
+                    for (int64_t r = r0; r < r0 + w && r < H; ++r) pos[s++] = r * W + c;
+    }
+}
+
+/* Position table of any order (win: window size of the windowed orders, >= 1).
+ * Returns 0, or -1 for an unknown order or a bad window size. */
+int ssor_order_table(int order, int64_t H, int64_t W, int64_t win, int64_t *pos) {
+    const int64_t L = H * W;
+    if (H <= 0 || W <= 0 || !pos) return -1;
+    if (order >= SSOR_ORDER_WIN && order <= SSOR_ORDER_WIN_COL_REV) {
+        if (win < 1) return -1;
+        const int col = (order == SSOR_ORDER_WIN_COL || order == SSOR_ORDER_WIN_COL_REV);
+        ssor_window_walk(H, W, win, col, pos);
+        if (order == SSOR_ORDER_WIN_REV || order == SSOR_ORDER_WIN_COL_REV)
+            for (int64_t i = 0, j = L - 1; i < j; ++i, --j) {
+                const int64_t t = pos[i];
+                pos[i] = pos[j];
+                pos[j] = t;
+            }
+        return 0;
+    }
+    for (int64_t s = 0; s < L; ++s) {
+        pos[s] = ssor_position(order, s, H, W);
+        if (pos[s] < 0) return -1;
+    }
+    return 0;
+}
+
 /*
  * ssor_scan: the general oracle.
  *
@@ -84,10 +136,11 @@ static int64_t ssor_position(int order, int64_t s, int64_t H, int64_t W) {
  *   out        [batch, dim, L]
  *   last_state [batch, K, dim, N] (NULL: not written)
  *   orders     [K]  one SSOR_ORDER_* per direction
+ *   win        window size of the windowed orders (ignored by the others)
  * Returns 0, or -1 on an invalid argument.
  */
 int ssor_scan(int64_t batch, int64_t dim, int64_t H, int64_t W, int64_t N, int64_t ngroups,
-              int64_t K, const int *orders,
+              int64_t K, const int *orders, int64_t win,
               const double *u, const double *delta, const double *A, const double *Bm,
               const double *Cm, const double *Dv, const double *z, const double *bias,
               int delta_softplus, int zoh, const double *h0, double *out, double *last_state,
@@ -99,6 +152,20 @@ int ssor_scan(int64_t batch, int64_t dim, int64_t H, int64_t W, int64_t N, int64
     const int64_t dpg = dim / ngroups;
 
     for (int64_t i = 0; i < batch * dim * L; ++i) out[i] = 0.0;
+
+    /* windowed orders: the position of each step from a table */
+    int64_t *wtab = NULL;
+    for (int64_t k = 0; k < K; ++k)
+        if (orders[k] >= SSOR_ORDER_WIN) {
+            wtab = (int64_t *)malloc(sizeof(int64_t) * L * K);
+            if (!wtab) return -1;
+            break;
+        }
+    for (int64_t k = 0; wtab && k < K; ++k)
+        if (orders[k] >= SSOR_ORDER_WIN && ssor_order_table(orders[k], H, W, win, wtab + k * L)) {
+            free(wtab);
+            return -1;
+        }
 
     for (int64_t b = 0; b < batch; ++b) {
         for (int64_t k = 0; k < K; ++k) {
@@ -117,8 +184,12 @@ int ssor_scan(int64_t batch, int64_t dim, int64_t H, int64_t W, int64_t N, int64
                     h[n] = h0 ? h0[((b * K + k) * dim + d) * N + n] : 0.0;
 
                 for (int64_t s = 0; s < L; ++s) {
-                    const int64_t p = ssor_position(orders[k], s, H, W);
-                    if (p < 0) return -1;
+                    const int64_t p = orders[k] >= SSOR_ORDER_WIN ? wtab[k * L + s]
+                                                                  : ssor_position(orders[k], s, H, W);
+                    if (p < 0) {
+                        free(wtab);
+                        return -1;
+                    }
                     double dt = dl_row[s] + bd;
                     if (delta_softplus) dt = ssor_softplus(dt);
                     const double up = u_row[p];
@@ -142,6 +213,7 @@ int ssor_scan(int64_t batch, int64_t dim, int64_t H, int64_t W, int64_t N, int64
             }
         }
     }
+    free(wtab);
 
     if (z) {
         for (int64_t i = 0; i < batch * dim * L; ++i) {

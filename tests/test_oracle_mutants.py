@@ -42,6 +42,9 @@ MUTANTS = {
     "bwd_softplus_derivative": ("1.0 / (1.0 + exp(-r)) : 1.0;", "1.0 / (1.0 + exp(r)) : 1.0;"),
     "conv_history_off_by_one": ("else xv = x0r ? x0r[(KW - 1) + s] : 0.0;",
                                 "else xv = x0r ? x0r[(KW - 2) + s] : 0.0;"),
+    "window_cells_transposed": ("for (int64_t c = c0; c < c0 + w && c < W; ++c) pos[s++] = r * W + c;",
+                                "for (int64_t c = c0; c < c0 + w && c < W; ++c) pos[s++] = c * H + r;"),
+    "window_reverse_missing": ("const int64_t t = pos[i];", "const int64_t t = pos[j];"),
     "group_map_interleaved": ("const int64_t g = d / dpg;", "const int64_t g = d % ngroups;"),
     "ignores_initial_state": ("h[n] = h0 ? h0[((b * K + k) * dim + d) * N + n] : 0.0;",
                               "h[n] = 0.0;"),
@@ -55,6 +58,8 @@ class _Variant:
     ORDER_FWD, ORDER_REV = _oracle.ORDER_FWD, _oracle.ORDER_REV
     ORDER_COL, ORDER_COL_REV = _oracle.ORDER_COL, _oracle.ORDER_COL_REV
     SS2D_ORDERS = _oracle.SS2D_ORDERS
+    ORDER_WIN, ORDER_WIN_REV = _oracle.ORDER_WIN, _oracle.ORDER_WIN_REV
+    ORDER_WIN_COL, ORDER_WIN_COL_REV = _oracle.ORDER_WIN_COL, _oracle.ORDER_WIN_COL_REV
 
     def __init__(self, path):
         self.lib = _oracle._bind(path)
@@ -99,6 +104,14 @@ class _Variant:
 
     def position(self, order, s, H, W):
         return self.lib.ssor_position_of(int(order), int(s), int(H), int(W))
+
+    def order_table(self, order, H, W, win=0):
+        pos = np.empty(H * W, dtype=np.int64)
+        rc = self.lib.ssor_order_table(int(order), int(H), int(W), int(win),
+                                       pos.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)))
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+        return pos
 
 
 def _pin_calls():

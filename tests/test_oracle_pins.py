@@ -434,3 +434,68 @@ def test_backward_single_step_closed_form(oracle):
     np.testing.assert_allclose(g["dC"].ravel(), [dt * B * u], rtol=1e-15)
     np.testing.assert_allclose(g["dD"].ravel(), [u], rtol=1e-15)
     np.testing.assert_array_equal(g["dA"], np.zeros((1, 1)))
+
+
+# ---------------------------------------------------------------- windowed orders
+def test_window_orders_golden(oracle):
+    """Windowed orders written out by hand (tests/golden/window_orders.json),
+    with a divisible and a cut-short case; the reversed orders are their flips."""
+    g = json.load(open(os.path.join(GOLDEN, "window_orders.json")))
+    for case in g["cases"]:
+        H, W, w = case["H"], case["W"], case["w"]
+        for name, order, rev in (("win", oracle.ORDER_WIN, oracle.ORDER_WIN_REV),
+                                 ("win_col", oracle.ORDER_WIN_COL, oracle.ORDER_WIN_COL_REV)):
+            assert oracle.order_table(order, H, W, w).tolist() == case[name], (H, W, name)
+            assert oracle.order_table(rev, H, W, w).tolist() == case[name][::-1], (H, W, name)
+
+
+@pytest.mark.parametrize("H,W,w", [(4, 6, 2), (14, 14, 7), (8, 12, 4), (6, 6, 3)])
+def test_window_orders_equal_numpy_reshape(oracle, H, W, w):
+    """When w divides H and W, the windowed order is the map reshaped to
+    (H/w, w, W/w, w) with the window axes outermost: (0, 2, 1, 3) for windows
+    row-major, (2, 0, 3, 1) for windows and cells column-major."""
+    idx = np.arange(H * W).reshape(H // w, w, W // w, w)
+    assert np.array_equal(oracle.order_table(oracle.ORDER_WIN, H, W, w),
+                          idx.transpose(0, 2, 1, 3).reshape(-1))
+    assert np.array_equal(oracle.order_table(oracle.ORDER_WIN_COL, H, W, w),
+                          idx.transpose(2, 0, 3, 1).reshape(-1))
+
+
+@pytest.mark.parametrize("H,W", [(5, 7), (1, 9), (9, 1), (3, 3)])
+def test_window_orders_limits(oracle, H, W):
+    """w = 1 and w >= max(H, W) leave one cell or one window: row-major and
+    column-major traversals; every windowed order is a permutation."""
+    row = [oracle.position(oracle.ORDER_FWD, s, H, W) for s in range(H * W)]
+    col = [oracle.position(oracle.ORDER_COL, s, H, W) for s in range(H * W)]
+    for w in (1, max(H, W), max(H, W) + 3):
+        assert oracle.order_table(oracle.ORDER_WIN, H, W, w).tolist() == row
+        assert oracle.order_table(oracle.ORDER_WIN_COL, H, W, w).tolist() == col
+    for order in (oracle.ORDER_WIN, oracle.ORDER_WIN_REV, oracle.ORDER_WIN_COL,
+                  oracle.ORDER_WIN_COL_REV):
+        assert sorted(oracle.order_table(order, H, W, 2).tolist()) == list(range(H * W))
+
+
+@pytest.mark.parametrize("H,W,w", [(6, 8, 2), (5, 7, 3)])
+def test_windowed_scan_equals_scan_of_permuted_copy(oracle, H, W, w):
+    """A windowed direction equals a 1-D scan of the map's values taken in the
+    window order (NumPy fancy indexing), with the outputs put back in place."""
+    rng = np.random.default_rng(41)
+    batch, dim, N, L = 2, 3, 4, H * W
+    u = rng.standard_normal((batch, dim, L))
+    z = rng.standard_normal((batch, dim, L))
+    dl = rng.standard_normal((batch, dim, L)) * 0.3
+    A = -rng.uniform(0.5, 2.0, (dim, N))
+    B = rng.standard_normal((batch, 1, N, L))
+    C = rng.standard_normal((batch, 1, N, L))
+    D = rng.standard_normal(dim)
+    bias = rng.standard_normal(dim) * 0.1
+    for order in (oracle.ORDER_WIN, oracle.ORDER_WIN_REV, oracle.ORDER_WIN_COL,
+                  oracle.ORDER_WIN_COL_REV):
+        pos = oracle.order_table(order, H, W, w)
+        got, got_last = oracle.scan(u, dl, A, B, C, D, z, bias, True, (order,), H=H, W=W, win=w)
+        y, last = oracle.scan(u[..., pos], dl, A, B, C, D, None, bias, True)
+        want = np.empty_like(y)
+        want[..., pos] = y
+        want *= z / (1.0 + np.exp(-z))
+        np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(got_last, last, rtol=1e-13, atol=1e-13)
