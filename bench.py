@@ -50,9 +50,9 @@ FALLBACK_HBM_GBS = 6400.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 CSRC = os.path.join(ROOT, "selective_state_space_120_b300", "csrc")
 
-WORKLOADS = {w.name: w for w in wk.ALL + (wk.MAMBA_LAYER_CONV,)}
+WORKLOADS = {w.name: w for w in wk.ALL + (wk.MAMBA_LAYER_CONV, wk.LOCAL_WIN)}
 HEADLINE = wk.MAMBA_LAYER
-OTHERS = (wk.LONG_SEQ, wk.VIM_BIDIR, wk.VMAMBA_SS2D, wk.MAMBA_LAYER_CONV)
+OTHERS = (wk.LONG_SEQ, wk.VIM_BIDIR, wk.VMAMBA_SS2D, wk.MAMBA_LAYER_CONV, wk.LOCAL_WIN)
 
 
 # ------------------------------------------------------------------ accounting
@@ -243,9 +243,13 @@ class Runner:
         self.opts = b.options(0, b.SS_SCAN_CONV_SILU if wl.conv else 0, None,
                               None if conv_w is None else conv_w.data_ptr(),
                               None if conv_b is None else conv_b.data_ptr())
-        kind = {1: b.SS_KIND_SCAN, 2: b.SS_KIND_BIDIR, 4: b.SS_KIND_CROSS2D}[wl.K]
-        wsb = int(self.lib.ss_workspace_bytes_opts(kind, wl.batch, wl.dim, wl.L, wl.N,
-                                                   ctypes.byref(self.opts)))
+        if wl.orders:
+            wsb = int(self.lib.ss_multi_scan_workspace_bytes(wl.batch, wl.dim, wl.H, wl.W, wl.K))
+            self.ords = (ctypes.c_int * wl.K)(*wl.orders)
+        else:
+            kind = {1: b.SS_KIND_SCAN, 2: b.SS_KIND_BIDIR, 4: b.SS_KIND_CROSS2D}[wl.K]
+            wsb = int(self.lib.ss_workspace_bytes_opts(kind, wl.batch, wl.dim, wl.L, wl.N,
+                                                       ctypes.byref(self.opts)))
         if wsb:
             self.ws = torch.empty(wsb, dtype=torch.uint8, device=device)
         self.args = [self._args(s) for s in self.sets]
@@ -268,6 +272,11 @@ class Runner:
         st = ctypes.c_void_p(self.stream.cuda_stream)
         ws = p(self.ws)
         wsb = 0 if self.ws is None else self.ws.numel()
+        if wl.orders:
+            return (self.lib.ss_multi_scan_fwd,
+                    (wl.batch, wl.dim, wl.H, wl.W, wl.K, self.ords, wl.win, wl.N, wl.G, io,
+                     p(s["u"]), p(s["delta"]), p(s["A"]), p(s["B"]), p(s["C"]), p(s["D"]),
+                     p(s["delta_bias"]), 1, p(s["z"]), p(s["out"]), p(s["last"]), ws, wsb, st))
         if wl.K == 1:
             return (self.lib.ss_selective_scan_fwd_opts,
                     (wl.batch, wl.dim, wl.L, wl.N, wl.G, io, p(s["u"]), p(s["delta"]), p(s["A"]),
@@ -285,7 +294,10 @@ class Runner:
 
     def _launches(self):
         """Kernels one step launches: 1; 3 on the chunked long-sequence path; one
-        per direction when the multi-direction call merges through its workspace."""
+        per direction when the multi-direction call merges through its workspace
+        (plus the merge for an any-order call)."""
+        if self.wl.orders:
+            return (self.wl.K + 1) // 2 + 1
         if self.ws is None:
             return 1
         return 3 if self.wl.K == 1 else self.wl.K
@@ -379,9 +391,16 @@ def oracle_sample(wl: wk.Workload, budget_s: float = 12.0, threads: int | None =
     small = wk.scaled(wl, wl.name + "_oracle_sample", batch=1, dim=dim)
     inp = wk.make_inputs(small, seed=0)
     K = wl.K
-    orders = {1: (oracle.ORDER_FWD,), 2: (oracle.ORDER_FWD, oracle.ORDER_REV),
-              4: oracle.SS2D_ORDERS}[K]
-    H, W = (wl.H, wl.W) if K == 4 else (1, wl.L)
+    if wl.orders:
+        # the library's SS_DIR_* codes in the oracle's numbering
+        lib_to_oracle = {0: oracle.ORDER_FWD, 1: oracle.ORDER_COL, 2: oracle.ORDER_REV,
+                         3: oracle.ORDER_COL_REV, 4: oracle.ORDER_WIN, 5: oracle.ORDER_WIN_COL,
+                         6: oracle.ORDER_WIN_REV, 7: oracle.ORDER_WIN_COL_REV}
+        orders = tuple(lib_to_oracle[o] for o in wl.orders)
+    else:
+        orders = {1: (oracle.ORDER_FWD,), 2: (oracle.ORDER_FWD, oracle.ORDER_REV),
+                  4: oracle.SS2D_ORDERS}[K]
+    H, W = (wl.H, wl.W) if (K == 4 or wl.orders) else (1, wl.L)
     u, dl, A, B, C = (inp.as_f64(n) for n in ("u", "delta", "A", "B", "C"))
     D, z, bias = inp.as_f64("D"), inp.as_f64("z"), inp.as_f64("delta_bias")
     dpg = small.dim // wl.G
@@ -394,7 +413,7 @@ def oracle_sample(wl: wk.Workload, budget_s: float = 12.0, threads: int | None =
         oracle.scan(u[b:b + 1, d:d + 1], dl[b:b + 1, :, d:d + 1], A[sel],
                     B[b:b + 1, :, g:g + 1], C[b:b + 1, :, g:g + 1],
                     None if D is None else D[sel], None if z is None else z[b:b + 1, d:d + 1],
-                    bias[sel], True, orders, H=H, W=W)
+                    bias[sel], True, orders, H=H, W=W, win=wl.win)
 
     done = 0
     t0 = time.perf_counter()
@@ -451,8 +470,11 @@ def config_of(wl: wk.Workload, n_gpus: int, copies: int | None = None):
          "state_dtype": "f32", "z_gate": wl.with_z, "d_skip": wl.with_D,
          "last_state": wl.last_state, "delta_softplus": True,
          "parallelism": f"replicas{n_gpus}" if n_gpus > 1 else "single"}
-    if wl.K == 4:
+    if wl.K == 4 or wl.orders:
         c["H"], c["W"] = wl.H, wl.W
+    if wl.orders:
+        c["orders"] = list(wl.orders)
+        c["window"] = wl.win
     if copies:
         c["l2"] = (f"inputs rotate over {copies} copies "
                    f"({copies * algorithmic_bytes(wl) / 1e6:.0f} MB > 126 MB L2)")

@@ -78,6 +78,14 @@ typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
 #define SS_DIR_COL 1     /* column-major: position (t % H) * W + t / H     */
 #define SS_DIR_ROW_REV 2 /* reversed row-major                             */
 #define SS_DIR_COL_REV 3 /* reversed column-major                          */
+/* Windowed orders of ss_multi_scan_fwd ("LocalMamba: Visual State Space Model with
+ * Windowed Selective Scan": the map is scanned window by window).  The map is cut
+ * into window x window windows -- those of the last band of rows and of the last
+ * column cut short when the window does not divide H or W. */
+#define SS_DIR_WIN 4         /* windows row-major, each window row-major       */
+#define SS_DIR_WIN_COL 5     /* windows column-major, each window column-major */
+#define SS_DIR_WIN_REV 6     /* reversed SS_DIR_WIN                            */
+#define SS_DIR_WIN_COL_REV 7 /* reversed SS_DIR_WIN_COL                        */
 
 /* Kinds for ss_workspace_bytes. */
 #define SS_KIND_SCAN 0
@@ -281,6 +289,41 @@ ss_status ss_selective_state_update(int64_t batch, int64_t dim, int dstate, int 
                                     const float *D, const void *z, const float *delta_bias,
                                     int delta_softplus, unsigned int flags, float *state,
                                     void *out, ss_stream_t stream);
+
+/*
+ * ss_multi_scan_fwd -- ndirs (1..8) directions of any traversal over an H x W map,
+ * summed by position and gated: the SS2D computation for an arbitrary list of
+ * orders.  Direction k visits the map in the order orders[k] (an SS_DIR_* code;
+ * `window` is the window size of the windowed ones, ignored otherwise).  Besides
+ * SS2D's four orders and LocalMamba's windowed scans this covers the spatio-
+ * temporal scans of a video of T frames of h x w pixels (VideoMamba), taken as a
+ * map of H = T rows and W = h*w columns: SS_DIR_ROW is the spatial-first scan
+ * (frame by frame) and SS_DIR_COL the temporal-first one (pixel by pixel through
+ * the frames), with their reverses.
+ *
+ *   u, z, out   [batch, dim, H, W]          io (z nullable: no gate)
+ *   delta       [batch, ndirs, dim, H*W]    io, in each direction's scan order
+ *   A           [ndirs*dim, dstate]         float
+ *   B, C        [batch, ndirs, ngroups, dstate, H*W]  io, in each direction's scan order
+ *   D, delta_bias [ndirs*dim]               float, nullable
+ *   last_state  [batch, ndirs, dim, dstate] float, nullable
+ *   orders      host array of ndirs SS_DIR_* codes
+ *   workspace   ss_multi_scan_workspace_bytes(batch, dim, H, W, ndirs) =
+ *               ndirs*batch*dim*H*W*4 bytes, 16-byte aligned, contents ignored
+ * out = (sum_k y_k + D_k*u) * SiLU(z).  Rows must be 16-byte aligned (H*W *
+ * element size % 16 == 0), else SS_ERR_UNSUPPORTED.  Directions run two per
+ * launch of the scan kernel, each storing its terms by scan step into its own
+ * fp32 slice of the workspace; one more launch sums them by position.
+ */
+ss_status ss_multi_scan_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, int ndirs,
+                            const int *orders, int window, int dstate, int ngroups, ss_dtype io,
+                            const void *u, const void *delta, const float *A, const void *B,
+                            const void *C, const float *D, const float *delta_bias,
+                            int delta_softplus, const void *z, void *out, float *last_state,
+                            void *workspace, size_t workspace_bytes, ss_stream_t stream);
+
+/* Workspace of ss_multi_scan_fwd (0 for an empty or invalid shape). */
+size_t ss_multi_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t H, int64_t W, int ndirs);
 
 /*
  * ss_selective_scan_bwd -- gradients of ss_selective_scan_fwd (Euler input

@@ -9,6 +9,7 @@ in the library's sm_103a kernels; there is no fallback.
     out = bidir_scan_fwd(u, delta2, A2, B2, C2, D2, z, bias2)
     out = cross_scan2d_fwd(u_map, delta4, A4, B4, C4, D4, bias4)
     grads = selective_scan_bwd(u, delta, A, B, C, dout, D, z, delta_bias)
+    out = multi_scan_fwd(u_map, deltaK, AK, BK, CK, [DIR_WIN, DIR_WIN_COL], window=7)
 
 u, z and out are indexed by position; each direction's delta, B and C are in
 that direction's scan order.
@@ -160,6 +161,54 @@ def selective_scan_bwd(u, delta, A, B, C, dout, D=None, z=None, delta_bias=None,
         _ptr(workspace) if wsb else None, workspace.numel() if wsb else 0,
         _stream(stream, dev)))
     return g
+
+
+def multi_scan_fwd(u, delta, A, B, C, orders, window=0, D=None, delta_bias=None,
+                   delta_softplus=True, z=None, return_last_state=False, out=None,
+                   workspace=None, stream=None):
+    """Directions of any traversal over an H x W map, summed by position and gated.
+
+    u, z: [batch, dim, H, W]; delta: [batch, K, dim, H*W] and B, C: [batch, K, G,
+    N, H*W], each direction's in its own scan order; A: [K*dim, N]; D,
+    delta_bias: [K*dim].  ``orders`` lists K SS_DIR_* codes (DIR_* below);
+    ``window`` is the window size of the windowed ones.  Returns out [batch,
+    dim, H, W] (and last_state [batch, K, dim, N])."""
+    torch = _torch()
+    lib = _b.load()
+    batch, dim, H, W = u.shape
+    K = len(orders)
+    G, N = B.shape[2], B.shape[3]
+    L = H * W
+    io, dev = u.dtype, u.device
+    _check_io("u", u, io, dev)
+    _check_io("z", z, io, dev, (batch, dim, H, W))
+    _check_io("delta", delta, io, dev, (batch, K, dim, L))
+    _check_io("B", B, io, dev, (batch, K, G, N, L))
+    _check_io("C", C, io, dev, (batch, K, G, N, L))
+    _check_io("A", A, torch.float32, dev, (K * dim, N))
+    _check_io("D", D, torch.float32, dev, (K * dim,))
+    _check_io("delta_bias", delta_bias, torch.float32, dev, (K * dim,))
+    if out is None:
+        out = torch.empty_like(u)
+    _check_io("out", out, io, dev, (batch, dim, H, W))
+    last = (torch.empty(batch, K, dim, N, dtype=torch.float32, device=dev)
+            if return_last_state else None)
+    wsb = int(lib.ss_multi_scan_workspace_bytes(batch, dim, H, W, K))
+    if wsb and (workspace is None or workspace.numel() < wsb):
+        workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    ords = (ctypes.c_int * K)(*[int(o) for o in orders])
+    _b.check(lib.ss_multi_scan_fwd(
+        batch, dim, H, W, K, ords, int(window), N, G, _io_code(u), _ptr(u), _ptr(delta), _ptr(A),
+        _ptr(B), _ptr(C), _ptr(D), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(z), _ptr(out),
+        _ptr(last), _ptr(workspace) if wsb else None, workspace.numel() if wsb else 0,
+        _stream(stream, dev)))
+    return (out, last) if return_last_state else out
+
+
+from ._binding import (SS_DIR_COL as DIR_COL, SS_DIR_COL_REV as DIR_COL_REV,  # noqa: E402
+                       SS_DIR_ROW as DIR_ROW, SS_DIR_ROW_REV as DIR_ROW_REV,
+                       SS_DIR_WIN as DIR_WIN, SS_DIR_WIN_COL as DIR_WIN_COL,
+                       SS_DIR_WIN_COL_REV as DIR_WIN_COL_REV, SS_DIR_WIN_REV as DIR_WIN_REV)
 
 
 def _multidir_workspace(lib, kind, batch, dim, L, N, dev, workspace):

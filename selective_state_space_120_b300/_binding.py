@@ -24,6 +24,9 @@ SS_F32 = 0
 SS_BF16 = 1
 SS_KIND_SCAN, SS_KIND_BIDIR, SS_KIND_CROSS2D, SS_KIND_SCAN_BWD = 0, 1, 2, 3
 SS_DEBUG_SKIP_FIRST_COPY = 1
+# traversal orders (SS_DIR_*)
+(SS_DIR_ROW, SS_DIR_COL, SS_DIR_ROW_REV, SS_DIR_COL_REV, SS_DIR_WIN, SS_DIR_WIN_COL,
+ SS_DIR_WIN_REV, SS_DIR_WIN_COL_REV) = range(8)
 SS_NOALLOC_SCRATCH_BYTES = 16 << 20
 STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_ARG", 2: "SS_ERR_UNSUPPORTED",
                 3: "SS_ERR_ALIGNMENT", 4: "SS_ERR_WORKSPACE", 5: "SS_ERR_CUDA",
@@ -35,7 +38,7 @@ EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_opts", "ss_bidir_scan
            "ss_get_device_status", "ss_last_error_string", "ss_version",
            "ss_debug_set_wait_budget_ns", "ss_debug_set_flags",
            "ss_selective_scan_fwd_noalloc", "ss_selective_state_update",
-           "ss_selective_scan_bwd")
+           "ss_selective_scan_bwd", "ss_multi_scan_fwd", "ss_multi_scan_workspace_bytes")
 
 
 class SSError(RuntimeError):
@@ -83,10 +86,17 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         # u ... delta_softplus as the forward call, then dout, du, ddelta, dA, dB, dC, dD, dz,
         # ddelta_bias, workspace, workspace_bytes, stream
         lib.ss_selective_scan_bwd.argtypes = scan_args[:15] + [vp] * 9 + [vp, sz, vp]
+        # batch, dim, H, W, ndirs, orders (host int array), window, dstate, ngroups, io,
+        # u, delta, A, B, C, D, delta_bias, delta_softplus, z, out, last_state, workspace,
+        # workspace_bytes, stream
+        lib.ss_multi_scan_fwd.argtypes = [i64, i64, i64, i64, i32, ctypes.POINTER(i32), i32, i32,
+                                          i32, i32] + [vp] * 7 + [i32, vp, vp, vp, vp, sz, vp]
+        lib.ss_multi_scan_workspace_bytes.argtypes = [i64, i64, i64, i64, i32]
+        lib.ss_multi_scan_workspace_bytes.restype = sz
         for f in ("ss_selective_scan_fwd", "ss_selective_scan_fwd_opts", "ss_bidir_scan_fwd",
                   "ss_cross_scan2d_fwd", "ss_get_device_status", "ss_debug_set_wait_budget_ns",
                   "ss_debug_set_flags", "ss_selective_scan_fwd_noalloc",
-                  "ss_selective_state_update", "ss_selective_scan_bwd"):
+                  "ss_selective_state_update", "ss_selective_scan_bwd", "ss_multi_scan_fwd"):
             getattr(lib, f).restype = ctypes.c_int
         lib.ss_workspace_bytes.argtypes = [i32, i64, i64, i64, i32]
         lib.ss_workspace_bytes.restype = sz

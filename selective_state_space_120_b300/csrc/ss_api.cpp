@@ -428,6 +428,56 @@ ss_status ss_selective_state_update(int64_t batch, int64_t dim, int dstate, int 
     return launch_step(a, state);
 }
 
+ss_status ss_multi_scan_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, int ndirs,
+                            const int *orders, int window, int dstate, int ngroups, ss_dtype io,
+                            const void *u, const void *delta, const float *A, const void *B,
+                            const void *C, const float *D, const float *delta_bias,
+                            int delta_softplus, const void *z, void *out, float *last_state,
+                            void *workspace, size_t workspace_bytes, ss_stream_t stream) {
+    static const char *fn = "ss_multi_scan_fwd";
+    if (H < 0 || W < 0) return fail(SS_ERR_INVALID_ARG, "%s: negative map size", fn);
+    if (H >= (1ll << 31) || W >= (1ll << 31) || (H > 0 && W > (INT64_MAX / H)))
+        return fail(SS_ERR_UNSUPPORTED, "%s: map too large", fn);
+    if (ndirs < 1 || ndirs > 8)
+        return fail(SS_ERR_INVALID_ARG, "%s: ndirs %d is not in 1..8", fn, ndirs);
+    if (!orders) return fail(SS_ERR_INVALID_ARG, "%s: orders is required", fn);
+    bool windowed = false;
+    for (int k = 0; k < ndirs; ++k) {
+        if (orders[k] < SS_DIR_ROW || orders[k] > SS_DIR_WIN_COL_REV)
+            return fail(SS_ERR_INVALID_ARG, "%s: orders[%d] = %d is not an SS_DIR_* code", fn, k,
+                        orders[k]);
+        windowed = windowed || orders[k] >= SS_DIR_WIN;
+    }
+    if (windowed && window < 1)
+        return fail(SS_ERR_INVALID_ARG, "%s: a windowed order needs window >= 1", fn);
+    bool empty = false;
+    ss_status st = check_common(fn, batch, dim, H * W, dstate, ngroups, io, ndirs, u, delta, A, B,
+                                C, D, z, delta_bias, out, last_state, &empty);
+    if (st != SS_OK || empty) return st;
+    const int64_t es = io == SS_BF16 ? 2 : 4;
+    if ((H * W * es) % 16 != 0)
+        return fail(SS_ERR_UNSUPPORTED,
+                    "%s: rows must be 16-byte aligned (H * W * element size %% 16 == 0)", fn);
+    ScanArgs a = scan_args(batch, dim, H * W, dstate, ngroups, io, u, delta, A, B, C, D, z,
+                           delta_bias, delta_softplus, out, last_state, workspace,
+                           workspace_bytes, stream);
+    a.K = ndirs;
+    a.H = H;
+    a.W = W;
+    for (int k = 0; k < ndirs; ++k) a.orders[k] = orders[k];
+    // a window at least as large as the map is one window: the same traversal
+    const int64_t big = H > W ? H : W;
+    a.win = windowed ? (int)(window < big ? window : big) : 1;
+    if ((st = check_workspace(fn, steps_workspace_bytes(a), workspace, workspace_bytes))) return st;
+    if ((st = check_ws_overlap(fn, a))) return st;
+    return launch_steps(a);
+}
+
+size_t ss_multi_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t H, int64_t W, int ndirs) {
+    if (batch <= 0 || dim <= 0 || H <= 0 || W <= 0 || ndirs < 1 || ndirs > 8) return 0;
+    return (size_t)ndirs * batch * dim * H * W * sizeof(float);
+}
+
 ss_status ss_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, int dstate,
                                 int ngroups, ss_dtype io, const void *u, const void *delta,
                                 const float *A, const void *B, const void *C, const float *D,

@@ -259,6 +259,86 @@ __device__ __forceinline__ int64_t position_of(int order, int64_t s, int64_t L, 
     return s;
 }
 
+// Windowed traversals ("LocalMamba: Visual State Space Model with Windowed
+// Selective Scan": the map is divided into windows and scanned window by
+// window).  The Hm x Wm map is cut into w x w windows -- those of the last band
+// of rows and of the last column cut short -- visited row-major, each window
+// row-major.  The column-major variant is the same walk on the transposed map.
+// WinWalk steps through it one cell at a time, forward or backward, without
+// divisions; seek() places it at a step.
+struct WinWalk {
+    int Hm, Wm, w;
+    int band, j, rr, cc;  // band of rows (band*w ..), window in the band, cell in the window
+    __device__ __forceinline__ int hb() const { return min(w, Hm - band * w); }
+    __device__ __forceinline__ int wj() const { return min(w, Wm - j * w); }
+    __device__ __forceinline__ void seek(uint32_t s) {
+        const uint64_t bandsz = (uint64_t)w * (uint64_t)Wm;  // cells of a full band
+        band = (int)(s / bandsz);
+        uint32_t rem = (uint32_t)(s - (uint64_t)band * bandsz);
+        const int h = hb();
+        j = (int)(rem / (uint32_t)(h * w));
+        rem -= (uint32_t)(j * h * w);
+        const int ww = wj();
+        rr = (int)(rem / (uint32_t)ww);
+        cc = (int)rem - rr * ww;
+    }
+    __device__ __forceinline__ void next() {
+        if (++cc < wj()) return;
+        cc = 0;
+        if (++rr < hb()) return;
+        rr = 0;
+        if (++j * w < Wm) return;
+        j = 0;
+        ++band;
+    }
+    __device__ __forceinline__ void prev() {
+        if (--cc >= 0) return;
+        if (--rr >= 0) {
+            cc = wj() - 1;
+            return;
+        }
+        if (--j >= 0) {
+            rr = hb() - 1;
+            cc = wj() - 1;
+            return;
+        }
+        --band;
+        j = (Wm - 1) / w;
+        rr = hb() - 1;
+        cc = wj() - 1;
+    }
+    __device__ __forceinline__ int row() const { return band * w + rr; }
+    __device__ __forceinline__ int col() const { return j * w + cc; }
+};
+
+// Step of the windowed walk over an Hm x Wm map at which cell (r, c) is visited.
+__device__ __forceinline__ uint32_t win_step(int r, int c, int Hm, int Wm, int w) {
+    const int band = r / w, rr = r - band * w, j = c / w, cc = c - j * w;
+    const int hb = min(w, Hm - band * w), wj = min(w, Wm - j * w);
+    // band * w * Wm and j * hb * w count cells before this one: below H*W < 2^31
+    return (uint32_t)((int64_t)band * w * Wm + (int64_t)j * hb * w + rr * wj + cc);
+}
+
+// Traversal codes beyond the four of SS2D (match SS_DIR_* of the C ABI).
+enum { ORD_K_WIN = 4, ORD_K_WIN_COL = 5, ORD_K_WIN_REV = 6, ORD_K_WIN_COL_REV = 7 };
+
+// Step at which a direction with the given order visits cell (r, c) of the
+// H x W map: the inverse of the traversal.
+__device__ __forceinline__ uint32_t step_of(int order, int r, int c, int H, int W, int w) {
+    const uint32_t L = (uint32_t)H * (uint32_t)W;
+    uint32_t s;
+    switch (order) {
+    case 0: return (uint32_t)(r * W + c);
+    case 1: return (uint32_t)(c * H + r);
+    case 2: return L - 1 - (uint32_t)(r * W + c);
+    case 3: return L - 1 - (uint32_t)(c * H + r);
+    case ORD_K_WIN: return win_step(r, c, H, W, w);
+    case ORD_K_WIN_COL: return win_step(c, r, W, H, w);
+    case ORD_K_WIN_REV: s = win_step(r, c, H, W, w); return L - 1 - s;
+    default: s = win_step(c, r, W, H, w); return L - 1 - s;
+    }
+}
+
 // ------------------------------------------------------------------ lane-group reduction
 // R lanes (R a power of two) each hold R partial sums v[0..R): one
 // per step of an R-step block.  Afterwards the lane with group index g holds the

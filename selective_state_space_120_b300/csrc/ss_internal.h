@@ -22,7 +22,8 @@ struct ScanArgs {
     float *last_state = nullptr;
     void *ws = nullptr;
     size_t ws_bytes = 0;
-    int orders[4] = {0, 1, 2, 3};
+    int orders[8] = {0, 1, 2, 3, 4, 5, 6, 7};
+    int win = 0;  // window size of the windowed orders
     int chunks = 0;  // single direction: 0 automatic, 1 direct, >= 2 chunked with that many L-chunks
     const float *h0 = nullptr;  // single direction: initial state [batch, dim, N] (nullable)
     int zoh = 0;                // single direction: zero-order-hold input matrix
@@ -31,6 +32,11 @@ struct ScanArgs {
     const float *conv_w = nullptr, *conv_b = nullptr, *conv_x0 = nullptr;
     ss_stream_t stream = nullptr;
 };
+
+// Directions of any order (including the windowed ones), each stored by scan
+// step, then merged by position.
+size_t steps_workspace_bytes(const ScanArgs &a);
+ss_status launch_steps(const ScanArgs &a);
 
 // Backward pass of one direction: the forward call's inputs in `f` (its out,
 // last_state and workspace fields unused), the upstream gradient and the
@@ -46,7 +52,8 @@ struct BwdArgs {
 };
 
 // Direction traversal codes used by the kernels (match SS_DIR_*).
-enum { ORD_ROW = 0, ORD_COL = 1, ORD_ROW_REV = 2, ORD_COL_REV = 3 };
+enum { ORD_ROW = 0, ORD_COL = 1, ORD_ROW_REV = 2, ORD_COL_REV = 3, ORD_WIN = 4, ORD_WIN_COL = 5,
+       ORD_WIN_REV = 6, ORD_WIN_COL_REV = 7 };
 
 // Sets the thread-local error message and returns `st`.
 ss_status fail(ss_status st, const char *fmt, ...);

@@ -238,6 +238,81 @@ struct Scan1d {
         return check_launch("merge");
     }
 
+    // K directions of any order: each launch stores its direction's y_k + D_k*u
+    // by scan step into its own fp32 accumulator; one merge inverts the
+    // traversals and sums by position.
+    static ss_status run_steps(const ScanArgs &a) {
+        using namespace ssk;
+        const int io = a.io;
+        const int64_t rows = a.batch * a.dim;
+        const int K = a.K;
+        CUtensorMap mu, md, mz, mb, mc;
+        ss_status st;
+        if ((st = make_map(&mu, a.u, io, a.L, rows, C::T, C::CB))) return st;
+        if ((st = make_map(&md, a.delta, io, a.L, (uint64_t)rows * K, C::T, C::CB))) return st;
+        if ((st = make_map(&mz, a.z ? a.z : a.u, io, a.L, rows, C::T, C::CB))) return st;
+        const uint64_t bcrows = (uint64_t)a.batch * K * a.G * C::N;
+        if ((st = make_map(&mb, a.B, io, a.L, bcrows, C::T, C::N))) return st;
+        if ((st = make_map(&mc, a.C, io, a.L, bcrows, C::T, C::N))) return st;
+        auto kern = k_scan1d<C, true>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
+        Scan1dParams p{};
+        p.dim = a.dim;
+        p.L = a.L;
+        p.G = a.G;
+        p.dpg = (int)(a.dim / a.G);
+        p.Lc = a.L;
+        p.J = 1;
+        p.jbase = 0;
+        p.pass = 0;
+        p.K = K;
+        p.H = (int)a.H;
+        p.W = (int)a.W;
+        p.divH = FastDiv((uint32_t)a.H);
+        p.win = a.win;
+        p.u_g = a.u;
+        p.z_g = a.z;
+        p.A = a.A;
+        p.D = a.D;
+        p.bias = a.bias;
+        p.softplus = a.softplus;
+        p.has_z = a.z != nullptr;
+        p.out = a.out;
+        p.last_state = a.last_state;
+        const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);
+        const unsigned bgs = (unsigned)(a.batch * a.G);
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(a.stream);
+        float *acc0 = reinterpret_cast<float *>(a.ws);
+        // directions two at a time, side by side (grid z), for twice the warps
+        for (int k = 0; k < K; k += 2) {
+            const int nz = (k + 1 < K) ? 2 : 1;
+            p.nz = nz;
+            p.k0 = k;
+            for (int d = 0; d < 2; ++d) {
+                const int kk = (d < nz) ? k + d : k;
+                p.orders_z[d] = a.orders[kk];
+                p.modes_z[d] = OUT_STEP;
+                p.accs_z[d] = acc0 + (int64_t)kk * rows * a.L;
+            }
+            kern<<<dim3(cblocks, bgs, (unsigned)nz), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
+            if ((st = check_launch("direction scan"))) return st;
+        }
+        using IO = typename C::IO;
+        OrderSet os{};
+        os.K = K;
+        os.H = (int)a.H;
+        os.W = (int)a.W;
+        os.win = a.win;
+        for (int k = 0; k < K; ++k) os.orders[k] = a.orders[k];
+        const unsigned bx = (unsigned)((a.L + 255) / 256);
+        const int64_t want_y = std::max<int64_t>(1, (int64_t)num_sms() * 32 / bx);
+        const unsigned by = (unsigned)std::min<int64_t>({rows, want_y, (int64_t)65535});
+        k_merge_steps<IO><<<dim3(bx, by), 256, 0, s>>>(acc0, rows, reinterpret_cast<const IO *>(a.z),
+                                                      reinterpret_cast<IO *>(a.out), os);
+        return check_launch("merge by step");
+    }
+
     // Steps per L-chunk for a requested chunk count: a multiple of the T-tile.
     static int64_t chunk_len(int64_t L, int J) {
         if (J <= 1) return L;
@@ -293,6 +368,26 @@ template <typename IO, int N>
 ss_status dispatch_dirs(const ScanArgs &a) {
     using C = typename Pick1d<IO, N>::C;
     return Scan1d<C>::run_dirs(a);
+}
+
+template <typename IO, int N>
+ss_status dispatch_steps(const ScanArgs &a) {
+    using C = typename Pick1d<IO, N>::C;
+    return Scan1d<C>::run_steps(a);
+}
+
+template <typename IO>
+ss_status dispatch_steps_n(const ScanArgs &a) {
+    switch (a.N) {
+    case 1: return dispatch_steps<IO, 1>(a);
+    case 2: return dispatch_steps<IO, 2>(a);
+    case 4: return dispatch_steps<IO, 4>(a);
+    case 8: return dispatch_steps<IO, 8>(a);
+    case 16: return dispatch_steps<IO, 16>(a);
+    case 32: return dispatch_steps<IO, 32>(a);
+    case 64: return dispatch_steps<IO, 64>(a);
+    default: return fail(SS_ERR_UNSUPPORTED, "dstate %d is not one of 1,2,4,8,16,32,64", a.N);
+    }
 }
 
 template <typename IO, int N>
@@ -453,6 +548,14 @@ size_t multidir_workspace_bytes(const ScanArgs &a) {
     if (!scan1d_uses_tma(a)) return 0;  // rows not 16-byte aligned: on-chip merge path
     // one fp32 accumulator; SS2D scans two pairs of directions side by side into two
     return (size_t)a.batch * a.dim * a.L * sizeof(float) * (a.K == 4 ? 2 : 1);
+}
+
+size_t steps_workspace_bytes(const ScanArgs &a) {
+    return (size_t)a.K * a.batch * a.dim * a.L * sizeof(float);
+}
+
+ss_status launch_steps(const ScanArgs &a) {
+    return a.io == SS_BF16 ? dispatch_steps_n<__nv_bfloat16>(a) : dispatch_steps_n<float>(a);
 }
 
 ss_status launch_multidir(const ScanArgs &a) {

@@ -102,7 +102,9 @@ struct Cfg1 {
 // ones add to it, and the last adds its own term, applies the gate and writes
 // the I/O-typed output.  Each position receives its terms in launch order, so
 // the merged result is deterministic.
-enum { OUT_STORE = 0, OUT_ACC_FIRST = 1, OUT_ACC_ADD = 2, OUT_ACC_LAST = 3 };
+// OUT_STEP (directions of any order, merged by a separate kernel): store
+// y_k + D_k*u in fp32 by scan step, i.e. in the direction's own order.
+enum { OUT_STORE = 0, OUT_ACC_FIRST = 1, OUT_ACC_ADD = 2, OUT_ACC_LAST = 3, OUT_STEP = 4 };
 
 struct Scan1dParams {
     int64_t dim, L;
@@ -115,6 +117,7 @@ struct Scan1dParams {
     int order;    // traversal of direction k (0 row, 1 column, 2, 3 reversed)
     int H, W;     // map of the column orders (a plain sequence: H = 1, W = L)
     FastDiv divH;
+    int win;      // window size of the windowed orders
     int mode;     // OUT_*
     float *acc;   // [batch*dim, L] fp32 merge accumulator by position (modes 1-3)
     // Multi-direction launches may scan several directions side by side:
@@ -539,7 +542,7 @@ __device__ __forceinline__ bool merge_task(const Scan1dParams &p, const MergeReg
 template <class C>
 __device__ __forceinline__ void load_partials(const Scan1dParams &p, MergeRegs<C> &mr, int64_t s0) {
     using IO = typename C::IO;
-    if (p.mode == OUT_ACC_FIRST) return;
+    if (p.mode == OUT_ACC_FIRST || p.mode == OUT_STEP) return;
 #pragma unroll
     for (int m = 0; m < MergeRegs<C>::TPL; ++m) {
         int64_t sg;
@@ -568,6 +571,10 @@ __device__ __forceinline__ void store_partials(const Scan1dParams &p, const Merg
         const float4 v = *reinterpret_cast<const float4 *>(smem + C::OFF_OB + mr.chr[m] * C::OBROW +
                                                            mr.qq[m] * 16);
         float *accr = p.acc + mr.rowL[m];
+        if (p.mode == OUT_STEP) {  // by scan step: steps sg .. sg+3
+            *reinterpret_cast<float4 *>(accr + sg) = v;
+            continue;
+        }
         IO *outr = reinterpret_cast<IO *>(p.out) + mr.rowL[m];
         const bool gate = p.mode == OUT_ACC_LAST && p.has_z;
         // w[j] is the term of step sg + j; a reversed order runs back to front
@@ -749,6 +756,29 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
         if (!MULTI || u_tiled) return;
         const IO *urow = reinterpret_cast<const IO *>(p.u_g) + prow * p.L;
         const IO *zrow = reinterpret_cast<const IO *>(p.z_g) + prow * p.L;
+        if (p.order >= ORD_K_WIN) {
+            // windowed orders: walk the windows from this thread's first step
+            // (forward for the plain orders, backward for the reversed ones)
+            const int64_t s_first = t_begin + (int64_t)i * T + pt0;
+            const bool tr = p.order == ORD_K_WIN_COL || p.order == ORD_K_WIN_COL_REV;
+            const bool rv = p.order >= ORD_K_WIN_REV;
+            WinWalk ww;
+            ww.Hm = tr ? p.W : p.H;
+            ww.Wm = tr ? p.H : p.W;
+            ww.w = p.win;
+            const int64_t sc = min(s_first, p.L - 1);
+            ww.seek((uint32_t)(rv ? p.L - 1 - sc : sc));
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const bool in = s_first + e < p.L;
+                const int64_t pos = tr ? (int64_t)ww.col() * p.W + ww.row()
+                                       : (int64_t)ww.row() * p.W + ww.col();
+                gu[e] = in ? IOT<IO>::load_raw(urow + pos) : Raw(0);
+                if (rv) ww.prev();
+                else ww.next();
+            }
+            return;
+        }
         // the map cell (r, c) of the first step, then one row down (forward) or
         // up (reversed) per step, wrapping into the next / previous column
         const int64_t s_first = t_begin + (int64_t)i * T + pt0;
@@ -1036,6 +1066,38 @@ __global__ void __launch_bounds__(256) k_merge2(const float *__restrict__ acc_ro
             if (zr) v *= silu(IOT<IO>::load(zr + pos));
             o[pos] = IOT<IO>::from_f(v);
         }
+    }
+}
+
+// Final merge of a call whose directions stored their terms by scan step
+// (OUT_STEP), for directions of any order: out[p] = (sum_k acc_k[step_k(p)]) *
+// SiLU(z[p]) in the I/O type, where step_k inverts direction k's traversal.
+// acc is [K][rows][L].  A thread owns one position: it inverts the K
+// traversals once and then walks rows blockIdx.y, blockIdx.y + gridDim.y, ...
+// (the traversals are the same for every row).
+struct OrderSet {
+    int K, H, W, win;
+    int orders[8];
+};
+template <typename IO>
+__global__ void __launch_bounds__(256) k_merge_steps(const float *__restrict__ acc, int64_t rows,
+                                                     const IO *__restrict__ z, IO *__restrict__ out,
+                                                     const OrderSet os) {
+    const int64_t L = (int64_t)os.H * os.W;
+    const int pos = blockIdx.x * blockDim.x + threadIdx.x;
+    if (pos >= L) return;
+    const int r = pos / os.W, c = pos - r * os.W;
+    uint32_t st[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) st[k] = k < os.K ? step_of(os.orders[k], r, c, os.H, os.W, os.win) : 0u;
+    for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
+        float y = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (k < os.K) y += acc[((int64_t)k * rows + row) * L + st[k]];
+        const int64_t i = row * L + pos;
+        if (z) y *= silu(IOT<IO>::load(z + i));
+        out[i] = IOT<IO>::from_f(y);
     }
 }
 

@@ -45,6 +45,8 @@ class Workload:
     H: int = 1
     W: int = 0            # W = L for a plain sequence
     conv: bool = False    # u is the input of a fused Conv1D(k=4) + SiLU
+    orders: tuple = ()    # traversal codes (SS_DIR_*) of an any-order call; () = the kind's own
+    win: int = 0          # window size of the windowed orders
 
     @property
     def elems(self) -> int:
@@ -52,6 +54,8 @@ class Workload:
 
     @property
     def kind(self) -> str:
+        if self.orders:
+            return "orders"
         return {1: "scan", 2: "bidir", 4: "ss2d"}[self.K]
 
 
@@ -64,6 +68,12 @@ VMAMBA_SS2D = Workload("vmamba_t_ss2d_b32_d192_56x56_n16", 32, 192, 56 * 56, K=4
                        with_z=False, H=56, W=56)
 
 ALL = (TINY_F32, MAMBA_LAYER, LONG_SEQ, VIM_BIDIR, VMAMBA_SS2D)
+
+# LocalMamba-style windowed scan on the VMamba-T stage-1 map: four windowed
+# directions (7 x 7 windows, row- and column-major, and their reverses; codes
+# SS_DIR_WIN, SS_DIR_WIN_COL, SS_DIR_WIN_REV, SS_DIR_WIN_COL_REV), no gate.
+LOCAL_WIN = Workload("localmamba_win7_b32_d192_56x56_n16", 32, 192, 56 * 56, K=4, with_z=False,
+                     H=56, W=56, orders=(4, 5, 6, 7), win=7)
 
 # The Mamba layer with its Conv1D(k=4) + SiLU input branch fused in front of the
 # scan (weights ~ N(0, 0.5^2), bias ~ N(0, 0.1^2)).

@@ -252,3 +252,24 @@ def test_backward_workspace_holds_a_checkpoint_per_8_steps(lib):
     assert b.workspace_bytes(b.SS_KIND_SCAN_BWD, 2, 3, 17, 4) == 2 * 3 * 3 * 4 * 4
     assert b.workspace_bytes(b.SS_KIND_SCAN_BWD, 2, 3, 0, 4) == 0
     assert b.workspace_bytes(b.SS_KIND_SCAN_BWD, 2, 3, 64, 12) == 0
+
+
+@fake_ptrs
+def test_multi_scan_validates(lib):
+    def call(ndirs=2, orders=(b.SS_DIR_WIN, b.SS_DIR_ROW), window=2, H=4, W=8, wsb=None, ws=A16 + 0x900000):
+        ords = (ctypes.c_int * max(1, len(orders)))(*orders)
+        if wsb is None:
+            wsb = b.load().ss_multi_scan_workspace_bytes(1, 8, H, W, ndirs)
+        return lib.ss_multi_scan_fwd(1, 8, H, W, ndirs, ords, window, 16, 1, b.SS_BF16, A16,
+                                     A16 + 0x100000, A16 + 0x200000, A16 + 0x300000, A16 + 0x400000,
+                                     None, None, 1, None, A16 + 0x500000, None, ws, wsb, None)
+    assert call(ndirs=0) == b.SS_ERR_INVALID_ARG
+    assert call(ndirs=9, orders=(0,) * 9) == b.SS_ERR_INVALID_ARG
+    assert call(orders=(b.SS_DIR_WIN, 8)) == b.SS_ERR_INVALID_ARG
+    assert "SS_DIR_" in b.last_error()
+    assert call(window=0) == b.SS_ERR_INVALID_ARG          # a windowed order needs a window
+    assert call(H=3, W=5) == b.SS_ERR_UNSUPPORTED          # rows of 15 bf16 values
+    assert call(ws=None) == b.SS_ERR_WORKSPACE
+    assert call(wsb=b.load().ss_multi_scan_workspace_bytes(1, 8, 4, 8, 2) - 4) == b.SS_ERR_WORKSPACE
+    assert call(ws=A16 + 0x100000) == b.SS_ERR_INVALID_ARG  # workspace on top of delta
+    assert b.load().ss_multi_scan_workspace_bytes(2, 8, 4, 8, 3) == 3 * 2 * 8 * 32 * 4
