@@ -69,6 +69,8 @@ def _bind(path: str):
     lib.ssor_softplus_scalar.argtypes = [ctypes.c_double]
     lib.ssor_position_of.restype = ctypes.c_int64
     lib.ssor_position_of.argtypes = [ctypes.c_int, i64, i64, i64]
+    lib.ssor_dwconv3x3_silu.restype = ctypes.c_int
+    lib.ssor_dwconv3x3_silu.argtypes = [i64, i64, i64, i64, dp, dp, dp, dp]
     lib.ssor_order_table.restype = ctypes.c_int
     lib.ssor_order_table.argtypes = [ctypes.c_int, i64, i64, i64, ctypes.POINTER(i64)]
     return lib
@@ -231,6 +233,21 @@ def conv_silu(x, w, bias=None, x0=None):
     x0 = _f64(x0, (batch, dim, KW - 1), "x0")
     u = np.empty_like(x)
     rc = _load().ssor_conv_silu(batch, dim, L, KW, _ptr(x), _ptr(w), _ptr(bias), _ptr(x0), _ptr(u))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return u
+
+
+def dwconv3x3_silu(x, w, bias=None):
+    """The SS2D block's input branch: depthwise 3 x 3 cross-correlation with zero
+    padding, plus bias, then SiLU.  x [batch, dim, H, W]; w [dim, 3, 3]; bias
+    [dim].  Returns u [batch, dim, H, W] float64."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    batch, dim, H, W = x.shape
+    w = _f64(w, (dim, 3, 3), "w")
+    bias = _f64(bias, (dim,), "bias")
+    u = np.empty_like(x)
+    rc = _load().ssor_dwconv3x3_silu(batch, dim, H, W, _ptr(x), _ptr(w), _ptr(bias), _ptr(u))
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return u

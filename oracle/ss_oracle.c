@@ -259,6 +259,39 @@ int ssor_conv_silu(int64_t batch, int64_t dim, int64_t L, int64_t KW, const doub
 }
 
 /*
+ * ssor_dwconv3x3_silu: the input branch of VMamba's SS2D block ("Mamba Series
+ * ...", VSS block structure and SS2Dv0.forwardv0: DWConv 3x3 -> SiLU): a
+ * depthwise 3 x 3 cross-correlation with zero padding of one cell and a bias,
+ * then SiLU:
+ *     v = bias[d] + sum_{i,j in -1..1} w[d, i+1, j+1] * x[b, d, r+i, c+j]   (0 outside the map)
+ *     u[b, d, r, c] = v * sigmoid(v)
+ *   x, u [batch, dim, H, W]; w [dim, 3, 3]; bias [dim] (NULL: 0).  Returns 0 or -1.
+ */
+int ssor_dwconv3x3_silu(int64_t batch, int64_t dim, int64_t H, int64_t W, const double *x,
+                        const double *w, const double *bias, double *u) {
+    if (batch < 0 || dim <= 0 || H <= 0 || W <= 0 || !x || !w || !u) return -1;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const double *xp = x + (b * dim + d) * H * W;
+            for (int64_t r = 0; r < H; ++r) {
+                for (int64_t c = 0; c < W; ++c) {
+                    double v = bias ? bias[d] : 0.0;
+                    for (int64_t i = -1; i <= 1; ++i) {
+                        for (int64_t j = -1; j <= 1; ++j) {
+                            const int64_t rr = r + i, cc = c + j;
+                            if (rr < 0 || rr >= H || cc < 0 || cc >= W) continue;
+                            v += w[d * 9 + (i + 1) * 3 + (j + 1)] * xp[rr * W + cc];
+                        }
+                    }
+                    u[((b * dim + d) * H + r) * W + c] = v / (1.0 + exp(-v));
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/*
  * ssor_scan_bwd: gradients of the single-direction scan (Euler input matrix,
  * zero initial state) for an upstream gradient dy of out.  The forward pass is
  * the recurrence above; the pages state that the backward pass recomputes the

@@ -45,6 +45,8 @@ MUTANTS = {
     "window_cells_transposed": ("for (int64_t c = c0; c < c0 + w && c < W; ++c) pos[s++] = r * W + c;",
                                 "for (int64_t c = c0; c < c0 + w && c < W; ++c) pos[s++] = c * H + r;"),
     "window_reverse_missing": ("const int64_t t = pos[i];", "const int64_t t = pos[j];"),
+    "dwconv_kernel_transposed": ("v += w[d * 9 + (i + 1) * 3 + (j + 1)] * xp[rr * W + cc];",
+                                 "v += w[d * 9 + (j + 1) * 3 + (i + 1)] * xp[rr * W + cc];"),
     "group_map_interleaved": ("const int64_t g = d / dpg;", "const int64_t g = d % ngroups;"),
     "ignores_initial_state": ("h[n] = h0 ? h0[((b * K + k) * dim + d) * N + n] : 0.0;",
                               "h[n] = 0.0;"),
@@ -95,6 +97,18 @@ class _Variant:
         u = np.empty_like(x)
         rc = self.lib.ssor_conv_silu(batch, dim, L, KW, _oracle._ptr(x), _oracle._ptr(w),
                                      _oracle._ptr(bias), _oracle._ptr(x0), _oracle._ptr(u))
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+        return u
+
+    def dwconv3x3_silu(self, x, w, bias=None):
+        x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+        batch, dim, H, W = x.shape
+        w = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
+        bias = None if bias is None else np.ascontiguousarray(np.asarray(bias, dtype=np.float64))
+        u = np.empty_like(x)
+        rc = self.lib.ssor_dwconv3x3_silu(batch, dim, H, W, _oracle._ptr(x), _oracle._ptr(w),
+                                          _oracle._ptr(bias), _oracle._ptr(u))
         if rc != 0:
             raise ValueError("oracle rejected its arguments")
         return u

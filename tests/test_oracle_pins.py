@@ -499,3 +499,40 @@ def test_windowed_scan_equals_scan_of_permuted_copy(oracle, H, W, w):
         want *= z / (1.0 + np.exp(-z))
         np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-13)
         np.testing.assert_allclose(got_last, last, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- DWConv 3x3 + SiLU (SS2D input branch)
+def test_dwconv_identity_kernel_is_silu(oracle):
+    """Centre tap 1, no bias: u = SiLU(x)."""
+    rng = np.random.default_rng(51)
+    x = rng.standard_normal((2, 3, 5, 7))
+    w = np.zeros((3, 3, 3))
+    w[:, 1, 1] = 1.0
+    np.testing.assert_allclose(oracle.dwconv3x3_silu(x, w), _silu(x), rtol=1e-15, atol=0)
+
+
+def test_dwconv_equals_scipy_correlate2d(oracle):
+    """Every channel against scipy.signal.correlate2d(mode='same') with zero fill."""
+    from scipy.signal import correlate2d
+    rng = np.random.default_rng(52)
+    batch, dim, H, W = 2, 3, 6, 9
+    x = rng.standard_normal((batch, dim, H, W))
+    w = rng.standard_normal((dim, 3, 3))
+    bias = rng.standard_normal(dim)
+    got = oracle.dwconv3x3_silu(x, w, bias)
+    for b in range(batch):
+        for d in range(dim):
+            v = correlate2d(x[b, d], w[d], mode="same", boundary="fill", fillvalue=0.0) + bias[d]
+            np.testing.assert_allclose(got[b, d], _silu(v), rtol=1e-13, atol=1e-14)
+
+
+def test_dwconv_separable_kernel(oracle):
+    """A kernel outer(a, c) is a 3-tap correlation along the columns with c, then
+    along the rows with a (np.convolve of the reversed taps, zero padded)."""
+    rng = np.random.default_rng(53)
+    x = rng.standard_normal((1, 1, 5, 8))
+    a, c = rng.standard_normal(3), rng.standard_normal(3)
+    got = oracle.dwconv3x3_silu(x, np.outer(a, c)[None])
+    rows = np.stack([np.convolve(row, c[::-1], mode="same") for row in x[0, 0]])
+    both = np.stack([np.convolve(col, a[::-1], mode="same") for col in rows.T]).T
+    np.testing.assert_allclose(got[0, 0], _silu(both), rtol=1e-13, atol=1e-14)
