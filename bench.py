@@ -702,6 +702,52 @@ def measure_bwd(steps: int, warmup: int, peak_gbs: float, peak_kind: str):
                        "l2": "inputs rotate over 2 copies (201 MB of inputs each > 126 MB L2)"}}
 
 
+DWCONV_NAME = "vmamba_t_dwconv3x3_b32_d192_56x56"
+
+
+def measure_dwconv(steps: int, warmup: int, peak_gbs: float, peak_kind: str):
+    """The SS2D block's input branch (DWConv 3x3 + SiLU) on the VMamba-T stage-1
+    map, 32 x 192 x 56 x 56, bf16: one call per step, rotating over input/output
+    copies larger than L2."""
+    import torch
+    from selective_state_space_120_b300 import _binding as b
+    lib = b.load()
+    wl = wk.Workload(DWCONV_NAME, 32, 192, 56 * 56, K=4, with_z=False, H=56, W=56, conv2d=True)
+    inp = wk.make_inputs(wl, 0)
+    x0 = Runner._to_dev(inp.u)
+    w = Runner._to_dev(inp.conv2d_w)
+    bias = Runner._to_dev(inp.conv2d_b)
+    es = 2
+    alg = 2 * wl.elems * es + wl.dim * 10 * 4
+    copies = max(2, int(np.ceil(3 * L2_BYTES / alg)) + 1)
+    xs = [x0 if i == 0 else x0.clone() for i in range(copies)]
+    us = [torch.empty_like(x0) for _ in range(copies)]
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    calls = [(wl.batch, wl.dim, wl.H, wl.W, 1, xs[i].data_ptr(), w.data_ptr(), bias.data_ptr(),
+              us[i].data_ptr(), st) for i in range(copies)]
+    for i in range(warmup):
+        b.check(lib.ss_dwconv3x3_silu_fwd(*calls[i % copies]))
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    stream = torch.cuda.current_stream()
+    for i in range(steps):
+        ev[i][0].record(stream)
+        b.check(lib.ss_dwconv3x3_silu_fwd(*calls[(warmup + i) % copies]))
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(c) for a, c in ev]))
+    ach = alg / (ms * 1e-3) / 1e9
+    return {"value": wl.elems / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
+            "kernel_launches_per_step": 1,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peak_gbs, "unit": "GB/s",
+                         "frac": ach / peak_gbs, "peak_source": f"{peak_kind} (copy bandwidth)",
+                         "algorithmic_bytes_per_launch": alg, "traffic": ncu_traffic_named(DWCONV_NAME)},
+            "config": {"workload": DWCONV_NAME, "batch": wl.batch, "dim": wl.dim, "H": wl.H,
+                       "W": wl.W, "io_dtype": "bf16",
+                       "l2": f"inputs rotate over {copies} copies ({copies * alg / 1e6:.0f} MB > 126 MB L2)"}}
+
+
 def roofline(wl, kern_ms, peak, peak_kind):
     alg = algorithmic_bytes(wl)
     ach = alg / (kern_ms * 1e-3) / 1e9
@@ -716,7 +762,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(WORKLOADS) + [BWD_NAME],
+    ap.add_argument("--workload", default=HEADLINE.name,
+                    choices=sorted(WORKLOADS) + [BWD_NAME, DWCONV_NAME],
                     help="forward workload to time (the backward pass: its own line only)")
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
@@ -741,6 +788,22 @@ def main(argv=None):
     ss.load_library()
 
     peak, peak_kind = measured_peaks()
+    if args.workload == DWCONV_NAME:
+        r = measure_dwconv(args.steps, args.warmup, peak, peak_kind)
+        ms = max_over_ranks(r["ms_per_step"], world, "cuda")
+        if rank == 0:
+            line = {"metric": "DWConv3x3+SiLU Gelem/s (B·D·H·W)",
+                    "value": r["value"] * world, "unit": UNIT, "n_gpus": world,
+                    "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                    "dtype": "f32", "data": "synthetic (seeded NumPy PCG64)",
+                    "config": r["config"], "roofline": r["roofline"],
+                    "gpu_launches": args.steps}
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
     if args.workload == BWD_NAME:
         # the backward pass alone, on one GPU per rank (replicas), device-resident inputs
         r = measure_bwd(args.steps, args.warmup, peak, peak_kind)
@@ -790,6 +853,10 @@ def main(argv=None):
             others[DECODE_NAME] = measure_decode(256)
         except Exception as e:  # noqa: BLE001 -- reported, not hidden
             others[DECODE_NAME] = {"error": f"{type(e).__name__}: {e}"}
+        try:
+            others[DWCONV_NAME] = measure_dwconv(max(3, min(args.steps, 100)), 5, peak, peak_kind)
+        except Exception as e:  # noqa: BLE001 -- reported, not hidden
+            others[DWCONV_NAME] = {"error": f"{type(e).__name__}: {e}"}
         try:
             others[BWD_NAME] = measure_bwd(max(3, min(args.steps, 30)), 3, peak, peak_kind)
             torch.cuda.empty_cache()

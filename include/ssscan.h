@@ -322,6 +322,21 @@ ss_status ss_multi_scan_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, in
                             int delta_softplus, const void *z, void *out, float *last_state,
                             void *workspace, size_t workspace_bytes, ss_stream_t stream);
 
+/*
+ * ss_dwconv3x3_silu_fwd -- the input branch of VMamba's SS2D block ("Mamba Series
+ * ...", VSS block structure and SS2Dv0.forwardv0: DWConv 3x3 -> SiLU -> SS2D):
+ *     u[b,d,r,c] = SiLU(bias[d] + sum_{i,j=-1..1} w[d,i+1,j+1] * x[b,d,r+i,c+j])
+ * with zero padding of one cell (cross-correlation, as a conv2d layer computes it).
+ *   x, u [batch, dim, H, W] io; w [dim, 3, 3] float; bias [dim] float, nullable.
+ * Device pointers, 16-byte aligned; u must not overlap x.  Empty shapes return
+ * SS_OK.  Asynchronous on `stream`.  It is a separate pass, not fused into the
+ * scan: in the SS2D block the x_proj projection that makes Delta, B, C reads u,
+ * so u is in memory before the scan starts anyway.
+ */
+ss_status ss_dwconv3x3_silu_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, ss_dtype io,
+                                const void *x, const float *w, const float *bias, void *u,
+                                ss_stream_t stream);
+
 /* Workspace of ss_multi_scan_fwd (0 for an empty or invalid shape). */
 size_t ss_multi_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t H, int64_t W, int ndirs);
 

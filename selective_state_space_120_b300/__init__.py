@@ -211,6 +211,25 @@ from ._binding import (SS_DIR_COL as DIR_COL, SS_DIR_COL_REV as DIR_COL_REV,  # 
                        SS_DIR_WIN_COL_REV as DIR_WIN_COL_REV, SS_DIR_WIN_REV as DIR_WIN_REV)
 
 
+def dwconv3x3_silu(x, w, bias=None, out=None, stream=None):
+    """SS2D's input branch: depthwise 3 x 3 convolution (zero padding) + bias, then
+    SiLU.  x [batch, dim, H, W] (bf16 or f32); w [dim, 3, 3] and bias [dim]
+    float32.  Returns u like x."""
+    torch = _torch()
+    lib = _b.load()
+    batch, dim, H, W = x.shape
+    dev = x.device
+    _check_io("x", x, x.dtype, dev)
+    _check_io("w", w, torch.float32, dev, (dim, 3, 3))
+    _check_io("bias", bias, torch.float32, dev, (dim,))
+    if out is None:
+        out = torch.empty_like(x)
+    _check_io("out", out, x.dtype, dev, tuple(x.shape))
+    _b.check(lib.ss_dwconv3x3_silu_fwd(batch, dim, H, W, _io_code(x), _ptr(x), _ptr(w), _ptr(bias),
+                                       _ptr(out), _stream(stream, dev)))
+    return out
+
+
 def _multidir_workspace(lib, kind, batch, dim, L, N, dev, workspace):
     torch = _torch()
     wsb = int(lib.ss_workspace_bytes(kind, batch, dim, L, N))

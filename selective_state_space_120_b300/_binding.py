@@ -38,7 +38,8 @@ EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_opts", "ss_bidir_scan
            "ss_get_device_status", "ss_last_error_string", "ss_version",
            "ss_debug_set_wait_budget_ns", "ss_debug_set_flags",
            "ss_selective_scan_fwd_noalloc", "ss_selective_state_update",
-           "ss_selective_scan_bwd", "ss_multi_scan_fwd", "ss_multi_scan_workspace_bytes")
+           "ss_selective_scan_bwd", "ss_multi_scan_fwd", "ss_multi_scan_workspace_bytes",
+           "ss_dwconv3x3_silu_fwd")
 
 
 class SSError(RuntimeError):
@@ -91,6 +92,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         # workspace_bytes, stream
         lib.ss_multi_scan_fwd.argtypes = [i64, i64, i64, i64, i32, ctypes.POINTER(i32), i32, i32,
                                           i32, i32] + [vp] * 7 + [i32, vp, vp, vp, vp, sz, vp]
+        lib.ss_dwconv3x3_silu_fwd.argtypes = [i64, i64, i64, i64, i32, vp, vp, vp, vp, vp]
+        lib.ss_dwconv3x3_silu_fwd.restype = ctypes.c_int
         lib.ss_multi_scan_workspace_bytes.argtypes = [i64, i64, i64, i64, i32]
         lib.ss_multi_scan_workspace_bytes.restype = sz
         for f in ("ss_selective_scan_fwd", "ss_selective_scan_fwd_opts", "ss_bidir_scan_fwd",

@@ -473,6 +473,26 @@ ss_status ss_multi_scan_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, in
     return launch_steps(a);
 }
 
+ss_status ss_dwconv3x3_silu_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, ss_dtype io,
+                                const void *x, const float *w, const float *bias, void *u,
+                                ss_stream_t stream) {
+    static const char *fn = "ss_dwconv3x3_silu_fwd";
+    if (batch < 0 || dim < 0 || H < 0 || W < 0)
+        return fail(SS_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (io != SS_F32 && io != SS_BF16) return fail(SS_ERR_UNSUPPORTED, "%s: unknown I/O dtype %d", fn, io);
+    if (batch == 0 || dim == 0 || H == 0 || W == 0) return SS_OK;
+    if (H >= (1ll << 31) || W >= (1ll << 31) || H * W >= (1ll << 31) || batch * dim >= (1ll << 40))
+        return fail(SS_ERR_UNSUPPORTED, "%s: map too large", fn);
+    if (!x || !w || !u) return fail(SS_ERR_INVALID_ARG, "%s: x, w and u are required", fn);
+    for (const void *q : {x, (const void *)w, (const void *)bias, (const void *)u})
+        if (q && !aligned16(q)) return fail(SS_ERR_ALIGNMENT, "%s: tensor at %p is not 16-byte aligned", fn, q);
+    const int64_t es = io == SS_BF16 ? 2 : 4;
+    const int64_t n = batch * dim * H * W * es;
+    if (overlaps({static_cast<const char *>(u), n}, {static_cast<const char *>(x), n}))
+        return fail(SS_ERR_INVALID_ARG, "%s: u overlaps x", fn);
+    return launch_dwconv3x3(batch, dim, H, W, io, x, w, bias, u, stream);
+}
+
 size_t ss_multi_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t H, int64_t W, int ndirs) {
     if (batch <= 0 || dim <= 0 || H <= 0 || W <= 0 || ndirs < 1 || ndirs > 8) return 0;
     return (size_t)ndirs * batch * dim * H * W * sizeof(float);

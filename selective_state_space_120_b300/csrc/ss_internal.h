@@ -75,6 +75,9 @@ size_t scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t L, int N);
 // Zeroes the summed gradient outputs, then runs the backward kernel (nothing
 // but the zeroing when `empty`).
 ss_status launch_scan_bwd(const BwdArgs &a, bool empty);
+// Depthwise 3 x 3 convolution + SiLU over [batch, dim, H, W] maps.
+ss_status launch_dwconv3x3(int64_t batch, int64_t dim, int64_t H, int64_t W, int io, const void *x,
+                           const float *w, const float *bias, void *u, ss_stream_t stream);
 ss_status read_device_status(ss_stream_t stream);
 ss_status set_wait_budget(unsigned long long ns);
 ss_status set_debug_flags(unsigned int flags);

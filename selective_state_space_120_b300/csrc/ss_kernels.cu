@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "ss_bwd.cuh"
+#include "ss_conv2d.cuh"
 #include "ss_device.cuh"
 #include "ss_internal.h"
 #include "ss_multidir.cuh"
@@ -701,6 +702,40 @@ ss_status launch_scan_bwd(const BwdArgs &a, bool empty) {
     if ((st = zero_async(a.dbias, (size_t)f.dim * sizeof(float), s))) return st;
     if (empty) return SS_OK;
     return f.io == SS_BF16 ? dispatch_bwd<__nv_bfloat16>(a) : dispatch_bwd<float>(a);
+}
+
+ss_status launch_dwconv3x3(int64_t batch, int64_t dim, int64_t H, int64_t W, int io, const void *x,
+                           const float *w, const float *bias, void *u, ss_stream_t stream) {
+    using namespace ssk;
+    const int64_t planes = batch * dim;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (W <= DWC_BAND_MAXW) {
+        // bands of up to ~24 KB of fp32 rows (the whole plane when it fits)
+        const int RB = (int)std::max<int64_t>(1, std::min<int64_t>(H, 6144 / (W + 2) - 2));
+        const size_t smem = (size_t)(RB + 2) * (W + 2) * sizeof(float);
+        const dim3 grid((unsigned)std::min<int64_t>(planes, (int64_t)num_sms() * 64),
+                        (unsigned)((H + RB - 1) / RB));
+        if (io == SS_BF16)
+            k_dwconv3x3_silu_band<__nv_bfloat16><<<grid, DWC_THREADS, smem, s>>>(
+                reinterpret_cast<const __nv_bfloat16 *>(x), w, bias,
+                reinterpret_cast<__nv_bfloat16 *>(u), planes, (int)dim, (int)H, (int)W, RB);
+        else
+            k_dwconv3x3_silu_band<float><<<grid, DWC_THREADS, smem, s>>>(
+                reinterpret_cast<const float *>(x), w, bias, reinterpret_cast<float *>(u), planes,
+                (int)dim, (int)H, (int)W, RB);
+        return check_launch("dwconv3x3");
+    }
+    const dim3 grid((unsigned)((W + DWC_TW - 1) / DWC_TW), (unsigned)((H + DWC_TH - 1) / DWC_TH),
+                    (unsigned)std::min<int64_t>(planes, 65535));
+    if (io == SS_BF16)
+        k_dwconv3x3_silu<__nv_bfloat16><<<grid, DWC_THREADS, 0, s>>>(
+            reinterpret_cast<const __nv_bfloat16 *>(x), w, bias, reinterpret_cast<__nv_bfloat16 *>(u),
+            planes, (int)dim, (int)H, (int)W);
+    else
+        k_dwconv3x3_silu<float><<<grid, DWC_THREADS, 0, s>>>(reinterpret_cast<const float *>(x), w, bias,
+                                                             reinterpret_cast<float *>(u), planes,
+                                                             (int)dim, (int)H, (int)W);
+    return check_launch("dwconv3x3");
 }
 
 ss_status read_device_status(ss_stream_t stream) {

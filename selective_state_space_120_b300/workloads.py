@@ -15,6 +15,7 @@ Recipe (the workloads of the Mamba / Vim / VMamba pages, with synthetic data):
     B_k, C_k        ~ N(0, 1)                           [batch, K, G, N, L]
     D               = 1                                 [K*dim]
     conv workloads, drawn last: conv_w ~ N(0, 0.5^2) [dim, 4], conv_b ~ N(0, 0.1^2)
+    conv2d workloads, drawn last: conv2d_w ~ N(0, 0.3^2) [dim, 3, 3], conv2d_b ~ N(0, 0.1^2)
     backward pass: the upstream gradient dout ~ N(0, 1) [batch, dim, L], from
                    its own PCG64 stream seeded with (seed, 1) (make_dout)
 Inputs of a bf16 workload are rounded to bf16 (round-to-nearest-even) on the
@@ -45,6 +46,7 @@ class Workload:
     H: int = 1
     W: int = 0            # W = L for a plain sequence
     conv: bool = False    # u is the input of a fused Conv1D(k=4) + SiLU
+    conv2d: bool = False  # u comes from the SS2D block's DWConv 3x3 + SiLU of an input map x
     orders: tuple = ()    # traversal codes (SS_DIR_*) of an any-order call; () = the kind's own
     win: int = 0          # window size of the windowed orders
 
@@ -121,6 +123,8 @@ class Inputs:
     extra: dict = field(default_factory=dict)
     conv_w: np.ndarray | None = None   # [dim, 4] float32 (conv workloads)
     conv_b: np.ndarray | None = None   # [dim] float32
+    conv2d_w: np.ndarray | None = None  # [dim, 3, 3] float32 (conv2d workloads)
+    conv2d_b: np.ndarray | None = None  # [dim] float32
 
     def as_f64(self, name: str) -> np.ndarray | None:
         """The exact values handed to the GPU, widened to float64."""
@@ -161,6 +165,10 @@ def make_inputs(wl: Workload, seed: int = 0) -> Inputs:
         # same workload without the conv
         inp.conv_w = (rng.standard_normal((d, 4)) * 0.5).astype(np.float32)
         inp.conv_b = (rng.standard_normal(d) * 0.1).astype(np.float32)
+    if wl.conv2d:
+        # drawn after everything else as well; u is then the map the convolution reads
+        inp.conv2d_w = (rng.standard_normal((d, 3, 3)) * 0.3).astype(np.float32)
+        inp.conv2d_b = (rng.standard_normal(d) * 0.1).astype(np.float32)
     return inp
 
 

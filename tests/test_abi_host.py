@@ -273,3 +273,18 @@ def test_multi_scan_validates(lib):
     assert call(wsb=b.load().ss_multi_scan_workspace_bytes(1, 8, 4, 8, 2) - 4) == b.SS_ERR_WORKSPACE
     assert call(ws=A16 + 0x100000) == b.SS_ERR_INVALID_ARG  # workspace on top of delta
     assert b.load().ss_multi_scan_workspace_bytes(2, 8, 4, 8, 3) == 3 * 2 * 8 * 32 * 4
+
+
+@fake_ptrs
+def test_dwconv_validates(lib):
+    args = [1, 4, 8, 8, b.SS_BF16, A16, A16 + 0x100000, None, A16 + 0x200000, None]
+    bad = list(args); bad[5] = None
+    assert lib.ss_dwconv3x3_silu_fwd(*bad) == b.SS_ERR_INVALID_ARG
+    bad = list(args); bad[8] = A16 + 0x40
+    assert lib.ss_dwconv3x3_silu_fwd(*bad) == b.SS_ERR_INVALID_ARG     # u on top of x
+    bad = list(args); bad[7] = A16 + 0x300004
+    assert lib.ss_dwconv3x3_silu_fwd(*bad) == b.SS_ERR_ALIGNMENT
+    bad = list(args); bad[4] = 7
+    assert lib.ss_dwconv3x3_silu_fwd(*bad) == b.SS_ERR_UNSUPPORTED
+    bad = list(args); bad[2] = 0
+    assert lib.ss_dwconv3x3_silu_fwd(*bad) == b.SS_OK                  # empty: nothing to do
