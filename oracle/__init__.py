@@ -221,6 +221,64 @@ def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None,
     return out
 
 
+def multi_scan_bwd(u, delta, A, B, C, dy, orders, H=None, W=None, win=0, D=None, z=None,
+                   delta_bias=None, delta_softplus=True):
+    """Gradients of :func:`scan` with K directions of any orders for the upstream
+    gradient ``dy`` [batch, dim, L] of its output.
+
+    Direction k of the forward pass is the single-direction scan of the inputs
+    taken in k's order, u_k[s] = u[pos_k(s)] (Delta_k, B_k, C_k already in that
+    order), added into the output at pos_k(s); the gate multiplies the sum.  So
+    direction k's gradients are those of :func:`selective_scan_bwd` on its
+    permuted inputs with the upstream gradient dy_k[s] = dy[pos_k(s)] and gate
+    z_k[s] = z[pos_k(s)] -- except dz, which belongs to the sum:
+    dz = dy * s * SiLU'(z) with s the pre-gate output of all directions.  du
+    adds every direction's du_k back at its positions.  Shapes as :func:`scan`;
+    returns a dict like :func:`selective_scan_bwd`, with ddelta [batch, K, dim,
+    L], dA [K*dim, N], dB, dC [batch, K, G, N, L], dD and ddelta_bias [K*dim]."""
+    u = np.asarray(u, dtype=np.float64)
+    batch, dim, L = u.shape
+    K = len(orders)
+    if H is None and W is None:
+        H, W = 1, L
+    delta = np.asarray(delta, dtype=np.float64).reshape(batch, K, dim, L)
+    B = np.asarray(B, dtype=np.float64)
+    C = np.asarray(C, dtype=np.float64)
+    G, N = B.shape[2], B.shape[3]
+    A = np.asarray(A, dtype=np.float64).reshape(K, dim, N)
+    Dk = None if D is None else np.asarray(D, dtype=np.float64).reshape(K, dim)
+    bk = None if delta_bias is None else np.asarray(delta_bias, dtype=np.float64).reshape(K, dim)
+    dy = np.asarray(dy, dtype=np.float64)
+    zz = None if z is None else np.asarray(z, dtype=np.float64)
+    out = {"du": np.zeros_like(u), "ddelta": np.empty((batch, K, dim, L)),
+           "dA": np.empty((K * dim, N)), "dB": np.empty((batch, K, G, N, L)),
+           "dC": np.empty((batch, K, G, N, L)),
+           "dD": None if D is None else np.empty(K * dim),
+           "ddelta_bias": None if delta_bias is None else np.empty(K * dim), "dz": None}
+    for k, order in enumerate(orders):
+        pos = order_table(order, H, W, win)
+        g = selective_scan_bwd(u[..., pos], delta[:, k], A[k], B[:, k], C[:, k], dy[..., pos],
+                               D=None if Dk is None else Dk[k],
+                               z=None if zz is None else zz[..., pos],
+                               delta_bias=None if bk is None else bk[k],
+                               delta_softplus=delta_softplus)
+        out["du"][..., pos] += g["du"]
+        out["ddelta"][:, k] = g["ddelta"]
+        out["dA"][k * dim:(k + 1) * dim] = g["dA"]
+        out["dB"][:, k] = g["dB"]
+        out["dC"][:, k] = g["dC"]
+        if D is not None:
+            out["dD"][k * dim:(k + 1) * dim] = g["dD"]
+        if delta_bias is not None:
+            out["ddelta_bias"][k * dim:(k + 1) * dim] = g["ddelta_bias"]
+    if zz is not None:
+        s_total, _ = scan(u, delta, A.reshape(K * dim, N), B, C, D, None, delta_bias,
+                          delta_softplus, orders, H=H, W=W, win=win)
+        sg = 1.0 / (1.0 + np.exp(-zz))
+        out["dz"] = dy * s_total * sg * (1.0 + zz * (1.0 - sg))
+    return out
+
+
 def conv_silu(x, w, bias=None, x0=None):
     """The Mamba block's Conv1D -> SiLU before the scan: x [batch, dim, L],
     w [dim, KW], bias [dim], x0 [batch, dim, KW-1] (inputs before the

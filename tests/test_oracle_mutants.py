@@ -87,6 +87,14 @@ class _Variant:
         finally:
             _oracle._load = real
 
+    def multi_scan_bwd(self, *a, **k):
+        real = _oracle._load
+        _oracle._load = lambda: self.lib
+        try:
+            return _oracle.multi_scan_bwd(*a, **k)
+        finally:
+            _oracle._load = real
+
     def conv_silu(self, x, w, bias=None, x0=None):
         x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
         batch, dim, L = x.shape

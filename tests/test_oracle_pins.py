@@ -536,3 +536,50 @@ def test_dwconv_separable_kernel(oracle):
     rows = np.stack([np.convolve(row, c[::-1], mode="same") for row in x[0, 0]])
     both = np.stack([np.convolve(col, a[::-1], mode="same") for col in rows.T]).T
     np.testing.assert_allclose(got[0, 0], _silu(both), rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("orders_name,H,W,win", [("bidir", 1, 7, 0), ("ss2d", 3, 4, 0),
+                                                 ("windowed", 4, 5, 2)])
+def test_multi_direction_backward_matches_finite_differences(oracle, orders_name, H, W, win):
+    """Every gradient of the multi-direction backward pass against central finite
+    differences of the multi-direction forward scan (loss sum(dy * out)): Vim's
+    two directions, SS2D's four, and four windowed ones on a cut-short map."""
+    orders = {"bidir": (oracle.ORDER_FWD, oracle.ORDER_REV), "ss2d": oracle.SS2D_ORDERS,
+              "windowed": (oracle.ORDER_WIN, oracle.ORDER_WIN_REV, oracle.ORDER_WIN_COL,
+                           oracle.ORDER_WIN_COL_REV)}[orders_name]
+    K, L = len(orders), H * W
+    rng = np.random.default_rng(61 + K)
+    batch, dim, N, G = 1, 2, 2, 1
+    args = dict(u=rng.standard_normal((batch, dim, L)),
+                delta=rng.standard_normal((batch, K, dim, L)) * 0.5,
+                A=-np.exp(rng.standard_normal((K * dim, N)) * 0.5),
+                B=rng.standard_normal((batch, K, G, N, L)),
+                C=rng.standard_normal((batch, K, G, N, L)),
+                D=rng.standard_normal(K * dim),
+                z=rng.standard_normal((batch, dim, L)),
+                delta_bias=rng.standard_normal(K * dim) * 0.5 - 0.5)
+    dy = rng.standard_normal((batch, dim, L))
+
+    def loss(a):
+        out, _ = oracle.scan(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                             a["delta_bias"], True, orders, H=H, W=W, win=win)
+        return float(np.sum(dy * out))
+
+    grads = oracle.multi_scan_bwd(args["u"], args["delta"], args["A"], args["B"], args["C"], dy,
+                                  orders, H=H, W=W, win=win, D=args["D"], z=args["z"],
+                                  delta_bias=args["delta_bias"])
+    names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "z": "dz", "delta_bias": "ddelta_bias"}
+    eps = 1e-6
+    for name, gname in names.items():
+        x = args[name]
+        fd = np.empty_like(x)
+        for idx in np.ndindex(x.shape):
+            keep = x[idx]
+            x[idx] = keep + eps
+            lp = loss(args)
+            x[idx] = keep - eps
+            lm = loss(args)
+            x[idx] = keep
+            fd[idx] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(grads[gname], fd, rtol=2e-6, atol=2e-7, err_msg=name)
