@@ -323,6 +323,40 @@ ss_status ss_multi_scan_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, in
                             void *workspace, size_t workspace_bytes, ss_stream_t stream);
 
 /*
+ * ss_multi_scan_bwd -- gradients of ss_multi_scan_fwd (Euler input matrix, zero
+ * initial states) for an upstream gradient `dout` [batch, dim, H, W] of out.
+ * Direction k's gradients are those of the single-direction scan of its inputs
+ * taken in its order (ss_selective_scan_bwd), with dout and z read at the
+ * positions it visits; du sums the directions back by position, and dz uses the
+ * sum of all directions' outputs before the gate.  Inputs as ss_multi_scan_fwd.
+ * Outputs, overwritten (the summed ones zeroed on `stream` first, then fp32
+ * atomic adds):
+ *   du, dz      [batch, dim, H, W]              io (dz iff z given, else NULL)
+ *   ddelta      [batch, ndirs, dim, H*W]        io, each direction in its scan order
+ *   dA          [ndirs*dim, dstate]             float
+ *   dB, dC      [batch, ndirs, ngroups, dstate, H*W] float, in each direction's scan order
+ *   dD, ddelta_bias [ndirs*dim]                 float, nullable
+ * workspace: ss_multi_scan_bwd_workspace_bytes(batch, dim, H, W, dstate, ndirs)
+ * bytes, 16-byte aligned.  Rows must be 16-byte aligned (H*W * element size % 16
+ * == 0), else SS_ERR_UNSUPPORTED.  No output may overlap an input, another output
+ * or the workspace.  With a gate, one forward pass without it computes the
+ * output sum dz needs; each direction is then one launch of the backward kernel,
+ * and one more sums du by position.
+ */
+ss_status ss_multi_scan_bwd(int64_t batch, int64_t dim, int64_t H, int64_t W, int ndirs,
+                            const int *orders, int window, int dstate, int ngroups, ss_dtype io,
+                            const void *u, const void *delta, const float *A, const void *B,
+                            const void *C, const float *D, const float *delta_bias,
+                            int delta_softplus, const void *z, const void *dout, void *du,
+                            void *ddelta, float *dA, float *dB, float *dC, float *dD, void *dz,
+                            float *ddelta_bias, void *workspace, size_t workspace_bytes,
+                            ss_stream_t stream);
+
+/* Workspace of ss_multi_scan_bwd (0 for an invalid shape). */
+size_t ss_multi_scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t H, int64_t W,
+                                         int dstate, int ndirs);
+
+/*
  * ss_dwconv3x3_silu_fwd -- the input branch of VMamba's SS2D block ("Mamba Series
  * ...", VSS block structure and SS2Dv0.forwardv0: DWConv 3x3 -> SiLU -> SS2D):
  *     u[b,d,r,c] = SiLU(bias[d] + sum_{i,j=-1..1} w[d,i+1,j+1] * x[b,d,r+i,c+j])

@@ -211,6 +211,49 @@ from ._binding import (SS_DIR_COL as DIR_COL, SS_DIR_COL_REV as DIR_COL_REV,  # 
                        SS_DIR_WIN_COL_REV as DIR_WIN_COL_REV, SS_DIR_WIN_REV as DIR_WIN_REV)
 
 
+def multi_scan_bwd(u, delta, A, B, C, dout, orders, window=0, D=None, delta_bias=None,
+                   delta_softplus=True, z=None, workspace=None, stream=None):
+    """Gradients of :func:`multi_scan_fwd` for the upstream gradient ``dout``
+    [batch, dim, H, W].  Returns a dict: du, dz (None without z) [batch, dim, H,
+    W] and ddelta [batch, K, dim, H*W] in the I/O dtype; dA [K*dim, N], dB, dC
+    [batch, K, G, N, H*W], dD and ddelta_bias [K*dim] (None when not given) in
+    float32."""
+    torch = _torch()
+    lib = _b.load()
+    batch, dim, H, W = u.shape
+    K = len(orders)
+    G, N = B.shape[2], B.shape[3]
+    L = H * W
+    io, dev = u.dtype, u.device
+    _check_io("u", u, io, dev)
+    _check_io("z", z, io, dev, (batch, dim, H, W))
+    _check_io("dout", dout, io, dev, (batch, dim, H, W))
+    _check_io("delta", delta, io, dev, (batch, K, dim, L))
+    _check_io("B", B, io, dev, (batch, K, G, N, L))
+    _check_io("C", C, io, dev, (batch, K, G, N, L))
+    _check_io("A", A, torch.float32, dev, (K * dim, N))
+    _check_io("D", D, torch.float32, dev, (K * dim,))
+    _check_io("delta_bias", delta_bias, torch.float32, dev, (K * dim,))
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = {"du": torch.empty_like(u), "ddelta": torch.empty_like(delta),
+         "dz": torch.empty_like(u) if z is not None else None,
+         "dA": torch.empty(K * dim, N, **f32), "dB": torch.empty(batch, K, G, N, L, **f32),
+         "dC": torch.empty(batch, K, G, N, L, **f32),
+         "dD": torch.empty(K * dim, **f32) if D is not None else None,
+         "ddelta_bias": torch.empty(K * dim, **f32) if delta_bias is not None else None}
+    wsb = int(lib.ss_multi_scan_bwd_workspace_bytes(batch, dim, H, W, N, K))
+    if wsb and (workspace is None or workspace.numel() < wsb):
+        workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    ords = (ctypes.c_int * K)(*[int(o) for o in orders])
+    _b.check(lib.ss_multi_scan_bwd(
+        batch, dim, H, W, K, ords, int(window), N, G, _io_code(u), _ptr(u), _ptr(delta), _ptr(A),
+        _ptr(B), _ptr(C), _ptr(D), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(z), _ptr(dout),
+        _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
+        _ptr(g["dz"]), _ptr(g["ddelta_bias"]), _ptr(workspace) if wsb else None,
+        workspace.numel() if wsb else 0, _stream(stream, dev)))
+    return g
+
+
 def dwconv3x3_silu(x, w, bias=None, out=None, stream=None):
     """SS2D's input branch: depthwise 3 x 3 convolution (zero padding) + bias, then
     SiLU.  x [batch, dim, H, W] (bf16 or f32); w [dim, 3, 3] and bias [dim]

@@ -39,7 +39,7 @@ EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_opts", "ss_bidir_scan
            "ss_debug_set_wait_budget_ns", "ss_debug_set_flags",
            "ss_selective_scan_fwd_noalloc", "ss_selective_state_update",
            "ss_selective_scan_bwd", "ss_multi_scan_fwd", "ss_multi_scan_workspace_bytes",
-           "ss_dwconv3x3_silu_fwd")
+           "ss_dwconv3x3_silu_fwd", "ss_multi_scan_bwd", "ss_multi_scan_bwd_workspace_bytes")
 
 
 class SSError(RuntimeError):
@@ -92,6 +92,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         # workspace_bytes, stream
         lib.ss_multi_scan_fwd.argtypes = [i64, i64, i64, i64, i32, ctypes.POINTER(i32), i32, i32,
                                           i32, i32] + [vp] * 7 + [i32, vp, vp, vp, vp, sz, vp]
+        # batch, dim, H, W, ndirs, orders, window, dstate, ngroups, io, u, delta, A, B, C, D,
+        # delta_bias, delta_softplus, z, dout, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias,
+        # workspace, workspace_bytes, stream
+        lib.ss_multi_scan_bwd.argtypes = ([i64, i64, i64, i64, i32, ctypes.POINTER(i32), i32, i32, i32,
+                                           i32] + [vp] * 7 + [i32] + [vp] * 10 + [vp, sz, vp])
+        lib.ss_multi_scan_bwd.restype = ctypes.c_int
+        lib.ss_multi_scan_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64, i32, i32]
+        lib.ss_multi_scan_bwd_workspace_bytes.restype = sz
         lib.ss_dwconv3x3_silu_fwd.argtypes = [i64, i64, i64, i64, i32, vp, vp, vp, vp, vp]
         lib.ss_dwconv3x3_silu_fwd.restype = ctypes.c_int
         lib.ss_multi_scan_workspace_bytes.argtypes = [i64, i64, i64, i64, i32]

@@ -212,7 +212,7 @@ ss_status check_bwd(const char *fn, int64_t batch, int64_t dim, int64_t L, int N
                     const void *C, const float *D, const void *z, const float *bias,
                     const void *dout, const void *du, const void *ddelta, const float *dA,
                     const float *dB, const float *dC, const float *dD, const void *dz,
-                    const float *dbias, const void *ws, size_t ws_bytes) {
+                    const float *dbias, const void *ws, size_t ws_bytes, int K = 1) {
     if (!dout || !du || !ddelta || !dA || !dB || !dC)
         return fail(SS_ERR_INVALID_ARG, "%s: dout, du, ddelta, dA, dB and dC are required", fn);
     if (z && !dz) return fail(SS_ERR_INVALID_ARG, "%s: dz is required when z is given", fn);
@@ -226,24 +226,25 @@ ss_status check_bwd(const char *fn, int64_t batch, int64_t dim, int64_t L, int N
         return fail(SS_ERR_UNSUPPORTED,
                     "%s: rows must be 16-byte aligned (seqlen * element size %% 16 == 0)", fn);
     const int64_t nel = batch * dim * L;
-    const int64_t nbc = batch * G * N * L;
+    const int64_t nbc = batch * K * G * N * L;
+    const int64_t kd = (int64_t)K * dim;
     const Span outs[] = {{static_cast<const char *>(du), nel * es},
-                         {static_cast<const char *>(ddelta), nel * es},
+                         {static_cast<const char *>(ddelta), nel * K * es},
                          {static_cast<const char *>(dz), dz ? nel * es : 0},
-                         {reinterpret_cast<const char *>(dA), dim * N * 4},
+                         {reinterpret_cast<const char *>(dA), kd * N * 4},
                          {reinterpret_cast<const char *>(dB), nbc * 4},
                          {reinterpret_cast<const char *>(dC), nbc * 4},
-                         {reinterpret_cast<const char *>(dD), dD ? dim * 4 : 0},
-                         {reinterpret_cast<const char *>(dbias), dbias ? dim * 4 : 0},
+                         {reinterpret_cast<const char *>(dD), dD ? kd * 4 : 0},
+                         {reinterpret_cast<const char *>(dbias), dbias ? kd * 4 : 0},
                          {static_cast<const char *>(ws), ws ? (int64_t)ws_bytes : 0}};
     const Span ins[] = {{static_cast<const char *>(u), nel * es},
-                        {static_cast<const char *>(delta), nel * es},
-                        {reinterpret_cast<const char *>(A), dim * N * 4},
+                        {static_cast<const char *>(delta), nel * K * es},
+                        {reinterpret_cast<const char *>(A), kd * N * 4},
                         {static_cast<const char *>(B), nbc * es},
                         {static_cast<const char *>(C), nbc * es},
-                        {reinterpret_cast<const char *>(D), D ? dim * 4 : 0},
+                        {reinterpret_cast<const char *>(D), D ? kd * 4 : 0},
                         {static_cast<const char *>(z), z ? nel * es : 0},
-                        {reinterpret_cast<const char *>(bias), bias ? dim * 4 : 0},
+                        {reinterpret_cast<const char *>(bias), bias ? kd * 4 : 0},
                         {static_cast<const char *>(dout), nel * es}};
     const int nout = sizeof(outs) / sizeof(outs[0]);
     for (int i = 0; i < nout; ++i) {
@@ -471,6 +472,71 @@ ss_status ss_multi_scan_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, in
     if ((st = check_workspace(fn, steps_workspace_bytes(a), workspace, workspace_bytes))) return st;
     if ((st = check_ws_overlap(fn, a))) return st;
     return launch_steps(a);
+}
+
+ss_status ss_multi_scan_bwd(int64_t batch, int64_t dim, int64_t H, int64_t W, int ndirs,
+                            const int *orders, int window, int dstate, int ngroups, ss_dtype io,
+                            const void *u, const void *delta, const float *A, const void *B,
+                            const void *C, const float *D, const float *delta_bias,
+                            int delta_softplus, const void *z, const void *dout, void *du,
+                            void *ddelta, float *dA, float *dB, float *dC, float *dD, void *dz,
+                            float *ddelta_bias, void *workspace, size_t workspace_bytes,
+                            ss_stream_t stream) {
+    static const char *fn = "ss_multi_scan_bwd";
+    if (H < 0 || W < 0) return fail(SS_ERR_INVALID_ARG, "%s: negative map size", fn);
+    if (H >= (1ll << 31) || W >= (1ll << 31) || (H > 0 && W > (INT64_MAX / H)))
+        return fail(SS_ERR_UNSUPPORTED, "%s: map too large", fn);
+    if (ndirs < 1 || ndirs > 8)
+        return fail(SS_ERR_INVALID_ARG, "%s: ndirs %d is not in 1..8", fn, ndirs);
+    if (!orders) return fail(SS_ERR_INVALID_ARG, "%s: orders is required", fn);
+    bool windowed = false;
+    for (int k = 0; k < ndirs; ++k) {
+        if (orders[k] < SS_DIR_ROW || orders[k] > SS_DIR_WIN_COL_REV)
+            return fail(SS_ERR_INVALID_ARG, "%s: orders[%d] = %d is not an SS_DIR_* code", fn, k,
+                        orders[k]);
+        windowed = windowed || orders[k] >= SS_DIR_WIN;
+    }
+    if (windowed && window < 1)
+        return fail(SS_ERR_INVALID_ARG, "%s: a windowed order needs window >= 1", fn);
+    bool empty = false;
+    ss_status st = check_common(fn, batch, dim, H * W, dstate, ngroups, io, ndirs, u, delta, A, B,
+                                C, D, z, delta_bias, du, nullptr, &empty);
+    if (st != SS_OK) return st;
+    BwdArgs a;
+    a.f = scan_args(batch, dim, H * W, dstate, ngroups, io, u, delta, A, B, C, D, z, delta_bias,
+                    delta_softplus, nullptr, nullptr, nullptr, 0, stream);
+    a.f.K = ndirs;
+    a.f.H = H;
+    a.f.W = W;
+    for (int k = 0; k < ndirs; ++k) a.f.orders[k] = orders[k];
+    const int64_t big = H > W ? H : W;
+    a.f.win = windowed ? (int)(window < big ? window : big) : 1;
+    a.dout = dout;
+    a.du = du;
+    a.ddelta = ddelta;
+    a.dz = dz;
+    a.dA = dA;
+    a.dB = dB;
+    a.dC = dC;
+    a.dD = dD;
+    a.dbias = ddelta_bias;
+    a.ws = workspace;
+    a.ws_bytes = workspace_bytes;
+    if (empty) return launch_multi_bwd(a, true);
+    if ((st = check_bwd(fn, batch, dim, H * W, dstate, ngroups, io, u, delta, A, B, C, D, z,
+                        delta_bias, dout, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias, workspace,
+                        workspace_bytes, ndirs)))
+        return st;
+    if ((st = check_workspace(fn, multi_bwd_workspace_bytes(batch, dim, H * W, dstate, ndirs),
+                              workspace, workspace_bytes)))
+        return st;
+    return launch_multi_bwd(a, false);
+}
+
+size_t ss_multi_scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t H, int64_t W,
+                                         int dstate, int ndirs) {
+    if (H <= 0 || W <= 0 || ndirs < 1 || ndirs > 8 || !valid_dstate(dstate)) return 0;
+    return multi_bwd_workspace_bytes(batch, dim, H * W, dstate, ndirs);
 }
 
 ss_status ss_dwconv3x3_silu_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, ss_dtype io,

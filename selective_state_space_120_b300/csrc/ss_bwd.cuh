@@ -109,6 +109,14 @@ struct BwdParams {
     float *dA;                // [dim, N]
     float *dB, *dC;           // [batch, G, N, L]
     float *dD, *dbias;        // [dim], nullable
+    // multi-direction calls (MULTI kernels): direction k of K, traversal `order` of
+    // an H x W map (window size win for the windowed orders).  Delta, B, C, ddelta,
+    // dB, dC are direction k's (scan order); u, z, dout are read by position from
+    // u_g, z_g, dy_g [batch, dim, L]; du goes by scan step, in fp32, to du_acc
+    // [batch*dim, L]; dz is left to the merge.
+    int K, k, order, H, W, win;
+    const void *u_g, *z_g, *dy_g;
+    float *du_acc;
 };
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
@@ -143,7 +151,7 @@ __device__ __forceinline__ void reduce_bc_store(float (&v)[V], int q, int g, flo
     }
 }
 
-template <class C>
+template <class C, bool MULTI = false>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
 k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
            const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dy,
@@ -163,8 +171,15 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
     const int b = bg / p.G, grp = bg % p.G;
     const int64_t L = p.L;
     const int64_t row0 = (int64_t)b * p.dim + (int64_t)grp * p.dpg;  // the group's channel 0
-    const int row_tma = (int)(row0 + (int64_t)cblk * C::CB);
-    const int bcrow_tma = (int)(((int64_t)b * p.G + grp) * N);
+    const int row_tma = (int)(row0 + (int64_t)cblk * C::CB);          // u, z, dout rows
+    const int Kd = MULTI ? p.K : 1, kdir = MULTI ? p.k : 0;           // directions, this one
+    const int order = MULTI ? p.order : 0;
+    const bool u_tiled = order == 0 || order == 2;  // u, z, dout as tiles (else gathered)
+    // Delta / ddelta rows [batch, K, dim]; B/C rows [batch, K, G, N]
+    const int64_t dlrow0 = ((int64_t)b * Kd + kdir) * p.dim + (int64_t)grp * p.dpg;
+    const int dlrow_tma = (int)(dlrow0 + (int64_t)cblk * C::CB);
+    const int bcrow_tma = (int)((((int64_t)b * Kd + kdir) * p.G + grp) * N);
+    const int64_t poff = (int64_t)kdir * p.dim;  // direction offset of A, D, bias and their gradients
     const int nt = (int)((L + T - 1) / T);
     const int nq = 2 * nt;  // ring order: pass F tiles 0..nt-1, then pass B tiles nt-1..0
 
@@ -186,13 +201,13 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
 #pragma unroll
         for (int k = 0; k < NP; ++k) {
             const int j0 = 2 * k, j1 = 2 * k + 1;
-            const float a0 = __ldg(p.A + dch[c] * N + g * NPT + j0) * kLog2e;
-            const float a1 = j1 < NPT ? __ldg(p.A + dch[c] * N + g * NPT + j1) * kLog2e : 0.f;
+            const float a0 = __ldg(p.A + (poff + dch[c]) * N + g * NPT + j0) * kLog2e;
+            const float a1 = j1 < NPT ? __ldg(p.A + (poff + dch[c]) * N + g * NPT + j1) * kLog2e : 0.f;
             A2[c][k] = make_float2(a0, a1);
             carry[c][k] = make_float2(0.f, 0.f);
             dA[c][k] = make_float2(0.f, 0.f);
         }
-        Dd[c] = p.D ? __ldg(p.D + dch[c]) : 0.f;
+        Dd[c] = p.D ? __ldg(p.D + poff + dch[c]) : 0.f;
         dD_acc[c] = 0.f;
         dbias_acc[c] = 0.f;
         ck[c] = p.ckpt + ((int64_t)b * p.dim + dch[c]) * p.nblk * N + g * NPT;
@@ -208,14 +223,17 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
     const int pdg = cblk * C::CB + pch;
     const bool pvalid = pdg < p.dpg;
     const int64_t pd = (int64_t)grp * p.dpg + (pvalid ? pdg : p.dpg - 1);
-    const float pbias = p.bias ? __ldg(p.bias + pd) : 0.f;
+    const float pbias = p.bias ? __ldg(p.bias + poff + pd) : 0.f;
+    const int64_t prow = (int64_t)b * p.dim + pd;  // the prep channel's row of u, z, dout
     float4 *q0row = reinterpret_cast<float4 *>(smem + C::OFF_P0 + C::prow(pch) * C::P0ROW);
     float2 *q1row = reinterpret_cast<float2 *>(smem + C::OFF_P1 + C::prow(pch) * C::P1ROW);
 
     const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
     const uint32_t smem0 = smem_u32(smem);
-    const uint32_t txF = 2u * C::CB * 64u + N * 64u;
-    const uint32_t txB = (3u + (p.has_z ? 1u : 0u)) * C::CB * 64u + 2u * N * 64u;
+    const uint32_t nuF = u_tiled ? 1u : 0u;                              // u
+    const uint32_t nuB = u_tiled ? (2u + (p.has_z ? 1u : 0u)) : 0u;     // u, dout, z
+    const uint32_t txF = (nuF + 1u) * C::CB * 64u + N * 64u;
+    const uint32_t txB = (nuB + 1u) * C::CB * 64u + 2u * N * 64u;
     const uint64_t budget = g_wait_budget_ns;
 
     if (tid == 0) {
@@ -246,13 +264,18 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
         const uint32_t st = smem0 + s * C::STAGE;
         const bool bwd = qs >= nt;
         const int x = tile_of(qs) * T;
+        // u, z, dout of a reversed row order: positions L-(i+1)T .. L-1-iT (the
+        // last tile may start below 0; the copy fills zeros there)
+        const int xu = order == 2 ? (int)(L - (int64_t)(tile_of(qs) + 1) * T) : x;
         mbar_expect_tx(bar, bwd ? txB : txF);
-        tma_load_2d(st + C::OFF_U, &tm_u, x, row_tma, bar);
-        tma_load_2d(st + C::OFF_DL, &tm_dl, x, row_tma, bar);
+        if (u_tiled) tma_load_2d(st + C::OFF_U, &tm_u, xu, row_tma, bar);
+        tma_load_2d(st + C::OFF_DL, &tm_dl, x, dlrow_tma, bar);
         tma_load_2d(st + C::OFF_B, &tm_B, x, bcrow_tma, bar);
         if (bwd) {
-            tma_load_2d(st + C::OFF_DY, &tm_dy, x, row_tma, bar);
-            if (p.has_z) tma_load_2d(st + C::OFF_Z, &tm_z, x, row_tma, bar);
+            if (u_tiled) {
+                tma_load_2d(st + C::OFF_DY, &tm_dy, xu, row_tma, bar);
+                if (p.has_z) tma_load_2d(st + C::OFF_Z, &tm_z, xu, row_tma, bar);
+            }
             tma_load_2d(st + C::OFF_C, &tm_C, x, bcrow_tma, bar);
         }
     };
@@ -278,14 +301,49 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
             for (int e = 0; e < VPC; ++e) bcf[(qq * VPC + e) * 2 * NB + arr * NB + n] = v[e];
         }
         const int64_t tb0 = (int64_t)i * T;
+        OrderWalk ow;  // the other orders: positions of this thread's steps
+        if (MULTI && !u_tiled) ow.start(order, p.H, p.W, p.win, L, tb0 + pt0);
 #pragma unroll
         for (int e0 = 0; e0 < E; e0 += EP) {
             float uu[EP], dd[EP], zz[EP], gy[EP];
-            load_tile_row<IO, EP>(st + C::OFF_U, pch, pt0 + e0, uu);
             load_tile_row<IO, EP>(st + C::OFF_DL, pch, pt0 + e0, dd);
-            if (bwd) {
-                load_tile_row<IO, EP>(st + C::OFF_DY, pch, pt0 + e0, gy);
-                if (p.has_z) load_tile_row<IO, EP>(st + C::OFF_Z, pch, pt0 + e0, zz);
+            if (!MULTI || order == 0) {
+                load_tile_row<IO, EP>(st + C::OFF_U, pch, pt0 + e0, uu);
+                if (bwd) {
+                    load_tile_row<IO, EP>(st + C::OFF_DY, pch, pt0 + e0, gy);
+                    if (p.has_z) load_tile_row<IO, EP>(st + C::OFF_Z, pch, pt0 + e0, zz);
+                }
+            } else if (order == 2) {
+                // reversed tile: step pt0+e0+e sits at tile column T-1-(pt0+e0+e)
+                float tmp[EP];
+                const int col = T - (pt0 + e0) - EP;
+                load_tile_row<IO, EP>(st + C::OFF_U, pch, col, tmp);
+#pragma unroll
+                for (int e = 0; e < EP; ++e) uu[e] = tmp[EP - 1 - e];
+                if (bwd) {
+                    load_tile_row<IO, EP>(st + C::OFF_DY, pch, col, tmp);
+#pragma unroll
+                    for (int e = 0; e < EP; ++e) gy[e] = tmp[EP - 1 - e];
+                    if (p.has_z) {
+                        load_tile_row<IO, EP>(st + C::OFF_Z, pch, col, tmp);
+#pragma unroll
+                        for (int e = 0; e < EP; ++e) zz[e] = tmp[EP - 1 - e];
+                    }
+                }
+            } else {
+                const IO *ur = reinterpret_cast<const IO *>(p.u_g) + prow * L;
+                const IO *yr = reinterpret_cast<const IO *>(p.dy_g) + prow * L;
+                const IO *zr = reinterpret_cast<const IO *>(p.z_g) + prow * L;
+#pragma unroll
+                for (int e = 0; e < EP; ++e) {
+                    const bool inr = tb0 + pt0 + e0 + e < L;
+                    const int64_t pos = ow.pos_next();
+                    uu[e] = inr ? IOT<IO>::load(ur + pos) : 0.f;
+                    if (bwd) {
+                        gy[e] = inr ? IOT<IO>::load(yr + pos) : 0.f;
+                        zz[e] = (inr && p.has_z) ? IOT<IO>::load(zr + pos) : 0.f;
+                    }
+                }
             }
 #pragma unroll
             for (int e = 0; e < EP; ++e) {
@@ -526,9 +584,16 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
                     dD_acc[c] = fmaf(pp.z, q1.x, dD_acc[c]);
                     dbias_acc[c] += ddelta;
                     IO *ob = reinterpret_cast<IO *>(smem + C::OFF_OB + chs[c] * C::OBROW);
-                    ob[tl] = IOT<IO>::from_f(fmaf(pp.z, Dd[c], pp.x * P2s));        // du
+                    const float du = fmaf(pp.z, Dd[c], pp.x * P2s);
+                    if constexpr (MULTI) {
+                        // this direction's du by scan step; the merge sums by position
+                        const int64_t t = (int64_t)i * T + tl;
+                        if (valid[c] && t < L) p.du_acc[((int64_t)b * p.dim + dch[c]) * L + t] = du;
+                    } else {
+                        ob[tl] = IOT<IO>::from_f(du);
+                    }
                     ob[C::CB * C::OBROW / C::ES + tl] = IOT<IO>::from_f(ddelta);
-                    if (p.has_z)                                                    // dz
+                    if (!MULTI && p.has_z)                                          // dz
                         ob[2 * C::CB * C::OBROW / C::ES + tl] =
                             IOT<IO>::from_f(fmaf(Dd[c], q1.x, sv[c][rb]) * q1.y);
                 }
@@ -555,7 +620,8 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
                     const int64_t t = (int64_t)k * TS + 4 * t4;
                     float *dBC = arr ? p.dC : p.dB;
                     if (t < L)
-                        atomicAdd(reinterpret_cast<float4 *>(dBC + (((int64_t)b * p.G + grp) * N + n) * L + t),
+                        atomicAdd(reinterpret_cast<float4 *>(
+                                      dBC + ((((int64_t)b * Kd + kdir) * p.G + grp) * N + n) * L + t),
                                   acc);
                 }
             }
@@ -566,10 +632,11 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
         __syncwarp();
         {
             constexpr int VPC = 16 / C::ES;
-            const int narr = p.has_z ? 3 : 2;
+            // single direction: du, ddelta (and dz); multi-direction: ddelta only
+            const int narr = MULTI ? 1 : (p.has_z ? 3 : 2);
 #pragma unroll 1
             for (int kk = lane; kk < narr * C::CHW * 4; kk += 32) {
-                const int arr = kk / (C::CHW * 4);
+                const int arr = MULTI ? 1 : kk / (C::CHW * 4);
                 const int rem = kk % (C::CHW * 4);
                 const int rr = rem >> 2, qq = rem & 3;
                 const int chr = warp * C::CHW + rr;
@@ -579,7 +646,8 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
                     const uint4 v = *reinterpret_cast<const uint4 *>(
                         smem + C::OFF_OB + (arr * C::CB + chr) * C::OBROW + qq * 16);
                     void *base = arr == 0 ? p.du : (arr == 1 ? p.ddelta : p.dz);
-                    *reinterpret_cast<uint4 *>(reinterpret_cast<IO *>(base) + (row0 + dgr) * L + t) = v;
+                    const int64_t orow = (arr == 1 ? dlrow0 : row0) + dgr;  // ddelta: direction k's row
+                    *reinterpret_cast<uint4 *>(reinterpret_cast<IO *>(base) + orow * L + t) = v;
                 }
             }
         }
@@ -597,12 +665,49 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
         if (!valid[c]) continue;
 #pragma unroll
         for (int kk = 0; kk < NP; ++kk) {
-            atomicAdd(p.dA + dch[c] * N + g * NPT + 2 * kk, dA[c][kk].x);
-            if (2 * kk + 1 < NPT) atomicAdd(p.dA + dch[c] * N + g * NPT + 2 * kk + 1, dA[c][kk].y);
+            atomicAdd(p.dA + (poff + dch[c]) * N + g * NPT + 2 * kk, dA[c][kk].x);
+            if (2 * kk + 1 < NPT) atomicAdd(p.dA + (poff + dch[c]) * N + g * NPT + 2 * kk + 1, dA[c][kk].y);
         }
         if (g == 0) {
-            if (p.dD) atomicAdd(p.dD + dch[c], dD_acc[c]);
-            if (p.dbias) atomicAdd(p.dbias + dch[c], dbias_acc[c]);
+            if (p.dD) atomicAdd(p.dD + poff + dch[c], dD_acc[c]);
+            if (p.dbias) atomicAdd(p.dbias + poff + dch[c], dbias_acc[c]);
+        }
+    }
+}
+
+// Merge of a multi-direction backward pass: du[p] = sum_k du_k[step_k(p)] (each
+// direction's du was stored by scan step) and, with a gate, dz[p] = dout[p] *
+// s[p] * SiLU'(z[p]), s being the sum of all directions' pre-gate outputs.  A
+// thread owns one position (the traversals are the same for every row) and
+// walks rows blockIdx.y, blockIdx.y + gridDim.y, ...
+struct BwdOrderSet {
+    int K, H, W, win;
+    int orders[8];
+};
+template <typename IO>
+__global__ void __launch_bounds__(256)
+k_merge_bwd(const float *__restrict__ du_acc, int64_t rows, const BwdOrderSet os,
+            const IO *__restrict__ dout, const IO *__restrict__ z, const IO *__restrict__ s,
+            IO *__restrict__ du, IO *__restrict__ dz) {
+    const int64_t L = (int64_t)os.H * os.W;
+    const int pos = blockIdx.x * blockDim.x + threadIdx.x;
+    if (pos >= L) return;
+    const int r = pos / os.W, c = pos - r * os.W;
+    uint32_t st[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) st[k] = k < os.K ? step_of(os.orders[k], r, c, os.H, os.W, os.win) : 0u;
+    for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
+        float g = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (k < os.K) g += du_acc[((int64_t)k * rows + row) * L + st[k]];
+        const int64_t i = row * L + pos;
+        du[i] = IOT<IO>::from_f(g);
+        if (z) {
+            const float zz = IOT<IO>::load(z + i);
+            const float sg = rcp(1.f + ex2(-zz * kLog2e));
+            dz[i] = IOT<IO>::from_f(IOT<IO>::load(dout + i) * IOT<IO>::load(s + i) * sg *
+                                    fmaf(zz, 1.f - sg, 1.f));
         }
     }
 }

@@ -339,6 +339,54 @@ __device__ __forceinline__ uint32_t step_of(int order, int r, int c, int H, int 
     }
 }
 
+// Positions of consecutive scan steps of a direction with a column order (1, 3)
+// or a windowed one (4..7), one step at a time: start() places it at step s (a
+// step past the end is treated as the last), pos_next() returns the position of
+// the current step and moves to the next.
+struct OrderWalk {
+    int order, H, W;
+    int r, c;    // column orders: cell of the current step
+    WinWalk ww;  // windowed orders
+    __device__ __forceinline__ void start(int ord, int H_, int W_, int win, int64_t L, int64_t s) {
+        order = ord;
+        H = H_;
+        W = W_;
+        const int64_t sc = s < L ? s : L - 1;
+        if (order == 1 || order == 3) {
+            const uint32_t cm = (uint32_t)(order == 3 ? L - 1 - sc : sc);  // column-major index
+            c = (int)(cm / (uint32_t)H);
+            r = (int)(cm - (uint32_t)c * (uint32_t)H);
+        } else {
+            const bool tr = order == ORD_K_WIN_COL || order == ORD_K_WIN_COL_REV;
+            ww.Hm = tr ? W : H;
+            ww.Wm = tr ? H : W;
+            ww.w = win;
+            ww.seek((uint32_t)(order >= ORD_K_WIN_REV ? L - 1 - sc : sc));
+        }
+    }
+    __device__ __forceinline__ int64_t pos_next() {
+        int64_t p;
+        if (order == 1 || order == 3) {
+            p = (int64_t)r * W + c;
+            if (order == 1) {
+                if (++r == H) {
+                    r = 0;
+                    ++c;
+                }
+            } else if (--r < 0) {
+                r = H - 1;
+                --c;
+            }
+        } else {
+            const bool tr = order == ORD_K_WIN_COL || order == ORD_K_WIN_COL_REV;
+            p = tr ? (int64_t)ww.col() * W + ww.row() : (int64_t)ww.row() * W + ww.col();
+            if (order >= ORD_K_WIN_REV) ww.prev();
+            else ww.next();
+        }
+        return p;
+    }
+};
+
 // ------------------------------------------------------------------ lane-group reduction
 // R lanes (R a power of two) each hold R partial sums v[0..R): one
 // per step of an R-step block.  Afterwards the lane with group index g holds the

@@ -51,6 +51,13 @@ struct BwdArgs {
     size_t ws_bytes = 0;
 };
 
+// Workspace of a multi-direction backward pass: the pre-gate output sum s
+// [rows, L] (I/O type), the directions' du by scan step [K, rows, L] fp32 (also
+// the forward pass's accumulators before that), the state checkpoints.
+size_t multi_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t L, int N, int K);
+// Backward pass of directions of any order (f.K, f.orders, f.H, f.W, f.win).
+ss_status launch_multi_bwd(const BwdArgs &a, bool empty);
+
 // Direction traversal codes used by the kernels (match SS_DIR_*).
 enum { ORD_ROW = 0, ORD_COL = 1, ORD_ROW_REV = 2, ORD_COL_REV = 3, ORD_WIN = 4, ORD_WIN_COL = 5,
        ORD_WIN_REV = 6, ORD_WIN_COL_REV = 7 };

@@ -611,26 +611,39 @@ namespace {
 // workspace is sized for 8.
 constexpr int kBwdMinBlock = 8;
 
-template <class C>
-ss_status run_scan_bwd(const BwdArgs &a) {
+// MULTI: direction k of a multi-direction call (ckpt and du_acc from the
+// caller); otherwise the single direction with its checkpoints in a.ws.
+template <class C, bool MULTI = false>
+ss_status run_scan_bwd(const BwdArgs &a, int k = 0, float *ckpt = nullptr, float *du_acc = nullptr) {
     using namespace ssk;
     static_assert(C::TS >= kBwdMinBlock, "checkpoint interval");
     const ScanArgs &f = a.f;
     const int io = f.io;
     const int64_t rows = f.batch * f.dim;
-    const uint64_t bcrows = (uint64_t)f.batch * f.G * C::N;
+    const int K = MULTI ? f.K : 1;
+    const uint64_t bcrows = (uint64_t)f.batch * K * f.G * C::N;
     CUtensorMap mu, md, mz, mdy, mb, mc;
     ss_status st;
     if ((st = make_map(&mu, f.u, io, f.L, rows, C::T, C::CB))) return st;
-    if ((st = make_map(&md, f.delta, io, f.L, rows, C::T, C::CB))) return st;
+    if ((st = make_map(&md, f.delta, io, f.L, (uint64_t)rows * K, C::T, C::CB))) return st;
     if ((st = make_map(&mz, f.z ? f.z : f.u, io, f.L, rows, C::T, C::CB))) return st;
     if ((st = make_map(&mdy, a.dout, io, f.L, rows, C::T, C::CB))) return st;
     if ((st = make_map(&mb, f.B, io, f.L, bcrows, C::T, C::N))) return st;
     if ((st = make_map(&mc, f.C, io, f.L, bcrows, C::T, C::N))) return st;
-    auto kern = k_scan_bwd<C>;
+    auto kern = k_scan_bwd<C, MULTI>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
     BwdParams p{};
+    p.K = K;
+    p.k = k;
+    p.order = MULTI ? f.orders[k] : 0;
+    p.H = (int)f.H;
+    p.W = (int)f.W;
+    p.win = f.win;
+    p.u_g = f.u;
+    p.z_g = f.z;
+    p.dy_g = a.dout;
+    p.du_acc = du_acc;
     p.dim = f.dim;
     p.L = f.L;
     p.G = f.G;
@@ -641,7 +654,7 @@ ss_status run_scan_bwd(const BwdArgs &a) {
     p.bias = f.bias;
     p.softplus = f.softplus;
     p.has_z = f.z != nullptr;
-    p.ckpt = reinterpret_cast<float *>(a.ws);
+    p.ckpt = MULTI ? ckpt : reinterpret_cast<float *>(a.ws);
     p.du = a.du;
     p.ddelta = a.ddelta;
     p.dz = a.dz;
@@ -657,21 +670,21 @@ ss_status run_scan_bwd(const BwdArgs &a) {
     return check_launch("scan backward");
 }
 
-template <typename IO>
-ss_status dispatch_bwd(const BwdArgs &a) {
+template <typename IO, bool MULTI = false>
+ss_status dispatch_bwd(const BwdArgs &a, int k = 0, float *ckpt = nullptr, float *du_acc = nullptr) {
     using namespace ssk;
     // CfgB<IO, N, warps per CTA, channels per lane, states per lane, steps per
     // block, CTAs per SM for the register budget>
     // float32 I/O has twice the prep registers: a budget of two CTAs per SM
     constexpr int MB = sizeof(IO) == 2 ? 3 : 2;
     switch (a.f.N) {
-    case 1: return run_scan_bwd<CfgB<IO, 1, 2, 1, 4, 16, 2>>(a);
-    case 2: return run_scan_bwd<CfgB<IO, 2, 2, 1, 4, 16, 2>>(a);
-    case 4: return run_scan_bwd<CfgB<IO, 4, 2, 1, 4, 16, 2>>(a);
-    case 8: return run_scan_bwd<CfgB<IO, 8, 2, 1, 4, 16, MB>>(a);
-    case 16: return run_scan_bwd<CfgB<IO, 16, 4, 1, 4, 16, MB>>(a);
-    case 32: return run_scan_bwd<CfgB<IO, 32, 4, 1, 4, 16, MB>>(a);
-    case 64: return run_scan_bwd<CfgB<IO, 64, 4, 1, 4, 16, 2>>(a);
+    case 1: return run_scan_bwd<CfgB<IO, 1, 2, 1, 4, 16, 2>, MULTI>(a, k, ckpt, du_acc);
+    case 2: return run_scan_bwd<CfgB<IO, 2, 2, 1, 4, 16, 2>, MULTI>(a, k, ckpt, du_acc);
+    case 4: return run_scan_bwd<CfgB<IO, 4, 2, 1, 4, 16, 2>, MULTI>(a, k, ckpt, du_acc);
+    case 8: return run_scan_bwd<CfgB<IO, 8, 2, 1, 4, 16, MB>, MULTI>(a, k, ckpt, du_acc);
+    case 16: return run_scan_bwd<CfgB<IO, 16, 4, 1, 4, 16, MB>, MULTI>(a, k, ckpt, du_acc);
+    case 32: return run_scan_bwd<CfgB<IO, 32, 4, 1, 4, 16, MB>, MULTI>(a, k, ckpt, du_acc);
+    case 64: return run_scan_bwd<CfgB<IO, 64, 4, 1, 4, 16, 2>, MULTI>(a, k, ckpt, du_acc);
     default: return fail(SS_ERR_UNSUPPORTED, "dstate %d is not one of 1,2,4,8,16,32,64", a.f.N);
     }
 }
@@ -736,6 +749,74 @@ ss_status launch_dwconv3x3(int64_t batch, int64_t dim, int64_t H, int64_t W, int
                                                              reinterpret_cast<float *>(u), planes,
                                                              (int)dim, (int)H, (int)W);
     return check_launch("dwconv3x3");
+}
+
+namespace {
+size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+}  // namespace
+
+size_t multi_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t L, int N, int K) {
+    if (batch <= 0 || dim <= 0 || L <= 0 || N <= 0 || K <= 0) return 0;
+    const size_t rows = (size_t)batch * dim;
+    return align256(rows * L * 4) + align256((size_t)K * rows * L * 4) +
+           rows * ((L + kBwdMinBlock - 1) / kBwdMinBlock) * N * sizeof(float);
+}
+
+ss_status launch_multi_bwd(const BwdArgs &a, bool empty) {
+    using namespace ssk;
+    const ScanArgs &f = a.f;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(f.stream);
+    const int K = f.K;
+    const size_t bc = (size_t)f.batch * K * f.G * f.N * f.L * sizeof(float);
+    ss_status st;
+    if ((st = zero_async(a.dA, (size_t)K * f.dim * f.N * sizeof(float), s))) return st;
+    if ((st = zero_async(a.dB, bc, s))) return st;
+    if ((st = zero_async(a.dC, bc, s))) return st;
+    if ((st = zero_async(a.dD, (size_t)K * f.dim * sizeof(float), s))) return st;
+    if ((st = zero_async(a.dbias, (size_t)K * f.dim * sizeof(float), s))) return st;
+    if (empty) return SS_OK;
+    const int64_t rows = f.batch * f.dim;
+    uint8_t *ws = reinterpret_cast<uint8_t *>(a.ws);
+    void *sbuf = ws;                                                   // pre-gate output sum
+    float *duacc = reinterpret_cast<float *>(ws + align256((size_t)rows * f.L * 4));
+    float *ckpt = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(duacc) +
+                                            align256((size_t)K * rows * f.L * 4));
+    if (f.z) {
+        // dz needs the sum of all directions' outputs before the gate
+        ScanArgs fa = f;
+        fa.z = nullptr;
+        fa.out = sbuf;
+        fa.last_state = nullptr;
+        fa.ws = duacc;
+        fa.ws_bytes = (size_t)K * rows * f.L * 4;
+        if ((st = launch_steps(fa))) return st;
+    }
+    for (int k = 0; k < K; ++k) {
+        st = f.io == SS_BF16 ? dispatch_bwd<__nv_bfloat16, true>(a, k, ckpt, duacc + (int64_t)k * rows * f.L)
+                             : dispatch_bwd<float, true>(a, k, ckpt, duacc + (int64_t)k * rows * f.L);
+        if (st) return st;
+    }
+    BwdOrderSet os{};
+    os.K = K;
+    os.H = (int)f.H;
+    os.W = (int)f.W;
+    os.win = f.win;
+    for (int k = 0; k < K; ++k) os.orders[k] = f.orders[k];
+    const unsigned bx = (unsigned)((f.L + 255) / 256);
+    const int64_t want_y = std::max<int64_t>(1, (int64_t)num_sms() * 32 / bx);
+    const unsigned by = (unsigned)std::min<int64_t>({rows, want_y, (int64_t)65535});
+    if (f.io == SS_BF16) {
+        using IO = __nv_bfloat16;
+        k_merge_bwd<IO><<<dim3(bx, by), 256, 0, s>>>(
+            duacc, rows, os, reinterpret_cast<const IO *>(a.dout), reinterpret_cast<const IO *>(f.z),
+            reinterpret_cast<const IO *>(sbuf), reinterpret_cast<IO *>(a.du), reinterpret_cast<IO *>(a.dz));
+    } else {
+        k_merge_bwd<float><<<dim3(bx, by), 256, 0, s>>>(
+            duacc, rows, os, reinterpret_cast<const float *>(a.dout), reinterpret_cast<const float *>(f.z),
+            reinterpret_cast<const float *>(sbuf), reinterpret_cast<float *>(a.du),
+            reinterpret_cast<float *>(a.dz));
+    }
+    return check_launch("backward merge");
 }
 
 ss_status read_device_status(ss_stream_t stream) {

@@ -288,3 +288,24 @@ def test_dwconv_validates(lib):
     assert lib.ss_dwconv3x3_silu_fwd(*bad) == b.SS_ERR_UNSUPPORTED
     bad = list(args); bad[2] = 0
     assert lib.ss_dwconv3x3_silu_fwd(*bad) == b.SS_OK                  # empty: nothing to do
+
+
+@fake_ptrs
+def test_multi_scan_bwd_validates(lib):
+    def call(ndirs=2, orders=(b.SS_DIR_ROW, b.SS_DIR_COL), window=0, H=4, W=8, dz=None, z=None,
+             wsb=None, ws=A16 + 0x2000000, du=A16 + 0x900000):
+        ords = (ctypes.c_int * max(1, len(orders)))(*orders)
+        if wsb is None:
+            wsb = b.load().ss_multi_scan_bwd_workspace_bytes(1, 8, H, W, 16, ndirs)
+        return lib.ss_multi_scan_bwd(1, 8, H, W, ndirs, ords, window, 16, 1, b.SS_BF16, A16,
+                                     A16 + 0x100000, A16 + 0x200000, A16 + 0x300000,
+                                     A16 + 0x400000, None, None, 1, z, A16 + 0x500000, du,
+                                     A16 + 0xa00000, A16 + 0xb00000, A16 + 0xc00000,
+                                     A16 + 0xd00000, None, dz, None, ws, wsb, None)
+    assert call(orders=(b.SS_DIR_WIN, 1), window=0) == b.SS_ERR_INVALID_ARG
+    assert call(z=A16 + 0x600000) == b.SS_ERR_INVALID_ARG           # dz missing
+    assert call(dz=A16 + 0x700000) == b.SS_ERR_INVALID_ARG          # dz without z
+    assert call(H=3, W=5) == b.SS_ERR_UNSUPPORTED
+    assert call(ws=None) == b.SS_ERR_WORKSPACE
+    assert call(du=A16 + 0x100000) == b.SS_ERR_INVALID_ARG          # du on top of delta
+    assert b.load().ss_multi_scan_bwd_workspace_bytes(1, 8, 4, 8, 16, 2) > 0

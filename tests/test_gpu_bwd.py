@@ -216,3 +216,76 @@ def test_bwd_full_size_sampled(oracle):
                                    delta_bias=f["delta_bias"][ch])
     sums = {"dA": got["dA"][ch], "dD": got["dD"][ch], "ddelta_bias": got["ddelta_bias"][ch]}
     assert_grads(sums, rc, wl.io, names=("dA", "dD", "ddelta_bias"))
+
+
+# ---------------------------------------------------------------- multi-direction backward
+def _oracle_order(oracle, code):
+    import selective_state_space_120_b300 as ss
+    return {ss.DIR_ROW: oracle.ORDER_FWD, ss.DIR_COL: oracle.ORDER_COL,
+            ss.DIR_ROW_REV: oracle.ORDER_REV, ss.DIR_COL_REV: oracle.ORDER_COL_REV,
+            ss.DIR_WIN: oracle.ORDER_WIN, ss.DIR_WIN_COL: oracle.ORDER_WIN_COL,
+            ss.DIR_WIN_REV: oracle.ORDER_WIN_REV, ss.DIR_WIN_COL_REV: oracle.ORDER_WIN_COL_REV}[code]
+
+
+def _multi_check(oracle, H, W, orders, window, batch=2, dim=24, N=16, G=1, io="bf16",
+                 with_z=True, with_D=True, use_bias=True):
+    import selective_state_space_120_b300 as ss
+    K, L = len(orders), H * W
+    wl = sc.workload(f"mb{H}x{W}k{K}", batch, dim, L, N=N, G=G, K=K, io=io, with_z=with_z,
+                     with_D=with_D, H=H, W=W)
+    inp = wk.make_inputs(wl, seed=9)
+    dout = wk.make_dout(wl, seed=9)
+    t = sc.device_inputs(inp)
+    m4 = lambda x: None if x is None else x.view(batch, dim, H, W)  # noqa: E731
+    g = ss.multi_scan_bwd(m4(t["u"]), t["delta"], t["A"], t["B"], t["C"], m4(sc.to_torch(dout)),
+                          orders, window, t["D"], t["delta_bias"] if use_bias else None, True,
+                          z=m4(t["z"]))
+    ref = oracle.multi_scan_bwd(inp.as_f64("u"), inp.as_f64("delta"), inp.as_f64("A"),
+                                inp.as_f64("B"), inp.as_f64("C"), _dout_f64(wl, dout),
+                                [_oracle_order(oracle, o) for o in orders], H=H, W=W, win=window,
+                                D=inp.as_f64("D"), z=inp.as_f64("z"),
+                                delta_bias=inp.as_f64("delta_bias") if use_bias else None)
+    got = {k: (None if v is None else sc.from_torch(v)) for k, v in g.items()}
+    for k in ("du", "dz"):
+        if got[k] is not None:
+            got[k] = got[k].reshape(batch, dim, L)
+    return assert_grads(got, ref, io)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_multi_bwd_bidirectional(oracle, io):
+    import selective_state_space_120_b300 as ss
+    _multi_check(oracle, 1, 200, [ss.DIR_ROW, ss.DIR_ROW_REV], 0, io=io)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_multi_bwd_ss2d(oracle, io):
+    import selective_state_space_120_b300 as ss
+    _multi_check(oracle, 8, 12, [ss.DIR_ROW, ss.DIR_COL, ss.DIR_ROW_REV, ss.DIR_COL_REV], 0, io=io)
+
+
+def test_multi_bwd_windowed_cut_short(oracle):
+    import selective_state_space_120_b300 as ss
+    _multi_check(oracle, 7, 8, [ss.DIR_WIN, ss.DIR_WIN_COL, ss.DIR_WIN_REV, ss.DIR_WIN_COL_REV], 3)
+
+
+def test_multi_bwd_video_orders(oracle):
+    import selective_state_space_120_b300 as ss
+    _multi_check(oracle, 4, 36, [ss.DIR_ROW, ss.DIR_ROW_REV, ss.DIR_COL, ss.DIR_COL_REV], 0)
+
+
+def test_multi_bwd_all_orders_groups(oracle):
+    _multi_check(oracle, 8, 8, list(range(8)), 3, dim=32, N=4, G=2, io="f32")
+
+
+def test_multi_bwd_without_gate_skip_bias(oracle):
+    import selective_state_space_120_b300 as ss
+    _multi_check(oracle, 6, 16, [ss.DIR_COL_REV, ss.DIR_WIN], 4, with_z=False)
+    _multi_check(oracle, 6, 16, [ss.DIR_ROW_REV, ss.DIR_COL], 0, with_D=False, use_bias=False)
+
+
+def test_multi_bwd_larger_map(oracle):
+    """Several tiles and checkpoint blocks per direction on a 32 x 40 map."""
+    import selective_state_space_120_b300 as ss
+    _multi_check(oracle, 32, 40, [ss.DIR_ROW, ss.DIR_COL, ss.DIR_ROW_REV, ss.DIR_COL_REV], 0,
+                 batch=1, dim=40)
