@@ -702,6 +702,72 @@ def measure_bwd(steps: int, warmup: int, peak_gbs: float, peak_kind: str):
                        "l2": "inputs rotate over 2 copies (201 MB of inputs each > 126 MB L2)"}}
 
 
+SS2D_BWD_NAME = "vmamba_t_ss2d_bwd_b32_d192_56x56_n16"
+
+
+def measure_ss2d_bwd(steps: int, warmup: int, peak_gbs: float, peak_kind: str):
+    """Backward pass of the SS2D workload (32 x 192 x 56 x 56, N = 16, bf16, four
+    directions, no gate) through ss_multi_scan_bwd, on resident inputs rotating
+    over two copies."""
+    import torch
+    from selective_state_space_120_b300 import _binding as b
+    wl = wk.VMAMBA_SS2D
+    lib = b.load()
+    inp = wk.make_inputs(wl, 0)
+    dout = wk.make_dout(wl, 0)
+    dev = lambda a: None if a is None else Runner._to_dev(a)  # noqa: E731
+    base = {"u": dev(inp.u), "delta": dev(inp.delta), "A": dev(inp.A), "B": dev(inp.B),
+            "C": dev(inp.C), "D": dev(inp.D), "bias": dev(inp.delta_bias), "dout": dev(dout)}
+    K = wl.K
+    f32 = dict(dtype=torch.float32, device="cuda")
+    sets = []
+    for i in range(2):
+        s = {k: (v if i == 0 else v.clone()) for k, v in base.items()}
+        s.update(du=torch.empty_like(s["u"]), ddelta=torch.empty_like(s["delta"]),
+                 dA=torch.empty(K * wl.dim, wl.N, **f32),
+                 dB=torch.empty(wl.batch, K, wl.G, wl.N, wl.L, **f32),
+                 dC=torch.empty(wl.batch, K, wl.G, wl.N, wl.L, **f32),
+                 dD=torch.empty(K * wl.dim, **f32), dbias=torch.empty(K * wl.dim, **f32))
+        sets.append(s)
+    wsb = int(lib.ss_multi_scan_bwd_workspace_bytes(wl.batch, wl.dim, wl.H, wl.W, wl.N, K))
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    ords = (ctypes.c_int * K)(0, 1, 2, 3)
+    stream = torch.cuda.current_stream()
+    st = ctypes.c_void_p(stream.cuda_stream)
+    p = lambda t: t.data_ptr()  # noqa: E731
+    calls = [(wl.batch, wl.dim, wl.H, wl.W, K, ords, 0, wl.N, wl.G, 1, p(s["u"]), p(s["delta"]),
+              p(s["A"]), p(s["B"]), p(s["C"]), p(s["D"]), p(s["bias"]), 1, None, p(s["dout"]),
+              p(s["du"]), p(s["ddelta"]), p(s["dA"]), p(s["dB"]), p(s["dC"]), p(s["dD"]), None,
+              p(s["dbias"]), p(ws), wsb, st) for s in sets]
+    for i in range(warmup):
+        b.check(lib.ss_multi_scan_bwd(*calls[i % 2]))
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        b.check(lib.ss_multi_scan_bwd(*calls[i % 2]))
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    import selective_state_space_120_b300 as ss
+    ss.device_status()
+    ms = float(np.mean([a.elapsed_time(c) for a, c in ev]))
+    props = torch.cuda.get_device_properties(0)
+    peak_tops = props.multi_processor_count * FP32_LANES_PER_SM * 2032 * 1e6 / 1e12
+    ops = wl.elems * K * (wl.N * BWD_OPS_PER_STATE + BWD_OPS_PER_ELEM)
+    ach = ops / (ms * 1e-3) / 1e12
+    return {"value": wl.elems / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
+            "kernel_launches_per_step": K + 1, "memsets_per_step": 5,
+            "roofline": {"bound": "alu", "achieved": ach, "peak": peak_tops, "unit": "TFLOP/s",
+                         "frac": ach / peak_tops,
+                         "peak_source": f"fp32 lane ops: {props.multi_processor_count} SMs x "
+                                        f"{FP32_LANES_PER_SM} lanes x 2032 MHz",
+                         "ops_per_launch": ops, "traffic": ncu_traffic_named(SS2D_BWD_NAME)},
+            "config": {"workload": SS2D_BWD_NAME, "batch": wl.batch, "dim": wl.dim, "H": wl.H,
+                       "W": wl.W, "d_state": wl.N, "directions": K, "io_dtype": "bf16",
+                       "z_gate": False, "orders": [0, 1, 2, 3]}}
+
+
 DWCONV_NAME = "vmamba_t_dwconv3x3_b32_d192_56x56"
 
 
@@ -748,12 +814,47 @@ def measure_dwconv(steps: int, warmup: int, peak_gbs: float, peak_kind: str):
                        "l2": f"inputs rotate over {copies} copies ({copies * alg / 1e6:.0f} MB > 126 MB L2)"}}
 
 
+# Algorithmic work of the forward scan (fp32 lane operations, an FMA counts once;
+# SFU operations counted apart): per element, state and direction Delta'*A, x*B,
+# the state FMA and the readout FMA (4) and one exponential; per element and
+# direction about 14 more (softplus, Delta'*u, SiLU of the gate, the skip and
+# gate FMAs) and 4 SFU operations (the softplus's exponential and logarithm, the
+# gate's exponential and reciprocal).
+FWD_OPS_PER_STATE, FWD_OPS_PER_ELEM = 4, 14
+FWD_SFU_PER_STATE, FWD_SFU_PER_ELEM = 1, 4
+SFU_LANES_PER_SM = 32   # ex2 results per SM and clock, measured on the B300
+
+
+def alu_peaks(max_mhz: int = 2032, sms: int = 148):
+    """fp32 lane operations and SFU operations per second at the maximum SM clock."""
+    return (sms * FP32_LANES_PER_SM * max_mhz * 1e6 / 1e12, sms * SFU_LANES_PER_SM * max_mhz * 1e6 / 1e12)
+
+
 def roofline(wl, kern_ms, peak, peak_kind):
+    """The forward scan's roofline: the ALU ceiling binds (the fp32 and SFU floors
+    of its work lie well above the HBM floor of its bytes); the SFU and HBM
+    figures are reported beside it."""
     alg = algorithmic_bytes(wl)
-    ach = alg / (kern_ms * 1e-3) / 1e9
-    return {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-            "peak_source": f"{peak_kind} (copy bandwidth)",
-            "algorithmic_bytes_per_launch": alg, "traffic": ncu_traffic(wl)}
+    ach_gbs = alg / (kern_ms * 1e-3) / 1e9
+    elem_dirs = wl.elems * wl.K
+    ops = elem_dirs * (wl.N * FWD_OPS_PER_STATE + FWD_OPS_PER_ELEM)
+    sfu = elem_dirs * (wl.N * FWD_SFU_PER_STATE + FWD_SFU_PER_ELEM)
+    fp32_peak, sfu_peak = alu_peaks()
+    ach = ops / (kern_ms * 1e-3) / 1e12
+    ach_sfu = sfu / (kern_ms * 1e-3) / 1e12
+    return {"bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
+            "frac": ach / fp32_peak,
+            "peak_source": "fp32 lane ops: 148 SMs x 128 lanes x 2032 MHz",
+            "ops_per_launch": ops,
+            "sfu": {"achieved": ach_sfu, "peak": sfu_peak, "unit": "T ops/s", "frac": ach_sfu / sfu_peak,
+                    "ops_per_launch": sfu, "peak_source": "148 SMs x 32 ex2/clk x 2032 MHz"},
+            "hbm": {"achieved": ach_gbs, "peak": peak, "unit": "GB/s", "frac": ach_gbs / peak,
+                    "peak_source": f"{peak_kind} (copy bandwidth)",
+                    "algorithmic_bytes_per_launch": alg},
+            "time_floors_us": {"fp32": ops / (fp32_peak * 1e12) * 1e6,
+                               "sfu": sfu / (sfu_peak * 1e12) * 1e6,
+                               "hbm": alg / (peak * 1e9) * 1e6},
+            "traffic": ncu_traffic(wl)}
 
 
 def main(argv=None):
@@ -763,7 +864,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=HEADLINE.name,
-                    choices=sorted(WORKLOADS) + [BWD_NAME, DWCONV_NAME],
+                    choices=sorted(WORKLOADS) + [BWD_NAME, SS2D_BWD_NAME, DWCONV_NAME],
                     help="forward workload to time (the backward pass: its own line only)")
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
@@ -804,13 +905,15 @@ def main(argv=None):
             import torch.distributed as dist
             dist.destroy_process_group()
         return 0
-    if args.workload == BWD_NAME:
-        # the backward pass alone, on one GPU per rank (replicas), device-resident inputs
-        r = measure_bwd(args.steps, args.warmup, peak, peak_kind)
+    if args.workload in (BWD_NAME, SS2D_BWD_NAME):
+        # a backward pass alone, on one GPU per rank (replicas), device-resident inputs
+        measure, bwl = ((measure_bwd, wk.MAMBA_LAYER) if args.workload == BWD_NAME
+                        else (measure_ss2d_bwd, wk.VMAMBA_SS2D))
+        r = measure(args.steps, args.warmup, peak, peak_kind)
         ms = max_over_ranks(r["ms_per_step"], world, "cuda")
         if rank == 0:
             line = {"metric": "selective-scan backward Gelem/s (B·D·L)",
-                    "value": job_value(wk.MAMBA_LAYER.elems, world, ms), "unit": UNIT,
+                    "value": job_value(bwl.elems, world, ms), "unit": UNIT,
                     "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                     "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                     "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded NumPy PCG64)",
@@ -857,6 +960,11 @@ def main(argv=None):
             others[DWCONV_NAME] = measure_dwconv(max(3, min(args.steps, 100)), 5, peak, peak_kind)
         except Exception as e:  # noqa: BLE001 -- reported, not hidden
             others[DWCONV_NAME] = {"error": f"{type(e).__name__}: {e}"}
+        try:
+            others[SS2D_BWD_NAME] = measure_ss2d_bwd(max(3, min(args.steps, 20)), 3, peak, peak_kind)
+            torch.cuda.empty_cache()
+        except Exception as e:  # noqa: BLE001 -- reported, not hidden
+            others[SS2D_BWD_NAME] = {"error": f"{type(e).__name__}: {e}"}
         try:
             others[BWD_NAME] = measure_bwd(max(3, min(args.steps, 30)), 3, peak, peak_kind)
             torch.cuda.empty_cache()
