@@ -114,9 +114,14 @@ struct BwdParams {
     // dB, dC are direction k's (scan order); u, z, dout are read by position from
     // u_g, z_g, dy_g [batch, dim, L]; du goes by scan step, in fp32, to du_acc
     // [batch*dim, L]; dz is left to the merge.
-    int K, k, order, H, W, win;
+    // Two directions may run side by side: blockIdx.z = j scans direction k_z[j]
+    // with traversal order_z[j] (as its u, z, dout maps present it), its
+    // checkpoints at ckpt + j*ck_zstride and its du at du_acc + k_z[j]*du_zstride.
+    int K, H, W, win;
+    int k_z[2], order_z[2];
     const void *u_g, *z_g, *dy_g;
     float *du_acc;
+    int64_t du_zstride, ck_zstride;
 };
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
@@ -172,8 +177,9 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
     const int64_t L = p.L;
     const int64_t row0 = (int64_t)b * p.dim + (int64_t)grp * p.dpg;  // the group's channel 0
     const int row_tma = (int)(row0 + (int64_t)cblk * C::CB);          // u, z, dout rows
-    const int Kd = MULTI ? p.K : 1, kdir = MULTI ? p.k : 0;           // directions, this one
-    const int order = MULTI ? p.order : 0;
+    const int zsl = MULTI ? (int)blockIdx.z : 0;                      // direction slice of the grid
+    const int Kd = MULTI ? p.K : 1, kdir = MULTI ? (zsl ? p.k_z[1] : p.k_z[0]) : 0;  // directions, this one
+    const int order = MULTI ? (zsl ? p.order_z[1] : p.order_z[0]) : 0;
     const bool u_tiled = order == 0 || order == 2;  // u, z, dout as tiles (else gathered)
     // Delta / ddelta rows [batch, K, dim]; B/C rows [batch, K, G, N]
     const int64_t dlrow0 = ((int64_t)b * Kd + kdir) * p.dim + (int64_t)grp * p.dpg;
@@ -210,7 +216,8 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
         Dd[c] = p.D ? __ldg(p.D + poff + dch[c]) : 0.f;
         dD_acc[c] = 0.f;
         dbias_acc[c] = 0.f;
-        ck[c] = p.ckpt + ((int64_t)b * p.dim + dch[c]) * p.nblk * N + g * NPT;
+        ck[c] = p.ckpt + (MULTI ? zsl * p.ck_zstride : 0) + ((int64_t)b * p.dim + dch[c]) * p.nblk * N +
+                g * NPT;
         P0[c] = reinterpret_cast<const float4 *>(smem + C::OFF_P0 + C::prow(chs[c]) * C::P0ROW);
         P1[c] = reinterpret_cast<const float2 *>(smem + C::OFF_P1 + C::prow(chs[c]) * C::P1ROW);
     }
@@ -255,7 +262,7 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
     __syncthreads();
 
     // diagnostics: this CTA leaves its first tile's barrier without arrivals
-    const bool skip_first = (g_debug_flags & 1u) && blockIdx.x == 0 && blockIdx.y == 0;
+    const bool skip_first = (g_debug_flags & 1u) && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
     auto tile_of = [&](int qs) { return qs < nt ? qs : nq - 1 - qs; };
     auto issue = [&](int qs) {
         if (qs == 0 && skip_first) return;
@@ -588,7 +595,8 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
                     if constexpr (MULTI) {
                         // this direction's du by scan step; the merge sums by position
                         const int64_t t = (int64_t)i * T + tl;
-                        if (valid[c] && t < L) p.du_acc[((int64_t)b * p.dim + dch[c]) * L + t] = du;
+                        if (valid[c] && t < L)
+                            p.du_acc[kdir * p.du_zstride + ((int64_t)b * p.dim + dch[c]) * L + t] = du;
                     } else {
                         ob[tl] = IOT<IO>::from_f(du);
                     }
@@ -672,6 +680,32 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
             if (p.dD) atomicAdd(p.dD + poff + dch[c], dD_acc[c]);
             if (p.dbias) atomicAdd(p.dbias + poff + dch[c], dbias_acc[c]);
         }
+    }
+}
+
+// Transposes each [H, W] plane of src [rows, H, W] into dst [rows, W, H], so that
+// a column-order direction can read its inputs as tiles of a row order.  32 x 32
+// tiles through shared memory; grid (rows, ceil(H/32), ceil(W/32)).
+template <typename IO>
+__global__ void __launch_bounds__(256) k_transpose_maps(const IO *__restrict__ src, IO *__restrict__ dst,
+                                                        int H, int W) {
+    __shared__ IO tile[32][33];
+    const int64_t row = blockIdx.x;
+    const int64_t L = (int64_t)H * W;
+    const int r0 = blockIdx.y * 32, c0 = blockIdx.z * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+    const IO *s = src + row * L;
+    IO *d = dst + row * L;
+#pragma unroll
+    for (int k = 0; k < 32; k += 8) {
+        const int r = r0 + ty + k, c = c0 + tx;
+        if (r < H && c < W) tile[ty + k][tx] = s[(int64_t)r * W + c];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 32; k += 8) {
+        const int c = c0 + ty + k, r = r0 + tx;
+        if (r < H && c < W) d[(int64_t)c * H + r] = tile[tx][ty + k];
     }
 }
 

@@ -244,6 +244,8 @@ struct Scan1d {
     // traversals and sums by position.
     static ss_status run_steps(const ScanArgs &a) {
         using namespace ssk;
+        bool windowed = false;
+        for (int k = 0; k < a.K; ++k) windowed = windowed || a.orders[k] >= ORD_WIN;
         const int io = a.io;
         const int64_t rows = a.batch * a.dim;
         const int K = a.K;
@@ -255,7 +257,8 @@ struct Scan1d {
         const uint64_t bcrows = (uint64_t)a.batch * K * a.G * C::N;
         if ((st = make_map(&mb, a.B, io, a.L, bcrows, C::T, C::N))) return st;
         if ((st = make_map(&mc, a.C, io, a.L, bcrows, C::T, C::N))) return st;
-        auto kern = k_scan1d<C, true>;
+        // the windowed orders' gather lives in the option instantiation
+        auto kern = windowed ? k_scan1d<C, true, true> : k_scan1d<C, true, false>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
             return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
         Scan1dParams p{};
@@ -613,8 +616,19 @@ constexpr int kBwdMinBlock = 8;
 
 // MULTI: direction k of a multi-direction call (ckpt and du_acc from the
 // caller); otherwise the single direction with its checkpoints in a.ws.
+// MULTI: directions ks[0..nz) of a multi-direction call, side by side, reading u,
+// z, dout from `tin` (the call's own tensors, or their transposed maps for column
+// orders, then presented as row orders `ords`).
+struct DirLaunch {
+    int nz = 1;
+    int ks[2] = {0, 0}, ords[2] = {0, 0};
+    const void *u = nullptr, *z = nullptr, *dout = nullptr;
+};
+
 template <class C, bool MULTI = false>
-ss_status run_scan_bwd(const BwdArgs &a, int k = 0, float *ckpt = nullptr, float *du_acc = nullptr) {
+ss_status run_scan_bwd(const BwdArgs &a, const DirLaunch &dl = DirLaunch(), float *ckpt = nullptr,
+                       float *du_acc = nullptr) {
+    const int nz = MULTI ? dl.nz : 1;
     using namespace ssk;
     static_assert(C::TS >= kBwdMinBlock, "checkpoint interval");
     const ScanArgs &f = a.f;
@@ -624,10 +638,11 @@ ss_status run_scan_bwd(const BwdArgs &a, int k = 0, float *ckpt = nullptr, float
     const uint64_t bcrows = (uint64_t)f.batch * K * f.G * C::N;
     CUtensorMap mu, md, mz, mdy, mb, mc;
     ss_status st;
-    if ((st = make_map(&mu, f.u, io, f.L, rows, C::T, C::CB))) return st;
+    const void *tu = MULTI ? dl.u : f.u, *tz = MULTI ? dl.z : f.z, *tdy = MULTI ? dl.dout : a.dout;
+    if ((st = make_map(&mu, tu, io, f.L, rows, C::T, C::CB))) return st;
     if ((st = make_map(&md, f.delta, io, f.L, (uint64_t)rows * K, C::T, C::CB))) return st;
-    if ((st = make_map(&mz, f.z ? f.z : f.u, io, f.L, rows, C::T, C::CB))) return st;
-    if ((st = make_map(&mdy, a.dout, io, f.L, rows, C::T, C::CB))) return st;
+    if ((st = make_map(&mz, tz ? tz : tu, io, f.L, rows, C::T, C::CB))) return st;
+    if ((st = make_map(&mdy, tdy, io, f.L, rows, C::T, C::CB))) return st;
     if ((st = make_map(&mb, f.B, io, f.L, bcrows, C::T, C::N))) return st;
     if ((st = make_map(&mc, f.C, io, f.L, bcrows, C::T, C::N))) return st;
     auto kern = k_scan_bwd<C, MULTI>;
@@ -635,20 +650,25 @@ ss_status run_scan_bwd(const BwdArgs &a, int k = 0, float *ckpt = nullptr, float
         return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
     BwdParams p{};
     p.K = K;
-    p.k = k;
-    p.order = MULTI ? f.orders[k] : 0;
+    for (int j = 0; j < 2; ++j) {
+        const int jj = j < nz ? j : 0;
+        p.k_z[j] = MULTI ? dl.ks[jj] : 0;
+        p.order_z[j] = MULTI ? dl.ords[jj] : 0;
+    }
     p.H = (int)f.H;
     p.W = (int)f.W;
     p.win = f.win;
-    p.u_g = f.u;
-    p.z_g = f.z;
-    p.dy_g = a.dout;
+    p.u_g = tu;
+    p.z_g = tz;
+    p.dy_g = tdy;
     p.du_acc = du_acc;
+    p.du_zstride = rows * f.L;
     p.dim = f.dim;
     p.L = f.L;
     p.G = f.G;
     p.dpg = (int)(f.dim / f.G);
     p.nblk = (int)((f.L + C::TS - 1) / C::TS);
+    p.ck_zstride = rows * p.nblk * C::N;
     p.A = f.A;
     p.D = f.D;
     p.bias = f.bias;
@@ -666,25 +686,26 @@ ss_status run_scan_bwd(const BwdArgs &a, int k = 0, float *ckpt = nullptr, float
     const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);
     const unsigned bgs = (unsigned)(f.batch * f.G);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(f.stream);
-    kern<<<dim3(cblocks, bgs, 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mdy, mb, mc, p);
+    kern<<<dim3(cblocks, bgs, (unsigned)nz), C::THREADS, C::SMEM, s>>>(mu, md, mz, mdy, mb, mc, p);
     return check_launch("scan backward");
 }
 
 template <typename IO, bool MULTI = false>
-ss_status dispatch_bwd(const BwdArgs &a, int k = 0, float *ckpt = nullptr, float *du_acc = nullptr) {
+ss_status dispatch_bwd(const BwdArgs &a, const DirLaunch &dl = DirLaunch(), float *ckpt = nullptr,
+                       float *du_acc = nullptr) {
     using namespace ssk;
     // CfgB<IO, N, warps per CTA, channels per lane, states per lane, steps per
     // block, CTAs per SM for the register budget>
     // float32 I/O has twice the prep registers: a budget of two CTAs per SM
     constexpr int MB = sizeof(IO) == 2 ? 3 : 2;
     switch (a.f.N) {
-    case 1: return run_scan_bwd<CfgB<IO, 1, 2, 1, 4, 16, 2>, MULTI>(a, k, ckpt, du_acc);
-    case 2: return run_scan_bwd<CfgB<IO, 2, 2, 1, 4, 16, 2>, MULTI>(a, k, ckpt, du_acc);
-    case 4: return run_scan_bwd<CfgB<IO, 4, 2, 1, 4, 16, 2>, MULTI>(a, k, ckpt, du_acc);
-    case 8: return run_scan_bwd<CfgB<IO, 8, 2, 1, 4, 16, MB>, MULTI>(a, k, ckpt, du_acc);
-    case 16: return run_scan_bwd<CfgB<IO, 16, 4, 1, 4, 16, MB>, MULTI>(a, k, ckpt, du_acc);
-    case 32: return run_scan_bwd<CfgB<IO, 32, 4, 1, 4, 16, MB>, MULTI>(a, k, ckpt, du_acc);
-    case 64: return run_scan_bwd<CfgB<IO, 64, 4, 1, 4, 16, 2>, MULTI>(a, k, ckpt, du_acc);
+    case 1: return run_scan_bwd<CfgB<IO, 1, 2, 1, 4, 16, 2>, MULTI>(a, dl, ckpt, du_acc);
+    case 2: return run_scan_bwd<CfgB<IO, 2, 2, 1, 4, 16, 2>, MULTI>(a, dl, ckpt, du_acc);
+    case 4: return run_scan_bwd<CfgB<IO, 4, 2, 1, 4, 16, 2>, MULTI>(a, dl, ckpt, du_acc);
+    case 8: return run_scan_bwd<CfgB<IO, 8, 2, 1, 4, 16, MB>, MULTI>(a, dl, ckpt, du_acc);
+    case 16: return run_scan_bwd<CfgB<IO, 16, 4, 1, 4, 16, MB>, MULTI>(a, dl, ckpt, du_acc);
+    case 32: return run_scan_bwd<CfgB<IO, 32, 4, 1, 4, 16, MB>, MULTI>(a, dl, ckpt, du_acc);
+    case 64: return run_scan_bwd<CfgB<IO, 64, 4, 1, 4, 16, 2>, MULTI>(a, dl, ckpt, du_acc);
     default: return fail(SS_ERR_UNSUPPORTED, "dstate %d is not one of 1,2,4,8,16,32,64", a.f.N);
     }
 }
@@ -758,8 +779,11 @@ size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 size_t multi_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t L, int N, int K) {
     if (batch <= 0 || dim <= 0 || L <= 0 || N <= 0 || K <= 0) return 0;
     const size_t rows = (size_t)batch * dim;
+    // two checkpoint buffers (directions run two per launch) and the transposed
+    // maps of u, dout and z for the column orders
     return align256(rows * L * 4) + align256((size_t)K * rows * L * 4) +
-           rows * ((L + kBwdMinBlock - 1) / kBwdMinBlock) * N * sizeof(float);
+           align256(2 * rows * ((L + kBwdMinBlock - 1) / kBwdMinBlock) * N * sizeof(float)) +
+           3 * align256(rows * L * 4);
 }
 
 ss_status launch_multi_bwd(const BwdArgs &a, bool empty) {
@@ -781,6 +805,10 @@ ss_status launch_multi_bwd(const BwdArgs &a, bool empty) {
     float *duacc = reinterpret_cast<float *>(ws + align256((size_t)rows * f.L * 4));
     float *ckpt = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(duacc) +
                                             align256((size_t)K * rows * f.L * 4));
+    uint8_t *tmaps = reinterpret_cast<uint8_t *>(ckpt) +
+                     align256(2 * (size_t)rows * ((f.L + kBwdMinBlock - 1) / kBwdMinBlock) * f.N * 4);
+    const size_t mapb = align256((size_t)rows * f.L * 4);
+    void *uT = tmaps, *dyT = tmaps + mapb, *zT = f.z ? (void *)(tmaps + 2 * mapb) : nullptr;
     if (f.z) {
         // dz needs the sum of all directions' outputs before the gate
         ScanArgs fa = f;
@@ -791,10 +819,55 @@ ss_status launch_multi_bwd(const BwdArgs &a, bool empty) {
         fa.ws_bytes = (size_t)K * rows * f.L * 4;
         if ((st = launch_steps(fa))) return st;
     }
+    // Column-order directions read u, dout and z as row-order tiles of the
+    // transposed maps (one transpose each, instead of gathers in every tile).
+    bool cols = false;
+    for (int k = 0; k < K; ++k) cols = cols || f.orders[k] == ORD_COL || f.orders[k] == ORD_COL_REV;
+    // (maps beyond the transpose grid's limits keep the gathers)
+    cols = cols && (f.H + 31) / 32 <= 65535 && (f.W + 31) / 32 <= 65535 && rows < (1ll << 31);
+    if (cols) {
+        const dim3 tg((unsigned)rows, (unsigned)((f.H + 31) / 32), (unsigned)((f.W + 31) / 32));
+        const void *srcs[3] = {f.u, a.dout, f.z};
+        void *dsts[3] = {uT, dyT, zT};
+        for (int j = 0; j < 3; ++j) {
+            if (!srcs[j]) continue;
+            if (f.io == SS_BF16)
+                k_transpose_maps<__nv_bfloat16><<<tg, 256, 0, s>>>(
+                    reinterpret_cast<const __nv_bfloat16 *>(srcs[j]), reinterpret_cast<__nv_bfloat16 *>(dsts[j]),
+                    (int)f.H, (int)f.W);
+            else
+                k_transpose_maps<float><<<tg, 256, 0, s>>>(reinterpret_cast<const float *>(srcs[j]),
+                                                           reinterpret_cast<float *>(dsts[j]), (int)f.H,
+                                                           (int)f.W);
+            if ((st = check_launch("map transpose"))) return st;
+        }
+    }
+    // directions two per launch (grid z), each with its own checkpoints; a
+    // launch pairs directions that read the same maps
+    int plain[8], colk[8], np = 0, nc = 0;
     for (int k = 0; k < K; ++k) {
-        st = f.io == SS_BF16 ? dispatch_bwd<__nv_bfloat16, true>(a, k, ckpt, duacc + (int64_t)k * rows * f.L)
-                             : dispatch_bwd<float, true>(a, k, ckpt, duacc + (int64_t)k * rows * f.L);
-        if (st) return st;
+        if (cols && (f.orders[k] == ORD_COL || f.orders[k] == ORD_COL_REV)) colk[nc++] = k;
+        else plain[np++] = k;
+    }
+    for (int grp = 0; grp < 2; ++grp) {
+        const int *ks = grp ? colk : plain;
+        const int n = grp ? nc : np;
+        for (int j = 0; j < n; j += 2) {
+            DirLaunch dl;
+            dl.nz = j + 1 < n ? 2 : 1;
+            for (int q = 0; q < dl.nz; ++q) {
+                const int k = ks[j + q];
+                dl.ks[q] = k;
+                // the transposed maps present the column orders as row orders
+                dl.ords[q] = grp ? (f.orders[k] == ORD_COL ? ORD_ROW : ORD_ROW_REV) : f.orders[k];
+            }
+            dl.u = grp ? uT : f.u;
+            dl.dout = grp ? dyT : a.dout;
+            dl.z = grp ? zT : f.z;
+            st = f.io == SS_BF16 ? dispatch_bwd<__nv_bfloat16, true>(a, dl, ckpt, duacc)
+                                 : dispatch_bwd<float, true>(a, dl, ckpt, duacc);
+            if (st) return st;
+        }
     }
     BwdOrderSet os{};
     os.K = K;

@@ -612,9 +612,10 @@ __device__ __forceinline__ void store_partials(const Scan1dParams &p, const Merg
 // MULTI = false: a single-direction scan (order 0, OUT_STORE, one direction),
 // with those fields fixed at compile time; MULTI = true: one direction of a
 // multi-direction call, as the params say.
-// EXT = true compiles the optional input paths of a single direction (the
-// zero-order hold and the fused Conv1D); the plain instantiation carries none
-// of their code, which keeps the default scan's registers and schedule.
+// EXT = true compiles the optional paths: for a single direction the
+// zero-order hold and the fused Conv1D, for a multi-direction launch the
+// windowed orders; the plain instantiations carry none of their code, which
+// keeps the default scans' registers and schedule.
 template <class C, bool MULTI, bool EXT = false>
 __global__ void __launch_bounds__(C::THREADS)
 k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
@@ -756,8 +757,9 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
         if (!MULTI || u_tiled) return;
         const IO *urow = reinterpret_cast<const IO *>(p.u_g) + prow * p.L;
         const IO *zrow = reinterpret_cast<const IO *>(p.z_g) + prow * p.L;
-        if (p.order >= ORD_K_WIN) {
-            // windowed orders: walk the windows from this thread's first step
+        if (EXT && p.order >= ORD_K_WIN) {
+            // windowed orders (the option instantiation only): walk the windows
+            // from this thread's first step
             // (forward for the plain orders, backward for the reversed ones)
             const int64_t s_first = t_begin + (int64_t)i * T + pt0;
             const bool tr = p.order == ORD_K_WIN_COL || p.order == ORD_K_WIN_COL_REV;
