@@ -213,7 +213,8 @@ ss_status ss_bidir_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dsta
  * directions run as TMA-staged scans, two side by side per launch, that merge
  * through the workspace: two fp32 [batch, dim, H*W] accumulators (row pair,
  * column pair; each receives its terms in a fixed order, so the result is
- * deterministic), summed and gated by a final merge.
+ * deterministic), summed and gated by a final merge, and a transposed copy of u
+ * that the column directions read as row-order tiles.
  * Otherwise the whole map of a channel is merged in shared memory: H*W is then
  * limited by the per-block shared-memory size (SS_ERR_UNSUPPORTED beyond it).
  */

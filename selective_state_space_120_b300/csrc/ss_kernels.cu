@@ -131,7 +131,7 @@ struct Scan1d {
             p.J = 1;
             p.jbase = 0;
             p.pass = 0;
-            kern<<<dim3(cblocks, bgs, 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
+            kern<<<dim3(cblocks, bgs, 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, mu, p);
             return check_launch("scan");
         }
         // chunked path: L-chunks of Lc steps (a multiple of T)
@@ -143,7 +143,7 @@ struct Scan1d {
         p.sdt = ws + 2 * rows * J * C::N;
         p.pass = 1;
         p.jbase = 0;
-        kern<<<dim3(cblocks, bgs, J - 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
+        kern<<<dim3(cblocks, bgs, J - 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, mu, p);
         if ((st = check_launch("scan chunk-local pass"))) return st;
         const int64_t nthr = rows * C::N;
         k_carry<<<(unsigned)((nthr + 255) / 256), 256, 0, s>>>(rows, a.dim, J, C::N, a.A, p.hend,
@@ -151,7 +151,7 @@ struct Scan1d {
         if ((st = check_launch("carry"))) return st;
         p.pass = 2;
         p.jbase = 1;
-        kern<<<dim3(cblocks, bgs, J - 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
+        kern<<<dim3(cblocks, bgs, J - 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, mu, p);
         return check_launch("scan fix-up pass");
     }
     // K directions (bidirectional or SS2D) as K launches over one fp32
@@ -209,7 +209,7 @@ struct Scan1d {
                 p.orders_z[0] = a.orders[k];
                 p.modes_z[0] = (k == 0) ? OUT_ACC_FIRST : (k == K - 1) ? OUT_ACC_LAST : OUT_ACC_ADD;
                 p.accs_z[0] = acc0;
-                kern<<<dim3(cblocks, bgs, 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
+                kern<<<dim3(cblocks, bgs, 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, mu, p);
                 if ((st = check_launch("direction scan"))) return st;
             }
             return SS_OK;
@@ -221,15 +221,33 @@ struct Scan1d {
         // pair's accumulator is the transposed map, so its accesses stay
         // contiguous; the merge transposes it back.
         float *acc1 = acc0 + rows * a.L;
+        // The column directions read u as row-order tiles of the transposed map
+        // (one transpose, instead of a gather per element): slice 1 of each pair
+        // launch takes that map, and its order is presented as a row order
+        // (column -> row, reversed column -> reversed row); its accumulator is
+        // already indexed by column-major position, i.e. by that row order.
+        // (maps beyond the transpose grid's limits keep the per-element gathers)
+        const bool tr = (a.H + 31) / 32 <= 65535 && (a.W + 31) / 32 <= 65535 && rows < (1ll << 31);
+        CUtensorMap mu2 = mu;
+        if (tr) {
+            void *uT = reinterpret_cast<uint8_t *>(a.ws) + 2 * (size_t)rows * a.L * sizeof(float);
+            using IOt = typename C::IO;
+            const dim3 tg((unsigned)rows, (unsigned)((a.H + 31) / 32), (unsigned)((a.W + 31) / 32));
+            k_transpose_maps<IOt><<<tg, 256, 0, s>>>(reinterpret_cast<const IOt *>(a.u),
+                                                    reinterpret_cast<IOt *>(uT), (int)a.H, (int)a.W);
+            if ((st = check_launch("map transpose"))) return st;
+            if ((st = make_map(&mu2, uT, io, a.L, rows, C::T, C::CB))) return st;
+        }
         for (int half = 0; half < 2; ++half) {
             p.nz = 2;
             p.k0 = 2 * half;
             for (int d = 0; d < 2; ++d) {
-                p.orders_z[d] = a.orders[2 * half + d];
+                const int o = a.orders[2 * half + d];
+                p.orders_z[d] = (d == 0 || !tr) ? o : (o == ORD_COL ? ORD_ROW : ORD_ROW_REV);
                 p.modes_z[d] = half == 0 ? OUT_ACC_FIRST : OUT_ACC_ADD;
                 p.accs_z[d] = d == 0 ? acc0 : acc1;
             }
-            kern<<<dim3(cblocks, bgs, 2), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
+            kern<<<dim3(cblocks, bgs, 2), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, mu2, p);
             if ((st = check_launch("direction pair scan"))) return st;
         }
         using IO = typename C::IO;
@@ -299,7 +317,7 @@ struct Scan1d {
                 p.modes_z[d] = OUT_STEP;
                 p.accs_z[d] = acc0 + (int64_t)kk * rows * a.L;
             }
-            kern<<<dim3(cblocks, bgs, (unsigned)nz), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
+            kern<<<dim3(cblocks, bgs, (unsigned)nz), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, mu, p);
             if ((st = check_launch("direction scan"))) return st;
         }
         using IO = typename C::IO;
@@ -550,8 +568,10 @@ ss_status launch_scan1d(const ScanArgs &a) {
 
 size_t multidir_workspace_bytes(const ScanArgs &a) {
     if (!scan1d_uses_tma(a)) return 0;  // rows not 16-byte aligned: on-chip merge path
-    // one fp32 accumulator; SS2D scans two pairs of directions side by side into two
-    return (size_t)a.batch * a.dim * a.L * sizeof(float) * (a.K == 4 ? 2 : 1);
+    // one fp32 accumulator; SS2D scans two pairs of directions side by side into
+    // two, and reads u of its column directions from a transposed copy
+    const size_t map = (size_t)a.batch * a.dim * a.L * sizeof(float);
+    return a.K == 4 ? 3 * map : map;
 }
 
 size_t steps_workspace_bytes(const ScanArgs &a) {

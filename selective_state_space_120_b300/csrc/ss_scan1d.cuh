@@ -620,7 +620,8 @@ template <class C, bool MULTI, bool EXT = false>
 __global__ void __launch_bounds__(C::THREADS)
 k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
          const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
-         const __grid_constant__ CUtensorMap tm_C, const Scan1dParams p_in) {
+         const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_u2,
+         const Scan1dParams p_in) {
     using IO = typename C::IO;
     Scan1dParams p = p_in;
     if constexpr (!MULTI) {
@@ -636,6 +637,9 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
         p.acc = z1 ? p_in.accs_z[1] : p_in.accs_z[0];        // the params to the stack)
     }
     constexpr int N = C::N, NPT = C::NPT, T = C::T, E = C::E, CL = C::CL;
+    // u tiles: a multi-direction launch's second slice may read another map (the
+    // transposed map, whose rows present a column order as a row order)
+    const CUtensorMap *umap = (MULTI && blockIdx.z != 0) ? &tm_u2 : &tm_u;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -713,7 +717,7 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
     const uint64_t budget = g_wait_budget_ns;
 
     if (tid == 0) {
-        prefetch_tensormap(&tm_u);
+        prefetch_tensormap(umap);
         prefetch_tensormap(&tm_dl);
         prefetch_tensormap(&tm_B);
         prefetch_tensormap(&tm_C);
@@ -737,7 +741,7 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
         // start below 0 on the last chunk; the copy fills zeros there)
         const int xu = (p.order == 2) ? (int)(p.L - (int64_t)(i + 1) * T) : x;
         mbar_expect_tx(bar, tx_bytes);
-        if (u_tiled) tma_load_2d(st + C::OFF_U, &tm_u, xu, row_tma, bar);
+        if (u_tiled) tma_load_2d(st + C::OFF_U, umap, xu, row_tma, bar);
         tma_load_2d(st + C::OFF_DL, &tm_dl, x, dlrow_tma, bar);
         if (z_tiled) tma_load_2d(st + C::OFF_Z, &tm_z, xu, row_tma, bar);
         tma_load_2d(st + C::OFF_B, &tm_B, x, bcrow_tma, bar);

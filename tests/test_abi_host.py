@@ -196,7 +196,8 @@ def test_workspace_sizing_is_host_only(lib):
     # multi-direction calls: unaligned rows merge on chip (no workspace); aligned
     # rows merge through an fp32 [batch, dim, L] accumulator
     assert b.workspace_bytes(b.SS_KIND_BIDIR, 128, 768, 197, 16) == 0
-    assert b.workspace_bytes(b.SS_KIND_CROSS2D, 32, 192, 3136, 16) == 2 * 32 * 192 * 3136 * 4
+    # (SS2D: two accumulators and a transposed copy of u for the column directions)
+    assert b.workspace_bytes(b.SS_KIND_CROSS2D, 32, 192, 3136, 16) == 3 * 32 * 192 * 3136 * 4
     assert b.workspace_bytes(b.SS_KIND_BIDIR, 2, 24, 256, 16) == 2 * 24 * 256 * 4
     # plenty of batch*dim parallelism: single pass, no workspace
     assert b.workspace_bytes(b.SS_KIND_SCAN, 8, 1536, 2048, 16) == 0
