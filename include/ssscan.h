@@ -309,12 +309,19 @@ ss_status ss_selective_state_update(int64_t batch, int64_t dim, int dstate, int 
  *   D, delta_bias [ndirs*dim]               float, nullable
  *   last_state  [batch, ndirs, dim, dstate] float, nullable
  *   orders      host array of ndirs SS_DIR_* codes
- *   workspace   ss_multi_scan_workspace_bytes(batch, dim, H, W, ndirs) =
- *               ndirs*batch*dim*H*W*4 bytes, 16-byte aligned, contents ignored
+ *   workspace   ss_multi_scan_workspace_bytes(batch, dim, H, W, ndirs) bytes,
+ *               16-byte aligned, contents ignored: the fp32 accumulators by step
+ *               (ndirs*batch*dim*H*W*4 bytes, rounded up to 256), then room for
+ *               up to min(ndirs, 3) copies of u (batch*dim*H*W*4 bytes each,
+ *               rounded up to 256)
  * out = (sum_k y_k + D_k*u) * SiLU(z).  Rows must be 16-byte aligned (H*W *
- * element size % 16 == 0), else SS_ERR_UNSUPPORTED.  Directions run two per
- * launch of the scan kernel, each storing its terms by scan step into its own
- * fp32 slice of the workspace; one more launch sums them by position.
+ * element size % 16 == 0), else SS_ERR_UNSUPPORTED.  Every direction reads u
+ * as row-order tiles, forward or back to front: of u itself (the row orders),
+ * or of a copy of u permuted into its base traversal's step order (column-major,
+ * windows, windows column-major), made once per call in the workspace.
+ * Directions run two per launch of the scan kernel, each storing its terms by
+ * scan step into its own fp32 slice of the workspace; one more launch sums them
+ * by position.
  */
 ss_status ss_multi_scan_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, int ndirs,
                             const int *orders, int window, int dstate, int ngroups, ss_dtype io,

@@ -1,6 +1,7 @@
 // C ABI of the selective-scan library: argument validation and dispatch.
 // The arithmetic is in the kernels (ss_kernels.cu); nothing here touches tensor
 // data, so every check below runs before any work is enqueued.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -561,7 +562,12 @@ ss_status ss_dwconv3x3_silu_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W
 
 size_t ss_multi_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t H, int64_t W, int ndirs) {
     if (batch <= 0 || dim <= 0 || H <= 0 || W <= 0 || ndirs < 1 || ndirs > 8) return 0;
-    return (size_t)ndirs * batch * dim * H * W * sizeof(float);
+    // the fp32 accumulators by step, then up to three copies of u permuted into
+    // the column and windowed traversals (sized for float32 I/O, which covers
+    // every order list and I/O type)
+    auto a256 = [](size_t n) { return (n + 255) & ~size_t(255); };
+    const size_t map = (size_t)batch * dim * H * W * sizeof(float);
+    return a256((size_t)ndirs * map) + (size_t)std::min(ndirs, 3) * a256(map);
 }
 
 ss_status ss_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, int dstate,

@@ -74,6 +74,75 @@ int num_sms() {
     return n;
 }
 
+// ---------------------------------------------------------------- traversal copies
+// Base traversal of an order: the step order of the copy of u its direction
+// reads.  0 = u itself (row orders), 1 = column-major, 2 = windows, 3 = windows
+// taken column-major; a reversed order reads its base's copy back to front.
+int order_base(int o) {
+    if (o == ORD_ROW || o == ORD_ROW_REV) return 0;
+    if (o == ORD_COL || o == ORD_COL_REV) return 1;
+    return (o == ORD_WIN || o == ORD_WIN_REV) ? 2 : 3;
+}
+bool order_reversed(int o) {
+    return o == ORD_ROW_REV || o == ORD_COL_REV || o == ORD_WIN_REV || o == ORD_WIN_COL_REV;
+}
+constexpr int kBaseOrder[4] = {ORD_ROW, ORD_COL, ORD_WIN, ORD_WIN_COL};
+
+size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+// Workspace of a call over directions of any order: the fp32 accumulators by
+// step [K][rows][L], then one permuted copy of u per base traversal in use.
+size_t steps_acc_bytes(const ScanArgs &a) {
+    return align256((size_t)a.K * a.batch * a.dim * a.L * sizeof(float));
+}
+size_t steps_copy_bytes(const ScanArgs &a) {
+    return align256((size_t)a.batch * a.dim * a.L * (a.io == SS_BF16 ? 2 : 4));
+}
+// slot[b] = index of base b's copy, or -1 when no direction reads it; returns
+// the number of copies.
+int steps_copy_slots(const ScanArgs &a, int slot[4]) {
+    bool used[4] = {false, false, false, false};
+    for (int k = 0; k < a.K; ++k) used[order_base(a.orders[k])] = true;
+    int n = 0;
+    slot[0] = -1;
+    for (int b = 1; b < 4; ++b) slot[b] = used[b] ? n++ : -1;
+    return n;
+}
+
+// Writes u permuted into the step order of `order` (a column or windowed base
+// order) to `dst`: the column order by 32 x 32 shared-memory transposes, any
+// order by one walk of the traversal per step.
+ss_status permuted_copy(const ScanArgs &a, int order, void *dst) {
+    const int64_t rows = a.batch * a.dim;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(a.stream);
+    const bool tiles = order == ORD_COL && (a.H + 31) / 32 <= 65535 && (a.W + 31) / 32 <= 65535 &&
+                       rows < (1ll << 31);
+    if (tiles) {
+        const dim3 tg((unsigned)rows, (unsigned)((a.H + 31) / 32), (unsigned)((a.W + 31) / 32));
+        if (a.io == SS_BF16)
+            ssk::k_transpose_maps<__nv_bfloat16><<<tg, 256, 0, s>>>(
+                reinterpret_cast<const __nv_bfloat16 *>(a.u), reinterpret_cast<__nv_bfloat16 *>(dst),
+                (int)a.H, (int)a.W);
+        else
+            ssk::k_transpose_maps<float><<<tg, 256, 0, s>>>(reinterpret_cast<const float *>(a.u),
+                                                            reinterpret_cast<float *>(dst), (int)a.H,
+                                                            (int)a.W);
+        return check_launch("map transpose");
+    }
+    const unsigned bx = (unsigned)((a.L + 255) / 256);
+    const int64_t want_y = std::max<int64_t>(1, (int64_t)num_sms() * 32 / bx);
+    const dim3 grid(bx, (unsigned)std::min<int64_t>({rows, want_y, (int64_t)65535}));
+    if (a.io == SS_BF16)
+        ssk::k_permute_order<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            reinterpret_cast<const __nv_bfloat16 *>(a.u), reinterpret_cast<__nv_bfloat16 *>(dst), rows,
+            order, (int)a.H, (int)a.W, a.win);
+    else
+        ssk::k_permute_order<float><<<grid, 256, 0, s>>>(reinterpret_cast<const float *>(a.u),
+                                                         reinterpret_cast<float *>(dst), rows, order,
+                                                         (int)a.H, (int)a.W, a.win);
+    return check_launch("order permute");
+}
+
 // ---------------------------------------------------------------- single direction
 template <class C>
 struct Scan1d {
@@ -102,9 +171,6 @@ struct Scan1d {
         p.K = 1;
         p.k = 0;
         p.order = ORD_ROW;
-        p.H = 1;
-        p.W = (int)a.L;
-        p.divH = FastDiv(1);
         p.mode = OUT_STORE;
         p.u_g = a.u;
         p.z_g = a.z;
@@ -184,9 +250,6 @@ struct Scan1d {
         p.jbase = 0;
         p.pass = 0;
         p.K = K;
-        p.H = (int)a.H;
-        p.W = (int)a.W;
-        p.divH = FastDiv((uint32_t)a.H);
         p.acc = reinterpret_cast<float *>(a.ws);
         p.u_g = a.u;
         p.z_g = a.z;
@@ -226,24 +289,16 @@ struct Scan1d {
         // launch takes that map, and its order is presented as a row order
         // (column -> row, reversed column -> reversed row); its accumulator is
         // already indexed by column-major position, i.e. by that row order.
-        // (maps beyond the transpose grid's limits keep the per-element gathers)
-        const bool tr = (a.H + 31) / 32 <= 65535 && (a.W + 31) / 32 <= 65535 && rows < (1ll << 31);
-        CUtensorMap mu2 = mu;
-        if (tr) {
-            void *uT = reinterpret_cast<uint8_t *>(a.ws) + 2 * (size_t)rows * a.L * sizeof(float);
-            using IOt = typename C::IO;
-            const dim3 tg((unsigned)rows, (unsigned)((a.H + 31) / 32), (unsigned)((a.W + 31) / 32));
-            k_transpose_maps<IOt><<<tg, 256, 0, s>>>(reinterpret_cast<const IOt *>(a.u),
-                                                    reinterpret_cast<IOt *>(uT), (int)a.H, (int)a.W);
-            if ((st = check_launch("map transpose"))) return st;
-            if ((st = make_map(&mu2, uT, io, a.L, rows, C::T, C::CB))) return st;
-        }
+        CUtensorMap mu2;
+        void *uT = reinterpret_cast<uint8_t *>(a.ws) + 2 * (size_t)rows * a.L * sizeof(float);
+        if ((st = permuted_copy(a, ORD_COL, uT))) return st;
+        if ((st = make_map(&mu2, uT, io, a.L, rows, C::T, C::CB))) return st;
         for (int half = 0; half < 2; ++half) {
             p.nz = 2;
             p.k0 = 2 * half;
             for (int d = 0; d < 2; ++d) {
                 const int o = a.orders[2 * half + d];
-                p.orders_z[d] = (d == 0 || !tr) ? o : (o == ORD_COL ? ORD_ROW : ORD_ROW_REV);
+                p.orders_z[d] = (d == 0) ? o : (o == ORD_COL ? ORD_ROW : ORD_ROW_REV);
                 p.modes_z[d] = half == 0 ? OUT_ACC_FIRST : OUT_ACC_ADD;
                 p.accs_z[d] = d == 0 ? acc0 : acc1;
             }
@@ -251,6 +306,15 @@ struct Scan1d {
             if ((st = check_launch("direction pair scan"))) return st;
         }
         using IO = typename C::IO;
+        // whole maps in shared memory when the column map fits (odd stride P)
+        const int P = (a.H & 1) ? (int)a.H : (int)a.H + 1;
+        const size_t msm = (size_t)a.W * P * sizeof(float);
+        if (msm <= 48 * 1024 && rows < (1ll << 31)) {
+            k_merge2_map<IO><<<(unsigned)rows, 256, msm, s>>>(acc0, acc1, reinterpret_cast<const IO *>(a.z),
+                                                              reinterpret_cast<IO *>(a.out), (int)a.H,
+                                                              (int)a.W, P);
+            return check_launch("merge");
+        }
         const dim3 mgrid((unsigned)rows, (unsigned)((a.W + 31) / 32), (unsigned)((a.H + 31) / 32));
         k_merge2<IO><<<mgrid, dim3(32, 8), 0, s>>>(acc0, acc1, reinterpret_cast<const IO *>(a.z),
                                                   reinterpret_cast<IO *>(a.out), (int)a.H, (int)a.W);
@@ -262,8 +326,6 @@ struct Scan1d {
     // traversals and sums by position.
     static ss_status run_steps(const ScanArgs &a) {
         using namespace ssk;
-        bool windowed = false;
-        for (int k = 0; k < a.K; ++k) windowed = windowed || a.orders[k] >= ORD_WIN;
         const int io = a.io;
         const int64_t rows = a.batch * a.dim;
         const int K = a.K;
@@ -275,8 +337,22 @@ struct Scan1d {
         const uint64_t bcrows = (uint64_t)a.batch * K * a.G * C::N;
         if ((st = make_map(&mb, a.B, io, a.L, bcrows, C::T, C::N))) return st;
         if ((st = make_map(&mc, a.C, io, a.L, bcrows, C::T, C::N))) return st;
-        // the windowed orders' gather lives in the option instantiation
-        auto kern = windowed ? k_scan1d<C, true, true> : k_scan1d<C, true, false>;
+        // Directions read u as row-order tiles: of u itself (row orders), or of
+        // a copy permuted into their base traversal's step order (made once per
+        // call, after the accumulators), forward or back to front.
+        CUtensorMap umaps[4];
+        umaps[0] = mu;
+        int slot[4];
+        steps_copy_slots(a, slot);
+        uint8_t *copies = reinterpret_cast<uint8_t *>(a.ws) + steps_acc_bytes(a);
+        const size_t copyb = steps_copy_bytes(a);
+        for (int b = 1; b < 4; ++b) {
+            if (slot[b] < 0) continue;
+            void *dst = copies + (size_t)slot[b] * copyb;
+            if ((st = permuted_copy(a, kBaseOrder[b], dst))) return st;
+            if ((st = make_map(&umaps[b], dst, io, a.L, rows, C::T, C::CB))) return st;
+        }
+        auto kern = k_scan1d<C, true>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
             return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
         Scan1dParams p{};
@@ -289,10 +365,6 @@ struct Scan1d {
         p.jbase = 0;
         p.pass = 0;
         p.K = K;
-        p.H = (int)a.H;
-        p.W = (int)a.W;
-        p.divH = FastDiv((uint32_t)a.H);
-        p.win = a.win;
         p.u_g = a.u;
         p.z_g = a.z;
         p.A = a.A;
@@ -311,13 +383,16 @@ struct Scan1d {
             const int nz = (k + 1 < K) ? 2 : 1;
             p.nz = nz;
             p.k0 = k;
+            const CUtensorMap *um[2];
             for (int d = 0; d < 2; ++d) {
                 const int kk = (d < nz) ? k + d : k;
-                p.orders_z[d] = a.orders[kk];
+                p.orders_z[d] = order_reversed(a.orders[kk]) ? ORD_ROW_REV : ORD_ROW;
                 p.modes_z[d] = OUT_STEP;
                 p.accs_z[d] = acc0 + (int64_t)kk * rows * a.L;
+                um[d] = &umaps[order_base(a.orders[kk])];
             }
-            kern<<<dim3(cblocks, bgs, (unsigned)nz), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, mu, p);
+            kern<<<dim3(cblocks, bgs, (unsigned)nz), C::THREADS, C::SMEM, s>>>(*um[0], md, mz, mb, mc,
+                                                                              *um[1], p);
             if ((st = check_launch("direction scan"))) return st;
         }
         using IO = typename C::IO;
@@ -575,7 +650,8 @@ size_t multidir_workspace_bytes(const ScanArgs &a) {
 }
 
 size_t steps_workspace_bytes(const ScanArgs &a) {
-    return (size_t)a.K * a.batch * a.dim * a.L * sizeof(float);
+    int slot[4];
+    return steps_acc_bytes(a) + (size_t)steps_copy_slots(a, slot) * steps_copy_bytes(a);
 }
 
 ss_status launch_steps(const ScanArgs &a) {
@@ -792,18 +868,15 @@ ss_status launch_dwconv3x3(int64_t batch, int64_t dim, int64_t H, int64_t W, int
     return check_launch("dwconv3x3");
 }
 
-namespace {
-size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
-}  // namespace
-
 size_t multi_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t L, int N, int K) {
     if (batch <= 0 || dim <= 0 || L <= 0 || N <= 0 || K <= 0) return 0;
     const size_t rows = (size_t)batch * dim;
-    // two checkpoint buffers (directions run two per launch) and the transposed
-    // maps of u, dout and z for the column orders
-    return align256(rows * L * 4) + align256((size_t)K * rows * L * 4) +
-           align256(2 * rows * ((L + kBwdMinBlock - 1) / kBwdMinBlock) * N * sizeof(float)) +
-           3 * align256(rows * L * 4);
+    // the pre-gate output sum, the directions' du by step (first the forward
+    // pass's accumulators), the transposed maps of u, dout and z for the column
+    // orders (first the forward pass's permuted copies of u), and two checkpoint
+    // buffers (directions run two per launch)
+    return align256(rows * L * 4) + align256((size_t)K * rows * L * 4) + 3 * align256(rows * L * 4) +
+           align256(2 * rows * ((L + kBwdMinBlock - 1) / kBwdMinBlock) * N * sizeof(float));
 }
 
 ss_status launch_multi_bwd(const BwdArgs &a, bool empty) {
@@ -823,20 +896,20 @@ ss_status launch_multi_bwd(const BwdArgs &a, bool empty) {
     uint8_t *ws = reinterpret_cast<uint8_t *>(a.ws);
     void *sbuf = ws;                                                   // pre-gate output sum
     float *duacc = reinterpret_cast<float *>(ws + align256((size_t)rows * f.L * 4));
-    float *ckpt = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(duacc) +
-                                            align256((size_t)K * rows * f.L * 4));
-    uint8_t *tmaps = reinterpret_cast<uint8_t *>(ckpt) +
-                     align256(2 * (size_t)rows * ((f.L + kBwdMinBlock - 1) / kBwdMinBlock) * f.N * 4);
+    uint8_t *tmaps = reinterpret_cast<uint8_t *>(duacc) + align256((size_t)K * rows * f.L * 4);
     const size_t mapb = align256((size_t)rows * f.L * 4);
+    float *ckpt = reinterpret_cast<float *>(tmaps + 3 * mapb);
     void *uT = tmaps, *dyT = tmaps + mapb, *zT = f.z ? (void *)(tmaps + 2 * mapb) : nullptr;
     if (f.z) {
-        // dz needs the sum of all directions' outputs before the gate
+        // dz needs the sum of all directions' outputs before the gate (its
+        // accumulators and copies of u are followed by the transposed maps'
+        // space, which is written only after it)
         ScanArgs fa = f;
         fa.z = nullptr;
         fa.out = sbuf;
         fa.last_state = nullptr;
         fa.ws = duacc;
-        fa.ws_bytes = (size_t)K * rows * f.L * 4;
+        fa.ws_bytes = align256((size_t)K * rows * f.L * 4) + 3 * mapb;
         if ((st = launch_steps(fa))) return st;
     }
     // Column-order directions read u, dout and z as row-order tiles of the

@@ -114,10 +114,7 @@ struct Scan1dParams {
     int jbase;    // L-chunk index of blockIdx.z == 0
     int pass;     // 0 direct, 1 chunk-local pass, 2 chunk fix-up pass
     int K, k;     // directions of the call, and the one this launch scans
-    int order;    // traversal of direction k (0 row, 1 column, 2, 3 reversed)
-    int H, W;     // map of the column orders (a plain sequence: H = 1, W = L)
-    FastDiv divH;
-    int win;      // window size of the windowed orders
+    int order;    // 0: u tiles in step order; 2: the same, read back to front
     int mode;     // OUT_*
     float *acc;   // [batch*dim, L] fp32 merge accumulator by position (modes 1-3)
     // Multi-direction launches may scan several directions side by side:
@@ -126,7 +123,8 @@ struct Scan1dParams {
     int nz, k0;
     int orders_z[2], modes_z[2];
     float *accs_z[2];
-    const void *u_g, *z_g;  // u and z for the gathers of the column orders
+    const void *u_g;        // u (the fused Conv1D's history across L-chunks)
+    const void *z_g;        // z (the gate of the last direction of a merge)
     const float *A, *D, *bias;
     int softplus, has_z;
     int zoh;                // zero-order-hold input matrix (single direction)
@@ -612,10 +610,12 @@ __device__ __forceinline__ void store_partials(const Scan1dParams &p, const Merg
 // MULTI = false: a single-direction scan (order 0, OUT_STORE, one direction),
 // with those fields fixed at compile time; MULTI = true: one direction of a
 // multi-direction call, as the params say.
-// EXT = true compiles the optional paths: for a single direction the
-// zero-order hold and the fused Conv1D, for a multi-direction launch the
-// windowed orders; the plain instantiations carry none of their code, which
-// keeps the default scans' registers and schedule.
+// Every traversal other than the row order and its reverse reaches the kernel
+// as one of those two over a copy of u permuted into its step order, so u
+// always arrives as TMA tiles.
+// EXT = true compiles the optional paths of a single direction, the
+// zero-order hold and the fused Conv1D; the plain instantiations carry none of
+// their code, which keeps the default scans' registers and schedule.
 template <class C, bool MULTI, bool EXT = false>
 __global__ void __launch_bounds__(C::THREADS)
 k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
@@ -637,8 +637,8 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
         p.acc = z1 ? p_in.accs_z[1] : p_in.accs_z[0];        // the params to the stack)
     }
     constexpr int N = C::N, NPT = C::NPT, T = C::T, E = C::E, CL = C::CL;
-    // u tiles: a multi-direction launch's second slice may read another map (the
-    // transposed map, whose rows present a column order as a row order)
+    // u tiles: the two slices of a multi-direction launch may read different
+    // maps (u, or the copies of u permuted into other traversals' step orders)
     const CUtensorMap *umap = (MULTI && blockIdx.z != 0) ? &tm_u2 : &tm_u;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -656,7 +656,6 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
     const int dlrow_tma = (int)(((int64_t)b * p.K + p.k) * p.dim + (int64_t)grp * p.dpg +
                                 (int64_t)cblk * C::CB);
     const int bcrow_tma = (int)((((int64_t)b * p.K + p.k) * p.G + grp) * N);
-    const bool u_tiled = (p.order == 0 || p.order == 2);  // u (and z) arrive as tiles
     const bool gate_in_prep = (p.mode == OUT_STORE) && p.has_z;
     const int64_t t_begin = (int64_t)jc * p.Lc;
     const int64_t t_end = min(p.L, t_begin + p.Lc);
@@ -711,8 +710,8 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
     for (int c = 0; c < CL; ++c) obrows[c] = smem + C::OFF_OB + chs[c] * C::OBROW;
     const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
     const uint32_t smem0 = smem_u32(smem);
-    const bool z_tiled = u_tiled && gate_in_prep;
-    const uint32_t tx_bytes = (1u + (u_tiled ? 1u : 0u) + (z_tiled ? 1u : 0u)) * C::CB * 64u +
+    const bool z_tiled = gate_in_prep;
+    const uint32_t tx_bytes = (2u + (z_tiled ? 1u : 0u)) * C::CB * 64u +
                               2u * N * 64u;
     const uint64_t budget = g_wait_budget_ns;
 
@@ -741,7 +740,7 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
         // start below 0 on the last chunk; the copy fills zeros there)
         const int xu = (p.order == 2) ? (int)(p.L - (int64_t)(i + 1) * T) : x;
         mbar_expect_tx(bar, tx_bytes);
-        if (u_tiled) tma_load_2d(st + C::OFF_U, umap, xu, row_tma, bar);
+        tma_load_2d(st + C::OFF_U, umap, xu, row_tma, bar);
         tma_load_2d(st + C::OFF_DL, &tm_dl, x, dlrow_tma, bar);
         if (z_tiled) tma_load_2d(st + C::OFF_Z, &tm_z, xu, row_tma, bar);
         tma_load_2d(st + C::OFF_B, &tm_B, x, bcrow_tma, bar);
@@ -753,59 +752,6 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
     }
 
     float sdt_acc = 0.f;
-    // Column orders: this thread's u (and z) values of a chunk, gathered at the
-    // positions the steps visit one chunk before they are prepped.
-    using Raw = typename IOT<IO>::Raw;
-    Raw gu[E], gz[E];
-    auto gather = [&](int i) {
-        if (!MULTI || u_tiled) return;
-        const IO *urow = reinterpret_cast<const IO *>(p.u_g) + prow * p.L;
-        const IO *zrow = reinterpret_cast<const IO *>(p.z_g) + prow * p.L;
-        if (EXT && p.order >= ORD_K_WIN) {
-            // windowed orders (the option instantiation only): walk the windows
-            // from this thread's first step
-            // (forward for the plain orders, backward for the reversed ones)
-            const int64_t s_first = t_begin + (int64_t)i * T + pt0;
-            const bool tr = p.order == ORD_K_WIN_COL || p.order == ORD_K_WIN_COL_REV;
-            const bool rv = p.order >= ORD_K_WIN_REV;
-            WinWalk ww;
-            ww.Hm = tr ? p.W : p.H;
-            ww.Wm = tr ? p.H : p.W;
-            ww.w = p.win;
-            const int64_t sc = min(s_first, p.L - 1);
-            ww.seek((uint32_t)(rv ? p.L - 1 - sc : sc));
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const bool in = s_first + e < p.L;
-                const int64_t pos = tr ? (int64_t)ww.col() * p.W + ww.row()
-                                       : (int64_t)ww.row() * p.W + ww.col();
-                gu[e] = in ? IOT<IO>::load_raw(urow + pos) : Raw(0);
-                if (rv) ww.prev();
-                else ww.next();
-            }
-            return;
-        }
-        // the map cell (r, c) of the first step, then one row down (forward) or
-        // up (reversed) per step, wrapping into the next / previous column
-        const int64_t s_first = t_begin + (int64_t)i * T + pt0;
-        const bool rev = p.order == 3;
-        // column-major index of the first step's cell: s (forward) or L-1-s (reversed)
-        const uint32_t cm = (uint32_t)(rev ? p.L - 1 - min(s_first, p.L - 1) : min(s_first, p.L - 1));
-        int c = (int)p.divH.div(cm);
-        int r = (int)(cm - (uint32_t)c * (uint32_t)p.H);
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const bool in = s_first + e < p.L;
-            const int64_t pos = (int64_t)r * p.W + c;
-            gu[e] = in ? IOT<IO>::load_raw(urow + pos) : Raw(0);
-            if (gate_in_prep) gz[e] = in ? IOT<IO>::load_raw(zrow + pos) : Raw(0);
-            if (!rev) {
-                if (++r == p.H) { r = 0; ++c; }
-            } else {
-                if (--r < 0) { r = p.H - 1; --c; }
-            }
-        }
-    };
     MergeRegs<C> mr;
     if (MULTI) mr.init(p, warp, lane, cblk, row0);
     // Converts B/C and preps the steps of chunk i into buffer half (i & 1).
@@ -823,7 +769,7 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
         if (p.order == 0) {
             load_tile_row<IO, E>(st + C::OFF_U, pch, pt0, uu);
             if (z_tiled) load_tile_row<IO, E>(st + C::OFF_Z, pch, pt0, zz);
-        } else if (p.order == 2) {
+        } else {
             // reversed tile: step pt0+e sits at tile column T-1-(pt0+e)
             float tmp[E];
             load_tile_row<IO, E>(st + C::OFF_U, pch, T - pt0 - E, tmp);
@@ -833,13 +779,6 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
                 load_tile_row<IO, E>(st + C::OFF_Z, pch, T - pt0 - E, tmp);
 #pragma unroll
                 for (int e = 0; e < E; ++e) zz[e] = tmp[E - 1 - e];
-            }
-        } else {
-            // column orders: u (and z) were gathered one chunk early
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                uu[e] = IOT<IO>::widen(gu[e]);
-                if (gate_in_prep) zz[e] = IOT<IO>::widen(gz[e]);
             }
         }
         if (conv) {
@@ -919,11 +858,9 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
         return true;
     };
 
-    if (nchunks > 0) gather(0);
     if (C::OVL && nchunks > 0) {
         const bool ok = mbar_wait_bounded(bar0, 0, budget);
         if (ok) prep_chunk(0);
-        if (nchunks > 1) gather(1);
         if (abandon(0, ok)) return;
         if (tid == 0 && C::STAGES < nchunks) {
             fence_proxy_async_smem();
@@ -939,13 +876,11 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
                 ok = mbar_wait_bounded(bar0 + 8 * ((i + 1) % C::STAGES), ((i + 1) / C::STAGES) & 1,
                                        budget);
                 if (ok) prep_chunk(i + 1);
-                if (i + 2 < nchunks) gather(i + 2);
             }
         } else {
             // classic order: tiles of chunk i, prep, barrier, refill, scan
             ok = mbar_wait_bounded(bar0 + 8 * (i % C::STAGES), (i / C::STAGES) & 1, budget);
             if (ok) prep_chunk(i);
-            if (more) gather(i + 1);
             if (abandon(i, ok)) return;
             if (tid == 0 && i + C::STAGES < nchunks) {
                 fence_proxy_async_smem();
@@ -1075,6 +1010,76 @@ __global__ void __launch_bounds__(256) k_merge2(const float *__restrict__ acc_ro
     }
 }
 
+// k_merge2 for maps whose column accumulator fits in shared memory: one CTA
+// (256 threads) per row stages the whole column-major map with an odd column
+// stride P >= H, so a warp reading one map row across consecutive columns hits
+// 32 distinct banks, then sums every position.  Loads go four per thread at a
+// time, for enough bytes in flight.  Dynamic shared memory: W * P floats.
+template <typename IO>
+__global__ void __launch_bounds__(256) k_merge2_map(const float *__restrict__ acc_row,
+                                                    const float *__restrict__ acc_col,
+                                                    const IO *__restrict__ z, IO *__restrict__ out,
+                                                    int H, int W, int P) {
+    extern __shared__ float colmap[];  // [W][P]
+    const int64_t row = blockIdx.x;
+    const int L = H * W;
+    const int t = threadIdx.x;
+    constexpr int U = 4;
+    {
+        // column-major index i -> cell (r, c) = (i % H, i / H), stepped by 256
+        const float *ac = acc_col + row * (int64_t)L;
+        int c = t / H, r = t - c * H;
+        const int dc = 256 / H, dr = 256 - dc * H;
+        for (int i0 = t; i0 < L; i0 += U * 256) {
+            float v[U];
+            int at[U];
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                const int i = i0 + j * 256;
+                v[j] = i < L ? ac[i] : 0.f;
+                at[j] = c * P + r;
+                r += dr;
+                c += dc;
+                if (r >= H) {
+                    r -= H;
+                    ++c;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < U; ++j)
+                if (i0 + j * 256 < L) colmap[at[j]] = v[j];
+        }
+    }
+    __syncthreads();
+    const float *ar = acc_row + row * (int64_t)L;
+    IO *o = out + row * (int64_t)L;
+    const IO *zr = z ? z + row * (int64_t)L : nullptr;
+    // map position -> cell (r, c) = (pos / W, pos % W), stepped by 256
+    int r = t / W, c = t - r * W;
+    const int dr = 256 / W, dc = 256 - dr * W;
+    for (int p0 = t; p0 < L; p0 += U * 256) {
+        float v[U], g[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const int pos = p0 + j * 256;
+            const bool in = pos < L;
+            v[j] = in ? ar[pos] + colmap[c * P + r] : 0.f;
+            g[j] = (in && zr) ? IOT<IO>::load(zr + pos) : 0.f;
+            c += dc;
+            r += dr;
+            if (c >= W) {
+                c -= W;
+                ++r;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const int pos = p0 + j * 256;
+            if (pos < L) o[pos] = IOT<IO>::from_f(zr ? v[j] * silu(g[j]) : v[j]);
+        }
+    }
+}
+
 // Final merge of a call whose directions stored their terms by scan step
 // (OUT_STEP), for directions of any order: out[p] = (sum_k acc_k[step_k(p)]) *
 // SiLU(z[p]) in the I/O type, where step_k inverts direction k's traversal.
@@ -1105,6 +1110,23 @@ __global__ void __launch_bounds__(256) k_merge_steps(const float *__restrict__ a
         if (z) y *= silu(IOT<IO>::load(z + i));
         out[i] = IOT<IO>::from_f(y);
     }
+}
+
+// Copy of u permuted into the step order of one traversal: out[row][s] =
+// u[row][pos(s)].  A direction of that traversal (or of its reverse) then reads
+// u as row-order tiles of the copy.  A thread owns one step: it finds the
+// step's position once and walks rows blockIdx.y, blockIdx.y + gridDim.y, ...
+// (the traversal is the same for every row).
+template <typename IO>
+__global__ void __launch_bounds__(256) k_permute_order(const IO *__restrict__ u, IO *__restrict__ out,
+                                                       int64_t rows, int order, int H, int W, int win) {
+    const int64_t L = (int64_t)H * W;
+    const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= L) return;
+    OrderWalk ow;
+    ow.start(order, H, W, win, L, s);
+    const int64_t pos = ow.pos_next();
+    for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) out[row * L + s] = u[row * L + pos];
 }
 
 // Chains the L-chunks: carry[j] = state entering chunk j, from the chunk-local

@@ -271,9 +271,13 @@ def test_multi_scan_validates(lib):
     assert call(window=0) == b.SS_ERR_INVALID_ARG          # a windowed order needs a window
     assert call(H=3, W=5) == b.SS_ERR_UNSUPPORTED          # rows of 15 bf16 values
     assert call(ws=None) == b.SS_ERR_WORKSPACE
-    assert call(wsb=b.load().ss_multi_scan_workspace_bytes(1, 8, 4, 8, 2) - 4) == b.SS_ERR_WORKSPACE
+    # (WIN, ROW) needs the two accumulators and one bf16 copy of u in window order
+    need = 2 * 8 * 32 * 4 + 8 * 32 * 2
+    assert call(wsb=need - 4) == b.SS_ERR_WORKSPACE
     assert call(ws=A16 + 0x100000) == b.SS_ERR_INVALID_ARG  # workspace on top of delta
-    assert b.load().ss_multi_scan_workspace_bytes(2, 8, 4, 8, 3) == 3 * 2 * 8 * 32 * 4
+    # the bound: three accumulators and three fp32-sized copies
+    assert b.load().ss_multi_scan_workspace_bytes(2, 8, 4, 8, 3) == 3 * 2 * 8 * 32 * 4 + 3 * 2 * 8 * 32 * 4
+    assert b.load().ss_multi_scan_workspace_bytes(2, 8, 4, 8, 8) == 8 * 2 * 8 * 32 * 4 + 3 * 2 * 8 * 32 * 4
 
 
 @fake_ptrs
