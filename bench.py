@@ -703,15 +703,17 @@ def measure_bwd(steps: int, warmup: int, peak_gbs: float, peak_kind: str):
 
 
 SS2D_BWD_NAME = "vmamba_t_ss2d_bwd_b32_d192_56x56_n16"
+WIN_BWD_NAME = "localmamba_win7_bwd_b32_d192_56x56_n16"
 
 
-def measure_ss2d_bwd(steps: int, warmup: int, peak_gbs: float, peak_kind: str):
-    """Backward pass of the SS2D workload (32 x 192 x 56 x 56, N = 16, bf16, four
-    directions, no gate) through ss_multi_scan_bwd, on resident inputs rotating
-    over two copies."""
+def measure_ss2d_bwd(steps: int, warmup: int, peak_gbs: float, peak_kind: str,
+                     wl: wk.Workload = wk.VMAMBA_SS2D, name: str = SS2D_BWD_NAME):
+    """Backward pass of a four-direction map workload through ss_multi_scan_bwd,
+    on resident inputs rotating over two copies: SS2D (32 x 192 x 56 x 56, N = 16,
+    bf16, row/column orders and their reverses, no gate), or the same shape with
+    LocalMamba's four windowed orders (7 x 7 windows)."""
     import torch
     from selective_state_space_120_b300 import _binding as b
-    wl = wk.VMAMBA_SS2D
     lib = b.load()
     inp = wk.make_inputs(wl, 0)
     dout = wk.make_dout(wl, 0)
@@ -731,11 +733,13 @@ def measure_ss2d_bwd(steps: int, warmup: int, peak_gbs: float, peak_kind: str):
         sets.append(s)
     wsb = int(lib.ss_multi_scan_bwd_workspace_bytes(wl.batch, wl.dim, wl.H, wl.W, wl.N, K))
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
-    ords = (ctypes.c_int * K)(0, 1, 2, 3)
+    order_list = list(wl.orders) if wl.orders else [0, 1, 2, 3]
+    ords = (ctypes.c_int * K)(*order_list)
+    window = int(wl.win or 0)
     stream = torch.cuda.current_stream()
     st = ctypes.c_void_p(stream.cuda_stream)
     p = lambda t: t.data_ptr()  # noqa: E731
-    calls = [(wl.batch, wl.dim, wl.H, wl.W, K, ords, 0, wl.N, wl.G, 1, p(s["u"]), p(s["delta"]),
+    calls = [(wl.batch, wl.dim, wl.H, wl.W, K, ords, window, wl.N, wl.G, 1, p(s["u"]), p(s["delta"]),
               p(s["A"]), p(s["B"]), p(s["C"]), p(s["D"]), p(s["bias"]), 1, None, p(s["dout"]),
               p(s["du"]), p(s["ddelta"]), p(s["dA"]), p(s["dB"]), p(s["dC"]), p(s["dD"]), None,
               p(s["dbias"]), p(ws), wsb, st) for s in sets]
@@ -762,10 +766,10 @@ def measure_ss2d_bwd(steps: int, warmup: int, peak_gbs: float, peak_kind: str):
                          "frac": ach / peak_tops,
                          "peak_source": f"fp32 lane ops: {props.multi_processor_count} SMs x "
                                         f"{FP32_LANES_PER_SM} lanes x 2032 MHz",
-                         "ops_per_launch": ops, "traffic": ncu_traffic_named(SS2D_BWD_NAME)},
-            "config": {"workload": SS2D_BWD_NAME, "batch": wl.batch, "dim": wl.dim, "H": wl.H,
+                         "ops_per_launch": ops, "traffic": ncu_traffic_named(name)},
+            "config": {"workload": name, "batch": wl.batch, "dim": wl.dim, "H": wl.H,
                        "W": wl.W, "d_state": wl.N, "directions": K, "io_dtype": "bf16",
-                       "z_gate": False, "orders": [0, 1, 2, 3]}}
+                       "z_gate": False, "orders": order_list, "window": window}}
 
 
 DWCONV_NAME = "vmamba_t_dwconv3x3_b32_d192_56x56"
@@ -864,7 +868,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=HEADLINE.name,
-                    choices=sorted(WORKLOADS) + [BWD_NAME, SS2D_BWD_NAME, DWCONV_NAME],
+                    choices=sorted(WORKLOADS) + [BWD_NAME, SS2D_BWD_NAME, WIN_BWD_NAME, DWCONV_NAME],
                     help="forward workload to time (the backward pass: its own line only)")
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
@@ -905,11 +909,14 @@ def main(argv=None):
             import torch.distributed as dist
             dist.destroy_process_group()
         return 0
-    if args.workload in (BWD_NAME, SS2D_BWD_NAME):
+    if args.workload in (BWD_NAME, SS2D_BWD_NAME, WIN_BWD_NAME):
         # a backward pass alone, on one GPU per rank (replicas), device-resident inputs
-        measure, bwl = ((measure_bwd, wk.MAMBA_LAYER) if args.workload == BWD_NAME
-                        else (measure_ss2d_bwd, wk.VMAMBA_SS2D))
-        r = measure(args.steps, args.warmup, peak, peak_kind)
+        if args.workload == BWD_NAME:
+            bwl = wk.MAMBA_LAYER
+            r = measure_bwd(args.steps, args.warmup, peak, peak_kind)
+        else:
+            bwl = wk.VMAMBA_SS2D if args.workload == SS2D_BWD_NAME else wk.LOCAL_WIN
+            r = measure_ss2d_bwd(args.steps, args.warmup, peak, peak_kind, bwl, args.workload)
         ms = max_over_ranks(r["ms_per_step"], world, "cuda")
         if rank == 0:
             line = {"metric": "selective-scan backward Gelem/s (B·D·L)",
@@ -965,6 +972,12 @@ def main(argv=None):
             torch.cuda.empty_cache()
         except Exception as e:  # noqa: BLE001 -- reported, not hidden
             others[SS2D_BWD_NAME] = {"error": f"{type(e).__name__}: {e}"}
+        try:
+            others[WIN_BWD_NAME] = measure_ss2d_bwd(max(3, min(args.steps, 20)), 3, peak, peak_kind,
+                                                    wk.LOCAL_WIN, WIN_BWD_NAME)
+            torch.cuda.empty_cache()
+        except Exception as e:  # noqa: BLE001 -- reported, not hidden
+            others[WIN_BWD_NAME] = {"error": f"{type(e).__name__}: {e}"}
         try:
             others[BWD_NAME] = measure_bwd(max(3, min(args.steps, 30)), 3, peak, peak_kind)
             torch.cuda.empty_cache()

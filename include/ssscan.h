@@ -30,8 +30,9 @@
  * POSITION p (token order, or the H x W map in row-major order).  Each
  * direction's Delta_k, B_k and C_k are indexed by its own SCAN STEP s, the
  * layout in which the key code computes them (by projecting the already
- * reordered sequences); u is gathered by index arithmetic, with no permuted
- * copy.
+ * reordered sequences).  The caller's u stays in position order; internally
+ * the column and windowed orders read a copy of u permuted into their step
+ * order, made in the workspace.
  *
  * Layouts: every tensor is dense and C-contiguous (last index fastest).
  *   dtype ss_dtype io:  u, delta, B, C, z, out          (SS_F32 or SS_BF16)

@@ -109,17 +109,16 @@ struct BwdParams {
     float *dA;                // [dim, N]
     float *dB, *dC;           // [batch, G, N, L]
     float *dD, *dbias;        // [dim], nullable
-    // multi-direction calls (MULTI kernels): direction k of K, traversal `order` of
-    // an H x W map (window size win for the windowed orders).  Delta, B, C, ddelta,
-    // dB, dC are direction k's (scan order); u, z, dout are read by position from
-    // u_g, z_g, dy_g [batch, dim, L]; du goes by scan step, in fp32, to du_acc
-    // [batch*dim, L]; dz is left to the merge.
+    // multi-direction calls (MULTI kernels): direction k of K.  Delta, B, C,
+    // ddelta, dB, dC are direction k's (scan order); u, z, dout come as tiles of
+    // maps in direction k's step order, read forward (order 0) or back to front
+    // (order 2); du goes by scan step, in fp32, to du_acc [batch*dim, L]; dz is
+    // left to the merge.
     // Two directions may run side by side: blockIdx.z = j scans direction k_z[j]
-    // with traversal order_z[j] (as its u, z, dout maps present it), its
-    // checkpoints at ckpt + j*ck_zstride and its du at du_acc + k_z[j]*du_zstride.
-    int K, H, W, win;
+    // with order_z[j] over the u, z, dout maps of the launch, its checkpoints at
+    // ckpt + j*ck_zstride and its du at du_acc + k_z[j]*du_zstride.
+    int K;
     int k_z[2], order_z[2];
-    const void *u_g, *z_g, *dy_g;
     float *du_acc;
     int64_t du_zstride, ck_zstride;
 };
@@ -180,7 +179,6 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
     const int zsl = MULTI ? (int)blockIdx.z : 0;                      // direction slice of the grid
     const int Kd = MULTI ? p.K : 1, kdir = MULTI ? (zsl ? p.k_z[1] : p.k_z[0]) : 0;  // directions, this one
     const int order = MULTI ? (zsl ? p.order_z[1] : p.order_z[0]) : 0;
-    const bool u_tiled = order == 0 || order == 2;  // u, z, dout as tiles (else gathered)
     // Delta / ddelta rows [batch, K, dim]; B/C rows [batch, K, G, N]
     const int64_t dlrow0 = ((int64_t)b * Kd + kdir) * p.dim + (int64_t)grp * p.dpg;
     const int dlrow_tma = (int)(dlrow0 + (int64_t)cblk * C::CB);
@@ -237,8 +235,8 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
 
     const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
     const uint32_t smem0 = smem_u32(smem);
-    const uint32_t nuF = u_tiled ? 1u : 0u;                              // u
-    const uint32_t nuB = u_tiled ? (2u + (p.has_z ? 1u : 0u)) : 0u;     // u, dout, z
+    const uint32_t nuF = 1u;                           // u
+    const uint32_t nuB = 2u + (p.has_z ? 1u : 0u);     // u, dout, z
     const uint32_t txF = (nuF + 1u) * C::CB * 64u + N * 64u;
     const uint32_t txB = (nuB + 1u) * C::CB * 64u + 2u * N * 64u;
     const uint64_t budget = g_wait_budget_ns;
@@ -275,14 +273,12 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
         // last tile may start below 0; the copy fills zeros there)
         const int xu = order == 2 ? (int)(L - (int64_t)(tile_of(qs) + 1) * T) : x;
         mbar_expect_tx(bar, bwd ? txB : txF);
-        if (u_tiled) tma_load_2d(st + C::OFF_U, &tm_u, xu, row_tma, bar);
+        tma_load_2d(st + C::OFF_U, &tm_u, xu, row_tma, bar);
         tma_load_2d(st + C::OFF_DL, &tm_dl, x, dlrow_tma, bar);
         tma_load_2d(st + C::OFF_B, &tm_B, x, bcrow_tma, bar);
         if (bwd) {
-            if (u_tiled) {
-                tma_load_2d(st + C::OFF_DY, &tm_dy, xu, row_tma, bar);
-                if (p.has_z) tma_load_2d(st + C::OFF_Z, &tm_z, xu, row_tma, bar);
-            }
+            tma_load_2d(st + C::OFF_DY, &tm_dy, xu, row_tma, bar);
+            if (p.has_z) tma_load_2d(st + C::OFF_Z, &tm_z, xu, row_tma, bar);
             tma_load_2d(st + C::OFF_C, &tm_C, x, bcrow_tma, bar);
         }
     };
@@ -308,8 +304,6 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
             for (int e = 0; e < VPC; ++e) bcf[(qq * VPC + e) * 2 * NB + arr * NB + n] = v[e];
         }
         const int64_t tb0 = (int64_t)i * T;
-        OrderWalk ow;  // the other orders: positions of this thread's steps
-        if (MULTI && !u_tiled) ow.start(order, p.H, p.W, p.win, L, tb0 + pt0);
 #pragma unroll
         for (int e0 = 0; e0 < E; e0 += EP) {
             float uu[EP], dd[EP], zz[EP], gy[EP];
@@ -320,7 +314,7 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
                     load_tile_row<IO, EP>(st + C::OFF_DY, pch, pt0 + e0, gy);
                     if (p.has_z) load_tile_row<IO, EP>(st + C::OFF_Z, pch, pt0 + e0, zz);
                 }
-            } else if (order == 2) {
+            } else {
                 // reversed tile: step pt0+e0+e sits at tile column T-1-(pt0+e0+e)
                 float tmp[EP];
                 const int col = T - (pt0 + e0) - EP;
@@ -335,20 +329,6 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
                         load_tile_row<IO, EP>(st + C::OFF_Z, pch, col, tmp);
 #pragma unroll
                         for (int e = 0; e < EP; ++e) zz[e] = tmp[EP - 1 - e];
-                    }
-                }
-            } else {
-                const IO *ur = reinterpret_cast<const IO *>(p.u_g) + prow * L;
-                const IO *yr = reinterpret_cast<const IO *>(p.dy_g) + prow * L;
-                const IO *zr = reinterpret_cast<const IO *>(p.z_g) + prow * L;
-#pragma unroll
-                for (int e = 0; e < EP; ++e) {
-                    const bool inr = tb0 + pt0 + e0 + e < L;
-                    const int64_t pos = ow.pos_next();
-                    uu[e] = inr ? IOT<IO>::load(ur + pos) : 0.f;
-                    if (bwd) {
-                        gy[e] = inr ? IOT<IO>::load(yr + pos) : 0.f;
-                        zz[e] = (inr && p.has_z) ? IOT<IO>::load(zr + pos) : 0.f;
                     }
                 }
             }

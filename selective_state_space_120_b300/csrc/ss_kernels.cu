@@ -710,11 +710,11 @@ namespace {
 // workspace is sized for 8.
 constexpr int kBwdMinBlock = 8;
 
-// MULTI: direction k of a multi-direction call (ckpt and du_acc from the
-// caller); otherwise the single direction with its checkpoints in a.ws.
-// MULTI: directions ks[0..nz) of a multi-direction call, side by side, reading u,
-// z, dout from `tin` (the call's own tensors, or their transposed maps for column
-// orders, then presented as row orders `ords`).
+// MULTI: directions ks[0..nz) of a multi-direction call, side by side (ckpt and
+// du_acc from the caller), reading u, z, dout from the maps given here (the
+// call's own tensors, or copies permuted into the directions' step order), in
+// the row order or its reverse (`ords`); otherwise the single direction with its
+// checkpoints in a.ws.
 struct DirLaunch {
     int nz = 1;
     int ks[2] = {0, 0}, ords[2] = {0, 0};
@@ -751,12 +751,6 @@ ss_status run_scan_bwd(const BwdArgs &a, const DirLaunch &dl = DirLaunch(), floa
         p.k_z[j] = MULTI ? dl.ks[jj] : 0;
         p.order_z[j] = MULTI ? dl.ords[jj] : 0;
     }
-    p.H = (int)f.H;
-    p.W = (int)f.W;
-    p.win = f.win;
-    p.u_g = tu;
-    p.z_g = tz;
-    p.dy_g = tdy;
     p.du_acc = du_acc;
     p.du_zstride = rows * f.L;
     p.dim = f.dim;
@@ -912,51 +906,41 @@ ss_status launch_multi_bwd(const BwdArgs &a, bool empty) {
         fa.ws_bytes = align256((size_t)K * rows * f.L * 4) + 3 * mapb;
         if ((st = launch_steps(fa))) return st;
     }
-    // Column-order directions read u, dout and z as row-order tiles of the
-    // transposed maps (one transpose each, instead of gathers in every tile).
-    bool cols = false;
-    for (int k = 0; k < K; ++k) cols = cols || f.orders[k] == ORD_COL || f.orders[k] == ORD_COL_REV;
-    // (maps beyond the transpose grid's limits keep the gathers)
-    cols = cols && (f.H + 31) / 32 <= 65535 && (f.W + 31) / 32 <= 65535 && rows < (1ll << 31);
-    if (cols) {
-        const dim3 tg((unsigned)rows, (unsigned)((f.H + 31) / 32), (unsigned)((f.W + 31) / 32));
-        const void *srcs[3] = {f.u, a.dout, f.z};
-        void *dsts[3] = {uT, dyT, zT};
-        for (int j = 0; j < 3; ++j) {
-            if (!srcs[j]) continue;
-            if (f.io == SS_BF16)
-                k_transpose_maps<__nv_bfloat16><<<tg, 256, 0, s>>>(
-                    reinterpret_cast<const __nv_bfloat16 *>(srcs[j]), reinterpret_cast<__nv_bfloat16 *>(dsts[j]),
-                    (int)f.H, (int)f.W);
-            else
-                k_transpose_maps<float><<<tg, 256, 0, s>>>(reinterpret_cast<const float *>(srcs[j]),
-                                                           reinterpret_cast<float *>(dsts[j]), (int)f.H,
-                                                           (int)f.W);
-            if ((st = check_launch("map transpose"))) return st;
+    // Every direction reads u, dout and z as row-order tiles, forward or back to
+    // front: the call's own maps for the row orders, else copies permuted into
+    // its base traversal's step order.  The bases take turns in the three maps'
+    // space (stream order keeps a base's copies until its launches are done);
+    // within a base, directions run two per launch (grid z), each with its own
+    // checkpoints.
+    for (int base = 0; base < 4; ++base) {
+        int ks[8], n = 0;
+        for (int k = 0; k < K; ++k)
+            if (order_base(f.orders[k]) == base) ks[n++] = k;
+        if (n == 0) continue;
+        const void *tu = f.u, *tdy = a.dout, *tz = f.z;
+        if (base != 0) {
+            ScanArgs pa = f;
+            const void *srcs[3] = {f.u, a.dout, f.z};
+            void *dsts[3] = {uT, dyT, zT};
+            for (int j = 0; j < 3; ++j) {
+                if (!srcs[j]) continue;
+                pa.u = srcs[j];
+                if ((st = permuted_copy(pa, kBaseOrder[base], dsts[j]))) return st;
+            }
+            tu = uT;
+            tdy = dyT;
+            tz = zT;
         }
-    }
-    // directions two per launch (grid z), each with its own checkpoints; a
-    // launch pairs directions that read the same maps
-    int plain[8], colk[8], np = 0, nc = 0;
-    for (int k = 0; k < K; ++k) {
-        if (cols && (f.orders[k] == ORD_COL || f.orders[k] == ORD_COL_REV)) colk[nc++] = k;
-        else plain[np++] = k;
-    }
-    for (int grp = 0; grp < 2; ++grp) {
-        const int *ks = grp ? colk : plain;
-        const int n = grp ? nc : np;
         for (int j = 0; j < n; j += 2) {
             DirLaunch dl;
             dl.nz = j + 1 < n ? 2 : 1;
             for (int q = 0; q < dl.nz; ++q) {
-                const int k = ks[j + q];
-                dl.ks[q] = k;
-                // the transposed maps present the column orders as row orders
-                dl.ords[q] = grp ? (f.orders[k] == ORD_COL ? ORD_ROW : ORD_ROW_REV) : f.orders[k];
+                dl.ks[q] = ks[j + q];
+                dl.ords[q] = order_reversed(f.orders[ks[j + q]]) ? ORD_ROW_REV : ORD_ROW;
             }
-            dl.u = grp ? uT : f.u;
-            dl.dout = grp ? dyT : a.dout;
-            dl.z = grp ? zT : f.z;
+            dl.u = tu;
+            dl.dout = tdy;
+            dl.z = tz;
             st = f.io == SS_BF16 ? dispatch_bwd<__nv_bfloat16, true>(a, dl, ckpt, duacc)
                                  : dispatch_bwd<float, true>(a, dl, ckpt, duacc);
             if (st) return st;

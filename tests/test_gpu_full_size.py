@@ -1,7 +1,8 @@
 """GPU parity at the benchmark's full sizes, in the launch configurations the
 benchmark times, for the paths the other full-size cases do not cover: the
 windowed four-direction scan, the Mamba layer with its fused Conv1D + SiLU,
-the SS2D block's DWConv 3x3 + SiLU, and the SS2D backward pass (B300 only).
+the SS2D block's DWConv 3x3 + SiLU, and the backward pass of the SS2D and
+windowed scans (B300 only).
 
 The oracle computes sampled channels one by one (every scan channel depends on
 its own inputs and on B, C of its group only); the backward pass is checked on
@@ -128,20 +129,21 @@ def test_dwconv_full_size_sampled(oracle):
     assert torch.isfinite(u.float()).all()
 
 
-def test_ss2d_bwd_full_size_sampled(oracle):
-    """Backward pass of the SS2D workload (32 x 192 x 56 x 56, four directions,
-    no gate).  Against the oracle: du, ddelta, dB, dC of batch 0 (all 192
-    channels, so dB and dC are complete sums), and dA, dD, ddelta_bias of eight
-    channels summed over all 32 batches."""
+@pytest.mark.parametrize("wl", [wk.VMAMBA_SS2D, wk.LOCAL_WIN], ids=lambda w: w.name)
+def test_multi_bwd_full_size_sampled(oracle, wl):
+    """Backward pass of the four-direction map workloads (32 x 192 x 56 x 56, no
+    gate): SS2D's row/column orders, and LocalMamba's 7 x 7 windowed orders.
+    Against the oracle: du, ddelta, dB, dC of batch 0 (all 192 channels, so dB
+    and dC are complete sums), and dA, dD, ddelta_bias of eight channels summed
+    over all 32 batches."""
     import selective_state_space_120_b300 as ss
-    wl = wk.VMAMBA_SS2D
     inp = wk.make_inputs(wl, seed=0)
     dout = wk.make_dout(wl, seed=0)
     t = sc.device_inputs(inp)
     bsz, dim, H, W, K = wl.batch, wl.dim, wl.H, wl.W, wl.K
-    orders = [ss.DIR_ROW, ss.DIR_COL, ss.DIR_ROW_REV, ss.DIR_COL_REV]
+    orders = list(wl.orders) or [ss.DIR_ROW, ss.DIR_COL, ss.DIR_ROW_REV, ss.DIR_COL_REV]
     g = ss.multi_scan_bwd(t["u"].view(bsz, dim, H, W), t["delta"], t["A"], t["B"], t["C"],
-                          sc.to_torch(dout).view(bsz, dim, H, W), orders, 0, t["D"],
+                          sc.to_torch(dout).view(bsz, dim, H, W), orders, wl.win, t["D"],
                           t["delta_bias"], True)
     got = {k: (None if v is None else sc.from_torch(v)) for k, v in g.items()}
     got["du"] = got["du"].reshape(bsz, dim, wl.L)
@@ -149,13 +151,13 @@ def test_ss2d_bwd_full_size_sampled(oracle):
     dy = _dout_f64(wl, dout)
     ords = [_oracle_order(oracle, o) for o in orders]
     r0 = oracle.multi_scan_bwd(f["u"][:1], f["delta"][:1], f["A"], f["B"][:1], f["C"][:1], dy[:1],
-                               ords, H=H, W=W, D=f["D"], delta_bias=f["delta_bias"])
+                               ords, H=H, W=W, win=wl.win, D=f["D"], delta_bias=f["delta_bias"])
     sub = {k: got[k][:1] for k in ("du", "ddelta", "dB", "dC")}
     assert_grads(sub, r0, wl.io, names=("du", "ddelta", "dB", "dC"))
     ch = np.array([0, 1, 31, 32, 95, 128, 190, 191])
     sel = np.concatenate([k * dim + ch for k in range(K)])
     rc = oracle.multi_scan_bwd(f["u"][:, ch], f["delta"][:, :, ch], f["A"][sel], f["B"], f["C"],
-                               dy[:, ch], ords, H=H, W=W, D=f["D"][sel],
+                               dy[:, ch], ords, H=H, W=W, win=wl.win, D=f["D"][sel],
                                delta_bias=f["delta_bias"][sel])
     sums = {"dA": got["dA"][sel], "dD": got["dD"][sel], "ddelta_bias": got["ddelta_bias"][sel]}
     assert_grads(sums, rc, wl.io, names=("dA", "dD", "ddelta_bias"))
