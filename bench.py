@@ -29,6 +29,7 @@ import argparse
 import ctypes
 import hashlib
 import json
+import re
 import os
 import statistics
 import sys
@@ -73,11 +74,17 @@ def algorithmic_bytes(wl: wk.Workload) -> int:
     return n
 
 
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code, comments removed: it keys the committed
+    ncu traffic figures, which a change of code (not of a comment) invalidates."""
     h = hashlib.sha256()
     for f in sorted(os.listdir(CSRC)):
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+        with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
+            code = _COMMENT.sub("", fh.read())
+        h.update(f.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 

@@ -866,9 +866,9 @@ size_t multi_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t L, int N, i
     if (batch <= 0 || dim <= 0 || L <= 0 || N <= 0 || K <= 0) return 0;
     const size_t rows = (size_t)batch * dim;
     // the pre-gate output sum, the directions' du by step (first the forward
-    // pass's accumulators), the transposed maps of u, dout and z for the column
-    // orders (first the forward pass's permuted copies of u), and two checkpoint
-    // buffers (directions run two per launch)
+    // pass's accumulators), three map slots for the copies of u, dout and z in a
+    // base traversal's step order (first the forward pass's copies of u), and two
+    // checkpoint buffers (directions run two per launch)
     return align256(rows * L * 4) + align256((size_t)K * rows * L * 4) + 3 * align256(rows * L * 4) +
            align256(2 * rows * ((L + kBwdMinBlock - 1) / kBwdMinBlock) * N * sizeof(float));
 }
