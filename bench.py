@@ -994,9 +994,12 @@ def main(argv=None):
     cpu = None
     if rank == 0 and not args.no_cpu:
         v, rows, thr, dt = oracle_sample(wl, budget_s=12.0)
+        v1, rows1, _, dt1 = oracle_sample(wl, budget_s=5.0, threads=1)
         cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
                "sample": f"{rows} whole (batch, channel) rows of the workload (L={wl.L}) "
-                         f"in {dt:.1f} s, threads over rows; host CPU {cpu_model()}"}
+                         f"in {dt:.1f} s, threads over rows; host CPU {cpu_model()}",
+               "single_core": {"value": v1, "unit": UNIT, "cores": 1,
+                               "sample": f"{rows1} rows in {dt1:.1f} s on one thread"}}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
