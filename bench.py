@@ -410,21 +410,22 @@ class Runner:
 
 
 # ------------------------------------------------------------------ CPU oracle arm
-def oracle_sample(wl: wk.Workload, budget_s: float = 12.0, threads: int | None = None):
-    """Times the float64 oracle on whole (batch, channel) rows of the workload
-    until about `budget_s` of wall time is spent, in parallel over rows (ctypes
-    releases the GIL).  Returns (Gelem/s, rows, threads, seconds)."""
-    from concurrent.futures import ThreadPoolExecutor
+_OS: dict = {}  # the oracle sample's inputs, in the process that computes rows
 
-    import oracle
-    oracle.build()
-    threads = threads or os.cpu_count() or 1
-    # a reduced copy of the workload: one batch entry and as many channels as keep
-    # the host arrays near 4 M elements, with the same per-row shape and recipe
+
+def _oracle_sample_workload(wl: wk.Workload) -> wk.Workload:
+    """A reduced copy of the workload: one batch entry and as many channels as
+    keep the host arrays near 4 M elements, with the same per-row shape and
+    recipe."""
     dim = min(wl.dim, max(wl.G, ((1 << 22) // wl.L) // wl.G * wl.G))
-    small = wk.scaled(wl, wl.name + "_oracle_sample", batch=1, dim=dim)
+    return wk.scaled(wl, wl.name + "_oracle_sample", batch=1, dim=dim)
+
+
+def _oracle_sample_init(wl: wk.Workload):
+    """Builds the sample's inputs (seeded, so every process holds the same)."""
+    import oracle
+    small = _oracle_sample_workload(wl)
     inp = wk.make_inputs(small, seed=0)
-    K = wl.K
     if wl.orders:
         # the library's SS_DIR_* codes in the oracle's numbering
         lib_to_oracle = {0: oracle.ORDER_FWD, 1: oracle.ORDER_COL, 2: oracle.ORDER_REV,
@@ -433,31 +434,86 @@ def oracle_sample(wl: wk.Workload, budget_s: float = 12.0, threads: int | None =
         orders = tuple(lib_to_oracle[o] for o in wl.orders)
     else:
         orders = {1: (oracle.ORDER_FWD,), 2: (oracle.ORDER_FWD, oracle.ORDER_REV),
-                  4: oracle.SS2D_ORDERS}[K]
-    H, W = (wl.H, wl.W) if (K == 4 or wl.orders) else (1, wl.L)
-    u, dl, A, B, C = (inp.as_f64(n) for n in ("u", "delta", "A", "B", "C"))
-    D, z, bias = inp.as_f64("D"), inp.as_f64("z"), inp.as_f64("delta_bias")
-    dpg = small.dim // wl.G
-    rows = [(0, d) for d in range(small.dim)]
+                  4: oracle.SS2D_ORDERS}[wl.K]
+    _OS.clear()
+    _OS.update(wl=wl, small=small, orders=orders,
+               HW=(wl.H, wl.W) if (wl.K == 4 or wl.orders) else (1, wl.L),
+               **{n: inp.as_f64(n) for n in ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")})
 
-    def one(bd):
-        b, d = bd
+
+def _oracle_sample_ready(_):
+    return bool(_OS)
+
+
+def _oracle_sample_rows(rows) -> int:
+    """Runs the oracle on whole (batch, channel) rows of the sample."""
+    import oracle
+    S = _OS
+    wl, small = S["wl"], S["small"]
+    K, dpg = wl.K, small.dim // wl.G
+    H, W = S["HW"]
+    u, dl, A, B, C, D, z, bias = (S[n] for n in ("u", "delta", "A", "B", "C", "D", "z",
+                                                 "delta_bias"))
+    for b, d in rows:
         g = d // dpg
         sel = [k * small.dim + d for k in range(K)]
         oracle.scan(u[b:b + 1, d:d + 1], dl[b:b + 1, :, d:d + 1], A[sel],
                     B[b:b + 1, :, g:g + 1], C[b:b + 1, :, g:g + 1],
                     None if D is None else D[sel], None if z is None else z[b:b + 1, d:d + 1],
-                    bias[sel], True, orders, H=H, W=W, win=wl.win)
+                    bias[sel], True, S["orders"], H=H, W=W, win=wl.win)
+    return len(rows)
 
-    done = 0
-    t0 = time.perf_counter()
-    with ThreadPoolExecutor(threads) as ex:
+
+class OracleSampler:
+    """Times the float64 oracle, as it stands, on whole (batch, channel) rows of a
+    workload: in this process (processes = 1), or over a pool of spawned worker
+    processes, each with its own copy of the sample's inputs (threads would
+    serialise on the Python work around each row's call into the C oracle).
+    Only the rows' computation is timed, not the workers' start."""
+
+    def __init__(self, wl: wk.Workload, processes: int | None = None):
+        import oracle
+        oracle.build()
+        self.wl = wl
+        self.n = processes or os.cpu_count() or 1
+        small = _oracle_sample_workload(wl)
+        self.rows = [(0, d) for d in range(small.dim)]
+        self.pool = None
+        if self.n == 1:
+            _oracle_sample_init(wl)
+        else:
+            import multiprocessing as mp
+            self.pool = mp.get_context("spawn").Pool(self.n, _oracle_sample_init, (wl,))
+            self.pool.map(_oracle_sample_ready, range(4 * self.n), chunksize=1)
+
+    def run(self, budget_s: float):
+        """Rows until about `budget_s` of wall time: (Gelem/s, rows, processes, s)."""
+        done = 0
+        t0 = time.perf_counter()
         while time.perf_counter() - t0 < budget_s:
-            batch = [rows[(done + i) % len(rows)] for i in range(threads * 4)]
-            list(ex.map(one, batch))
-            done += len(batch)
-    dt = time.perf_counter() - t0
-    return done * wl.L / dt / 1e9, done, threads, dt
+            batch = [self.rows[(done + i) % len(self.rows)] for i in range(4 * self.n)]
+            if self.pool is None:
+                done += _oracle_sample_rows(batch)
+            else:
+                chunks = [batch[i:i + 4] for i in range(0, len(batch), 4)]
+                done += sum(self.pool.map(_oracle_sample_rows, chunks, chunksize=1))
+        dt = time.perf_counter() - t0
+        return done * self.wl.L / dt / 1e9, done, self.n, dt
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.close()
+            self.pool.join()
+            self.pool = None
+
+
+def oracle_sample(wl: wk.Workload, budget_s: float = 12.0, processes: int | None = None):
+    """One timed sample of the oracle (see OracleSampler)."""
+    sampler = OracleSampler(wl, processes)
+    try:
+        return sampler.run(budget_s)
+    finally:
+        sampler.close()
 
 
 def cpu_model() -> str:
@@ -523,15 +579,19 @@ def run_reference(args, rank, world):
     budget = max(1.0, min(20.0, 60.0 / max(1, steps + warmup)))
     vals = []
     info = None
-    for i in range(warmup + steps):
-        v, rows, thr, dt = oracle_sample(wl, budget_s=budget)
-        if i >= warmup:
-            vals.append(v)
-            info = (rows, thr, dt)
+    sampler = OracleSampler(wl)
+    try:
+        for i in range(warmup + steps):
+            v, rows, thr, dt = sampler.run(budget)
+            if i >= warmup:
+                vals.append(v)
+                info = (rows, thr, dt)
+    finally:
+        sampler.close()
     v = float(np.median(vals))
     rows, thr, dt = info
     sample = (f"whole (batch, channel) rows of the workload (L={wl.L}, N={wl.N}, K={wl.K}), "
-              f"{rows} rows in {dt:.1f} s per step, parallel over rows on {thr} threads; "
+              f"{rows} rows in {dt:.1f} s per step, parallel over rows on {thr} processes; "
               f"host CPU {cpu_model()}")
     line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": steps,
             "warmup": warmup, "ms_per_step": wl.elems / (v * 1e9) * 1e3,
@@ -994,10 +1054,10 @@ def main(argv=None):
     cpu = None
     if rank == 0 and not args.no_cpu:
         v, rows, thr, dt = oracle_sample(wl, budget_s=12.0)
-        v1, rows1, _, dt1 = oracle_sample(wl, budget_s=5.0, threads=1)
+        v1, rows1, _, dt1 = oracle_sample(wl, budget_s=5.0, processes=1)
         cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
                "sample": f"{rows} whole (batch, channel) rows of the workload (L={wl.L}) "
-                         f"in {dt:.1f} s, threads over rows; host CPU {cpu_model()}",
+                         f"in {dt:.1f} s, worker processes over rows; host CPU {cpu_model()}",
                "single_core": {"value": v1, "unit": UNIT, "cores": 1,
                                "sample": f"{rows1} rows in {dt1:.1f} s on one thread"}}
 
