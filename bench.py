@@ -78,12 +78,13 @@ _COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
 
 
 def kernel_source_hash() -> str:
-    """Hash of the kernel sources' code, comments removed: it keys the committed
-    ncu traffic figures, which a change of code (not of a comment) invalidates."""
+    """Hash of the kernel sources' code, comments removed and whitespace runs
+    collapsed: it keys the committed ncu traffic figures, which a change of code
+    (not of a comment or of layout) invalidates."""
     h = hashlib.sha256()
     for f in sorted(os.listdir(CSRC)):
         with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
-            code = _COMMENT.sub("", fh.read())
+            code = " ".join(_COMMENT.sub(" ", fh.read()).split())
         h.update(f.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 

@@ -1,4 +1,5 @@
-// Backward pass of the single-direction selective scan (sm_103a).
+// Backward pass of the selective scan (sm_103a): one direction, and the
+// directions of multi-direction calls (MULTI = true, below the description).
 //
 // Forward (Euler input matrix, zero initial state), per channel d and state n:
 //   Delta'_t = softplus(delta_t + bias_d)     Abar_t = exp(Delta'_t A_n)
@@ -36,8 +37,17 @@
 // in shared memory that the CTA adds up after each block and adds to the fp32
 // outputs with 16-byte atomic adds.  The shared-memory footprint is kept small
 // enough (two ring stages, one sums buffer) for three CTAs of the N = 16
-// configuration to share an SM: a Mamba-layer call then runs in a single wave.  dA, dD and dbias are per-channel sums over
-// time held in registers, added over the batch with atomics at the end.
+// configuration to share an SM: a Mamba-layer call then runs in a single wave.
+// dA, dD and dbias are per-channel sums over time held in registers, added
+// over the batch with atomics at the end.
+//
+// Multi-direction calls: direction k's gradients are those of one direction
+// over its inputs taken in its traversal order.  Two directions run side by
+// side over grid z; u, dout and z come as row-order tiles, forward or back to
+// front, of the call's maps or of copies permuted into the direction's step
+// order (k_transpose_maps for the column order); du goes by scan step to an
+// fp32 buffer per direction, which k_merge_bwd sums by position while forming
+// dz from the sum of all directions' outputs before the gate.
 #pragma once
 
 #include "ss_device.cuh"

@@ -38,6 +38,13 @@
 // The same kernel runs the long-sequence chunked path: pass 1 scans L-chunks
 // from a zero state and records each chunk's end state and sum of Delta';
 // a carry kernel chains them; pass 2 rescans each chunk from its carried state.
+//
+// It also runs the directions of multi-direction calls (MULTI = true): two
+// directions side by side over grid z, each reading u as row-order tiles,
+// forward or back to front, of u itself or of a copy of u permuted into its
+// traversal's step order, and merging through fp32 accumulators (the merge
+// modes below; the final sums by position are k_merge2_map, k_merge2 and
+// k_merge_steps at the end of this file).
 #pragma once
 
 #include "ss_device.cuh"
