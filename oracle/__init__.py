@@ -63,8 +63,13 @@ def _bind(path: str):
                               ctypes.c_int, ctypes.c_int, dp, dp, dp, dp]
     lib.ssor_scan_bwd.restype = ctypes.c_int
     lib.ssor_scan_bwd.argtypes = [i64, i64, i64, i64, i64] + [dp] * 8 + [ctypes.c_int] + [dp] * 10
+    lib.ssor_scan_bwd_ext.restype = ctypes.c_int
+    lib.ssor_scan_bwd_ext.argtypes = ([i64, i64, i64, i64, i64] + [dp] * 8 + [ctypes.c_int] * 2 +
+                                      [dp] * 12)
     lib.ssor_conv_silu.restype = ctypes.c_int
     lib.ssor_conv_silu.argtypes = [i64, i64, i64, i64, dp, dp, dp, dp, dp]
+    lib.ssor_conv_silu_bwd.restype = ctypes.c_int
+    lib.ssor_conv_silu_bwd.argtypes = [i64, i64, i64, i64] + [dp] * 9
     lib.ssor_softplus_scalar.restype = ctypes.c_double
     lib.ssor_softplus_scalar.argtypes = [ctypes.c_double]
     lib.ssor_position_of.restype = ctypes.c_int64
@@ -187,13 +192,14 @@ def cross_scan2d(u, delta, A, B, C, H, W, D=None, z=None, delta_bias=None, delta
 
 
 def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None,
-                       delta_softplus=True):
-    """Gradients of one forward direction (Euler, zero initial state) for the
-    upstream gradient dy [batch, dim, L].  delta [batch, dim, L], B/C
+                       delta_softplus=True, zoh=False, h0=None):
+    """Gradients of one forward direction for the upstream gradient dy
+    [batch, dim, L]: Euler input matrix, or the zero-order hold with zoh; zero
+    initial state, or h0 [batch, dim, N].  delta [batch, dim, L], B/C
     [batch, G, N, L], A [dim, N].  Returns a dict of float64 arrays: du, ddelta
     [batch, dim, L]; dA [dim, N]; dB, dC [batch, G, N, L]; dD, ddelta_bias
     [dim] (None when D / delta_bias are None); dz [batch, dim, L] (None
-    without z)."""
+    without z); dh0 [batch, dim, N] (None without h0)."""
     u = _f64(u, np.asarray(u).shape, "u")
     batch, dim, L = u.shape
     G, N = np.asarray(B).shape[1], np.asarray(B).shape[2]
@@ -210,12 +216,15 @@ def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None,
     out["dD"] = np.empty(dim) if D is not None else None
     out["dz"] = np.empty(u.shape) if z is not None else None
     out["ddelta_bias"] = np.empty(dim) if bias is not None else None
+    h0 = _f64(h0, (batch, dim, N), "h0")
+    out["dh0"] = np.empty((batch, dim, N)) if h0 is not None else None
     work = np.empty(L * N)
-    rc = _load().ssor_scan_bwd(batch, dim, L, N, G, _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
-                               _ptr(D), _ptr(z), _ptr(bias), int(bool(delta_softplus)), _ptr(dy),
-                               _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dA"]),
-                               _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dz"]),
-                               _ptr(out["ddelta_bias"]), _ptr(work))
+    rc = _load().ssor_scan_bwd_ext(batch, dim, L, N, G, _ptr(u), _ptr(delta), _ptr(A), _ptr(B),
+                                   _ptr(C), _ptr(D), _ptr(z), _ptr(bias), int(bool(delta_softplus)),
+                                   int(bool(zoh)), _ptr(h0), _ptr(dy), _ptr(out["du"]),
+                                   _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]),
+                                   _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dz"]),
+                                   _ptr(out["ddelta_bias"]), _ptr(out["dh0"]), _ptr(work))
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return out
@@ -294,6 +303,28 @@ def conv_silu(x, w, bias=None, x0=None):
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return u
+
+
+def conv_silu_bwd(x, w, du, bias=None, x0=None):
+    """Gradients of :func:`conv_silu` for the upstream gradient du [batch, dim, L]
+    of u.  Returns a dict of float64 arrays: dx [batch, dim, L], dw [dim, KW],
+    dbias [dim] (None without bias), dx0 [batch, dim, KW-1] (None without x0)."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    batch, dim, L = x.shape
+    w = _f64(w, (dim, np.asarray(w).shape[-1]), "w")
+    KW = w.shape[1]
+    du = _f64(du, (batch, dim, L), "du")
+    bias = _f64(bias, (dim,), "bias")
+    x0 = _f64(x0, (batch, dim, KW - 1), "x0")
+    g = {"dx": np.empty_like(x), "dw": np.empty_like(w),
+         "dbias": np.empty(dim) if bias is not None else None,
+         "dx0": np.empty((batch, dim, KW - 1)) if x0 is not None else None}
+    rc = _load().ssor_conv_silu_bwd(batch, dim, L, KW, _ptr(x), _ptr(w), _ptr(bias), _ptr(x0),
+                                    _ptr(du), _ptr(g["dx"]), _ptr(g["dw"]), _ptr(g["dbias"]),
+                                    _ptr(g["dx0"]))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return g
 
 
 def dwconv3x3_silu(x, w, bias=None):

@@ -308,13 +308,24 @@ int ssor_dwconv3x3_silu(int64_t batch, int64_t dim, int64_t H, int64_t W, const 
  * dA, dD, dbias sum over the batch; dB, dC sum over the channels of a group.
  * Layouts as ssor_scan with K = 1; h_work holds L*N doubles.  Outputs are
  * overwritten.  Returns 0 or -1.
+ *
+ * The forward options of ssor_scan change the recurrence as follows.
+ *   zoh: the input term is q_n = (abar_n - 1)/a_n * B_n u ("Mamba Series ...",
+ *     discretisation rule; the Euler term Delta' B_n u where a_n = 0, its limit),
+ *     so, from dq/dDelta' = abar B u and dq/da = B u (Delta' abar a - (abar - 1)) / a^2:
+ *       dDelta'_t += dh abar B u (in place of dh B u),
+ *       dA_n += dh B u (Delta' abar a - (abar - 1)) / a^2,
+ *       dB_t += dh (abar - 1)/a u,   du_t += sum_n dh (abar - 1)/a B.
+ *   h0 [batch, dim, N] (NULL: zero): the state before step 0, so step 0's decay
+ *     term uses it, and its gradient is dh0 = abar_0 (.) dh_0, written to dh0
+ *     (nullable).
  */
-int ssor_scan_bwd(int64_t batch, int64_t dim, int64_t L, int64_t N, int64_t ngroups,
-                  const double *u, const double *delta, const double *A, const double *Bm,
-                  const double *Cm, const double *Dv, const double *z, const double *bias,
-                  int delta_softplus, const double *dy, double *du, double *ddelta, double *dA,
-                  double *dB, double *dC, double *dD, double *dz, double *dbias,
-                  double *h_work) {
+int ssor_scan_bwd_ext(int64_t batch, int64_t dim, int64_t L, int64_t N, int64_t ngroups,
+                      const double *u, const double *delta, const double *A, const double *Bm,
+                      const double *Cm, const double *Dv, const double *z, const double *bias,
+                      int delta_softplus, int zoh, const double *h0, const double *dy, double *du,
+                      double *ddelta, double *dA, double *dB, double *dC, double *dD, double *dz,
+                      double *dbias, double *dh0, double *h_work) {
     if (batch < 0 || dim <= 0 || L <= 0 || N <= 0 || ngroups <= 0 || dim % ngroups) return -1;
     if (!u || !delta || !A || !Bm || !Cm || !dy || !du || !ddelta || !dA || !dB || !dC || !h_work)
         return -1;
@@ -337,13 +348,17 @@ int ssor_scan_bwd(int64_t batch, int64_t dim, int64_t L, int64_t N, int64_t ngro
             const double *Cg = Cm + (b * ngroups + grp) * N * L;
             double *dBg = dB + (b * ngroups + grp) * N * L;
             double *dCg = dC + (b * ngroups + grp) * N * L;
+            const double *h0r = h0 ? h0 + (b * dim + d) * N : NULL;
             /* forward: states of every step */
             for (int64_t t = 0; t < L; ++t) {
                 double dt = delta[row + t] + bd;
                 if (delta_softplus) dt = ssor_softplus(dt);
                 for (int64_t n = 0; n < N; ++n) {
-                    const double prev = t ? h_work[(t - 1) * N + n] : 0.0;
-                    h_work[t * N + n] = exp(dt * Ar[n]) * prev + dt * Bg[n * L + t] * u[row + t];
+                    const double a = Ar[n];
+                    const double abar = exp(dt * a);
+                    const double prev = t ? h_work[(t - 1) * N + n] : (h0r ? h0r[n] : 0.0);
+                    const double bq = (zoh && a != 0.0) ? (abar - 1.0) / a : dt;  /* Bbar / B */
+                    h_work[t * N + n] = abar * prev + bq * Bg[n * L + t] * u[row + t];
                 }
             }
             /* reverse: dh carries the gradient of the state after step t */
@@ -371,19 +386,92 @@ int ssor_scan_bwd(int64_t batch, int64_t dim, int64_t L, int64_t N, int64_t ngro
                 for (int64_t n = 0; n < N; ++n) {
                     const double a = Ar[n];
                     const double abar = exp(a * dt);
-                    const double prev = t ? h_work[(t - 1) * N + n] : 0.0;
+                    const double prev = t ? h_work[(t - 1) * N + n] : (h0r ? h0r[n] : 0.0);
                     const double dh = ds * Cg[n * L + t] + carry[n];
                     dCg[n * L + t] += ds * h_work[t * N + n];
                     const double dabar = dh * prev;
-                    ddt += dabar * abar * a + dh * Bg[n * L + t] * u[row + t];
-                    dA[d * N + n] += dabar * abar * dt;
-                    dBg[n * L + t] += dh * dt * u[row + t];
-                    dut += dh * dt * Bg[n * L + t];
+                    if (zoh && a != 0.0) {
+                        const double bq = (abar - 1.0) / a;
+                        const double bu = Bg[n * L + t] * u[row + t];
+                        ddt += dabar * abar * a + dh * abar * bu;
+                        dA[d * N + n] += dabar * abar * dt + dh * bu * (dt * abar * a - (abar - 1.0)) / (a * a);
+                        dBg[n * L + t] += dh * bq * u[row + t];
+                        dut += dh * bq * Bg[n * L + t];
+                    } else {
+                        ddt += dabar * abar * a + dh * Bg[n * L + t] * u[row + t];
+                        dA[d * N + n] += dabar * abar * dt;
+                        dBg[n * L + t] += dh * dt * u[row + t];
+                        dut += dh * dt * Bg[n * L + t];
+                    }
                     carry[n] = abar * dh;
                 }
                 du[row + t] = dut;
                 ddelta[row + t] = ddt * dsp;
                 if (dbias) dbias[d] += ddt * dsp;
+            }
+            if (dh0)
+                for (int64_t n = 0; n < N; ++n) dh0[(b * dim + d) * N + n] = carry[n];
+        }
+    }
+    return 0;
+}
+
+/* The Euler, zero-initial-state case of ssor_scan_bwd_ext. */
+int ssor_scan_bwd(int64_t batch, int64_t dim, int64_t L, int64_t N, int64_t ngroups,
+                  const double *u, const double *delta, const double *A, const double *Bm,
+                  const double *Cm, const double *Dv, const double *z, const double *bias,
+                  int delta_softplus, const double *dy, double *du, double *ddelta, double *dA,
+                  double *dB, double *dC, double *dD, double *dz, double *dbias,
+                  double *h_work) {
+    return ssor_scan_bwd_ext(batch, dim, L, N, ngroups, u, delta, A, Bm, Cm, Dv, z, bias,
+                             delta_softplus, 0, NULL, dy, du, ddelta, dA, dB, dC, dD, dz, dbias,
+                             NULL, h_work);
+}
+
+/*
+ * ssor_conv_silu_bwd: gradients of ssor_conv_silu for an upstream gradient du
+ * of u.  With v_t the pre-activation, dv_t = du_t SiLU'(v_t),
+ * SiLU'(v) = sigmoid(v) (1 + v (1 - sigmoid(v))), and, for each tap j reading
+ * input step s = t - (KW-1) + j:
+ *     dx[s] += w[j] dv_t  (s >= 0),   dx0[(KW-1) + s] += w[j] dv_t  (s < 0)
+ *     dw[d, j] += x[s] dv_t (x0 for s < 0),   dbias[d] += dv_t
+ * dw and dbias sum over the batch.  dx [batch, dim, L]; dw [dim, KW]; dbias
+ * [dim] and dx0 [batch, dim, KW-1] nullable.  Outputs are overwritten.
+ * Returns 0 or -1.
+ */
+int ssor_conv_silu_bwd(int64_t batch, int64_t dim, int64_t L, int64_t KW, const double *x,
+                       const double *w, const double *bias, const double *x0, const double *du,
+                       double *dx, double *dw, double *dbias, double *dx0) {
+    if (batch < 0 || dim <= 0 || L < 0 || KW <= 0 || !x || !w || !du || !dx || !dw) return -1;
+    for (int64_t i = 0; i < batch * dim * L; ++i) dx[i] = 0.0;
+    for (int64_t i = 0; i < dim * KW; ++i) dw[i] = 0.0;
+    if (dbias) for (int64_t i = 0; i < dim; ++i) dbias[i] = 0.0;
+    if (dx0) for (int64_t i = 0; i < batch * dim * (KW - 1); ++i) dx0[i] = 0.0;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const double *xr = x + (b * dim + d) * L;
+            const double *x0r = x0 ? x0 + (b * dim + d) * (KW - 1) : NULL;
+            double *dxr = dx + (b * dim + d) * L;
+            double *dx0r = dx0 ? dx0 + (b * dim + d) * (KW - 1) : NULL;
+            for (int64_t t = 0; t < L; ++t) {
+                double v = bias ? bias[d] : 0.0;
+                for (int64_t j = 0; j < KW; ++j) {
+                    const int64_t s = t - (KW - 1) + j;
+                    v += w[d * KW + j] * (s >= 0 ? xr[s] : (x0r ? x0r[(KW - 1) + s] : 0.0));
+                }
+                const double sg = 1.0 / (1.0 + exp(-v));
+                const double dv = du[(b * dim + d) * L + t] * sg * (1.0 + v * (1.0 - sg));
+                if (dbias) dbias[d] += dv;
+                for (int64_t j = 0; j < KW; ++j) {
+                    const int64_t s = t - (KW - 1) + j;
+                    if (s >= 0) {
+                        dxr[s] += w[d * KW + j] * dv;
+                        dw[d * KW + j] += xr[s] * dv;
+                    } else {
+                        if (dx0r) dx0r[(KW - 1) + s] += w[d * KW + j] * dv;
+                        if (x0r) dw[d * KW + j] += x0r[(KW - 1) + s] * dv;
+                    }
+                }
             }
         }
     }

@@ -52,6 +52,15 @@ MUTANTS = {
                               "h[n] = 0.0;"),
     "last_state_not_final": ("last_state[((b * K + k) * dim + d) * N + n] = h[n];",
                              "last_state[((b * K + k) * dim + d) * N + n] = h[n] * 0.5;"),
+    "bwd_zoh_delta_uses_euler_input": ("ddt += dabar * abar * a + dh * abar * bu;",
+                                       "ddt += dabar * abar * a + dh * bu;"),
+    "bwd_h0_ignored_in_decay": (
+        "const double prev = t ? h_work[(t - 1) * N + n] : (h0r ? h0r[n] : 0.0);\n"
+        "                    const double dh = ds",
+        "const double prev = t ? h_work[(t - 1) * N + n] : 0.0;\n"
+        "                    const double dh = ds"),
+    "conv_bwd_dw_missing_input": ("dw[d * KW + j] += xr[s] * dv;", "dw[d * KW + j] += dv;"),
+    "conv_bwd_silu_derivative": ("sg * (1.0 + v * (1.0 - sg));", "sg;"),
 }
 
 
@@ -92,6 +101,14 @@ class _Variant:
         _oracle._load = lambda: self.lib
         try:
             return _oracle.multi_scan_bwd(*a, **k)
+        finally:
+            _oracle._load = real
+
+    def conv_silu_bwd(self, *a, **k):
+        real = _oracle._load
+        _oracle._load = lambda: self.lib
+        try:
+            return _oracle.conv_silu_bwd(*a, **k)
         finally:
             _oracle._load = real
 

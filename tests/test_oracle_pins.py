@@ -387,21 +387,32 @@ def _fd_case(seed, softplus=True, with_z=True, G=2):
     return dict(u=u, delta=delta, A=A, B=B, C=C, D=D, z=z, delta_bias=bias), dy, softplus
 
 
-@pytest.mark.parametrize("seed,softplus,with_z,G", [(41, True, True, 2), (42, False, False, 1)])
-def test_backward_matches_finite_differences(oracle, seed, softplus, with_z, G):
+@pytest.mark.parametrize("seed,softplus,with_z,G,zoh,with_h0",
+                         [(41, True, True, 2, False, False), (42, False, False, 1, False, False),
+                          (43, True, True, 1, True, False), (44, True, False, 2, False, True),
+                          (45, False, True, 1, True, True)])
+def test_backward_matches_finite_differences(oracle, seed, softplus, with_z, G, zoh, with_h0):
     """Every gradient of the oracle's backward pass against central finite
-    differences of its forward scan, for the loss sum(dy * out)."""
+    differences of its forward scan, for the loss sum(dy * out): the Euler and
+    the zero-order-hold input matrix, a zero or a given initial state (whose
+    gradient is checked too)."""
     args, dy, sp = _fd_case(seed, softplus, with_z, G)
+    batch, dim, _ = args["u"].shape
+    N = args["A"].shape[1]
+    args["h0"] = (np.random.default_rng(seed + 100).standard_normal((batch, dim, N))
+                  if with_h0 else None)
 
     def loss(a):
+        h0 = None if a["h0"] is None else a["h0"][:, None]
         out, _ = oracle.selective_scan(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"],
-                                       a["delta_bias"], sp)
+                                       a["delta_bias"], sp, zoh=zoh, h0=h0)
         return float(np.sum(dy * out))
 
     grads = oracle.selective_scan_bwd(args["u"], args["delta"], args["A"], args["B"], args["C"], dy,
-                                      args["D"], args["z"], args["delta_bias"], sp)
+                                      args["D"], args["z"], args["delta_bias"], sp, zoh=zoh,
+                                      h0=args["h0"])
     names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
-             "z": "dz", "delta_bias": "ddelta_bias"}
+             "z": "dz", "delta_bias": "ddelta_bias", "h0": "dh0"}
     eps = 1e-6
     for name, gname in names.items():
         if args[name] is None:
@@ -418,6 +429,40 @@ def test_backward_matches_finite_differences(oracle, seed, softplus, with_z, G):
             x[idx] = keep
             fd[idx] = (lp - lm) / (2 * eps)
         np.testing.assert_allclose(grads[gname], fd, rtol=2e-6, atol=2e-7, err_msg=name)
+
+
+@pytest.mark.parametrize("with_bias,with_x0", [(True, True), (False, False)])
+def test_conv_backward_matches_finite_differences(oracle, with_bias, with_x0):
+    """Every gradient of the Conv1D + SiLU backward pass against central finite
+    differences of its forward, for the loss sum(du * u), with and without the
+    bias and the inputs before the sequence."""
+    rng = np.random.default_rng(46)
+    batch, dim, L, KW = 2, 3, 7, 4
+    a = {"x": rng.standard_normal((batch, dim, L)), "w": rng.standard_normal((dim, KW)) * 0.5,
+         "bias": rng.standard_normal(dim) * 0.3 if with_bias else None,
+         "x0": rng.standard_normal((batch, dim, KW - 1)) if with_x0 else None}
+    du = rng.standard_normal((batch, dim, L))
+
+    def loss(a):
+        return float(np.sum(du * oracle.conv_silu(a["x"], a["w"], a["bias"], a["x0"])))
+
+    g = oracle.conv_silu_bwd(a["x"], a["w"], du, a["bias"], a["x0"])
+    eps = 1e-6
+    for name, gname in (("x", "dx"), ("w", "dw"), ("bias", "dbias"), ("x0", "dx0")):
+        if a[name] is None:
+            assert g[gname] is None
+            continue
+        x = a[name]
+        fd = np.empty_like(x)
+        for idx in np.ndindex(x.shape):
+            keep = x[idx]
+            x[idx] = keep + eps
+            lp = loss(a)
+            x[idx] = keep - eps
+            lm = loss(a)
+            x[idx] = keep
+            fd[idx] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(g[gname], fd, rtol=2e-6, atol=2e-7, err_msg=name)
 
 
 def test_backward_single_step_closed_form(oracle):
