@@ -355,7 +355,7 @@ int ssor_scan_bwd_ext(int64_t batch, int64_t dim, int64_t L, int64_t N, int64_t 
                 if (delta_softplus) dt = ssor_softplus(dt);
                 for (int64_t n = 0; n < N; ++n) {
                     const double a = Ar[n];
-                    const double abar = exp(dt * a);
+                    const double abar = exp(a * dt);
                     const double prev = t ? h_work[(t - 1) * N + n] : (h0r ? h0r[n] : 0.0);
                     const double bq = (zoh && a != 0.0) ? (abar - 1.0) / a : dt;  /* Bbar / B */
                     h_work[t * N + n] = abar * prev + bq * Bg[n * L + t] * u[row + t];
