@@ -349,8 +349,11 @@ ss_status ss_multi_scan_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, in
  * bytes, 16-byte aligned.  Rows must be 16-byte aligned (H*W * element size % 16
  * == 0), else SS_ERR_UNSUPPORTED.  No output may overlap an input, another output
  * or the workspace.  With a gate, one forward pass without it computes the
- * output sum dz needs; each direction is then one launch of the backward kernel,
- * and one more sums du by position.
+ * output sum dz needs.  Then, per base traversal of the order list (row-major,
+ * column-major, windows, windows column-major), u, dout and z are copied into
+ * that traversal's step order (no copy for the row orders) and its directions
+ * run two per launch of the backward kernel, reading the copies as row-order
+ * tiles, forward or back to front; one more launch sums du by position.
  */
 ss_status ss_multi_scan_bwd(int64_t batch, int64_t dim, int64_t H, int64_t W, int ndirs,
                             const int *orders, int window, int dstate, int ngroups, ss_dtype io,
