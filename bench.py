@@ -51,7 +51,7 @@ FALLBACK_HBM_GBS = 6400.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 CSRC = os.path.join(ROOT, "selective_state_space_120_b300", "csrc")
 
-WORKLOADS = {w.name: w for w in wk.ALL + (wk.MAMBA_LAYER_CONV, wk.LOCAL_WIN)}
+WORKLOADS = {w.name: w for w in wk.ALL + (wk.MAMBA_LAYER_CONV, wk.LOCAL_WIN, wk.LONG_SEQ_PROFILE)}
 HEADLINE = wk.MAMBA_LAYER
 OTHERS = (wk.LONG_SEQ, wk.VIM_BIDIR, wk.VMAMBA_SS2D, wk.MAMBA_LAYER_CONV, wk.LOCAL_WIN)
 
