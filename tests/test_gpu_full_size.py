@@ -1,8 +1,8 @@
 """GPU parity at the benchmark's full sizes, in the launch configurations the
 benchmark times, for the paths the other full-size cases do not cover: the
 windowed four-direction scan, the Mamba layer with its fused Conv1D + SiLU,
-the SS2D block's DWConv 3x3 + SiLU, and the backward pass of the SS2D and
-windowed scans (B300 only).
+the SS2D block's DWConv 3x3 + SiLU, the backward pass of the SS2D and
+windowed scans, and token-by-token decoding (B300 only).
 
 The oracle computes sampled channels one by one (every scan channel depends on
 its own inputs and on B, C of its group only); the backward pass is checked on
@@ -161,3 +161,37 @@ def test_multi_bwd_full_size_sampled(oracle, wl):
                                delta_bias=f["delta_bias"][sel])
     sums = {"dA": got["dA"][sel], "dD": got["dD"][sel], "ddelta_bias": got["ddelta_bias"][sel]}
     assert_grads(sums, rc, wl.io, names=("dA", "dD", "ddelta_bias"))
+
+
+def test_decode_full_size_sampled(oracle):
+    """Token-by-token decoding on the Mamba-130M layer shape (batch 8, dim 1536,
+    N = 16, bf16), the launch configuration the benchmark times: eight steps
+    from a random state against the oracle's eight-step scan from that state,
+    on sampled channels (outputs and the final state)."""
+    import torch
+    import selective_state_space_120_b300 as ss
+    wl = wk.scaled(wk.MAMBA_LAYER, "decode_full", L=8, last_state=True)
+    inp = wk.make_inputs(wl, seed=0)
+    h0 = np.random.default_rng(7).standard_normal((wl.batch, wl.dim, wl.N)).astype(np.float32)
+    t = sc.device_inputs(inp)
+    state = torch.from_numpy(h0).cuda()
+    outs = []
+    for k in range(wl.L):
+        outs.append(ss.selective_state_update(
+            t["u"][:, :, k].contiguous(), t["delta"][:, 0, :, k].contiguous(), t["A"],
+            t["B"][:, 0, :, :, k].contiguous(), t["C"][:, 0, :, :, k].contiguous(), state, t["D"],
+            t["z"][:, :, k].contiguous(), t["delta_bias"], True))
+    torch.cuda.synchronize()
+    got = torch.stack(outs, dim=-1)
+    f = _f64(inp)
+    rows = _rows(wl, n=20)
+    refs, ref_last = [], []
+    for b, d in rows:
+        r = _row_inputs(f, wl, b, d)
+        o, l = oracle.scan(r["u"], r["delta"], r["A"], r["B"], r["C"], r["D"], r["z"],
+                           r["delta_bias"], True, h0=h0[b:b + 1, None, d:d + 1].astype(np.float64))
+        refs.append(o[0, 0])
+        ref_last.append(l[0, 0, 0])
+    sc.assert_close(np.stack([sc.from_torch(got[b, d]) for b, d in rows]), np.stack(refs), wl.io)
+    sc.assert_close(np.stack([state[b, d].cpu().numpy() for b, d in rows]), np.stack(ref_last),
+                    wl.io, "state")
