@@ -196,8 +196,8 @@ ss_status ss_bidir_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dsta
                             ss_stream_t stream);
 
 /*
- * ss_cross_scan2d_fwd -- VMamba SS2D cross-scan, four selective scans and
- * cross-merge, fused: no permuted copies of the map are made.
+ * ss_cross_scan2d_fwd -- VMamba SS2D cross-scan: four selective scans, one per
+ * traversal order, and the cross-merge that sums them by position.
  *
  *   u          [batch, dim, H, W]                 io
  *   delta      [batch, 4, dim, H*W]               io (direction k = SS_DIR_*, in its scan order)
@@ -245,8 +245,9 @@ ss_status ss_cross_scan2d_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, 
  * no cudaFree and no allocating library routine.  Arguments, layouts, options
  * and results are those of ss_selective_scan_fwd_opts, without the workspace.
  *
- * - The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current).  Make that first call
+ * - Each call looks up the array's device address on the current device
+ *   (cudaGetSymbolAddress, which allocates nothing).  The first call on a
+ *   device may also load the library's kernels there: make that first call
  *   before any stream capture on the device.
  * - Calls whose chunked path would need more than SS_NOALLOC_SCRATCH_BYTES
  *   (see ss_workspace_bytes_opts) return SS_ERR_UNSUPPORTED before launching

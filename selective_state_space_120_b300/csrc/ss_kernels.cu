@@ -985,26 +985,17 @@ ss_status read_device_status(ss_stream_t stream) {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SS_NOALLOC_SCRATCH_BYTES];
 
 // In host code g_noalloc_scratch names a host-side shadow, not device memory:
-// the device address comes from cudaGetSymbolAddress, once per device, with
-// that device current.  Guarded by a mutex for callers on several threads.
+// the device address comes from cudaGetSymbolAddress, with the device current.
+// It is looked up on every call (it allocates nothing and is cheap), so a
+// context that was torn down and created again, which may place the array at a
+// new address, never sees a stale pointer.
 ss_status noalloc_scratch(void **ptr) {
-    constexpr int kMaxDevices = 64;
-    static std::mutex mu;
-    static void *addr[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return fail(SS_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices) return fail(SS_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p)
-            return fail(SS_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed: %s",
-                        cudaGetErrorString(e));
-        addr[dev] = p;
-    }
-    *ptr = addr[dev];
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+        return fail(SS_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed: %s",
+                    cudaGetErrorString(e));
+    *ptr = p;
     return SS_OK;
 }
 

@@ -8,13 +8,12 @@ a fixed scratch array that the library keeps in static device memory.
 
 These tests call it through the C ABI and compare it with the existing entry
 point (ss_selective_scan_fwd_opts with a caller-provided workspace) on the same
-inputs, within the suite's tolerance, for two calls in a row: the shared
-scratch keeps the first call's contents, and the second call must not be
-affected by them.  The file is named so that pytest collects it last.
+inputs, bit for bit (same kernels, same L-chunks), for two calls in a row: the
+shared scratch keeps the first call's contents, and the second call must not
+be affected by them.  The file is named so that pytest collects it last.
 """
 import ctypes
 
-import numpy as np
 import pytest
 
 from selective_state_space_120_b300 import workloads as wk
@@ -80,10 +79,15 @@ def _run_both(lib, wl, seed, chunks):
 
 
 def _compare(wl, got, want):
+    """Both entry points run the same kernels with the same L-chunks on the same
+    inputs, so their results must be identical bit for bit; a stale word of the
+    shared scratch would show up here even where it stays within the tolerance."""
+    import torch
     (o1, l1), (o2, l2) = got, want
-    sc.assert_close(sc.from_torch(o1), sc.from_torch(o2), wl.io)
-    sc.assert_close(l1.cpu().numpy().astype(np.float64), l2.cpu().numpy().astype(np.float64),
-                    wl.io, "last_state")
+    assert torch.equal(o1.view(torch.int16) if o1.dtype == torch.bfloat16 else o1.view(torch.int32),
+                       o2.view(torch.int16) if o2.dtype == torch.bfloat16 else o2.view(torch.int32)), \
+        f"out differs: max relative difference {sc.rel_err(sc.from_torch(o1), sc.from_torch(o2)):.3e}"
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32)), "last_state differs"
 
 
 @pytest.mark.parametrize("chunks", [4, 0])
