@@ -1,17 +1,21 @@
 """Benchmark of the B300 selective-scan library.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-others] [--no-cpu]
+                    [--workload NAME] [--all] [--no-others] [--no-cpu]
 
 Prints ONE JSON line.  A step is one call of the library over one batch of the
-workload (inputs resident in HBM).  The headline workload is the Mamba-130M
-layer-shaped scan (batch 8, 1536 channels, L = 2048, N = 16, bf16 I/O, fp32
-state, z gate and D skip); the long-sequence, bidirectional and SS2D workloads
-are measured the same way and reported under "workloads".
+workload (inputs resident in HBM).  The headline workload is the largest one
+that fits one GPU: the long-sequence scan (batch 1, 5120 channels, L = 131072,
+N = 16, bf16 I/O, fp32 state, z gate, D skip, last_state; the chunked path).
+The Mamba-130M layer scan, the Vision Mamba bidirectional scan and the VMamba
+SS2D scan are measured the same way and reported under "workloads", each with
+its own roofline, end-to-end and CPU-oracle figures.  --all adds the other
+measured paths (fused Conv1D, windowed orders, decode, DWConv, backward passes)
+under "more"; --workload NAME prints one workload's line alone.
 
 Timing: W untimed warm-up steps, then K steps between a barrier and a device
 synchronisation on each side, timed with CUDA events on the launching stream;
-each launch is also bracketed by its own events to give the kernel's average
+each call is also bracketed by its own events to give the kernels' average
 duration for the roofline.  Inputs rotate over several copies whose total size
 exceeds the 126 MB L2, so every step reads cold data.  SM clocks and throttle
 reasons are sampled through NVML during the timed region.
@@ -52,8 +56,11 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 CSRC = os.path.join(ROOT, "selective_state_space_120_b300", "csrc")
 
 WORKLOADS = {w.name: w for w in wk.ALL + (wk.MAMBA_LAYER_CONV, wk.LOCAL_WIN, wk.LONG_SEQ_PROFILE)}
-HEADLINE = wk.MAMBA_LAYER
-OTHERS = (wk.LONG_SEQ, wk.VIM_BIDIR, wk.VMAMBA_SS2D, wk.MAMBA_LAYER_CONV, wk.LOCAL_WIN)
+HEADLINE = wk.LONG_SEQ
+# the other workloads of the target set, one compact record each
+TARGETS = (wk.MAMBA_LAYER, wk.VIM_BIDIR, wk.VMAMBA_SS2D)
+# further measured paths (--all)
+EXTRA = (wk.MAMBA_LAYER_CONV, wk.LOCAL_WIN)
 
 
 # ------------------------------------------------------------------ accounting
@@ -406,8 +413,7 @@ class Runner:
         ms = t0.elapsed_time(t1) / steps
         return {"value": self.wl.elems / (ms * 1e-3) / 1e9, "unit": UNIT,
                 "ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipelined": "3 streams, 2 buffer sets: H2D of step i+1 and D2H of step i-1 "
-                             "overlap step i"}
+                "pipelined": "3 streams, 2 buffer sets"}
 
 
 # ------------------------------------------------------------------ CPU oracle arm
@@ -894,7 +900,9 @@ def measure_dwconv(steps: int, warmup: int, peak_gbs: float, peak_kind: str):
 # gate's exponential and reciprocal).
 FWD_OPS_PER_STATE, FWD_OPS_PER_ELEM = 4, 14
 FWD_SFU_PER_STATE, FWD_SFU_PER_ELEM = 1, 4
-SFU_LANES_PER_SM = 32   # ex2 results per SM and clock, measured on the B300
+# ex2 results per SM and clock: 30 measured on the B300 by a probe of
+# independent ex2.approx streams over all 148 SMs (32 nominal).
+SFU_LANES_PER_SM = 30
 
 
 def alu_peaks(max_mhz: int = 2032, sms: int = 148):
@@ -903,44 +911,68 @@ def alu_peaks(max_mhz: int = 2032, sms: int = 148):
 
 
 def roofline(wl, kern_ms, peak, peak_kind):
-    """The forward scan's roofline: the ALU ceiling binds (the fp32 and SFU floors
-    of its work lie well above the HBM floor of its bytes); the SFU and HBM
-    figures are reported beside it."""
+    """The forward scan's roofline.  Of its three floors the SFU one binds at
+    N = 16 (20 SFU operations per element at 30 per SM and clock, against 78
+    fp32 lane operations at 128, and 8-13 bytes per element of HBM traffic), so
+    `frac` is the SFU fraction; the fp32 and HBM fractions sit beside it."""
     alg = algorithmic_bytes(wl)
     ach_gbs = alg / (kern_ms * 1e-3) / 1e9
     elem_dirs = wl.elems * wl.K
     ops = elem_dirs * (wl.N * FWD_OPS_PER_STATE + FWD_OPS_PER_ELEM)
     sfu = elem_dirs * (wl.N * FWD_SFU_PER_STATE + FWD_SFU_PER_ELEM)
     fp32_peak, sfu_peak = alu_peaks()
-    ach = ops / (kern_ms * 1e-3) / 1e12
     ach_sfu = sfu / (kern_ms * 1e-3) / 1e12
-    return {"bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
-            "frac": ach / fp32_peak,
-            "peak_source": "fp32 lane ops: 148 SMs x 128 lanes x 2032 MHz",
-            "ops_per_launch": ops,
-            "sfu": {"achieved": ach_sfu, "peak": sfu_peak, "unit": "T ops/s", "frac": ach_sfu / sfu_peak,
-                    "ops_per_launch": sfu, "peak_source": "148 SMs x 32 ex2/clk x 2032 MHz"},
-            "hbm": {"achieved": ach_gbs, "peak": peak, "unit": "GB/s", "frac": ach_gbs / peak,
-                    "peak_source": f"{peak_kind} (copy bandwidth)",
-                    "algorithmic_bytes_per_launch": alg},
-            "time_floors_us": {"fp32": ops / (fp32_peak * 1e12) * 1e6,
-                               "sfu": sfu / (sfu_peak * 1e12) * 1e6,
-                               "hbm": alg / (peak * 1e9) * 1e6},
-            "traffic": ncu_traffic(wl)}
+    return {"bound": "alu", "achieved": round(ach_sfu, 3), "peak": round(sfu_peak, 3),
+            "unit": "Tops/s", "frac": round(ach_sfu / sfu_peak, 4),
+            "peak_source": f"SFU: 148 SMs x {SFU_LANES_PER_SM}/clk x 2032 MHz",
+            "fp32_frac": round(ops / (kern_ms * 1e-3) / 1e12 / fp32_peak, 4),
+            "hbm_gbs": round(ach_gbs, 1), "hbm_peak": peak,
+            "hbm_frac": round(ach_gbs / peak, 4), "traffic": ncu_traffic(wl)}
+
+
+def cpu_sample(wl, budget_s):
+    """The oracle on whole rows of the workload, over worker processes on all cores."""
+    v, rows, thr, dt = oracle_sample(wl, budget_s=budget_s)
+    return {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
+            "sample": f"{rows} whole rows (L={wl.L}, K={wl.K}) in {dt:.1f} s"}
+
+
+def measure_record(wl, steps, warmup, peak, peak_kind, e2e_steps, cpu_s, barrier=None):
+    """One workload's compact record: device-resident throughput, the kernels'
+    roofline, the end-to-end figure and (cpu_s > 0) the oracle's."""
+    import torch
+    r, ms, kern_ms, _ = measure_gpu(wl, steps, warmup, barrier)
+    e2e = r.e2e(e2e_steps, 3)
+    rf = roofline(wl, kern_ms, peak, peak_kind)
+    rec = {"value": round(wl.elems / (ms * 1e-3) / 1e9, 3), "ms_per_step": round(ms, 5),
+           "kernel_ms": round(kern_ms, 5), "launches_per_step": r.launches_per_step,
+           "roofline": {k: rf[k] for k in ("bound", "frac", "fp32_frac", "hbm_frac", "hbm_gbs",
+                                          "traffic")},
+           "e2e": {"value": round(e2e["value"], 3), "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                   "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]}}
+    del r
+    torch.cuda.empty_cache()
+    if cpu_s > 0:
+        c = cpu_sample(wl, cpu_s)
+        rec["cpu_baseline"] = {"value": round(c["value"], 5), "cores": c["cores"],
+                               "sample": c["sample"]}
+    return rec
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=HEADLINE.name,
                     choices=sorted(WORKLOADS) + [BWD_NAME, SS2D_BWD_NAME, WIN_BWD_NAME, DWCONV_NAME],
-                    help="forward workload to time (the backward pass: its own line only)")
-    ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
+                    help="workload to time (a non-default one prints its own line only)")
+    ap.add_argument("--all", action="store_true",
+                    help="also the fused Conv1D, windowed, decode, DWConv and backward lines")
+    ap.add_argument("--no-others", action="store_true", help="skip the other target workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -961,34 +993,21 @@ def main(argv=None):
     ss.load_library()
 
     peak, peak_kind = measured_peaks()
-    if args.workload == DWCONV_NAME:
-        r = measure_dwconv(args.steps, args.warmup, peak, peak_kind)
-        ms = max_over_ranks(r["ms_per_step"], world, "cuda")
-        if rank == 0:
-            line = {"metric": "DWConv3x3+SiLU Gelem/s (B·D·H·W)",
-                    "value": r["value"] * world, "unit": UNIT, "n_gpus": world,
-                    "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                    "dtype": "f32", "data": "synthetic (seeded NumPy PCG64)",
-                    "config": r["config"], "roofline": r["roofline"],
-                    "gpu_launches": args.steps}
-            print(json.dumps(line), flush=True)
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return 0
-    if args.workload in (BWD_NAME, SS2D_BWD_NAME, WIN_BWD_NAME):
-        # a backward pass alone, on one GPU per rank (replicas), device-resident inputs
-        if args.workload == BWD_NAME:
-            bwl = wk.MAMBA_LAYER
+    if args.workload in (DWCONV_NAME, BWD_NAME, SS2D_BWD_NAME, WIN_BWD_NAME):
+        # one of the further paths alone, on one GPU per rank (replicas), device-resident inputs
+        if args.workload == DWCONV_NAME:
+            r = measure_dwconv(args.steps, args.warmup, peak, peak_kind)
+            metric, elems = "DWConv3x3+SiLU Gelem/s (B·D·H·W)", 32 * 192 * 56 * 56
+        elif args.workload == BWD_NAME:
             r = measure_bwd(args.steps, args.warmup, peak, peak_kind)
+            metric, elems = "selective-scan backward Gelem/s (B·D·L)", wk.MAMBA_LAYER.elems
         else:
             bwl = wk.VMAMBA_SS2D if args.workload == SS2D_BWD_NAME else wk.LOCAL_WIN
             r = measure_ss2d_bwd(args.steps, args.warmup, peak, peak_kind, bwl, args.workload)
+            metric, elems = "selective-scan backward Gelem/s (B·D·L)", bwl.elems
         ms = max_over_ranks(r["ms_per_step"], world, "cuda")
         if rank == 0:
-            line = {"metric": "selective-scan backward Gelem/s (B·D·L)",
-                    "value": job_value(bwl.elems, world, ms), "unit": UNIT,
+            line = {"metric": metric, "value": job_value(elems, world, ms), "unit": UNIT,
                     "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                     "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                     "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded NumPy PCG64)",
@@ -999,68 +1018,57 @@ def main(argv=None):
             import torch.distributed as dist
             dist.destroy_process_group()
         return 0
+
     wl = WORKLOADS[args.workload]
     r, ms, kern_ms, clocks = measure_gpu(wl, args.steps, args.warmup, barrier)
     ms = max_over_ranks(ms, world, "cuda")
     value = job_value(wl.elems, world, ms)
     e2e = r.e2e(args.e2e_steps, 3)
     e2e["value"] *= world
+    e2e.pop("ms_per_step", None)
     copies = r.copies
     launches = r.launches_per_step * args.steps
     del r
     torch.cuda.empty_cache()
 
+    default = args.workload == HEADLINE.name
+    cpu_s = 0.0 if (args.no_cpu or rank != 0) else 8.0
     others = {}
-    if not args.no_others:
-        for owl in OTHERS:
-            if owl.name == wl.name:
-                continue
+    if default and not args.no_others:
+        for owl in TARGETS:
             try:
-                osteps = max(3, min(args.steps, 50))
-                r2, oms, okern, _ = measure_gpu(owl, osteps, max(3, min(args.warmup, 5)), barrier)
-                others[owl.name] = {
-                    "value": owl.elems / (oms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": oms,
-                    "kernel_launches_per_step": r2.launches_per_step,
-                    "roofline": roofline(owl, oms, peak, peak_kind),
-                    "config": config_of(owl, world, r2.copies)}
+                others[owl.name] = measure_record(owl, max(3, min(args.steps, 50)),
+                                                  max(3, min(args.warmup, 5)), peak, peak_kind,
+                                                  max(3, min(args.e2e_steps, 10)), cpu_s, barrier)
+            except Exception as e:  # noqa: BLE001 -- reported, not hidden
+                others[owl.name] = {"error": f"{type(e).__name__}: {e}"}
+    more = {}
+    if default and args.all:
+        for owl in EXTRA:
+            try:
+                r2, oms, okern, _ = measure_gpu(owl, max(3, min(args.steps, 50)), 3, barrier)
+                more[owl.name] = {"value": owl.elems / (oms * 1e-3) / 1e9, "ms_per_step": oms,
+                                  "launches_per_step": r2.launches_per_step,
+                                  "roofline": roofline(owl, okern, peak, peak_kind)}
                 del r2
                 torch.cuda.empty_cache()
             except Exception as e:  # noqa: BLE001 -- reported, not hidden
-                others[owl.name] = {"error": f"{type(e).__name__}: {e}"}
-        try:
-            others[DECODE_NAME] = measure_decode(256)
-        except Exception as e:  # noqa: BLE001 -- reported, not hidden
-            others[DECODE_NAME] = {"error": f"{type(e).__name__}: {e}"}
-        try:
-            others[DWCONV_NAME] = measure_dwconv(max(3, min(args.steps, 100)), 5, peak, peak_kind)
-        except Exception as e:  # noqa: BLE001 -- reported, not hidden
-            others[DWCONV_NAME] = {"error": f"{type(e).__name__}: {e}"}
-        try:
-            others[SS2D_BWD_NAME] = measure_ss2d_bwd(max(3, min(args.steps, 20)), 3, peak, peak_kind)
-            torch.cuda.empty_cache()
-        except Exception as e:  # noqa: BLE001 -- reported, not hidden
-            others[SS2D_BWD_NAME] = {"error": f"{type(e).__name__}: {e}"}
-        try:
-            others[WIN_BWD_NAME] = measure_ss2d_bwd(max(3, min(args.steps, 20)), 3, peak, peak_kind,
-                                                    wk.LOCAL_WIN, WIN_BWD_NAME)
-            torch.cuda.empty_cache()
-        except Exception as e:  # noqa: BLE001 -- reported, not hidden
-            others[WIN_BWD_NAME] = {"error": f"{type(e).__name__}: {e}"}
-        try:
-            others[BWD_NAME] = measure_bwd(max(3, min(args.steps, 30)), 3, peak, peak_kind)
-            torch.cuda.empty_cache()
-        except Exception as e:  # noqa: BLE001 -- reported, not hidden
-            others[BWD_NAME] = {"error": f"{type(e).__name__}: {e}"}
+                more[owl.name] = {"error": f"{type(e).__name__}: {e}"}
+        for name, fn in ((DECODE_NAME, lambda: measure_decode(256)),
+                         (DWCONV_NAME, lambda: measure_dwconv(50, 5, peak, peak_kind)),
+                         (SS2D_BWD_NAME, lambda: measure_ss2d_bwd(20, 3, peak, peak_kind)),
+                         (WIN_BWD_NAME, lambda: measure_ss2d_bwd(20, 3, peak, peak_kind,
+                                                                 wk.LOCAL_WIN, WIN_BWD_NAME)),
+                         (BWD_NAME, lambda: measure_bwd(30, 3, peak, peak_kind))):
+            try:
+                more[name] = fn()
+                torch.cuda.empty_cache()
+            except Exception as e:  # noqa: BLE001 -- reported, not hidden
+                more[name] = {"error": f"{type(e).__name__}: {e}"}
 
     cpu = None
-    if rank == 0 and not args.no_cpu:
-        v, rows, thr, dt = oracle_sample(wl, budget_s=12.0)
-        v1, rows1, _, dt1 = oracle_sample(wl, budget_s=5.0, processes=1)
-        cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
-               "sample": f"{rows} whole (batch, channel) rows of the workload (L={wl.L}) "
-                         f"in {dt:.1f} s, worker processes over rows; host CPU {cpu_model()}",
-               "single_core": {"value": v1, "unit": UNIT, "cores": 1,
-                               "sample": f"{rows1} rows in {dt1:.1f} s on one thread"}}
+    if cpu_s > 0:
+        cpu = cpu_sample(wl, 12.0)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -1070,7 +1078,12 @@ def main(argv=None):
                 "config": config_of(wl, world, copies),
                 "roofline": roofline(wl, kern_ms, peak, peak_kind),
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-                "clocks": clocks, "kernel_ms": kern_ms, "workloads": others}
+                "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+                "kernel_ms": kern_ms}
+        if others:
+            line["workloads"] = others
+        if more:
+            line["more"] = more
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -162,6 +162,7 @@ struct Scan1d {
         auto kern = (a.zoh || a.conv) ? k_scan1d<C, false, true> : k_scan1d<C, false, false>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
             return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
+        const bool plain = !a.zoh && !a.conv;
 
         Scan1dParams p{};
         p.dim = a.dim;
@@ -197,7 +198,15 @@ struct Scan1d {
             p.J = 1;
             p.jbase = 0;
             p.pass = 0;
-            kern<<<dim3(cblocks, bgs, 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, mu, p);
+            if (plain) {
+                auto kd = k_scan1d_direct<C>;
+                if (cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+                    cudaSuccess)
+                    return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
+                kd<<<dim3(cblocks, bgs, 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, p);
+            } else {
+                kern<<<dim3(cblocks, bgs, 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, mu, p);
+            }
             return check_launch("scan");
         }
         // chunked path: L-chunks of Lc steps (a multiple of T)
@@ -431,17 +440,18 @@ template <typename IO> struct Pick1d<IO, 32> { using C = ssk::Cfg1<IO, 32, 4, 4,
 template <typename IO> struct Pick1d<IO, 64> { using C = ssk::Cfg1<IO, 64, 8, 4, 3, 1, 1>; };
 
 // L-chunks to use: 1 (direct) when the direct path gives every SM sub-partition
-// at least two warps; otherwise enough chunks for about eight warps each (the
+// at least two warps; otherwise enough chunks for about twelve warps each (the
 // chunked path rescans all but the first chunk, so it only pays off when the
 // direct path would leave the sub-partitions short of warps; on the B300 the
-// 1 x 5120 x 131072 scan is fastest at 8-12 chunks).
+// 1 x 5120 x 131072 scan measured 5.52 ms at 12 chunks, 5.61 at 10, 5.62 at 8,
+// 5.84 at 14 and 16, 6.04 at 4).
 template <class C>
 int choose_chunks(const ScanArgs &a) {
     const int64_t rows = a.batch * a.dim;
     const int64_t threads = rows * C::R / C::CL;
     const int64_t one_per_smsp = (int64_t)num_sms() * 4 * 32;
     if (threads >= 2 * one_per_smsp) return 1;
-    int64_t J = (8 * one_per_smsp + threads - 1) / threads;
+    int64_t J = (12 * one_per_smsp + threads - 1) / threads;
     const int64_t maxJ = a.L / (4 * C::T);  // keep L-chunks at least 4 T-chunks long
     if (J > maxJ) J = maxJ;
     return J < 2 ? 1 : (int)J;

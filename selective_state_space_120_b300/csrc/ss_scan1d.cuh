@@ -440,11 +440,17 @@ __device__ __forceinline__ void stage_step(StepRegs<C> &r, const float4 *const (
 
 // scan_chunk_cl with a one-step-pair software pipeline: the loads and
 // exponentials of step pair tp+1 are issued before the state updates of tp, so
-// their latency overlaps the dependent FMA chain.
+// their latency overlaps the dependent FMA chain.  With DEFER the per-step
+// partial readouts of the whole chunk stay in registers and are combined
+// (butterflies, then emit) after the chunk's last step: the step loop then
+// holds no shuffle chains, and the T/R butterflies of a chunk are independent
+// of one another -- faster when the kernel may use the registers it needs
+// (the plain single-direction scan); otherwise (DEFER false) every R-step block
+// is combined as soon as its partials are complete.
 // ZOH selects the zero-order-hold input matrix at compile time (iA = 1/A per
 // state); a runtime branch inside the unrolled step loop costs the scheduler
 // its freedom to interleave across states and step pairs.
-template <class C, bool DO_Y, bool ZOH = false, class Emit>
+template <class C, bool DO_Y, bool ZOH = false, bool DEFER = false, class Emit>
 __device__ __forceinline__ void scan_chunk_pipe(const float4 *const (&dxrow)[C::CL], const float *bc,
                                                 int g, float (&h)[C::CL][C::NPT],
                                                 const float2 (&A2p)[C::CL][C::NPT], Emit &&emit,
@@ -452,14 +458,15 @@ __device__ __forceinline__ void scan_chunk_pipe(const float4 *const (&dxrow)[C::
     constexpr int R = C::R, NPT = C::NPT, CL = C::CL;
     constexpr int BS = R >= 2 ? R : 2;  // steps per readout block
     constexpr int PPB = BS / 2;
+    constexpr int VN = DEFER ? C::T : BS;
     StepRegs<C> cur, nxt;
     stage_step<C, DO_Y, ZOH>(nxt, dxrow, bc, g, 0, A2p, iA);
-    float v[CL][BS];
+    float v[CL][VN];  // partial readouts: of the chunk (DEFER) or of one block
 #pragma unroll
     for (int tp = 0; tp < C::TP; ++tp) {
         cur = nxt;
         if (tp + 1 < C::TP) stage_step<C, DO_Y, ZOH>(nxt, dxrow, bc, g, tp + 1, A2p, iA);
-        const int pp = tp % PPB;
+        const int vi = DEFER ? 2 * tp : 2 * (tp % PPB);
 #pragma unroll
         for (int c = 0; c < CL; ++c) {
             // written phase by phase (every state's first step, then every
@@ -478,12 +485,12 @@ __device__ __forceinline__ void scan_chunk_pipe(const float4 *const (&dxrow)[C::
                     y2[j & 1] = __ffma2_rn(make_float2(cur.Cv[2 * j], cur.Cv[2 * j + 1]),
                                            make_float2(hs0[j], h[c][j]), y2[j & 1]);
                 if constexpr (NPT > 1) y2[0] = __fadd2_rn(y2[0], y2[1]);
-                v[c][2 * pp] = y2[0].x;
-                v[c][2 * pp + 1] = y2[0].y;
+                v[c][vi] = y2[0].x;
+                v[c][vi + 1] = y2[0].y;
             }
         }
-        if constexpr (DO_Y) {
-            if (pp == PPB - 1) {
+        if constexpr (DO_Y && !DEFER) {
+            if (tp % PPB == PPB - 1) {
                 const int blk = tp / PPB;
 #pragma unroll
                 for (int c = 0; c < CL; ++c) {
@@ -494,6 +501,24 @@ __device__ __forceinline__ void scan_chunk_pipe(const float4 *const (&dxrow)[C::
                         emit(c, v[c][0], blk * 2);
                         emit(c, v[c][1], blk * 2 + 1);
                     }
+                }
+            }
+        }
+    }
+    if constexpr (DO_Y && DEFER) {
+#pragma unroll
+        for (int blk = 0; blk < C::T / BS; ++blk) {
+#pragma unroll
+            for (int c = 0; c < CL; ++c) {
+                if constexpr (R >= 2) {
+                    float w[BS];
+#pragma unroll
+                    for (int i = 0; i < BS; ++i) w[i] = v[c][blk * BS + i];
+                    const float y = transpose_reduce<R, C::CPW>(w, g);
+                    emit(c, y, blk * R + g);
+                } else {
+                    emit(c, v[c][blk * 2], blk * 2);
+                    emit(c, v[c][blk * 2 + 1], blk * 2 + 1);
                 }
             }
         }
@@ -623,12 +648,13 @@ __device__ __forceinline__ void store_partials(const Scan1dParams &p, const Merg
 // EXT = true compiles the optional paths of a single direction, the
 // zero-order hold and the fused Conv1D; the plain instantiations carry none of
 // their code, which keeps the default scans' registers and schedule.
-template <class C, bool MULTI, bool EXT = false>
-__global__ void __launch_bounds__(C::THREADS)
-k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
-         const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
-         const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_u2,
-         const Scan1dParams p_in) {
+// The body of the scan kernels; DEFER selects the chunk-deferred readout
+// combination of scan_chunk_pipe.
+template <class C, bool MULTI, bool EXT, bool DEFER>
+__device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUtensorMap &tm_dl,
+                                            const CUtensorMap &tm_z, const CUtensorMap &tm_B,
+                                            const CUtensorMap &tm_C, const CUtensorMap &tm_u2,
+                                            const Scan1dParams &p_in) {
     using IO = typename C::IO;
     Scan1dParams p = p_in;
     if constexpr (!MULTI) {
@@ -919,8 +945,8 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
                 if (do_y) scan_chunk_pipe<C, true, true>(dxrows, bc, g, h, A2p, emit, zoh_iA);
                 else scan_chunk_pipe<C, false, true>(dxrows, bc, g, h, A2p, none, zoh_iA);
             } else {
-                if (do_y) scan_chunk_pipe<C, true>(dxrows, bc, g, h, A2p, emit);
-                else scan_chunk_pipe<C, false>(dxrows, bc, g, h, A2p, none);
+                if (do_y) scan_chunk_pipe<C, true, false, DEFER>(dxrows, bc, g, h, A2p, emit);
+                else scan_chunk_pipe<C, false, false, DEFER>(dxrows, bc, g, h, A2p, none);
             }
         } else {
             if (do_y) scan_chunk_cl<C, true>(dxrows, bc, g, h, A2p, emit);
@@ -978,6 +1004,33 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
             for (int j = 0; j < NPT; ++j) p.hend[(rows[c] * p.J + jc) * N + g * NPT + j] = h[c][j];
         }
     }
+}
+
+// The scan kernel of every path but the direct single-direction one: the
+// compiler's default register target; readouts combined block by block.
+template <class C, bool MULTI, bool EXT = false>
+__global__ void __launch_bounds__(C::THREADS)
+k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
+         const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
+         const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_u2,
+         const Scan1dParams p) {
+    scan1d_body<C, MULTI, EXT, false>(tm_u, tm_dl, tm_z, tm_B, tm_C, tm_u2, p);
+}
+
+// The direct single-direction scan (one pass over the whole sequence, no
+// options).  Its grid is one CTA per CB channels, a few per SM -- all the
+// parallelism a scan has -- so warps are few and each must hide its own
+// latencies: it may take as many registers as it wants (at least one CTA per
+// SM), keeps the chunk's partial readouts in them and combines them after the
+// chunk (DEFER).  On the chunked path, whose grids fill the SMs several times
+// over, the same choice measured slower (a lower CTA residency), so that path
+// keeps k_scan1d.
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+k_scan1d_direct(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
+                const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
+                const __grid_constant__ CUtensorMap tm_C, const Scan1dParams p) {
+    scan1d_body<C, false, false, true>(tm_u, tm_dl, tm_z, tm_B, tm_C, tm_u, p);
 }
 
 // Final merge of a four-direction call scanned as two pairs: out = (row-pair
