@@ -185,8 +185,14 @@ ss_status ss_selective_scan_fwd_opts(int64_t batch, int64_t dim, int64_t seqlen,
  * When rows are 16-byte aligned (seqlen * element size % 16 == 0) the two
  * directions run as two TMA-staged scans that merge through the workspace, an
  * fp32 [batch, dim, seqlen] accumulator (first direction stores, second adds,
- * gates and writes out: deterministic).  Otherwise the call merges on chip and
- * needs no workspace.
+ * gates and writes out: deterministic).
+ * Otherwise the workspace is optional.  Given one of at least the size the
+ * query reports (which assumes ngroups = 1: the re-pitched B and C grow with
+ * ngroups), the call copies u (forward and reversed), delta, B and C into rows
+ * padded to 16-byte multiples in it, scans both directions side by side as TMA
+ * tiles of those copies into two fp32 slices, and merges the slices by
+ * position in one more launch.  Without a workspace (NULL), or with a smaller
+ * one, the call merges on chip.
  */
 ss_status ss_bidir_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int ngroups,
                             ss_dtype io, const void *u, const void *delta, const float *A,

@@ -376,7 +376,15 @@ ss_status ss_bidir_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dsta
     a.K = 2;
     a.orders[0] = ORD_ROW;
     a.orders[1] = ORD_ROW_REV;
-    if ((st = check_workspace(fn, multidir_workspace_bytes(a), workspace, workspace_bytes))) return st;
+    // Rows that are not 16-byte aligned: a workspace is optional -- with one of
+    // at least the re-pitched path's size (which grows with ngroups) the inputs
+    // are re-pitched into it, otherwise the call merges on chip.
+    if (!scan1d_uses_tma(a)) {
+        if (workspace && !aligned16(workspace))
+            return fail(SS_ERR_ALIGNMENT, "%s: workspace is not 16-byte aligned", fn);
+    } else if ((st = check_workspace(fn, multidir_workspace_bytes(a), workspace, workspace_bytes))) {
+        return st;
+    }
     if ((st = check_ws_overlap(fn, a))) return st;
     return launch_multidir(a);
 }

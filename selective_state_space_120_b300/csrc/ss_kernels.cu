@@ -39,15 +39,16 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D map over a [rows, cols] row-major tensor; boxes of [box_rows, box_cols]
-// with 64-byte rows and the 64-byte swizzle.  Out-of-range boxes read zeros.
+// 2-D map over a [rows, cols] row-major tensor with a row pitch of `pitch`
+// elements (0: cols); boxes of [box_rows, box_cols] with 64-byte rows and the
+// 64-byte swizzle.  Out-of-range boxes read zeros.
 ss_status make_map(CUtensorMap *m, const void *base, int io, uint64_t cols, uint64_t rows,
-                   uint32_t box_cols, uint32_t box_rows) {
+                   uint32_t box_cols, uint32_t box_rows, uint64_t pitch = 0) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(SS_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const uint64_t es = (io == SS_BF16) ? 2 : 4;
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * es};
+    cuuint64_t strides[1] = {(pitch ? pitch : cols) * es};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(m, io == SS_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
@@ -89,6 +90,23 @@ bool order_reversed(int o) {
 constexpr int kBaseOrder[4] = {ORD_ROW, ORD_COL, ORD_WIN, ORD_WIN_COL};
 
 size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+// Row length rounded up to a multiple of 16 bytes (the pitch of re-pitched copies).
+int64_t padded_len(const ScanArgs &a) {
+    const int64_t vpv = a.io == SS_BF16 ? 8 : 4;
+    return (a.L + vpv - 1) / vpv * vpv;
+}
+
+// Workspace of a bidirectional call over rows that are not 16-byte aligned:
+// the two directions' fp32 terms [2, rows, Lp], u forward and reversed [rows,
+// Lp], Delta [2 rows, Lp], B and C [batch*2*G*N, Lp].
+size_t bidir_padded_bytes(const ScanArgs &a) {
+    const int64_t rows = a.batch * a.dim, Lp = padded_len(a);
+    const size_t es = a.io == SS_BF16 ? 2 : 4;
+    const int64_t bcrows = a.batch * 2 * a.G * a.N;
+    return align256((size_t)2 * rows * Lp * sizeof(float)) + 2 * align256((size_t)rows * Lp * es) +
+           align256((size_t)2 * rows * Lp * es) + 2 * align256((size_t)bcrows * Lp * es);
+}
 
 // Workspace of a call over directions of any order: the fp32 accumulators by
 // step [K][rows][L], then one permuted copy of u per base traversal in use.
@@ -167,6 +185,7 @@ struct Scan1d {
         Scan1dParams p{};
         p.dim = a.dim;
         p.L = a.L;
+        p.pitch = a.L;
         p.G = a.G;
         p.dpg = (int)(a.dim / a.G);
         p.K = 1;
@@ -252,6 +271,7 @@ struct Scan1d {
         Scan1dParams p{};
         p.dim = a.dim;
         p.L = a.L;
+        p.pitch = a.L;
         p.G = a.G;
         p.dpg = (int)(a.dim / a.G);
         p.Lc = a.L;
@@ -330,6 +350,91 @@ struct Scan1d {
         return check_launch("merge");
     }
 
+    // Bidirectional call over rows that are not 16-byte aligned: the inputs are
+    // re-pitched into the workspace (u twice, forward and reversed; Delta, B,
+    // C) so that both directions read TMA tiles in their own step order; they
+    // scan side by side, each storing y_k + D_k*u by scan step into an fp32
+    // slice, and one more launch sums the slices by position and gates.
+    static ss_status run_bidir_padded(const ScanArgs &a) {
+        using namespace ssk;
+        using IO = typename C::IO;
+        const int io = a.io;
+        const int64_t rows = a.batch * a.dim;
+        const int64_t Lp = padded_len(a);
+        const size_t es = io == SS_BF16 ? 2 : 4;
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(a.stream);
+        uint8_t *ws = reinterpret_cast<uint8_t *>(a.ws);
+        const int64_t bcrows = a.batch * 2 * a.G * C::N;
+        float *s0 = reinterpret_cast<float *>(ws);
+        float *s1 = s0 + rows * Lp;
+        uint8_t *cp = ws + align256((size_t)2 * rows * Lp * sizeof(float));
+        void *uf = cp;
+        void *ur = cp + align256((size_t)rows * Lp * es);
+        void *dlp = reinterpret_cast<uint8_t *>(ur) + align256((size_t)rows * Lp * es);
+        void *bp = reinterpret_cast<uint8_t *>(dlp) + align256((size_t)2 * rows * Lp * es);
+        void *cpp = reinterpret_cast<uint8_t *>(bp) + align256((size_t)bcrows * Lp * es);
+        RepitchJobs jobs{};
+        jobs.L = a.L;
+        jobs.Lp = Lp;
+        jobs.n = 5;
+        jobs.job[0] = {a.u, uf, rows, 0};
+        jobs.job[1] = {a.u, ur, rows, 1};
+        jobs.job[2] = {a.delta, dlp, 2 * rows, 0};
+        jobs.job[3] = {a.B, bp, bcrows, 0};
+        jobs.job[4] = {a.C, cpp, bcrows, 0};
+        ss_status st;
+        {
+            const int64_t vmax = 2 * rows * (Lp * (int64_t)es / 16);
+            const unsigned bx = (unsigned)std::min<int64_t>((vmax + 255) / 256, (int64_t)num_sms() * 16);
+            k_repitch<IO><<<dim3(bx, 5), 256, 0, s>>>(jobs);
+            if ((st = check_launch("re-pitch"))) return st;
+        }
+        CUtensorMap mu, mur, md, mb, mc;
+        if ((st = make_map(&mu, uf, io, a.L, rows, C::T, C::CB, Lp))) return st;
+        if ((st = make_map(&mur, ur, io, a.L, rows, C::T, C::CB, Lp))) return st;
+        if ((st = make_map(&md, dlp, io, a.L, (uint64_t)rows * 2, C::T, C::CB, Lp))) return st;
+        if ((st = make_map(&mb, bp, io, a.L, (uint64_t)bcrows, C::T, C::N, Lp))) return st;
+        if ((st = make_map(&mc, cpp, io, a.L, (uint64_t)bcrows, C::T, C::N, Lp))) return st;
+        auto kern = k_scan1d<C, true>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
+        Scan1dParams p{};
+        p.dim = a.dim;
+        p.L = a.L;
+        p.pitch = Lp;
+        p.G = a.G;
+        p.dpg = (int)(a.dim / a.G);
+        p.Lc = a.L;
+        p.J = 1;
+        p.jbase = 0;
+        p.pass = 0;
+        p.K = 2;
+        p.u_g = a.u;
+        p.A = a.A;
+        p.D = a.D;
+        p.bias = a.bias;
+        p.softplus = a.softplus;
+        p.has_z = 0;
+        p.out = a.out;
+        p.last_state = a.last_state;
+        p.nz = 2;
+        p.k0 = 0;
+        for (int d = 0; d < 2; ++d) {
+            p.orders_z[d] = ORD_ROW;  // each over its own copy of u, in its step order
+            p.modes_z[d] = OUT_STEP;
+            p.accs_z[d] = d == 0 ? s0 : s1;
+        }
+        const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);
+        const unsigned bgs = (unsigned)(a.batch * a.G);
+        kern<<<dim3(cblocks, bgs, 2), C::THREADS, C::SMEM, s>>>(mu, md, mu, mb, mc, mur, p);
+        if ((st = check_launch("direction pair scan"))) return st;
+        const int64_t groups = rows * ((a.L + 3) / 4);
+        const unsigned mblocks = (unsigned)std::min<int64_t>((groups + 255) / 256, (int64_t)num_sms() * 32);
+        k_merge_bidir<IO><<<mblocks, 256, 0, s>>>(s0, s1, reinterpret_cast<const IO *>(a.z),
+                                                  reinterpret_cast<IO *>(a.out), rows, a.L, Lp);
+        return check_launch("bidirectional merge");
+    }
+
     // K directions of any order: each launch stores its direction's y_k + D_k*u
     // by scan step into its own fp32 accumulator; one merge inverts the
     // traversals and sums by position.
@@ -367,6 +472,7 @@ struct Scan1d {
         Scan1dParams p{};
         p.dim = a.dim;
         p.L = a.L;
+        p.pitch = a.L;
         p.G = a.G;
         p.dpg = (int)(a.dim / a.G);
         p.Lc = a.L;
@@ -475,6 +581,26 @@ template <typename IO, int N>
 ss_status dispatch_dirs(const ScanArgs &a) {
     using C = typename Pick1d<IO, N>::C;
     return Scan1d<C>::run_dirs(a);
+}
+
+template <typename IO, int N>
+ss_status dispatch_bidir_padded(const ScanArgs &a) {
+    using C = typename Pick1d<IO, N>::C;
+    return Scan1d<C>::run_bidir_padded(a);
+}
+
+template <typename IO>
+ss_status dispatch_bidir_padded_n(const ScanArgs &a) {
+    switch (a.N) {
+    case 1: return dispatch_bidir_padded<IO, 1>(a);
+    case 2: return dispatch_bidir_padded<IO, 2>(a);
+    case 4: return dispatch_bidir_padded<IO, 4>(a);
+    case 8: return dispatch_bidir_padded<IO, 8>(a);
+    case 16: return dispatch_bidir_padded<IO, 16>(a);
+    case 32: return dispatch_bidir_padded<IO, 32>(a);
+    case 64: return dispatch_bidir_padded<IO, 64>(a);
+    default: return fail(SS_ERR_UNSUPPORTED, "dstate %d is not one of 1,2,4,8,16,32,64", a.N);
+    }
 }
 
 template <typename IO, int N>
@@ -651,7 +777,16 @@ ss_status launch_scan1d(const ScanArgs &a) {
     return a.io == SS_BF16 ? dispatch1d_n<__nv_bfloat16>(a) : dispatch1d_n<float>(a);
 }
 
+// Bidirectional calls over rows that are not 16-byte aligned re-pitch their
+// inputs when the row counts fit the TMA maps (else they merge on chip).
+bool bidir_padded_ok(const ScanArgs &a) {
+    if (a.K != 2 || scan1d_uses_tma(a)) return false;
+    const int64_t rows = a.batch * a.dim;
+    return 2 * rows < (1ll << 31) && a.batch * 2 * a.G * a.N < (1ll << 31) && a.L < (1ll << 30);
+}
+
 size_t multidir_workspace_bytes(const ScanArgs &a) {
+    if (bidir_padded_ok(a)) return bidir_padded_bytes(a);
     if (!scan1d_uses_tma(a)) return 0;  // rows not 16-byte aligned: on-chip merge path
     // one fp32 accumulator; SS2D scans two pairs of directions side by side into
     // two, and reads u of its column directions from a transposed copy
@@ -669,6 +804,13 @@ ss_status launch_steps(const ScanArgs &a) {
 }
 
 ss_status launch_multidir(const ScanArgs &a) {
+    if (bidir_padded_ok(a)) {
+        // re-pitched TMA path when the caller gave the workspace, else on chip
+        if (a.ws && a.ws_bytes >= bidir_padded_bytes(a))
+            return a.io == SS_BF16 ? dispatch_bidir_padded_n<__nv_bfloat16>(a)
+                                   : dispatch_bidir_padded_n<float>(a);
+        return a.io == SS_BF16 ? dispatch_multi<__nv_bfloat16>(a) : dispatch_multi<float>(a);
+    }
     if (multidir_workspace_bytes(a) > 0)
         return a.io == SS_BF16 ? dispatch_dirs_n<__nv_bfloat16>(a) : dispatch_dirs_n<float>(a);
     return a.io == SS_BF16 ? dispatch_multi<__nv_bfloat16>(a) : dispatch_multi<float>(a);

@@ -124,6 +124,7 @@ struct Scan1dParams {
     int order;    // 0: u tiles in step order; 2: the same, read back to front
     int mode;     // OUT_*
     float *acc;   // [batch*dim, L] fp32 merge accumulator by position (modes 1-3)
+    int64_t pitch;  // row pitch (elements) of the accumulators; L unless the inputs are re-pitched
     // Multi-direction launches may scan several directions side by side:
     // blockIdx.z = d selects direction k0 + d with its own order, mode and
     // accumulator (entries [0, nz)).
@@ -555,7 +556,7 @@ struct MergeRegs {
             qq[m] = task % QG;
             chr[m] = warp * C::CHW + rr;
             const int dgr = cblk * C::CB + chr[m];
-            rowL[m] = (task < C::CHW * QG && dgr < p.dpg) ? (row0 + dgr) * p.L : -1;
+            rowL[m] = (task < C::CHW * QG && dgr < p.dpg) ? (row0 + dgr) * p.pitch : -1;
         }
     }
 };
@@ -1187,6 +1188,137 @@ __global__ void __launch_bounds__(256) k_permute_order(const IO *__restrict__ u,
     ow.start(order, H, W, win, L, s);
     const int64_t pos = ow.pos_next();
     for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) out[row * L + s] = u[row * L + pos];
+}
+
+// Rows whose length is not a multiple of 16 bytes cannot be TMA tiles.  Such
+// inputs are copied once per call into padded rows of pitch Lp (a multiple of
+// 16 bytes) in the workspace; a job may also reverse its rows (the reversed
+// direction of a bidirectional scan then reads u in its own step order).
+// dst[r][c] = src[r][rev ? L-1-c : c] for c < L, zero for L <= c < Lp.
+struct RepitchJob {
+    const void *src;
+    void *dst;
+    int64_t rows;
+    int rev;
+};
+struct RepitchJobs {
+    RepitchJob job[6];
+    int n;
+    int64_t L, Lp;
+};
+// 128 bits of a 256-bit window (four 64-bit words, low first) starting at bit
+// 8 * sb (sb a multiple of the element size, below 16).
+__device__ __forceinline__ uint4 window_bits(const uint64_t (&q)[4], int sb) {
+    const int j = sb >> 3, b = (sb & 7) * 8;
+    const uint64_t a0 = j ? q[1] : q[0], a1 = j ? q[2] : q[1], a2 = j ? q[3] : q[2];
+    const uint64_t lo = b ? (a0 >> b) | (a1 << (64 - b)) : a0;
+    const uint64_t hi = b ? (a1 >> b) | (a2 << (64 - b)) : a1;
+    return make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+}
+
+// One thread writes one 16-byte vector of a padded row (8 bf16 or 4 fp32);
+// blockIdx.y selects the job.  The source span of the vector (unaligned in
+// general) is read as the two aligned 16-byte vectors that cover it and
+// shifted into place; vectors at the ends of the tensor, where that window
+// would leave it, are read element by element.
+template <typename IO>
+__global__ void __launch_bounds__(256) k_repitch(const RepitchJobs jobs) {
+    constexpr int ES = sizeof(IO), VPV = 16 / ES;
+    const RepitchJob jb = jobs.job[blockIdx.y];
+    const int64_t L = jobs.L;
+    const int64_t vpr = jobs.Lp / VPV;  // vectors per padded row
+    const int64_t nvec = jb.rows * vpr;
+    const int64_t nel = jb.rows * L;    // source elements
+    const IO *src = reinterpret_cast<const IO *>(jb.src);
+    const uint4 *src4 = reinterpret_cast<const uint4 *>(jb.src);
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
+         v += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = v / vpr;
+        const int64_t c0 = (v - r * vpr) * VPV;
+        const int nv = (int)min((int64_t)VPV, max((int64_t)0, L - c0));  // valid elements
+        uint4 out = make_uint4(0, 0, 0, 0);
+        if (nv > 0) {
+            // source elements of the vector, in output order: e0 + e (forward) or
+            // e0 + VPV-1 - e (reversed); e0 = first element of the window
+            const int64_t e0 = jb.rev ? r * L + L - c0 - VPV : r * L + c0;
+            const int64_t w0 = e0 >= 0 ? e0 / VPV : -1;
+            if (w0 >= 0 && (w0 + 2) * VPV <= nel) {
+                const uint4 va = src4[w0], vb = src4[w0 + 1];
+                const uint64_t q[4] = {(uint64_t)va.x | ((uint64_t)va.y << 32),
+                                       (uint64_t)va.z | ((uint64_t)va.w << 32),
+                                       (uint64_t)vb.x | ((uint64_t)vb.y << 32),
+                                       (uint64_t)vb.z | ((uint64_t)vb.w << 32)};
+                out = window_bits(q, (int)(e0 - w0 * VPV) * ES);
+                if (jb.rev) {  // reverse the element order
+                    if constexpr (ES == 2)
+                        out = make_uint4(__byte_perm(out.w, 0, 0x1032), __byte_perm(out.z, 0, 0x1032),
+                                         __byte_perm(out.y, 0, 0x1032), __byte_perm(out.x, 0, 0x1032));
+                    else
+                        out = make_uint4(out.w, out.z, out.y, out.x);
+                }
+            } else {
+                typename IOT<IO>::Raw w[VPV];
+#pragma unroll
+                for (int e = 0; e < VPV; ++e) {
+                    const int64_t c = c0 + e;
+                    w[e] = 0;
+                    if (c < L) w[e] = IOT<IO>::load_raw(src + r * L + (jb.rev ? L - 1 - c : c));
+                }
+                if constexpr (ES == 2)
+                    out = make_uint4((uint32_t)w[0] | ((uint32_t)w[1] << 16), (uint32_t)w[2] | ((uint32_t)w[3] << 16),
+                                     (uint32_t)w[4] | ((uint32_t)w[5] << 16), (uint32_t)w[6] | ((uint32_t)w[7] << 16));
+                else
+                    out = make_uint4(__float_as_uint(w[0]), __float_as_uint(w[1]), __float_as_uint(w[2]),
+                                     __float_as_uint(w[3]));
+            }
+            if (nv < VPV) {  // zero the columns past the row's end
+                uint32_t o[4] = {out.x, out.y, out.z, out.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int lo_e = i * 4 / ES;  // first element held by word i
+                    if (ES == 2) {
+                        if (lo_e >= nv) o[i] = 0;
+                        else if (lo_e + 1 >= nv) o[i] &= 0xffffu;
+                    } else if (lo_e >= nv) {
+                        o[i] = 0;
+                    }
+                }
+                out = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+        reinterpret_cast<uint4 *>(jb.dst)[v] = out;
+    }
+}
+
+// Final merge of a bidirectional call over re-pitched rows: the forward and the
+// reversed direction stored y_k + D_k*u by scan step into fp32 slices of pitch
+// Lp (s0 by position, s1 by position L-1-step); out[r][p] = (s0[r][p] +
+// s1[r][L-1-p]) * SiLU(z[r][p]) in the I/O type, rows of the caller's pitch L.
+// A thread takes four consecutive positions of a row: one 16-byte load of s0,
+// four of s1 (read backwards) and of z, four stores.
+template <typename IO>
+__global__ void __launch_bounds__(256) k_merge_bidir(const float *__restrict__ s0,
+                                                     const float *__restrict__ s1,
+                                                     const IO *__restrict__ z, IO *__restrict__ out,
+                                                     int64_t rows, int64_t L, int64_t Lp) {
+    const int64_t qpr = (L + 3) / 4;  // groups of four positions per row
+    const int64_t n = rows * qpr;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / qpr;
+        const int64_t p0 = (i - r * qpr) * 4;
+        const float4 a = *reinterpret_cast<const float4 *>(s0 + r * Lp + p0);
+        const float av[4] = {a.x, a.y, a.z, a.w};
+        const float *b = s1 + r * Lp + (L - 1);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t p = p0 + j;
+            if (p >= L) break;
+            float y = av[j] + b[-p];
+            if (z) y *= silu(IOT<IO>::load(z + r * L + p));
+            out[r * L + p] = IOT<IO>::from_f(y);
+        }
+    }
 }
 
 // Chains the L-chunks: carry[j] = state entering chunk j, from the chunk-local

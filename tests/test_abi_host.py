@@ -193,9 +193,16 @@ def test_debug_flags_reject_unknown_bits(lib):
 
 
 def test_workspace_sizing_is_host_only(lib):
-    # multi-direction calls: unaligned rows merge on chip (no workspace); aligned
-    # rows merge through an fp32 [batch, dim, L] accumulator
-    assert b.workspace_bytes(b.SS_KIND_BIDIR, 128, 768, 197, 16) == 0
+    # multi-direction calls: unaligned bidirectional rows are re-pitched (with
+    # ngroups = 1: both directions' terms, fp32 [2, rows, Lp], u forward and reversed, Delta of
+    # both directions [rows, Lp] each in the I/O type, B and C [batch*2*N, Lp];
+    # Lp = L rounded up to 16 bytes, the larger of the two dtypes: float32);
+    # aligned rows merge through an fp32 [batch, dim, L] accumulator
+    rows, Lp = 128 * 768, 200
+    a256 = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    want = (a256(2 * rows * Lp * 4) + 2 * a256(rows * Lp * 4) + a256(2 * rows * Lp * 4) +
+            2 * a256(128 * 2 * 16 * Lp * 4))
+    assert b.workspace_bytes(b.SS_KIND_BIDIR, 128, 768, 197, 16) == want
     # (SS2D: two accumulators and a transposed copy of u for the column directions)
     assert b.workspace_bytes(b.SS_KIND_CROSS2D, 32, 192, 3136, 16) == 3 * 32 * 192 * 3136 * 4
     assert b.workspace_bytes(b.SS_KIND_BIDIR, 2, 24, 256, 16) == 2 * 24 * 256 * 4

@@ -334,6 +334,62 @@ def test_bidirectional_groups_dstate(oracle):
     _check(oracle, sc.workload("bi_g", 2, 32, 50, N=8, G=2, K=2))
 
 
+@pytest.mark.parametrize("L", [7, 197])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bidirectional_unaligned_rows_without_workspace(oracle, L, io):
+    """Rows that are not 16-byte aligned with no workspace given: the call
+    merges on chip instead of re-pitching its inputs (same results)."""
+    import ctypes
+    import torch
+    from selective_state_space_120_b300 import _binding as b
+    lib = b.load()
+    wl = sc.workload(f"bi_nows{L}", 2, 24, L, K=2, io=io)
+    inp = wk.make_inputs(wl, seed=0)
+    t = sc.device_inputs(inp)
+    out = torch.empty_like(t["u"])
+    last = torch.empty(wl.batch, 2, wl.dim, wl.N, dtype=torch.float32, device="cuda")
+    p = lambda x: None if x is None else x.data_ptr()  # noqa: E731
+    b.check(lib.ss_bidir_scan_fwd(wl.batch, wl.dim, L, wl.N, wl.G, b.SS_BF16 if io == "bf16" else b.SS_F32,
+                                  p(t["u"]), p(t["delta"]), p(t["A"]), p(t["B"]), p(t["C"]), p(t["D"]),
+                                  p(t["z"]), p(t["delta_bias"]), 1, p(out), p(last), None, 0,
+                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)))
+    torch.cuda.synchronize()
+    ref, ref_last = sc.oracle_run(oracle, inp)
+    sc.assert_close(sc.from_torch(out), ref, io)
+    sc.assert_close(last.cpu().numpy().astype(np.float64), ref_last, io, "last_state")
+
+
+@pytest.mark.parametrize("L", [1, 5, 9, 197, 1001])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bidirectional_repitched_rows(oracle, L, io):
+    """Rows that are not 16-byte aligned, with the workspace: the inputs are
+    re-pitched and both directions run as TMA scans (several channel blocks and
+    a partial last one, N = 8)."""
+    _check(oracle, sc.workload(f"bi_rp{L}", 3, 72, L, N=8, K=2, io=io))
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bidirectional_repitched_rows_groups(oracle, io):
+    """Two groups: the re-pitched B and C grow with ngroups, so the workspace
+    the size query reports (one group) is too small and the call merges on
+    chip; given room for both groups' copies it re-pitches.  Both agree with
+    the oracle."""
+    import torch
+    import selective_state_space_120_b300 as ss
+    wl = sc.workload("bi_rpg", 2, 48, 197, N=8, G=2, K=2, io=io)
+    inp = wk.make_inputs(wl, seed=0)
+    t = sc.device_inputs(inp)
+    ref, ref_last = sc.oracle_run(oracle, inp)
+    for extra in (0, 1 << 20):
+        need = ss.workspace_bytes(1, wl.batch, wl.dim, wl.L, wl.N) + extra
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        out, last = ss.bidir_scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                                      t["delta_bias"], True, return_last_state=True, workspace=ws)
+        torch.cuda.synchronize()
+        sc.assert_close(sc.from_torch(out), ref, io)
+        sc.assert_close(last.cpu().numpy().astype(np.float64), ref_last, io, "last_state")
+
+
 # ---------------------------------------------------------------- SS2D
 @pytest.mark.parametrize("H,W", [(1, 1), (3, 5), (5, 3), (8, 8), (7, 16), (56, 56)])
 @pytest.mark.parametrize("io", ["f32", "bf16"])
