@@ -217,11 +217,12 @@ ss_status ss_bidir_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dsta
  *   workspace  ss_workspace_bytes(SS_KIND_CROSS2D, batch, dim, H*W, dstate) bytes,
  *              16-byte aligned, not overlapping any tensor; NULL when that is 0.
  * When rows are 16-byte aligned (H*W * element size % 16 == 0) the four
- * directions run as TMA-staged scans, two side by side per launch, that merge
- * through the workspace: two fp32 [batch, dim, H*W] accumulators (row pair,
- * column pair; each receives its terms in a fixed order, so the result is
- * deterministic), summed and gated by a final merge, and a transposed copy of u
- * that the column directions read as row-order tiles.
+ * directions run side by side in one launch of TMA-staged scans, each storing
+ * its terms into its own fp32 [batch, dim, H*W] slice of the workspace (the
+ * row orders by position, the column orders by column-major index); one more
+ * launch sums the four slices by position (a fixed order: deterministic) and
+ * gates.  The column directions read u as row-order tiles of a transposed copy
+ * of u that the call makes in the workspace first.
  * Otherwise the whole map of a channel is merged in shared memory: H*W is then
  * limited by the per-block shared-memory size (SS_ERR_UNSUPPORTED beyond it).
  */

@@ -306,46 +306,45 @@ struct Scan1d {
             }
             return SS_OK;
         }
-        // SS2D: two launches of two directions side by side -- (row, column) into
-        // two accumulators, then (reversed row, reversed column) added to them --
-        // then one merge.  Twice the warps of one direction per launch, and each
-        // accumulator still receives its terms in a fixed order.  The column
-        // pair's accumulator is the transposed map, so its accesses stay
-        // contiguous; the merge transposes it back.
-        float *acc1 = acc0 + rows * a.L;
+        // SS2D: one launch of the four directions side by side (grid z), each
+        // storing y_k + D_k*u into its own fp32 slice in its pair's traversal
+        // (the row orders by position, the column orders by column-major index,
+        // so every access is a contiguous 16-byte vector), then one merge.
         // The column directions read u as row-order tiles of the transposed map
-        // (one transpose, instead of a gather per element): slice 1 of each pair
-        // launch takes that map, and its order is presented as a row order
-        // (column -> row, reversed column -> reversed row); its accumulator is
-        // already indexed by column-major position, i.e. by that row order.
+        // (one transpose, instead of a gather per element): the odd slices of
+        // the launch take that map, and their orders are presented as row
+        // orders (column -> row, reversed column -> reversed row).
+        const size_t map4 = (size_t)rows * a.L;
+        float *sl[4] = {acc0, acc0 + map4, acc0 + 2 * map4, acc0 + 3 * map4};
         CUtensorMap mu2;
-        void *uT = reinterpret_cast<uint8_t *>(a.ws) + 2 * (size_t)rows * a.L * sizeof(float);
+        void *uT = reinterpret_cast<uint8_t *>(a.ws) + 4 * map4 * sizeof(float);
         if ((st = permuted_copy(a, ORD_COL, uT))) return st;
         if ((st = make_map(&mu2, uT, io, a.L, rows, C::T, C::CB))) return st;
-        for (int half = 0; half < 2; ++half) {
-            p.nz = 2;
-            p.k0 = 2 * half;
-            for (int d = 0; d < 2; ++d) {
-                const int o = a.orders[2 * half + d];
-                p.orders_z[d] = (d == 0) ? o : (o == ORD_COL ? ORD_ROW : ORD_ROW_REV);
-                p.modes_z[d] = half == 0 ? OUT_ACC_FIRST : OUT_ACC_ADD;
-                p.accs_z[d] = d == 0 ? acc0 : acc1;
-            }
-            kern<<<dim3(cblocks, bgs, 2), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, mu2, p);
-            if ((st = check_launch("direction pair scan"))) return st;
+        p.nz = 4;
+        p.k0 = 0;
+        for (int d = 0; d < 4; ++d) {
+            const int o = a.orders[d];
+            p.orders_z[d] = (o == ORD_ROW || o == ORD_COL) ? ORD_ROW : ORD_ROW_REV;
+            p.modes_z[d] = OUT_ACC_FIRST;
+            p.accs_z[d] = sl[d];
         }
+        kern<<<dim3(cblocks, bgs, 4), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, mu2, p);
+        if ((st = check_launch("four-direction scan"))) return st;
         using IO = typename C::IO;
+        // slices: 0 row, 1 column, 2 reversed row, 3 reversed column
         // whole maps in shared memory when the column map fits (odd stride P)
         const int P = (a.H & 1) ? (int)a.H : (int)a.H + 1;
         const size_t msm = (size_t)a.W * P * sizeof(float);
         if (msm <= 48 * 1024 && rows < (1ll << 31)) {
-            k_merge2_map<IO><<<(unsigned)rows, 256, msm, s>>>(acc0, acc1, reinterpret_cast<const IO *>(a.z),
+            k_merge2_map<IO><<<(unsigned)rows, 256, msm, s>>>(sl[0], sl[2], sl[1], sl[3],
+                                                              reinterpret_cast<const IO *>(a.z),
                                                               reinterpret_cast<IO *>(a.out), (int)a.H,
                                                               (int)a.W, P);
             return check_launch("merge");
         }
         const dim3 mgrid((unsigned)rows, (unsigned)((a.W + 31) / 32), (unsigned)((a.H + 31) / 32));
-        k_merge2<IO><<<mgrid, dim3(32, 8), 0, s>>>(acc0, acc1, reinterpret_cast<const IO *>(a.z),
+        k_merge2<IO><<<mgrid, dim3(32, 8), 0, s>>>(sl[0], sl[2], sl[1], sl[3],
+                                                  reinterpret_cast<const IO *>(a.z),
                                                   reinterpret_cast<IO *>(a.out), (int)a.H, (int)a.W);
         return check_launch("merge");
     }
@@ -788,10 +787,11 @@ bool bidir_padded_ok(const ScanArgs &a) {
 size_t multidir_workspace_bytes(const ScanArgs &a) {
     if (bidir_padded_ok(a)) return bidir_padded_bytes(a);
     if (!scan1d_uses_tma(a)) return 0;  // rows not 16-byte aligned: on-chip merge path
-    // one fp32 accumulator; SS2D scans two pairs of directions side by side into
-    // two, and reads u of its column directions from a transposed copy
+    // one fp32 accumulator; SS2D scans its four directions side by side into
+    // four fp32 slices, and reads u of its column directions from a transposed
+    // copy (sized as an fp32 map, for either dtype)
     const size_t map = (size_t)a.batch * a.dim * a.L * sizeof(float);
-    return a.K == 4 ? 3 * map : map;
+    return a.K == 4 ? 5 * map : map;
 }
 
 size_t steps_workspace_bytes(const ScanArgs &a) {

@@ -127,10 +127,10 @@ struct Scan1dParams {
     int64_t pitch;  // row pitch (elements) of the accumulators; L unless the inputs are re-pitched
     // Multi-direction launches may scan several directions side by side:
     // blockIdx.z = d selects direction k0 + d with its own order, mode and
-    // accumulator (entries [0, nz)).
+    // accumulator (entries [0, nz)); odd d read u through the second map.
     int nz, k0;
-    int orders_z[2], modes_z[2];
-    float *accs_z[2];
+    int orders_z[4], modes_z[4];
+    float *accs_z[4];
     const void *u_g;        // u (the fused Conv1D's history across L-chunks)
     const void *z_g;        // z (the gate of the last direction of a merge)
     const float *A, *D, *bias;
@@ -664,16 +664,19 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
         p.order = 0;
         p.mode = OUT_STORE;
     } else {
-        const bool z1 = blockIdx.z != 0;  // direction of this slice of the grid
-        p.k = p.k0 + (z1 ? 1 : 0);
-        p.order = z1 ? p_in.orders_z[1] : p_in.orders_z[0];  // selects, not a dynamic
-        p.mode = z1 ? p_in.modes_z[1] : p_in.modes_z[0];     // index (which would copy
-        p.acc = z1 ? p_in.accs_z[1] : p_in.accs_z[0];        // the params to the stack)
+        // direction of this slice of the grid: selects, not a dynamic index
+        // (which would copy the params to the stack)
+        const unsigned zi = blockIdx.z;
+        const bool z1 = zi & 1u, z2 = zi & 2u;
+        p.k = p.k0 + (int)zi;
+        p.order = z2 ? (z1 ? p_in.orders_z[3] : p_in.orders_z[2]) : (z1 ? p_in.orders_z[1] : p_in.orders_z[0]);
+        p.mode = z2 ? (z1 ? p_in.modes_z[3] : p_in.modes_z[2]) : (z1 ? p_in.modes_z[1] : p_in.modes_z[0]);
+        p.acc = z2 ? (z1 ? p_in.accs_z[3] : p_in.accs_z[2]) : (z1 ? p_in.accs_z[1] : p_in.accs_z[0]);
     }
     constexpr int N = C::N, NPT = C::NPT, T = C::T, E = C::E, CL = C::CL;
     // u tiles: the two slices of a multi-direction launch may read different
     // maps (u, or the copies of u permuted into other traversals' step orders)
-    const CUtensorMap *umap = (MULTI && blockIdx.z != 0) ? &tm_u2 : &tm_u;
+    const CUtensorMap *umap = (MULTI && (blockIdx.z & 1u)) ? &tm_u2 : &tm_u;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -1034,51 +1037,56 @@ k_scan1d_direct(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     scan1d_body<C, false, false, true>(tm_u, tm_dl, tm_z, tm_B, tm_C, tm_u, p);
 }
 
-// Final merge of a four-direction call scanned as two pairs: out = (row-pair
-// accumulator + column-pair accumulator transposed back) gated by SiLU(z), in
-// the I/O type.  acc_row is [rows, H, W]; acc_col is [rows, W, H] (column-major
-// map).  One 32 x 32 tile of one row per block: the column-pair tile is read
-// along its contiguous axis into shared memory and written out along the map's.
+// Final merge of a four-direction call (SS2D) whose directions stored their
+// terms y_k + D_k*u into four fp32 slices: the row orders by position
+// (r0 forward, r1 reversed), the column orders by column-major index (c0, c1),
+// i.e. each direction's steps in its pair's traversal.  out = (r0 + r1 +
+// (c0 + c1) transposed back) gated by SiLU(z), in the I/O type.  Slices are
+// [rows, H, W] (rows) and [rows, W, H] (columns).  One 32 x 32 tile of one row
+// per block: the column tiles are read along their contiguous axis into shared
+// memory and written out along the map's.
 template <typename IO>
-__global__ void __launch_bounds__(256) k_merge2(const float *__restrict__ acc_row,
-                                                const float *__restrict__ acc_col,
+__global__ void __launch_bounds__(256) k_merge2(const float *__restrict__ r0, const float *__restrict__ r1,
+                                                const float *__restrict__ c0, const float *__restrict__ c1,
                                                 const IO *__restrict__ z, IO *__restrict__ out,
                                                 int H, int W) {
     __shared__ float tile[32][33];
     const int64_t row = blockIdx.x;
     const int64_t L = (int64_t)H * W;
-    const int c0 = blockIdx.y * 32, r0 = blockIdx.z * 32;
+    const int cb = blockIdx.y * 32, rb = blockIdx.z * 32;
     const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-    const float *ac = acc_col + row * L;
 #pragma unroll
     for (int k = 0; k < 32; k += 8) {
-        const int c = c0 + ty + k, r = r0 + tx;
-        if (c < W && r < H) tile[ty + k][tx] = ac[(int64_t)c * H + r];
+        const int c = cb + ty + k, r = rb + tx;
+        if (c < W && r < H) {
+            const int64_t i = row * L + (int64_t)c * H + r;
+            tile[ty + k][tx] = c0[i] + c1[i];
+        }
     }
     __syncthreads();
-    const float *ar = acc_row + row * L;
     IO *o = out + row * L;
     const IO *zr = z ? z + row * L : nullptr;
 #pragma unroll
     for (int k = 0; k < 32; k += 8) {
-        const int r = r0 + ty + k, c = c0 + tx;
+        const int r = rb + ty + k, c = cb + tx;
         if (c < W && r < H) {
             const int64_t pos = (int64_t)r * W + c;
-            float v = ar[pos] + tile[tx][ty + k];
+            float v = r0[row * L + pos] + r1[row * L + pos] + tile[tx][ty + k];
             if (zr) v *= silu(IOT<IO>::load(zr + pos));
             o[pos] = IOT<IO>::from_f(v);
         }
     }
 }
 
-// k_merge2 for maps whose column accumulator fits in shared memory: one CTA
-// (256 threads) per row stages the whole column-major map with an odd column
-// stride P >= H, so a warp reading one map row across consecutive columns hits
-// 32 distinct banks, then sums every position.  Loads go four per thread at a
-// time, for enough bytes in flight.  Dynamic shared memory: W * P floats.
+// k_merge2 for maps whose column slices fit in shared memory: one CTA (256
+// threads) per row stages the sum of the two column slices as a whole
+// column-major map with an odd column stride P >= H, so a warp reading one
+// map row across consecutive columns hits 32 distinct banks, then sums every
+// position.  Loads go four per thread at a time, for enough bytes in flight.
+// Dynamic shared memory: W * P floats.
 template <typename IO>
-__global__ void __launch_bounds__(256) k_merge2_map(const float *__restrict__ acc_row,
-                                                    const float *__restrict__ acc_col,
+__global__ void __launch_bounds__(256) k_merge2_map(const float *__restrict__ r0, const float *__restrict__ r1,
+                                                    const float *__restrict__ c0, const float *__restrict__ c1,
                                                     const IO *__restrict__ z, IO *__restrict__ out,
                                                     int H, int W, int P) {
     extern __shared__ float colmap[];  // [W][P]
@@ -1088,7 +1096,7 @@ __global__ void __launch_bounds__(256) k_merge2_map(const float *__restrict__ ac
     constexpr int U = 4;
     {
         // column-major index i -> cell (r, c) = (i % H, i / H), stepped by 256
-        const float *ac = acc_col + row * (int64_t)L;
+        const float *a0 = c0 + row * (int64_t)L, *a1 = c1 + row * (int64_t)L;
         int c = t / H, r = t - c * H;
         const int dc = 256 / H, dr = 256 - dc * H;
         for (int i0 = t; i0 < L; i0 += U * 256) {
@@ -1097,7 +1105,7 @@ __global__ void __launch_bounds__(256) k_merge2_map(const float *__restrict__ ac
 #pragma unroll
             for (int j = 0; j < U; ++j) {
                 const int i = i0 + j * 256;
-                v[j] = i < L ? ac[i] : 0.f;
+                v[j] = i < L ? a0[i] + a1[i] : 0.f;
                 at[j] = c * P + r;
                 r += dr;
                 c += dc;
@@ -1112,7 +1120,7 @@ __global__ void __launch_bounds__(256) k_merge2_map(const float *__restrict__ ac
         }
     }
     __syncthreads();
-    const float *ar = acc_row + row * (int64_t)L;
+    const float *b0 = r0 + row * (int64_t)L, *b1 = r1 + row * (int64_t)L;
     IO *o = out + row * (int64_t)L;
     const IO *zr = z ? z + row * (int64_t)L : nullptr;
     // map position -> cell (r, c) = (pos / W, pos % W), stepped by 256
@@ -1124,7 +1132,7 @@ __global__ void __launch_bounds__(256) k_merge2_map(const float *__restrict__ ac
         for (int j = 0; j < U; ++j) {
             const int pos = p0 + j * 256;
             const bool in = pos < L;
-            v[j] = in ? ar[pos] + colmap[c * P + r] : 0.f;
+            v[j] = in ? b0[pos] + b1[pos] + colmap[c * P + r] : 0.f;
             g[j] = (in && zr) ? IOT<IO>::load(zr + pos) : 0.f;
             c += dc;
             r += dr;

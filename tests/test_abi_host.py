@@ -203,8 +203,9 @@ def test_workspace_sizing_is_host_only(lib):
     want = (a256(2 * rows * Lp * 4) + 2 * a256(rows * Lp * 4) + a256(2 * rows * Lp * 4) +
             2 * a256(128 * 2 * 16 * Lp * 4))
     assert b.workspace_bytes(b.SS_KIND_BIDIR, 128, 768, 197, 16) == want
-    # (SS2D: two accumulators and a transposed copy of u for the column directions)
-    assert b.workspace_bytes(b.SS_KIND_CROSS2D, 32, 192, 3136, 16) == 3 * 32 * 192 * 3136 * 4
+    # (SS2D: four fp32 slices, one per direction, and a transposed copy of u for
+    # the column directions)
+    assert b.workspace_bytes(b.SS_KIND_CROSS2D, 32, 192, 3136, 16) == 5 * 32 * 192 * 3136 * 4
     assert b.workspace_bytes(b.SS_KIND_BIDIR, 2, 24, 256, 16) == 2 * 24 * 256 * 4
     # plenty of batch*dim parallelism: single pass, no workspace
     assert b.workspace_bytes(b.SS_KIND_SCAN, 8, 1536, 2048, 16) == 0
