@@ -150,7 +150,8 @@ struct Scan1dParams {
 // pairs, or (C::BCW) as bf16 pairs packed in one 32-bit word -- which is
 // exactly the word the tile holds at columns (t, t+1), so it is only moved.
 template <class C>
-__device__ __forceinline__ void convert_bc(const uint8_t *tB, const uint8_t *tC, float *bc, int tid) {
+__device__ __forceinline__ void convert_bc(const uint8_t *tB, const uint8_t *tC, float *bc, int tid,
+                                           bool with_c = true) {
     using IO = typename C::IO;
     constexpr int VPC = 16 / C::ES;  // values per 16-byte chunk
     if constexpr (C::BCW) {
@@ -175,6 +176,7 @@ __device__ __forceinline__ void convert_bc(const uint8_t *tB, const uint8_t *tC,
         const int n = task % C::N;
         const int isC = (task / C::N) & 1;
         const int q = task / (2 * C::N);  // 16-byte chunk of the 64-byte row
+        if (isC && !with_c) continue;
         float v[VPC];
         load_tile_row<IO, VPC>(isC ? tC : tB, n, q * VPC, v);
 #pragma unroll
@@ -693,11 +695,13 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
     const int dlrow_tma = (int)(((int64_t)b * p.K + p.k) * p.dim + (int64_t)grp * p.dpg +
                                 (int64_t)cblk * C::CB);
     const int bcrow_tma = (int)((((int64_t)b * p.K + p.k) * p.G + grp) * N);
-    const bool gate_in_prep = (p.mode == OUT_STORE) && p.has_z;
     const int64_t t_begin = (int64_t)jc * p.Lc;
     const int64_t t_end = min(p.L, t_begin + p.Lc);
     const int nchunks = (int)((t_end - t_begin + T - 1) / T);
+    // the chunk-local pass needs only the end states of chunks 1..J-2: no
+    // readout, so no C tiles, no gate and no skip term
     const bool do_y = (p.pass != 1) || (jc == 0);
+    const bool gate_in_prep = do_y && (p.mode == OUT_STORE) && p.has_z;
 
     // scan role: channels ch[c] (within the CTA) of this lane's group
     int chs[CL];
@@ -749,7 +753,7 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
     const uint32_t smem0 = smem_u32(smem);
     const bool z_tiled = gate_in_prep;
     const uint32_t tx_bytes = (2u + (z_tiled ? 1u : 0u)) * C::CB * 64u +
-                              2u * N * 64u;
+                              (do_y ? 2u : 1u) * N * 64u;
     const uint64_t budget = g_wait_budget_ns;
 
     if (tid == 0) {
@@ -781,7 +785,7 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
         tma_load_2d(st + C::OFF_DL, &tm_dl, x, dlrow_tma, bar);
         if (z_tiled) tma_load_2d(st + C::OFF_Z, &tm_z, xu, row_tma, bar);
         tma_load_2d(st + C::OFF_B, &tm_B, x, bcrow_tma, bar);
-        tma_load_2d(st + C::OFF_C, &tm_C, x, bcrow_tma, bar);
+        if (do_y) tma_load_2d(st + C::OFF_C, &tm_C, x, bcrow_tma, bar);
     };
     if (tid == 0) {
 #pragma unroll 1
@@ -795,7 +799,7 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
     auto prep_chunk = [&](int i) {
         const int s = i % C::STAGES;
         const uint8_t *st = smem + s * C::STAGE;
-        convert_bc<C>(st + C::OFF_B, st + C::OFF_C, bcbuf0 + (i & 1) * (C::BCBUF / 4), tid);
+        convert_bc<C>(st + C::OFF_B, st + C::OFF_C, bcbuf0 + (i & 1) * (C::BCBUF / 4), tid, do_y);
         const int pb = C::OVL ? (i & 1) : 0;
         float4 *pdxrow = reinterpret_cast<float4 *>(smem + C::OFF_DX + pb * C::PREPBUF +
                                                     pch * C::DXROW);
@@ -876,7 +880,7 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
             }
             const int slot = swz_slot((pt0 + e) >> 1);
             pdxrow[slot] = make_float4(dl[0], dl[1], xx[0], xx[1]);
-            pgdrow[slot] = make_float4(ga[0], du[0], ga[1], du[1]);
+            if (do_y) pgdrow[slot] = make_float4(ga[0], du[0], ga[1], du[1]);
         }
     };
     // Bounded wait for chunk i's tiles; on timeout the whole CTA drains its
