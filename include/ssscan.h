@@ -396,7 +396,8 @@ size_t ss_multi_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t H, int6
 
 /*
  * ss_selective_scan_bwd -- gradients of ss_selective_scan_fwd (Euler input
- * matrix, zero initial state, no options) for an upstream gradient `dout` of
+ * matrix, zero initial state, no options; ss_selective_scan_bwd_opts below
+ * takes the options) for an upstream gradient `dout` of
  * out.  The forward call computes ("Mamba Series from Selective State Spaces
  * to Visual State Space Models": mathematical form of the selective SSM, and
  * the Mamba Block (1D) diagram)
@@ -430,6 +431,52 @@ ss_status ss_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, int 
                                 const void *dout, void *du, void *ddelta, float *dA, float *dB,
                                 float *dC, float *dD, void *dz, float *ddelta_bias,
                                 void *workspace, size_t workspace_bytes, ss_stream_t stream);
+
+/*
+ * ss_selective_scan_bwd_opts -- gradients of ss_selective_scan_fwd_opts: the
+ * backward pass of a single-direction scan run with options.  The arguments
+ * up to ddelta_bias are those of ss_selective_scan_bwd; `options` are the
+ * forward call's (chunks must be 0), and the options' tensors get their
+ * gradients in `extras`:
+ *   SS_SCAN_ZOH        the zero-order-hold input matrix Bbar = (exp(Delta'A) - 1)/A * B
+ *                      ("Mamba Series ...", mathematical form of the selective
+ *                      SSM): dDelta' gains exp(Delta'A) B u in place of B u,
+ *                      du and dB use (exp(Delta'A) - 1)/A in place of Delta', and
+ *                      dA gains the derivative of that factor.
+ *   options.h0         the initial state; extras.dh0 [batch, dim, dstate] float
+ *                      (nullable) receives Abar_0 (.) dh_0, its gradient.
+ *   SS_SCAN_CONV_SILU  the fused Conv1D + SiLU: `u` is its input x, `du`
+ *                      receives the gradient with respect to x, and
+ *                      extras.dconv_w [dim, 4] (required), dconv_b [dim] and
+ *                      dconv_x0 [batch, dim, 3] (nullable; each only with its
+ *                      tensor in the options) the gradients of the weights, bias
+ *                      and history.  The convolution runs as passes of its own
+ *                      around the scan's backward kernel: its output u is
+ *                      recomputed into the workspace in the I/O type (so for
+ *                      bf16 I/O the backward pass sees u rounded to bf16, where
+ *                      the fused forward kept it in float32) and the scan's du
+ *                      goes to the workspace in float32 before the
+ *                      convolution's gradients are formed.
+ * dA, dB, dC, dD, ddelta_bias, dconv_w and dconv_b are sums: zeroed on
+ * `stream`, then accumulated with fp32 atomic adds.  Workspace: at least
+ * ss_workspace_bytes_opts(SS_KIND_SCAN_BWD, batch, dim, seqlen, dstate,
+ * options) bytes.  Every extras tensor is a device pointer, 16-byte aligned.
+ */
+typedef struct ss_scan_bwd_extras {
+    float *dh0;      /* [batch, dim, dstate], nullable */
+    float *dconv_w;  /* [dim, 4] */
+    float *dconv_b;  /* [dim], nullable */
+    float *dconv_x0; /* [batch, dim, 3], nullable */
+    int reserved[8]; /* must be zero */
+} ss_scan_bwd_extras;
+ss_status ss_selective_scan_bwd_opts(int64_t batch, int64_t dim, int64_t seqlen, int dstate,
+                                     int ngroups, ss_dtype io, const void *u, const void *delta,
+                                     const float *A, const void *B, const void *C, const float *D,
+                                     const void *z, const float *delta_bias, int delta_softplus,
+                                     const void *dout, void *du, void *ddelta, float *dA, float *dB,
+                                     float *dC, float *dD, void *dz, float *ddelta_bias,
+                                     const ss_scan_options *options, const ss_scan_bwd_extras *extras,
+                                     void *workspace, size_t workspace_bytes, ss_stream_t stream);
 
 /* Workspace bytes a call of the given kind and shape needs (0 if none), for
  * either I/O dtype (the larger of the two).  For SS_KIND_CROSS2D pass

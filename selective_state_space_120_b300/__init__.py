@@ -122,14 +122,20 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta
 
 
 def selective_scan_bwd(u, delta, A, B, C, dout, D=None, z=None, delta_bias=None,
-                       delta_softplus=True, workspace=None, stream=None):
-    """Gradients of :func:`selective_scan_fwd` (Euler, zero initial state, no
-    options) for the upstream gradient ``dout`` [batch, dim, L] of its output.
+                       delta_softplus=True, workspace=None, stream=None, h0=None, zoh=False,
+                       conv_w=None, conv_b=None, conv_x0=None):
+    """Gradients of :func:`selective_scan_fwd` for the upstream gradient
+    ``dout`` [batch, dim, L] of its output, with the forward call's options
+    (``h0``, ``zoh``, and the fused Conv1D ``conv_w``, ``conv_b``, ``conv_x0``,
+    ``u`` then being the convolution's input).
 
     Returns a dict: du, ddelta [batch, dim, L] and dz (None without z) in the
     I/O dtype; dA [dim, N], dB, dC [batch, G, N, L], dD (None without D) and
-    ddelta_bias (None without delta_bias) in float32.  ``workspace`` is an
-    optional preallocated uint8 CUDA tensor for the 16-step state checkpoints."""
+    ddelta_bias (None without delta_bias) in float32; with the options also dh0
+    [batch, dim, N] (given h0), dconv_w [dim, 4], dconv_b [dim] and dconv_x0
+    [batch, dim, 3] (each given its tensor) in float32.  ``workspace`` is an
+    optional preallocated uint8 CUDA tensor (state checkpoints; with the Conv1D
+    also the recomputed u and its gradient)."""
     torch = _torch()
     lib = _b.load()
     batch, dim, L = u.shape
@@ -150,15 +156,28 @@ def selective_scan_bwd(u, delta, A, B, C, dout, D=None, z=None, delta_bias=None,
          "dC": torch.empty(batch, G, N, L, **f32),
          "dD": torch.empty(dim, **f32) if D is not None else None,
          "ddelta_bias": torch.empty(dim, **f32) if delta_bias is not None else None}
-    wsb = int(lib.ss_workspace_bytes(_b.SS_KIND_SCAN_BWD, batch, dim, L, N))
+    _check_io("h0", h0, torch.float32, dev, (batch, dim, N))
+    _check_io("conv_w", conv_w, torch.float32, dev, (dim, 4))
+    _check_io("conv_b", conv_b, torch.float32, dev, (dim,))
+    _check_io("conv_x0", conv_x0, torch.float32, dev, (batch, dim, 3))
+    flags = (_b.SS_SCAN_ZOH if zoh else 0) | (_b.SS_SCAN_CONV_SILU if conv_w is not None else 0)
+    opts = _b.options(0, flags, _ptr(h0), _ptr(conv_w), _ptr(conv_b), _ptr(conv_x0))
+    g["dh0"] = torch.empty(batch, dim, N, **f32) if h0 is not None else None
+    g["dconv_w"] = torch.empty(dim, 4, **f32) if conv_w is not None else None
+    g["dconv_b"] = torch.empty(dim, **f32) if conv_b is not None else None
+    g["dconv_x0"] = torch.empty(batch, dim, 3, **f32) if conv_x0 is not None else None
+    ext = _b.BwdExtras()
+    ext.dh0, ext.dconv_w = _ptr(g["dh0"]), _ptr(g["dconv_w"])
+    ext.dconv_b, ext.dconv_x0 = _ptr(g["dconv_b"]), _ptr(g["dconv_x0"])
+    wsb = int(lib.ss_workspace_bytes_opts(_b.SS_KIND_SCAN_BWD, batch, dim, L, N, ctypes.byref(opts)))
     if wsb and (workspace is None or workspace.numel() < wsb):
         workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    _b.check(lib.ss_selective_scan_bwd(
+    _b.check(lib.ss_selective_scan_bwd_opts(
         batch, dim, L, N, G, _io_code(u), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
         _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(dout),
         _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
-        _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["ddelta_bias"]),
-        _ptr(workspace) if wsb else None, workspace.numel() if wsb else 0,
+        _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["ddelta_bias"]), ctypes.byref(opts),
+        ctypes.byref(ext), _ptr(workspace) if wsb else None, workspace.numel() if wsb else 0,
         _stream(stream, dev)))
     return g
 

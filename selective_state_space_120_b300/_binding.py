@@ -39,7 +39,8 @@ EXPORTS = ("ss_selective_scan_fwd", "ss_selective_scan_fwd_opts", "ss_bidir_scan
            "ss_debug_set_wait_budget_ns", "ss_debug_set_flags",
            "ss_selective_scan_fwd_noalloc", "ss_selective_state_update",
            "ss_selective_scan_bwd", "ss_multi_scan_fwd", "ss_multi_scan_workspace_bytes",
-           "ss_dwconv3x3_silu_fwd", "ss_multi_scan_bwd", "ss_multi_scan_bwd_workspace_bytes")
+           "ss_dwconv3x3_silu_fwd", "ss_multi_scan_bwd", "ss_multi_scan_bwd_workspace_bytes",
+           "ss_selective_scan_bwd_opts")
 
 
 class SSError(RuntimeError):
@@ -52,6 +53,12 @@ class ScanOptions(ctypes.Structure):
     _fields_ = [("chunks", ctypes.c_int), ("flags", ctypes.c_uint), ("h0", ctypes.c_void_p),
                 ("conv_w", ctypes.c_void_p), ("conv_b", ctypes.c_void_p),
                 ("conv_x0", ctypes.c_void_p), ("reserved", ctypes.c_int * 6)]
+
+
+class BwdExtras(ctypes.Structure):
+    _fields_ = [("dh0", ctypes.c_void_p), ("dconv_w", ctypes.c_void_p),
+                ("dconv_b", ctypes.c_void_p), ("dconv_x0", ctypes.c_void_p),
+                ("reserved", ctypes.c_int * 8)]
 
 
 SS_SCAN_ZOH = 1
@@ -87,6 +94,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         # u ... delta_softplus as the forward call, then dout, du, ddelta, dA, dB, dC, dD, dz,
         # ddelta_bias, workspace, workspace_bytes, stream
         lib.ss_selective_scan_bwd.argtypes = scan_args[:15] + [vp] * 9 + [vp, sz, vp]
+        # the same, with the forward call's options and the gradients of their tensors
+        lib.ss_selective_scan_bwd_opts.argtypes = scan_args[:15] + [vp] * 9 + [
+            ctypes.POINTER(ScanOptions), ctypes.POINTER(BwdExtras), vp, sz, vp]
         # batch, dim, H, W, ndirs, orders (host int array), window, dstate, ngroups, io,
         # u, delta, A, B, C, D, delta_bias, delta_softplus, z, out, last_state, workspace,
         # workspace_bytes, stream
@@ -107,7 +117,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         for f in ("ss_selective_scan_fwd", "ss_selective_scan_fwd_opts", "ss_bidir_scan_fwd",
                   "ss_cross_scan2d_fwd", "ss_get_device_status", "ss_debug_set_wait_budget_ns",
                   "ss_debug_set_flags", "ss_selective_scan_fwd_noalloc",
-                  "ss_selective_state_update", "ss_selective_scan_bwd", "ss_multi_scan_fwd"):
+                  "ss_selective_state_update", "ss_selective_scan_bwd", "ss_multi_scan_fwd",
+                  "ss_selective_scan_bwd_opts"):
             getattr(lib, f).restype = ctypes.c_int
         lib.ss_workspace_bytes.argtypes = [i32, i64, i64, i64, i32]
         lib.ss_workspace_bytes.restype = sz

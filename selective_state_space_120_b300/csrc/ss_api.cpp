@@ -615,12 +615,85 @@ ss_status ss_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, int 
     return launch_scan_bwd(a, false);
 }
 
+ss_status ss_selective_scan_bwd_opts(int64_t batch, int64_t dim, int64_t seqlen, int dstate,
+                                     int ngroups, ss_dtype io, const void *u, const void *delta,
+                                     const float *A, const void *B, const void *C, const float *D,
+                                     const void *z, const float *delta_bias, int delta_softplus,
+                                     const void *dout, void *du, void *ddelta, float *dA, float *dB,
+                                     float *dC, float *dD, void *dz, float *ddelta_bias,
+                                     const ss_scan_options *options, const ss_scan_bwd_extras *extras,
+                                     void *workspace, size_t workspace_bytes, ss_stream_t stream) {
+    static const char *fn = "ss_selective_scan_bwd_opts";
+    bool empty = false;
+    ss_status st = check_common(fn, batch, dim, seqlen, dstate, ngroups, io, 1, u, delta, A, B, C,
+                                D, z, delta_bias, du, nullptr, &empty);
+    if (st != SS_OK) return st;
+    if ((st = check_options(fn, options, batch, dim, dstate, du, io, seqlen))) return st;
+    if (options && options->chunks != 0)
+        return fail(SS_ERR_INVALID_ARG, "%s: options.chunks has no meaning here (must be 0)", fn);
+    const bool conv = options && (options->flags & SS_SCAN_CONV_SILU);
+    ss_scan_bwd_extras ex{};
+    if (extras) ex = *extras;
+    for (int r : ex.reserved)
+        if (r != 0) return fail(SS_ERR_INVALID_ARG, "%s: reserved extras fields must be zero", fn);
+    if (conv && !ex.dconv_w)
+        return fail(SS_ERR_INVALID_ARG, "%s: SS_SCAN_CONV_SILU needs extras.dconv_w", fn);
+    if (!conv && (ex.dconv_w || ex.dconv_b || ex.dconv_x0))
+        return fail(SS_ERR_INVALID_ARG, "%s: conv gradients given without SS_SCAN_CONV_SILU", fn);
+    if (conv && ((ex.dconv_b && !options->conv_b) || (ex.dconv_x0 && !options->conv_x0)))
+        return fail(SS_ERR_INVALID_ARG, "%s: a conv gradient is given without its tensor", fn);
+    if (ex.dh0 && !(options && options->h0))
+        return fail(SS_ERR_INVALID_ARG, "%s: extras.dh0 given without options.h0", fn);
+    for (const void *q : {(const void *)ex.dh0, (const void *)ex.dconv_w, (const void *)ex.dconv_b,
+                          (const void *)ex.dconv_x0})
+        if (q && !aligned16(q))
+            return fail(SS_ERR_ALIGNMENT, "%s: an extras tensor is not 16-byte aligned", fn);
+    BwdArgs a;
+    a.f = scan_args(batch, dim, seqlen, dstate, ngroups, io, u, delta, A, B, C, D, z, delta_bias,
+                    delta_softplus, nullptr, nullptr, nullptr, 0, stream);
+    if (options) {
+        a.f.h0 = options->h0;
+        a.f.zoh = (options->flags & SS_SCAN_ZOH) ? 1 : 0;
+        a.f.conv = conv ? 1 : 0;
+        a.f.conv_w = options->conv_w;
+        a.f.conv_b = options->conv_b;
+        a.f.conv_x0 = options->conv_x0;
+    }
+    a.dout = dout;
+    a.du = du;
+    a.ddelta = ddelta;
+    a.dz = dz;
+    a.dA = dA;
+    a.dB = dB;
+    a.dC = dC;
+    a.dD = dD;
+    a.dbias = ddelta_bias;
+    a.dh0 = ex.dh0;
+    a.dconv_w = ex.dconv_w;
+    a.dconv_b = ex.dconv_b;
+    a.dconv_x0 = ex.dconv_x0;
+    a.ws = workspace;
+    a.ws_bytes = workspace_bytes;
+    if (empty) return launch_scan_bwd(a, true);  // the gradient of an empty sum is zero
+    if ((st = check_bwd(fn, batch, dim, seqlen, dstate, ngroups, io, u, delta, A, B, C, D, z,
+                        delta_bias, dout, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias, workspace,
+                        workspace_bytes)))
+        return st;
+    if ((st = check_workspace(fn, scan_bwd_workspace_bytes(batch, dim, seqlen, dstate, conv),
+                              workspace, workspace_bytes)))
+        return st;
+    return launch_scan_bwd(a, false);
+}
+
 size_t ss_workspace_bytes_opts(int kind, int64_t batch, int64_t dim, int64_t seqlen, int dstate,
                                const ss_scan_options *options) {
     if (kind == SS_KIND_BIDIR || kind == SS_KIND_CROSS2D)
         return ws_multidir_any_dtype(batch, dim, seqlen, dstate, kind == SS_KIND_BIDIR ? 2 : 4);
     if (kind == SS_KIND_SCAN_BWD)
-        return valid_dstate(dstate) ? scan_bwd_workspace_bytes(batch, dim, seqlen, dstate) : 0;
+        return valid_dstate(dstate)
+                   ? scan_bwd_workspace_bytes(batch, dim, seqlen, dstate,
+                                              options && (options->flags & SS_SCAN_CONV_SILU))
+                   : 0;
     if (kind != SS_KIND_SCAN) return 0;
     return ws_scan1d_any_dtype(batch, dim, seqlen, dstate, options ? options->chunks : 0);
 }

@@ -131,7 +131,29 @@ struct BwdParams {
     int k_z[2], order_z[2];
     float *du_acc;
     int64_t du_zstride, ck_zstride;
+    // single direction, option instantiations (EXT kernels): the zero-order-hold
+    // input matrix, an initial state h0 [batch*dim, N] (nullable) and the
+    // gradient of the loss with respect to it, dh0 [batch*dim, N] (nullable)
+    int zoh;
+    const float *h0;
+    float *dh0;
 };
+
+// Zero-order hold: Bbar u = psi * B u with psi = (exp(x) - 1)/A, x = Delta' A,
+// and its derivative with respect to A, (Delta' exp(x) - psi)/A.  For |x| <
+// 1/16 both come from the Taylor series of (exp(x) - 1)/x (truncation below
+// x^4/120 relative), which avoids the cancellation of exp(x) - 1:
+//   psi = Delta' (1 + x/2 + x^2/6 + x^3/24),  dpsi/dA = Delta'^2 (1/2 + x/3 + x^2/8 + x^3/30).
+// A = 0 gives psi = Delta' (x = 0) through the series.  ia = 1/A (0 for A = 0).
+__device__ __forceinline__ float zoh_psi(float dl, float a, float xn, float ia) {
+    return fabsf(xn) < 0.0625f ? dl * fmaf(xn, fmaf(xn, fmaf(xn, 1.f / 24.f, 1.f / 6.f), 0.5f), 1.f)
+                               : (a - 1.f) * ia;
+}
+__device__ __forceinline__ float zoh_dpsi_dA(float dl, float a, float xn, float ia, float psi) {
+    return fabsf(xn) < 0.0625f
+               ? dl * dl * fmaf(xn, fmaf(xn, fmaf(xn, 1.f / 30.f, 0.125f), 1.f / 3.f), 0.5f)
+               : (dl * a - psi) * ia;
+}
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 __device__ __forceinline__ float2 ex2x2(float2 v) { return make_float2(ex2(v.x), ex2(v.y)); }
@@ -165,7 +187,10 @@ __device__ __forceinline__ void reduce_bc_store(float (&v)[V], int q, int g, flo
     }
 }
 
-template <class C, bool MULTI = false>
+// EXT (single direction only) compiles the options: the zero-order hold and the
+// initial state with its gradient; the plain instantiations carry none of
+// their code.
+template <class C, bool MULTI = false, bool EXT = false>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
 k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
            const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dy,
@@ -202,6 +227,8 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
     bool valid[CL];
     int64_t dch[CL];
     float2 A2[CL][NP], carry[CL][NP], dA[CL][NP];
+    float2 iA2[EXT ? CL : 1][EXT ? NP : 1];  // 1/A per state (0 for A = 0), zero-order hold
+    const bool zoh = EXT && p.zoh;
     float Dd[CL], dD_acc[CL], dbias_acc[CL];
     float *ck[CL];
     const float4 *P0[CL];
@@ -220,6 +247,8 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
             A2[c][k] = make_float2(a0, a1);
             carry[c][k] = make_float2(0.f, 0.f);
             dA[c][k] = make_float2(0.f, 0.f);
+            if constexpr (EXT)
+                iA2[c][k] = make_float2(a0 != 0.f ? kLog2e / a0 : 0.f, a1 != 0.f ? kLog2e / a1 : 0.f);
         }
         Dd[c] = p.D ? __ldg(p.D + poff + dch[c]) : 0.f;
         dD_acc[c] = 0.f;
@@ -357,7 +386,9 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
                     dsp = v > 15.f ? 1.f - rcp(ev) : ev * rcp(1.f + ev);
                 }
                 if (!in) dl = 0.f;
-                const float x = dl * uu[e];
+                // the state's input term per unit B: Delta' u (Euler), or u, to be
+                // scaled by psi per state (zero-order hold)
+                const float x = zoh ? uu[e] : dl * uu[e];
                 if (!bwd) {
                     *reinterpret_cast<float2 *>(q0row + tl) = make_float2(dl, x);
                 } else {
@@ -399,25 +430,36 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
         }
     };
 
-    // checkpoint kc of channel c (the state after block kc; zero before block 0)
+    // checkpoint kc of channel c (the state after block kc; before block 0 the
+    // initial state: zero, or h0)
     auto ld_ckpt = [&](int c, int kc, float2 (&v)[NP]) {
 #pragma unroll
         for (int kk = 0; kk < NP; ++kk) v[kk] = make_float2(0.f, 0.f);
-        if (kc >= 0) {
+        const float *base = nullptr;
+        if (kc >= 0) base = ck[c] + (int64_t)kc * N;
+        else if (EXT && p.h0) base = p.h0 + ((int64_t)b * p.dim + dch[c]) * N + g * NPT;
+        if (base) {
 #pragma unroll
             for (int kk = 0; kk < NP; ++kk) {
-                const float *src = ck[c] + (int64_t)kc * N + 2 * kk;
+                const float *src = base + 2 * kk;
                 v[kk].x = src[0];
                 if (2 * kk + 1 < NPT) v[kk].y = src[1];
             }
         }
     };
+    // Bbar u of the lane's state pair kk of channel c at a step: (Delta' B) u, or
+    // psi (B u) for the zero-order hold (pp = {Delta', x}, da = Delta' A log2 e)
+    auto bx_pair = [&](int c, int kk, float2 pp, float2 da, float2 a, const float2 &B2) -> float2 {
+        const float2 bu = __fmul2_rn(f2(pp.y), B2);
+        if (!zoh) return bu;
+        const float psi0 = zoh_psi(pp.x, a.x, da.x * kLn2, iA2[c][kk].x);
+        const float psi1 = zoh_psi(pp.x, a.y, da.y * kLn2, iA2[c][kk].y);
+        return __fmul2_rn(make_float2(psi0, psi1), bu);
+    };
 
     float2 h[CL][NP], hbn[CL][NP];
 #pragma unroll
-    for (int c = 0; c < CL; ++c)
-#pragma unroll
-        for (int k = 0; k < NP; ++k) h[c][k] = make_float2(0.f, 0.f);
+    for (int c = 0; c < CL; ++c) ld_ckpt(c, -1, h[c]);
 
 #pragma unroll 1
     for (int qs = 0; qs < nq; ++qs) {
@@ -448,8 +490,9 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
                         const float2 pp = *reinterpret_cast<const float2 *>(P0[c] + t);
 #pragma unroll
                         for (int kk = 0; kk < NP; ++kk) {
-                            const float2 a = ex2x2(__fmul2_rn(f2(pp.x), A2[c][kk]));
-                            h[c][kk] = __ffma2_rn(a, h[c][kk], __fmul2_rn(f2(pp.y), B2[kk]));
+                            const float2 da = __fmul2_rn(f2(pp.x), A2[c][kk]);
+                            const float2 a = ex2x2(da);
+                            h[c][kk] = __ffma2_rn(a, h[c][kk], bx_pair(c, kk, pp, da, a, B2[kk]));
                         }
                     }
                 }
@@ -512,8 +555,9 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
                             float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                             for (int kk = 0; kk < NP; ++kk) {
-                                const float2 a = ex2x2(__fmul2_rn(f2(pp.x), A2[c][kk]));
-                                hc[c][kk] = __ffma2_rn(a, hc[c][kk], __fmul2_rn(f2(pp.y), B2[kk]));
+                                const float2 da = __fmul2_rn(f2(pp.x), A2[c][kk]);
+                                const float2 a = ex2x2(da);
+                                hc[c][kk] = __ffma2_rn(a, hc[c][kk], bx_pair(c, kk, pp, da, a, B2[kk]));
                                 hs[tb][c][kk] = hc[c][kk];
                                 acc = __ffma2_rn(C2[kk], hc[c][kk], acc);
                             }
@@ -530,6 +574,7 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
 #pragma unroll
             for (int rb = C::RB - 1; rb >= 0; --rb) {
                 float p1v[CL][R], p2v[CL][R];
+                float p3v[EXT ? CL : 1][EXT ? R : 1];  // zero-order hold: sum_n dh psi B (du)
 #pragma unroll
                 for (int r = R - 1; r >= 0; --r) {
                     const int tb = rb * R + r;
@@ -541,16 +586,35 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
                         const float4 pp = P0[c][t0b + tb];  // Delta', Delta'u, ds, softplus'
                         const float2 dl2 = f2(pp.x), x2 = f2(pp.y), ds2 = f2(pp.z);
                         float2 p1 = make_float2(0.f, 0.f), p2 = make_float2(0.f, 0.f);
+                        float2 p3 = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int kk = 0; kk < NP; ++kk) {
-                            const float2 a = ex2x2(__fmul2_rn(dl2, A2[c][kk]));
+                            const float2 da = __fmul2_rn(dl2, A2[c][kk]);
+                            const float2 a = ex2x2(da);
                             const float2 dh = __ffma2_rn(ds2, C2[kk], carry[c][kk]);
                             const float2 hp = tb > 0 ? hs[tb - 1][c][kk] : hb[c][kk];
                             const float2 w = __fmul2_rn(__fmul2_rn(dh, hp), a);
                             p1 = __ffma2_rn(w, A2[c][kk], p1);
                             dA[c][kk] = __ffma2_rn(w, dl2, dA[c][kk]);
-                            p2 = __ffma2_rn(dh, B2[kk], p2);
-                            const float2 db = __fmul2_rn(dh, x2);
+                            float2 db;
+                            if (zoh) {
+                                // Bbar u = psi B u: d/dDelta' = Abar B u, d/du = psi B,
+                                // d/dB = psi u, d/dA = (dpsi/dA) B u
+                                const float2 xn = __fmul2_rn(da, f2(kLn2));
+                                const float ps0 = zoh_psi(pp.x, a.x, xn.x, iA2[c][kk].x);
+                                const float ps1 = zoh_psi(pp.x, a.y, xn.y, iA2[c][kk].y);
+                                const float2 psi = make_float2(ps0, ps1);
+                                const float2 dpa = make_float2(zoh_dpsi_dA(pp.x, a.x, xn.x, iA2[c][kk].x, ps0),
+                                                               zoh_dpsi_dA(pp.x, a.y, xn.y, iA2[c][kk].y, ps1));
+                                const float2 dhb = __fmul2_rn(dh, B2[kk]);
+                                p2 = __ffma2_rn(dhb, a, p2);
+                                p3 = __ffma2_rn(dhb, psi, p3);
+                                dA[c][kk] = __ffma2_rn(__fmul2_rn(dhb, x2), dpa, dA[c][kk]);
+                                db = __fmul2_rn(__fmul2_rn(dh, psi), x2);
+                            } else {
+                                p2 = __ffma2_rn(dh, B2[kk], p2);
+                                db = __fmul2_rn(dh, x2);
+                            }
                             const float2 dc = __fmul2_rn(ds2, hs[tb][c][kk]);
                             vb[kk] = c == 0 ? db : __fadd2_rn(vb[kk], db);
                             vc[kk] = c == 0 ? dc : __fadd2_rn(vc[kk], dc);
@@ -558,6 +622,7 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
                         }
                         p1v[c][r] = p1.x + p1.y;
                         p2v[c][r] = p2.x + p2.y;
+                        if constexpr (EXT) p3v[c][r] = p3.x + p3.y;
                     }
                     float vals[C::V];
 #pragma unroll
@@ -574,16 +639,24 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
 #pragma unroll
                 for (int c = 0; c < CL; ++c) {
                     const float P1s = transpose_reduce<R, CPW>(p1v[c], g) * kLn2;  // sum dh h Abar A
-                    const float P2s = transpose_reduce<R, CPW>(p2v[c], g);         // sum dh B
+                    // sum dh B (Euler), sum dh Abar B (zero-order hold)
+                    const float P2s = transpose_reduce<R, CPW>(p2v[c], g);
                     const float4 pp = P0[c][tl];
                     const float2 q1 = P1[c][tl];
                     const float ddelta = fmaf(P2s, q1.x, P1s) * pp.w;
                     dD_acc[c] = fmaf(pp.z, q1.x, dD_acc[c]);
                     dbias_acc[c] += ddelta;
                     IO *ob = reinterpret_cast<IO *>(smem + C::OFF_OB + chs[c] * C::OBROW);
-                    const float du = fmaf(pp.z, Dd[c], pp.x * P2s);
-                    if constexpr (MULTI) {
-                        // this direction's du by scan step; the merge sums by position
+                    float du_in = pp.x * P2s;  // sum_n dh Delta' B
+                    if constexpr (EXT) {
+                        const float P3s = transpose_reduce<R, CPW>(p3v[c], g);  // sum_n dh psi B
+                        if (zoh) du_in = P3s;
+                    }
+                    const float du = fmaf(pp.z, Dd[c], du_in);
+                    if (MULTI || (EXT && p.du_acc)) {
+                        // this direction's du by scan step, in fp32: the merge sums by
+                        // position (multi-direction), or the fused Conv1D's backward
+                        // reads it (single direction)
                         const int64_t t = (int64_t)i * T + tl;
                         if (valid[c] && t < L)
                             p.du_acc[kdir * p.du_zstride + ((int64_t)b * p.dim + dch[c]) * L + t] = du;
@@ -635,6 +708,7 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
 #pragma unroll 1
             for (int kk = lane; kk < narr * C::CHW * 4; kk += 32) {
                 const int arr = MULTI ? 1 : kk / (C::CHW * 4);
+                if (EXT && arr == 0 && p.du_acc) continue;  // du went out in fp32
                 const int rem = kk % (C::CHW * 4);
                 const int rr = rem >> 2, qq = rem & 3;
                 const int chr = warp * C::CHW + rr;
@@ -650,6 +724,21 @@ k_scan_bwd(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUt
             }
         }
         __syncwarp();
+    }
+
+    // the gradient with respect to the initial state: Abar_0 (.) dh_0, the carry
+    // left by the first step
+    if (EXT && p.dh0) {
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+            if (!valid[c]) continue;
+            float *dst = p.dh0 + ((int64_t)b * p.dim + dch[c]) * N + g * NPT;
+#pragma unroll
+            for (int kk = 0; kk < NP; ++kk) {
+                dst[2 * kk] = carry[c][kk].x;
+                if (2 * kk + 1 < NPT) dst[2 * kk + 1] = carry[c][kk].y;
+            }
+        }
     }
 
     // per-channel sums: over the channel's R lanes, then over the batch (atomics)
@@ -733,6 +822,122 @@ k_merge_bwd(const float *__restrict__ du_acc, int64_t rows, const BwdOrderSet os
             dz[i] = IOT<IO>::from_f(IOT<IO>::load(dout + i) * IOT<IO>::load(s + i) * sg *
                                     fmaf(zz, 1.f - sg, 1.f));
         }
+    }
+}
+
+}  // namespace ssk
+
+namespace ssk {
+
+// The Mamba block's Conv1D + SiLU input branch (causal depthwise convolution
+// of width 4 with bias, then SiLU) as passes of their own, for the backward
+// pass of a scan that fused it in front: k_conv_silu_fwd recomputes the scan's
+// input u, and k_conv_silu_bwd turns the scan's du into the gradients of the
+// convolution's input x, weights, bias and history x0.
+//   v_t = b + sum_{j<4} w_j x_{t-3+j}   (x_s for s < 0 is x0[3+s], or 0)
+//   u_t = SiLU(v_t)
+//   dv_t = du_t SiLU'(v_t),  SiLU'(v) = sigmoid(v) (1 + v (1 - sigmoid(v)))
+//   dx_s = sum_j w_j dv_{s+3-j},  dx0_k = sum_{j<=k} w_j dv_{k-j}
+//   dw_j = sum_t dv_t x_{t-3+j},  db = sum_t dv_t      (over batch and time)
+struct ConvSiluParams {
+    int64_t rows, dim, L;
+    const void *x;
+    const float *w, *bias, *x0;  // [dim, 4], [dim] (nullable), [rows, 3] (nullable)
+    void *u;                     // k_conv_silu_fwd: [rows, L] (I/O type)
+    const float *du;             // k_conv_silu_bwd: [rows, L] fp32 (the scan's du)
+    void *dx;                    // [rows, L] (I/O type)
+    float *dw, *dbias, *dx0;     // [dim, 4] and [dim] summed with atomics; [rows, 3]
+};
+
+template <typename IO>
+__device__ __forceinline__ float conv_x(const ConvSiluParams &p, int64_t row, int64_t s) {
+    if (s >= 0) return IOT<IO>::load(reinterpret_cast<const IO *>(p.x) + row * p.L + s);
+    return p.x0 ? __ldg(p.x0 + row * 3 + 3 + s) : 0.f;
+}
+
+template <typename IO>
+__device__ __forceinline__ float conv_pre(const ConvSiluParams &p, int64_t row, int64_t t, const float4 &w,
+                                          float b) {
+    return fmaf(w.w, conv_x<IO>(p, row, t),
+                fmaf(w.z, conv_x<IO>(p, row, t - 1), fmaf(w.y, conv_x<IO>(p, row, t - 2),
+                                                          fmaf(w.x, conv_x<IO>(p, row, t - 3), b))));
+}
+
+// One thread per element, grid-stride over [rows, L].
+template <typename IO>
+__global__ void __launch_bounds__(256) k_conv_silu_fwd(const ConvSiluParams p) {
+    const int64_t n = p.rows * p.L;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = i / p.L, t = i - row * p.L;
+        const int64_t d = row % p.dim;
+        const float4 w = __ldg(reinterpret_cast<const float4 *>(p.w) + d);
+        const float b = p.bias ? __ldg(p.bias + d) : 0.f;
+        reinterpret_cast<IO *>(p.u)[i] = IOT<IO>::from_f(silu(conv_pre<IO>(p, row, t, w, b)));
+    }
+}
+
+// One block of CONV_TS threads per (row, tile of CONV_TS steps): dv of the
+// tile's steps and of the three after it (the taps reaching back into the
+// tile) go to shared memory; each thread then forms dx of its step and its
+// partial dw and db, which the block sums and adds with atomics.
+constexpr int CONV_TS = 256;
+template <typename IO>
+__global__ void __launch_bounds__(CONV_TS) k_conv_silu_bwd(const ConvSiluParams p) {
+    __shared__ float dv[CONV_TS + 3];
+    __shared__ float red[5][CONV_TS / 32];
+    const int64_t row = blockIdx.y;
+    const int64_t d = row % p.dim;
+    const int64_t t0 = (int64_t)blockIdx.x * CONV_TS;
+    const float4 w = __ldg(reinterpret_cast<const float4 *>(p.w) + d);
+    const float b = p.bias ? __ldg(p.bias + d) : 0.f;
+    const float *dur = p.du + row * p.L;
+    for (int k = threadIdx.x; k < CONV_TS + 3; k += CONV_TS) {
+        const int64_t t = t0 + k;
+        float g = 0.f;
+        if (t < p.L) {
+            const float v = conv_pre<IO>(p, row, t, w, b);
+            const float sg = rcp(1.f + ex2(-v * kLog2e));
+            g = __ldg(dur + t) * sg * fmaf(v, 1.f - sg, 1.f);
+        }
+        dv[k] = g;
+    }
+    __syncthreads();
+    const int k = threadIdx.x;
+    const int64_t t = t0 + k;
+    float pw[4] = {0.f, 0.f, 0.f, 0.f}, pb = 0.f;
+    if (t < p.L) {
+        // dx_t = w_0 dv_{t+3} + w_1 dv_{t+2} + w_2 dv_{t+1} + w_3 dv_t
+        const float dxt = fmaf(w.x, dv[k + 3], fmaf(w.y, dv[k + 2], fmaf(w.z, dv[k + 1], w.w * dv[k])));
+        reinterpret_cast<IO *>(p.dx)[row * p.L + t] = IOT<IO>::from_f(dxt);
+        const float g = dv[k];
+        pw[0] = g * conv_x<IO>(p, row, t - 3);
+        pw[1] = g * conv_x<IO>(p, row, t - 2);
+        pw[2] = g * conv_x<IO>(p, row, t - 1);
+        pw[3] = g * conv_x<IO>(p, row, t);
+        pb = g;
+    }
+    if (t0 == 0 && p.dx0 && k < 3) {
+        // the history: dx0_k = sum_{j <= k} w_j dv_{k-j}
+        const float wj[4] = {w.x, w.y, w.z, w.w};
+        float acc = 0.f;
+        for (int j = 0; j <= k; ++j) acc = fmaf(wj[j], dv[k - j], acc);
+        p.dx0[row * 3 + k] = acc;
+    }
+    // block sums of dw and db
+    float vals[5] = {pw[0], pw[1], pw[2], pw[3], pb};
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) vals[i] += __shfl_xor_sync(kFull, vals[i], m);
+        if ((threadIdx.x & 31) == 0) red[i][threadIdx.x >> 5] = vals[i];
+    }
+    __syncthreads();
+    if (threadIdx.x < 5) {
+        float s = 0.f;
+        for (int i = 0; i < CONV_TS / 32; ++i) s += red[threadIdx.x][i];
+        if (threadIdx.x < 4) atomicAdd(p.dw + d * 4 + threadIdx.x, s);
+        else if (p.dbias) atomicAdd(p.dbias + d, s);
     }
 }
 

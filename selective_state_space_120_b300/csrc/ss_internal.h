@@ -47,6 +47,12 @@ struct BwdArgs {
     void *du = nullptr, *ddelta = nullptr, *dz = nullptr;  // I/O type
     float *dA = nullptr, *dB = nullptr, *dC = nullptr;     // fp32
     float *dD = nullptr, *dbias = nullptr;                 // fp32, nullable
+    // single direction with options (f.zoh, f.h0, f.conv): the gradient of h0
+    // and, with the fused Conv1D (du is then the gradient of its input x), of
+    // its weights, bias and history
+    float *dh0 = nullptr;
+    float *dconv_w = nullptr, *dconv_b = nullptr, *dconv_x0 = nullptr;
+    float *du_f32 = nullptr;  // internal: du in fp32 [batch*dim, L] instead of du (Conv1D path)
     void *ws = nullptr;
     size_t ws_bytes = 0;
 };
@@ -77,8 +83,10 @@ ss_status launch_scan1d(const ScanArgs &a);
 // One recurrence step (seqlen 1) updating `state` [batch*dim, N] in place.
 ss_status launch_step(const ScanArgs &a, float *state);
 ss_status launch_multidir(const ScanArgs &a);
-// Checkpoint workspace of the backward pass: 16-step state checkpoints, fp32.
-size_t scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t L, int N);
+// Checkpoint workspace of the backward pass: 16-step state checkpoints, fp32;
+// with the fused Conv1D also the recomputed u and the scan's du (sized for
+// either dtype).
+size_t scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t L, int N, bool conv = false);
 // Zeroes the summed gradient outputs, then runs the backward kernel (nothing
 // but the zeroing when `empty`).
 ss_status launch_scan_bwd(const BwdArgs &a, bool empty);
@@ -89,7 +97,7 @@ ss_status read_device_status(ss_stream_t stream);
 ss_status set_wait_budget(unsigned long long ns);
 ss_status set_debug_flags(unsigned int flags);
 // Device address of the fixed scratch array of ss_selective_scan_fwd_noalloc on
-// the current device (looked up once per device).
+// the current device (looked up on every call).
 ss_status noalloc_scratch(void **ptr);
 
 }  // namespace ssi

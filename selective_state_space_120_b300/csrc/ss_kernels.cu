@@ -873,7 +873,7 @@ struct DirLaunch {
     const void *u = nullptr, *z = nullptr, *dout = nullptr;
 };
 
-template <class C, bool MULTI = false>
+template <class C, bool MULTI = false, bool EXT = false>
 ss_status run_scan_bwd(const BwdArgs &a, const DirLaunch &dl = DirLaunch(), float *ckpt = nullptr,
                        float *du_acc = nullptr) {
     const int nz = MULTI ? dl.nz : 1;
@@ -893,7 +893,7 @@ ss_status run_scan_bwd(const BwdArgs &a, const DirLaunch &dl = DirLaunch(), floa
     if ((st = make_map(&mdy, tdy, io, f.L, rows, C::T, C::CB))) return st;
     if ((st = make_map(&mb, f.B, io, f.L, bcrows, C::T, C::N))) return st;
     if ((st = make_map(&mc, f.C, io, f.L, bcrows, C::T, C::N))) return st;
-    auto kern = k_scan_bwd<C, MULTI>;
+    auto kern = k_scan_bwd<C, MULTI, EXT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
     BwdParams p{};
@@ -925,6 +925,13 @@ ss_status run_scan_bwd(const BwdArgs &a, const DirLaunch &dl = DirLaunch(), floa
     p.dC = a.dC;
     p.dD = a.dD;
     p.dbias = a.dbias;
+    p.zoh = f.zoh;
+    p.h0 = f.h0;
+    p.dh0 = a.dh0;
+    if (!MULTI) {
+        p.du_acc = a.du_f32;  // nullable: du in the I/O type otherwise
+        p.du_zstride = 0;
+    }
     const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);
     const unsigned bgs = (unsigned)(f.batch * f.G);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(f.stream);
@@ -932,7 +939,7 @@ ss_status run_scan_bwd(const BwdArgs &a, const DirLaunch &dl = DirLaunch(), floa
     return check_launch("scan backward");
 }
 
-template <typename IO, bool MULTI = false>
+template <typename IO, bool MULTI = false, bool EXT = false>
 ss_status dispatch_bwd(const BwdArgs &a, const DirLaunch &dl = DirLaunch(), float *ckpt = nullptr,
                        float *du_acc = nullptr) {
     using namespace ssk;
@@ -941,13 +948,13 @@ ss_status dispatch_bwd(const BwdArgs &a, const DirLaunch &dl = DirLaunch(), floa
     // float32 I/O has twice the prep registers: a budget of two CTAs per SM
     constexpr int MB = sizeof(IO) == 2 ? 3 : 2;
     switch (a.f.N) {
-    case 1: return run_scan_bwd<CfgB<IO, 1, 2, 1, 4, 16, 2>, MULTI>(a, dl, ckpt, du_acc);
-    case 2: return run_scan_bwd<CfgB<IO, 2, 2, 1, 4, 16, 2>, MULTI>(a, dl, ckpt, du_acc);
-    case 4: return run_scan_bwd<CfgB<IO, 4, 2, 1, 4, 16, 2>, MULTI>(a, dl, ckpt, du_acc);
-    case 8: return run_scan_bwd<CfgB<IO, 8, 2, 1, 4, 16, MB>, MULTI>(a, dl, ckpt, du_acc);
-    case 16: return run_scan_bwd<CfgB<IO, 16, 4, 1, 4, 16, MB>, MULTI>(a, dl, ckpt, du_acc);
-    case 32: return run_scan_bwd<CfgB<IO, 32, 4, 1, 4, 16, MB>, MULTI>(a, dl, ckpt, du_acc);
-    case 64: return run_scan_bwd<CfgB<IO, 64, 4, 1, 4, 16, 2>, MULTI>(a, dl, ckpt, du_acc);
+    case 1: return run_scan_bwd<CfgB<IO, 1, 2, 1, 4, 16, 2>, MULTI, EXT>(a, dl, ckpt, du_acc);
+    case 2: return run_scan_bwd<CfgB<IO, 2, 2, 1, 4, 16, 2>, MULTI, EXT>(a, dl, ckpt, du_acc);
+    case 4: return run_scan_bwd<CfgB<IO, 4, 2, 1, 4, 16, 2>, MULTI, EXT>(a, dl, ckpt, du_acc);
+    case 8: return run_scan_bwd<CfgB<IO, 8, 2, 1, 4, 16, MB>, MULTI, EXT>(a, dl, ckpt, du_acc);
+    case 16: return run_scan_bwd<CfgB<IO, 16, 4, 1, 4, 16, MB>, MULTI, EXT>(a, dl, ckpt, du_acc);
+    case 32: return run_scan_bwd<CfgB<IO, 32, 4, 1, 4, 16, MB>, MULTI, EXT>(a, dl, ckpt, du_acc);
+    case 64: return run_scan_bwd<CfgB<IO, 64, 4, 1, 4, 16, 2>, MULTI, EXT>(a, dl, ckpt, du_acc);
     default: return fail(SS_ERR_UNSUPPORTED, "dstate %d is not one of 1,2,4,8,16,32,64", a.f.N);
     }
 }
@@ -960,10 +967,60 @@ ss_status zero_async(void *p, size_t bytes, cudaStream_t s) {
 }
 }  // namespace
 
-size_t scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t L, int N) {
+size_t scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t L, int N, bool conv) {
     if (batch <= 0 || dim <= 0 || L <= 0 || N <= 0) return 0;
-    return (size_t)batch * dim * ((L + kBwdMinBlock - 1) / kBwdMinBlock) * N * sizeof(float);
+    const size_t ck = (size_t)batch * dim * ((L + kBwdMinBlock - 1) / kBwdMinBlock) * N * sizeof(float);
+    if (!conv) return ck;
+    return align256(ck) + 2 * align256((size_t)batch * dim * L * sizeof(float));
 }
+
+namespace {
+template <typename IO>
+ss_status bwd_with_options(const BwdArgs &a) {
+    using namespace ssk;
+    const ScanArgs &f = a.f;
+    const bool ext = f.zoh || f.h0;
+    if (!f.conv) return ext ? dispatch_bwd<IO, false, true>(a) : dispatch_bwd<IO>(a);
+    // the fused Conv1D: recompute its output u, run the scan's backward pass on
+    // it into a du buffer, then turn du into the gradients of x, w, b and x0
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(f.stream);
+    const int64_t rows = f.batch * f.dim;
+    uint8_t *ws = reinterpret_cast<uint8_t *>(a.ws);
+    const size_t ck = align256((size_t)rows * ((f.L + kBwdMinBlock - 1) / kBwdMinBlock) * f.N *
+                               sizeof(float));
+    void *um = ws + ck;
+    void *dum = ws + ck + align256((size_t)rows * f.L * sizeof(float));
+    ConvSiluParams cp{};
+    cp.rows = rows;
+    cp.dim = f.dim;
+    cp.L = f.L;
+    cp.x = f.u;
+    cp.w = f.conv_w;
+    cp.bias = f.conv_b;
+    cp.x0 = f.conv_x0;
+    cp.u = um;
+    cp.du = reinterpret_cast<const float *>(dum);
+    cp.dx = a.du;
+    cp.dw = a.dconv_w;
+    cp.dbias = a.dconv_b;
+    cp.dx0 = a.dconv_x0;
+    const int64_t n = rows * f.L;
+    k_conv_silu_fwd<IO><<<(unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 32), 256, 0, s>>>(cp);
+    ss_status st = check_launch("conv1d forward");
+    if (st) return st;
+    BwdArgs b = a;
+    b.f.u = um;
+    b.du = dum;  // (unused: du goes to du_f32)
+    b.du_f32 = reinterpret_cast<float *>(dum);
+    st = dispatch_bwd<IO, false, true>(b);  // (the option instantiation writes du in fp32)
+    if (st) return st;
+    if ((st = zero_async(a.dconv_w, (size_t)f.dim * 4 * sizeof(float), s))) return st;
+    if ((st = zero_async(a.dconv_b, (size_t)f.dim * sizeof(float), s))) return st;
+    const dim3 grid((unsigned)((f.L + CONV_TS - 1) / CONV_TS), (unsigned)rows);
+    k_conv_silu_bwd<IO><<<grid, CONV_TS, 0, s>>>(cp);
+    return check_launch("conv1d backward");
+}
+}  // namespace
 
 ss_status launch_scan_bwd(const BwdArgs &a, bool empty) {
     const ScanArgs &f = a.f;
@@ -976,8 +1033,19 @@ ss_status launch_scan_bwd(const BwdArgs &a, bool empty) {
     if ((st = zero_async(a.dC, bc, s))) return st;
     if ((st = zero_async(a.dD, (size_t)f.dim * sizeof(float), s))) return st;
     if ((st = zero_async(a.dbias, (size_t)f.dim * sizeof(float), s))) return st;
-    if (empty) return SS_OK;
-    return f.io == SS_BF16 ? dispatch_bwd<__nv_bfloat16>(a) : dispatch_bwd<float>(a);
+    if (empty) {
+        // gradients of the options' tensors over an empty sequence
+        if ((st = zero_async(a.dconv_w, (size_t)f.dim * 4 * sizeof(float), s))) return st;
+        if ((st = zero_async(a.dconv_b, (size_t)f.dim * sizeof(float), s))) return st;
+        if (f.L == 0 && a.dh0) {
+            // no step: dh0 is zero (the state is not used)
+            if ((st = zero_async(a.dh0, (size_t)f.batch * f.dim * f.N * sizeof(float), s))) return st;
+        }
+        if (f.L == 0 && a.dconv_x0)
+            if ((st = zero_async(a.dconv_x0, (size_t)f.batch * f.dim * 3 * sizeof(float), s))) return st;
+        return SS_OK;
+    }
+    return f.io == SS_BF16 ? bwd_with_options<__nv_bfloat16>(a) : bwd_with_options<float>(a);
 }
 
 ss_status launch_dwconv3x3(int64_t batch, int64_t dim, int64_t H, int64_t W, int io, const void *x,

@@ -255,6 +255,40 @@ def test_backward_validates(lib):
         b.SS_ERR_WORKSPACE
 
 
+@fake_ptrs
+def test_backward_with_options_validates(lib):
+    """ss_selective_scan_bwd_opts: the options as the forward call validates
+    them, plus the gradients of their tensors."""
+    def call(chunks=0, flags=0, h0=None, conv_w=None, conv_b=None, conv_x0=None, dh0=None,
+             dconv_w=None, dconv_b=None, dconv_x0=None, wsb=None, reserved=0):
+        o = b.options(chunks, flags, h0, conv_w, conv_b, conv_x0)
+        ex = b.BwdExtras()
+        ex.dh0, ex.dconv_w, ex.dconv_b, ex.dconv_x0 = dh0, dconv_w, dconv_b, dconv_x0
+        ex.reserved[0] = reserved
+        args = list(_bwd_args())
+        if wsb is not None:
+            args[-2] = wsb
+        return lib.ss_selective_scan_bwd_opts(*args[:-3], ctypes.byref(o), ctypes.byref(ex),
+                                              *args[-3:])
+    F = A16 + 0x2000000  # a free window
+    assert call(chunks=2) == b.SS_ERR_INVALID_ARG                       # no sequence split here
+    assert call(dh0=F) == b.SS_ERR_INVALID_ARG                          # dh0 without h0
+    assert "h0" in b.last_error()
+    assert call(flags=b.SS_SCAN_CONV_SILU, conv_w=F) == b.SS_ERR_INVALID_ARG  # dconv_w missing
+    assert call(dconv_w=F + 0x100000) == b.SS_ERR_INVALID_ARG           # conv gradient, no conv
+    assert call(flags=b.SS_SCAN_CONV_SILU, conv_w=F, dconv_w=F + 0x100000,
+                dconv_b=F + 0x200000) == b.SS_ERR_INVALID_ARG           # dconv_b without conv_b
+    assert call(h0=F, dh0=F + 0x100008) == b.SS_ERR_ALIGNMENT
+    assert call(reserved=1) == b.SS_ERR_INVALID_ARG
+    assert call(flags=4) == b.SS_ERR_INVALID_ARG                        # unknown flag
+    # the Conv1D path needs room for the recomputed u and its gradient too
+    o = b.options(0, b.SS_SCAN_CONV_SILU, None, F)
+    need = int(lib.ss_workspace_bytes_opts(b.SS_KIND_SCAN_BWD, 1, 8, 32, 16, ctypes.byref(o)))
+    assert need == 8 * 4 * 16 * 4 + 2 * 8 * 32 * 4  # checkpoints + u + du, fp32 (256-aligned)
+    assert call(flags=b.SS_SCAN_CONV_SILU, conv_w=F, dconv_w=F + 0x100000,
+                wsb=need - 1) == b.SS_ERR_WORKSPACE
+
+
 def test_backward_workspace_holds_a_checkpoint_per_8_steps(lib):
     # [batch*dim, ceil(L/8), N] float32
     assert b.workspace_bytes(b.SS_KIND_SCAN_BWD, 8, 1536, 2048, 16) == 8 * 1536 * 256 * 16 * 4

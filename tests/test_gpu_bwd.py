@@ -289,3 +289,118 @@ def test_multi_bwd_larger_map(oracle):
     import selective_state_space_120_b300 as ss
     _multi_check(oracle, 32, 40, [ss.DIR_ROW, ss.DIR_COL, ss.DIR_ROW_REV, ss.DIR_COL_REV], 0,
                  batch=1, dim=40)
+
+
+# ---------------------------------------------------------------- options: ZOH, h0, Conv1D
+def _h0(wl, seed=11):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((wl.batch, wl.dim, wl.N)) * 0.5).astype(np.float32)
+
+
+def _conv(wl, seed=31, bias=True, history=True):
+    rng = np.random.default_rng(seed)
+    w = (rng.standard_normal((wl.dim, 4)) * 0.5).astype(np.float32)
+    b = (rng.standard_normal(wl.dim) * 0.1).astype(np.float32) if bias else None
+    x0 = rng.standard_normal((wl.batch, wl.dim, 3)).astype(np.float32) if history else None
+    return w, b, x0
+
+
+def _opts_case(oracle, wl, zoh=False, with_h0=False, conv=None, seed=0):
+    """The backward pass with the forward call's options against the oracle:
+    its scan gradients (zero-order hold, initial state) and, with the Conv1D,
+    its convolution followed by the scan, differentiated through both."""
+    import torch
+    import selective_state_space_120_b300 as ss
+    inp = wk.make_inputs(wl, seed=seed)
+    dout = wk.make_dout(wl, seed=seed)
+    h0 = _h0(wl) if with_h0 else None
+    t = sc.device_inputs(inp)
+    kw = {}
+    if conv is not None:
+        w, b, x0 = conv
+        kw = dict(conv_w=sc.to_torch(w), conv_b=sc.to_torch(b), conv_x0=sc.to_torch(x0))
+    g = ss.selective_scan_bwd(t["u"], t["delta"][:, 0], t["A"], t["B"][:, 0], t["C"][:, 0],
+                              sc.to_torch(dout), t["D"], t["z"], t["delta_bias"], True,
+                              h0=None if h0 is None else sc.to_torch(h0), zoh=zoh, **kw)
+    torch.cuda.synchronize()
+    got = {k: (None if v is None else sc.from_torch(v)) for k, v in g.items()}
+    u = inp.as_f64("u")
+    if conv is not None:
+        w, b, x0 = conv
+        f64 = lambda a: None if a is None else a.astype(np.float64)  # noqa: E731
+        u = oracle.conv_silu(u, f64(w), f64(b), f64(x0))
+    ref = oracle.selective_scan_bwd(u, inp.as_f64("delta")[:, 0], inp.as_f64("A"),
+                                    inp.as_f64("B")[:, 0], inp.as_f64("C")[:, 0],
+                                    _dout_f64(wl, dout), D=inp.as_f64("D"), z=inp.as_f64("z"),
+                                    delta_bias=inp.as_f64("delta_bias"), delta_softplus=True,
+                                    zoh=zoh, h0=None if h0 is None else h0.astype(np.float64))
+    names = list(NAMES)
+    if with_h0:
+        names.append("dh0")
+    if conv is not None:
+        w, b, x0 = conv
+        cg = oracle.conv_silu_bwd(inp.as_f64("u"), w.astype(np.float64), ref["du"],
+                                  None if b is None else b.astype(np.float64),
+                                  None if x0 is None else x0.astype(np.float64))
+        ref = dict(ref)
+        ref["du"] = cg["dx"]
+        ref["dconv_w"], ref["dconv_b"], ref["dconv_x0"] = cg["dw"], cg["dbias"], cg["dx0"]
+        names += ["dconv_w", "dconv_b", "dconv_x0"]
+    return assert_grads(got, ref, wl.io, names)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("L", [48, 200])
+def test_bwd_zero_order_hold(oracle, io, L):
+    """The zero-order-hold input matrix: every gradient, including dA's term
+    from the derivative of (exp(Delta'A) - 1)/A, on a ragged tail."""
+    _opts_case(oracle, sc.workload(f"bzoh{L}", 2, 40, L, io=io), zoh=True)
+
+
+def test_bwd_zero_order_hold_large_steps(oracle):
+    """|Delta' A| well above the series threshold for every state."""
+    wl = sc.workload("bzohl", 1, 24, 96, io="f32")
+    inp = wk.make_inputs(wl, seed=0)
+    inp.delta_bias[:] = 1.5
+    dout = wk.make_dout(wl, seed=0)
+    import torch
+    import selective_state_space_120_b300 as ss
+    t = sc.device_inputs(inp)
+    g = ss.selective_scan_bwd(t["u"], t["delta"][:, 0], t["A"], t["B"][:, 0], t["C"][:, 0],
+                              sc.to_torch(dout), t["D"], t["z"], t["delta_bias"], True, zoh=True)
+    torch.cuda.synchronize()
+    got = {k: (None if v is None else sc.from_torch(v)) for k, v in g.items()}
+    ref = oracle.selective_scan_bwd(inp.as_f64("u"), inp.as_f64("delta")[:, 0], inp.as_f64("A"),
+                                    inp.as_f64("B")[:, 0], inp.as_f64("C")[:, 0],
+                                    _dout_f64(wl, dout), D=inp.as_f64("D"), z=inp.as_f64("z"),
+                                    delta_bias=inp.as_f64("delta_bias"), zoh=True)
+    assert_grads(got, ref, "f32")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("L", [8, 200, 520])
+def test_bwd_initial_state(oracle, io, L):
+    """A given initial state and its gradient dh0 = Abar_0 (.) dh_0: one
+    checkpoint block, a ragged tail, and several tiles."""
+    _opts_case(oracle, sc.workload(f"bh0{L}", 2, 40, L, io=io), with_h0=True)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bwd_zero_order_hold_and_initial_state(oracle, io):
+    _opts_case(oracle, sc.workload("bzh", 2, 36, 136, G=2, io=io), zoh=True, with_h0=True)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("bias,history", [(True, True), (False, False), (True, False)])
+def test_bwd_fused_conv_silu(oracle, io, bias, history):
+    """The Conv1D + SiLU fused in front: gradients of its input x, weights,
+    bias and history, and every scan gradient, against the oracle's
+    convolution followed by its scan, differentiated through both; the
+    sequence spans two convolution tiles and a ragged tail."""
+    wl = sc.workload("bconv", 2, 40, 264, io=io)
+    _opts_case(oracle, wl, conv=_conv(wl, bias=bias, history=history))
+
+
+def test_bwd_fused_conv_with_every_option(oracle):
+    wl = sc.workload("bconvall", 2, 24, 520, io="f32")
+    _opts_case(oracle, wl, zoh=True, with_h0=True, conv=_conv(wl))
