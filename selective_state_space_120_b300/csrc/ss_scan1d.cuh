@@ -1243,8 +1243,9 @@ __global__ void __launch_bounds__(256) k_repitch(const RepitchJobs jobs) {
     const int64_t nel = jb.rows * L;    // source elements
     const IO *src = reinterpret_cast<const IO *>(jb.src);
     const uint4 *src4 = reinterpret_cast<const uint4 *>(jb.src);
-    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
-         v += (int64_t)gridDim.x * blockDim.x) {
+    // two vectors per thread and iteration, so that four 16-byte loads are in flight
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    auto vector_at = [&](int64_t v) -> uint4 {
         const int64_t r = v / vpr;
         const int64_t c0 = (v - r * vpr) * VPV;
         const int nv = (int)min((int64_t)VPV, max((int64_t)0, L - c0));  // valid elements
@@ -1298,7 +1299,14 @@ __global__ void __launch_bounds__(256) k_repitch(const RepitchJobs jobs) {
                 out = make_uint4(o[0], o[1], o[2], o[3]);
             }
         }
-        reinterpret_cast<uint4 *>(jb.dst)[v] = out;
+        return out;
+    };
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += 2 * stride) {
+        const int64_t v2 = v + stride;
+        const uint4 o1 = vector_at(v);
+        const uint4 o2 = v2 < nvec ? vector_at(v2) : make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4 *>(jb.dst)[v] = o1;
+        if (v2 < nvec) reinterpret_cast<uint4 *>(jb.dst)[v2] = o2;
     }
 }
 
@@ -1322,13 +1330,20 @@ __global__ void __launch_bounds__(256) k_merge_bidir(const float *__restrict__ s
         const float4 a = *reinterpret_cast<const float4 *>(s0 + r * Lp + p0);
         const float av[4] = {a.x, a.y, a.z, a.w};
         const float *b = s1 + r * Lp + (L - 1);
+        // every load of the group is issued before the first use
+        float bv[4], zv[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int64_t p = p0 + j;
-            if (p >= L) break;
-            float y = av[j] + b[-p];
-            if (z) y *= silu(IOT<IO>::load(z + r * L + p));
-            out[r * L + p] = IOT<IO>::from_f(y);
+            const bool in = p0 + j < L;
+            bv[j] = in ? b[-(p0 + j)] : 0.f;
+            zv[j] = (in && z) ? IOT<IO>::load(z + r * L + p0 + j) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (p0 + j >= L) break;
+            float y = av[j] + bv[j];
+            if (z) y *= silu(zv[j]);
+            out[r * L + p0 + j] = IOT<IO>::from_f(y);
         }
     }
 }
