@@ -895,11 +895,12 @@ def measure_dwconv(steps: int, warmup: int, peak_gbs: float, peak_kind: str):
 # Algorithmic work of the forward scan (fp32 lane operations, an FMA counts once;
 # SFU operations counted apart): per element, state and direction Delta'*A, x*B,
 # the state FMA and the readout FMA (4) and one exponential; per element and
-# direction about 14 more (softplus, Delta'*u, SiLU of the gate, the skip and
-# gate FMAs) and 4 SFU operations (the softplus's exponential and logarithm, the
-# gate's exponential and reciprocal).
-FWD_OPS_PER_STATE, FWD_OPS_PER_ELEM = 4, 14
-FWD_SFU_PER_STATE, FWD_SFU_PER_ELEM = 1, 4
+# direction about 10 more (the softplus, Delta'*u, the skip term, the sum over
+# directions) and 2 SFU operations (the softplus's exponential and logarithm);
+# per element, once, the gate: about 4 lane operations and 2 SFU operations
+# (SiLU's exponential and reciprocal).
+FWD_OPS_PER_STATE, FWD_OPS_PER_ELEM_DIR, FWD_OPS_GATE = 4, 10, 4
+FWD_SFU_PER_STATE, FWD_SFU_PER_ELEM_DIR, FWD_SFU_GATE = 1, 2, 2
 # ex2 results per SM and clock: 30 measured on the B300 by a probe of
 # independent ex2.approx streams over all 148 SMs (32 nominal).
 SFU_LANES_PER_SM = 30
@@ -912,14 +913,16 @@ def alu_peaks(max_mhz: int = 2032, sms: int = 148):
 
 def roofline(wl, kern_ms, peak, peak_kind):
     """The forward scan's roofline.  Of its three floors the SFU one binds at
-    N = 16 (20 SFU operations per element at 30 per SM and clock, against 78
-    fp32 lane operations at 128, and 8-13 bytes per element of HBM traffic), so
-    `frac` is the SFU fraction; the fp32 and HBM fractions sit beside it."""
+    N = 16 (20 SFU operations per element of a gated single direction at 30 per
+    SM and clock, against 78 fp32 lane operations at 128, and 8-13 bytes per
+    element of HBM traffic), so `frac` is the SFU fraction; the fp32 and HBM
+    fractions sit beside it."""
     alg = algorithmic_bytes(wl)
     ach_gbs = alg / (kern_ms * 1e-3) / 1e9
     elem_dirs = wl.elems * wl.K
-    ops = elem_dirs * (wl.N * FWD_OPS_PER_STATE + FWD_OPS_PER_ELEM)
-    sfu = elem_dirs * (wl.N * FWD_SFU_PER_STATE + FWD_SFU_PER_ELEM)
+    gated = wl.elems if wl.with_z else 0
+    ops = elem_dirs * (wl.N * FWD_OPS_PER_STATE + FWD_OPS_PER_ELEM_DIR) + gated * FWD_OPS_GATE
+    sfu = elem_dirs * (wl.N * FWD_SFU_PER_STATE + FWD_SFU_PER_ELEM_DIR) + gated * FWD_SFU_GATE
     fp32_peak, sfu_peak = alu_peaks()
     ach_sfu = sfu / (kern_ms * 1e-3) / 1e12
     return {"bound": "alu", "achieved": round(ach_sfu, 3), "peak": round(sfu_peak, 3),
