@@ -308,14 +308,20 @@ class Runner:
                  p(s["out"]), p(s["last"]), ws, wsb, st))
 
     def _launches(self):
-        """Kernels one step launches: 1; 3 on the chunked long-sequence path; one
-        per direction when the multi-direction call merges through its workspace
-        (plus the merge for an any-order call)."""
+        """Kernels one step launches: 1 on the direct path; 3 on the chunked
+        long-sequence path (two passes and the carry); 2 for a bidirectional call
+        through its workspace (the two directions over one accumulator, or the
+        direction pair and its merge over rows read through a view); 3 for SS2D
+        (the transposed copy, the four directions, the merge); for an any-order
+        call, one permuted copy of u per base traversal other than the row order,
+        one launch per two directions and the merge."""
         if self.wl.orders:
-            return (self.wl.K + 1) // 2 + 1
+            bases = {0 if o in (0, 2) else 1 if o in (1, 3) else 2 if o in (4, 6) else 3
+                     for o in self.wl.orders}
+            return len(bases - {0}) + (self.wl.K + 1) // 2 + 1
         if self.ws is None:
             return 1
-        return 3 if self.wl.K == 1 else self.wl.K
+        return {1: 3, 2: 2, 4: 3}[self.wl.K]
 
     def step(self, i: int):
         fn, args = self.args[i % self.copies]

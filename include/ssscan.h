@@ -186,13 +186,19 @@ ss_status ss_selective_scan_fwd_opts(int64_t batch, int64_t dim, int64_t seqlen,
  * directions run as two TMA-staged scans that merge through the workspace, an
  * fp32 [batch, dim, seqlen] accumulator (first direction stores, second adds,
  * gates and writes out: deterministic).
- * Otherwise the workspace is optional.  Given one of at least the size the
- * query reports (which assumes ngroups = 1: the re-pitched B and C grow with
- * ngroups), the call copies u (forward and reversed), delta, B and C into rows
- * padded to 16-byte multiples in it, scans both directions side by side as TMA
- * tiles of those copies into two fp32 slices, and merges the slices by
- * position in one more launch.  Without a workspace (NULL), or with a smaller
- * one, the call merges on chip.
+ * Otherwise the workspace is optional.  With P = (16 / element size) /
+ * gcd(seqlen, 16 / element size), the number of rows whose lengths add up to a
+ * 16-byte multiple: when P divides dim / ngroups and dstate, and the workspace
+ * holds two fp32 slices of [batch, dim, Lp] (Lp = seqlen rounded up to a
+ * 16-byte multiple), both directions run side by side as TMA scans reading the
+ * tensors in place through a view whose rows hold P of theirs, each storing
+ * its terms into one slice, and one more launch merges the slices by position.
+ * Otherwise, given at least the size the query reports (which assumes
+ * ngroups = 1: the copied B and C grow with ngroups), the call first copies u
+ * (forward and reversed), delta, B and C into rows of pitch Lp in the
+ * workspace and scans those.  Without a workspace (NULL), or with a smaller
+ * one, the call merges on chip.  The size the query reports always covers the
+ * two slices.
  */
 ss_status ss_bidir_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int ngroups,
                             ss_dtype io, const void *u, const void *delta, const float *A,

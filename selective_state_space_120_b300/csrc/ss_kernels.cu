@@ -59,6 +59,26 @@ ss_status make_map(CUtensorMap *m, const void *base, int io, uint64_t cols, uint
     return SS_OK;
 }
 
+// View of a [rows, cols] row-major tensor whose rows are not 16-byte aligned
+// as a [rows / P, P * cols] tensor (P * cols * element size a multiple of 16),
+// boxes of [box_rows, box_cols] unswizzled (the VIEW tiles of the scan).
+ss_status make_view_map(CUtensorMap *m, const void *base, int io, uint64_t cols, uint64_t rows, int P,
+                        uint32_t box_cols, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(SS_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const uint64_t es = (io == SS_BF16) ? 2 : 4;
+    cuuint64_t dims[2] = {(uint64_t)P * cols, rows / (uint64_t)P};
+    cuuint64_t strides[1] = {(uint64_t)P * cols * es};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, io == SS_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(SS_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return SS_OK;
+}
+
 ss_status check_launch(const char *what) {
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SS_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
@@ -434,6 +454,72 @@ struct Scan1d {
         return check_launch("bidirectional merge");
     }
 
+    // Bidirectional call over rows that are not 16-byte aligned, read in place
+    // through VIEW tiles (C is a VIEW configuration; P = 1 << vshift rows per
+    // view row): the two directions scan side by side, direction 1 reading u's
+    // tiles back to front, each storing y_k + D_k*u by scan step into an fp32
+    // slice of pitch Lp, and one more launch sums the slices by position and
+    // gates -- the re-pitched path without its copies.
+    static ss_status run_bidir_view(const ScanArgs &a, int vshift) {
+        using namespace ssk;
+        using IO = typename C::IO;
+        static_assert(C::VIEW, "a VIEW configuration");
+        const int io = a.io;
+        const int P = 1 << vshift;
+        const int64_t rows = a.batch * a.dim;
+        const int64_t Lp = padded_len(a);
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(a.stream);
+        float *s0 = reinterpret_cast<float *>(a.ws);
+        float *s1 = s0 + rows * Lp;
+        const int64_t bcrows = a.batch * 2 * a.G * C::N;
+        ss_status st;
+        CUtensorMap mu, md, mb, mc;
+        if ((st = make_view_map(&mu, a.u, io, a.L, rows, P, C::BW, C::CB >> vshift))) return st;
+        if ((st = make_view_map(&md, a.delta, io, a.L, (uint64_t)rows * 2, P, C::BW, C::CB >> vshift))) return st;
+        if ((st = make_view_map(&mb, a.B, io, a.L, (uint64_t)bcrows, P, C::BW, C::N >> vshift))) return st;
+        if ((st = make_view_map(&mc, a.C, io, a.L, (uint64_t)bcrows, P, C::BW, C::N >> vshift))) return st;
+        auto kern = k_scan1d<C, true>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
+        Scan1dParams p{};
+        p.dim = a.dim;
+        p.L = a.L;
+        p.pitch = Lp;
+        p.vshift = vshift;
+        p.G = a.G;
+        p.dpg = (int)(a.dim / a.G);
+        p.Lc = a.L;
+        p.J = 1;
+        p.jbase = 0;
+        p.pass = 0;
+        p.K = 2;
+        p.u_g = a.u;
+        p.A = a.A;
+        p.D = a.D;
+        p.bias = a.bias;
+        p.softplus = a.softplus;
+        p.has_z = 0;
+        p.out = a.out;
+        p.last_state = a.last_state;
+        p.nz = 2;
+        p.k0 = 0;
+        p.orders_z[0] = ORD_ROW;
+        p.orders_z[1] = ORD_ROW_REV;
+        for (int d = 0; d < 2; ++d) {
+            p.modes_z[d] = OUT_STEP;
+            p.accs_z[d] = d == 0 ? s0 : s1;
+        }
+        const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);
+        const unsigned bgs = (unsigned)(a.batch * a.G);
+        kern<<<dim3(cblocks, bgs, 2), C::THREADS, C::SMEM, s>>>(mu, md, mu, mb, mc, mu, p);
+        if ((st = check_launch("direction pair scan"))) return st;
+        const int64_t groups = rows * ((a.L + 3) / 4);
+        const unsigned mblocks = (unsigned)std::min<int64_t>((groups + 255) / 256, (int64_t)num_sms() * 32);
+        k_merge_bidir<IO><<<mblocks, 256, 0, s>>>(s0, s1, reinterpret_cast<const IO *>(a.z),
+                                                  reinterpret_cast<IO *>(a.out), rows, a.L, Lp);
+        return check_launch("bidirectional merge");
+    }
+
     // K directions of any order: each launch stores its direction's y_k + D_k*u
     // by scan step into its own fp32 accumulator; one merge inverts the
     // traversals and sums by position.
@@ -586,6 +672,33 @@ template <typename IO, int N>
 ss_status dispatch_bidir_padded(const ScanArgs &a) {
     using C = typename Pick1d<IO, N>::C;
     return Scan1d<C>::run_bidir_padded(a);
+}
+
+// The VIEW configuration of a (I/O type, N) configuration: a 2-stage ring
+// (a third stage measured no faster on the Vision Mamba shape).
+template <class C>
+using ViewCfg = ssk::Cfg1<typename C::IO, C::N, C::NPT, C::W, 2, C::CL, C::PIPE ? 1 : 0, 0, 1>;
+// four CTAs per SM (by shared memory) for the Vision Mamba shape's configuration
+static_assert(ViewCfg<Pick1d<__nv_bfloat16, 16>::C>::SMEM + 1024 <= 228 * 1024 / 4,
+              "VIEW tiles of N = 16 fit four CTAs per SM");
+
+template <typename IO, int N>
+ss_status dispatch_bidir_view(const ScanArgs &a, int vshift) {
+    using C = ViewCfg<typename Pick1d<IO, N>::C>;
+    return Scan1d<C>::run_bidir_view(a, vshift);
+}
+
+template <typename IO>
+ss_status dispatch_bidir_view_n(const ScanArgs &a, int vshift) {
+    switch (a.N) {
+    case 2: return dispatch_bidir_view<IO, 2>(a, vshift);
+    case 4: return dispatch_bidir_view<IO, 4>(a, vshift);
+    case 8: return dispatch_bidir_view<IO, 8>(a, vshift);
+    case 16: return dispatch_bidir_view<IO, 16>(a, vshift);
+    case 32: return dispatch_bidir_view<IO, 32>(a, vshift);
+    case 64: return dispatch_bidir_view<IO, 64>(a, vshift);
+    default: return fail(SS_ERR_UNSUPPORTED, "dstate %d cannot be read through VIEW tiles", a.N);
+    }
 }
 
 template <typename IO>
@@ -784,6 +897,26 @@ bool bidir_padded_ok(const ScanArgs &a) {
     return 2 * rows < (1ll << 31) && a.batch * 2 * a.G * a.N < (1ll << 31) && a.L < (1ll << 30);
 }
 
+// log2 of the rows folded into one view row for a bidirectional call read in
+// place through VIEW tiles, or -1 when the call cannot take that path: its rows
+// are 16-byte aligned, or P does not divide the channels per group or N (so
+// that every box holds whole rows of one channel block or one B/C tile).
+int bidir_view_shift(const ScanArgs &a) {
+    if (!bidir_padded_ok(a)) return -1;
+    const int64_t vpc = a.io == SS_BF16 ? 8 : 4;  // values per 16 bytes (a power of two)
+    int64_t g = 1;
+    while (g < vpc && a.L % (2 * g) == 0) g *= 2;  // gcd(L, vpc)
+    const int64_t P = vpc / g;
+    const int64_t dpg = a.dim / a.G;
+    if (P < 2 || dpg % P != 0 || a.N % P != 0) return -1;
+    if (P * a.L >= (1ll << 31)) return -1;
+    return P == 2 ? 1 : P == 4 ? 2 : 3;
+}
+// Workspace of the VIEW path: the two directions' fp32 slices [2, rows, Lp].
+size_t bidir_view_bytes(const ScanArgs &a) {
+    return align256((size_t)2 * a.batch * a.dim * padded_len(a) * sizeof(float));
+}
+
 size_t multidir_workspace_bytes(const ScanArgs &a) {
     if (bidir_padded_ok(a)) return bidir_padded_bytes(a);
     if (!scan1d_uses_tma(a)) return 0;  // rows not 16-byte aligned: on-chip merge path
@@ -805,7 +938,12 @@ ss_status launch_steps(const ScanArgs &a) {
 
 ss_status launch_multidir(const ScanArgs &a) {
     if (bidir_padded_ok(a)) {
-        // re-pitched TMA path when the caller gave the workspace, else on chip
+        // rows read in place through VIEW tiles, or re-pitched, when the caller
+        // gave the workspace; else on chip
+        const int vshift = bidir_view_shift(a);
+        if (vshift > 0 && a.ws && a.ws_bytes >= bidir_view_bytes(a))
+            return a.io == SS_BF16 ? dispatch_bidir_view_n<__nv_bfloat16>(a, vshift)
+                                   : dispatch_bidir_view_n<float>(a, vshift);
         if (a.ws && a.ws_bytes >= bidir_padded_bytes(a))
             return a.io == SS_BF16 ? dispatch_bidir_padded_n<__nv_bfloat16>(a)
                                    : dispatch_bidir_padded_n<float>(a);

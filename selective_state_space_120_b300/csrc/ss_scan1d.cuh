@@ -52,7 +52,7 @@
 namespace ssk {
 
 template <typename IO_, int N_, int NPT_, int W_, int STAGES_, int CL_ = 1, int PIPE_ = 0,
-          int OVL_ = 0>
+          int OVL_ = 0, int VIEW_ = 0>
 struct Cfg1 {
     using IO = IO_;
     static constexpr int N = N_, NPT = NPT_, W = W_, STAGES = STAGES_, CL = CL_;
@@ -70,17 +70,40 @@ struct Cfg1 {
     static constexpr int TP = T / 2;     // step pairs per chunk
     static constexpr int PT = R / CL;    // prep threads per channel
     static constexpr int E = T / PT;     // consecutive steps prepped by one thread
+    static constexpr int VPC = 16 / ES;  // values per 16 bytes
     static_assert(N % NPT == 0 && R >= 1 && R <= 32 && (R & (R - 1)) == 0, "lane split");
     static_assert(CL >= 1 && CL <= R && R % CL == 0, "channels per lane");
     static_assert(E >= 2 && E % 2 == 0 && E * ES >= 4, "a prep thread owns whole step pairs");
     static_assert(CB <= 256 && N <= 256, "TMA box rows");
 
-    static constexpr int al(int x) { return (x + 1023) & ~1023; }
-    static constexpr int TILE_CH = al(CB * 64);
-    static constexpr int TILE_BC = al(N * 64);
-    static constexpr int STAGE = 3 * TILE_CH + 2 * TILE_BC;
+    // VIEW: rows whose length is not a multiple of 16 bytes, read in place
+    // through a view of the tensor whose rows hold P consecutive rows of it
+    // (P * L * ES a multiple of 16, P a power of two dividing CB and N).  Each
+    // chunk is P boxes, one per residue of the row index mod P, each starting
+    // at the 16-byte boundary at or below its first step: tile rows hold
+    // BW = T + VPC values, unswizzled, with the chunk's first step at a per-box
+    // offset below VPC.  Used by the direction-pair launch, which has no z tile.
+    // A box lands at a 128-byte boundary (the copy's rule for its shared-memory
+    // address): box j of a tile of `rows` rows starts at j * box_stride.
+    static constexpr bool VIEW = VIEW_ != 0;
+    static constexpr int BW = VIEW ? T + VPC : T;  // values per tile row
+    static constexpr int ROWB = BW * ES;           // bytes per tile row
+    static constexpr int al(int x) { return VIEW ? (x + 127) & ~127 : (x + 1023) & ~1023; }
+    static __host__ __device__ constexpr int box_stride(int rows, int vshift) {
+        return (((rows >> vshift) * ROWB) + 127) & ~127;
+    }
+    static constexpr int view_tile(int rows) {  // the largest over P = 2, 4, 8
+        int m = 0;
+        for (int vs = 1; vs <= 3; ++vs)
+            if ((rows >> vs) > 0 && (1 << vs) * box_stride(rows, vs) > m) m = (1 << vs) * box_stride(rows, vs);
+        return m;
+    }
+    static constexpr int TILE_CH = VIEW ? view_tile(CB) : al(CB * ROWB);
+    static constexpr int TILE_BC = VIEW ? view_tile(N) : al(N * ROWB);
+    static constexpr int NCHT = VIEW ? 2 : 3;      // channel tiles per stage: u, Delta (, z)
+    static constexpr int STAGE = NCHT * TILE_CH + 2 * TILE_BC;
     static constexpr int OFF_U = 0, OFF_DL = TILE_CH, OFF_Z = 2 * TILE_CH;
-    static constexpr int OFF_B = 3 * TILE_CH, OFF_C = 3 * TILE_CH + TILE_BC;
+    static constexpr int OFF_B = NCHT * TILE_CH, OFF_C = NCHT * TILE_CH + TILE_BC;
     // BCW: keep B/C as bf16 pairs (B[t], B[t+1]) in one 32-bit word (exact for
     // bf16 inputs), halving the shared-memory bytes each lane reads at the cost
     // of two integer ops per word to widen them.  Measured slower on the B300
@@ -90,7 +113,10 @@ struct Cfg1 {
     static_assert(!BCW || PIPE, "packed B/C words are read by the pipelined step loop");
     static constexpr int OFF_BC = STAGES * STAGE;
     static constexpr int DXROW = (TP + 1) * 16;  // one padding slot per row
-    static constexpr int PREPBUF = 2 * CB * DXROW;  // dx and gd rows of one chunk
+    // gd rows: (gate, D*u*gate) per step; a VIEW launch has no gate: D*u only
+    // (two padding slots: the channels of a warp start on distinct 16-byte groups)
+    static constexpr int GDROW = VIEW ? (TP + 2) * 8 : DXROW;
+    static constexpr int PREPBUF = CB * (DXROW + GDROW);  // dx and gd rows of one chunk
     static constexpr int NPREP = OVL ? 2 : 1;      // prep row buffers
     static constexpr int OFF_DX = OFF_BC + 2 * BCBUF;
     static constexpr int OFF_GD = OFF_DX + CB * DXROW;
@@ -98,8 +124,11 @@ struct Cfg1 {
     static constexpr int OFF_OB = OFF_DX + NPREP * PREPBUF;
     // fused Conv1D: each channel's last three inputs of a chunk, double-buffered
     static constexpr int OFF_HALO = OFF_OB + CB * OBROW;
-    static constexpr int OFF_BAR = (OFF_HALO + 2 * CB * 16 + 7) & ~7;
-    static constexpr int SMEM = OFF_BAR + 8 * STAGES + 1024;  // + alignment slack
+    static constexpr int HALO = VIEW ? 0 : 2 * CB * 16;
+    static constexpr int OFF_BAR = (OFF_HALO + HALO + 7) & ~7;
+    // alignment of the tiles: 1024 bytes for the swizzled ones, 128 for VIEW
+    static constexpr int SALIGN = VIEW ? 128 : 1024;
+    static constexpr int SMEM = OFF_BAR + 8 * STAGES + SALIGN;  // + alignment slack
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
 };
 
@@ -125,6 +154,7 @@ struct Scan1dParams {
     int mode;     // OUT_*
     float *acc;   // [batch*dim, L] fp32 merge accumulator by position (modes 1-3)
     int64_t pitch;  // row pitch (elements) of the accumulators; L unless the inputs are re-pitched
+    int vshift;     // VIEW tiles: log2 of the rows folded into one view row
     // Multi-direction launches may scan several directions side by side:
     // blockIdx.z = d selects direction k0 + d with its own order, mode and
     // accumulator (entries [0, nz)); odd d read u through the second map.
@@ -263,6 +293,75 @@ __device__ __forceinline__ float load_tile_elem(const uint8_t *tile, int row, in
         return __uint_as_float((uint32_t)(*reinterpret_cast<const unsigned short *>(tile + off)) << 16);
     else
         return *reinterpret_cast<const float *>(tile + off);
+}
+
+// VIEW tiles.  Byte offset of row r of a tile of `rows` rows: box r mod P,
+// row r / P of that box.
+template <class C>
+__device__ __forceinline__ int view_row_off(int r, int rows, int vshift) {
+    return (r & ((1 << vshift) - 1)) * C::box_stride(rows, vshift) + (r >> vshift) * C::ROWB;
+}
+// Offset of a chunk's first step in the box of row residue j: the distance
+// from view column j*L + x down to a 16-byte boundary.  Chunks start on
+// multiples of T (forward) or end on L less one (back to front), so the offset
+// is (j*L) mod VPC forward and ((j+1)*L) mod VPC back to front for every chunk.
+template <class C>
+__device__ __forceinline__ int view_mis(int j, int L) {
+    return (j * L) & (C::VPC - 1);
+}
+// E consecutive values from column col0 of the tile row at byte offset rowoff
+// (ROWB bytes a row, no swizzle), which need not start on a 16-byte boundary:
+// aligned 32-bit words, shifted into place (a shift of 0 or 16 bits for bf16).
+// Callers keep col0 + E <= BW - 1, which keeps every word read inside the row.
+template <class C, int E>
+__device__ __forceinline__ void load_view_row(const uint8_t *tile, int rowoff, int col0, float *v) {
+    using IO = typename C::IO;
+    constexpr int PER = 4 / C::ES;
+    constexpr int NW = E * C::ES / 4;  // whole words of output
+    const int off = rowoff + col0 * C::ES;
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(tile + (off & ~3));
+    if constexpr (C::ES == 4) {
+#pragma unroll
+        for (int k = 0; k < NW; ++k) unpack_word(w[k], v + k * PER, (IO *)nullptr);
+    } else {
+        const uint32_t sh = (uint32_t)(off & 3) * 8u;
+        uint32_t ww[NW + 1];
+#pragma unroll
+        for (int k = 0; k <= NW; ++k) ww[k] = w[k];
+#pragma unroll
+        for (int k = 0; k < NW; ++k) unpack_word(__funnelshift_r(ww[k], ww[k + 1], sh), v + k * PER, (IO *)nullptr);
+    }
+}
+
+// convert_bc over VIEW tiles: the B/C rows of a chunk of T steps starting on a
+// multiple of T, of which the first `nvalid` exist (the rest are zeroed: in the
+// view they are the next row's values or past the tensor).
+template <class C>
+__device__ __forceinline__ void convert_bc_view(const uint8_t *tB, const uint8_t *tC, float *bc, int tid,
+                                                bool with_c, int L, int vshift, int nvalid) {
+    constexpr int VPC = C::VPC;
+    // segment-fastest tasks: the rows of one LDS start on the same bank (boxes
+    // sit on 128-byte boundaries), so a warp spreads over segments first
+#pragma unroll 1
+    for (int task = tid; task < 8 * C::N; task += C::THREADS) {
+        const int q = task & 3;  // VPC steps of the chunk
+        const int n = (task >> 2) % C::N;
+        const int isC = (task >> 2) / C::N;
+        if (isC && !with_c) continue;
+        float v[VPC];
+        const int col0 = view_mis<C>(n & ((1 << vshift) - 1), L) + q * VPC;
+        load_view_row<C, VPC>(isC ? tC : tB, view_row_off<C>(n, C::N, vshift), col0, v);
+        if (nvalid < C::T) {
+#pragma unroll
+            for (int e = 0; e < VPC; ++e)
+                if (q * VPC + e >= nvalid) v[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < VPC; e += 2) {
+            const int tp = (q * VPC + e) >> 1;
+            *reinterpret_cast<float2 *>(bc + tp * 4 * C::N + isC * 2 * C::N + 2 * n) = make_float2(v[e], v[e + 1]);
+        }
+    }
 }
 
 // Scans one chunk of T steps for this lane's CL channels and state slice.
@@ -681,7 +780,7 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
     const CUtensorMap *umap = (MULTI && (blockIdx.z & 1u)) ? &tm_u2 : &tm_u;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t *smem = smem_raw + ((C::SALIGN - (raw_addr & (C::SALIGN - 1u))) & (C::SALIGN - 1u));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q = lane % C::CPW, g = lane / C::CPW;
@@ -701,7 +800,8 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
     // the chunk-local pass needs only the end states of chunks 1..J-2: no
     // readout, so no C tiles, no gate and no skip term
     const bool do_y = (p.pass != 1) || (jc == 0);
-    const bool gate_in_prep = do_y && (p.mode == OUT_STORE) && p.has_z;
+    const bool gate_in_prep = !C::VIEW && do_y && (p.mode == OUT_STORE) && p.has_z;
+    static_assert(!C::VIEW || MULTI, "VIEW tiles serve the direction-pair launch");
 
     // scan role: channels ch[c] (within the CTA) of this lane's group
     int chs[CL];
@@ -731,6 +831,12 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
     // prep role: E consecutive steps of channel pch, starting at step pt0 of the chunk
     const int pch = tid / C::PT;
     const int pt0 = (tid % C::PT) * E;
+    // VIEW tiles: the prep channel's row in a tile and its chunks' offsets
+    // there (forward, and back to front for u of a reversed order)
+    const int vj = C::VIEW ? pch & ((1 << p.vshift) - 1) : 0;
+    const int vroff = C::VIEW ? view_row_off<C>(pch, C::CB, p.vshift) : 0;
+    const int vmis_f = C::VIEW ? view_mis<C>(vj, (int)p.L) : 0;
+    const int vmis_r = C::VIEW ? view_mis<C>(vj + 1, (int)p.L) : 0;
     const int pdg = cblk * C::CB + pch;
     const bool pvalid = pdg < p.dpg;
     const int64_t pd = (int64_t)grp * p.dpg + (pvalid ? pdg : p.dpg - 1);
@@ -752,9 +858,13 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
     const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
     const uint32_t smem0 = smem_u32(smem);
     const bool z_tiled = gate_in_prep;
-    const uint32_t tx_bytes = (2u + (z_tiled ? 1u : 0u)) * C::CB * 64u +
-                              (do_y ? 2u : 1u) * N * 64u;
+    const uint32_t tx_bytes = (2u + (z_tiled ? 1u : 0u)) * C::CB * (uint32_t)C::ROWB +
+                              (do_y ? 2u : 1u) * N * (uint32_t)C::ROWB;
     const uint64_t budget = g_wait_budget_ns;
+    // VIEW tiles take P boxes per tensor a chunk: lane 0 of every warp issues
+    // those of its tensors (each warp arrives on the stage's barrier with its
+    // own bytes); other tiles, one box per tensor, all issued by thread 0
+    const bool issuer = C::VIEW ? (lane == 0) : (tid == 0);
 
     if (tid == 0) {
         prefetch_tensormap(umap);
@@ -763,7 +873,7 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
         prefetch_tensormap(&tm_C);
         if (p.has_z) prefetch_tensormap(&tm_z);
 #pragma unroll 1
-        for (int s = 0; s < C::STAGES; ++s) mbar_init(bar0 + 8 * s, 1);
+        for (int s = 0; s < C::STAGES; ++s) mbar_init(bar0 + 8 * s, C::VIEW ? C::W : 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -780,6 +890,28 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
         // u/z tile of a reversed row order: positions L-(i+1)T .. L-1-iT (may
         // start below 0 on the last chunk; the copy fills zeros there)
         const int xu = (p.order == 2) ? (int)(p.L - (int64_t)(i + 1) * T) : x;
+        if constexpr (C::VIEW) {
+            // warp w issues tensors w, w + W, ... of (u, Delta, B, C): box j
+            // holds the rows r = j mod P, from view column j*L + first step
+            // rounded down to a 16-byte boundary (a negative column reads
+            // zeros; columns of a neighbouring row are masked by the prep)
+            const int vs = p.vshift, P = 1 << vs, L32 = (int)p.L;
+            const int ntens = do_y ? 4 : 3;
+            uint32_t bytes = 0;
+            for (int tsel = warp; tsel < ntens; tsel += C::W) bytes += (tsel < 2 ? C::CB : N) * C::ROWB;
+            mbar_expect_tx(bar, bytes);
+            for (int tsel = warp; tsel < ntens; tsel += C::W) {
+                const CUtensorMap *map = tsel == 0 ? umap : tsel == 1 ? &tm_dl : tsel == 2 ? &tm_B : &tm_C;
+                const int vrow = (tsel == 0 ? row_tma : tsel == 1 ? dlrow_tma : bcrow_tma) >> vs;
+                const uint32_t dst = st + (tsel == 0 ? C::OFF_U : tsel == 1 ? C::OFF_DL : tsel == 2 ? C::OFF_B : C::OFF_C);
+                const int bs = C::box_stride(tsel < 2 ? C::CB : N, vs);
+                int xj = tsel == 0 ? xu : x;  // view column of box j's first step
+#pragma unroll 1
+                for (int j = 0; j < P; ++j, xj += L32)
+                    tma_load_2d(dst + j * bs, map, xj & ~(C::VPC - 1), vrow, bar);
+            }
+            return;
+        }
         mbar_expect_tx(bar, tx_bytes);
         tma_load_2d(st + C::OFF_U, umap, xu, row_tma, bar);
         tma_load_2d(st + C::OFF_DL, &tm_dl, x, dlrow_tma, bar);
@@ -787,7 +919,7 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
         tma_load_2d(st + C::OFF_B, &tm_B, x, bcrow_tma, bar);
         if (do_y) tma_load_2d(st + C::OFF_C, &tm_C, x, bcrow_tma, bar);
     };
-    if (tid == 0) {
+    if (issuer) {
 #pragma unroll 1
         for (int i = 0; i < C::STAGES && i < nchunks; ++i) issue(i);
     }
@@ -799,13 +931,29 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
     auto prep_chunk = [&](int i) {
         const int s = i % C::STAGES;
         const uint8_t *st = smem + s * C::STAGE;
-        convert_bc<C>(st + C::OFF_B, st + C::OFF_C, bcbuf0 + (i & 1) * (C::BCBUF / 4), tid, do_y);
+        const int64_t xc = t_begin + (int64_t)i * T;  // first step of the chunk
+        if constexpr (C::VIEW)
+            convert_bc_view<C>(st + C::OFF_B, st + C::OFF_C, bcbuf0 + (i & 1) * (C::BCBUF / 4), tid, do_y,
+                               (int)p.L, p.vshift, (int)min((int64_t)T, t_end - xc));
+        else
+            convert_bc<C>(st + C::OFF_B, st + C::OFF_C, bcbuf0 + (i & 1) * (C::BCBUF / 4), tid, do_y);
         const int pb = C::OVL ? (i & 1) : 0;
         float4 *pdxrow = reinterpret_cast<float4 *>(smem + C::OFF_DX + pb * C::PREPBUF +
                                                     pch * C::DXROW);
         float4 *pgdrow = reinterpret_cast<float4 *>(smem + C::OFF_GD + pb * C::PREPBUF +
-                                                    pch * C::DXROW);
+                                                    pch * C::GDROW);
         float uu[E], dd[E], zz[E];
+        if constexpr (C::VIEW) {
+            load_view_row<C, E>(st + C::OFF_DL, vroff, vmis_f + pt0, dd);
+            if (p.order == 0) {
+                load_view_row<C, E>(st + C::OFF_U, vroff, vmis_f + pt0, uu);
+            } else {
+                float tmp[E];
+                load_view_row<C, E>(st + C::OFF_U, vroff, vmis_r + T - pt0 - E, tmp);
+#pragma unroll
+                for (int e = 0; e < E; ++e) uu[e] = tmp[E - 1 - e];
+            }
+        } else {
         load_tile_row<IO, E>(st + C::OFF_DL, pch, pt0, dd);
         if (p.order == 0) {
             load_tile_row<IO, E>(st + C::OFF_U, pch, pt0, uu);
@@ -821,6 +969,7 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
 #pragma unroll
                 for (int e = 0; e < E; ++e) zz[e] = tmp[E - 1 - e];
             }
+        }
         }
         if (conv) {
             // raw inputs at columns pt0-3 .. pt0-1: this tile, or the previous
@@ -876,11 +1025,17 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
                 xx[k] = (EXT && !MULTI && p.zoh) ? uu[e + k] : v * uu[e + k];
                 ga[k] = gate_in_prep ? silu(zz[e + k]) : 1.f;
                 du[k] = Dd * uu[e + k] * ga[k];
+                if (C::VIEW && lim < E && e + k >= lim) {
+                    // a VIEW tile holds the neighbouring row's values there
+                    xx[k] = 0.f;
+                    du[k] = 0.f;
+                }
                 if (p.pass == 1) sdt_acc += v;
             }
             const int slot = swz_slot((pt0 + e) >> 1);
             pdxrow[slot] = make_float4(dl[0], dl[1], xx[0], xx[1]);
-            if (do_y) pgdrow[slot] = make_float4(ga[0], du[0], ga[1], du[1]);
+            if constexpr (C::VIEW) reinterpret_cast<float2 *>(pgdrow)[slot] = make_float2(du[0], du[1]);
+            else if (do_y) pgdrow[slot] = make_float4(ga[0], du[0], ga[1], du[1]);
         }
     };
     // Bounded wait for chunk i's tiles; on timeout the whole CTA drains its
@@ -903,7 +1058,7 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
         const bool ok = mbar_wait_bounded(bar0, 0, budget);
         if (ok) prep_chunk(0);
         if (abandon(0, ok)) return;
-        if (tid == 0 && C::STAGES < nchunks) {
+        if (issuer && C::STAGES < nchunks) {
             fence_proxy_async_smem();
             issue(C::STAGES);
         }
@@ -923,7 +1078,7 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
             ok = mbar_wait_bounded(bar0 + 8 * (i % C::STAGES), (i / C::STAGES) & 1, budget);
             if (ok) prep_chunk(i);
             if (abandon(i, ok)) return;
-            if (tid == 0 && i + C::STAGES < nchunks) {
+            if (issuer && i + C::STAGES < nchunks) {
                 fence_proxy_async_smem();
                 issue(i + C::STAGES);
             }
@@ -939,11 +1094,17 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
             dxrows[c] = reinterpret_cast<const float4 *>(smem + C::OFF_DX + rb * C::PREPBUF +
                                                          chs[c] * C::DXROW);
             gdrows[c] = reinterpret_cast<const float4 *>(smem + C::OFF_GD + rb * C::PREPBUF +
-                                                         chs[c] * C::DXROW);
+                                                         chs[c] * C::GDROW);
         }
         auto emit = [&](int c, float y, int t) {
-            const float2 ge = reinterpret_cast<const float2 *>(gdrows[c] + swz_slot(t >> 1))[t & 1];
-            const float v = fmaf(y, ge.x, ge.y);
+            float v;
+            if constexpr (C::VIEW) {
+                // D*u only (VIEW rows of GDROW bytes: two floats a step pair)
+                v = y + reinterpret_cast<const float *>(gdrows[c])[2 * swz_slot(t >> 1) + (t & 1)];
+            } else {
+                const float2 ge = reinterpret_cast<const float2 *>(gdrows[c] + swz_slot(t >> 1))[t & 1];
+                v = fmaf(y, ge.x, ge.y);
+            }
             if (p.mode == OUT_STORE) reinterpret_cast<IO *>(obrows[c])[t] = IOT<IO>::from_f(v);
             else reinterpret_cast<float *>(obrows[c])[t] = v;
         };
@@ -984,7 +1145,7 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
         if constexpr (C::OVL) {
             // chunk i+1's tiles are consumed and chunk i's rows are read: refill
             if (abandon(i + 1, ok)) return;
-            if (tid == 0 && more && i + 1 + C::STAGES < nchunks) {
+            if (issuer && more && i + 1 + C::STAGES < nchunks) {
                 fence_proxy_async_smem();
                 issue(i + 1 + C::STAGES);
             }

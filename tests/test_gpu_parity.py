@@ -361,22 +361,66 @@ def test_bidirectional_unaligned_rows_without_workspace(oracle, L, io):
 
 @pytest.mark.parametrize("L", [1, 5, 9, 197, 1001])
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_bidirectional_repitched_rows(oracle, L, io):
-    """Rows that are not 16-byte aligned, with the workspace: the inputs are
-    re-pitched and both directions run as TMA scans (several channel blocks and
-    a partial last one, N = 8)."""
-    _check(oracle, sc.workload(f"bi_rp{L}", 3, 72, L, N=8, K=2, io=io))
+def test_bidirectional_view_rows(oracle, L, io):
+    """Rows that are not 16-byte aligned, with the workspace: both directions
+    run as TMA scans that read the rows in place through a view of P rows to a
+    view row (P = 8 in bf16, 4 in fp32; several channel blocks and a partial
+    last one, N = 8)."""
+    _check(oracle, sc.workload(f"bi_v{L}", 3, 72, L, N=8, K=2, io=io))
+
+
+@pytest.mark.parametrize("L,io", [(198, "bf16"), (196, "bf16"), (198, "f32"), (102, "f32")])
+@pytest.mark.parametrize("N", [4, 16])
+def test_bidirectional_view_rows_fold(oracle, L, io, N):
+    """Two or four rows to a view row (L = 198 and 196 in bf16, 198 and 102 in
+    fp32), with N = 4 (one B row to a box) and N = 16."""
+    _check(oracle, sc.workload(f"bi_vf{L}", 2, 40, L, N=N, K=2, io=io))
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_bidirectional_repitched_rows_groups(oracle, io):
-    """Two groups: the re-pitched B and C grow with ngroups, so the workspace
-    the size query reports (one group) is too small and the call merges on
-    chip; given room for both groups' copies it re-pitches.  Both agree with
-    the oracle."""
+def test_bidirectional_view_rows_isolate_channels(oracle, io):
+    """A view tile holds the neighbouring rows' values past each row's ends: a
+    NaN in one channel's u and an infinite Delta in another's must not reach
+    any other channel (the rest match the oracle on the clean inputs)."""
     import torch
     import selective_state_space_120_b300 as ss
-    wl = sc.workload("bi_rpg", 2, 48, 197, N=8, G=2, K=2, io=io)
+    wl = sc.workload("bi_viso", 2, 16, 197, N=8, K=2, io=io)
+    inp = wk.make_inputs(wl, seed=0)
+    t = sc.device_inputs(inp)
+    t["u"][0, 5] = float("nan")
+    t["delta"][0, :, 10] = float("inf")
+    out, last = ss.bidir_scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                                  t["delta_bias"], True, return_last_state=True)
+    torch.cuda.synchronize()
+    ref, ref_last = sc.oracle_run(oracle, inp)
+    keep = [d for d in range(wl.dim) if d not in (5, 10)]
+    got = sc.from_torch(out)
+    sc.assert_close(got[0, keep], ref[0, keep], io)
+    sc.assert_close(got[1], ref[1], io)
+    got_last = last.cpu().numpy().astype(np.float64)
+    sc.assert_close(got_last[0][:, keep], ref_last[0][:, keep], io, "last_state")
+
+
+@pytest.mark.parametrize("L", [5, 197])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bidirectional_repitched_rows(oracle, L, io):
+    """Channels per group that P does not divide (18): the inputs are copied
+    into rows of a 16-byte pitch, and both directions run as TMA scans."""
+    _check(oracle, sc.workload(f"bi_rp{L}", 3, 18, L, N=8, K=2, io=io))
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("dim", [48, 36])
+def test_bidirectional_repitched_rows_groups(oracle, io, dim):
+    """Two groups, given the workspace the size query reports (sized for one
+    group) and given more.  24 channels a group: read in place through the view
+    either way (its two slices do not grow with the groups).  18 channels a
+    group: the re-pitched B and C grow with the groups, so the reported size is
+    too small and the call merges on chip; with room it re-pitches.  All agree
+    with the oracle."""
+    import torch
+    import selective_state_space_120_b300 as ss
+    wl = sc.workload(f"bi_rpg{dim}", 2, dim, 197, N=8, G=2, K=2, io=io)
     inp = wk.make_inputs(wl, seed=0)
     t = sc.device_inputs(inp)
     ref, ref_last = sc.oracle_run(oracle, inp)
