@@ -674,13 +674,17 @@ ss_status dispatch_bidir_padded(const ScanArgs &a) {
     return Scan1d<C>::run_bidir_padded(a);
 }
 
-// The VIEW configuration of a (I/O type, N) configuration: a 2-stage ring
-// (a third stage measured no faster on the Vision Mamba shape).
+// The VIEW configuration of a (I/O type, N) configuration: a 2-stage ring, and
+// twice the warps when a CTA has at most 32 channels.  A VIEW chunk takes P
+// boxes per tensor and the copy engine's time goes by boxes, so more channels
+// per box pays: on the Vision Mamba shape 328 us a call with 8 warps of 64
+// channels, 338 with 4 warps, 350 with 16 (a third ring stage: no faster).
 template <class C>
-using ViewCfg = ssk::Cfg1<typename C::IO, C::N, C::NPT, C::W, 2, C::CL, C::PIPE ? 1 : 0, 0, 1>;
-// four CTAs per SM (by shared memory) for the Vision Mamba shape's configuration
-static_assert(ViewCfg<Pick1d<__nv_bfloat16, 16>::C>::SMEM + 1024 <= 228 * 1024 / 4,
-              "VIEW tiles of N = 16 fit four CTAs per SM");
+using ViewCfg = ssk::Cfg1<typename C::IO, C::N, C::NPT, (C::CB <= 32 ? 2 * C::W : C::W), 2, C::CL,
+                          C::PIPE ? 1 : 0, 0, 1>;
+// two CTAs of 8 warps per SM (by shared memory) for the Vision Mamba shape's configuration
+static_assert(ViewCfg<Pick1d<__nv_bfloat16, 16>::C>::SMEM + 1024 <= 228 * 1024 / 2,
+              "VIEW tiles of N = 16 fit two CTAs per SM");
 
 template <typename IO, int N>
 ss_status dispatch_bidir_view(const ScanArgs &a, int vshift) {

@@ -1013,6 +1013,14 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
         }
         // steps of this chunk at or past the end of the L-chunk leave h unchanged
         const int lim = (int)min((int64_t)T, t_end - (t_begin + (int64_t)i * T)) - pt0;
+        if (C::VIEW && t_end - xc < T) {
+            // a VIEW tile holds the neighbouring row's values past the row's
+            // ends (only in a chunk that runs past the end): zero them, so that
+            // the terms of those steps are zero whatever the values were
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                if (e >= lim) uu[e] = 0.f;
+        }
 #pragma unroll
         for (int e = 0; e < E; e += 2) {
             float dl[2], xx[2], ga[2], du[2];
@@ -1025,11 +1033,6 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
                 xx[k] = (EXT && !MULTI && p.zoh) ? uu[e + k] : v * uu[e + k];
                 ga[k] = gate_in_prep ? silu(zz[e + k]) : 1.f;
                 du[k] = Dd * uu[e + k] * ga[k];
-                if (C::VIEW && lim < E && e + k >= lim) {
-                    // a VIEW tile holds the neighbouring row's values there
-                    xx[k] = 0.f;
-                    du[k] = 0.f;
-                }
                 if (p.pass == 1) sdt_acc += v;
             }
             const int slot = swz_slot((pt0 + e) >> 1);
