@@ -193,10 +193,11 @@ def test_debug_flags_reject_unknown_bits(lib):
 
 
 def test_workspace_sizing_is_host_only(lib):
-    # multi-direction calls: unaligned bidirectional rows are re-pitched (with
-    # ngroups = 1: both directions' terms, fp32 [2, rows, Lp], u forward and reversed, Delta of
-    # both directions [rows, Lp] each in the I/O type, B and C [batch*2*N, Lp];
-    # Lp = L rounded up to 16 bytes, the larger of the two dtypes: float32);
+    # multi-direction calls: unaligned bidirectional rows are read through view tiles (both
+    # directions' terms, fp32 [2, rows, Lp]) or re-pitched; the size covers the re-pitched path
+    # (with ngroups = 1: the terms, u forward and reversed, Delta of both directions [rows, Lp]
+    # each in the I/O type, B and C [batch*2*N, Lp]; Lp = L rounded up to 16 bytes, the larger of
+    # the two dtypes: float32);
     # aligned rows merge through an fp32 [batch, dim, L] accumulator
     rows, Lp = 128 * 768, 200
     a256 = lambda n: (n + 255) // 256 * 256  # noqa: E731
