@@ -377,6 +377,15 @@ def test_bidirectional_view_rows_fold(oracle, L, io, N):
     _check(oracle, sc.workload(f"bi_vf{L}", 2, 40, L, N=N, K=2, io=io))
 
 
+@pytest.mark.parametrize("L,N", [(197, 32), (197, 64), (196, 2), (197, 8)])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bidirectional_view_rows_dstates(oracle, L, N, io):
+    """View tiles of the other state counts' configurations: N = 32 and 64
+    (8 warps of 32 channels a CTA), N = 2 with two rows to a view row in bf16,
+    N = 8 with eight (bf16) or four (fp32) rows to a view row."""
+    _check(oracle, sc.workload(f"bi_vn{N}_{L}", 2, 40, L, N=N, K=2, io=io))
+
+
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_bidirectional_view_rows_isolate_channels(oracle, io):
     """A view tile holds the neighbouring rows' values past each row's ends: a
