@@ -113,6 +113,12 @@ typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
  * Empty inputs (batch, dim or seqlen = 0) return SS_OK without touching memory.
  * Long sequences with little batch*dim parallelism run a chunked path (per-chunk
  * local states, a carry pass, a fix-up pass) that uses the workspace.
+ * Rows that are not 16-byte aligned (seqlen * element size % 16 != 0) are read
+ * in place through a view whose rows hold P of theirs (P = (16 / element size)
+ * / gcd(seqlen, 16 / element size)) when P divides dim / ngroups and dstate; for
+ * them the workspace is optional: given one of the reported size they may take
+ * the chunked path, without it they run in one pass.  Other unaligned rows run
+ * an on-chip kernel that needs no workspace.
  */
 ss_status ss_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dstate,
                                 int ngroups, ss_dtype io, const void *u, const void *delta,

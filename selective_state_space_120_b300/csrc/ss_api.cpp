@@ -302,7 +302,16 @@ ss_status ss_selective_scan_fwd_opts(int64_t batch, int64_t dim, int64_t seqlen,
         a.conv_b = options->conv_b;
         a.conv_x0 = options->conv_x0;
     }
-    if ((st = check_workspace(fn, scan1d_workspace_bytes(a), workspace, workspace_bytes))) return st;
+    // Rows that are not 16-byte aligned: a workspace is optional -- with one of
+    // at least the reported size the view-tiled scan may take the chunked
+    // path, otherwise it runs in one pass.
+    if (!scan1d_uses_tma(a)) {
+        if (workspace && !aligned16(workspace))
+            return fail(SS_ERR_ALIGNMENT, "%s: workspace is not 16-byte aligned", fn);
+    } else if ((st = check_workspace(fn, scan1d_workspace_bytes(a), workspace, workspace_bytes))) {
+        return st;
+    }
+    if ((st = check_ws_overlap(fn, a))) return st;
     return launch_scan1d(a);
 }
 
@@ -343,7 +352,9 @@ ss_status ss_selective_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t seql
         a.conv_b = options->conv_b;
         a.conv_x0 = options->conv_x0;
     }
-    const size_t need = scan1d_workspace_bytes(a);
+    // rows that are not 16-byte aligned run in one pass here (their workspace
+    // is optional)
+    const size_t need = scan1d_uses_tma(a) ? scan1d_workspace_bytes(a) : 0;
     if (need > SS_NOALLOC_SCRATCH_BYTES)
         return fail(SS_ERR_UNSUPPORTED,
                     "%s: this shape needs %zu bytes of scratch, more than the fixed %zu bytes "

@@ -184,20 +184,37 @@ ss_status permuted_copy(const ScanArgs &a, int order, void *dst) {
 // ---------------------------------------------------------------- single direction
 template <class C>
 struct Scan1d {
-    static ss_status run(const ScanArgs &a, int J) {
+    // One direction; a VIEW configuration (rows not 16-byte aligned, read in
+    // place through views of 1 << vshift rows to a view row) takes the plain
+    // kernel only.
+    static ss_status run(const ScanArgs &a, int J, int vshift = 0) {
         using namespace ssk;
         const int io = a.io;
         const int64_t rows = a.batch * a.dim;
+        const uint64_t bcrows = (uint64_t)a.batch * a.G * C::N;
         CUtensorMap mu, md, mz, mb, mc;
         ss_status st;
-        if ((st = make_map(&mu, a.u, io, a.L, rows, C::T, C::CB))) return st;
-        if ((st = make_map(&md, a.delta, io, a.L, rows, C::T, C::CB))) return st;
-        if ((st = make_map(&mz, a.z ? a.z : a.u, io, a.L, rows, C::T, C::CB))) return st;
-        if ((st = make_map(&mb, a.B, io, a.L, (uint64_t)a.batch * a.G * C::N, C::T, C::N))) return st;
-        if ((st = make_map(&mc, a.C, io, a.L, (uint64_t)a.batch * a.G * C::N, C::T, C::N))) return st;
+        if constexpr (C::VIEW) {
+            const int P = 1 << vshift;
+            const uint32_t bch = (uint32_t)(C::CB >> vshift), bbc = (uint32_t)(C::N >> vshift);
+            if ((st = make_view_map(&mu, a.u, io, a.L, rows, P, C::BW, bch))) return st;
+            if ((st = make_view_map(&md, a.delta, io, a.L, rows, P, C::BW, bch))) return st;
+            if ((st = make_view_map(&mz, a.z ? a.z : a.u, io, a.L, rows, P, C::BW, bch))) return st;
+            if ((st = make_view_map(&mb, a.B, io, a.L, bcrows, P, C::BW, bbc))) return st;
+            if ((st = make_view_map(&mc, a.C, io, a.L, bcrows, P, C::BW, bbc))) return st;
+        } else {
+            if ((st = make_map(&mu, a.u, io, a.L, rows, C::T, C::CB))) return st;
+            if ((st = make_map(&md, a.delta, io, a.L, rows, C::T, C::CB))) return st;
+            if ((st = make_map(&mz, a.z ? a.z : a.u, io, a.L, rows, C::T, C::CB))) return st;
+            if ((st = make_map(&mb, a.B, io, a.L, bcrows, C::T, C::N))) return st;
+            if ((st = make_map(&mc, a.C, io, a.L, bcrows, C::T, C::N))) return st;
+        }
 
         // the plain kernel unless the zero-order hold or the fused Conv1D is asked for
-        auto kern = (a.zoh || a.conv) ? k_scan1d<C, false, true> : k_scan1d<C, false, false>;
+        auto kern = k_scan1d<C, false, false>;
+        if constexpr (!C::VIEW) {
+            if (a.zoh || a.conv) kern = k_scan1d<C, false, true>;
+        }
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
             return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
         const bool plain = !a.zoh && !a.conv;
@@ -206,6 +223,7 @@ struct Scan1d {
         p.dim = a.dim;
         p.L = a.L;
         p.pitch = a.L;
+        p.vshift = vshift;
         p.G = a.G;
         p.dpg = (int)(a.dim / a.G);
         p.K = 1;
@@ -747,6 +765,36 @@ size_t ws1d(const ScanArgs &a) {
     return (size_t)rows * J * (2 * N + 1) * sizeof(float);
 }
 
+// The single-direction VIEW configuration of a (I/O type, N) configuration: a
+// z tile and the gate in the prep, a 2-stage ring, the warps of the aligned
+// configuration (the direct path's few CTAs per SM need its registers).
+template <class C>
+using ViewCfgZ = ssk::Cfg1<typename C::IO, C::N, C::NPT, C::W, 2, C::CL, C::PIPE ? 1 : 0, 0, 2>;
+
+// One direction over rows read through views: chunked when the caller's
+// workspace holds the chunked path's, else in one pass.
+template <typename IO, int N>
+ss_status dispatch1d_view(const ScanArgs &a, int vshift) {
+    using C = ViewCfgZ<typename Pick1d<IO, N>::C>;
+    int J = chunks_for<IO, N>(a);
+    if (J > 1 && (!a.ws || a.ws_bytes < ws1d<IO, N>(a))) J = 1;
+    return Scan1d<C>::run(a, J, vshift);
+}
+
+template <typename IO>
+ss_status dispatch1d_view_n(const ScanArgs &a, int vshift) {
+    switch (a.N) {
+    case 2: return dispatch1d_view<IO, 2>(a, vshift);
+    case 4: return dispatch1d_view<IO, 4>(a, vshift);
+    case 8: return dispatch1d_view<IO, 8>(a, vshift);
+    case 16: return dispatch1d_view<IO, 16>(a, vshift);
+    case 32: return dispatch1d_view<IO, 32>(a, vshift);
+    case 64: return dispatch1d_view<IO, 64>(a, vshift);
+    default: return fail(SS_ERR_UNSUPPORTED, "dstate %d cannot be read through VIEW tiles", a.N);
+    }
+}
+
+
 // ---------------------------------------------------------------- multi direction
 template <class C>
 ss_status run_multi(const ScanArgs &a) {
@@ -876,13 +924,43 @@ bool scan1d_uses_tma(const ScanArgs &a) {
            a.batch * a.G * a.N < (1ll << 31) && a.L < (1ll << 31);
 }
 
+// log2 of the rows folded into one view row for a call over rows that are not
+// 16-byte aligned, or -1: P = (16 / element size) / gcd(L, 16 / element size)
+// must divide the channels per group and N (so that every box holds whole rows
+// of one channel block or one B/C tile), and the view's sizes fit its map.
+int view_fold_shift(const ScanArgs &a) {
+    const int64_t vpc = a.io == SS_BF16 ? 8 : 4;  // values per 16 bytes (a power of two)
+    int64_t g = 1;
+    while (g < vpc && a.L % (2 * g) == 0) g *= 2;  // gcd(L, vpc)
+    const int64_t P = vpc / g;
+    const int64_t dpg = a.dim / a.G;
+    if (P < 2 || dpg % P != 0 || a.N % P != 0) return -1;
+    if (P * a.L >= (1ll << 31) || (int64_t)a.K * a.batch * a.dim >= (1ll << 31) ||
+        (int64_t)a.K * a.batch * a.G * a.N >= (1ll << 31))
+        return -1;
+    return P == 2 ? 1 : P == 4 ? 2 : 3;
+}
+
+// One direction over rows that are not 16-byte aligned, without the zero-order
+// hold or the fused Conv1D: read through views (else the on-chip kernel).
+int scan1d_view_shift(const ScanArgs &a) {
+    if (scan1d_uses_tma(a) || a.zoh || a.conv || a.N < 2) return -1;
+    return view_fold_shift(a);
+}
+
 size_t scan1d_workspace_bytes(const ScanArgs &a) {
-    if (!scan1d_uses_tma(a)) return 0;
+    // rows read through views may take the chunked path too (their workspace
+    // is optional: without it they run in one pass)
+    if (!scan1d_uses_tma(a) && scan1d_view_shift(a) < 0) return 0;
     return a.io == SS_BF16 ? ws1d_n<__nv_bfloat16>(a) : ws1d_n<float>(a);
 }
 
 ss_status launch_scan1d(const ScanArgs &a) {
     if (!scan1d_uses_tma(a)) {
+        const int vshift = scan1d_view_shift(a);
+        if (vshift > 0)
+            return a.io == SS_BF16 ? dispatch1d_view_n<__nv_bfloat16>(a, vshift)
+                                   : dispatch1d_view_n<float>(a, vshift);
         ScanArgs m = a;
         m.K = 1;
         m.H = 1;
@@ -907,14 +985,7 @@ bool bidir_padded_ok(const ScanArgs &a) {
 // that every box holds whole rows of one channel block or one B/C tile).
 int bidir_view_shift(const ScanArgs &a) {
     if (!bidir_padded_ok(a)) return -1;
-    const int64_t vpc = a.io == SS_BF16 ? 8 : 4;  // values per 16 bytes (a power of two)
-    int64_t g = 1;
-    while (g < vpc && a.L % (2 * g) == 0) g *= 2;  // gcd(L, vpc)
-    const int64_t P = vpc / g;
-    const int64_t dpg = a.dim / a.G;
-    if (P < 2 || dpg % P != 0 || a.N % P != 0) return -1;
-    if (P * a.L >= (1ll << 31)) return -1;
-    return P == 2 ? 1 : P == 4 ? 2 : 3;
+    return view_fold_shift(a);
 }
 // Workspace of the VIEW path: the two directions' fp32 slices [2, rows, Lp].
 size_t bidir_view_bytes(const ScanArgs &a) {

@@ -82,10 +82,12 @@ struct Cfg1 {
     // chunk is P boxes, one per residue of the row index mod P, each starting
     // at the 16-byte boundary at or below its first step: tile rows hold
     // BW = T + VPC values, unswizzled, with the chunk's first step at a per-box
-    // offset below VPC.  Used by the direction-pair launch, which has no z tile.
+    // offset below VPC.  VIEW_ = 1: the direction-pair launch (no z tile, no
+    // gate in the prep); VIEW_ = 2: the single-direction scan (with both).
     // A box lands at a 128-byte boundary (the copy's rule for its shared-memory
     // address): box j of a tile of `rows` rows starts at j * box_stride.
     static constexpr bool VIEW = VIEW_ != 0;
+    static constexpr bool VIEWZ = VIEW_ == 2;      // a z tile and the gate in the prep
     static constexpr int BW = VIEW ? T + VPC : T;  // values per tile row
     static constexpr int ROWB = BW * ES;           // bytes per tile row
     static constexpr int al(int x) { return VIEW ? (x + 127) & ~127 : (x + 1023) & ~1023; }
@@ -100,7 +102,7 @@ struct Cfg1 {
     }
     static constexpr int TILE_CH = VIEW ? view_tile(CB) : al(CB * ROWB);
     static constexpr int TILE_BC = VIEW ? view_tile(N) : al(N * ROWB);
-    static constexpr int NCHT = VIEW ? 2 : 3;      // channel tiles per stage: u, Delta (, z)
+    static constexpr int NCHT = (VIEW && !VIEWZ) ? 2 : 3;  // channel tiles per stage: u, Delta (, z)
     static constexpr int STAGE = NCHT * TILE_CH + 2 * TILE_BC;
     static constexpr int OFF_U = 0, OFF_DL = TILE_CH, OFF_Z = 2 * TILE_CH;
     static constexpr int OFF_B = NCHT * TILE_CH, OFF_C = NCHT * TILE_CH + TILE_BC;
@@ -113,9 +115,11 @@ struct Cfg1 {
     static_assert(!BCW || PIPE, "packed B/C words are read by the pipelined step loop");
     static constexpr int OFF_BC = STAGES * STAGE;
     static constexpr int DXROW = (TP + 1) * 16;  // one padding slot per row
-    // gd rows: (gate, D*u*gate) per step; a VIEW launch has no gate: D*u only
-    // (two padding slots: the channels of a warp start on distinct 16-byte groups)
-    static constexpr int GDROW = VIEW ? (TP + 2) * 8 : DXROW;
+    // gd rows: (gate, D*u*gate) per step; a direction-pair VIEW launch has no
+    // gate: D*u only (two padding slots: the channels of a warp start on
+    // distinct 16-byte groups)
+    static constexpr bool DU_ONLY = VIEW && !VIEWZ;
+    static constexpr int GDROW = DU_ONLY ? (TP + 2) * 8 : DXROW;
     static constexpr int PREPBUF = CB * (DXROW + GDROW);  // dx and gd rows of one chunk
     static constexpr int NPREP = OVL ? 2 : 1;      // prep row buffers
     static constexpr int OFF_DX = OFF_BC + 2 * BCBUF;
@@ -800,8 +804,10 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
     // the chunk-local pass needs only the end states of chunks 1..J-2: no
     // readout, so no C tiles, no gate and no skip term
     const bool do_y = (p.pass != 1) || (jc == 0);
-    const bool gate_in_prep = !C::VIEW && do_y && (p.mode == OUT_STORE) && p.has_z;
-    static_assert(!C::VIEW || MULTI, "VIEW tiles serve the direction-pair launch");
+    const bool gate_in_prep = !C::DU_ONLY && do_y && (p.mode == OUT_STORE) && p.has_z;
+    static_assert(!C::VIEW || (MULTI != C::VIEWZ), "pair VIEW tiles for multi-direction launches, "
+                  "z-carrying ones for the single direction");
+    static_assert(!(C::VIEW && EXT), "VIEW tiles carry no optional input paths");
 
     // scan role: channels ch[c] (within the CTA) of this lane's group
     int chs[CL];
@@ -891,21 +897,27 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
         // start below 0 on the last chunk; the copy fills zeros there)
         const int xu = (p.order == 2) ? (int)(p.L - (int64_t)(i + 1) * T) : x;
         if constexpr (C::VIEW) {
-            // warp w issues tensors w, w + W, ... of (u, Delta, B, C): box j
+            // the chunk's tensors, in the order u, Delta, z (when tiled), B, C
+            // (when read): warp w issues those of rank w, w + W, ...; box j
             // holds the rows r = j mod P, from view column j*L + first step
             // rounded down to a 16-byte boundary (a negative column reads
             // zeros; columns of a neighbouring row are masked by the prep)
             const int vs = p.vshift, P = 1 << vs, L32 = (int)p.L;
-            const int ntens = do_y ? 4 : 3;
+            const int ntens = 3 + (z_tiled ? 1 : 0) + (do_y ? 1 : 0);
+            // rank -> tensor: 0 u, 1 Delta, 2 z, 3 B, 4 C
+            auto tensor_of = [&](int r) { return r < 2 ? r : (z_tiled ? r : r + 1); };
             uint32_t bytes = 0;
-            for (int tsel = warp; tsel < ntens; tsel += C::W) bytes += (tsel < 2 ? C::CB : N) * C::ROWB;
+            for (int r = warp; r < ntens; r += C::W) bytes += (tensor_of(r) < 3 ? C::CB : N) * C::ROWB;
             mbar_expect_tx(bar, bytes);
-            for (int tsel = warp; tsel < ntens; tsel += C::W) {
-                const CUtensorMap *map = tsel == 0 ? umap : tsel == 1 ? &tm_dl : tsel == 2 ? &tm_B : &tm_C;
-                const int vrow = (tsel == 0 ? row_tma : tsel == 1 ? dlrow_tma : bcrow_tma) >> vs;
-                const uint32_t dst = st + (tsel == 0 ? C::OFF_U : tsel == 1 ? C::OFF_DL : tsel == 2 ? C::OFF_B : C::OFF_C);
-                const int bs = C::box_stride(tsel < 2 ? C::CB : N, vs);
-                int xj = tsel == 0 ? xu : x;  // view column of box j's first step
+            for (int r = warp; r < ntens; r += C::W) {
+                const int tsel = tensor_of(r);
+                const CUtensorMap *map = tsel == 0 ? umap : tsel == 1 ? &tm_dl : tsel == 2 ? &tm_z
+                                         : tsel == 3 ? &tm_B : &tm_C;
+                const int vrow = (tsel == 0 || tsel == 2 ? row_tma : tsel == 1 ? dlrow_tma : bcrow_tma) >> vs;
+                const uint32_t dst = st + (tsel == 0 ? C::OFF_U : tsel == 1 ? C::OFF_DL : tsel == 2 ? C::OFF_Z
+                                           : tsel == 3 ? C::OFF_B : C::OFF_C);
+                const int bs = C::box_stride(tsel < 3 ? C::CB : N, vs);
+                int xj = (tsel == 0 || tsel == 2) ? xu : x;  // view column of box j's first step
 #pragma unroll 1
                 for (int j = 0; j < P; ++j, xj += L32)
                     tma_load_2d(dst + j * bs, map, xj & ~(C::VPC - 1), vrow, bar);
@@ -947,6 +959,7 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
             load_view_row<C, E>(st + C::OFF_DL, vroff, vmis_f + pt0, dd);
             if (p.order == 0) {
                 load_view_row<C, E>(st + C::OFF_U, vroff, vmis_f + pt0, uu);
+                if (z_tiled) load_view_row<C, E>(st + C::OFF_Z, vroff, vmis_f + pt0, zz);
             } else {
                 float tmp[E];
                 load_view_row<C, E>(st + C::OFF_U, vroff, vmis_r + T - pt0 - E, tmp);
@@ -1019,7 +1032,10 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
             // the terms of those steps are zero whatever the values were
 #pragma unroll
             for (int e = 0; e < E; ++e)
-                if (e >= lim) uu[e] = 0.f;
+                if (e >= lim) {
+                    uu[e] = 0.f;
+                    if (z_tiled) zz[e] = 0.f;
+                }
         }
 #pragma unroll
         for (int e = 0; e < E; e += 2) {
@@ -1037,7 +1053,7 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
             }
             const int slot = swz_slot((pt0 + e) >> 1);
             pdxrow[slot] = make_float4(dl[0], dl[1], xx[0], xx[1]);
-            if constexpr (C::VIEW) reinterpret_cast<float2 *>(pgdrow)[slot] = make_float2(du[0], du[1]);
+            if constexpr (C::DU_ONLY) reinterpret_cast<float2 *>(pgdrow)[slot] = make_float2(du[0], du[1]);
             else if (do_y) pgdrow[slot] = make_float4(ga[0], du[0], ga[1], du[1]);
         }
     };
@@ -1101,8 +1117,8 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
         }
         auto emit = [&](int c, float y, int t) {
             float v;
-            if constexpr (C::VIEW) {
-                // D*u only (VIEW rows of GDROW bytes: two floats a step pair)
+            if constexpr (C::DU_ONLY) {
+                // D*u only (rows of GDROW bytes: two floats a step pair)
                 v = y + reinterpret_cast<const float *>(gdrows[c])[2 * swz_slot(t >> 1) + (t & 1)];
             } else {
                 const float2 ge = reinterpret_cast<const float2 *>(gdrows[c] + swz_slot(t >> 1))[t & 1];
@@ -1128,6 +1144,20 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
 
         if (do_y && p.mode != OUT_STORE) {
             store_partials<C>(p, mr, smem, (int64_t)i * T);
+            __syncwarp();
+        } else if (C::VIEW && do_y) {
+            // rows that do not start on 16-byte boundaries: one value per lane,
+            // consecutive lanes on consecutive steps of a channel
+#pragma unroll 1
+            for (int k = lane; k < C::CHW * T; k += 32) {
+                const int rr = k / T, e = k % T;
+                const int chr = warp * C::CHW + rr;
+                const int dgr = cblk * C::CB + chr;
+                const int64_t t = t_begin + (int64_t)i * T + e;
+                if (dgr < p.dpg && t < t_end)
+                    reinterpret_cast<IO *>(p.out)[(row0 + dgr) * p.L + t] =
+                        reinterpret_cast<const IO *>(smem + C::OFF_OB + chr * C::OBROW)[e];
+            }
             __syncwarp();
         } else if (do_y) {
             constexpr int VPC = 16 / C::ES;
@@ -1197,8 +1227,10 @@ k_scan1d(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUten
 // chunk (DEFER).  On the chunked path, whose grids fill the SMs several times
 // over, the same choice measured slower (a lower CTA residency), so that path
 // keeps k_scan1d.
+// (A VIEW configuration, whose shifted reads take more registers, is held to
+// three CTAs per SM, as many as the plain one reaches unconstrained.)
 template <class C>
-__global__ void __launch_bounds__(C::THREADS, 1)
+__global__ void __launch_bounds__(C::THREADS, C::VIEW ? 3 : 1)
 k_scan1d_direct(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
                 const __grid_constant__ CUtensorMap tm_C, const Scan1dParams p) {

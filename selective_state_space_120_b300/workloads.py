@@ -77,7 +77,7 @@ ALL = (TINY_F32, MAMBA_LAYER, LONG_SEQ, VIM_BIDIR, VMAMBA_SS2D)
 LOCAL_WIN = Workload("localmamba_win7_b32_d192_56x56_n16", 32, 192, 56 * 56, K=4, with_z=False,
                      H=56, W=56, orders=(4, 5, 6, 7), win=7)
 
-# The long sequence cut to L = 16384: the same 5120 rows and the same eight
+# The long sequence cut to L = 16384: the same 5120 rows and the same twelve
 # L-chunks, with 1/8 of the data, for ncu captures of the chunked path (whose
 # full size is beyond a multi-pass capture); not a benchmark line.
 LONG_SEQ_PROFILE = Workload("long_seq_b1_d5120_l16384_n16", 1, 5120, 16384, last_state=True)
@@ -85,6 +85,10 @@ LONG_SEQ_PROFILE = Workload("long_seq_b1_d5120_l16384_n16", 1, 5120, 16384, last
 # The Mamba layer with its Conv1D(k=4) + SiLU input branch fused in front of the
 # scan (weights ~ N(0, 0.5^2), bias ~ N(0, 0.1^2)).
 MAMBA_LAYER_CONV = Workload("mamba130m_layer_conv_b8_d1536_l2048_n16", 8, 1536, 2048, conv=True)
+
+# The Mamba layer one step shorter: rows of 2047 bf16 values are not 16-byte
+# multiples (the scan reads them through views of eight rows to a view row).
+MAMBA_LAYER_UNALIGNED = Workload("mamba130m_layer_b8_d1536_l2047_n16", 8, 1536, 2047)
 
 
 def round_bf16_bits(x: np.ndarray) -> np.ndarray:

@@ -54,8 +54,59 @@ def test_scan_ragged_lengths_tma_path(oracle, L):
 
 @pytest.mark.parametrize("L", [1, 7, 31, 33, 197, 257])
 def test_scan_unaligned_lengths(oracle, L):
-    """Rows that are not 16-byte multiples take the gather path."""
+    """Rows that are not 16-byte multiples, 20 channels (which P = 8 rows to a
+    view row does not divide): the on-chip gather path."""
     _check(oracle, sc.workload(f"u{L}", 2, 20, L))
+
+
+@pytest.mark.parametrize("L", [1, 7, 33, 197, 1001])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_scan_view_rows(oracle, L, io):
+    """Rows that are not 16-byte multiples, read in place through view tiles
+    (P = 8 rows to a view row in bf16, 4 in fp32), several channel blocks and a
+    partial last one, the gate and last_state."""
+    _check(oracle, sc.workload(f"sv{L}", 2, 72, L, io=io))
+
+
+@pytest.mark.parametrize("L,N,G,io", [(198, 2, 1, "bf16"), (196, 4, 2, "bf16"), (197, 8, 2, "f32"),
+                                      (197, 32, 1, "bf16"), (99, 64, 1, "f32")])
+def test_scan_view_rows_dstates_groups(oracle, L, N, G, io):
+    """View tiles with two, four and eight rows to a view row, every state
+    count's configuration, groups, no gate."""
+    _check(oracle, sc.workload(f"svn{N}_{L}", 2, 48, L, N=N, G=G, io=io, with_z=False))
+
+
+@pytest.mark.parametrize("chunks", [0, 3])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_scan_view_rows_chunked(oracle, chunks, io):
+    """Few rows of an unaligned length: the chunked path over view tiles
+    (automatic chunking, and three chunks)."""
+    _check(oracle, sc.workload("svc", 1, 16, 3001, io=io), chunks=chunks)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_scan_view_rows_isolate_channels(oracle, io):
+    """A view tile holds the neighbouring rows' values past each row's ends: a
+    NaN in one channel's u and z and an infinite Delta in another's must not
+    reach any other channel."""
+    import torch
+    import selective_state_space_120_b300 as ss
+    wl = sc.workload("sv_iso", 2, 16, 197, io=io)
+    inp = wk.make_inputs(wl, seed=0)
+    t = sc.device_inputs(inp)
+    t["u"][0, 5] = float("nan")
+    t["z"][0, 5] = float("nan")
+    t["delta"][0, 0, 10] = float("inf")
+    out, last = ss.selective_scan_fwd(t["u"], t["delta"][:, 0], t["A"], t["B"][:, 0], t["C"][:, 0],
+                                      t["D"], t["z"], t["delta_bias"], True, return_last_state=True)
+    torch.cuda.synchronize()
+    ref, ref_last = sc.oracle_run(oracle, inp)
+    keep = [d for d in range(wl.dim) if d not in (5, 10)]
+    got = sc.from_torch(out)
+    sc.assert_close(got[0, keep], ref[0, keep], io)
+    sc.assert_close(got[1], ref[1], io)
+    got_last = last.cpu().numpy().astype(np.float64)
+    sc.assert_close(got_last[0, keep], ref_last[0, 0, keep], io, "last_state")
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
@@ -490,7 +541,7 @@ def _sampled(oracle, wl, nrows=12, seed=1):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("wl", [wk.MAMBA_LAYER, wk.LONG_SEQ, wk.VIM_BIDIR, wk.VMAMBA_SS2D],
-                         ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", [wk.MAMBA_LAYER, wk.LONG_SEQ, wk.VIM_BIDIR, wk.VMAMBA_SS2D,
+                                wk.MAMBA_LAYER_UNALIGNED], ids=lambda w: w.name)
 def test_full_size_sampled(oracle, wl):
     _sampled(oracle, wl)
