@@ -468,7 +468,8 @@ struct Scan1d {
         const int64_t groups = rows * ((a.L + 3) / 4);
         const unsigned mblocks = (unsigned)std::min<int64_t>((groups + 255) / 256, (int64_t)num_sms() * 32);
         k_merge_bidir<IO><<<mblocks, 256, 0, s>>>(s0, s1, reinterpret_cast<const IO *>(a.z),
-                                                  reinterpret_cast<IO *>(a.out), rows, a.L, Lp);
+                                                  reinterpret_cast<IO *>(a.out), rows, a.L, Lp,
+                                                  FastDiv((uint32_t)((a.L + 3) / 4)));
         return check_launch("bidirectional merge");
     }
 
@@ -534,7 +535,8 @@ struct Scan1d {
         const int64_t groups = rows * ((a.L + 3) / 4);
         const unsigned mblocks = (unsigned)std::min<int64_t>((groups + 255) / 256, (int64_t)num_sms() * 32);
         k_merge_bidir<IO><<<mblocks, 256, 0, s>>>(s0, s1, reinterpret_cast<const IO *>(a.z),
-                                                  reinterpret_cast<IO *>(a.out), rows, a.L, Lp);
+                                                  reinterpret_cast<IO *>(a.out), rows, a.L, Lp,
+                                                  FastDiv((uint32_t)((a.L + 3) / 4)));
         return check_launch("bidirectional merge");
     }
 

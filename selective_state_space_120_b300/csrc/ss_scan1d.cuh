@@ -1516,12 +1516,15 @@ template <typename IO>
 __global__ void __launch_bounds__(256) k_merge_bidir(const float *__restrict__ s0,
                                                      const float *__restrict__ s1,
                                                      const IO *__restrict__ z, IO *__restrict__ out,
-                                                     int64_t rows, int64_t L, int64_t Lp) {
+                                                     int64_t rows, int64_t L, int64_t Lp, FastDiv dq) {
     const int64_t qpr = (L + 3) / 4;  // groups of four positions per row
     const int64_t n = rows * qpr;
+    // group -> row by a multiply-shift when the group count fits 32 bits (dq
+    // divides by qpr), a 64-bit division otherwise
+    const bool narrow = n <= 0xffffffffll;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i / qpr;
+        const int64_t r = narrow ? (int64_t)dq.div((uint32_t)i) : i / qpr;
         const int64_t p0 = (i - r * qpr) * 4;
         const float4 a = *reinterpret_cast<const float4 *>(s0 + r * Lp + p0);
         const float av[4] = {a.x, a.y, a.z, a.w};
