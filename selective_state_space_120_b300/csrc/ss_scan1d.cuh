@@ -368,19 +368,22 @@ __device__ __forceinline__ void convert_bc_view(const uint8_t *tB, const uint8_t
     }
 }
 
-// Scans one chunk of T steps for this lane's CL channels and state slice.
-// DO_Y selects the readout (off in the chunk-local pass, which only needs the
-// end states).  `emit(c, y, t)` receives the full readout y of channel c of the
-// lane's group at local step t (one lane per step).
-template <class C, bool DO_Y, class Emit>
+// Scans one chunk of T steps, or its first nblk readout blocks (TAIL: a
+// chunk that runs past the end of the sequence, whose later steps would leave
+// h unchanged), for this lane's CL channels and state slice, one readout block
+// at a time without the step pipeline of scan_chunk_pipe.  DO_Y selects the
+// readout (off in the chunk-local pass, which only needs the end states).
+// `emit(c, y, t)` receives the full readout y of channel c of the lane's group
+// at local step t (one lane per step).
+template <class C, bool DO_Y, bool TAIL = false, class Emit>
 __device__ __forceinline__ void scan_chunk_cl(const float4 *const (&dxrow)[C::CL], const float *bc,
                                               int g, float (&h)[C::CL][C::NPT],
-                                              const float2 (&A2p)[C::CL][C::NPT], Emit &&emit) {
+                                              const float2 (&A2p)[C::CL][C::NPT], Emit &&emit,
+                                              int nblk = 0) {
     constexpr int R = C::R, NPT = C::NPT, N = C::N, CL = C::CL;
     constexpr int BS = R >= 2 ? R : 2;  // steps per readout block
     constexpr int PPB = BS / 2;
-#pragma unroll
-    for (int blk = 0; blk < C::T / BS; ++blk) {
+    auto block = [&](int blk) {
         float v[CL][BS];
 #pragma unroll
         for (int pp = 0; pp < PPB; ++pp) {
@@ -439,6 +442,13 @@ __device__ __forceinline__ void scan_chunk_cl(const float4 *const (&dxrow)[C::CL
                 }
             }
         }
+    };
+    if constexpr (TAIL) {
+#pragma unroll 1
+        for (int blk = 0; blk < nblk; ++blk) block(blk);
+    } else {
+#pragma unroll
+        for (int blk = 0; blk < C::T / BS; ++blk) block(blk);
     }
 }
 
@@ -1127,9 +1137,21 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
             if (p.mode == OUT_STORE) reinterpret_cast<IO *>(obrows[c])[t] = IOT<IO>::from_f(v);
             else reinterpret_cast<float *>(obrows[c])[t] = v;
         };
+        // valid steps of this chunk: fewer than T only in a chunk that runs
+        // past the end of the sequence (or of the L-chunk)
+        const int nvs = (int)min((int64_t)T, t_end - (t_begin + (int64_t)i * T));
         if constexpr (C::PIPE) {
             auto none = [](int, float, int) {};
-            if (EXT && zoh_iA) {
+            constexpr int BS = C::R >= 2 ? C::R : 2;  // steps per readout block
+            if (C::VIEW && nvs < T) {
+                // only the readout blocks holding valid steps: the later steps
+                // would leave h unchanged and their outputs are not stored (VIEW
+                // configurations only: the aligned kernels keep their schedule;
+                // a 197-step row wastes 27 of its 224 scanned steps otherwise)
+                const int nb = (nvs + BS - 1) / BS;
+                if (do_y) scan_chunk_cl<C, true, true>(dxrows, bc, g, h, A2p, emit, nb);
+                else scan_chunk_cl<C, false, true>(dxrows, bc, g, h, A2p, none, nb);
+            } else if (EXT && zoh_iA) {
                 if (do_y) scan_chunk_pipe<C, true, true>(dxrows, bc, g, h, A2p, emit, zoh_iA);
                 else scan_chunk_pipe<C, false, true>(dxrows, bc, g, h, A2p, none, zoh_iA);
             } else {
