@@ -1143,11 +1143,12 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
         if constexpr (C::PIPE) {
             auto none = [](int, float, int) {};
             constexpr int BS = C::R >= 2 ? C::R : 2;  // steps per readout block
-            if (C::VIEW && nvs < T) {
+            if (C::VIEW && MULTI && nvs < T) {
                 // only the readout blocks holding valid steps: the later steps
-                // would leave h unchanged and their outputs are not stored (VIEW
-                // configurations only: the aligned kernels keep their schedule;
-                // a 197-step row wastes 27 of its 224 scanned steps otherwise)
+                // would leave h unchanged and their outputs are not stored (the
+                // view-tiled direction pair only, whose 197-step rows would waste
+                // 27 of 224 scanned steps; in the other kernels the extra path
+                // costs their schedule more than it saves)
                 const int nb = (nvs + BS - 1) / BS;
                 if (do_y) scan_chunk_cl<C, true, true>(dxrows, bc, g, h, A2p, emit, nb);
                 else scan_chunk_cl<C, false, true>(dxrows, bc, g, h, A2p, none, nb);
