@@ -55,13 +55,13 @@ FALLBACK_HBM_GBS = 6400.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 CSRC = os.path.join(ROOT, "selective_state_space_120_b300", "csrc")
 
-WORKLOADS = {w.name: w for w in wk.ALL + (wk.MAMBA_LAYER_CONV, wk.MAMBA_LAYER_UNALIGNED, wk.LOCAL_WIN,
-                                           wk.LONG_SEQ_PROFILE)}
+WORKLOADS = {w.name: w for w in wk.ALL + (wk.MAMBA_LAYER_CONV, wk.MAMBA_LAYER_UNALIGNED,
+                                           wk.VMAMBA_SS2D_14, wk.LOCAL_WIN, wk.LONG_SEQ_PROFILE)}
 HEADLINE = wk.LONG_SEQ
 # the other workloads of the target set, one compact record each
 TARGETS = (wk.MAMBA_LAYER, wk.VIM_BIDIR, wk.VMAMBA_SS2D)
 # further measured paths (--all)
-EXTRA = (wk.MAMBA_LAYER_CONV, wk.MAMBA_LAYER_UNALIGNED, wk.LOCAL_WIN)
+EXTRA = (wk.MAMBA_LAYER_CONV, wk.MAMBA_LAYER_UNALIGNED, wk.VMAMBA_SS2D_14, wk.LOCAL_WIN)
 
 
 # ------------------------------------------------------------------ accounting

@@ -235,8 +235,15 @@ ss_status ss_bidir_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int dsta
  * launch sums the four slices by position (a fixed order: deterministic) and
  * gates.  The column directions read u as row-order tiles of a transposed copy
  * of u that the call makes in the workspace first.
- * Otherwise the whole map of a channel is merged in shared memory: H*W is then
- * limited by the per-block shared-memory size (SS_ERR_UNSUPPORTED beyond it).
+ * Otherwise the workspace is optional.  With P = (16 / element size) /
+ * gcd(H*W, 16 / element size): when P divides dim / ngroups and dstate, and a
+ * workspace of the reported size is given, the four directions run side by
+ * side as TMA scans reading the maps in place through a view whose rows hold P
+ * of theirs (the column directions over the transposed copy of u), each storing
+ * its terms by scan step into its own fp32 slice of rows padded to 16 bytes,
+ * and one more launch sums them by position.  Otherwise the whole map of a
+ * channel is merged in shared memory: H*W is then limited by the per-block
+ * shared-memory size (SS_ERR_UNSUPPORTED beyond it).
  */
 ss_status ss_cross_scan2d_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, int dstate,
                               int ngroups, ss_dtype io, const void *u, const void *delta,

@@ -424,7 +424,15 @@ ss_status ss_cross_scan2d_fwd(int64_t batch, int64_t dim, int64_t H, int64_t W, 
     a.orders[1] = ORD_COL;
     a.orders[2] = ORD_ROW_REV;
     a.orders[3] = ORD_COL_REV;
-    if ((st = check_workspace(fn, multidir_workspace_bytes(a), workspace, workspace_bytes))) return st;
+    // Maps whose rows are not 16-byte aligned: a workspace is optional -- with
+    // one of at least the reported size the call reads the rows through view
+    // tiles, otherwise it merges on chip.
+    if (!scan1d_uses_tma(a)) {
+        if (workspace && !aligned16(workspace))
+            return fail(SS_ERR_ALIGNMENT, "%s: workspace is not 16-byte aligned", fn);
+    } else if ((st = check_workspace(fn, multidir_workspace_bytes(a), workspace, workspace_bytes))) {
+        return st;
+    }
     if ((st = check_ws_overlap(fn, a))) return st;
     return launch_multidir(a);
 }

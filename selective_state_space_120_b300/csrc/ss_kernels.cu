@@ -540,6 +540,83 @@ struct Scan1d {
         return check_launch("bidirectional merge");
     }
 
+    // SS2D over maps whose rows (H*W values) are not 16-byte aligned, read in
+    // place through VIEW tiles (C is a VIEW configuration; P = 1 << vshift rows
+    // per view row): the transposed copy of u for the column directions, one
+    // launch of the four directions side by side (grid z; the odd slots read
+    // the copy), each storing y_k + D_k*u by scan step into its own fp32 slice
+    // of pitch Lp, then one merge by step of the four slices, in a fixed order.
+    static ss_status run_ss2d_view(const ScanArgs &a, int vshift) {
+        using namespace ssk;
+        using IO = typename C::IO;
+        static_assert(C::VIEW && !C::VIEWZ, "a direction-pair VIEW configuration");
+        const int io = a.io;
+        const int P = 1 << vshift;
+        const int64_t rows = a.batch * a.dim;
+        const int64_t Lp = padded_len(a);
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(a.stream);
+        float *acc0 = reinterpret_cast<float *>(a.ws);
+        void *uT = reinterpret_cast<uint8_t *>(a.ws) + align256((size_t)4 * rows * Lp * sizeof(float));
+        ss_status st;
+        if ((st = permuted_copy(a, ORD_COL, uT))) return st;
+        const uint64_t bcrows = (uint64_t)a.batch * 4 * a.G * C::N;
+        const uint32_t bch = (uint32_t)(C::CB >> vshift), bbc = (uint32_t)(C::N >> vshift);
+        CUtensorMap mu, mu2, md, mb, mc;
+        if ((st = make_view_map(&mu, a.u, io, a.L, rows, P, C::BW, bch))) return st;
+        if ((st = make_view_map(&mu2, uT, io, a.L, rows, P, C::BW, bch))) return st;
+        if ((st = make_view_map(&md, a.delta, io, a.L, (uint64_t)rows * 4, P, C::BW, bch))) return st;
+        if ((st = make_view_map(&mb, a.B, io, a.L, bcrows, P, C::BW, bbc))) return st;
+        if ((st = make_view_map(&mc, a.C, io, a.L, bcrows, P, C::BW, bbc))) return st;
+        auto kern = k_scan1d<C, true>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return fail(SS_ERR_CUDA, "cannot reserve %d bytes of shared memory", C::SMEM);
+        Scan1dParams p{};
+        p.dim = a.dim;
+        p.L = a.L;
+        p.pitch = Lp;
+        p.vshift = vshift;
+        p.G = a.G;
+        p.dpg = (int)(a.dim / a.G);
+        p.Lc = a.L;
+        p.J = 1;
+        p.jbase = 0;
+        p.pass = 0;
+        p.K = 4;
+        p.u_g = a.u;
+        p.A = a.A;
+        p.D = a.D;
+        p.bias = a.bias;
+        p.softplus = a.softplus;
+        p.has_z = 0;
+        p.out = a.out;
+        p.last_state = a.last_state;
+        p.nz = 4;
+        p.k0 = 0;
+        for (int d = 0; d < 4; ++d) {
+            const int o = a.orders[d];
+            p.orders_z[d] = (o == ORD_ROW || o == ORD_COL) ? ORD_ROW : ORD_ROW_REV;
+            p.modes_z[d] = OUT_STEP;
+            p.accs_z[d] = acc0 + (int64_t)d * rows * Lp;
+        }
+        const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);
+        const unsigned bgs = (unsigned)(a.batch * a.G);
+        kern<<<dim3(cblocks, bgs, 4), C::THREADS, C::SMEM, s>>>(mu, md, mu, mb, mc, mu2, p);
+        if ((st = check_launch("four-direction scan"))) return st;
+        OrderSet os{};
+        os.K = 4;
+        os.H = (int)a.H;
+        os.W = (int)a.W;
+        os.win = 0;
+        for (int k = 0; k < 4; ++k) os.orders[k] = a.orders[k];
+        os.pitch = Lp;
+        const unsigned bx = (unsigned)((a.L + 255) / 256);
+        const int64_t want_y = std::max<int64_t>(1, (int64_t)num_sms() * 32 / bx);
+        const unsigned by = (unsigned)std::min<int64_t>({rows, want_y, (int64_t)65535});
+        k_merge_steps<IO><<<dim3(bx, by), 256, 0, s>>>(acc0, rows, reinterpret_cast<const IO *>(a.z),
+                                                      reinterpret_cast<IO *>(a.out), os);
+        return check_launch("merge by step");
+    }
+
     // K directions of any order: each launch stores its direction's y_k + D_k*u
     // by scan step into its own fp32 accumulator; one merge inverts the
     // traversals and sums by position.
@@ -622,6 +699,7 @@ struct Scan1d {
         os.W = (int)a.W;
         os.win = a.win;
         for (int k = 0; k < K; ++k) os.orders[k] = a.orders[k];
+        os.pitch = a.L;
         const unsigned bx = (unsigned)((a.L + 255) / 256);
         const int64_t want_y = std::max<int64_t>(1, (int64_t)num_sms() * 32 / bx);
         const unsigned by = (unsigned)std::min<int64_t>({rows, want_y, (int64_t)65535});
@@ -709,7 +787,7 @@ static_assert(ViewCfg<Pick1d<__nv_bfloat16, 16>::C>::SMEM + 1024 <= 228 * 1024 /
 template <typename IO, int N>
 ss_status dispatch_bidir_view(const ScanArgs &a, int vshift) {
     using C = ViewCfg<typename Pick1d<IO, N>::C>;
-    return Scan1d<C>::run_bidir_view(a, vshift);
+    return a.K == 4 ? Scan1d<C>::run_ss2d_view(a, vshift) : Scan1d<C>::run_bidir_view(a, vshift);
 }
 
 template <typename IO>
@@ -994,8 +1072,24 @@ size_t bidir_view_bytes(const ScanArgs &a) {
     return align256((size_t)2 * a.batch * a.dim * padded_len(a) * sizeof(float));
 }
 
+// SS2D over maps whose rows are not 16-byte aligned, read through VIEW tiles
+// (else the on-chip kernel): log2 of the rows to a view row, or -1.
+int ss2d_view_shift(const ScanArgs &a) {
+    if (a.K != 4 || scan1d_uses_tma(a)) return -1;
+    for (int k = 0; k < 4; ++k)
+        if (a.orders[k] > ORD_COL_REV) return -1;
+    return view_fold_shift(a);
+}
+// Workspace of that path: four fp32 slices [rows, Lp] and the transposed copy of u.
+size_t ss2d_view_bytes(const ScanArgs &a) {
+    const int64_t rows = a.batch * a.dim;
+    return align256((size_t)4 * rows * padded_len(a) * sizeof(float)) +
+           align256((size_t)rows * a.L * (a.io == SS_BF16 ? 2 : 4));
+}
+
 size_t multidir_workspace_bytes(const ScanArgs &a) {
     if (bidir_padded_ok(a)) return bidir_padded_bytes(a);
+    if (ss2d_view_shift(a) > 0) return ss2d_view_bytes(a);  // optional: else on chip
     if (!scan1d_uses_tma(a)) return 0;  // rows not 16-byte aligned: on-chip merge path
     // one fp32 accumulator; SS2D scans its four directions side by side into
     // four fp32 slices, and reads u of its column directions from a transposed
@@ -1024,6 +1118,15 @@ ss_status launch_multidir(const ScanArgs &a) {
         if (a.ws && a.ws_bytes >= bidir_padded_bytes(a))
             return a.io == SS_BF16 ? dispatch_bidir_padded_n<__nv_bfloat16>(a)
                                    : dispatch_bidir_padded_n<float>(a);
+        return a.io == SS_BF16 ? dispatch_multi<__nv_bfloat16>(a) : dispatch_multi<float>(a);
+    }
+    if (!scan1d_uses_tma(a)) {
+        // SS2D over unaligned rows: view tiles when the caller gave the
+        // workspace, else on chip
+        const int vshift = ss2d_view_shift(a);
+        if (vshift > 0 && a.ws && a.ws_bytes >= ss2d_view_bytes(a))
+            return a.io == SS_BF16 ? dispatch_bidir_view_n<__nv_bfloat16>(a, vshift)
+                                   : dispatch_bidir_view_n<float>(a, vshift);
         return a.io == SS_BF16 ? dispatch_multi<__nv_bfloat16>(a) : dispatch_multi<float>(a);
     }
     if (multidir_workspace_bytes(a) > 0)

@@ -1381,6 +1381,7 @@ __global__ void __launch_bounds__(256) k_merge2_map(const float *__restrict__ r0
 struct OrderSet {
     int K, H, W, win;
     int orders[8];
+    int64_t pitch;  // row pitch (floats) of the accumulators: H*W, or more for view-tiled rows
 };
 template <typename IO>
 __global__ void __launch_bounds__(256) k_merge_steps(const float *__restrict__ acc, int64_t rows,
@@ -1397,7 +1398,7 @@ __global__ void __launch_bounds__(256) k_merge_steps(const float *__restrict__ a
         float y = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            if (k < os.K) y += acc[((int64_t)k * rows + row) * L + st[k]];
+            if (k < os.K) y += acc[((int64_t)k * rows + row) * os.pitch + st[k]];
         const int64_t i = row * L + pos;
         if (z) y *= silu(IOT<IO>::load(z + i));
         out[i] = IOT<IO>::from_f(y);

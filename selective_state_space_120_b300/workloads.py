@@ -86,6 +86,11 @@ LONG_SEQ_PROFILE = Workload("long_seq_b1_d5120_l16384_n16", 1, 5120, 16384, last
 # scan (weights ~ N(0, 0.5^2), bias ~ N(0, 0.1^2)).
 MAMBA_LAYER_CONV = Workload("mamba130m_layer_conv_b8_d1536_l2048_n16", 8, 1536, 2048, conv=True)
 
+# VMamba-T's third stage (the deepest): SS2D on a 14 x 14 map of 384 channels,
+# whose 196-value rows are not 16-byte multiples in bf16 (views of two rows).
+VMAMBA_SS2D_14 = Workload("vmamba_t_ss2d_b32_d384_14x14_n16", 32, 384, 14 * 14, K=4,
+                          with_z=False, H=14, W=14)
+
 # The Mamba layer one step shorter: rows of 2047 bf16 values are not 16-byte
 # multiples (the scan reads them through views of eight rows to a view row).
 MAMBA_LAYER_UNALIGNED = Workload("mamba130m_layer_b8_d1536_l2047_n16", 8, 1536, 2047)

@@ -502,8 +502,47 @@ def test_cross_scan2d(oracle, H, W, io):
 
 
 def test_cross_scan2d_gated_groups(oracle):
-    """Unaligned rows (60 bf16 = 120 bytes): the on-chip merge path."""
+    """Unaligned rows (60 bf16 = 120 bytes) with 8 channels a group and N = 4,
+    which the view's P = 2 divides: view tiles, with a gate and two groups."""
     _check(oracle, sc.workload("ss2d_gz", 1, 16, 6 * 10, N=4, G=2, K=4, H=6, W=10))
+
+
+@pytest.mark.parametrize("H,W", [(1, 1), (3, 5), (5, 3), (7, 7), (14, 14), (6, 10)])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_cross_scan2d_view_maps(oracle, H, W, io):
+    """Maps whose rows are not 16-byte aligned (VMamba's 14 x 14 and 7 x 7
+    stages among them), 24 channels: the four directions over view tiles (the
+    column pair over the transposed copy), merged by step."""
+    _check(oracle, sc.workload(f"ss2dv{H}x{W}", 2, 24, H * W, K=4, io=io, with_z=False, H=H, W=W))
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_cross_scan2d_unaligned_on_chip(oracle, io):
+    """Unaligned rows with 12 channels, which P = 8 (bf16) or 4 (fp32) rows to a
+    view row does not divide: the on-chip merge path."""
+    _check(oracle, sc.workload("ss2d_oc", 2, 12, 7 * 7, K=4, io=io, H=7, W=7))
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_cross_scan2d_view_isolate_channels(oracle, io):
+    """A view tile holds the neighbouring rows' values past each row's ends: a
+    NaN in one channel's map must not reach any other channel."""
+    import torch
+    import selective_state_space_120_b300 as ss
+    H, W = 7, 7
+    wl = sc.workload("ss2dv_iso", 2, 16, H * W, K=4, io=io, with_z=False, H=H, W=W)
+    inp = wk.make_inputs(wl, seed=0)
+    t = sc.device_inputs(inp)
+    t["u"][0, 5] = float("nan")
+    bsz, dim, L = t["u"].shape
+    out, last = ss.cross_scan2d_fwd(t["u"].view(bsz, dim, H, W), t["delta"], t["A"], t["B"], t["C"],
+                                    t["D"], t["delta_bias"], True, return_last_state=True)
+    torch.cuda.synchronize()
+    ref, ref_last = sc.oracle_run(oracle, inp)
+    keep = [d for d in range(wl.dim) if d != 5]
+    got = sc.from_torch(out.view(bsz, dim, L))
+    sc.assert_close(got[0, keep], ref[0, keep], io)
+    sc.assert_close(got[1], ref[1], io)
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
@@ -542,6 +581,6 @@ def _sampled(oracle, wl, nrows=12, seed=1):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("wl", [wk.MAMBA_LAYER, wk.LONG_SEQ, wk.VIM_BIDIR, wk.VMAMBA_SS2D,
-                                wk.MAMBA_LAYER_UNALIGNED], ids=lambda w: w.name)
+                                wk.MAMBA_LAYER_UNALIGNED, wk.VMAMBA_SS2D_14], ids=lambda w: w.name)
 def test_full_size_sampled(oracle, wl):
     _sampled(oracle, wl)
