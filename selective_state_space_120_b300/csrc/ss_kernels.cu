@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -181,6 +182,44 @@ ss_status permuted_copy(const ScanArgs &a, int order, void *dst) {
     return check_launch("order permute");
 }
 
+// Steps of the L-chunks of the chunked single-direction path: chunk 0 covers
+// [0, L0), chunks 1..J-2 Lm steps each after it, chunk J-1 the rest up to L.
+struct ChunkGeom {
+    int J;
+    int64_t L0, Lm;
+};
+
+// Cost of a chunk of the chunk-local pass (no readout, no C tiles, no gate)
+// relative to a chunk that writes outputs: 284.6 us for one chunk with outputs
+// and ten without against 408.7 us for eleven with, on 5120 rows of 16384 steps.
+constexpr double kMidNoReadoutCost = 0.67;
+
+// L-chunk geometry of the chunked path for a request of J chunks of R CTAs
+// each on a GPU of S CTA slots.  Chunk 0 has no pass-2 rescan and chunk J-1
+// no pass-1 scan, so making them longer than the middle chunks removes
+// rescanned steps -- as long as each pass still keeps every slot busy: its
+// long chunk's R CTAs run the whole pass while the other S - R slots work
+// through the R*(J-2) middle CTAs.  Balancing the two gives the last chunk
+// (J-2)*R/(S-R) middle lengths, and the first chunk that times the relative
+// cost of a middle chunk in pass 1 (no readout: about two thirds of one with
+// it, measured on the B300).  Every chunk starts on a multiple of T.
+ChunkGeom chunk_geom(int64_t L, int J, int64_t R, int64_t S, int T) {
+    if (J <= 1) return {1, L, L};
+    const int mid = J - 2;
+    double wf = 1.0, wl = 1.0;
+    if (mid > 0 && 2 * R <= S) {
+        wl = std::max(1.0, (double)mid * (double)R / (double)(S - R));
+        wf = std::max(1.0, wl * kMidNoReadoutCost);
+    }
+    const double wsum = wf + mid + wl;
+    const int64_t Lm = std::max<int64_t>(T, ((int64_t)std::ceil((double)L / wsum) + T - 1) / T * T);
+    const int64_t L0 = std::max<int64_t>(T, ((int64_t)std::ceil(wf * (double)L / wsum) + T - 1) / T * T);
+    int m = mid;
+    while (m >= 0 && L - L0 - (int64_t)m * Lm <= 0) --m;
+    if (m < 0) return {1, L, L};
+    return {m + 2, L0, Lm};
+}
+
 // ---------------------------------------------------------------- single direction
 template <class C>
 struct Scan1d {
@@ -248,12 +287,13 @@ struct Scan1d {
         const unsigned cblocks = (unsigned)((p.dpg + C::CB - 1) / C::CB);
         const unsigned bgs = (unsigned)(a.batch * a.G);
         cudaStream_t s = reinterpret_cast<cudaStream_t>(a.stream);
-        const int64_t Lc = chunk_len(a.L, J);
-        J = (int)((a.L + Lc - 1) / Lc);
+        const ChunkGeom geo = chunk_geom(a.L, J, (int64_t)cblocks * bgs,
+                                         (int64_t)num_sms() * slots_per_sm(), C::T);
+        J = geo.J;
         if (J <= 1) {
             p.Lc = a.L;
             p.J = 1;
-            p.jbase = 0;
+            p.L0 = a.L;
             p.pass = 0;
             if (plain) {
                 auto kd = k_scan1d_direct<C>;
@@ -266,15 +306,15 @@ struct Scan1d {
             }
             return check_launch("scan");
         }
-        // chunked path: L-chunks of Lc steps (a multiple of T)
+        // chunked path: the L-chunks of `geo`
         float *ws = reinterpret_cast<float *>(a.ws);
-        p.Lc = Lc;
+        p.L0 = geo.L0;
+        p.Lc = geo.Lm;
         p.J = J;
         p.hend = ws;
         p.carry = ws + rows * J * C::N;
         p.sdt = ws + 2 * rows * J * C::N;
         p.pass = 1;
-        p.jbase = 0;
         kern<<<dim3(cblocks, bgs, J - 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, mu, p);
         if ((st = check_launch("scan chunk-local pass"))) return st;
         const int64_t nthr = rows * C::N;
@@ -282,7 +322,6 @@ struct Scan1d {
                                                             p.sdt, const_cast<float *>(p.carry));
         if ((st = check_launch("carry"))) return st;
         p.pass = 2;
-        p.jbase = 1;
         kern<<<dim3(cblocks, bgs, J - 1), C::THREADS, C::SMEM, s>>>(mu, md, mz, mb, mc, mu, p);
         return check_launch("scan fix-up pass");
     }
@@ -314,7 +353,7 @@ struct Scan1d {
         p.dpg = (int)(a.dim / a.G);
         p.Lc = a.L;
         p.J = 1;
-        p.jbase = 0;
+        p.L0 = a.L;
         p.pass = 0;
         p.K = K;
         p.acc = reinterpret_cast<float *>(a.ws);
@@ -443,7 +482,7 @@ struct Scan1d {
         p.dpg = (int)(a.dim / a.G);
         p.Lc = a.L;
         p.J = 1;
-        p.jbase = 0;
+        p.L0 = a.L;
         p.pass = 0;
         p.K = 2;
         p.u_g = a.u;
@@ -509,7 +548,7 @@ struct Scan1d {
         p.dpg = (int)(a.dim / a.G);
         p.Lc = a.L;
         p.J = 1;
-        p.jbase = 0;
+        p.L0 = a.L;
         p.pass = 0;
         p.K = 2;
         p.u_g = a.u;
@@ -579,7 +618,7 @@ struct Scan1d {
         p.dpg = (int)(a.dim / a.G);
         p.Lc = a.L;
         p.J = 1;
-        p.jbase = 0;
+        p.L0 = a.L;
         p.pass = 0;
         p.K = 4;
         p.u_g = a.u;
@@ -659,7 +698,7 @@ struct Scan1d {
         p.dpg = (int)(a.dim / a.G);
         p.Lc = a.L;
         p.J = 1;
-        p.jbase = 0;
+        p.L0 = a.L;
         p.pass = 0;
         p.K = K;
         p.u_g = a.u;
@@ -708,10 +747,23 @@ struct Scan1d {
         return check_launch("merge by step");
     }
 
-    // Steps per L-chunk for a requested chunk count: a multiple of the T-tile.
-    static int64_t chunk_len(int64_t L, int J) {
-        if (J <= 1) return L;
-        return ((L + J - 1) / J + C::T - 1) / C::T * C::T;
+    // CTAs of the plain scan kernel resident on one SM (registers and shared
+    // memory), the slots the chunked passes fill.
+    static int slots_per_sm() {
+        static int cached = 0;
+        if (cached > 0) return cached;
+        int nb = 0;
+        auto kern = ssk::k_scan1d<C, false, false>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+                cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, C::THREADS, C::SMEM) !=
+                cudaSuccess ||
+            nb < 1) {
+            cudaGetLastError();  // no device: one CTA per SM
+            return 1;
+        }
+        cached = nb;
+        return nb;
     }
 };
 
@@ -729,11 +781,16 @@ template <typename IO> struct Pick1d<IO, 32> { using C = ssk::Cfg1<IO, 32, 4, 4,
 template <typename IO> struct Pick1d<IO, 64> { using C = ssk::Cfg1<IO, 64, 8, 4, 3, 1, 1>; };
 
 // L-chunks to use: 1 (direct) when the direct path gives every SM sub-partition
-// at least two warps; otherwise enough chunks for about twelve warps each (the
-// chunked path rescans all but the first chunk, so it only pays off when the
-// direct path would leave the sub-partitions short of warps; on the B300 the
-// 1 x 5120 x 131072 scan measured 5.52 ms at 12 chunks, 5.61 at 10, 5.62 at 8,
-// 5.84 at 14 and 16, 6.04 at 4).
+// at least two warps.  Otherwise, when one L-chunk's CTAs fill at most half the
+// GPU's slots, enough middle chunks for about kMidWaves waves of the slots that
+// the long first and last chunks leave free (chunk_geom); else enough chunks
+// for about twelve warps per sub-partition (the chunked path rescans all but
+// the first chunk, so it only pays off when the direct path would leave the
+// sub-partitions short of warps).  On the B300 the 1 x 5120 x 131072 scan
+// measured 5.52 ms at 12 equal chunks, 5.61 at 10, 5.62 at 8, 5.84 at 14 and
+// 16, 6.04 at 4.
+constexpr double kMidWaves = 6.0;
+
 template <class C>
 int choose_chunks(const ScanArgs &a) {
     const int64_t rows = a.batch * a.dim;
@@ -741,6 +798,9 @@ int choose_chunks(const ScanArgs &a) {
     const int64_t one_per_smsp = (int64_t)num_sms() * 4 * 32;
     if (threads >= 2 * one_per_smsp) return 1;
     int64_t J = (12 * one_per_smsp + threads - 1) / threads;
+    const int64_t R = (a.dim / a.G + C::CB - 1) / C::CB * a.batch * a.G;
+    const int64_t S = (int64_t)num_sms() * Scan1d<C>::slots_per_sm();
+    if (2 * R <= S) J = 2 + (int64_t)std::ceil(kMidWaves * (double)(S - R) / (double)R);
     const int64_t maxJ = a.L / (4 * C::T);  // keep L-chunks at least 4 T-chunks long
     if (J > maxJ) J = maxJ;
     return J < 2 ? 1 : (int)J;
@@ -750,8 +810,8 @@ template <typename IO, int N>
 int chunks_for(const ScanArgs &a) {
     using C = typename Pick1d<IO, N>::C;
     const int J = a.chunks > 0 ? a.chunks : choose_chunks<C>(a);
-    const int64_t Lc = Scan1d<C>::chunk_len(a.L, J);
-    return (int)((a.L + Lc - 1) / Lc);
+    const int64_t R = (a.dim / a.G + C::CB - 1) / C::CB * a.batch * a.G;
+    return chunk_geom(a.L, J, R, (int64_t)num_sms() * Scan1d<C>::slots_per_sm(), C::T).J;
 }
 
 template <typename IO, int N>

@@ -149,9 +149,14 @@ enum { OUT_STORE = 0, OUT_ACC_FIRST = 1, OUT_ACC_ADD = 2, OUT_ACC_LAST = 3, OUT_
 struct Scan1dParams {
     int64_t dim, L;
     int G, dpg;
-    int64_t Lc;   // steps per L-chunk (multiple of T); L for the direct path
+    // L-chunks: chunk 0 covers steps [0, L0), chunk j in 1..J-2 the Lc steps
+    // from L0 + (j-1)*Lc, chunk J-1 the rest up to L (L0 and Lc multiples of
+    // T; J = 1 and L0 = Lc = L for the direct path).  Pass 1 runs chunks
+    // 0..J-2 as blockIdx.z = 0..J-2; pass 2 runs chunk J-1 as blockIdx.z = 0
+    // and chunks 1..J-2 as blockIdx.z = 1..J-2, so that each pass's longest
+    // chunk is dispatched first.
+    int64_t L0, Lc;
     int J;        // number of L-chunks
-    int jbase;    // L-chunk index of blockIdx.z == 0
     int pass;     // 0 direct, 1 chunk-local pass, 2 chunk fix-up pass
     int K, k;     // directions of the call, and the one this launch scans
     int order;    // 0: u tiles in step order; 2: the same, read back to front
@@ -801,15 +806,15 @@ __device__ __forceinline__ void scan1d_body(const CUtensorMap &tm_u, const CUten
     const int cblk = blockIdx.x;
     const int bg = blockIdx.y;
     const int b = bg / p.G, grp = bg % p.G;
-    const int jc = MULTI ? 0 : p.jbase + (int)blockIdx.z;
+    const int jc = MULTI ? 0 : (p.pass == 2 && blockIdx.z == 0) ? p.J - 1 : (int)blockIdx.z;
     const int64_t row0 = (int64_t)b * p.dim + (int64_t)grp * p.dpg;  // row of the group's channel 0
     const int row_tma = (int)(row0 + (int64_t)cblk * C::CB);          // u, z, out rows
     // Delta rows of direction k: [batch, K, dim]; B/C rows: [batch, K, G, N]
     const int dlrow_tma = (int)(((int64_t)b * p.K + p.k) * p.dim + (int64_t)grp * p.dpg +
                                 (int64_t)cblk * C::CB);
     const int bcrow_tma = (int)((((int64_t)b * p.K + p.k) * p.G + grp) * N);
-    const int64_t t_begin = (int64_t)jc * p.Lc;
-    const int64_t t_end = min(p.L, t_begin + p.Lc);
+    const int64_t t_begin = jc == 0 ? 0 : p.L0 + (int64_t)(jc - 1) * p.Lc;
+    const int64_t t_end = jc == p.J - 1 ? p.L : jc == 0 ? p.L0 : t_begin + p.Lc;
     const int nchunks = (int)((t_end - t_begin + T - 1) / T);
     // the chunk-local pass needs only the end states of chunks 1..J-2: no
     // readout, so no C tiles, no gate and no skip term

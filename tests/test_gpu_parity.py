@@ -130,6 +130,27 @@ def test_chunked_equals_direct_to_fp32_rounding():
     assert sc.rel_err(l4.cpu().numpy(), l1.cpu().numpy()) < 2e-5
 
 
+def test_chunked_long_edge_chunks_equal_direct():
+    """Few rows (160 CTAs of 32 channels, a quarter of the GPU's slots): the
+    automatic split makes the first and last L-chunks several times longer
+    than the middle ones; every row still equals the single pass to fp32
+    rounding."""
+    wl = sc.workload("edges", 1, 5120, 4096, io="f32")
+    inp = wk.make_inputs(wl)
+    o1, l1 = sc.gpu_run(inp, chunks=1)
+    oa, la = sc.gpu_run(inp, chunks=0)
+    assert sc.rel_err(sc.from_torch(oa), sc.from_torch(o1)) < 2e-5
+    assert sc.rel_err(la.cpu().numpy(), l1.cpu().numpy()) < 2e-5
+
+
+@pytest.mark.parametrize("io,L", [("f32", 8192), ("bf16", 16384)])
+def test_chunked_long_edge_chunks_against_oracle(oracle, io, L):
+    """The long-sequence shape's rows with fewer steps, automatic split (long
+    first and last L-chunks, middle ones between): sampled channels over the
+    whole sequence and their last states against the oracle."""
+    _sampled(oracle, sc.workload("edges_" + io, 1, 5120, L, io=io), nrows=6)
+
+
 def test_deterministic_and_guarded():
     """Two runs give identical bits; nothing is written outside `out`."""
     import torch
