@@ -112,7 +112,10 @@ typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
  *
  * Empty inputs (batch, dim or seqlen = 0) return SS_OK without touching memory.
  * Long sequences with little batch*dim parallelism run a chunked path (per-chunk
- * local states, a carry pass, a fix-up pass) that uses the workspace.
+ * local states, a carry pass, a fix-up pass) that uses the workspace.  Only the
+ * middle L-chunks are scanned twice, so when one chunk's CTAs fill at most half
+ * of the GPU the first and last chunks are made longer than the others, by as
+ * much as keeps every SM busy in both passes.
  * Rows that are not 16-byte aligned (seqlen * element size % 16 != 0) are read
  * in place through a view whose rows hold P of theirs (P = (16 / element size)
  * / gcd(seqlen, 16 / element size)) when P divides dim / ngroups and dstate; for
@@ -130,8 +133,9 @@ ss_status ss_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int 
 /* Options of ss_selective_scan_fwd_opts.  Zero-initialise, then set fields. */
 typedef struct ss_scan_options {
     /* Sequence split.  0: automatic; 1: one pass over the whole sequence;
-     * n >= 2: the chunked long-sequence path with at most n L-chunks (each a
-     * multiple of the kernel's step tile; fewer if the sequence is short). */
+     * n >= 2: the chunked long-sequence path with at most n L-chunks (each
+     * starting on a multiple of the kernel's step tile, the first and last
+     * possibly longer than the others; fewer if the sequence is short). */
     int chunks;
     /* Bit flags, SS_SCAN_* (0 for the default Euler step from a zero state). */
     unsigned int flags;
