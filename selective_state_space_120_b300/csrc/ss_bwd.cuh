@@ -50,6 +50,7 @@
 // dz from the sum of all directions' outputs before the gate.
 #pragma once
 
+#include <type_traits>
 #include "ss_device.cuh"
 
 namespace ssk {
@@ -785,6 +786,49 @@ __global__ void __launch_bounds__(256) k_transpose_maps(const IO *__restrict__ s
     for (int k = 0; k < 32; k += 8) {
         const int c = c0 + ty + k, r = r0 + tx;
         if (r < H && c < W) d[(int64_t)c * H + r] = tile[tx][ty + k];
+    }
+}
+
+// k_transpose_maps for planes that fit in shared memory whole, H a multiple of
+// the V = 16 / sizeof(IO) elements of a 16-byte vector, and 16-byte aligned
+// planes.  One CTA per plane copies it into shared memory as 16-byte vectors
+// (all of a thread's loads issued before its stores), then each thread gathers
+// V consecutive rows of one column and writes them as one 16-byte vector of the
+// [W, H] plane; consecutive lanes take consecutive columns, so a warp's
+// shared-memory reads are consecutive.  Dynamic shared memory: H * W elements.
+template <typename IO>
+__global__ void __launch_bounds__(256) k_transpose_planes(const IO *__restrict__ src, IO *__restrict__ dst,
+                                                          int H, int W) {
+    using R = typename std::conditional<sizeof(IO) == 2, unsigned short, unsigned int>::type;
+    constexpr int V = 16 / (int)sizeof(IO);
+    constexpr int U = 4;
+    extern __shared__ uint4 plane_v[];
+    const R *plane = reinterpret_cast<const R *>(plane_v);
+    const int t = threadIdx.x;
+    const int L = H * W;
+    const int nv = L / V;
+    const uint4 *s = reinterpret_cast<const uint4 *>(src + blockIdx.x * (int64_t)L);
+    for (int i0 = t; i0 < nv; i0 += U * 256) {
+        uint4 v[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+            if (i0 + j * 256 < nv) v[j] = __ldg(s + i0 + j * 256);
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+            if (i0 + j * 256 < nv) plane_v[i0 + j * 256] = v[j];
+    }
+    __syncthreads();
+    uint4 *d = reinterpret_cast<uint4 *>(dst + blockIdx.x * (int64_t)L);
+    const int nb = H / V;  // 16-byte vectors in a row of the [W, H] plane
+    for (int k = t; k < nv; k += 256) {
+        const int rb = k / W, c = k - rb * W;  // column c, rows rb*V .. rb*V + V - 1
+        union {
+            uint4 v;
+            R e[V];
+        } o;
+#pragma unroll
+        for (int j = 0; j < V; ++j) o.e[j] = plane[(rb * V + j) * W + c];
+        d[c * nb + rb] = o.v;
     }
 }
 

@@ -149,13 +149,29 @@ int steps_copy_slots(const ScanArgs &a, int slot[4]) {
 }
 
 // Writes u permuted into the step order of `order` (a column or windowed base
-// order) to `dst`: the column order by 32 x 32 shared-memory transposes, any
-// order by one walk of the traversal per step.
+// order) to `dst`: the column order by whole-plane shared-memory transposes
+// (planes of at most 48 KB whose H is a multiple of a 16-byte vector) or 32 x
+// 32 tiles, any order by one walk of the traversal per step.
 ss_status permuted_copy(const ScanArgs &a, int order, void *dst) {
     const int64_t rows = a.batch * a.dim;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(a.stream);
     const bool tiles = order == ORD_COL && (a.H + 31) / 32 <= 65535 && (a.W + 31) / 32 <= 65535 &&
                        rows < (1ll << 31);
+    const int es = a.io == SS_BF16 ? 2 : 4;
+    const bool planes = order == ORD_COL && a.H % (16 / es) == 0 && a.L * es <= 48 * 1024 &&
+                        rows < (1ll << 31) && reinterpret_cast<uintptr_t>(a.u) % 16 == 0 &&
+                        reinterpret_cast<uintptr_t>(dst) % 16 == 0;
+    if (planes) {
+        const size_t sm = (size_t)a.L * es;
+        if (a.io == SS_BF16)
+            ssk::k_transpose_planes<__nv_bfloat16><<<(unsigned)rows, 256, sm, s>>>(
+                reinterpret_cast<const __nv_bfloat16 *>(a.u), reinterpret_cast<__nv_bfloat16 *>(dst),
+                (int)a.H, (int)a.W);
+        else
+            ssk::k_transpose_planes<float><<<(unsigned)rows, 256, sm, s>>>(
+                reinterpret_cast<const float *>(a.u), reinterpret_cast<float *>(dst), (int)a.H, (int)a.W);
+        return check_launch("map transpose");
+    }
     if (tiles) {
         const dim3 tg((unsigned)rows, (unsigned)((a.H + 31) / 32), (unsigned)((a.W + 31) / 32));
         if (a.io == SS_BF16)
@@ -412,6 +428,15 @@ struct Scan1d {
         // whole maps in shared memory when the column map fits (odd stride P)
         const int P = (a.H & 1) ? (int)a.H : (int)a.H + 1;
         const size_t msm = (size_t)a.W * P * sizeof(float);
+        const uintptr_t al = 4 * sizeof(IO);
+        if (msm <= 48 * 1024 && rows < (1ll << 31) && a.H % 4 == 0 && a.W % 4 == 0 &&
+            reinterpret_cast<uintptr_t>(a.out) % al == 0 && reinterpret_cast<uintptr_t>(a.z) % al == 0) {
+            k_merge2_map4<IO><<<(unsigned)rows, 256, msm, s>>>(sl[0], sl[2], sl[1], sl[3],
+                                                               reinterpret_cast<const IO *>(a.z),
+                                                               reinterpret_cast<IO *>(a.out), (int)a.H,
+                                                               (int)a.W, P);
+            return check_launch("merge");
+        }
         if (msm <= 48 * 1024 && rows < (1ll << 31)) {
             k_merge2_map<IO><<<(unsigned)rows, 256, msm, s>>>(sl[0], sl[2], sl[1], sl[3],
                                                               reinterpret_cast<const IO *>(a.z),
