@@ -318,6 +318,28 @@ def test_split_invariance(oracle):
     np.testing.assert_allclose(lb, last, rtol=1e-13)
 
 
+def test_chunk_carry_rule(oracle):
+    """The rule the chunked long-sequence path chains its L-chunks by: a chunk
+    scanned from a state h0 ends in exp(A * sum of Delta') * h0 plus the end
+    state of the same chunk scanned from zero, and each of its outputs exceeds
+    the zero-state one by C_t . (exp(A * S_t) * h0), gated, S_t being the sum
+    of Delta' up to and including step t.  Delta' is computed here with NumPy's
+    softplus, not the oracle's."""
+    rng = np.random.default_rng(21)
+    batch, dim, L, N = 2, 3, 23, 4
+    u, delta, A, B, C, D, z, bias = _rand_case(rng, batch, dim, L, N, 1)
+    delta, B, C = delta[:, 0], B[:, 0], C[:, 0]
+    h0 = rng.standard_normal((batch, dim, N))
+    y0, l0 = oracle.scan(u, delta, A, B, C, D, z, bias, True)
+    y1, l1 = oracle.scan(u, delta, A, B, C, D, z, bias, True, h0=h0)
+    dp = _softplus(delta + bias[None, :, None])      # [batch, dim, L]
+    S = np.cumsum(dp, axis=-1)
+    decay = np.exp(A[None, :, :, None] * S[:, :, None, :])   # [batch, dim, N, L]
+    np.testing.assert_allclose(l1[:, 0], decay[..., -1] * h0 + l0[:, 0], rtol=1e-12, atol=1e-13)
+    extra = np.einsum("bnl,bdnl,bdn->bdl", C[:, 0], decay, h0) * _silu(z)
+    np.testing.assert_allclose(y1 - y0, extra, rtol=1e-10, atol=1e-12)
+
+
 def test_group_mapping_contiguous_blocks(oracle):
     """Channel d uses group d // (dim / G): changing group 1's B/C leaves channels 0..dim/G-1 alone."""
     rng = np.random.default_rng(13)
