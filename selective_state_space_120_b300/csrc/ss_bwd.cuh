@@ -45,9 +45,10 @@
 // over its inputs taken in its traversal order.  Two directions run side by
 // side over grid z; u, dout and z come as row-order tiles, forward or back to
 // front, of the call's maps or of copies permuted into the direction's step
-// order (k_transpose_maps for the column order); du goes by scan step to an
-// fp32 buffer per direction, which k_merge_bwd sums by position while forming
-// dz from the sum of all directions' outputs before the gate.
+// order (k_transpose_planes or k_transpose_maps for the column order); du goes
+// by scan step to an fp32 buffer per direction, which k_merge_bwd sums by
+// position while forming dz from the sum of all directions' outputs before the
+// gate.
 #pragma once
 
 #include <type_traits>
